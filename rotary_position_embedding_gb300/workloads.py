@@ -1,0 +1,215 @@
+"""Seeded synthetic inputs for the RoPE / M-RoPE workloads.
+
+This module draws inputs only: activations X, position ids and the inv_freq
+parameter vector. It holds none of the operator's arithmetic; the cos/sin
+tables are produced by whichever side is under test (the library's
+``rope_cache_build`` on the GPU, the oracle's cache build on the CPU). Both
+the test suite and ``bench.py`` take their inputs from here, so both sides of
+every parity check see identical bytes.
+
+Recipes (one seed per tensor: X seed 0, positions seed 1, out-of-range mask
+seed 2):
+  X            N(0, 1) drawn in float32, rounded to the storage type.
+  RoPE ids     ``pos[b, s] = s + off_b`` with ``off_b ~ U[0, 4096)`` (gather
+               workload), or uniform over the cache rows.
+  M-RoPE ids   per batch: 1024 text tokens (t = h = w), 4 frames of a 32x32
+               image grid (t = st + f, h = st + r, w = st + c), 1024 text
+               tokens starting at the previous maximum + 1, 2 frames of a
+               32x32 grid; a per-batch offset ~ U[0, 16384) on all three
+               streams; then 1 % of the 3*B*S ids set past the cache.
+  inv_freq     ``base ** (-2 i / d)`` in binary64, rounded to float32 (a model
+               parameter, built identically for both sides).
+"""
+
+from dataclasses import dataclass, field
+
+import numpy as np
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    kind: str                 # "rope" | "mrope" | "fused"
+    rank: int
+    shape: tuple              # X shape
+    dtype: str                # "float16" | "float32"
+    num_heads: int            # heads N (explicit for rank 4 too)
+    interleaved: int = 0
+    rotary_embedding_dim: int = 0
+    positions: str = "none"   # "none" | "offset" | "uniform" | "mrope"
+    cache_rows: int = 0       # rows of the 2-D cache (or S for the 3-D cache)
+    rope_base: float = 10000.0
+    rope_dim: int = 0         # d in base ** (-2i/d); 0 = rotary dim
+    mrope_section: tuple = ()
+    mrope_layout: int = 0
+    scale: float = 1.0
+    attention_scaling: float = 1.0
+    extra: dict = field(default_factory=dict)
+
+    @property
+    def head_size(self):
+        return self.shape[2] // self.num_heads if self.rank == 3 else self.shape[3]
+
+    @property
+    def batch(self):
+        return self.shape[0]
+
+    @property
+    def seq(self):
+        return self.shape[1] if self.rank == 3 else self.shape[2]
+
+    @property
+    def rotary_dim(self):
+        return self.rotary_embedding_dim or self.head_size
+
+    @property
+    def half(self):
+        return self.rotary_dim // 2
+
+    @property
+    def tokens(self):
+        return self.batch * self.seq
+
+    @property
+    def numel(self):
+        return int(np.prod(self.shape))
+
+    def with_shape(self, **kw):
+        """Same recipe at another size: keys B, S, N (and H for rank 4)."""
+        B = kw.get("B", self.batch)
+        S = kw.get("S", self.seq)
+        N = kw.get("N", self.num_heads)
+        H = kw.get("H", self.head_size)
+        shape = (B, S, N * H) if self.rank == 3 else (B, N, S, H)
+        d = dict(self.__dict__)
+        d.update(shape=shape, num_heads=N, name=self.name + f"@{shape}")
+        for k in ("cache_rows", "rotary_embedding_dim", "mrope_section", "scale", "mrope_layout",
+                  "interleaved", "dtype", "positions", "attention_scaling"):
+            if k in kw:
+                d[k] = kw[k]
+        return Workload(**d)
+
+
+# The five workloads. Sizes follow the operator's published configurations;
+# the gather workload is the headline benchmark.
+WORKLOADS = {
+    "rope_r4_f32_cache3d": Workload(
+        name="rope_r4_f32_cache3d", kind="rope", rank=4, shape=(1, 2, 8, 16), dtype="float32",
+        num_heads=2, interleaved=0, positions="none", cache_rows=8, rope_base=10000.0, rope_dim=16),
+    "rope_r3_f16_gather": Workload(
+        name="rope_r3_f16_gather", kind="rope", rank=3, shape=(4, 2048, 32 * 128), dtype="float16",
+        num_heads=32, interleaved=0, positions="offset", cache_rows=8192, rope_base=10000.0,
+        rope_dim=128),
+    "rope_r4_f16_interleaved_partial": Workload(
+        name="rope_r4_f16_interleaved_partial", kind="rope", rank=4, shape=(8, 32, 4096, 128),
+        dtype="float16", num_heads=32, interleaved=1, rotary_embedding_dim=64, positions="uniform",
+        cache_rows=16384, rope_base=10000.0, rope_dim=64),
+    "mrope_r3_f16_layout0": Workload(
+        name="mrope_r3_f16_layout0", kind="mrope", rank=3, shape=(2, 8192, 28 * 128), dtype="float16",
+        num_heads=28, positions="mrope", cache_rows=32768, rope_base=10000.0, rope_dim=128,
+        mrope_section=(16, 24, 24), mrope_layout=0, scale=1.0),
+    "mrope_r3_f16_layout1": Workload(
+        name="mrope_r3_f16_layout1", kind="mrope", rank=3, shape=(2, 8192, 28 * 128), dtype="float16",
+        num_heads=28, positions="mrope", cache_rows=32768, rope_base=10000.0, rope_dim=128,
+        mrope_section=(16, 24, 24), mrope_layout=1, scale=1.0),
+    "fused_decode_r3_f16": Workload(
+        name="fused_decode_r3_f16", kind="fused", rank=3, shape=(256, 1, 40 * 128), dtype="float16",
+        num_heads=40, positions="uniform", cache_rows=32768, rope_base=1.0e6, rope_dim=128,
+        attention_scaling=1.0),
+}
+
+HEADLINE = "rope_r3_f16_gather"
+
+
+def x_normal(shape, dtype, seed=0):
+    """N(0, 1) drawn in float32 and rounded to ``dtype`` (numpy rounds to nearest-even)."""
+    rng = np.random.default_rng(seed)
+    x = rng.standard_normal(size=shape, dtype=np.float32)
+    return x.astype(dtype)
+
+
+def inv_freq(base, d, half):
+    """``base ** (-2 i / d)`` for i < half: binary64 power, rounded to float32."""
+    i = np.arange(half, dtype=np.float64)
+    return np.power(np.float64(base), -(2.0 * i) / np.float64(d)).astype(np.float32)
+
+
+def positions_offset(B, S, seed=1, max_offset=4096):
+    rng = np.random.default_rng(seed)
+    off = rng.integers(0, max_offset, size=(B, 1), dtype=np.int64)
+    return np.arange(S, dtype=np.int64)[None, :] + off
+
+
+def positions_uniform(B, S, rows, seed=1):
+    rng = np.random.default_rng(seed)
+    return rng.integers(0, rows, size=(B, S), dtype=np.int64)
+
+
+def mrope_ids(B, S, rows, seed=1, oor_seed=2, oor_fraction=0.01, grid=32, max_offset=16384):
+    """(3, B, S) t/h/w ids: text and image spans, a per-batch offset, 1 % past the cache."""
+    rng = np.random.default_rng(seed)
+    ids = np.empty((3, B, S), dtype=np.int64)
+    spans = [("text", 1024), ("image", 4), ("text", 1024), ("image", 2)]
+    for b in range(B):
+        t, h, w = [], [], []
+        nxt = 0
+        for kind, n in spans:
+            if kind == "text":
+                q = np.arange(nxt, nxt + n, dtype=np.int64)
+                t.append(q), h.append(q), w.append(q)
+                nxt = nxt + n
+            else:
+                f, r, c = np.meshgrid(np.arange(n), np.arange(grid), np.arange(grid), indexing="ij")
+                t.append(nxt + f.ravel()), h.append(nxt + r.ravel()), w.append(nxt + c.ravel())
+                nxt = int(max(t[-1].max(), h[-1].max(), w[-1].max())) + 1
+        row = np.stack([np.concatenate(t), np.concatenate(h), np.concatenate(w)])
+        # tile or truncate the span pattern to S tokens
+        reps = -(-S // row.shape[1])
+        if reps > 1:
+            width = int(row.max()) + 1
+            row = np.concatenate([row + k * width for k in range(reps)], axis=1)
+        ids[:, b, :] = row[:, :S] + rng.integers(0, max_offset, dtype=np.int64)
+    ids = np.minimum(ids, rows - 1) if rows > 0 else ids
+    orng = np.random.default_rng(oor_seed)
+    flat = ids.reshape(-1)
+    n_oor = int(round(oor_fraction * flat.size))
+    if n_oor:
+        where = orng.choice(flat.size, size=n_oor, replace=False)
+        flat[where] = rows + orng.integers(0, 1 << 20, size=n_oor, dtype=np.int64)
+    return ids
+
+
+def make_inputs(w: Workload):
+    """Host arrays for workload ``w``: x, position_ids (or None), inv_freq."""
+    x = x_normal(w.shape, np.dtype(w.dtype), seed=0)
+    B, S = w.batch, w.seq
+    if w.positions == "none":
+        pos = None
+    elif w.positions == "offset":
+        pos = positions_offset(B, S, seed=1)
+    elif w.positions == "uniform":
+        pos = positions_uniform(B, S, w.cache_rows, seed=1)
+    elif w.positions == "mrope":
+        pos = mrope_ids(B, S, w.cache_rows, seed=1, oor_seed=2)
+    else:
+        raise ValueError(w.positions)
+    inv = inv_freq(w.rope_base, w.rope_dim or w.rotary_dim, w.half)
+    return {"x": x, "position_ids": pos, "inv_freq": inv}
+
+
+def algorithmic_bytes(w: Workload, cached=True):
+    """Bytes one pass must move: X + Y + cos/sin touched + positions (+ inv_freq).
+
+    cos/sin "touched" counts rd/2 cosines and rd/2 sines per token (a
+    per-token gather, not unique rows); the on-the-fly variant reads inv_freq
+    once instead.
+    """
+    esz = np.dtype(w.dtype).itemsize
+    xy = 2 * w.numel * esz
+    npos = 3 if w.kind == "mrope" else (0 if w.positions == "none" else 1)
+    pos = npos * w.tokens * 8
+    if w.kind == "fused" and not cached:
+        coef = w.half * 4
+    else:
+        coef = 2 * w.tokens * w.half * esz
+    return xy + pos + coef

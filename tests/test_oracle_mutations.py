@@ -1,0 +1,58 @@
+"""The oracle's pins must catch plausible mistakes in the oracle itself.
+
+Each case plants one mistake in a temporary copy of the oracle's C source (a
+flipped sign, a wrong pair index, a transposed row formula, a skipped
+rounding, an off-by-one range check...), rebuilds that copy and runs the pin
+suite against it; the suite must fail. Nothing here touches the real oracle
+or the CUDA path.
+"""
+
+import os
+import shutil
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+MUTATIONS = {
+    "sign_of_second_output": ("double y1 = x1 * c + x0 * s;", "double y1 = x1 * c - x0 * s;"),
+    "interleaved_partner": ("*j1 = 2 * i + 1;", "*j1 = 2 * i + 2;"),
+    "rank4_row_transposed": ("return ((b * g->N + n) * g->S + s) * g->H;",
+                             "return ((b * g->S + s) * g->N + n) * g->H;"),
+    "scaled_coefficient_not_rounded": (
+        "double c = round_to(dt, ld(dt, cos_t, p * half + i) * (double)scale);",
+        "double c = ld(dt, cos_t, p * half + i) * (double)scale;"),
+    "range_check_off_by_one": ("if (p < 0 || p >= cache_rows) {", "if (p < 0 || p > cache_rows) {"),
+    "angle_in_binary64": ("float theta = pf * inv;", "double theta = (double)pf * inv;"),
+    "half_rounding_truncates": ("double r = nearbyint(ldexp(a, 10 - E));",
+                                "double r = floor(ldexp(a, 10 - E));"),
+    "interleaved_map_order": ("for (int st = 0; st < 3; ++st)\n      if (r < sec[st]) {",
+                              "for (int st = 2; st >= 0; --st)\n      if (r < sec[st]) {"),
+    "per_token_row_shifted": ("crow = tok * half;", "crow = tok * half + (tok > 0);"),
+    "sin_from_cos_table": ("double sn = ld(dt, sin_t, crow + i);", "double sn = ld(dt, cos_t, crow + i);"),
+    "scaling_dropped": ("float cs = c32 * scaling;", "float cs = c32;"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTATIONS))
+def test_pins_catch_planted_mistake(tmp_path, name):
+    if shutil.which("gcc") is None:
+        pytest.skip("gcc not available")
+    src = open(os.path.join(ROOT, "oracle", "rope_oracle.c")).read()
+    old, new = MUTATIONS[name]
+    assert src.count(old) >= 1, f"mutation anchor for {name} no longer in the oracle source"
+    ign = shutil.ignore_patterns("_build", "*.so", "__pycache__")
+    shutil.copytree(os.path.join(ROOT, "oracle"), tmp_path / "oracle", ignore=ign)
+    (tmp_path / "oracle" / "rope_oracle.c").write_text(src.replace(old, new, 1))
+    shutil.copytree(os.path.join(ROOT, "tests"), tmp_path / "tests", ignore=ign)
+    pkg = tmp_path / "rotary_position_embedding_gb300"
+    pkg.mkdir()
+    for f in ("__init__.py", "workloads.py"):
+        shutil.copy(os.path.join(ROOT, "rotary_position_embedding_gb300", f), pkg / f)
+    r = subprocess.run([sys.executable, "-m", "pytest", "tests/test_oracle_pins.py", "-x", "-q",
+                        "-p", "no:cacheprovider"], cwd=tmp_path, capture_output=True, text=True,
+                       timeout=600)
+    assert r.returncode != 0, f"planted mistake {name!r} passed every pin:\n{r.stdout[-2000:]}"
+    assert "failed" in r.stdout, r.stdout[-2000:] + r.stderr[-2000:]
