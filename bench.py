@@ -1,0 +1,534 @@
+#!/usr/bin/env python
+"""Throughput benchmark of the rotary position embedding hot path on GB300.
+
+One step = one pass of RotaryEmbedding over one batch of the headline
+workload (rank-3 float16 X (4, 2048, 32*128), half split, position_ids
+gather from an (8192, 64) cos/sin cache), launched through the library's C
+ABI. Inputs are resident in HBM when the timed region starts; X/Y rotate over
+enough buffer sets that no step finds its inputs in L2.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gpu|reference]
+
+Prints one JSON line (rank 0). ``--impl reference`` times the CPU oracle (the
+only comparison implementation available) on a bounded sample of the same
+workload, on the host's cores. Under torchrun (N > 1) each rank runs the same
+per-GPU workload on its own batch (weak scaling, no data-path collective);
+the time is the maximum over ranks.
+"""
+
+import argparse
+import ctypes
+import hashlib
+import json
+import math
+import os
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from rotary_position_embedding_gb300 import workloads as wl  # noqa: E402
+
+L2_BYTES = 129 * 2 ** 20
+FALLBACK_HBM_GBS = 6800.0
+METRIC = "RoPE achieved HBM GB/s and Gelem/s, fp16, as % of GB300 HBM roofline"
+KERNEL_SOURCES = ["rope_kernels.cuh", "rope_internal.h", "rope_api.cu", "k_rope.cu", "k_mrope.cu",
+                  "k_fused.cu"]
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--impl", choices=["gpu", "reference"], default="gpu")
+    ap.add_argument("--workload", default=wl.HEADLINE, choices=list(wl.WORKLOADS))
+    ap.add_argument("--no-rows", action="store_true", help="skip the per-workload table")
+    ap.add_argument("--row-steps", type=int, default=400)
+    ap.add_argument("--e2e-steps", type=int, default=30)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (host-side timing reduction only)
+# ---------------------------------------------------------------------------
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), \
+        int(os.environ.get("LOCAL_RANK", 0))
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "rotary_position_embedding_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs: torch copy_, 1 Gi bf16)"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback (no MEASURED_PEAKS.json)"
+
+
+def profiled_traffic(kernel, workload):
+    """DRAM bytes per launch from a committed ncu capture, if taken on the current kernel source."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        e = d[f"{kernel}:{workload}"]
+        if e.get("source_hash") == kernel_source_hash():
+            return e["dram_bytes_per_launch"]
+    except Exception:
+        pass
+    return None
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-f", self.path], stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+        except FileNotFoundError:
+            self.proc = None
+        time.sleep(0.4)
+
+    def stop(self, t0, t1):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.strip().split(",")]
+                if len(parts) < 10:
+                    continue
+                try:
+                    ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                    ts += float("0." + parts[0].split(".")[1]) if "." in parts[0] else 0.0
+                    rows.append((ts, float(parts[2]), float(parts[3]), parts[5:]))
+                except (ValueError, IndexError):
+                    continue
+        os.unlink(self.path)
+        inside = [r for r in rows if t0 <= r[0] <= t1]
+        note = "samples inside the timed region"
+        if not inside and rows:  # region shorter than the sampling period: nearest samples
+            rows.sort(key=lambda r: min(abs(r[0] - t0), abs(r[0] - t1)))
+            inside = rows[:2]
+            note = "timed region shorter than the 100 ms sampling period: nearest samples"
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        names = ["active", "hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for r in inside:
+            for name, v in zip(names[1:], r[3][1:]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": float(np.median([r[1] for r in inside])), "sm_max_mhz": max(r[2] for r in inside),
+                "reasons": sorted(reasons), "samples": len(inside), "note": note}
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+
+class Step:
+    """One workload pass through the C ABI with pre-marshalled ctypes arguments."""
+
+    def __init__(self, rp, torch, w, device, n_sets):
+        self.w = w
+        self.torch = torch
+        lib = rp.load_library()
+        self.lib = lib
+        inp = wl.make_inputs(w)
+        self.x_host = inp["x"]
+        self.pos_host = inp["position_ids"]
+        tdt = torch.float16 if w.dtype == "float16" else torch.float32
+        self.code = 1 if w.dtype == "float16" else 0
+        self.inv = torch.from_numpy(inp["inv_freq"]).to(device)
+        x0 = torch.from_numpy(self.x_host).to(device)
+        self.xs = [x0] + [x0.clone() for _ in range(n_sets - 1)]
+        self.ys = [torch.empty_like(x0) for _ in range(n_sets)]
+        self.pos = None if self.pos_host is None else torch.from_numpy(self.pos_host).to(device)
+        self.nh = w.num_heads if w.rank == 3 else 0
+        self.xshape = (ctypes.c_int64 * w.rank)(*w.shape)
+        if w.kind == "rope" and w.positions == "none":
+            c, s = rp.rope_cache_build(self.inv, w.tokens, tdt)
+            self.cos, self.sin = c.view(w.batch, w.seq, w.half), s.view(w.batch, w.seq, w.half)
+        elif w.kind in ("rope", "mrope") or w.kind == "fused":
+            self.cos, self.sin = rp.rope_cache_build(self.inv, w.cache_rows, tdt,
+                                                     attention_scaling=w.attention_scaling)
+        self.cshape = (ctypes.c_int64 * self.cos.dim())(*self.cos.shape)
+        self.sec = (ctypes.c_int32 * 3)(*(w.mrope_section or (0, 0, 0)))
+        torch.cuda.synchronize()
+
+    def launch(self, k, stream, fused=False):
+        w = self.w
+        x = ctypes.c_void_p(self.xs[k].data_ptr())
+        y = ctypes.c_void_p(self.ys[k].data_ptr())
+        return self.call(x, y, stream, fused)
+
+    def call(self, x, y, stream, fused=False):
+        w = self.w
+        lib = self.lib
+        pos = None if self.pos is None else ctypes.c_void_p(self.pos.data_ptr())
+        cos = ctypes.c_void_p(self.cos.data_ptr())
+        sin = ctypes.c_void_p(self.sin.data_ptr())
+        if w.kind == "mrope":
+            st = lib.mrope_apply(self.code, w.rank, self.xshape, x, y, w.cache_rows, cos, sin, pos, self.sec,
+                                 w.mrope_layout, w.scale, w.interleaved, w.rotary_embedding_dim, self.nh, 0,
+                                 None, stream)
+        elif w.kind == "fused" and fused:
+            st = lib.rope_apply_fused(self.code, w.rank, self.xshape, x, y, ctypes.c_void_p(self.inv.data_ptr()),
+                                      w.attention_scaling, pos, w.interleaved, w.rotary_embedding_dim, self.nh,
+                                      stream)
+        else:
+            st = lib.rope_apply(self.code, w.rank, self.xshape, x, y, self.cos.dim(), self.cshape, cos, sin, pos,
+                                w.interleaved, w.rotary_embedding_dim, self.nh, None, stream)
+        if st != 0:
+            raise RuntimeError(f"{w.name}: status {st}: {lib.rope_last_error().decode()}")
+
+
+def n_buffer_sets(w):
+    per_set = 2 * w.numel * np.dtype(w.dtype).itemsize
+    return max(2, math.ceil(4 * L2_BYTES / per_set))
+
+
+def time_steps(torch, step, steps, stream_handle, fused=False, per_kernel=True):
+    """Time `steps` launches (rotating buffer sets) with CUDA events on the launching stream."""
+    n_sets = len(step.xs)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)] if per_kernel else None
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)] if per_kernel else None
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    torch.cuda._sleep(2_000_000)  # let the host queue launches ahead of the GPU
+    t_start.record()
+    for k in range(steps):
+        if per_kernel:
+            starts[k].record()
+        step.launch(k % n_sets, stream_handle, fused)
+        if per_kernel:
+            ends[k].record()
+    t_end.record()
+    torch.cuda.synchronize()
+    total_ms = t_start.elapsed_time(t_end)
+    kern = [s.elapsed_time(e) for s, e in zip(starts, ends)] if per_kernel else []
+    return total_ms, kern
+
+
+def gpu_arm(args, rank, world, local_rank):
+    import torch
+
+    import rotary_position_embedding_gb300 as rp
+
+    device = torch.device("cuda", local_rank)
+    torch.cuda.set_device(device)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=device)
+    rp.load_library()
+    w = wl.WORKLOADS[args.workload]
+    stream = torch.cuda.current_stream(device)
+    sh = ctypes.c_void_p(stream.cuda_stream)
+    nbytes = wl.algorithmic_bytes(w)
+    step = Step(rp, torch, w, device, n_buffer_sets(w))
+    for k in range(args.warmup):
+        step.launch(k % len(step.xs), sh)
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(local_rank if "CUDA_VISIBLE_DEVICES" not in os.environ else
+                           os.environ["CUDA_VISIBLE_DEVICES"].split(",")[local_rank])
+    if rank == 0:
+        sampler.start()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t0 = time.time()
+    total_ms, kern = time_steps(torch, step, args.steps, sh)
+    t1 = time.time()
+    if world > 1:
+        torch.distributed.barrier()
+        tt = torch.tensor([total_ms], dtype=torch.float64, device=device)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(tt.item())
+    clocks = sampler.stop(t0, t1) if rank == 0 else None
+
+    ms_per_step = total_ms / args.steps
+    value = world * nbytes * args.steps / (total_ms * 1e-3) / 1e9
+    gelem = world * w.numel * args.steps / (total_ms * 1e-3) / 1e9
+    kern_ms = float(np.mean(kern))
+    peak, peak_src = measured_peak()
+    achieved = nbytes / (kern_ms * 1e-3) / 1e9
+
+    out = None
+    if rank == 0:
+        rows = {} if args.no_rows else measure_rows(args, torch, rp, device, peak)
+        e2e = measure_e2e(args, torch, step, sh, nbytes)
+        cpu = cpu_baseline(args, w) if world == 1 else None
+        out = {
+            "metric": METRIC,
+            "value": round(value, 2),
+            "unit": "GB/s",
+            "gelem_per_s": round(gelem, 3),
+            "n_gpus": world,
+            "steps": args.steps,
+            "warmup": args.warmup,
+            "ms_per_step": round(ms_per_step, 6),
+            "higher_is_better": True,
+            "scaling": "weak",
+            "vs_baseline": None,
+            "dtype": "f16",
+            "data": "synthetic (seeded N(0,1) X, position ids per the workload recipe; caches from "
+                    "rope_cache_build)",
+            "config": {
+                "workload": w.name, "shape": list(w.shape), "num_heads": w.num_heads,
+                "head_size": w.head_size, "rotary_dim": w.rotary_dim, "interleaved": w.interleaved,
+                "cache_rows": w.cache_rows, "positions": "s + U[0,4096) per batch",
+                "algorithmic_bytes_per_step": nbytes,
+                "l2": f"inputs rotate over {len(step.xs)} X/Y buffer sets "
+                      f"({len(step.xs) * 2 * w.numel * 2 / 2**20:.0f} MiB) > 129 MiB L2; no flush kernel",
+                "launch": "one C-ABI call per step on torch's current stream; the host queues launches "
+                          "ahead of the GPU; timed region = CUDA events around the K steps",
+                "parallelism": f"{world} independent replicas (per-GPU batch)",
+            },
+            "roofline": {
+                "bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "traffic": profiled_traffic("rope_rows_kernel", w.name),
+                "peak_source": peak_src, "kernel": "rope_rows_kernel<half,8,half-split,rank3,cache2d>",
+                "kernel_us": round(kern_ms * 1e3, 3),
+                "frac_of_nominal_8tbs": round(achieved / 8000.0, 4),
+            },
+            "clocks": clocks,
+            "e2e": e2e,
+            "gpu_launches": args.steps,
+            "cpu_baseline": cpu,
+            "rows": rows,
+        }
+    if world > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+    return out
+
+
+def measure_rows(args, torch, rp, device, peak):
+    """Every workload (and both M-RoPE layouts, fused and cached decode), timed the same way."""
+    stream = torch.cuda.current_stream(device)
+    sh = ctypes.c_void_p(stream.cuda_stream)
+    rows = {}
+    for name, w in wl.WORKLOADS.items():
+        variants = [("cached", False)]
+        if w.kind == "fused":
+            variants = [("fused", True), ("cached", False)]
+        step = Step(rp, torch, w, device, n_buffer_sets(w))
+        for label, fused in variants:
+            for k in range(20):
+                step.launch(k % len(step.xs), sh, fused)
+            total_ms, kern = time_steps(torch, step, args.row_steps, sh, fused)
+            nbytes = wl.algorithmic_bytes(w, cached=not fused)
+            kern_ms = float(np.median(kern))
+            gbs = nbytes / (kern_ms * 1e-3) / 1e9
+            key = name if len(variants) == 1 else f"{name}:{label}"
+            rows[key] = {
+                "us_per_launch_median": round(kern_ms * 1e3, 3),
+                "us_per_step_incl_gaps": round(total_ms / args.row_steps * 1e3, 3),
+                "GB_s": round(gbs, 1), "Gelem_s": round(w.numel / (kern_ms * 1e-3) / 1e9, 2),
+                "frac_of_measured_peak": round(gbs / peak, 4), "frac_of_nominal_8tbs": round(gbs / 8000, 4),
+                "bytes": nbytes,
+            }
+        del step
+        torch.cuda.empty_cache()
+    # one-time setup row: cache build of the largest table
+    inv = torch.from_numpy(wl.inv_freq(1e6, 128, 64)).to(device)
+    c, s = rp.rope_cache_build(inv, 32768, torch.float16)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record()
+    for _ in range(10):
+        rp.rope_cache_build(inv, 32768, torch.float16, cos_out=c, sin_out=s)
+    ev1.record()
+    torch.cuda.synchronize()
+    rows["rope_cache_build(32768x64,f16)"] = {"us_per_launch": round(ev0.elapsed_time(ev1) / 10 * 1e3, 2)}
+    return rows
+
+
+def measure_e2e(args, torch, step, sh, nbytes):
+    """Same metric through the C ABI with host buffers: H2D of X and positions from
+    pinned memory, the launch, D2H of Y into pinned memory, every step."""
+    x_host = torch.from_numpy(step.x_host).pin_memory()
+    y_host = torch.empty_like(x_host).pin_memory()
+    pos_host = None if step.pos_host is None else torch.from_numpy(step.pos_host).pin_memory()
+    xd, yd = step.xs[0], step.ys[0]
+
+    def one():
+        xd.copy_(x_host, non_blocking=True)
+        if pos_host is not None:
+            step.pos.copy_(pos_host, non_blocking=True)
+        step.call(ctypes.c_void_p(xd.data_ptr()), ctypes.c_void_p(yd.data_ptr()), sh)
+        y_host.copy_(yd, non_blocking=True)
+
+    for _ in range(3):
+        one()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.e2e_steps):
+        one()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / args.e2e_steps
+    h2d = x_host.numel() * x_host.element_size() + (0 if pos_host is None else pos_host.numel() * 8)
+    d2h = y_host.numel() * y_host.element_size()
+    return {"value": round(nbytes / (ms * 1e-3) / 1e9, 2), "unit": "GB/s", "ms_per_step": round(ms, 4),
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "note": "pinned host X/positions -> device, rope_apply, device Y -> pinned host; cos/sin cache "
+                    "stays resident (model constant)"}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle (baseline leg and the reference arm)
+# ---------------------------------------------------------------------------
+
+class OracleStep:
+    """The oracle on the first `tokens` tokens of the workload (a bounded sample)."""
+
+    def __init__(self, w, tokens=None):
+        import oracle
+
+        self.oracle = oracle
+        self.w = w
+        inp = wl.make_inputs(w)
+        x, pos = inp["x"], inp["position_ids"]
+        dtype = np.dtype(w.dtype)
+        T = w.tokens if tokens is None else max(1, min(tokens, w.tokens))
+        S = w.seq
+        nb = max(1, math.ceil(T / S))
+        s_keep = S if T >= S else T
+        # rank 3 (B, S, N*H): whole batches, or a prefix of one sequence
+        if w.rank == 3:
+            self.x = np.ascontiguousarray(x[:nb, :s_keep])
+        else:
+            self.x = np.ascontiguousarray(x[:nb, :, :s_keep])
+        if pos is None:
+            self.pos = None
+        elif w.kind == "mrope":
+            self.pos = np.ascontiguousarray(pos[:, :nb, :s_keep])
+        else:
+            self.pos = np.ascontiguousarray(pos[:nb, :s_keep])
+        self.tokens = nb * s_keep
+        self.nh = w.num_heads if w.rank == 3 else 0
+        self.cos, self.sin = oracle.cache_build(inp["inv_freq"], w.cache_rows if w.positions != "none"
+                                                else w.tokens, dtype, w.attention_scaling)
+        if w.positions == "none":
+            self.cos = self.cos.reshape(w.batch, w.seq, w.half)[:nb, :s_keep]
+            self.sin = self.sin.reshape(w.batch, w.seq, w.half)[:nb, :s_keep]
+        self.inv = inp["inv_freq"]
+        self.bytes = wl.algorithmic_bytes(w) * self.tokens / w.tokens
+
+    def run(self):
+        w, o = self.w, self.oracle
+        if w.kind == "mrope":
+            o.mrope(self.x, self.cos, self.sin, self.pos, w.mrope_section, w.mrope_layout, w.scale,
+                    w.interleaved, w.rotary_embedding_dim, self.nh)
+        else:
+            o.rope(self.x, self.cos, self.sin, self.pos, w.interleaved, w.rotary_embedding_dim, self.nh)
+
+
+def cpu_baseline(args, w):
+    st = OracleStep(w)
+    st.run()  # warm
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        st.run()
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= args.cpu_seconds or reps >= 1000:
+            break
+    gbs = st.bytes * reps / el / 1e9
+    return {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{reps} full passes of {w.name} ({st.tokens} tokens each) in {el:.1f} s, "
+                      f"single-threaded C oracle (binary64 arithmetic)",
+            "host_cpus": os.cpu_count()}
+
+
+def reference_arm(args, rank, world):
+    if rank != 0:
+        return None
+    w = wl.WORKLOADS[args.workload]
+    # size each step so warmup + steps take about two minutes at the oracle's rate
+    probe = OracleStep(w, tokens=64)
+    t0 = time.perf_counter()
+    probe.run()
+    per_token = (time.perf_counter() - t0) / probe.tokens
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    tokens = int(max(1, min(w.tokens, budget / max(per_token, 1e-9))))
+    st = OracleStep(w, tokens=tokens)
+    for _ in range(args.warmup):
+        st.run()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        st.run()
+    el = time.perf_counter() - t0
+    gbs = st.bytes * args.steps / el / 1e9
+    gelem = (w.numel * st.tokens / w.tokens) * args.steps / el / 1e9
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(gbs, 5), "unit": "GB/s",
+        "gelem_per_s": round(gelem, 6), "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(el / args.steps * 1e3, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f16", "data": "synthetic (same generator as the GPU arm)",
+        "config": {"workload": w.name, "shape": list(w.shape), "sample_tokens_per_step": st.tokens,
+                   "note": "the pages publish no implementation to run; the reference arm is the CPU "
+                           "oracle on a bounded sample of the workload per step"},
+        "cpu_baseline": {"value": round(gbs, 5), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{st.tokens} of {w.tokens} tokens per step"},
+        "e2e": {"value": round(gbs, 5), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+
+
+def main():
+    args = parse_args()
+    rank, world, local_rank = dist_env()
+    if args.impl == "reference":
+        out = reference_arm(args, rank, world)
+    else:
+        out = gpu_arm(args, rank, world, local_rank)
+    if rank == 0 and out is not None:
+        print(json.dumps(out), flush=True)
+
+
+if __name__ == "__main__":
+    main()

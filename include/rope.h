@@ -1,0 +1,206 @@
+/*
+ * rope.h -- C ABI of the GB300 (sm_103a) rotary position embedding library
+ * (librope_gb300.so).
+ *
+ * Operations (web pages cited by title and section):
+ *   rope_apply        ONNX opset-23 RotaryEmbedding: "ai.onnx.RotaryEmbedding"
+ *                     WebGPU manifest (manifest.json) -- "inputs", "attributes",
+ *                     "attributeDescriptions", "derive" shape contracts.
+ *   mrope_apply       com.microsoft.MRotaryEmbedding: its README -- Description,
+ *                     Inputs, Attributes, Implementation variants.
+ *   rope_apply_fused  the on-the-fly cos/sin form of Qwen3 RoPE: onnxruntime
+ *                     pull request "Add RotaryEmbedding fusion for Qwen3
+ *                     on-the-fly RoPE patterns" -- Motivation and Context,
+ *                     Modeling Code Alignment Check.
+ *   rope_cache_build  the cos/sin cache that pull request precomputes from
+ *                     inv_freq -- Critical Issues 1, Medium Issues 4.
+ *
+ * Conventions shared by every entry point
+ *   - All tensors are dense, contiguous, row-major. Tensor pointers are DEVICE
+ *     pointers owned by the caller; the library never allocates, frees or
+ *     synchronises, keeps no state between calls and is safe to call from
+ *     several host threads. Shape and attribute arrays are HOST pointers read
+ *     during the call only.
+ *   - Work is enqueued asynchronously on `stream` (NULL = legacy default
+ *     stream) on the current CUDA device; all device pointers must belong to
+ *     that device.
+ *   - Element type T is float32 (ROPE_F32) or float16 (ROPE_F16); positions
+ *     are int64. Every pointer must be aligned to its element size. 16-byte
+ *     aligned tensors whose head and half-rotary widths are multiples of 16
+ *     bytes take the 128-bit vector path; anything else takes the scalar path.
+ *     Alignment is never an error.
+ *   - y may equal x (in place). Any other overlap between outputs and inputs
+ *     is undefined.
+ *   - Arithmetic: each pair (x0, x1) with coefficients (c, s) becomes
+ *     y0 = x0*c - x1*s, y1 = x1*c + x0*s, computed in float32 and rounded to
+ *     nearest-even to T. Elements past the rotary width, and pairs whose
+ *     position is out of range, are copied bit-exactly.
+ *   - Errors: on ROPE_ERR_INVALID_ARG / ROPE_ERR_UNSUPPORTED nothing is
+ *     launched and no output is written. ROPE_ERR_CUDA means a CUDA call
+ *     failed while launching. rope_last_error() returns a message for the
+ *     last failure on the calling thread.
+ *   - An empty X (any dimension 0) is valid and launches nothing.
+ */
+#ifndef ROPE_GB300_H
+#define ROPE_GB300_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum rope_status {
+  ROPE_OK = 0,
+  ROPE_ERR_INVALID_ARG = 1, /* shape / attribute contract violated */
+  ROPE_ERR_UNSUPPORTED = 2, /* valid ONNX, not implemented (other dtypes, packed batching) */
+  ROPE_ERR_CUDA = 3         /* a CUDA runtime call failed */
+} rope_status;
+
+typedef enum rope_dtype { ROPE_F32 = 0, ROPE_F16 = 1 } rope_dtype;
+
+/* A cudaStream_t (the two types are the same pointer type). */
+typedef struct CUstream_st* rope_stream_t;
+
+/*
+ * rope_apply -- RotaryEmbedding.
+ *
+ * x, y          X and Y, same shape: rank 3 (B, S, num_heads*H) or rank 4
+ *               (B, N, S, H). H must be even. ([RotaryEmbedding manifest,
+ *               inputs/X and outputs/Y])
+ * x_shape       x_rank (3 or 4) host int64 values.
+ * cos_cache,    With position_ids: rank 2, (max_sequence_length, rd/2); row p
+ * sin_cache     is the coefficient row of position p. Without position_ids:
+ *               rank 3, (B, S, rd/2); row (b, s) belongs to token (b, s).
+ *               cache_shape holds cache_rank host int64 values. Both tables
+ *               have this shape. ([manifest, inputs/cos_cache, sin_cache])
+ * position_ids  NULL, or device int64 (B, S). ([manifest, inputs/position_ids])
+ *               A position outside [0, max_sequence_length) never reads the
+ *               cache: every element of that token is copied through and, if
+ *               oor_flag is not NULL, the device int32 *oor_flag is set to 1
+ *               (it is never cleared by the library).
+ * interleaved   0: pair i is (i, i + rd/2); 1: pair i is (2i, 2i+1).
+ * rotary_embedding_dim  0 = H; otherwise an even rd with 0 < rd <= H. Elements
+ *               [rd, H) of every head are copied through.
+ * num_heads     required (>= 1, dividing the last dimension) for rank 3; for
+ *               rank 4 it must be 0 or equal to N.
+ * The shape contract is the manifest's "derive" rank3Contract, rank4Contract,
+ * rank3PosContract, rank4PosContract: cache width * 2 == rd, 3-D cache
+ * leading dims == (B, S), position_ids present iff the cache is 2-D.
+ */
+rope_status rope_apply(rope_dtype dtype, int32_t x_rank, const int64_t* x_shape, const void* x,
+                       void* y, int32_t cache_rank, const int64_t* cache_shape,
+                       const void* cos_cache, const void* sin_cache, const int64_t* position_ids,
+                       int32_t interleaved, int32_t rotary_embedding_dim, int32_t num_heads,
+                       int32_t* oor_flag, rope_stream_t stream);
+
+/*
+ * mrope_apply -- MRotaryEmbedding (multimodal RoPE).
+ *
+ * x, y, x_shape, interleaved, rotary_embedding_dim, num_heads: as rope_apply,
+ *               except that H may be odd when rd is a smaller even number
+ *               ([MRotaryEmbedding README, Description, Attributes/
+ *               rotary_embedding_dim]). rd/2 must not exceed 1024.
+ * cos_cache, sin_cache  device (cache_rows, rd/2), shared by the three
+ *               streams ([README, Inputs/cos]).
+ * position_ids  device int64 (3, B, S): temporal, height and width streams
+ *               ([README, Inputs/positionIds]). A pair whose stream position
+ *               is negative or >= cache_rows is copied through unchanged and
+ *               *oor_flag (if not NULL) is set to 1.
+ * mrope_section host int32[3], non-negative, summing to rd/2: how many
+ *               half-rotary indices each stream drives ([README, Attributes/
+ *               mrope_section]).
+ * mrope_layout  0: chunked -- indices [0, t) use t, the next h use h, the rest
+ *               w. 1: interleaved -- the streams are dealt round by round in
+ *               the order t, h, w, each for as many rounds as its section
+ *               count. ([README, Attributes/mrope_layout]; the page names the
+ *               interleaved layout without printing its order, this is the
+ *               reading that keeps each stream's count equal to its section.)
+ * scale         multiplies the gathered cos and sin; each scaled coefficient
+ *               is rounded to T before the rotation ([README, Attributes/
+ *               scale; Implementation variants/pairs4]). The product is
+ *               rounded once from its exact value.
+ * is_packed_batching  must be 0; 1 returns ROPE_ERR_UNSUPPORTED ([README,
+ *               Attributes/is_packed_batching]).
+ */
+rope_status mrope_apply(rope_dtype dtype, int32_t x_rank, const int64_t* x_shape, const void* x,
+                        void* y, int64_t cache_rows, const void* cos_cache,
+                        const void* sin_cache, const int64_t* position_ids,
+                        const int32_t* mrope_section, int32_t mrope_layout, float scale,
+                        int32_t interleaved, int32_t rotary_embedding_dim, int32_t num_heads,
+                        int32_t is_packed_batching, int32_t* oor_flag, rope_stream_t stream);
+
+/*
+ * mrope_apply_stream_map -- MRotaryEmbedding with an explicit stream per
+ * half-rotary index instead of (mrope_section, mrope_layout).
+ *
+ * stream_map    host uint8[rd/2], each 0 (t), 1 (h) or 2 (w). Lets a caller
+ *               use another interleaving convention than mrope_apply's layout 1
+ *               (for example fixed stride-3 slots). Everything else as
+ *               mrope_apply.
+ */
+rope_status mrope_apply_stream_map(rope_dtype dtype, int32_t x_rank, const int64_t* x_shape,
+                                   const void* x, void* y, int64_t cache_rows,
+                                   const void* cos_cache, const void* sin_cache,
+                                   const int64_t* position_ids, const uint8_t* stream_map,
+                                   float scale, int32_t interleaved,
+                                   int32_t rotary_embedding_dim, int32_t num_heads,
+                                   int32_t* oor_flag, rope_stream_t stream);
+
+/*
+ * mrope_stream_map -- host-only helper: the stream of each of the `half`
+ * half-rotary indices for (mrope_section, mrope_layout), as mrope_apply uses
+ * it. map_out is a host uint8[half]. ROPE_ERR_INVALID_ARG if the sections are
+ * negative or do not sum to half, or the layout is not 0 or 1. No CUDA call.
+ */
+rope_status mrope_stream_map(const int32_t* mrope_section, int32_t mrope_layout, int32_t half,
+                             uint8_t* map_out);
+
+/*
+ * rope_apply_fused -- RotaryEmbedding with cos/sin computed on the fly.
+ *
+ * For token (b, s) at position p = position_ids[b, s] and index i < rd/2
+ * ([Qwen3 fusion pull request, Motivation and Context; Modeling Code
+ * Alignment Check]):
+ *   theta = float32(float32(p) * inv_freq[i]),
+ *   c = T(float32(float32(cos(theta)) * attention_scaling)), s likewise,
+ * where cos/sin of the float32 angle are evaluated in double precision and
+ * rounded to float32; then the rotation of rope_apply. Any int64 position is
+ * valid (there is no cache to overrun).
+ *
+ * inv_freq      device float32[rd/2].
+ * position_ids  device int64 (B, S), required.
+ * Other arguments as rope_apply. The result equals rope_apply with tables from
+ * rope_cache_build(inv_freq, attention_scaling) gathered at the same positions.
+ */
+rope_status rope_apply_fused(rope_dtype dtype, int32_t x_rank, const int64_t* x_shape,
+                             const void* x, void* y, const float* inv_freq,
+                             float attention_scaling, const int64_t* position_ids,
+                             int32_t interleaved, int32_t rotary_embedding_dim,
+                             int32_t num_heads, rope_stream_t stream);
+
+/*
+ * rope_cache_build -- the (rows, half) cos and sin tables of rope_apply's
+ * 2-D cache: row p holds the coefficients rope_apply_fused computes for
+ * position p ([Qwen3 fusion pull request, Medium Issues 4: cos(freqs) *
+ * scaling with freqs[p, i] = p * inv_freq[i]]).
+ *
+ * inv_freq      device float32[half]; cos_out, sin_out device T[rows * half].
+ * half >= 1, rows >= 0.
+ */
+rope_status rope_cache_build(rope_dtype dtype, const float* inv_freq, int32_t half, int64_t rows,
+                             float attention_scaling, void* cos_out, void* sin_out,
+                             rope_stream_t stream);
+
+/* Static name of a status code. */
+const char* rope_status_string(rope_status status);
+
+/* Message describing the last failed call on the calling thread ("" if none).
+   Valid until the next call into the library on this thread. */
+const char* rope_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ROPE_GB300_H */

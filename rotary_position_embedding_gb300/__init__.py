@@ -1,4 +1,259 @@
-"""GB300-native rotary position embedding (RoPE / M-RoPE).
+"""GB300-native rotary position embedding: RoPE, M-RoPE, on-the-fly RoPE.
 
-Placeholder during bring-up; the binding is added with the CUDA library.
+A thin binding over the C ABI of ``librope_gb300.so`` (``include/rope.h``).
+This module only marshals arguments -- tensor pointers, shapes, attributes,
+the current CUDA stream -- and allocates outputs the way the operators' own
+JavaScript API does; every step of the computation runs in the library's
+CUDA kernels. PyTorch supplies device memory and streams.
+
+There is no CPU fallback: if the library cannot be loaded, every call raises.
 """
+
+import ctypes
+import os
+import threading
+
+from .build import LIB_PATH, build_library  # noqa: F401
+
+__all__ = [
+    "RopeError", "load_library", "build_library", "rope_apply", "mrope_apply",
+    "mrope_apply_stream_map", "mrope_stream_map", "rope_apply_fused", "rope_cache_build",
+    "ROPE_OK", "ROPE_ERR_INVALID_ARG", "ROPE_ERR_UNSUPPORTED", "ROPE_ERR_CUDA",
+]
+
+ROPE_OK, ROPE_ERR_INVALID_ARG, ROPE_ERR_UNSUPPORTED, ROPE_ERR_CUDA = 0, 1, 2, 3
+ROPE_F32, ROPE_F16 = 0, 1
+_UNSUPPORTED_DTYPE = 99  # passed through so the library reports ROPE_ERR_UNSUPPORTED
+
+_lock = threading.Lock()
+_lib = None
+
+_vp = ctypes.c_void_p
+_i32 = ctypes.c_int32
+_i64 = ctypes.c_int64
+_f32 = ctypes.c_float
+_i64p = ctypes.POINTER(ctypes.c_int64)
+_i32p = ctypes.POINTER(ctypes.c_int32)
+_u8p = ctypes.POINTER(ctypes.c_uint8)
+
+# name -> argtypes (restype is the int status unless listed in _RESTYPES)
+SIGNATURES = {
+    "rope_apply": [_i32, _i32, _i64p, _vp, _vp, _i32, _i64p, _vp, _vp, _vp, _i32, _i32, _i32, _vp, _vp],
+    "mrope_apply": [_i32, _i32, _i64p, _vp, _vp, _i64, _vp, _vp, _vp, _i32p, _i32, _f32, _i32, _i32,
+                    _i32, _i32, _vp, _vp],
+    "mrope_apply_stream_map": [_i32, _i32, _i64p, _vp, _vp, _i64, _vp, _vp, _vp, _u8p, _f32, _i32,
+                               _i32, _i32, _vp, _vp],
+    "mrope_stream_map": [_i32p, _i32, _i32, _u8p],
+    "rope_apply_fused": [_i32, _i32, _i64p, _vp, _vp, _vp, _f32, _vp, _i32, _i32, _i32, _vp],
+    "rope_cache_build": [_i32, _vp, _i32, _i64, _f32, _vp, _vp, _vp],
+    "rope_status_string": [_i32],
+    "rope_last_error": [],
+}
+_RESTYPES = {"rope_status_string": ctypes.c_char_p, "rope_last_error": ctypes.c_char_p}
+
+
+class RopeError(RuntimeError):
+    def __init__(self, fn, status, message):
+        self.status = status
+        self.message = message
+        names = {1: "ROPE_ERR_INVALID_ARG", 2: "ROPE_ERR_UNSUPPORTED", 3: "ROPE_ERR_CUDA"}
+        super().__init__(f"{fn}: {names.get(status, status)}: {message}")
+
+
+def load_library(path=None):
+    """Load librope_gb300.so (built in-tree by ``build_library()``)."""
+    global _lib
+    with _lock:
+        if _lib is not None and path is None:
+            return _lib
+        p = path or LIB_PATH
+        if not os.path.exists(p):
+            raise RuntimeError(
+                f"librope_gb300.so not found at {p}: run "
+                "`python -c 'import __graft_entry__ as g; g.build()'` (needs nvcc); "
+                "there is no CPU fallback")
+        lib = ctypes.CDLL(p)
+        for name, args in SIGNATURES.items():
+            fn = getattr(lib, name)
+            fn.argtypes = args
+            fn.restype = _RESTYPES.get(name, ctypes.c_int)
+        if path is None:
+            _lib = lib
+        return lib
+
+
+def _check(fn, status):
+    if status != ROPE_OK:
+        msg = load_library().rope_last_error().decode()
+        raise RopeError(fn, status, msg)
+
+
+# --------------------------------------------------------------------------
+# marshalling helpers (torch is imported lazily: the host-only helpers work
+# without it)
+# --------------------------------------------------------------------------
+
+def _dtype_code(t):
+    import torch
+
+    return {torch.float32: ROPE_F32, torch.float16: ROPE_F16}.get(t.dtype, _UNSUPPORTED_DTYPE)
+
+
+def _shape(t):
+    return (ctypes.c_int64 * max(1, t.dim()))(*[int(d) for d in t.shape])
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _cuda(name, t, dtype=None):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must have dtype {dtype}, got {t.dtype}")
+    return t
+
+
+def _stream(x, stream):
+    import torch
+
+    s = stream if stream is not None else torch.cuda.current_stream(x.device)
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _out(x, out):
+    import torch
+
+    if out is None:
+        return torch.empty_like(x)
+    _cuda("out", out, x.dtype)
+    if out.shape != x.shape:
+        raise ValueError(f"out shape {tuple(out.shape)} != x shape {tuple(x.shape)}")
+    return out
+
+
+# --------------------------------------------------------------------------
+# public API (same names as the C ABI)
+# --------------------------------------------------------------------------
+
+def rope_apply(x, cos_cache, sin_cache, position_ids=None, *, interleaved=0, rotary_embedding_dim=0,
+               num_heads=0, out=None, oor_flag=None, stream=None):
+    """RotaryEmbedding (see ``rope_apply`` in include/rope.h). Returns Y."""
+    import torch
+
+    lib = load_library()
+    _cuda("x", x)
+    _cuda("cos_cache", cos_cache)
+    _cuda("sin_cache", sin_cache)
+    _cuda("position_ids", position_ids, torch.int64)
+    _cuda("oor_flag", oor_flag, torch.int32)
+    y = _out(x, out)
+    with torch.cuda.device(x.device):
+        st = lib.rope_apply(_dtype_code(x), x.dim(), _shape(x), _ptr(x), _ptr(y), cos_cache.dim(),
+                            _shape(cos_cache), _ptr(cos_cache), _ptr(sin_cache), _ptr(position_ids),
+                            int(interleaved), int(rotary_embedding_dim), int(num_heads), _ptr(oor_flag),
+                            _stream(x, stream))
+    _check("rope_apply", st)
+    return y
+
+
+def mrope_apply(x, cos_cache, sin_cache, position_ids, mrope_section, *, mrope_layout=0, scale=1.0,
+                interleaved=0, rotary_embedding_dim=0, num_heads=0, is_packed_batching=0, out=None,
+                oor_flag=None, stream=None):
+    """MRotaryEmbedding (see ``mrope_apply`` in include/rope.h). Returns Y."""
+    import torch
+
+    lib = load_library()
+    _cuda("x", x)
+    _cuda("cos_cache", cos_cache)
+    _cuda("sin_cache", sin_cache)
+    _cuda("position_ids", position_ids, torch.int64)
+    _cuda("oor_flag", oor_flag, torch.int32)
+    y = _out(x, out)
+    sec = (ctypes.c_int32 * 3)(*[int(v) for v in mrope_section])
+    with torch.cuda.device(x.device):
+        st = lib.mrope_apply(_dtype_code(x), x.dim(), _shape(x), _ptr(x), _ptr(y), int(cos_cache.shape[0]),
+                             _ptr(cos_cache), _ptr(sin_cache), _ptr(position_ids), sec, int(mrope_layout),
+                             float(scale), int(interleaved), int(rotary_embedding_dim), int(num_heads),
+                             int(is_packed_batching), _ptr(oor_flag), _stream(x, stream))
+    _check("mrope_apply", st)
+    return y
+
+
+def mrope_apply_stream_map(x, cos_cache, sin_cache, position_ids, stream_map, *, scale=1.0, interleaved=0,
+                           rotary_embedding_dim=0, num_heads=0, out=None, oor_flag=None, stream=None):
+    """MRotaryEmbedding with an explicit stream (0 t, 1 h, 2 w) per half-rotary index."""
+    import torch
+
+    lib = load_library()
+    _cuda("x", x)
+    _cuda("cos_cache", cos_cache)
+    _cuda("sin_cache", sin_cache)
+    _cuda("position_ids", position_ids, torch.int64)
+    _cuda("oor_flag", oor_flag, torch.int32)
+    y = _out(x, out)
+    m = list(int(v) for v in stream_map)
+    arr = (ctypes.c_uint8 * max(1, len(m)))(*m)
+    with torch.cuda.device(x.device):
+        st = lib.mrope_apply_stream_map(_dtype_code(x), x.dim(), _shape(x), _ptr(x), _ptr(y),
+                                        int(cos_cache.shape[0]), _ptr(cos_cache), _ptr(sin_cache),
+                                        _ptr(position_ids), arr, float(scale), int(interleaved),
+                                        int(rotary_embedding_dim), int(num_heads), _ptr(oor_flag),
+                                        _stream(x, stream))
+    _check("mrope_apply_stream_map", st)
+    return y
+
+
+def mrope_stream_map(mrope_section, mrope_layout, half):
+    """Host helper: the stream of each half-rotary index, as mrope_apply uses it."""
+    lib = load_library()
+    sec = (ctypes.c_int32 * 3)(*[int(v) for v in mrope_section])
+    out = (ctypes.c_uint8 * max(1, int(half)))()
+    _check("mrope_stream_map", lib.mrope_stream_map(sec, int(mrope_layout), int(half), out))
+    return list(out)[: int(half)]
+
+
+def rope_apply_fused(x, inv_freq, position_ids, *, attention_scaling=1.0, interleaved=0,
+                     rotary_embedding_dim=0, num_heads=0, out=None, stream=None):
+    """RotaryEmbedding with cos/sin computed on the fly from inv_freq."""
+    import torch
+
+    lib = load_library()
+    _cuda("x", x)
+    _cuda("inv_freq", inv_freq, torch.float32)
+    _cuda("position_ids", position_ids, torch.int64)
+    y = _out(x, out)
+    with torch.cuda.device(x.device):
+        st = lib.rope_apply_fused(_dtype_code(x), x.dim(), _shape(x), _ptr(x), _ptr(y), _ptr(inv_freq),
+                                  float(attention_scaling), _ptr(position_ids), int(interleaved),
+                                  int(rotary_embedding_dim), int(num_heads), _stream(x, stream))
+    _check("rope_apply_fused", st)
+    return y
+
+
+def rope_cache_build(inv_freq, rows, dtype=None, *, attention_scaling=1.0, cos_out=None, sin_out=None,
+                     stream=None):
+    """(rows, len(inv_freq)) cos and sin tables. Returns (cos, sin)."""
+    import torch
+
+    lib = load_library()
+    _cuda("inv_freq", inv_freq, torch.float32)
+    dtype = dtype or torch.float16
+    half = int(inv_freq.shape[0])
+    if cos_out is None:
+        cos_out = torch.empty((int(rows), half), dtype=dtype, device=inv_freq.device)
+    if sin_out is None:
+        sin_out = torch.empty((int(rows), half), dtype=dtype, device=inv_freq.device)
+    _cuda("cos_out", cos_out, dtype)
+    _cuda("sin_out", sin_out, dtype)
+    code = _dtype_code(cos_out)
+    with torch.cuda.device(inv_freq.device):
+        st = lib.rope_cache_build(code, _ptr(inv_freq), half, int(rows), float(attention_scaling),
+                                  _ptr(cos_out), _ptr(sin_out), _stream(inv_freq, stream))
+    _check("rope_cache_build", st)
+    return cos_out, sin_out

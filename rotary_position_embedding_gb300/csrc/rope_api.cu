@@ -1,0 +1,525 @@
+// C ABI of librope_gb300.so: argument validation (the operators' shape and
+// attribute contracts), variant selection and launch geometry. Kernels live
+// in k_rope.cu, k_mrope.cu and k_fused.cu.
+//
+// Contracts followed (web pages, by title and section):
+//  - "ai.onnx.RotaryEmbedding" WebGPU manifest, "derive": rank3Contract,
+//    rank4Contract, rank3PosContract, rank4PosContract; attributeConstraints
+//    (interleaved in {0, 1}); typeConstraints (T in {float32, float16}).
+//  - "com.microsoft.MRotaryEmbedding" README, Attributes: mrope_section (three
+//    non-negative counts summing to rd/2), mrope_layout (0 chunked, 1
+//    interleaved), is_packed_batching (only 0), rotary_embedding_dim (even,
+//    may leave an odd head size), num_heads.
+// The library allocates nothing, keeps no per-call state and never
+// synchronises; host-side failures return before any launch.
+#include <cuda_runtime.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <string>
+#include <tuple>
+
+#include "../../include/rope.h"
+#include "rope_internal.h"
+
+// Launch-shape defaults (threads a CTA aims for; resident-CTA waves in the
+// persistent grid). Overridable at compile time.
+#ifndef ROPE_TARGET_THREADS
+#define ROPE_TARGET_THREADS 256
+#endif
+#ifndef ROPE_GRID_WAVES
+#define ROPE_GRID_WAVES 1
+#endif
+
+using namespace rope_gb300;
+
+namespace {
+
+thread_local std::string g_last_error;
+
+rope_status fail(rope_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return st;
+}
+
+rope_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(ROPE_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+int elem_size(rope_dtype dt) { return dt == ROPE_F16 ? 2 : 4; }
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Multiply non-negative sizes; false on int64 overflow.
+bool mul_ok(int64_t a, int64_t b, int64_t* out) {
+  if (a == 0 || b == 0) {
+    *out = 0;
+    return true;
+  }
+  if (a > INT64_MAX / b) return false;
+  *out = a * b;
+  return true;
+}
+
+// ---------------------------------------------------------------------------
+// Device facts, cached per device (SM count) and per kernel configuration
+// (resident CTAs per SM).
+// ---------------------------------------------------------------------------
+std::mutex g_mu;
+std::map<int, int> g_sm_count;
+std::map<std::tuple<int, const void*, int, size_t>, int> g_occupancy;
+
+rope_status device_facts(const void* fn, int threads, size_t smem, int* sms, int* per_sm) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  std::lock_guard<std::mutex> lk(g_mu);
+  auto it = g_sm_count.find(dev);
+  if (it == g_sm_count.end()) {
+    int n = 0;
+    e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute(SM count)");
+    it = g_sm_count.emplace(dev, n).first;
+  }
+  *sms = it->second;
+  auto key = std::make_tuple(dev, fn, threads, smem);
+  auto oc = g_occupancy.find(key);
+  if (oc == g_occupancy.end()) {
+    int b = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, fn, threads, smem);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
+    if (b < 1) b = 1;
+    oc = g_occupancy.emplace(key, b).first;
+  }
+  *per_sm = oc->second;
+  return ROPE_OK;
+}
+
+// ---------------------------------------------------------------------------
+// X geometry.
+// ---------------------------------------------------------------------------
+struct Geom {
+  int64_t B = 0, S = 0, N = 0, H = 0, ntok = 0, numel = 0;
+  int64_t rd = 0, h = 0;
+};
+
+// RotaryEmbedding manifest, inputs/X and attributeDescriptions/num_heads:
+// rank 3 is (B, S, num_heads*H) and needs num_heads; rank 4 is (B, N, S, H).
+rope_status x_geometry(int32_t rank, const int64_t* xs, int32_t num_heads, Geom* g) {
+  if (!xs) return fail(ROPE_ERR_INVALID_ARG, "x_shape is NULL");
+  if (rank != 3 && rank != 4) return fail(ROPE_ERR_INVALID_ARG, "X must be rank 3 or 4, got %d", rank);
+  for (int i = 0; i < rank; ++i)
+    if (xs[i] < 0) return fail(ROPE_ERR_INVALID_ARG, "x_shape[%d] = %lld is negative", i, (long long)xs[i]);
+  if (rank == 3) {
+    if (num_heads < 1)
+      return fail(ROPE_ERR_INVALID_ARG, "num_heads must be >= 1 for rank-3 X (got %d)", num_heads);
+    if (xs[2] % num_heads != 0)
+      return fail(ROPE_ERR_INVALID_ARG, "hidden size %lld is not a multiple of num_heads %d",
+                  (long long)xs[2], num_heads);
+    g->B = xs[0];
+    g->S = xs[1];
+    g->N = num_heads;
+    g->H = xs[2] / num_heads;
+  } else {
+    if (num_heads != 0 && num_heads != xs[1])
+      return fail(ROPE_ERR_INVALID_ARG, "num_heads %d does not match rank-4 X dim 1 (%lld)", num_heads,
+                  (long long)xs[1]);
+    g->B = xs[0];
+    g->N = xs[1];
+    g->S = xs[2];
+    g->H = xs[3];
+  }
+  int64_t t;
+  if (!mul_ok(g->B, g->S, &g->ntok) || !mul_ok(g->ntok, g->N, &t) || !mul_ok(t, g->H, &g->numel))
+    return fail(ROPE_ERR_INVALID_ARG, "X has more than 2^63 elements");
+  return ROPE_OK;
+}
+
+// rotary_embedding_dim: 0 = the whole head; else even, 0 < rd <= H.
+rope_status rotary_width(int32_t rde, bool odd_head_ok, Geom* g) {
+  if (rde < 0) return fail(ROPE_ERR_INVALID_ARG, "rotary_embedding_dim %d is negative", rde);
+  if (rde > g->H)
+    return fail(ROPE_ERR_INVALID_ARG, "rotary_embedding_dim %d exceeds the head size %lld", rde,
+                (long long)g->H);
+  if (!odd_head_ok && g->H % 2)
+    return fail(ROPE_ERR_INVALID_ARG, "head size %lld must be even", (long long)g->H);
+  g->rd = rde ? rde : g->H;
+  if (g->rd % 2)
+    return fail(ROPE_ERR_INVALID_ARG, "rotary width %lld must be even (a head size of %lld needs an "
+                "even rotary_embedding_dim)", (long long)g->rd, (long long)g->H);
+  g->h = g->rd / 2;
+  return ROPE_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Launch geometry: fixed thread roles (see KParams).
+// ---------------------------------------------------------------------------
+struct Launch {
+  dim3 grid, block;
+  size_t smem = 0;
+};
+
+rope_status plan(const Geom& g, int es, bool vec, const void* fn, bool smem_table, KParams* kp,
+                 Launch* L) {
+  const int V = vec ? 16 / es : 1;
+  const int64_t nP = g.h / V;
+  const int64_t nT = (g.H - g.rd) / V;
+  const int64_t U = nP + nT;
+  if (U < 1) return fail(ROPE_ERR_INVALID_ARG, "empty head");
+  const int64_t Ublk = U < 1024 ? U : 1024;
+  int64_t NG = g.N;
+  if (NG * Ublk > 1024) {
+    NG = 512 / Ublk;
+    if (NG < 1) NG = 1;
+  }
+  const int64_t per_tok = NG * Ublk;
+  int64_t TTs = ROPE_TARGET_THREADS / per_tok;
+  if (TTs < 1) TTs = 1;
+  if (TTs * per_tok > 1024) TTs = 1024 / per_tok;
+  if (TTs > g.ntok) TTs = g.ntok;
+  const int threads = (int)(TTs * per_tok);
+  const size_t smem = smem_table ? (size_t)2 * TTs * g.h * es : 0;
+  int sms = 0, per_sm = 0;
+  rope_status st = device_facts(fn, threads, smem, &sms, &per_sm);
+  if (st != ROPE_OK) return st;
+  const int64_t tiles = (g.ntok + TTs - 1) / TTs;
+  int64_t gx = (int64_t)sms * per_sm * ROPE_GRID_WAVES;
+  if (gx > tiles) gx = tiles;
+  if (gx > 0x7fffffff) gx = 0x7fffffff;
+  const int64_t gy = (g.N + NG - 1) / NG;
+  if (gy > 65535) return fail(ROPE_ERR_UNSUPPORTED, "too many head groups (%lld)", (long long)gy);
+
+  kp->ntok = g.ntok;
+  kp->S = g.S;
+  kp->N = g.N;
+  kp->H = g.H;
+  kp->h = (int32_t)g.h;
+  kp->rd = (int32_t)g.rd;
+  kp->U = (int32_t)U;
+  kp->nP = (int32_t)nP;
+  kp->Ublk = (int32_t)Ublk;
+  kp->NG = (int32_t)NG;
+  kp->TTs = (int32_t)TTs;
+  kp->step_tok = gx * TTs;
+  kp->step_b = g.S ? kp->step_tok / g.S : 0;
+  kp->step_s = g.S ? kp->step_tok % g.S : 0;
+  L->grid = dim3((unsigned)gx, (unsigned)gy, 1);
+  L->block = dim3((unsigned)threads, 1, 1);
+  L->smem = smem;
+  return ROPE_OK;
+}
+
+rope_status launch(const void* fn, const Launch& L, KParams* kp, rope_stream_t stream) {
+  void* args[] = {kp};
+  cudaError_t e = cudaLaunchKernel(fn, L.grid, L.block, args, L.smem, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
+  return ROPE_OK;
+}
+
+bool vector_ok(const Geom& g, int es, std::initializer_list<const void*> ptrs) {
+  const int V = 16 / es;
+  if (g.H % V || g.h % V) return false;
+  for (const void* p : ptrs)
+    if (p && !aligned(p, 16)) return false;
+  return true;
+}
+
+rope_status check_dtype(rope_dtype dt) {
+  if (dt != ROPE_F32 && dt != ROPE_F16)
+    return fail(ROPE_ERR_UNSUPPORTED, "dtype %d: only float32 (0) and float16 (1) are implemented",
+                (int)dt);
+  return ROPE_OK;
+}
+
+rope_status check_elem_ptr(const void* p, const char* name, size_t align) {
+  if (!p) return fail(ROPE_ERR_INVALID_ARG, "%s is NULL", name);
+  if (!aligned(p, align))
+    return fail(ROPE_ERR_INVALID_ARG, "%s is not aligned to %zu bytes", name, align);
+  return ROPE_OK;
+}
+
+#define ROPE_TRY(expr)               \
+  do {                               \
+    rope_status _s = (expr);         \
+    if (_s != ROPE_OK) return _s;    \
+  } while (0)
+
+// Interleaved stream map: walk t, h, w cyclically, skipping streams whose
+// section count is used up, so every stream gets exactly its section count.
+rope_status build_stream_map(const int32_t* sec, int32_t layout, int64_t half, uint8_t* map) {
+  if (!sec) return fail(ROPE_ERR_INVALID_ARG, "mrope_section is NULL");
+  int64_t total = 0;
+  for (int k = 0; k < 3; ++k) {
+    if (sec[k] < 0) return fail(ROPE_ERR_INVALID_ARG, "mrope_section[%d] = %d is negative", k, sec[k]);
+    total += sec[k];
+  }
+  if (total != half)
+    return fail(ROPE_ERR_INVALID_ARG, "mrope_section sums to %lld, rotary width / 2 is %lld",
+                (long long)total, (long long)half);
+  if (layout == 0) {
+    int64_t i = 0;
+    for (int k = 0; k < 3; ++k)
+      for (int32_t c = 0; c < sec[k]; ++c) map[i++] = (uint8_t)k;
+    return ROPE_OK;
+  }
+  if (layout == 1) {
+    int64_t used[3] = {0, 0, 0};
+    int cur = 0;
+    for (int64_t i = 0; i < half; ++i) {
+      while (used[cur] >= sec[cur]) cur = (cur + 1) % 3;  // total == half: some stream has room
+      map[i] = (uint8_t)cur;
+      ++used[cur];
+      cur = (cur + 1) % 3;
+    }
+    return ROPE_OK;
+  }
+  return fail(ROPE_ERR_INVALID_ARG, "mrope_layout must be 0 or 1 (got %d)", layout);
+}
+
+// Shared M-RoPE body for mrope_apply and mrope_apply_stream_map.
+rope_status mrope_common(rope_dtype dtype, int32_t x_rank, const int64_t* x_shape, const void* x,
+                         void* y, int64_t cache_rows, const void* cos_cache, const void* sin_cache,
+                         const int64_t* position_ids, const int32_t* sec, int32_t layout,
+                         const uint8_t* explicit_map, float scale, int32_t interleaved,
+                         int32_t rde, int32_t num_heads, int32_t* oor_flag, rope_stream_t stream) {
+  ROPE_TRY(check_dtype(dtype));
+  Geom g;
+  ROPE_TRY(x_geometry(x_rank, x_shape, num_heads, &g));
+  if (interleaved != 0 && interleaved != 1)
+    return fail(ROPE_ERR_INVALID_ARG, "interleaved must be 0 or 1 (got %d)", interleaved);
+  ROPE_TRY(rotary_width(rde, /*odd_head_ok=*/true, &g));
+  if (g.h > kMaxMRopeHalf)
+    return fail(ROPE_ERR_UNSUPPORTED, "M-RoPE rotary width / 2 = %lld exceeds %d", (long long)g.h,
+                kMaxMRopeHalf);
+  if (cache_rows < 0) return fail(ROPE_ERR_INVALID_ARG, "cache_rows is negative");
+  uint8_t map[kMaxMRopeHalf];
+  if (explicit_map) {
+    for (int64_t i = 0; i < g.h; ++i) {
+      if (explicit_map[i] > 2)
+        return fail(ROPE_ERR_INVALID_ARG, "stream_map[%lld] = %d is not 0, 1 or 2", (long long)i,
+                    explicit_map[i]);
+      map[i] = explicit_map[i];
+    }
+  } else if (g.h > 0) {
+    ROPE_TRY(build_stream_map(sec, layout, g.h, map));
+  }
+  if (g.numel == 0) return ROPE_OK;
+  const int es = elem_size(dtype);
+  ROPE_TRY(check_elem_ptr(x, "x", es));
+  ROPE_TRY(check_elem_ptr(y, "y", es));
+  ROPE_TRY(check_elem_ptr(position_ids, "position_ids", 8));
+  if (cache_rows > 0) {
+    ROPE_TRY(check_elem_ptr(cos_cache, "cos_cache", es));
+    ROPE_TRY(check_elem_ptr(sin_cache, "sin_cache", es));
+  }
+  if (oor_flag && !aligned(oor_flag, 4)) return fail(ROPE_ERR_INVALID_ARG, "oor_flag is misaligned");
+
+  const bool vec = vector_ok(g, es, {x, y, cos_cache, sin_cache});
+  const void* fn = rope_kernel_mrope(dtype, vec, interleaved != 0, x_rank == 4);
+  KParams kp;
+  memset(&kp, 0, sizeof(kp));
+  kp.x = x;
+  kp.y = y;
+  kp.cos = cos_cache;
+  kp.sin = sin_cache;
+  kp.pos = position_ids;
+  kp.oor_flag = oor_flag;
+  kp.scale = scale;
+  kp.scale_is_one = scale == 1.0f;
+  kp.cache_rows = cache_rows;
+  for (int64_t i = 0; i < g.h; ++i) kp.smap[i >> 4] |= (uint32_t)map[i] << ((i & 15) * 2);
+  Launch L;
+  ROPE_TRY(plan(g, es, vec, fn, false, &kp, &L));
+  return launch(fn, L, &kp, stream);
+}
+
+}  // namespace
+
+extern "C" {
+
+rope_status rope_apply(rope_dtype dtype, int32_t x_rank, const int64_t* x_shape, const void* x,
+                       void* y, int32_t cache_rank, const int64_t* cache_shape,
+                       const void* cos_cache, const void* sin_cache, const int64_t* position_ids,
+                       int32_t interleaved, int32_t rotary_embedding_dim, int32_t num_heads,
+                       int32_t* oor_flag, rope_stream_t stream) {
+  g_last_error.clear();
+  ROPE_TRY(check_dtype(dtype));
+  Geom g;
+  ROPE_TRY(x_geometry(x_rank, x_shape, num_heads, &g));
+  if (interleaved != 0 && interleaved != 1)
+    return fail(ROPE_ERR_INVALID_ARG, "interleaved must be 0 or 1 (got %d)", interleaved);
+  ROPE_TRY(rotary_width(rotary_embedding_dim, /*odd_head_ok=*/false, &g));
+  if (!cache_shape) return fail(ROPE_ERR_INVALID_ARG, "cache_shape is NULL");
+  int64_t rows = 0;
+  if (position_ids) {
+    if (cache_rank != 2)
+      return fail(ROPE_ERR_INVALID_ARG, "with position_ids the cos/sin cache must be rank 2, got %d",
+                  cache_rank);
+    if (cache_shape[0] < 0) return fail(ROPE_ERR_INVALID_ARG, "cache rows are negative");
+    if (cache_shape[1] * 2 != g.rd)
+      return fail(ROPE_ERR_INVALID_ARG, "cache width %lld * 2 != rotary width %lld",
+                  (long long)cache_shape[1], (long long)g.rd);
+    rows = cache_shape[0];
+  } else {
+    if (cache_rank != 3)
+      return fail(ROPE_ERR_INVALID_ARG, "without position_ids the cos/sin cache must be rank 3, got %d",
+                  cache_rank);
+    if (cache_shape[0] != g.B || cache_shape[1] != g.S || cache_shape[2] * 2 != g.rd)
+      return fail(ROPE_ERR_INVALID_ARG,
+                  "3-D cache shape (%lld, %lld, %lld) must be (B, S, rd/2) = (%lld, %lld, %lld)",
+                  (long long)cache_shape[0], (long long)cache_shape[1], (long long)cache_shape[2],
+                  (long long)g.B, (long long)g.S, (long long)g.h);
+  }
+  if (g.numel == 0) return ROPE_OK;
+  const int es = elem_size(dtype);
+  ROPE_TRY(check_elem_ptr(x, "x", es));
+  ROPE_TRY(check_elem_ptr(y, "y", es));
+  if (!position_ids || rows > 0) {
+    ROPE_TRY(check_elem_ptr(cos_cache, "cos_cache", es));
+    ROPE_TRY(check_elem_ptr(sin_cache, "sin_cache", es));
+  }
+  if (position_ids && !aligned(position_ids, 8))
+    return fail(ROPE_ERR_INVALID_ARG, "position_ids is not aligned to 8 bytes");
+  if (oor_flag && !aligned(oor_flag, 4)) return fail(ROPE_ERR_INVALID_ARG, "oor_flag is misaligned");
+
+  const bool vec = vector_ok(g, es, {x, y, cos_cache, sin_cache});
+  const Coef mode = position_ids ? Coef::kCache2D : Coef::kCache3D;
+  const void* fn = rope_kernel_cached(dtype, vec, interleaved != 0, x_rank == 4, mode);
+  KParams kp;
+  memset(&kp, 0, sizeof(kp));
+  kp.x = x;
+  kp.y = y;
+  kp.cos = cos_cache;
+  kp.sin = sin_cache;
+  kp.pos = position_ids;
+  kp.oor_flag = oor_flag;
+  kp.scale = 1.0f;
+  kp.scale_is_one = 1;
+  kp.cache_rows = rows;
+  Launch L;
+  ROPE_TRY(plan(g, es, vec, fn, false, &kp, &L));
+  return launch(fn, L, &kp, stream);
+}
+
+rope_status mrope_apply(rope_dtype dtype, int32_t x_rank, const int64_t* x_shape, const void* x,
+                        void* y, int64_t cache_rows, const void* cos_cache,
+                        const void* sin_cache, const int64_t* position_ids,
+                        const int32_t* mrope_section, int32_t mrope_layout, float scale,
+                        int32_t interleaved, int32_t rotary_embedding_dim, int32_t num_heads,
+                        int32_t is_packed_batching, int32_t* oor_flag, rope_stream_t stream) {
+  g_last_error.clear();
+  if (is_packed_batching == 1)
+    return fail(ROPE_ERR_UNSUPPORTED, "is_packed_batching = 1 (packed batching) is not implemented");
+  if (is_packed_batching != 0)
+    return fail(ROPE_ERR_INVALID_ARG, "is_packed_batching must be 0 or 1 (got %d)", is_packed_batching);
+  if (!mrope_section) return fail(ROPE_ERR_INVALID_ARG, "mrope_section is NULL");
+  return mrope_common(dtype, x_rank, x_shape, x, y, cache_rows, cos_cache, sin_cache, position_ids,
+                      mrope_section, mrope_layout, nullptr, scale, interleaved,
+                      rotary_embedding_dim, num_heads, oor_flag, stream);
+}
+
+rope_status mrope_apply_stream_map(rope_dtype dtype, int32_t x_rank, const int64_t* x_shape,
+                                   const void* x, void* y, int64_t cache_rows,
+                                   const void* cos_cache, const void* sin_cache,
+                                   const int64_t* position_ids, const uint8_t* stream_map,
+                                   float scale, int32_t interleaved,
+                                   int32_t rotary_embedding_dim, int32_t num_heads,
+                                   int32_t* oor_flag, rope_stream_t stream) {
+  g_last_error.clear();
+  if (!stream_map) return fail(ROPE_ERR_INVALID_ARG, "stream_map is NULL");
+  return mrope_common(dtype, x_rank, x_shape, x, y, cache_rows, cos_cache, sin_cache, position_ids,
+                      nullptr, 0, stream_map, scale, interleaved, rotary_embedding_dim, num_heads,
+                      oor_flag, stream);
+}
+
+rope_status mrope_stream_map(const int32_t* mrope_section, int32_t mrope_layout, int32_t half,
+                             uint8_t* map_out) {
+  g_last_error.clear();
+  if (half < 0) return fail(ROPE_ERR_INVALID_ARG, "half is negative");
+  if (!map_out && half > 0) return fail(ROPE_ERR_INVALID_ARG, "map_out is NULL");
+  return build_stream_map(mrope_section, mrope_layout, half, map_out);
+}
+
+rope_status rope_apply_fused(rope_dtype dtype, int32_t x_rank, const int64_t* x_shape,
+                             const void* x, void* y, const float* inv_freq,
+                             float attention_scaling, const int64_t* position_ids,
+                             int32_t interleaved, int32_t rotary_embedding_dim,
+                             int32_t num_heads, rope_stream_t stream) {
+  g_last_error.clear();
+  ROPE_TRY(check_dtype(dtype));
+  Geom g;
+  ROPE_TRY(x_geometry(x_rank, x_shape, num_heads, &g));
+  if (interleaved != 0 && interleaved != 1)
+    return fail(ROPE_ERR_INVALID_ARG, "interleaved must be 0 or 1 (got %d)", interleaved);
+  ROPE_TRY(rotary_width(rotary_embedding_dim, /*odd_head_ok=*/false, &g));
+  if (g.numel == 0) return ROPE_OK;
+  const int es = elem_size(dtype);
+  ROPE_TRY(check_elem_ptr(x, "x", es));
+  ROPE_TRY(check_elem_ptr(y, "y", es));
+  ROPE_TRY(check_elem_ptr(inv_freq, "inv_freq", 4));
+  ROPE_TRY(check_elem_ptr(position_ids, "position_ids", 8));
+
+  const bool vec = vector_ok(g, es, {x, y});
+  const void* fn = fused_kernel(dtype, vec, interleaved != 0, x_rank == 4);
+  KParams kp;
+  memset(&kp, 0, sizeof(kp));
+  kp.x = x;
+  kp.y = y;
+  kp.pos = position_ids;
+  kp.inv_freq = inv_freq;
+  kp.scale = attention_scaling;
+  Launch L;
+  ROPE_TRY(plan(g, es, vec, fn, true, &kp, &L));
+  return launch(fn, L, &kp, stream);
+}
+
+rope_status rope_cache_build(rope_dtype dtype, const float* inv_freq, int32_t half, int64_t rows,
+                             float attention_scaling, void* cos_out, void* sin_out,
+                             rope_stream_t stream) {
+  g_last_error.clear();
+  ROPE_TRY(check_dtype(dtype));
+  if (half < 1) return fail(ROPE_ERR_INVALID_ARG, "half must be >= 1 (got %d)", half);
+  if (rows < 0) return fail(ROPE_ERR_INVALID_ARG, "rows is negative");
+  int64_t total;
+  if (!mul_ok(rows, half, &total)) return fail(ROPE_ERR_INVALID_ARG, "rows * half overflows");
+  if (total == 0) return ROPE_OK;
+  const int es = elem_size(dtype);
+  ROPE_TRY(check_elem_ptr(inv_freq, "inv_freq", 4));
+  ROPE_TRY(check_elem_ptr(cos_out, "cos_out", es));
+  ROPE_TRY(check_elem_ptr(sin_out, "sin_out", es));
+  const void* fn = cache_build_kernel(dtype);
+  int sms = 0, per_sm = 0;
+  ROPE_TRY(device_facts(fn, 256, 0, &sms, &per_sm));
+  int64_t blocks = (total + 255) / 256;
+  if (blocks > (int64_t)sms * per_sm) blocks = (int64_t)sms * per_sm;
+  void* args[] = {&inv_freq, &half, &rows, &attention_scaling, &cos_out, &sin_out};
+  cudaError_t e = cudaLaunchKernel(fn, dim3((unsigned)blocks), dim3(256), args, 0, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "rope_cache_build launch");
+  return ROPE_OK;
+}
+
+const char* rope_status_string(rope_status status) {
+  switch (status) {
+    case ROPE_OK:
+      return "ROPE_OK";
+    case ROPE_ERR_INVALID_ARG:
+      return "ROPE_ERR_INVALID_ARG";
+    case ROPE_ERR_UNSUPPORTED:
+      return "ROPE_ERR_UNSUPPORTED";
+    case ROPE_ERR_CUDA:
+      return "ROPE_ERR_CUDA";
+  }
+  return "ROPE_ERR_UNKNOWN";
+}
+
+const char* rope_last_error(void) { return g_last_error.c_str(); }
+
+}  // extern "C"

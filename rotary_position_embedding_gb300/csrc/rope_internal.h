@@ -1,0 +1,57 @@
+// Internal interface between the C-ABI layer (rope_api.cu) and the kernel
+// translation units. Not installed; not part of the public ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace rope_gb300 {
+
+enum class Coef : int {
+  kCache2D = 0,  // (rows, rd/2) table gathered at position_ids[b, s]
+  kCache3D = 1,  // (B, S, rd/2) table, row (b, s)
+  kMRope = 2,    // (rows, rd/2) table gathered per pair at one of three streams
+};
+
+// Largest half-rotary width the M-RoPE stream map (2 bits per index) holds.
+constexpr int kMaxMRopeHalf = 1024;
+
+// Everything a kernel needs, passed by value (kernel parameter space).
+//
+// Work decomposition. A head row of H elements is split into U "units":
+//   nP pair units, each covering V rotation pairs (V = 16 bytes / sizeof(T) on
+//   the vector path, 1 on the scalar path), then (H - rd) / V tail units that
+//   copy V elements each. A CTA owns TTs tokens ("token slots") times NG heads
+//   times Ublk units; thread t has the fixed role
+//     slot = t / (NG*Ublk), head = blockIdx.y*NG + (t / Ublk) % NG, unit = t % Ublk
+//   and walks tokens slot + blockIdx.x*TTs, + step_tok, ... (and units
+//   unit, unit + Ublk, ... when a row has more than Ublk units).
+struct KParams {
+  const void* x;
+  void* y;
+  const void* cos;
+  const void* sin;
+  const int64_t* pos;
+  int32_t* oor_flag;
+  const float* inv_freq;
+  float scale;           // M-RoPE coefficient scale, or on-the-fly attention scaling
+  int32_t scale_is_one;  // M-RoPE: skip the scale-and-round step
+  int64_t ntok;          // B*S tokens
+  int64_t S, N, H;       // sequence length, heads, head size (elements)
+  int64_t cache_rows;    // rows of a 2-D table (range check)
+  int32_t h, rd;         // half rotary width, rotary width (elements)
+  int32_t U, nP, Ublk;
+  int32_t NG, TTs;
+  int64_t step_tok;      // gridDim.x * TTs
+  int64_t step_b, step_s;  // step_tok = step_b * S + step_s
+  uint32_t smap[kMaxMRopeHalf / 16];  // M-RoPE: 2-bit stream of each coefficient index
+};
+
+// Kernel entry points for cudaLaunchKernel / occupancy queries. `vec` selects
+// the 128-bit vector path. Return nullptr for unsupported combinations.
+const void* rope_kernel_cached(int dtype, bool vec, bool interleaved, bool rank4, Coef mode);
+const void* rope_kernel_mrope(int dtype, bool vec, bool interleaved, bool rank4);
+const void* fused_kernel(int dtype, bool vec, bool interleaved, bool rank4);
+const void* cache_build_kernel(int dtype);
+
+}  // namespace rope_gb300

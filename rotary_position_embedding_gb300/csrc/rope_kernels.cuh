@@ -1,0 +1,419 @@
+// Rotary position embedding kernels for sm_103a (GB300).
+//
+// The operation is a streaming, HBM-bound gather/rotate/copy: every element of
+// X is read once and every element of Y written once; the cos/sin rows are a
+// few percent of the traffic and are shared by all heads of a token. No tensor
+// cores: nothing here is a contraction.
+//
+// Definitions followed (web pages, by title and section):
+//  - "ai.onnx.RotaryEmbedding" WebGPU manifest: inputs/X (rank 3
+//    (B, S, N*H), rank 4 (B, N, S, H)), inputs/cos_cache and position_ids (2-D
+//    table gathered at position_ids[b, s], or a (B, S, rd/2) table),
+//    attributeDescriptions/interleaved and rotary_embedding_dim (pairing,
+//    partial rotation with pass-through tail).
+//  - "com.microsoft.MRotaryEmbedding" README: Inputs/positionIds (three
+//    streams, out-of-range pairs copied through), Attributes/mrope_section,
+//    mrope_layout, scale, Implementation variants/pairs4 (scaled coefficient
+//    rounded to the storage type).
+//  - onnxruntime pull request "Add RotaryEmbedding fusion for Qwen3 on-the-fly
+//    RoPE patterns": Modeling Code Alignment Check (apply_rotary_pos_emb,
+//    rotate_half; cos/sin from inv_freq times attention_scaling), Medium
+//    Issues 4 (cache = cos(freqs) * scaling).
+#pragma once
+
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#include "rope_internal.h"
+
+namespace rope_gb300 {
+
+// ---------------------------------------------------------------------------
+// Element types: values are carried as their storage bits and converted to
+// float32 for arithmetic.
+// ---------------------------------------------------------------------------
+template <class T>
+struct Elem;
+
+template <>
+struct Elem<float> {
+  using bits = float;
+  static __device__ __forceinline__ float tof(float v) { return v; }
+  static __device__ __forceinline__ float fromf(float v) { return v; }
+  // T(a * b) rounded once from the exact product: a float32 product is
+  // already that.
+  static __device__ __forceinline__ float mul_round(float a, float b) { return __fmul_rn(a, b); }
+};
+
+template <>
+struct Elem<__half> {
+  using bits = unsigned short;
+  static __device__ __forceinline__ float tof(unsigned short v) {
+    return __half2float(__ushort_as_half(v));
+  }
+  static __device__ __forceinline__ unsigned short fromf(float v) {
+    return __half_as_ushort(__float2half_rn(v));
+  }
+  // float16(a * b) rounded once from the exact product. The float32 product
+  // is formed with round-to-odd (truncate, then set the last bit if the
+  // truncation was inexact); rounding a round-to-odd value with at least two
+  // extra bits to nearest-even gives the correctly rounded result (Boldo and
+  // Melquiond, "Emulation of FMA and correctly rounded sums: proved
+  // algorithms using rounding to odd", IEEE Trans. Computers 57(4), 2008).
+  static __device__ __forceinline__ float mul_round(float a, float b) {
+    float t = __fmul_rz(a, b);
+    float lo = __fmul_rd(a, b);
+    float hi = __fmul_ru(a, b);
+    if (lo != hi && isfinite(t)) t = __int_as_float(__float_as_int(t) | 1);
+    return __half2float(__float2half_rn(t));
+  }
+};
+
+template <class T, int V>
+struct alignas(V * sizeof(typename Elem<T>::bits)) VecT {
+  typename Elem<T>::bits v[V];
+};
+
+template <int BYTES>
+struct Raw;
+template <>
+struct Raw<16> {
+  using t = uint4;
+};
+template <>
+struct Raw<8> {
+  using t = uint2;
+};
+template <>
+struct Raw<4> {
+  using t = unsigned int;
+};
+template <>
+struct Raw<2> {
+  using t = unsigned short;
+};
+
+// X is read exactly once: streaming load (evict-first).
+template <class VT>
+__device__ __forceinline__ VT ld_stream(const VT* p) {
+  using R = typename Raw<sizeof(VT)>::t;
+  R r = __ldcs(reinterpret_cast<const R*>(p));
+  VT v;
+  __builtin_memcpy(&v, &r, sizeof(VT));
+  return v;
+}
+
+// Y is written exactly once: streaming store.
+template <class VT>
+__device__ __forceinline__ void st_stream(VT* p, const VT& v) {
+  using R = typename Raw<sizeof(VT)>::t;
+  R r;
+  __builtin_memcpy(&r, &v, sizeof(VT));
+  __stcs(reinterpret_cast<R*>(p), r);
+}
+
+// cos/sin rows and positions are shared by every head of a token: read-only
+// path, cached in L1.
+template <class VT>
+__device__ __forceinline__ VT ld_shared_ro(const VT* p) {
+  using R = typename Raw<sizeof(VT)>::t;
+  R r = __ldg(reinterpret_cast<const R*>(p));
+  VT v;
+  __builtin_memcpy(&v, &r, sizeof(VT));
+  return v;
+}
+
+// One rotation pair in float32: y0 = x0*c - x1*s, y1 = x1*c + x0*s.
+__device__ __forceinline__ void rotate(float x0, float x1, float c, float s, float& y0,
+                                       float& y1) {
+  y0 = __fmaf_rn(x0, c, -__fmul_rn(x1, s));
+  y1 = __fmaf_rn(x1, c, __fmul_rn(x0, s));
+}
+
+// Pair j of a unit: half-split pairs a[j] with b[j]; interleaved pairs
+// elements 2j and 2j+1 of the 2V-element run a||b. Coefficient index j.
+template <class T, int V, bool INTER>
+struct Pairs {
+  using E = Elem<T>;
+  using VT = VecT<T, V>;
+  static __device__ __forceinline__ typename E::bits get(const VT& a, const VT& b, int q) {
+    return q < V ? a.v[q] : b.v[q - V];
+  }
+  static __device__ __forceinline__ void set(VT& a, VT& b, int q, typename E::bits v) {
+    if (q < V)
+      a.v[q] = v;
+    else
+      b.v[q - V] = v;
+  }
+  static __device__ __forceinline__ int i0(int j) { return INTER ? 2 * j : j; }
+  static __device__ __forceinline__ int i1(int j) { return INTER ? 2 * j + 1 : j + V; }
+};
+
+// Rotate all V pairs of a unit with coefficient vectors c, s.
+template <class T, int V, bool INTER>
+__device__ __forceinline__ void rotate_unit(const VecT<T, V>& a, const VecT<T, V>& b,
+                                            const VecT<T, V>& c, const VecT<T, V>& s,
+                                            VecT<T, V>& ya, VecT<T, V>& yb) {
+  using E = Elem<T>;
+  using P = Pairs<T, V, INTER>;
+#pragma unroll
+  for (int j = 0; j < V; ++j) {
+    float x0 = E::tof(P::get(a, b, P::i0(j)));
+    float x1 = E::tof(P::get(a, b, P::i1(j)));
+    float y0, y1;
+    rotate(x0, x1, E::tof(c.v[j]), E::tof(s.v[j]), y0, y1);
+    P::set(ya, yb, P::i0(j), E::fromf(y0));
+    P::set(ya, yb, P::i1(j), E::fromf(y1));
+  }
+}
+
+// Offsets (elements, within a head row) of a pair unit's two X vectors.
+template <int V, bool INTER>
+__device__ __forceinline__ void unit_offsets(int k, int h, int& oa, int& ob) {
+  if (INTER) {
+    oa = 2 * k * V;
+    ob = oa + V;
+  } else {
+    oa = k * V;
+    ob = h + k * V;
+  }
+}
+
+__device__ __forceinline__ void flag_oor(int32_t* flag) {
+  if (flag) atomicOr(flag, 1);
+}
+
+// ---------------------------------------------------------------------------
+// Cached RoPE and M-RoPE: coefficients read straight from the table. Each
+// thread keeps one (token slot, head, unit) role for its whole life, so there
+// is no per-element index arithmetic and no barrier; the 32+ threads of a
+// token that need the same cos/sin bytes hit in L1.
+// ---------------------------------------------------------------------------
+template <class T, int V, bool INTER, bool RANK4, Coef MODE>
+__global__ void __launch_bounds__(1024) rope_rows_kernel(const KParams p) {
+  using E = Elem<T>;
+  using VT = VecT<T, V>;
+  using bits = typename E::bits;
+  const int tid = threadIdx.x;
+  const int per_tok = p.NG * p.Ublk;
+  const int slot = tid / per_tok;
+  const int r = tid - slot * per_tok;
+  const int ng = r / p.Ublk;
+  const int k0 = r - ng * p.Ublk;
+  const int64_t n = (int64_t)blockIdx.y * p.NG + ng;
+  if (slot >= p.TTs || n >= p.N) return;  // no barrier below
+
+  const bits* __restrict__ x = static_cast<const bits*>(p.x);
+  bits* __restrict__ y = static_cast<bits*>(p.y);
+  const bits* __restrict__ cosb = static_cast<const bits*>(p.cos);
+  const bits* __restrict__ sinb = static_cast<const bits*>(p.sin);
+
+  int64_t tok = (int64_t)blockIdx.x * p.TTs + slot;
+  int64_t b = 0, s = 0;
+  if (RANK4) {
+    b = tok / p.S;
+    s = tok - b * p.S;
+  }
+  for (; tok < p.ntok; tok += p.step_tok) {
+    const int64_t row = RANK4 ? ((b * p.N + n) * p.S + s) * p.H : (tok * p.N + n) * p.H;
+    const bits* xr = x + row;
+    bits* yr = y + row;
+    for (int k = k0; k < p.U; k += p.Ublk) {
+      if (k >= p.nP) {  // tail unit: bit copy
+        const int off = p.rd + (k - p.nP) * V;
+        st_stream(reinterpret_cast<VT*>(yr + off), ld_stream(reinterpret_cast<const VT*>(xr + off)));
+        continue;
+      }
+      int oa, ob;
+      unit_offsets<V, INTER>(k, p.h, oa, ob);
+      const int oc = k * V;
+      const VT a = ld_stream(reinterpret_cast<const VT*>(xr + oa));
+      const VT bv = ld_stream(reinterpret_cast<const VT*>(xr + ob));
+      VT ya, yb;
+      if (MODE == Coef::kCache2D || MODE == Coef::kCache3D) {
+        int64_t crow;
+        if (MODE == Coef::kCache2D) {
+          const int64_t pp = __ldg(p.pos + tok);
+          if ((uint64_t)pp >= (uint64_t)p.cache_rows) {  // negative or past the table
+            if (ng == 0 && k == 0) flag_oor(p.oor_flag);
+            st_stream(reinterpret_cast<VT*>(yr + oa), a);
+            st_stream(reinterpret_cast<VT*>(yr + ob), bv);
+            continue;
+          }
+          crow = pp * p.h;
+        } else {
+          crow = tok * p.h;
+        }
+        const VT c = ld_shared_ro(reinterpret_cast<const VT*>(cosb + crow + oc));
+        const VT sn = ld_shared_ro(reinterpret_cast<const VT*>(sinb + crow + oc));
+        rotate_unit<T, V, INTER>(a, bv, c, sn, ya, yb);
+      } else {  // M-RoPE
+        using P = Pairs<T, V, INTER>;
+        const uint32_t word = p.smap[oc >> 4];
+        const uint32_t um = (word >> ((oc & 15) * 2)) & (uint32_t)((1ull << (2 * V)) - 1);
+        uint32_t present = 0;
+#pragma unroll
+        for (int j = 0; j < V; ++j) present |= 1u << ((um >> (2 * j)) & 3);
+        int64_t ps[3];
+        bool ok[3];
+        VT cs[3], ss[3];
+#pragma unroll
+        for (int st = 0; st < 3; ++st) {
+          ok[st] = false;
+          if (present & (1u << st)) {
+            ps[st] = __ldg(p.pos + st * p.ntok + tok);
+            ok[st] = (uint64_t)ps[st] < (uint64_t)p.cache_rows;
+            if (ok[st]) {
+              cs[st] = ld_shared_ro(reinterpret_cast<const VT*>(cosb + ps[st] * p.h + oc));
+              ss[st] = ld_shared_ro(reinterpret_cast<const VT*>(sinb + ps[st] * p.h + oc));
+            } else if (ng == 0) {
+              flag_oor(p.oor_flag);
+            }
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < V; ++j) {
+          const int st = (um >> (2 * j)) & 3;
+          const bits x0b = P::get(a, bv, P::i0(j));
+          const bits x1b = P::get(a, bv, P::i1(j));
+          const bool okj = st == 0 ? ok[0] : (st == 1 ? ok[1] : ok[2]);
+          bits y0b = x0b, y1b = x1b;
+          if (okj) {
+            const bits cb = st == 0 ? cs[0].v[j] : (st == 1 ? cs[1].v[j] : cs[2].v[j]);
+            const bits sb = st == 0 ? ss[0].v[j] : (st == 1 ? ss[1].v[j] : ss[2].v[j]);
+            float c = E::tof(cb), sv = E::tof(sb);
+            if (!p.scale_is_one) {
+              c = E::mul_round(c, p.scale);
+              sv = E::mul_round(sv, p.scale);
+            }
+            float y0, y1;
+            rotate(E::tof(x0b), E::tof(x1b), c, sv, y0, y1);
+            y0b = E::fromf(y0);
+            y1b = E::fromf(y1);
+          }
+          P::set(ya, yb, P::i0(j), y0b);
+          P::set(ya, yb, P::i1(j), y1b);
+        }
+      }
+      st_stream(reinterpret_cast<VT*>(yr + oa), ya);
+      st_stream(reinterpret_cast<VT*>(yr + ob), yb);
+    }
+    if (RANK4) {
+      s += p.step_s;
+      b += p.step_b;
+      if (s >= p.S) {
+        s -= p.S;
+        ++b;
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// On-the-fly coefficients (float32 angle, double-precision cos/sin rounded to
+// float32, times attention scaling in float32, rounded to T). Shared by the
+// fused kernel and the cache build so the two agree bit for bit.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void coef_on_the_fly(int64_t pos, float inv, float scaling, float& c,
+                                                float& s) {
+  const float pf = __ll2float_rn(pos);
+  const float theta = __fmul_rn(pf, inv);
+  double sd, cd;
+  sincos((double)theta, &sd, &cd);
+  c = __fmul_rn(__double2float_rn(cd), scaling);
+  s = __fmul_rn(__double2float_rn(sd), scaling);
+}
+
+// Fused rotation: per tile of TTs tokens the CTA first fills a shared-memory
+// table of the tile's rd/2 coefficients (one double-precision sincos per
+// token and index, not per head), then every thread rotates its unit from it.
+template <class T, int V, bool INTER, bool RANK4>
+__global__ void __launch_bounds__(1024) rope_fused_kernel(const KParams p) {
+  using E = Elem<T>;
+  using VT = VecT<T, V>;
+  using bits = typename E::bits;
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  bits* sc = reinterpret_cast<bits*>(smem_raw);
+  bits* ss = sc + (size_t)p.TTs * p.h;
+
+  const int tid = threadIdx.x;
+  const int per_tok = p.NG * p.Ublk;
+  const int slot = tid / per_tok;
+  const int r = tid - slot * per_tok;
+  const int ng = r / p.Ublk;
+  const int k0 = r - ng * p.Ublk;
+  const int64_t n = (int64_t)blockIdx.y * p.NG + ng;
+  const bool active = slot < p.TTs && n < p.N;
+
+  const bits* __restrict__ x = static_cast<const bits*>(p.x);
+  bits* __restrict__ y = static_cast<bits*>(p.y);
+  const int items = p.TTs * p.h;
+
+  for (int64_t tile0 = (int64_t)blockIdx.x * p.TTs; tile0 < p.ntok; tile0 += p.step_tok) {
+    __syncthreads();  // the previous tile's readers are done with the table
+    for (int it = tid; it < items; it += blockDim.x) {
+      const int ls = it / p.h;
+      const int i = it - ls * p.h;
+      const int64_t t = tile0 + ls;
+      if (t < p.ntok) {
+        float c, s;
+        coef_on_the_fly(__ldg(p.pos + t), __ldg(p.inv_freq + i), p.scale, c, s);
+        sc[it] = E::fromf(c);
+        ss[it] = E::fromf(s);
+      }
+    }
+    __syncthreads();
+    const int64_t tok = tile0 + slot;
+    if (!active || tok >= p.ntok) continue;
+    int64_t row;
+    if (RANK4) {
+      const int64_t b = tok / p.S, s = tok - (tok / p.S) * p.S;
+      row = ((b * p.N + n) * p.S + s) * p.H;
+    } else {
+      row = (tok * p.N + n) * p.H;
+    }
+    const bits* xr = x + row;
+    bits* yr = y + row;
+    for (int k = k0; k < p.U; k += p.Ublk) {
+      if (k >= p.nP) {
+        const int off = p.rd + (k - p.nP) * V;
+        st_stream(reinterpret_cast<VT*>(yr + off), ld_stream(reinterpret_cast<const VT*>(xr + off)));
+        continue;
+      }
+      int oa, ob;
+      unit_offsets<V, INTER>(k, p.h, oa, ob);
+      const VT a = ld_stream(reinterpret_cast<const VT*>(xr + oa));
+      const VT bv = ld_stream(reinterpret_cast<const VT*>(xr + ob));
+      const VT c = *reinterpret_cast<const VT*>(sc + slot * p.h + k * V);
+      const VT sn = *reinterpret_cast<const VT*>(ss + slot * p.h + k * V);
+      VT ya, yb;
+      rotate_unit<T, V, INTER>(a, bv, c, sn, ya, yb);
+      st_stream(reinterpret_cast<VT*>(yr + oa), ya);
+      st_stream(reinterpret_cast<VT*>(yr + ob), yb);
+    }
+  }
+}
+
+// (rows, half) cos/sin tables: row p = on-the-fly coefficients of position p.
+template <class T>
+__global__ void __launch_bounds__(256) rope_cache_build_kernel(const float* __restrict__ inv,
+                                                               int32_t half, int64_t rows,
+                                                               float scaling, void* cos_out,
+                                                               void* sin_out) {
+  using E = Elem<T>;
+  using bits = typename E::bits;
+  bits* co = static_cast<bits*>(cos_out);
+  bits* so = static_cast<bits*>(sin_out);
+  const int64_t total = rows * half;
+  for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+       idx += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t pr = idx / half;
+    const int i = (int)(idx - pr * half);
+    float c, s;
+    coef_on_the_fly(pr, __ldg(inv + i), scaling, c, s);
+    co[idx] = E::fromf(c);
+    so[idx] = E::fromf(s);
+  }
+}
+
+}  // namespace rope_gb300

@@ -1,0 +1,169 @@
+"""C ABI checks that need no GPU: the library builds and loads, exports every
+function include/rope.h declares, and rejects malformed arguments with the
+right status before any CUDA call. The host-side M-RoPE stream map is checked
+against the oracle's independent construction."""
+
+import ctypes
+import os
+import re
+import shutil
+import subprocess
+
+import numpy as np
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "rope.h")
+
+F32, F16 = 0, 1
+OK, INVALID, UNSUPPORTED = 0, 1, 2
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_abi():
+    fns = declared_functions()
+    for name in ("rope_apply", "mrope_apply", "mrope_apply_stream_map", "mrope_stream_map",
+                 "rope_apply_fused", "rope_cache_build", "rope_status_string", "rope_last_error"):
+        assert name in fns
+
+
+def test_library_exports_every_declared_symbol(lib):
+    so = lib.load_library()
+    for name in declared_functions():
+        assert hasattr(so, name), name
+    if shutil.which("nm"):
+        out = subprocess.run(["nm", "-D", "--defined-only", lib.LIB_PATH], capture_output=True,
+                             text=True, check=True).stdout
+        exported = {ln.split()[-1] for ln in out.splitlines() if " T " in ln}
+        assert set(declared_functions()) <= exported
+    assert set(declared_functions()) == set(lib.SIGNATURES)
+
+
+def _i64(*v):
+    return (ctypes.c_int64 * len(v))(*v)
+
+
+FAKE = ctypes.c_void_p(0x10000)       # never dereferenced: every case fails before a CUDA call
+FAKE2 = ctypes.c_void_p(0x20000)
+
+
+def _rope(so, **kw):
+    a = dict(dtype=F16, rank=3, xs=_i64(2, 4, 64), x=FAKE, y=FAKE2, crank=2, cs=_i64(16, 8), cos=FAKE,
+             sin=FAKE, pos=FAKE, inter=0, rd=0, nh=4, flag=None, stream=None)
+    a.update(kw)
+    return so.rope_apply(a["dtype"], a["rank"], a["xs"], a["x"], a["y"], a["crank"], a["cs"], a["cos"],
+                         a["sin"], a["pos"], a["inter"], a["rd"], a["nh"], a["flag"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(dtype=99), UNSUPPORTED),                      # bfloat16 and others: not implemented
+    (dict(rank=5, xs=_i64(1, 1, 1, 1, 1)), INVALID),
+    (dict(nh=0), INVALID),                              # rank 3 needs num_heads
+    (dict(nh=3), INVALID),                              # 64 % 3 != 0
+    (dict(xs=_i64(2, 4, 60), nh=4, cs=_i64(16, 7)), INVALID),  # head size 15 is odd
+    (dict(inter=2), INVALID),
+    (dict(rd=-2), INVALID),
+    (dict(rd=18), INVALID),                             # rd > head size 16
+    (dict(rd=6), INVALID),                              # width 8 * 2 != 6
+    (dict(rd=7, cs=_i64(16, 3)), INVALID),              # odd rotary width
+    (dict(cs=_i64(16, 4)), INVALID),                    # width * 2 != 16
+    (dict(crank=3, cs=_i64(2, 4, 8)), INVALID),         # position_ids present -> 2-D cache
+    (dict(pos=None, crank=2), INVALID),                 # no position_ids -> 3-D cache
+    (dict(pos=None, crank=3, cs=_i64(2, 5, 8)), INVALID),   # 3-D cache must be (B, S, rd/2)
+    (dict(xs=_i64(2, -1, 64)), INVALID),
+    (dict(rank=4, xs=_i64(2, 4, 5, 16), nh=3), INVALID),    # num_heads != N
+    (dict(x=ctypes.c_void_p(0x10001)), INVALID),        # misaligned float16 pointer
+    (dict(pos=ctypes.c_void_p(0x10004)), INVALID),      # misaligned int64 pointer
+    (dict(x=None), INVALID),
+])
+def test_rope_apply_rejects_before_launch(lib, kw, status):
+    so = lib.load_library()
+    st = _rope(so, **kw)
+    assert st == status, so.rope_last_error().decode()
+    assert so.rope_last_error().decode() != ""
+
+
+def test_empty_inputs_launch_nothing(lib):
+    so = lib.load_library()
+    for xs in (_i64(0, 4, 64), _i64(2, 0, 64)):
+        assert _rope(so, xs=xs, x=None, y=None, cos=None, sin=None) == OK
+    assert so.rope_last_error().decode() == ""
+
+
+def _mrope(so, **kw):
+    a = dict(dtype=F16, rank=3, xs=_i64(2, 4, 32), x=FAKE, y=FAKE2, rows=16, cos=FAKE, sin=FAKE,
+             pos=FAKE, sec=(ctypes.c_int32 * 3)(2, 1, 1), layout=0, scale=1.0, inter=0, rd=0, nh=4,
+             packed=0, flag=None, stream=None)
+    a.update(kw)
+    return so.mrope_apply(a["dtype"], a["rank"], a["xs"], a["x"], a["y"], a["rows"], a["cos"], a["sin"],
+                          a["pos"], a["sec"], a["layout"], a["scale"], a["inter"], a["rd"], a["nh"],
+                          a["packed"], a["flag"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(packed=1), UNSUPPORTED),
+    (dict(packed=2), INVALID),
+    (dict(layout=2), INVALID),
+    (dict(sec=(ctypes.c_int32 * 3)(2, 1, 2)), INVALID),     # sums to 5, rd/2 is 4
+    (dict(sec=(ctypes.c_int32 * 3)(5, -1, 0)), INVALID),
+    (dict(sec=None), INVALID),
+    (dict(xs=_i64(2, 4, 36), nh=4), INVALID),               # head 9, rd 0 -> odd full width
+    (dict(dtype=99), UNSUPPORTED),
+    (dict(rows=-1), INVALID),
+    (dict(pos=None), INVALID),
+    (dict(xs=_i64(2, 4, 4 * 2100), rd=0, sec=(ctypes.c_int32 * 3)(1050, 0, 0)), UNSUPPORTED),
+])
+def test_mrope_apply_rejects_before_launch(lib, kw, status):
+    so = lib.load_library()
+    st = _mrope(so, **kw)
+    assert st == status, so.rope_last_error().decode()
+
+
+def test_mrope_odd_head_with_even_rotary_width_is_accepted_by_checks(lib):
+    """Odd head size is valid when rotary_embedding_dim is a smaller even number
+    (MRotaryEmbedding README, Attributes/rotary_embedding_dim); with an empty
+    batch the call returns OK without launching."""
+    so = lib.load_library()
+    assert _mrope(so, xs=_i64(0, 4, 36), nh=4, rd=8, sec=(ctypes.c_int32 * 3)(2, 1, 1)) == OK
+
+
+def test_fused_and_cache_build_reject_before_launch(lib):
+    so = lib.load_library()
+    st = so.rope_apply_fused(F16, 3, _i64(2, 4, 64), FAKE, FAKE2, None, 1.0, FAKE, 0, 0, 4, None)
+    assert st == INVALID  # inv_freq NULL
+    st = so.rope_apply_fused(F16, 3, _i64(2, 4, 64), FAKE, FAKE2, FAKE, 1.0, None, 0, 0, 4, None)
+    assert st == INVALID  # positions required
+    assert so.rope_cache_build(F16, FAKE, 0, 10, 1.0, FAKE, FAKE2, None) == INVALID
+    assert so.rope_cache_build(F16, FAKE, 4, -1, 1.0, FAKE, FAKE2, None) == INVALID
+    assert so.rope_cache_build(7, FAKE, 4, 10, 1.0, FAKE, FAKE2, None) == UNSUPPORTED
+    assert so.rope_cache_build(F16, FAKE, 4, 0, 1.0, None, None, None) == OK
+
+
+def test_status_strings(lib):
+    so = lib.load_library()
+    assert so.rope_status_string(0) == b"ROPE_OK"
+    assert so.rope_status_string(3) == b"ROPE_ERR_CUDA"
+
+
+def test_stream_map_matches_oracle(lib, orc):
+    """The library's host map (cycle pointer) and the oracle's (round by round)
+    are written independently; they must agree for layouts 0 and 1."""
+    rng = np.random.default_rng(0)
+    cases = [(16, 24, 24), (24, 20, 20), (2, 1, 1), (0, 0, 5), (7, 0, 3), (1, 30, 1), (64, 0, 0)]
+    cases += [tuple(int(v) for v in rng.integers(0, 40, 3)) for _ in range(300)]
+    for sec in cases:
+        half = sum(sec)
+        if half == 0:
+            continue
+        for layout in (0, 1):
+            got = lib.mrope_stream_map(sec, layout, half)
+            exp = orc.mrope_stream_map(sec, layout, half).tolist()
+            assert got == exp, (sec, layout)
+    with pytest.raises(lib.RopeError) as e:
+        lib.mrope_stream_map((1, 2, 3), 0, 7)
+    assert e.value.status == INVALID

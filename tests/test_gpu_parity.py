@@ -1,0 +1,404 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle on the
+same seeded inputs, element by element.
+
+Small cases span several CTA tiles with ragged tails, every variant (rank 3/4,
+2-D/3-D cache, half-split/interleaved, full/partial rotation, float32/float16,
+128-bit vector and scalar paths), out-of-range positions, in-place calls and
+edge sizes. The full-size workloads run in the launch configuration the
+benchmark times and are compared in full.
+"""
+
+import itertools
+import zlib
+
+import numpy as np
+import pytest
+
+from parity_util import compare, mrope_passthrough_mask, rope_passthrough_mask
+from rotary_position_embedding_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+DT = {"f16": np.float16, "f32": np.float32}
+
+
+def _dev(a, torch, cuda, offset=0):
+    """Device copy of a host array; offset > 0 places it that many elements past a
+    16-byte boundary (contiguous but misaligned for the vector path)."""
+    t = torch.from_numpy(np.ascontiguousarray(a))
+    if offset == 0:
+        return t.to(cuda)
+    big = torch.empty(t.numel() + offset, dtype=t.dtype, device=cuda)
+    v = big[offset:offset + t.numel()].view(t.shape)
+    v.copy_(t.to(cuda))
+    return v
+
+
+def _seed(*params):
+    return zlib.crc32(repr(params).encode())
+
+
+def _host(t):
+    return t.detach().cpu().numpy()
+
+
+def _x_shape(rank, B, S, N, H):
+    return (B, S, N * H) if rank == 3 else (B, N, S, H)
+
+
+@pytest.fixture(scope="module")
+def torch_mod():
+    import torch
+
+    return torch
+
+
+# ---------------------------------------------------------------------------
+# RotaryEmbedding: small exhaustive grid
+# ---------------------------------------------------------------------------
+
+ROPE_GRID = list(itertools.product(
+    ["f16", "f32"], [3, 4], ["pos", "cache3d"], [0, 1], ["full", "partial"],
+    ["vector", "scalar_shape", "scalar_misaligned"]))
+
+
+@pytest.mark.parametrize("dt,rank,cache,inter,rot,path", ROPE_GRID)
+def test_rope_grid(lib, orc, cuda, torch_mod, dt, rank, cache, inter, rot, path):
+    torch = torch_mod
+    dtype = DT[dt]
+    rng = np.random.default_rng(_seed(dt, rank, cache, inter, rot, path))
+    B, S, N = 3, 37, 5
+    H = 6 if path == "scalar_shape" else 32
+    rd = 0 if rot == "full" else (4 if H == 6 else 16)
+    h = (rd or H) // 2
+    shape = _x_shape(rank, B, S, N, H)
+    x = rng.standard_normal(shape).astype(dtype)
+    inv = wl.inv_freq(10000.0, rd or H, h)
+    if cache == "pos":
+        R = 97
+        cos, sin = orc.cache_build(inv, R, dtype)
+        pos = rng.integers(0, R, (B, S))
+        pos[0, 3], pos[1, 0], pos[2, S - 1], pos[2, 5] = -1, R, 1 << 40, R - 1
+    else:
+        R = 0
+        cos3, sin3 = orc.cache_build(inv, B * S, dtype)
+        cos, sin = cos3.reshape(B, S, h), sin3.reshape(B, S, h)
+        pos = None
+    nh = N if rank == 3 else 0
+    y_ref, n_oor = orc.rope(x, cos, sin, pos, inter, rd, nh)
+    off = 1 if path == "scalar_misaligned" else 0
+    xd = _dev(x, torch, cuda, off)
+    flag = torch.zeros(1, dtype=torch.int32, device=cuda)
+    yd = lib.rope_apply(xd, _dev(cos, torch, cuda), _dev(sin, torch, cuda),
+                        None if pos is None else _dev(pos, torch, cuda), interleaved=inter,
+                        rotary_embedding_dim=rd, num_heads=nh, oor_flag=flag)
+    torch.cuda.synchronize()
+    mask = rope_passthrough_mask(shape, rank, N, rd, pos, R)
+    compare(_host(yd), y_ref, x, rank, N, mask)
+    assert int(flag.item()) == (1 if n_oor else 0)
+
+
+@pytest.mark.parametrize("dt,rank,inter", list(itertools.product(["f16", "f32"], [3, 4], [0, 1])))
+def test_rope_in_place(lib, orc, cuda, torch_mod, dt, rank, inter):
+    torch = torch_mod
+    dtype = DT[dt]
+    rng = np.random.default_rng(21)
+    B, S, N, H = 2, 19, 4, 64
+    shape = _x_shape(rank, B, S, N, H)
+    x = rng.standard_normal(shape).astype(dtype)
+    inv = wl.inv_freq(10000.0, H, H // 2)
+    cos, sin = orc.cache_build(inv, 50, dtype)
+    pos = rng.integers(0, 50, (B, S))
+    nh = N if rank == 3 else 0
+    y_ref, _ = orc.rope(x, cos, sin, pos, inter, 0, nh)
+    xd = _dev(x, torch, cuda)
+    out = lib.rope_apply(xd, _dev(cos, torch, cuda), _dev(sin, torch, cuda), _dev(pos, torch, cuda),
+                         interleaved=inter, num_heads=nh, out=xd)
+    torch.cuda.synchronize()
+    assert out.data_ptr() == xd.data_ptr()
+    compare(_host(xd), y_ref, x, rank, N, rope_passthrough_mask(shape, rank, N, 0, pos, 50))
+
+
+@pytest.mark.parametrize("case", ["B1S1N1H2", "N1_long_S", "many_heads", "H8_f32_rank4", "all_oor",
+                                  "zero_rows", "big_positions"])
+def test_rope_edges(lib, orc, cuda, torch_mod, case):
+    torch = torch_mod
+    rng = np.random.default_rng(22)
+    rank, dtype, inter, rd = 3, np.float16, 0, 0
+    if case == "B1S1N1H2":
+        B, S, N, H, R = 1, 1, 1, 2, 4
+    elif case == "N1_long_S":
+        B, S, N, H, R = 2, 3001, 1, 16, 4000
+    elif case == "many_heads":
+        B, S, N, H, R = 1, 5, 160, 128, 16    # N*U > 1024 threads: heads split across CTAs
+    elif case == "H8_f32_rank4":
+        B, S, N, H, R, rank, dtype, inter = 3, 33, 2, 8, 40, 4, np.float32, 1
+    elif case == "all_oor":
+        B, S, N, H, R = 2, 7, 3, 16, 5
+    elif case == "zero_rows":
+        B, S, N, H, R = 2, 7, 3, 16, 0
+    else:
+        B, S, N, H, R = 2, 9, 2, 32, 1 << 20
+    shape = _x_shape(rank, B, S, N, H)
+    x = rng.standard_normal(shape).astype(dtype)
+    h = (rd or H) // 2
+    inv = wl.inv_freq(10000.0, H, h)
+    Rb = min(R, 4096) if case != "big_positions" else 4096
+    cos, sin = orc.cache_build(inv, max(Rb, 0), dtype)
+    if case == "big_positions":
+        # a (2^20)-row table is only partly materialised: gather rows < 4096 or >= 2^20
+        cos_full = np.zeros((R, h), dtype=dtype)
+        sin_full = np.zeros((R, h), dtype=dtype)
+        cos_full[:Rb], sin_full[:Rb] = cos, sin
+        cos, sin = cos_full, sin_full
+        pos = rng.integers(0, Rb, (B, S))
+        pos[0, 0], pos[1, 1] = R, (1 << 62)
+    elif case == "all_oor":
+        pos = rng.integers(R, 100, (B, S))
+    elif case == "zero_rows":
+        pos = rng.integers(0, 3, (B, S))
+    else:
+        pos = rng.integers(0, R, (B, S))
+    nh = N if rank == 3 else 0
+    y_ref, n_oor = orc.rope(x, cos, sin, pos, inter, rd, nh)
+    flag = torch.zeros(1, dtype=torch.int32, device=cuda)
+    cd = _dev(cos, torch, cuda) if cos.size else torch.empty((0, h), dtype=torch.float16, device=cuda)
+    sd = _dev(sin, torch, cuda) if sin.size else torch.empty((0, h), dtype=torch.float16, device=cuda)
+    yd = lib.rope_apply(_dev(x, torch, cuda), cd, sd, _dev(pos, torch, cuda), interleaved=inter,
+                        rotary_embedding_dim=rd, num_heads=nh, oor_flag=flag)
+    torch.cuda.synchronize()
+    compare(_host(yd), y_ref, x, rank, N, rope_passthrough_mask(shape, rank, N, rd, pos, R))
+    assert int(flag.item()) == (1 if n_oor else 0)
+
+
+def test_empty_and_errors_on_gpu(lib, cuda, torch_mod):
+    torch = torch_mod
+    x = torch.empty((0, 4, 64), dtype=torch.float16, device=cuda)
+    c = torch.empty((8, 8), dtype=torch.float16, device=cuda)
+    p = torch.empty((0, 4), dtype=torch.int64, device=cuda)
+    y = lib.rope_apply(x, c, c, p, num_heads=4)
+    assert y.shape == x.shape
+    xb = torch.zeros((2, 4, 64), dtype=torch.bfloat16, device=cuda)
+    cb = torch.zeros((8, 8), dtype=torch.bfloat16, device=cuda)
+    pp = torch.zeros((2, 4), dtype=torch.int64, device=cuda)
+    with pytest.raises(lib.RopeError) as e:
+        lib.rope_apply(xb, cb, cb, pp, num_heads=4)
+    assert e.value.status == lib.ROPE_ERR_UNSUPPORTED
+    with pytest.raises(lib.RopeError) as e:
+        lib.rope_apply(x.new_zeros((2, 4, 64)), c, c, pp, num_heads=3)
+    assert e.value.status == lib.ROPE_ERR_INVALID_ARG
+
+
+def test_side_stream(lib, orc, cuda, torch_mod):
+    torch = torch_mod
+    rng = np.random.default_rng(23)
+    x = rng.standard_normal((4, 64, 8 * 128)).astype(np.float16)
+    inv = wl.inv_freq(10000.0, 128, 64)
+    cos, sin = orc.cache_build(inv, 256, np.float16)
+    pos = rng.integers(0, 256, (4, 64))
+    y_ref, _ = orc.rope(x, cos, sin, pos, 0, 0, 8)
+    s = torch.cuda.Stream()
+    xd, cd, sd, pd = (_dev(a, torch, cuda) for a in (x, cos, sin, pos))
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        yd = lib.rope_apply(xd, cd, sd, pd, num_heads=8)
+    s.synchronize()
+    compare(_host(yd), y_ref, x, 3, 8, rope_passthrough_mask(x.shape, 3, 8, 0, pos, 256))
+
+
+# ---------------------------------------------------------------------------
+# MRotaryEmbedding
+# ---------------------------------------------------------------------------
+
+MROPE_GRID = list(itertools.product(
+    ["f16", "f32"], [3, 4], ["l0", "l1", "stride3"], [0, 1], ["full", "partial_odd_head"],
+    [1.0, 0.7], ["vector", "scalar_misaligned"]))
+
+
+@pytest.mark.parametrize("dt,rank,layout,inter,rot,scale,path", MROPE_GRID)
+def test_mrope_grid(lib, orc, cuda, torch_mod, dt, rank, layout, inter, rot, scale, path):
+    torch = torch_mod
+    dtype = DT[dt]
+    rng = np.random.default_rng(_seed(dt, rank, layout, inter, rot, scale, path))
+    B, S, N = 2, 45, 3
+    if rot == "full":
+        H, rd, sec = 64, 0, (8, 12, 12)
+    else:
+        H, rd, sec = 37, 32, (4, 6, 6)   # odd head size, even rotary width, 5-element tail
+    h = (rd or H) // 2
+    R = 120
+    shape = _x_shape(rank, B, S, N, H)
+    x = rng.standard_normal(shape).astype(dtype)
+    inv = wl.inv_freq(10000.0, rd or H, h)
+    cos, sin = orc.cache_build(inv, R, dtype)
+    pos3 = rng.integers(0, R, (3, B, S))
+    oor = rng.random((3, B, S)) < 0.08
+    pos3[oor] = rng.choice([-1, R, R + 5, 1 << 40], size=int(oor.sum()))
+    nh = N if rank == 3 else 0
+    scale = float(np.float32(scale))
+    if layout == "stride3":
+        smap = orc.mrope_stream_map(sec, 2, h)
+        y_ref, n_oor = orc.mrope_map(x, cos, sin, pos3, smap, scale, inter, rd, nh)
+    else:
+        lay = 0 if layout == "l0" else 1
+        smap = orc.mrope_stream_map(sec, lay, h)
+        y_ref, n_oor = orc.mrope(x, cos, sin, pos3, sec, lay, scale, inter, rd, nh)
+    off = 1 if path == "scalar_misaligned" else 0
+    xd = _dev(x, torch, cuda, off)
+    args = (xd, _dev(cos, torch, cuda), _dev(sin, torch, cuda), _dev(pos3, torch, cuda))
+    flag = torch.zeros(1, dtype=torch.int32, device=cuda)
+    kw = dict(scale=scale, interleaved=inter, rotary_embedding_dim=rd, num_heads=nh, oor_flag=flag)
+    if layout == "stride3":
+        yd = lib.mrope_apply_stream_map(*args, smap.tolist(), **kw)
+    else:
+        yd = lib.mrope_apply(*args, sec, mrope_layout=0 if layout == "l0" else 1, **kw)
+    torch.cuda.synchronize()
+    mask = mrope_passthrough_mask(shape, rank, N, rd, pos3, R, smap, inter)
+    compare(_host(yd), y_ref, x, rank, N, mask)
+    assert int(flag.item()) == (1 if n_oor else 0)
+
+
+def test_mrope_equal_streams_equals_rope_on_gpu(lib, orc, cuda, torch_mod):
+    """Text tokens (t = h = w) reduce M-RoPE to RotaryEmbedding, bit for bit on the GPU too."""
+    torch = torch_mod
+    rng = np.random.default_rng(24)
+    B, S, N, H, R = 2, 77, 4, 128, 300
+    x = rng.standard_normal((B, S, N * H)).astype(np.float16)
+    inv = wl.inv_freq(1e6, H, H // 2)
+    cos, sin = orc.cache_build(inv, R, np.float16)
+    p = rng.integers(0, R, (B, S))
+    xd, cd, sd = (_dev(a, torch, cuda) for a in (x, cos, sin))
+    yr = lib.rope_apply(xd, cd, sd, _dev(p, torch, cuda), num_heads=N)
+    for layout in (0, 1):
+        ym = lib.mrope_apply(xd, cd, sd, _dev(np.stack([p, p, p]), torch, cuda), (16, 24, 24),
+                             mrope_layout=layout, num_heads=N)
+        torch.cuda.synchronize()
+        assert torch.equal(ym.view(torch.int16), yr.view(torch.int16))
+
+
+# ---------------------------------------------------------------------------
+# On-the-fly coefficients and the cache build
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("dt,rank,inter,rd,scaling", list(itertools.product(
+    ["f16", "f32"], [3, 4], [0, 1], [0, 32], [1.0, 0.85])))
+def test_fused_grid(lib, orc, cuda, torch_mod, dt, rank, inter, rd, scaling):
+    torch = torch_mod
+    dtype = DT[dt]
+    rng = np.random.default_rng(_seed(dt, rank, inter, rd, scaling))
+    B, S, N, H = 5, 13, 6, 64
+    h = (rd or H) // 2
+    shape = _x_shape(rank, B, S, N, H)
+    x = rng.standard_normal(shape).astype(dtype)
+    inv = wl.inv_freq(1e6, rd or H, h)
+    pos = rng.integers(0, 32768, (B, S))
+    pos[0, 0], pos[1, 2] = 0, 32767
+    scaling = float(np.float32(scaling))
+    nh = N if rank == 3 else 0
+    y_ref = orc.rope_fused(x, inv, pos, scaling, inter, rd, nh)
+    xd, ind, pd = _dev(x, torch, cuda), _dev(inv, torch, cuda), _dev(pos, torch, cuda)
+    yf = lib.rope_apply_fused(xd, ind, pd, attention_scaling=scaling, interleaved=inter,
+                              rotary_embedding_dim=rd, num_heads=nh)
+    torch.cuda.synchronize()
+    compare(_host(yf), y_ref, x, rank, N, rope_passthrough_mask(shape, rank, N, rd, None, 0))
+    # fused == gathering the library's own cache, bit for bit
+    cd, sd = lib.rope_cache_build(ind, 32768, torch.float16 if dt == "f16" else torch.float32,
+                                  attention_scaling=scaling)
+    yc = lib.rope_apply(xd, cd, sd, pd, interleaved=inter, rotary_embedding_dim=rd, num_heads=nh)
+    torch.cuda.synchronize()
+    bits = torch.int16 if dt == "f16" else torch.int32
+    assert torch.equal(yc.view(bits), yf.view(bits))
+
+
+@pytest.mark.parametrize("dt,base,scaling", list(itertools.product(["f16", "f32"], [1e4, 1e6],
+                                                                    [1.0, 0.7071067690849304])))
+def test_cache_build_vs_oracle(lib, orc, cuda, torch_mod, dt, base, scaling):
+    torch = torch_mod
+    dtype = DT[dt]
+    rows, half = 8192, 64
+    inv = wl.inv_freq(base, 2 * half, half)
+    c_ref, s_ref = orc.cache_build(inv, rows, dtype, scaling)
+    cd, sd = lib.rope_cache_build(_dev(inv, torch, cuda), rows,
+                                  torch.float16 if dt == "f16" else torch.float32,
+                                  attention_scaling=scaling)
+    torch.cuda.synchronize()
+    for got, ref in ((_host(cd), c_ref), (_host(sd), s_ref)):
+        if dtype == np.float16:
+            from parity_util import f16_ordinal
+            d = np.abs(f16_ordinal(got) - f16_ordinal(ref))
+        else:
+            gi, ri = got.view(np.int32).astype(np.int64), ref.view(np.int32).astype(np.int64)
+            d = np.abs(gi - ri)
+        # cos/sin of the float32 angle are evaluated in binary64 on both sides and rounded to
+        # float32: the two libm results differ only when they straddle a rounding boundary
+        assert d.max() <= 1
+        assert (d == 0).mean() >= 0.99999
+
+
+# ---------------------------------------------------------------------------
+# Full-size workloads, launched exactly as the benchmark launches them
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("name", list(wl.WORKLOADS))
+def test_workload_full_size(lib, orc, cuda, torch_mod, name):
+    torch = torch_mod
+    w = wl.WORKLOADS[name]
+    inp = wl.make_inputs(w)
+    x, pos, inv = inp["x"], inp["position_ids"], inp["inv_freq"]
+    dtype = np.dtype(w.dtype)
+    tdt = torch.float16 if dtype == np.float16 else torch.float32
+    nh = w.num_heads if w.rank == 3 else 0
+    xd, ind = _dev(x, torch, cuda), _dev(inv, torch, cuda)
+    if w.kind == "rope" and w.positions == "none":
+        cos, sin = orc.cache_build(inv, w.tokens, dtype)   # row (b, s) at position s (B = 1)
+        cos, sin = cos.reshape(w.batch, w.seq, w.half), sin.reshape(w.batch, w.seq, w.half)
+        y_ref, _ = orc.rope(x, cos, sin, None, w.interleaved, w.rotary_embedding_dim, nh)
+        yd = lib.rope_apply(xd, _dev(cos, torch, cuda), _dev(sin, torch, cuda), None,
+                            interleaved=w.interleaved, rotary_embedding_dim=w.rotary_embedding_dim,
+                            num_heads=nh)
+        mask = rope_passthrough_mask(x.shape, w.rank, w.num_heads, w.rotary_embedding_dim, None, 0)
+    elif w.kind == "rope":
+        cd, sd = lib.rope_cache_build(ind, w.cache_rows, tdt)
+        cos, sin = orc.cache_build(inv, w.cache_rows, dtype)
+        y_ref, _ = orc.rope(x, cos, sin, pos, w.interleaved, w.rotary_embedding_dim, nh)
+        yd = lib.rope_apply(xd, _dev(cos, torch, cuda), _dev(sin, torch, cuda), _dev(pos, torch, cuda),
+                            interleaved=w.interleaved, rotary_embedding_dim=w.rotary_embedding_dim,
+                            num_heads=nh)
+        mask = rope_passthrough_mask(x.shape, w.rank, w.num_heads, w.rotary_embedding_dim, pos,
+                                     w.cache_rows)
+        torch.cuda.synchronize()
+        # the library's own cache gives the same result as the oracle's table
+        yc = lib.rope_apply(xd, cd, sd, _dev(pos, torch, cuda), interleaved=w.interleaved,
+                            rotary_embedding_dim=w.rotary_embedding_dim, num_heads=nh)
+        torch.cuda.synchronize()
+        compare(_host(yc), y_ref, x, w.rank, w.num_heads, mask)
+    elif w.kind == "mrope":
+        cos, sin = orc.cache_build(inv, w.cache_rows, dtype)
+        y_ref, n_oor = orc.mrope(x, cos, sin, pos, w.mrope_section, w.mrope_layout, w.scale,
+                                 w.interleaved, w.rotary_embedding_dim, nh)
+        assert n_oor > 0
+        flag = torch.zeros(1, dtype=torch.int32, device=cuda)
+        yd = lib.mrope_apply(xd, _dev(cos, torch, cuda), _dev(sin, torch, cuda), _dev(pos, torch, cuda),
+                             w.mrope_section, mrope_layout=w.mrope_layout, scale=w.scale,
+                             interleaved=w.interleaved, rotary_embedding_dim=w.rotary_embedding_dim,
+                             num_heads=nh, oor_flag=flag)
+        smap = orc.mrope_stream_map(w.mrope_section, w.mrope_layout, w.half)
+        mask = mrope_passthrough_mask(x.shape, w.rank, w.num_heads, w.rotary_embedding_dim, pos,
+                                      w.cache_rows, smap, w.interleaved)
+        torch.cuda.synchronize()
+        assert int(flag.item()) == 1
+    else:  # fused decode, and the cached path it replaces
+        y_ref = orc.rope_fused(x, inv, pos, w.attention_scaling, w.interleaved, w.rotary_embedding_dim, nh)
+        pd = _dev(pos, torch, cuda)
+        yd = lib.rope_apply_fused(xd, ind, pd, attention_scaling=w.attention_scaling,
+                                  interleaved=w.interleaved, rotary_embedding_dim=w.rotary_embedding_dim,
+                                  num_heads=nh)
+        cd, sd = lib.rope_cache_build(ind, w.cache_rows, tdt, attention_scaling=w.attention_scaling)
+        yc = lib.rope_apply(xd, cd, sd, pd, interleaved=w.interleaved,
+                            rotary_embedding_dim=w.rotary_embedding_dim, num_heads=nh)
+        torch.cuda.synchronize()
+        assert torch.equal(yc.view(torch.int16), yd.view(torch.int16))
+        mask = rope_passthrough_mask(x.shape, w.rank, w.num_heads, w.rotary_embedding_dim, None, 0)
+    torch.cuda.synchronize()
+    stats = compare(_host(yd), y_ref, x, w.rank, w.num_heads, mask)
+    print(name, stats)

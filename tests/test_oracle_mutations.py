@@ -49,8 +49,10 @@ def test_pins_catch_planted_mistake(tmp_path, name):
     shutil.copytree(os.path.join(ROOT, "tests"), tmp_path / "tests", ignore=ign)
     pkg = tmp_path / "rotary_position_embedding_gb300"
     pkg.mkdir()
-    for f in ("__init__.py", "workloads.py"):
-        shutil.copy(os.path.join(ROOT, "rotary_position_embedding_gb300", f), pkg / f)
+    src_pkg = os.path.join(ROOT, "rotary_position_embedding_gb300")
+    for f in os.listdir(src_pkg):
+        if f.endswith(".py"):
+            shutil.copy(os.path.join(src_pkg, f), pkg / f)
     r = subprocess.run([sys.executable, "-m", "pytest", "tests/test_oracle_pins.py", "-x", "-q",
                         "-p", "no:cacheprovider"], cwd=tmp_path, capture_output=True, text=True,
                        timeout=600)
