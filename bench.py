@@ -64,6 +64,22 @@ def dist_env():
         int(os.environ.get("LOCAL_RANK", 0))
 
 
+def max_over_ranks(x, device=None):
+    """Largest value of x over all ranks (host-side timing reduction, not a data-path collective)."""
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_throughput(nbytes, numel, steps, total_ms, world):
+    """Whole-job GB/s and Gelem/s: every rank moved `steps` passes of its own batch in <= total_ms."""
+    sec = total_ms * 1e-3
+    return world * nbytes * steps / sec / 1e9, world * numel * steps / sec / 1e9
+
+
 def kernel_source_hash():
     h = hashlib.sha256()
     for f in KERNEL_SOURCES:
@@ -168,12 +184,12 @@ class ClockSampler:
 class Step:
     """One workload pass through the C ABI with pre-marshalled ctypes arguments."""
 
-    def __init__(self, rp, torch, w, device, n_sets):
+    def __init__(self, rp, torch, w, device, n_sets, shard=0):
         self.w = w
         self.torch = torch
         lib = rp.load_library()
         self.lib = lib
-        inp = wl.make_inputs(w)
+        inp = wl.make_inputs(w, shard=shard)
         self.x_host = inp["x"]
         self.pos_host = inp["position_ids"]
         tdt = torch.float16 if w.dtype == "float16" else torch.float32
@@ -266,7 +282,7 @@ def gpu_arm(args, rank, world, local_rank):
     stream = torch.cuda.current_stream(device)
     sh = ctypes.c_void_p(stream.cuda_stream)
     nbytes = wl.algorithmic_bytes(w)
-    step = Step(rp, torch, w, device, n_buffer_sets(w))
+    step = Step(rp, torch, w, device, n_buffer_sets(w), shard=rank)
     for k in range(args.warmup):
         step.launch(k % len(step.xs), sh)
     torch.cuda.synchronize()
@@ -283,14 +299,11 @@ def gpu_arm(args, rank, world, local_rank):
     t1 = time.time()
     if world > 1:
         torch.distributed.barrier()
-        tt = torch.tensor([total_ms], dtype=torch.float64, device=device)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(tt.item())
+        total_ms = max_over_ranks(total_ms, device)
     clocks = sampler.stop(t0, t1) if rank == 0 else None
 
     ms_per_step = total_ms / args.steps
-    value = world * nbytes * args.steps / (total_ms * 1e-3) / 1e9
-    gelem = world * w.numel * args.steps / (total_ms * 1e-3) / 1e9
+    value, gelem = aggregate_throughput(nbytes, w.numel, args.steps, total_ms, world)
     kern_ms = float(np.mean(kern))
     peak, peak_src = measured_peak()
     achieved = nbytes / (kern_ms * 1e-3) / 1e9
@@ -302,6 +315,7 @@ def gpu_arm(args, rank, world, local_rank):
         cpu = cpu_baseline(args, w) if world == 1 else None
         out = {
             "metric": METRIC,
+            "variant": rp.get_variant(),
             "value": round(value, 2),
             "unit": "GB/s",
             "gelem_per_s": round(gelem, 3),
@@ -329,7 +343,9 @@ def gpu_arm(args, rank, world, local_rank):
             "roofline": {
                 "bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "traffic": profiled_traffic("rope_rows_kernel", w.name),
-                "peak_source": peak_src, "kernel": "rope_rows_kernel<half,8,half-split,rank3,cache2d>",
+                "peak_source": peak_src,
+                "kernel": "rope_tma_kernel<half,half-split,rank3,cache2d> (the automatic variant for "
+                          "X >= 8 MiB on the 128-bit path)",
                 "kernel_us": round(kern_ms * 1e3, 3),
                 "frac_of_nominal_8tbs": round(achieved / 8000.0, 4),
             },
@@ -351,18 +367,20 @@ def measure_rows(args, torch, rp, device, peak):
     sh = ctypes.c_void_p(stream.cuda_stream)
     rows = {}
     for name, w in wl.WORKLOADS.items():
-        variants = [("cached", False)]
+        variants = [("cached", False, "auto"), ("cached", False, "simt")]
         if w.kind == "fused":
-            variants = [("fused", True), ("cached", False)]
+            variants = [("fused", True, "auto"), ("cached", False, "auto")]
         step = Step(rp, torch, w, device, n_buffer_sets(w))
-        for label, fused in variants:
+        for label, fused, variant in variants:
+            rp.set_variant(variant)
             for k in range(20):
                 step.launch(k % len(step.xs), sh, fused)
             total_ms, kern = time_steps(torch, step, args.row_steps, sh, fused)
+            rp.set_variant("auto")
             nbytes = wl.algorithmic_bytes(w, cached=not fused)
             kern_ms = float(np.median(kern))
             gbs = nbytes / (kern_ms * 1e-3) / 1e9
-            key = name if len(variants) == 1 else f"{name}:{label}"
+            key = f"{name}:{label}:{variant}"
             rows[key] = {
                 "us_per_launch_median": round(kern_ms * 1e3, 3),
                 "us_per_step_incl_gaps": round(total_ms / args.row_steps * 1e3, 3),

@@ -69,12 +69,15 @@ typedef struct CUstream_st* rope_stream_t;
  *               (B, N, S, H). H must be even. ([RotaryEmbedding manifest,
  *               inputs/X and outputs/Y])
  * x_shape       x_rank (3 or 4) host int64 values.
- * cos_cache,    With position_ids: rank 2, (max_sequence_length, rd/2); row p
- * sin_cache     is the coefficient row of position p. Without position_ids:
- *               rank 3, (B, S, rd/2); row (b, s) belongs to token (b, s).
- *               cache_shape holds cache_rank host int64 values. Both tables
- *               have this shape. ([manifest, inputs/cos_cache, sin_cache])
- * position_ids  NULL, or device int64 (B, S). ([manifest, inputs/position_ids])
+ * cos_cache,    cache_rank 2: (max_sequence_length, rd/2), gathered at
+ * sin_cache     position_ids; row p is the coefficient row of position p.
+ *               cache_rank 3: (B, S, rd/2), row (b, s) belongs to token (b, s),
+ *               and no position_ids are taken. cache_shape holds cache_rank
+ *               host int64 values; both tables have this shape. ([manifest,
+ *               inputs/cos_cache, sin_cache])
+ * position_ids  device int64 (B, S), required with a rank-2 cache (it may be
+ *               NULL only when X is empty); must be NULL with a rank-3 cache.
+ *               ([manifest, inputs/position_ids])
  *               A position outside [0, max_sequence_length) never reads the
  *               cache: every element of that token is copied through and, if
  *               oor_flag is not NULL, the device int32 *oor_flag is set to 1
@@ -191,6 +194,27 @@ rope_status rope_apply_fused(rope_dtype dtype, int32_t x_rank, const int64_t* x_
 rope_status rope_cache_build(rope_dtype dtype, const float* inv_freq, int32_t half, int64_t rows,
                              float attention_scaling, void* cos_out, void* sin_out,
                              rope_stream_t stream);
+
+/*
+ * Kernel variant selection (process-wide; default ROPE_VARIANT_AUTO).
+ *   ROPE_VARIANT_AUTO  the 128-bit vector path of a large enough X goes
+ *                      through the TMA pipeline (shared-memory stage ring);
+ *                      everything else through the SIMT kernels.
+ *   ROPE_VARIANT_SIMT  always the SIMT kernels.
+ *   ROPE_VARIANT_TMA   the TMA pipeline whenever the shape allows it (vector
+ *                      path, head size <= 256 elements), whatever its size.
+ * All variants compute the same result. ([MRotaryEmbedding README,
+ * Implementation variants]: one implementation is selected per call from the
+ * device, the shapes and the dtypes.) Returns ROPE_ERR_INVALID_ARG for an
+ * unknown value. No CUDA call.
+ */
+typedef enum rope_variant {
+  ROPE_VARIANT_AUTO = 0,
+  ROPE_VARIANT_SIMT = 1,
+  ROPE_VARIANT_TMA = 2
+} rope_variant;
+rope_status rope_set_variant(rope_variant variant);
+rope_variant rope_get_variant(void);
 
 /* Static name of a status code. */
 const char* rope_status_string(rope_status status);

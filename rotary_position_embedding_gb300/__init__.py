@@ -18,11 +18,13 @@ from .build import LIB_PATH, build_library  # noqa: F401
 __all__ = [
     "RopeError", "load_library", "build_library", "rope_apply", "mrope_apply",
     "mrope_apply_stream_map", "mrope_stream_map", "rope_apply_fused", "rope_cache_build",
+    "set_variant", "get_variant", "variant",
     "ROPE_OK", "ROPE_ERR_INVALID_ARG", "ROPE_ERR_UNSUPPORTED", "ROPE_ERR_CUDA",
 ]
 
 ROPE_OK, ROPE_ERR_INVALID_ARG, ROPE_ERR_UNSUPPORTED, ROPE_ERR_CUDA = 0, 1, 2, 3
 ROPE_F32, ROPE_F16 = 0, 1
+VARIANTS = {"auto": 0, "simt": 1, "tma": 2}
 _UNSUPPORTED_DTYPE = 99  # passed through so the library reports ROPE_ERR_UNSUPPORTED
 
 _lock = threading.Lock()
@@ -46,6 +48,8 @@ SIGNATURES = {
     "mrope_stream_map": [_i32p, _i32, _i32, _u8p],
     "rope_apply_fused": [_i32, _i32, _i64p, _vp, _vp, _vp, _f32, _vp, _i32, _i32, _i32, _vp],
     "rope_cache_build": [_i32, _vp, _i32, _i64, _f32, _vp, _vp, _vp],
+    "rope_set_variant": [_i32],
+    "rope_get_variant": [],
     "rope_status_string": [_i32],
     "rope_last_error": [],
 }
@@ -257,3 +261,29 @@ def rope_cache_build(inv_freq, rows, dtype=None, *, attention_scaling=1.0, cos_o
                                   _ptr(cos_out), _ptr(sin_out), _stream(inv_freq, stream))
     _check("rope_cache_build", st)
     return cos_out, sin_out
+
+
+def set_variant(name):
+    """Kernel variant for later calls in this process: "auto", "simt" or "tma"."""
+    lib = load_library()
+    _check("rope_set_variant", lib.rope_set_variant(VARIANTS[name]))
+
+
+def get_variant():
+    code = load_library().rope_get_variant()
+    return {v: k for k, v in VARIANTS.items()}[code]
+
+
+class variant:
+    """Context manager: ``with variant("tma"): ...``."""
+
+    def __init__(self, name):
+        self.name = name
+
+    def __enter__(self):
+        self.prev = get_variant()
+        set_variant(self.name)
+        return self
+
+    def __exit__(self, *exc):
+        set_variant(self.prev)

@@ -12,8 +12,10 @@
 //    may leave an odd head size), num_heads.
 // The library allocates nothing, keeps no per-call state and never
 // synchronises; host-side failures return before any launch.
+#include <cuda.h>  // CUtensorMap and its enums; the encoder is fetched from the driver at run time
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -24,6 +26,7 @@
 
 #include "../../include/rope.h"
 #include "rope_internal.h"
+#include "rope_tma.cuh"
 
 // Launch-shape defaults (threads a CTA aims for; resident-CTA waves in the
 // persistent grid). Overridable at compile time.
@@ -33,12 +36,33 @@
 #ifndef ROPE_GRID_WAVES
 #define ROPE_GRID_WAVES 1
 #endif
+// TMA pipeline: bytes of one X tile, shared-memory budget of the stage ring,
+// smallest X (bytes) sent down the pipeline, most stages.
+#ifndef ROPE_TMA_TILE_BYTES
+#define ROPE_TMA_TILE_BYTES 32768
+#endif
+#ifndef ROPE_TMA_SMEM_BUDGET
+#define ROPE_TMA_SMEM_BUDGET (200 * 1024)
+#endif
+#ifndef ROPE_TMA_MIN_BYTES
+#define ROPE_TMA_MIN_BYTES (8 << 20)
+#endif
+#ifndef ROPE_TMA_MAX_STAGES
+#define ROPE_TMA_MAX_STAGES 8
+#endif
 
 using namespace rope_gb300;
+
+#define ROPE_TRY(expr)               \
+  do {                               \
+    rope_status _s = (expr);         \
+    if (_s != ROPE_OK) return _s;    \
+  } while (0)
 
 namespace {
 
 thread_local std::string g_last_error;
+std::atomic<int> g_variant{ROPE_VARIANT_AUTO};
 
 rope_status fail(rope_status st, const char* fmt, ...) {
   char buf[512];
@@ -93,6 +117,10 @@ rope_status device_facts(const void* fn, int threads, size_t smem, int* sms, int
   auto key = std::make_tuple(dev, fn, threads, smem);
   auto oc = g_occupancy.find(key);
   if (oc == g_occupancy.end()) {
+    if (smem > 48 * 1024) {
+      e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(max dynamic shared memory)");
+    }
     int b = 0;
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, fn, threads, smem);
     if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
@@ -217,6 +245,141 @@ rope_status plan(const Geom& g, int es, bool vec, const void* fn, bool smem_tabl
   return ROPE_OK;
 }
 
+// ---------------------------------------------------------------------------
+// TMA pipeline planning (see rope_tma.cuh).
+// ---------------------------------------------------------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*,
+                                  CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                  CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled() {
+  static std::once_flag once;
+  static EncodeTiledFn fn = nullptr;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(f);
+  });
+  return fn;
+}
+
+bool tma_eligible(const Geom& g, int es, bool vec) {
+  const int variant = g_variant.load(std::memory_order_relaxed);
+  if (variant == ROPE_VARIANT_SIMT) return false;
+  if (!vec || g.H > 256) return false;
+  const int64_t nP = g.h / (16 / es);
+  if (nP < 1 || nP > kTmaConsumers) return false;
+  if (g.ntok > INT32_MAX || g.N > INT32_MAX || g.S > INT32_MAX || g.B > INT32_MAX) return false;
+  if (variant == ROPE_VARIANT_AUTO && g.numel * es < (int64_t)ROPE_TMA_MIN_BYTES) return false;
+  return encode_tiled() != nullptr;
+}
+
+struct TmaLaunch {
+  TParams tp;
+  alignas(64) CUtensorMap mx;
+  alignas(64) CUtensorMap my;
+  Launch L;
+};
+
+rope_status encode_x_map(CUtensorMap* m, const Geom& g, int rank, int es, const void* base,
+                         const TParams& tp) {
+  cuuint64_t dims[4], strides[3];
+  cuuint32_t box[4], estr[4] = {1, 1, 1, 1};
+  cuuint32_t r;
+  if (rank == 3) {
+    r = 3;
+    dims[0] = g.H, dims[1] = g.N, dims[2] = g.ntok;
+    strides[0] = g.H * es, strides[1] = g.N * g.H * es;
+    box[0] = (cuuint32_t)g.H, box[1] = tp.NG, box[2] = tp.TS;
+  } else {
+    r = 4;
+    dims[0] = g.H, dims[1] = g.S, dims[2] = g.N, dims[3] = g.B;
+    strides[0] = g.H * es, strides[1] = g.S * g.H * es, strides[2] = g.N * g.S * g.H * es;
+    box[0] = (cuuint32_t)g.H, box[1] = tp.TS, box[2] = tp.NG, box[3] = 1;
+  }
+  CUresult e = encode_tiled()(m, es == 2 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                              r, const_cast<void*>(base), dims, strides, box, estr,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (e != CUDA_SUCCESS) return fail(ROPE_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)e);
+  return ROPE_OK;
+}
+
+// Fills kp's geometry and the TMA launch; ROPE_ERR_UNSUPPORTED (no message)
+// when the shape does not fit the pipeline, in which case the caller falls
+// back to the register-path kernel.
+rope_status plan_tma(const Geom& g, int es, int rank, int slots, const void* fn, const void* x, void* y,
+                     KParams* kp, TmaLaunch* T) {
+  const int V = 16 / es;
+  TParams& tp = T->tp;
+  memset(&tp, 0, sizeof(tp));
+  int64_t TS, NG;
+  if (rank == 3) {
+    NG = g.N < 256 ? g.N : 256;
+    TS = ROPE_TMA_TILE_BYTES / (NG * g.H * es);
+    if (TS < 1) TS = 1;
+    if (TS > 32) TS = 32;
+    if (TS > g.ntok) TS = g.ntok;
+    tp.head_groups = (int32_t)((g.N + NG - 1) / NG);
+    tp.ntiles = ((g.ntok + TS - 1) / TS) * tp.head_groups;
+  } else {
+    TS = g.S < 32 ? g.S : 32;
+    NG = ROPE_TMA_TILE_BYTES / (TS * g.H * es);
+    if (NG < 1) NG = 1;
+    if (NG > g.N) NG = g.N;
+    if (NG > 256) NG = 256;
+    tp.head_groups = (int32_t)((g.N + NG - 1) / NG);
+    tp.s_tiles = (int32_t)((g.S + TS - 1) / TS);
+    tp.ntiles = g.B * tp.head_groups * (int64_t)tp.s_tiles;
+  }
+  tp.TS = (int32_t)TS;
+  tp.NG = (int32_t)NG;
+  tp.slots = slots;
+  tp.x_bytes = (uint32_t)(TS * NG * g.H * es);
+  tp.coef_off = tp.x_bytes;
+  tp.flag_off = tp.coef_off + (uint32_t)(TS * slots * 2 * g.h * es);
+  tp.stage_bytes = (tp.flag_off + (uint32_t)TS * 4 + 1023) / 1024 * 1024;
+  tp.bar_bytes = 1024;
+  int64_t K = (ROPE_TMA_SMEM_BUDGET - tp.bar_bytes) / tp.stage_bytes;
+  if (K > ROPE_TMA_MAX_STAGES) K = ROPE_TMA_MAX_STAGES;
+  if (K < 2) return ROPE_ERR_UNSUPPORTED;
+  tp.K = (int32_t)K;
+  const size_t smem = tp.bar_bytes + (size_t)K * tp.stage_bytes;
+
+  kp->ntok = g.ntok;
+  kp->S = g.S;
+  kp->N = g.N;
+  kp->H = g.H;
+  kp->h = (int32_t)g.h;
+  kp->rd = (int32_t)g.rd;
+  kp->nP = (int32_t)(g.h / V);
+  kp->U = kp->nP;
+  kp->Ublk = kp->nP;
+
+  int sms = 0, per_sm = 0;
+  rope_status st = device_facts(fn, kTmaThreads, smem, &sms, &per_sm);
+  if (st != ROPE_OK) return st;
+  int64_t gx = (int64_t)sms * per_sm;
+  if (gx > tp.ntiles) gx = tp.ntiles;
+  T->L.grid = dim3((unsigned)gx, 1, 1);
+  T->L.block = dim3(kTmaThreads, 1, 1);
+  T->L.smem = smem;
+  ROPE_TRY(encode_x_map(&T->mx, g, rank, es, x, tp));
+  ROPE_TRY(encode_x_map(&T->my, g, rank, es, y, tp));
+  return ROPE_OK;
+}
+
+rope_status launch_tma(const void* fn, TmaLaunch* T, KParams* kp, rope_stream_t stream) {
+  void* args[] = {kp, &T->tp, &T->mx, &T->my};
+  cudaError_t e = cudaLaunchKernel(fn, T->L.grid, T->L.block, args, T->L.smem, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "TMA kernel launch");
+  return ROPE_OK;
+}
+
 rope_status launch(const void* fn, const Launch& L, KParams* kp, rope_stream_t stream) {
   void* args[] = {kp};
   cudaError_t e = cudaLaunchKernel(fn, L.grid, L.block, args, L.smem, (cudaStream_t)stream);
@@ -245,12 +408,6 @@ rope_status check_elem_ptr(const void* p, const char* name, size_t align) {
     return fail(ROPE_ERR_INVALID_ARG, "%s is not aligned to %zu bytes", name, align);
   return ROPE_OK;
 }
-
-#define ROPE_TRY(expr)               \
-  do {                               \
-    rope_status _s = (expr);         \
-    if (_s != ROPE_OK) return _s;    \
-  } while (0)
 
 // Interleaved stream map: walk t, h, w cyclically, skipping streams whose
 // section count is used up, so every stream gets exactly its section count.
@@ -323,7 +480,6 @@ rope_status mrope_common(rope_dtype dtype, int32_t x_rank, const int64_t* x_shap
   if (oor_flag && !aligned(oor_flag, 4)) return fail(ROPE_ERR_INVALID_ARG, "oor_flag is misaligned");
 
   const bool vec = vector_ok(g, es, {x, y, cos_cache, sin_cache});
-  const void* fn = rope_kernel_mrope(dtype, vec, interleaved != 0, x_rank == 4);
   KParams kp;
   memset(&kp, 0, sizeof(kp));
   kp.x = x;
@@ -336,6 +492,14 @@ rope_status mrope_common(rope_dtype dtype, int32_t x_rank, const int64_t* x_shap
   kp.scale_is_one = scale == 1.0f;
   kp.cache_rows = cache_rows;
   for (int64_t i = 0; i < g.h; ++i) kp.smap[i >> 4] |= (uint32_t)map[i] << ((i & 15) * 2);
+  if (tma_eligible(g, es, vec)) {
+    const void* tfn = tma_kernel(dtype, interleaved != 0, x_rank == 4, Coef::kMRope);
+    TmaLaunch T;
+    const rope_status ts = plan_tma(g, es, x_rank, 3, tfn, x, y, &kp, &T);
+    if (ts == ROPE_OK) return launch_tma(tfn, &T, &kp, stream);
+    if (ts != ROPE_ERR_UNSUPPORTED) return ts;
+  }
+  const void* fn = rope_kernel_mrope(dtype, vec, interleaved != 0, x_rank == 4);
   Launch L;
   ROPE_TRY(plan(g, es, vec, fn, false, &kp, &L));
   return launch(fn, L, &kp, stream);
@@ -357,42 +521,43 @@ rope_status rope_apply(rope_dtype dtype, int32_t x_rank, const int64_t* x_shape,
   if (interleaved != 0 && interleaved != 1)
     return fail(ROPE_ERR_INVALID_ARG, "interleaved must be 0 or 1 (got %d)", interleaved);
   ROPE_TRY(rotary_width(rotary_embedding_dim, /*odd_head_ok=*/false, &g));
+  // The variant is fixed by the cache rank (a NULL position_ids pointer may
+  // also be an empty tensor): rank 2 gathers at position_ids, rank 3 is the
+  // per-token table and takes no position_ids.
   if (!cache_shape) return fail(ROPE_ERR_INVALID_ARG, "cache_shape is NULL");
+  const bool gather = cache_rank == 2;
   int64_t rows = 0;
-  if (position_ids) {
-    if (cache_rank != 2)
-      return fail(ROPE_ERR_INVALID_ARG, "with position_ids the cos/sin cache must be rank 2, got %d",
-                  cache_rank);
+  if (cache_rank == 2) {
     if (cache_shape[0] < 0) return fail(ROPE_ERR_INVALID_ARG, "cache rows are negative");
     if (cache_shape[1] * 2 != g.rd)
       return fail(ROPE_ERR_INVALID_ARG, "cache width %lld * 2 != rotary width %lld",
                   (long long)cache_shape[1], (long long)g.rd);
     rows = cache_shape[0];
-  } else {
-    if (cache_rank != 3)
-      return fail(ROPE_ERR_INVALID_ARG, "without position_ids the cos/sin cache must be rank 3, got %d",
-                  cache_rank);
+  } else if (cache_rank == 3) {
+    if (position_ids)
+      return fail(ROPE_ERR_INVALID_ARG, "position_ids given with a 3-D (B, S, rd/2) cache");
     if (cache_shape[0] != g.B || cache_shape[1] != g.S || cache_shape[2] * 2 != g.rd)
       return fail(ROPE_ERR_INVALID_ARG,
                   "3-D cache shape (%lld, %lld, %lld) must be (B, S, rd/2) = (%lld, %lld, %lld)",
                   (long long)cache_shape[0], (long long)cache_shape[1], (long long)cache_shape[2],
                   (long long)g.B, (long long)g.S, (long long)g.h);
+  } else {
+    return fail(ROPE_ERR_INVALID_ARG, "the cos/sin cache must be rank 2 (with position_ids) or 3, got %d",
+                cache_rank);
   }
   if (g.numel == 0) return ROPE_OK;
   const int es = elem_size(dtype);
   ROPE_TRY(check_elem_ptr(x, "x", es));
   ROPE_TRY(check_elem_ptr(y, "y", es));
-  if (!position_ids || rows > 0) {
+  if (!gather || rows > 0) {
     ROPE_TRY(check_elem_ptr(cos_cache, "cos_cache", es));
     ROPE_TRY(check_elem_ptr(sin_cache, "sin_cache", es));
   }
-  if (position_ids && !aligned(position_ids, 8))
-    return fail(ROPE_ERR_INVALID_ARG, "position_ids is not aligned to 8 bytes");
+  if (gather) ROPE_TRY(check_elem_ptr(position_ids, "position_ids", 8));
   if (oor_flag && !aligned(oor_flag, 4)) return fail(ROPE_ERR_INVALID_ARG, "oor_flag is misaligned");
 
   const bool vec = vector_ok(g, es, {x, y, cos_cache, sin_cache});
-  const Coef mode = position_ids ? Coef::kCache2D : Coef::kCache3D;
-  const void* fn = rope_kernel_cached(dtype, vec, interleaved != 0, x_rank == 4, mode);
+  const Coef mode = gather ? Coef::kCache2D : Coef::kCache3D;
   KParams kp;
   memset(&kp, 0, sizeof(kp));
   kp.x = x;
@@ -404,6 +569,14 @@ rope_status rope_apply(rope_dtype dtype, int32_t x_rank, const int64_t* x_shape,
   kp.scale = 1.0f;
   kp.scale_is_one = 1;
   kp.cache_rows = rows;
+  if (tma_eligible(g, es, vec)) {
+    const void* tfn = tma_kernel(dtype, interleaved != 0, x_rank == 4, mode);
+    TmaLaunch T;
+    const rope_status ts = plan_tma(g, es, x_rank, 1, tfn, x, y, &kp, &T);
+    if (ts == ROPE_OK) return launch_tma(tfn, &T, &kp, stream);
+    if (ts != ROPE_ERR_UNSUPPORTED) return ts;
+  }
+  const void* fn = rope_kernel_cached(dtype, vec, interleaved != 0, x_rank == 4, mode);
   Launch L;
   ROPE_TRY(plan(g, es, vec, fn, false, &kp, &L));
   return launch(fn, L, &kp, stream);
@@ -505,6 +678,16 @@ rope_status rope_cache_build(rope_dtype dtype, const float* inv_freq, int32_t ha
   if (e != cudaSuccess) return cuda_fail(e, "rope_cache_build launch");
   return ROPE_OK;
 }
+
+rope_status rope_set_variant(rope_variant variant) {
+  g_last_error.clear();
+  if (variant != ROPE_VARIANT_AUTO && variant != ROPE_VARIANT_SIMT && variant != ROPE_VARIANT_TMA)
+    return fail(ROPE_ERR_INVALID_ARG, "unknown variant %d", (int)variant);
+  g_variant.store(variant, std::memory_order_relaxed);
+  return ROPE_OK;
+}
+
+rope_variant rope_get_variant(void) { return (rope_variant)g_variant.load(std::memory_order_relaxed); }
 
 const char* rope_status_string(rope_status status) {
   switch (status) {

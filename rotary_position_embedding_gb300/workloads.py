@@ -179,18 +179,23 @@ def mrope_ids(B, S, rows, seed=1, oor_seed=2, oor_fraction=0.01, grid=32, max_of
     return ids
 
 
-def make_inputs(w: Workload):
-    """Host arrays for workload ``w``: x, position_ids (or None), inv_freq."""
-    x = x_normal(w.shape, np.dtype(w.dtype), seed=0)
+def make_inputs(w: Workload, shard=0):
+    """Host arrays for workload ``w``: x, position_ids (or None), inv_freq.
+
+    ``shard`` selects an independent batch of the same recipe (one per rank
+    when several GPUs each process their own batch); shard 0 is the default.
+    """
+    base = 1000 * int(shard)
+    x = x_normal(w.shape, np.dtype(w.dtype), seed=base + 0)
     B, S = w.batch, w.seq
     if w.positions == "none":
         pos = None
     elif w.positions == "offset":
-        pos = positions_offset(B, S, seed=1)
+        pos = positions_offset(B, S, seed=base + 1)
     elif w.positions == "uniform":
-        pos = positions_uniform(B, S, w.cache_rows, seed=1)
+        pos = positions_uniform(B, S, w.cache_rows, seed=base + 1)
     elif w.positions == "mrope":
-        pos = mrope_ids(B, S, w.cache_rows, seed=1, oor_seed=2)
+        pos = mrope_ids(B, S, w.cache_rows, seed=base + 1, oor_seed=base + 2)
     else:
         raise ValueError(w.positions)
     inv = inv_freq(w.rope_base, w.rope_dim or w.rotary_dim, w.half)

@@ -28,7 +28,8 @@ def declared_functions():
 def test_header_declares_the_abi():
     fns = declared_functions()
     for name in ("rope_apply", "mrope_apply", "mrope_apply_stream_map", "mrope_stream_map",
-                 "rope_apply_fused", "rope_cache_build", "rope_status_string", "rope_last_error"):
+                 "rope_apply_fused", "rope_cache_build", "rope_status_string", "rope_last_error",
+                 "rope_set_variant", "rope_get_variant"):
         assert name in fns
 
 
@@ -72,8 +73,9 @@ def _rope(so, **kw):
     (dict(rd=6), INVALID),                              # width 8 * 2 != 6
     (dict(rd=7, cs=_i64(16, 3)), INVALID),              # odd rotary width
     (dict(cs=_i64(16, 4)), INVALID),                    # width * 2 != 16
-    (dict(crank=3, cs=_i64(2, 4, 8)), INVALID),         # position_ids present -> 2-D cache
-    (dict(pos=None, crank=2), INVALID),                 # no position_ids -> 3-D cache
+    (dict(crank=3, cs=_i64(2, 4, 8)), INVALID),         # a 3-D cache takes no position_ids
+    (dict(pos=None, crank=2), INVALID),                 # a 2-D cache needs position_ids
+    (dict(crank=1, cs=_i64(16)), INVALID),
     (dict(pos=None, crank=3, cs=_i64(2, 5, 8)), INVALID),   # 3-D cache must be (B, S, rd/2)
     (dict(xs=_i64(2, -1, 64)), INVALID),
     (dict(rank=4, xs=_i64(2, 4, 5, 16), nh=3), INVALID),    # num_heads != N
@@ -142,6 +144,18 @@ def test_fused_and_cache_build_reject_before_launch(lib):
     assert so.rope_cache_build(F16, FAKE, 4, -1, 1.0, FAKE, FAKE2, None) == INVALID
     assert so.rope_cache_build(7, FAKE, 4, 10, 1.0, FAKE, FAKE2, None) == UNSUPPORTED
     assert so.rope_cache_build(F16, FAKE, 4, 0, 1.0, None, None, None) == OK
+
+
+def test_variant_selection(lib):
+    so = lib.load_library()
+    assert lib.get_variant() == "auto"
+    with lib.variant("tma"):
+        assert so.rope_get_variant() == 2
+        with lib.variant("simt"):
+            assert lib.get_variant() == "simt"
+        assert lib.get_variant() == "tma"
+    assert lib.get_variant() == "auto"
+    assert so.rope_set_variant(7) == INVALID
 
 
 def test_status_strings(lib):

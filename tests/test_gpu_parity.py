@@ -57,13 +57,13 @@ def torch_mod():
 # RotaryEmbedding: small exhaustive grid
 # ---------------------------------------------------------------------------
 
-ROPE_GRID = list(itertools.product(
+ROPE_GRID = [c + (v,) for c in itertools.product(
     ["f16", "f32"], [3, 4], ["pos", "cache3d"], [0, 1], ["full", "partial"],
-    ["vector", "scalar_shape", "scalar_misaligned"]))
+    ["vector", "scalar_shape", "scalar_misaligned"]) for v in (["simt", "tma"] if c[-1] == "vector" else ["simt"])]
 
 
-@pytest.mark.parametrize("dt,rank,cache,inter,rot,path", ROPE_GRID)
-def test_rope_grid(lib, orc, cuda, torch_mod, dt, rank, cache, inter, rot, path):
+@pytest.mark.parametrize("dt,rank,cache,inter,rot,path,variant", ROPE_GRID)
+def test_rope_grid(lib, orc, cuda, torch_mod, dt, rank, cache, inter, rot, path, variant):
     torch = torch_mod
     dtype = DT[dt]
     rng = np.random.default_rng(_seed(dt, rank, cache, inter, rot, path))
@@ -89,9 +89,10 @@ def test_rope_grid(lib, orc, cuda, torch_mod, dt, rank, cache, inter, rot, path)
     off = 1 if path == "scalar_misaligned" else 0
     xd = _dev(x, torch, cuda, off)
     flag = torch.zeros(1, dtype=torch.int32, device=cuda)
-    yd = lib.rope_apply(xd, _dev(cos, torch, cuda), _dev(sin, torch, cuda),
-                        None if pos is None else _dev(pos, torch, cuda), interleaved=inter,
-                        rotary_embedding_dim=rd, num_heads=nh, oor_flag=flag)
+    with lib.variant(variant):
+        yd = lib.rope_apply(xd, _dev(cos, torch, cuda), _dev(sin, torch, cuda),
+                            None if pos is None else _dev(pos, torch, cuda), interleaved=inter,
+                            rotary_embedding_dim=rd, num_heads=nh, oor_flag=flag)
     torch.cuda.synchronize()
     mask = rope_passthrough_mask(shape, rank, N, rd, pos, R)
     compare(_host(yd), y_ref, x, rank, N, mask)
@@ -207,16 +208,81 @@ def test_side_stream(lib, orc, cuda, torch_mod):
 
 
 # ---------------------------------------------------------------------------
+# TMA pipeline: tiles that run past the tokens and past the heads, head sizes
+# from 16 to 256 elements, stage-ring phases that wrap many times, in place
+# ---------------------------------------------------------------------------
+
+TMA_SHAPES = [
+    # name, kind, rank, dtype, B, S, N, H, rd, inter
+    ("r3_head_groups", "rope", 3, "f16", 2, 9, 300, 64, 0, 0),      # 300 heads: two head groups
+    ("r4_both_tails", "rope", 4, "f16", 2, 70, 5, 128, 0, 1),       # S and N tails
+    ("r4_f32_h256", "rope", 4, "f32", 2, 45, 3, 256, 64, 0),        # 1 head per tile, partial
+    ("r3_decode", "rope", 3, "f16", 67, 1, 40, 128, 0, 0),
+    ("r3_h16", "rope", 3, "f16", 3, 101, 7, 16, 0, 1),
+    ("r3_many_rounds", "rope", 3, "f16", 8, 4096, 8, 128, 0, 0),    # ~13 tiles per CTA
+    ("r4_many_rounds", "rope", 4, "f16", 4, 4096, 8, 128, 64, 1),
+    ("mr3_l1", "mrope", 3, "f16", 2, 777, 28, 128, 0, 0),
+    ("mr4_l0_tails", "mrope", 4, "f16", 2, 70, 5, 128, 96, 1),
+    ("mr3_f32_scale", "mrope", 3, "f32", 2, 300, 6, 64, 0, 0),
+]
+
+
+@pytest.mark.parametrize("case", TMA_SHAPES, ids=[c[0] for c in TMA_SHAPES])
+@pytest.mark.parametrize("in_place", [False, True])
+def test_tma_pipeline_shapes(lib, orc, cuda, torch_mod, case, in_place):
+    torch = torch_mod
+    name, kind, rank, dt, B, S, N, H, rd, inter = case
+    dtype = DT[dt]
+    rng = np.random.default_rng(_seed(*case))
+    shape = _x_shape(rank, B, S, N, H)
+    x = rng.standard_normal(shape).astype(dtype)
+    h = (rd or H) // 2
+    R = 5000
+    inv = wl.inv_freq(10000.0, rd or H, h)
+    cos, sin = orc.cache_build(inv, R, dtype)
+    nh = N if rank == 3 else 0
+    xd = _dev(x, torch, cuda)
+    flag = torch.zeros(1, dtype=torch.int32, device=cuda)
+    if kind == "rope":
+        pos = rng.integers(0, R, (B, S))
+        pos.ravel()[rng.choice(pos.size, size=max(1, pos.size // 50), replace=False)] = R + 3
+        y_ref, _ = orc.rope(x, cos, sin, pos, inter, rd, nh)
+        with lib.variant("tma"):
+            yd = lib.rope_apply(xd, _dev(cos, torch, cuda), _dev(sin, torch, cuda), _dev(pos, torch, cuda),
+                                interleaved=inter, rotary_embedding_dim=rd, num_heads=nh, oor_flag=flag,
+                                out=xd if in_place else None)
+        mask = rope_passthrough_mask(shape, rank, N, rd, pos, R)
+    else:
+        sec = (h - 2 * (h // 3), h // 3, h // 3)
+        layout = 1 if name.startswith("mr3_l1") else 0
+        scale = float(np.float32(0.6)) if "scale" in name else 1.0
+        pos3 = rng.integers(0, R, (3, B, S))
+        pos3.ravel()[rng.choice(pos3.size, size=max(1, pos3.size // 50), replace=False)] = -2
+        y_ref, _ = orc.mrope(x, cos, sin, pos3, sec, layout, scale, inter, rd, nh)
+        with lib.variant("tma"):
+            yd = lib.mrope_apply(xd, _dev(cos, torch, cuda), _dev(sin, torch, cuda), _dev(pos3, torch, cuda),
+                                 sec, mrope_layout=layout, scale=scale, interleaved=inter,
+                                 rotary_embedding_dim=rd, num_heads=nh, oor_flag=flag,
+                                 out=xd if in_place else None)
+        smap = orc.mrope_stream_map(sec, layout, h)
+        mask = mrope_passthrough_mask(shape, rank, N, rd, pos3, R, smap, inter)
+    torch.cuda.synchronize()
+    compare(_host(yd), y_ref, x, rank, N, mask)
+    assert int(flag.item()) == 1   # some positions were out of range; no pipeline timeout (bit 1)
+
+
+# ---------------------------------------------------------------------------
 # MRotaryEmbedding
 # ---------------------------------------------------------------------------
 
-MROPE_GRID = list(itertools.product(
+MROPE_GRID = [c + (v,) for c in itertools.product(
     ["f16", "f32"], [3, 4], ["l0", "l1", "stride3"], [0, 1], ["full", "partial_odd_head"],
-    [1.0, 0.7], ["vector", "scalar_misaligned"]))
+    [1.0, 0.7], ["vector", "scalar_misaligned"])
+    for v in (["simt", "tma"] if c[-1] == "vector" and c[4] == "full" else ["simt"])]
 
 
-@pytest.mark.parametrize("dt,rank,layout,inter,rot,scale,path", MROPE_GRID)
-def test_mrope_grid(lib, orc, cuda, torch_mod, dt, rank, layout, inter, rot, scale, path):
+@pytest.mark.parametrize("dt,rank,layout,inter,rot,scale,path,variant", MROPE_GRID)
+def test_mrope_grid(lib, orc, cuda, torch_mod, dt, rank, layout, inter, rot, scale, path, variant):
     torch = torch_mod
     dtype = DT[dt]
     rng = np.random.default_rng(_seed(dt, rank, layout, inter, rot, scale, path))
@@ -248,10 +314,11 @@ def test_mrope_grid(lib, orc, cuda, torch_mod, dt, rank, layout, inter, rot, sca
     args = (xd, _dev(cos, torch, cuda), _dev(sin, torch, cuda), _dev(pos3, torch, cuda))
     flag = torch.zeros(1, dtype=torch.int32, device=cuda)
     kw = dict(scale=scale, interleaved=inter, rotary_embedding_dim=rd, num_heads=nh, oor_flag=flag)
-    if layout == "stride3":
-        yd = lib.mrope_apply_stream_map(*args, smap.tolist(), **kw)
-    else:
-        yd = lib.mrope_apply(*args, sec, mrope_layout=0 if layout == "l0" else 1, **kw)
+    with lib.variant(variant):
+        if layout == "stride3":
+            yd = lib.mrope_apply_stream_map(*args, smap.tolist(), **kw)
+        else:
+            yd = lib.mrope_apply(*args, sec, mrope_layout=0 if layout == "l0" else 1, **kw)
     torch.cuda.synchronize()
     mask = mrope_passthrough_mask(shape, rank, N, rd, pos3, R, smap, inter)
     compare(_host(yd), y_ref, x, rank, N, mask)
