@@ -21,6 +21,7 @@
 #include <cstring>
 #include <map>
 #include <mutex>
+#include <set>
 #include <string>
 #include <tuple>
 
@@ -100,6 +101,7 @@ bool mul_ok(int64_t a, int64_t b, int64_t* out) {
 std::mutex g_mu;
 std::map<int, int> g_sm_count;
 std::map<std::tuple<int, const void*, int, size_t>, int> g_occupancy;
+std::set<std::pair<int, const void*>> g_smem_raised;
 
 rope_status device_facts(const void* fn, int threads, size_t smem, int* sms, int* per_sm) {
   int dev = 0;
@@ -114,13 +116,21 @@ rope_status device_facts(const void* fn, int threads, size_t smem, int* sms, int
     it = g_sm_count.emplace(dev, n).first;
   }
   *sms = it->second;
+  // Kernels that take more than 48 KB of dynamic shared memory get the
+  // device's opt-in maximum once (a per-call value could later lower it below
+  // what an earlier, cached configuration launches with).
+  if (smem > 48 * 1024 && !g_smem_raised.count(std::make_pair(dev, fn))) {
+    int optin = 0;
+    e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute(shared memory opt-in)");
+    if ((size_t)optin < smem) return fail(ROPE_ERR_UNSUPPORTED, "needs %zu bytes of shared memory", smem);
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(max dynamic shared memory)");
+    g_smem_raised.insert(std::make_pair(dev, fn));
+  }
   auto key = std::make_tuple(dev, fn, threads, smem);
   auto oc = g_occupancy.find(key);
   if (oc == g_occupancy.end()) {
-    if (smem > 48 * 1024) {
-      e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(max dynamic shared memory)");
-    }
     int b = 0;
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, fn, threads, smem);
     if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
