@@ -52,6 +52,10 @@ def parse_args():
     ap.add_argument("--row-steps", type=int, default=400)
     ap.add_argument("--e2e-steps", type=int, default=30)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--variant", choices=["auto", "simt", "tma"], default="auto",
+                    help="kernel variant for the timed region (the library's automatic choice by default)")
+    ap.add_argument("--quick", action="store_true",
+                    help="timed region only: no per-workload rows, end-to-end or CPU legs (profiling runs)")
     return ap.parse_args()
 
 
@@ -278,6 +282,7 @@ def gpu_arm(args, rank, world, local_rank):
 
         dist.init_process_group("nccl", device_id=device)
     rp.load_library()
+    rp.set_variant(args.variant)
     w = wl.WORKLOADS[args.workload]
     stream = torch.cuda.current_stream(device)
     sh = ctypes.c_void_p(stream.cuda_stream)
@@ -310,12 +315,12 @@ def gpu_arm(args, rank, world, local_rank):
 
     out = None
     if rank == 0:
-        rows = {} if args.no_rows else measure_rows(args, torch, rp, device, peak)
-        e2e = measure_e2e(args, torch, step, sh, nbytes)
-        cpu = cpu_baseline(args, w) if world == 1 else None
+        rows = {} if (args.no_rows or args.quick) else measure_rows(args, torch, rp, device, peak)
+        e2e = None if args.quick else measure_e2e(args, torch, step, sh, nbytes)
+        cpu = cpu_baseline(args, w) if (world == 1 and not args.quick) else None
         out = {
             "metric": METRIC,
-            "variant": rp.get_variant(),
+            "variant": args.variant,
             "value": round(value, 2),
             "unit": "GB/s",
             "gelem_per_s": round(gelem, 3),
@@ -366,6 +371,7 @@ def measure_rows(args, torch, rp, device, peak):
     stream = torch.cuda.current_stream(device)
     sh = ctypes.c_void_p(stream.cuda_stream)
     rows = {}
+    prev = rp.get_variant()
     for name, w in wl.WORKLOADS.items():
         variants = [("cached", False, "auto"), ("cached", False, "simt")]
         if w.kind == "fused":
@@ -376,7 +382,7 @@ def measure_rows(args, torch, rp, device, peak):
             for k in range(20):
                 step.launch(k % len(step.xs), sh, fused)
             total_ms, kern = time_steps(torch, step, args.row_steps, sh, fused)
-            rp.set_variant("auto")
+            rp.set_variant(prev)
             nbytes = wl.algorithmic_bytes(w, cached=not fused)
             kern_ms = float(np.median(kern))
             gbs = nbytes / (kern_ms * 1e-3) / 1e9

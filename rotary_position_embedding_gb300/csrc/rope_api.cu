@@ -43,7 +43,7 @@
 #define ROPE_TMA_TILE_BYTES 32768
 #endif
 #ifndef ROPE_TMA_SMEM_BUDGET
-#define ROPE_TMA_SMEM_BUDGET (200 * 1024)
+#define ROPE_TMA_SMEM_BUDGET (110 * 1024)
 #endif
 #ifndef ROPE_TMA_MIN_BYTES
 #define ROPE_TMA_MIN_BYTES (8 << 20)
@@ -346,6 +346,21 @@ rope_status plan_tma(const Geom& g, int es, int rank, int slots, const void* fn,
     tp.s_tiles = (int32_t)((g.S + TS - 1) / TS);
     tp.ntiles = g.B * tp.head_groups * (int64_t)tp.s_tiles;
   }
+  // every consumer thread owns one pair unit of at most RU rows of a tile
+  const int64_t nPu = g.h / V;
+  const int64_t ru = slots == 3 ? 2 : 4;
+  const int64_t max_rows = ru * (kTmaConsumers / nPu);
+  while (TS * NG > max_rows && TS > 1) --TS;
+  while (TS * NG > max_rows && NG > 1) --NG;
+  if (rank == 3) {
+    tp.head_groups = (int32_t)((g.N + NG - 1) / NG);
+    tp.ntiles = ((g.ntok + TS - 1) / TS) * tp.head_groups;
+  } else {
+    tp.head_groups = (int32_t)((g.N + NG - 1) / NG);
+    tp.s_tiles = (int32_t)((g.S + TS - 1) / TS);
+    tp.ntiles = g.B * tp.head_groups * (int64_t)tp.s_tiles;
+  }
+  if (tp.ntiles >= INT32_MAX) return ROPE_ERR_UNSUPPORTED;
   tp.TS = (int32_t)TS;
   tp.NG = (int32_t)NG;
   tp.slots = slots;

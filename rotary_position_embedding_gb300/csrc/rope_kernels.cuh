@@ -151,20 +151,100 @@ struct Pairs {
 
 // Rotate all V pairs of a unit with coefficient vectors c, s.
 template <class T, int V, bool INTER>
+struct RotateUnit {
+  static __device__ __forceinline__ void run(const VecT<T, V>& a, const VecT<T, V>& b,
+                                             const VecT<T, V>& c, const VecT<T, V>& s,
+                                             VecT<T, V>& ya, VecT<T, V>& yb) {
+    using E = Elem<T>;
+    using P = Pairs<T, V, INTER>;
+#pragma unroll
+    for (int j = 0; j < V; ++j) {
+      float x0 = E::tof(P::get(a, b, P::i0(j)));
+      float x1 = E::tof(P::get(a, b, P::i1(j)));
+      float y0, y1;
+      rotate(x0, x1, E::tof(c.v[j]), E::tof(s.v[j]), y0, y1);
+      P::set(ya, yb, P::i0(j), E::fromf(y0));
+      P::set(ya, yb, P::i1(j), E::fromf(y1));
+    }
+  }
+};
+
+// float16 x 8: the same arithmetic on packed half2 words (two conversions and
+// one rounding pack per two values instead of one each).
+__device__ __forceinline__ void unpack8(const VecT<__half, 8>& v, __half2 (&w)[4]) {
+  __builtin_memcpy(&w, &v, 16);
+}
+__device__ __forceinline__ void pack8(VecT<__half, 8>& v, const __half2 (&w)[4]) {
+  __builtin_memcpy(&v, &w, 16);
+}
+
+template <>
+struct RotateUnit<__half, 8, false> {
+  static __device__ __forceinline__ void run(const VecT<__half, 8>& a, const VecT<__half, 8>& b,
+                                             const VecT<__half, 8>& c, const VecT<__half, 8>& s,
+                                             VecT<__half, 8>& ya, VecT<__half, 8>& yb) {
+    __half2 aw[4], bw[4], cw[4], sw[4], y0w[4], y1w[4];
+    unpack8(a, aw);
+    unpack8(b, bw);
+    unpack8(c, cw);
+    unpack8(s, sw);
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      const float2 x0 = __half22float2(aw[w]);
+      const float2 x1 = __half22float2(bw[w]);
+      const float2 cf = __half22float2(cw[w]);
+      const float2 sf = __half22float2(sw[w]);
+      float2 y0, y1;
+      rotate(x0.x, x1.x, cf.x, sf.x, y0.x, y1.x);
+      rotate(x0.y, x1.y, cf.y, sf.y, y0.y, y1.y);
+      y0w[w] = __floats2half2_rn(y0.x, y0.y);
+      y1w[w] = __floats2half2_rn(y1.x, y1.y);
+    }
+    pack8(ya, y0w);
+    pack8(yb, y1w);
+  }
+};
+
+template <>
+struct RotateUnit<__half, 8, true> {
+  // a||b holds pairs 0..7 as consecutive (even, odd) halves; pair j uses coefficient j.
+  static __device__ __forceinline__ void run(const VecT<__half, 8>& a, const VecT<__half, 8>& b,
+                                             const VecT<__half, 8>& c, const VecT<__half, 8>& s,
+                                             VecT<__half, 8>& ya, VecT<__half, 8>& yb) {
+    __half2 aw[4], bw[4], cw[4], sw[4], yaw[4], ybw[4];
+    unpack8(a, aw);
+    unpack8(b, bw);
+    unpack8(c, cw);
+    unpack8(s, sw);
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      const float2 cf = __half22float2(cw[w]);  // coefficients of pairs 2w, 2w+1
+      const float2 sf = __half22float2(sw[w]);
+      const float2 p0 = __half22float2(w < 2 ? aw[2 * w] : bw[2 * w - 4]);
+      const float2 p1 = __half22float2(w < 2 ? aw[2 * w + 1] : bw[2 * w - 3]);
+      float2 q0, q1;
+      rotate(p0.x, p0.y, cf.x, sf.x, q0.x, q0.y);
+      rotate(p1.x, p1.y, cf.y, sf.y, q1.x, q1.y);
+      const __half2 h0 = __floats2half2_rn(q0.x, q0.y);
+      const __half2 h1 = __floats2half2_rn(q1.x, q1.y);
+      if (w < 2) {
+        yaw[2 * w] = h0;
+        yaw[2 * w + 1] = h1;
+      } else {
+        ybw[2 * w - 4] = h0;
+        ybw[2 * w - 3] = h1;
+      }
+    }
+    pack8(ya, yaw);
+    pack8(yb, ybw);
+  }
+};
+
+template <class T, int V, bool INTER>
 __device__ __forceinline__ void rotate_unit(const VecT<T, V>& a, const VecT<T, V>& b,
                                             const VecT<T, V>& c, const VecT<T, V>& s,
                                             VecT<T, V>& ya, VecT<T, V>& yb) {
-  using E = Elem<T>;
-  using P = Pairs<T, V, INTER>;
-#pragma unroll
-  for (int j = 0; j < V; ++j) {
-    float x0 = E::tof(P::get(a, b, P::i0(j)));
-    float x1 = E::tof(P::get(a, b, P::i1(j)));
-    float y0, y1;
-    rotate(x0, x1, E::tof(c.v[j]), E::tof(s.v[j]), y0, y1);
-    P::set(ya, yb, P::i0(j), E::fromf(y0));
-    P::set(ya, yb, P::i1(j), E::fromf(y1));
-  }
+  RotateUnit<T, V, INTER>::run(a, b, c, s, ya, yb);
 }
 
 // Offsets (elements, within a head row) of a pair unit's two X vectors.

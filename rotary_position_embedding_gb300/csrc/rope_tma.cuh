@@ -193,31 +193,32 @@ struct Tile {
 };
 
 template <bool RANK4>
-__device__ __forceinline__ Tile tile_of(const KParams& p, const TParams& tp, int64_t t) {
+__device__ __forceinline__ Tile tile_of(const KParams& p, const TParams& tp, int64_t t64) {
   Tile tl;
+  const uint32_t t = (uint32_t)t64;  // tile counts stay below 2^31
   if (!RANK4) {
     // X viewed as (ntok, N, H); box (TS, NG, H)
-    const int64_t hg = t % tp.head_groups;
-    const int64_t tt = t / tp.head_groups;
-    tl.tok0 = tt * tp.TS;
+    const uint32_t hg = tp.head_groups == 1 ? 0u : t % (uint32_t)tp.head_groups;
+    const uint32_t tt = tp.head_groups == 1 ? t : t / (uint32_t)tp.head_groups;
+    tl.tok0 = (int64_t)tt * tp.TS;
     const int64_t left = p.ntok - tl.tok0;
     tl.ntok = (int)(left < tp.TS ? left : tp.TS);
-    tl.n0 = hg * tp.NG;
+    tl.n0 = (int64_t)hg * tp.NG;
     tl.c[0] = 0;
     tl.c[1] = (int)tl.n0;
     tl.c[2] = (int)tl.tok0;
     tl.c[3] = 0;
   } else {
     // X is (B, N, S, H); box (1, NG, TS, H)
-    const int64_t st = t % tp.s_tiles;
-    const int64_t rest = t / tp.s_tiles;
-    const int64_t hg = rest % tp.head_groups;
-    const int64_t b = rest / tp.head_groups;
-    const int64_t s0 = st * tp.TS;
-    tl.tok0 = b * p.S + s0;
+    const uint32_t st = t % (uint32_t)tp.s_tiles;
+    const uint32_t rest = t / (uint32_t)tp.s_tiles;
+    const uint32_t hg = tp.head_groups == 1 ? 0u : rest % (uint32_t)tp.head_groups;
+    const uint32_t b = tp.head_groups == 1 ? rest : rest / (uint32_t)tp.head_groups;
+    const int64_t s0 = (int64_t)st * tp.TS;
+    tl.tok0 = (int64_t)b * p.S + s0;
     const int64_t left = p.S - s0;
     tl.ntok = (int)(left < tp.TS ? left : tp.TS);
-    tl.n0 = hg * tp.NG;
+    tl.n0 = (int64_t)hg * tp.NG;
     tl.c[0] = 0;
     tl.c[1] = (int)s0;
     tl.c[2] = (int)tl.n0;
@@ -252,7 +253,7 @@ __device__ __forceinline__ TilePos<MODE> load_tile_pos(const KParams& p, const T
 // The kernel
 // ---------------------------------------------------------------------------
 template <class T, bool INTER, bool RANK4, Coef MODE>
-__global__ void __launch_bounds__(kTmaThreads, 1)
+__global__ void __launch_bounds__(kTmaThreads, 2)
     rope_tma_kernel(const KParams p, const TParams tp, const __grid_constant__ CUtensorMap tmx,
                     const __grid_constant__ CUtensorMap tmy) {
   using E = Elem<T>;
@@ -349,20 +350,34 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
   }
 
   // -------------------------------------------------------------- consumers
+  // Thread q owns pair unit k of rows r0, r0 + rpp, ... (at most RU rows of a
+  // tile; the host sizes tiles so). The rows' (token, head) coordinates are
+  // the same for every tile, so they are worked out once.
+  constexpr int RU = MODE == Coef::kMRope ? 2 : 4;
   const int q = threadIdx.x - 32;
   const int nP = p.nP;
   const int k = q % nP;
   const int r0 = q / nP;
-  const int rpp = kTmaConsumers / nP;  // rows per pass
+  const int rpp = kTmaConsumers / nP;
   const int nrows = tp.TS * tp.NG;
+  int row_ts[RU], row_ng[RU];
+  bool row_in[RU];
+#pragma unroll
+  for (int u = 0; u < RU; ++u) {
+    const int r = r0 + u * rpp;
+    row_in[u] = r0 < rpp && r < nrows;
+    row_ts[u] = RANK4 ? r % tp.TS : r / tp.NG;
+    row_ng[u] = RANK4 ? r / tp.TS : r % tp.NG;
+  }
   int oa, ob;
   unit_offsets<V, INTER>(k, p.h, oa, ob);
   const int oc = k * V;
-  // M-RoPE: the stream of each of this unit's V coefficient indices
-  uint32_t um = 0;
+  uint32_t um = 0, present = 0;  // M-RoPE: stream of each of the unit's V indices
   if (MODE == Coef::kMRope) {
     const uint32_t word = p.smap[oc >> 4];
     um = (word >> ((oc & 15) * 2)) & (uint32_t)((1ull << (2 * V)) - 1);
+#pragma unroll
+    for (int jj = 0; jj < V; ++jj) present |= 1u << ((um >> (2 * jj)) & 3);
   }
   const uint64_t pol = policy_evict_first();
   bool timed_out = false;
@@ -379,48 +394,69 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
     const uint32_t* sflags = reinterpret_cast<const uint32_t*>(st + tp.flag_off);
     const bits* scoef = reinterpret_cast<const bits*>(st + tp.coef_off);
     bits* sx = reinterpret_cast<bits*>(st);
-    if (r0 < rpp) {
-      for (int r = r0; r < nrows; r += rpp) {
-        const int ts = RANK4 ? r % tp.TS : r / tp.NG;
-        const int ng = RANK4 ? r / tp.TS : r % tp.NG;
-        if (ts >= tl.ntok || tl.n0 + ng >= p.N) continue;
-        const uint32_t fl = sflags[ts];
-        bits* row = sx + (size_t)r * p.H;
-        VT* pa = reinterpret_cast<VT*>(row + oa);
-        VT* pb = reinterpret_cast<VT*>(row + ob);
-        if (MODE != Coef::kMRope) {
-          if (!(fl & 1u)) continue;  // out-of-range position: the row stays as loaded
-          const bits* cr = scoef + (size_t)ts * 2 * p.h;
+    bool act[RU];
+    uint32_t fl[RU];
+    VT a[RU], bv[RU];
+#pragma unroll
+    for (int u = 0; u < RU; ++u) {
+      act[u] = row_in[u] && row_ts[u] < tl.ntok && tl.n0 + row_ng[u] < p.N;
+      fl[u] = act[u] ? sflags[row_ts[u]] : 0u;
+      if (MODE != Coef::kMRope) act[u] = act[u] && (fl[u] & 1u);  // out of range: row stays as loaded
+      if (act[u]) {
+        const bits* row = sx + (size_t)(r0 + u * rpp) * p.H;
+        a[u] = *reinterpret_cast<const VT*>(row + oa);
+        bv[u] = *reinterpret_cast<const VT*>(row + ob);
+      }
+    }
+    if (MODE != Coef::kMRope) {
+#pragma unroll
+      for (int u = 0; u < RU; ++u) {
+        if (act[u]) {
+          const bits* cr = scoef + (size_t)row_ts[u] * 2 * p.h;
           const VT c = *reinterpret_cast<const VT*>(cr + oc);
           const VT sn = *reinterpret_cast<const VT*>(cr + p.h + oc);
           VT ya, yb;
-          rotate_unit<T, V, INTER>(*pa, *pb, c, sn, ya, yb);
-          *pa = ya;
-          *pb = yb;
-        } else {
-          using P = Pairs<T, V, INTER>;
-          const VT a = *pa, bv = *pb;
-          VT ya = a, yb = bv;
-          const bits* cr = scoef + (size_t)ts * 3 * 2 * p.h;
-#pragma unroll
-          for (int jj = 0; jj < V; ++jj) {
-            const int stream = (um >> (2 * jj)) & 3;
-            if (!(fl & (1u << stream))) continue;  // out-of-range stream: the pair stays
-            const bits* rowc = cr + (size_t)stream * 2 * p.h;
-            float c = E::tof(rowc[oc + jj]);
-            float sv = E::tof(rowc[p.h + oc + jj]);
-            if (!p.scale_is_one) {
-              c = E::mul_round(c, p.scale);
-              sv = E::mul_round(sv, p.scale);
-            }
-            float y0, y1;
-            rotate(E::tof(P::get(a, bv, P::i0(jj))), E::tof(P::get(a, bv, P::i1(jj))), c, sv, y0, y1);
-            P::set(ya, yb, P::i0(jj), E::fromf(y0));
-            P::set(ya, yb, P::i1(jj), E::fromf(y1));
-          }
-          *pa = ya;
-          *pb = yb;
+          rotate_unit<T, V, INTER>(a[u], bv[u], c, sn, ya, yb);
+          bits* row = sx + (size_t)(r0 + u * rpp) * p.H;
+          *reinterpret_cast<VT*>(row + oa) = ya;
+          *reinterpret_cast<VT*>(row + ob) = yb;
         }
+      }
+    } else {
+      using P = Pairs<T, V, INTER>;
+#pragma unroll
+      for (int u = 0; u < RU; ++u) {
+        if (!act[u]) continue;
+        const bits* cr = scoef + (size_t)row_ts[u] * 3 * 2 * p.h;
+        VT cs[3], ss[3];
+#pragma unroll
+        for (int st3 = 0; st3 < 3; ++st3) {
+          if ((present >> st3) & (fl[u] >> st3) & 1u) {
+            cs[st3] = *reinterpret_cast<const VT*>(cr + (size_t)st3 * 2 * p.h + oc);
+            ss[st3] = *reinterpret_cast<const VT*>(cr + (size_t)st3 * 2 * p.h + p.h + oc);
+          }
+        }
+        VT ya = a[u], yb = bv[u];
+#pragma unroll
+        for (int jj = 0; jj < V; ++jj) {
+          const int stream = (um >> (2 * jj)) & 3;
+          if (!((fl[u] >> stream) & 1u)) continue;  // out-of-range stream: the pair stays
+          const bits cb = stream == 0 ? cs[0].v[jj] : (stream == 1 ? cs[1].v[jj] : cs[2].v[jj]);
+          const bits sb = stream == 0 ? ss[0].v[jj] : (stream == 1 ? ss[1].v[jj] : ss[2].v[jj]);
+          float c = E::tof(cb), sv = E::tof(sb);
+          if (!p.scale_is_one) {
+            c = E::mul_round(c, p.scale);
+            sv = E::mul_round(sv, p.scale);
+          }
+          float y0, y1;
+          rotate(E::tof(P::get(a[u], bv[u], P::i0(jj))), E::tof(P::get(a[u], bv[u], P::i1(jj))), c, sv,
+                 y0, y1);
+          P::set(ya, yb, P::i0(jj), E::fromf(y0));
+          P::set(ya, yb, P::i1(jj), E::fromf(y1));
+        }
+        bits* row = sx + (size_t)(r0 + u * rpp) * p.H;
+        *reinterpret_cast<VT*>(row + oa) = ya;
+        *reinterpret_cast<VT*>(row + ob) = yb;
       }
     }
     fence_async_smem();
