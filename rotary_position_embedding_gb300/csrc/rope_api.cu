@@ -212,16 +212,16 @@ rope_status plan(const Geom& g, int es, bool vec, const void* fn, bool smem_tabl
   const int64_t nT = (g.H - g.rd) / V;
   const int64_t U = nP + nT;
   if (U < 1) return fail(ROPE_ERR_INVALID_ARG, "empty head");
-  const int64_t Ublk = U < 1024 ? U : 1024;
+  const int64_t Ublk = U < kMaxRowThreads ? U : kMaxRowThreads;
   int64_t NG = g.N;
-  if (NG * Ublk > 1024) {
-    NG = 512 / Ublk;
+  if (NG * Ublk > kMaxRowThreads) {
+    NG = kMaxRowThreads / Ublk;
     if (NG < 1) NG = 1;
   }
   const int64_t per_tok = NG * Ublk;
   int64_t TTs = ROPE_TARGET_THREADS / per_tok;
   if (TTs < 1) TTs = 1;
-  if (TTs * per_tok > 1024) TTs = 1024 / per_tok;
+  if (TTs * per_tok > kMaxRowThreads) TTs = kMaxRowThreads / per_tok;
   if (TTs > g.ntok) TTs = g.ntok;
   const int threads = (int)(TTs * per_tok);
   const size_t smem = smem_table ? (size_t)2 * TTs * g.h * es : 0;
@@ -290,8 +290,8 @@ bool tma_eligible(const Geom& g, int es, bool vec) {
 
 struct TmaLaunch {
   TParams tp;
-  alignas(64) CUtensorMap mx;
-  alignas(64) CUtensorMap my;
+  CUtensorMap mx;  // the type carries the alignment TMA needs
+  CUtensorMap my;
   Launch L;
 };
 

@@ -13,6 +13,9 @@ enum class Coef : int {
   kMRope = 2,    // (rows, rd/2) table gathered per pair at one of three streams
 };
 
+// Most threads per CTA of the SIMT kernels (their register budget follows).
+constexpr int kMaxRowThreads = 512;
+
 // Largest half-rotary width the M-RoPE stream map (2 bits per index) holds.
 constexpr int kMaxMRopeHalf = 1024;
 

@@ -247,6 +247,91 @@ __device__ __forceinline__ void rotate_unit(const VecT<T, V>& a, const VecT<T, V
   RotateUnit<T, V, INTER>::run(a, b, c, s, ya, yb);
 }
 
+// ---------------------------------------------------------------------------
+// M-RoPE stream merge. A unit's V coefficient indices each follow one of the
+// three position streams; instead of choosing per element, the three gathered
+// coefficient vectors are merged word by word with bit masks that depend only
+// on the unit (so each thread builds them once).
+// ---------------------------------------------------------------------------
+template <int V>
+__device__ __forceinline__ void unit_mask(uint32_t sel, uint32_t (&m)[4]) {
+  constexpr int ES = 16 / V;  // bytes per element
+  constexpr uint32_t ONES = ES >= 4 ? 0xffffffffu : ((1u << (8 * ES)) - 1u);
+#pragma unroll
+  for (int w = 0; w < 4; ++w) m[w] = 0;
+#pragma unroll
+  for (int j = 0; j < V; ++j)
+    if ((sel >> j) & 1u) m[(j * ES) / 4] |= ONES << (((j * ES) % 4) * 8);
+}
+
+// m0 / m1 select the elements driven by stream 0 / stream 1 (the rest: 2).
+template <int V>
+__device__ __forceinline__ void stream_masks(uint32_t um, uint32_t (&m0)[4], uint32_t (&m1)[4]) {
+  uint32_t s0 = 0, s1 = 0;
+#pragma unroll
+  for (int j = 0; j < V; ++j) {
+    const uint32_t st = (um >> (2 * j)) & 3u;
+    s0 |= (st == 0u ? 1u : 0u) << j;
+    s1 |= (st == 1u ? 1u : 0u) << j;
+  }
+  unit_mask<V>(s0, m0);
+  unit_mask<V>(s1, m1);
+}
+
+// Element-wise m0 ? c0 : (m1 ? c1 : c2) on 16-byte vectors.
+template <class VT>
+__device__ __forceinline__ VT merge3(const VT& c0, const VT& c1, const VT& c2, const uint32_t (&m0)[4],
+                                     const uint32_t (&m1)[4]) {
+  static_assert(sizeof(VT) == 16, "16-byte units");
+  uint32_t a[4], b[4], c[4], r[4];
+  __builtin_memcpy(a, &c0, 16);
+  __builtin_memcpy(b, &c1, 16);
+  __builtin_memcpy(c, &c2, 16);
+#pragma unroll
+  for (int w = 0; w < 4; ++w) r[w] = (a[w] & m0[w]) | (((b[w] & m1[w]) | (c[w] & ~m1[w])) & ~m0[w]);
+  VT out;
+  __builtin_memcpy(&out, r, 16);
+  return out;
+}
+
+// The scaled coefficient rounded to T (M-RoPE attribute scale), element-wise.
+template <class T, int V>
+__device__ __forceinline__ void scale_round(VecT<T, V>& c, float scale) {
+  using E = Elem<T>;
+#pragma unroll
+  for (int j = 0; j < V; ++j) c.v[j] = E::fromf(E::mul_round(E::tof(c.v[j]), scale));
+}
+
+// M-RoPE unit with per-element stream choice and per-pair copy-through of
+// out-of-range streams (the general path: any V, any validity).
+template <class T, int V, bool INTER>
+__device__ __forceinline__ void mrope_unit_general(const VecT<T, V>& a, const VecT<T, V>& bv,
+                                                   const VecT<T, V> (&cs)[3], const VecT<T, V> (&ss)[3],
+                                                   uint32_t um, uint32_t valid, bool scaled, float scale,
+                                                   VecT<T, V>& ya, VecT<T, V>& yb) {
+  using E = Elem<T>;
+  using P = Pairs<T, V, INTER>;
+  using bits = typename E::bits;
+  ya = a;
+  yb = bv;
+#pragma unroll
+  for (int jj = 0; jj < V; ++jj) {
+    const int stream = (um >> (2 * jj)) & 3;
+    if (!((valid >> stream) & 1u)) continue;  // out-of-range stream: the pair stays
+    const bits cb = stream == 0 ? cs[0].v[jj] : (stream == 1 ? cs[1].v[jj] : cs[2].v[jj]);
+    const bits sb = stream == 0 ? ss[0].v[jj] : (stream == 1 ? ss[1].v[jj] : ss[2].v[jj]);
+    float c = E::tof(cb), sv = E::tof(sb);
+    if (scaled) {
+      c = E::mul_round(c, scale);
+      sv = E::mul_round(sv, scale);
+    }
+    float y0, y1;
+    rotate(E::tof(P::get(a, bv, P::i0(jj))), E::tof(P::get(a, bv, P::i1(jj))), c, sv, y0, y1);
+    P::set(ya, yb, P::i0(jj), E::fromf(y0));
+    P::set(ya, yb, P::i1(jj), E::fromf(y1));
+  }
+}
+
 // Offsets (elements, within a head row) of a pair unit's two X vectors.
 template <int V, bool INTER>
 __device__ __forceinline__ void unit_offsets(int k, int h, int& oa, int& ob) {
@@ -270,7 +355,7 @@ __device__ __forceinline__ void flag_oor(int32_t* flag) {
 // token that need the same cos/sin bytes hit in L1.
 // ---------------------------------------------------------------------------
 template <class T, int V, bool INTER, bool RANK4, Coef MODE>
-__global__ void __launch_bounds__(1024) rope_rows_kernel(const KParams p) {
+__global__ void __launch_bounds__(kMaxRowThreads) rope_rows_kernel(const KParams p) {
   using E = Elem<T>;
   using VT = VecT<T, V>;
   using bits = typename E::bits;
@@ -328,52 +413,46 @@ __global__ void __launch_bounds__(1024) rope_rows_kernel(const KParams p) {
         const VT sn = ld_shared_ro(reinterpret_cast<const VT*>(sinb + crow + oc));
         rotate_unit<T, V, INTER>(a, bv, c, sn, ya, yb);
       } else {  // M-RoPE
-        using P = Pairs<T, V, INTER>;
         const uint32_t word = p.smap[oc >> 4];
         const uint32_t um = (word >> ((oc & 15) * 2)) & (uint32_t)((1ull << (2 * V)) - 1);
         uint32_t present = 0;
 #pragma unroll
         for (int j = 0; j < V; ++j) present |= 1u << ((um >> (2 * j)) & 3);
-        int64_t ps[3];
-        bool ok[3];
+        uint32_t valid = 0;
         VT cs[3], ss[3];
 #pragma unroll
         for (int st = 0; st < 3; ++st) {
-          ok[st] = false;
+          cs[st] = VT{};
+          ss[st] = VT{};
           if (present & (1u << st)) {
-            ps[st] = __ldg(p.pos + st * p.ntok + tok);
-            ok[st] = (uint64_t)ps[st] < (uint64_t)p.cache_rows;
-            if (ok[st]) {
-              cs[st] = ld_shared_ro(reinterpret_cast<const VT*>(cosb + ps[st] * p.h + oc));
-              ss[st] = ld_shared_ro(reinterpret_cast<const VT*>(sinb + ps[st] * p.h + oc));
+            const int64_t ps = __ldg(p.pos + st * p.ntok + tok);
+            if ((uint64_t)ps < (uint64_t)p.cache_rows) {
+              valid |= 1u << st;
+              cs[st] = ld_shared_ro(reinterpret_cast<const VT*>(cosb + ps * p.h + oc));
+              ss[st] = ld_shared_ro(reinterpret_cast<const VT*>(sinb + ps * p.h + oc));
             } else if (ng == 0) {
               flag_oor(p.oor_flag);
             }
           }
         }
-#pragma unroll
-        for (int j = 0; j < V; ++j) {
-          const int st = (um >> (2 * j)) & 3;
-          const bits x0b = P::get(a, bv, P::i0(j));
-          const bits x1b = P::get(a, bv, P::i1(j));
-          const bool okj = st == 0 ? ok[0] : (st == 1 ? ok[1] : ok[2]);
-          bits y0b = x0b, y1b = x1b;
-          if (okj) {
-            const bits cb = st == 0 ? cs[0].v[j] : (st == 1 ? cs[1].v[j] : cs[2].v[j]);
-            const bits sb = st == 0 ? ss[0].v[j] : (st == 1 ? ss[1].v[j] : ss[2].v[j]);
-            float c = E::tof(cb), sv = E::tof(sb);
+        bool merged = false;
+        if constexpr (V * sizeof(bits) == 16) {
+          if ((present & ~valid) == 0) {
+            // every stream this unit uses is in range: merge, then one rotation
+            uint32_t m0[4], m1[4];
+            stream_masks<V>(um, m0, m1);
+            VT c = merge3(cs[0], cs[1], cs[2], m0, m1);
+            VT sn = merge3(ss[0], ss[1], ss[2], m0, m1);
             if (!p.scale_is_one) {
-              c = E::mul_round(c, p.scale);
-              sv = E::mul_round(sv, p.scale);
+              scale_round<T, V>(c, p.scale);
+              scale_round<T, V>(sn, p.scale);
             }
-            float y0, y1;
-            rotate(E::tof(x0b), E::tof(x1b), c, sv, y0, y1);
-            y0b = E::fromf(y0);
-            y1b = E::fromf(y1);
+            rotate_unit<T, V, INTER>(a, bv, c, sn, ya, yb);
+            merged = true;
           }
-          P::set(ya, yb, P::i0(j), y0b);
-          P::set(ya, yb, P::i1(j), y1b);
         }
+        if (!merged)
+          mrope_unit_general<T, V, INTER>(a, bv, cs, ss, um, valid, !p.scale_is_one, p.scale, ya, yb);
       }
       st_stream(reinterpret_cast<VT*>(yr + oa), ya);
       st_stream(reinterpret_cast<VT*>(yr + ob), yb);
@@ -408,7 +487,7 @@ __device__ __forceinline__ void coef_on_the_fly(int64_t pos, float inv, float sc
 // table of the tile's rd/2 coefficients (one double-precision sincos per
 // token and index, not per head), then every thread rotates its unit from it.
 template <class T, int V, bool INTER, bool RANK4>
-__global__ void __launch_bounds__(1024) rope_fused_kernel(const KParams p) {
+__global__ void __launch_bounds__(kMaxRowThreads) rope_fused_kernel(const KParams p) {
   using E = Elem<T>;
   using VT = VecT<T, V>;
   using bits = typename E::bits;

@@ -4,15 +4,17 @@
 // kernel reaches is set by how many bytes it keeps in flight. Here the bytes
 // in flight live in shared memory, not registers: a producer warp moves whole
 // tiles of X (TS tokens x NG heads x H) into a K-stage ring with TMA tensor
-// copies, and gathers each token's cos/sin rows next to the tile with 1-D bulk
-// copies; eight consumer warps rotate the tile in place; one consumer thread
+// copies, and gathers each token's cos/sin rows next to the tile with
+// coalesced loads; eight consumer warps rotate the tile in place; one consumer thread
 // writes the tile back with a TMA tensor store. Pass-through elements (the
 // tail past the rotary width, tokens or pairs whose position is out of range)
 // are never touched: the store writes back the bytes the load brought in.
 //
 // Pipeline protocol (per stage s, round r = tile index / K):
-//   full[s]   count 1: the producer's arrive.expect_tx(tile + coefficient
-//             bytes); the copies complete the transaction bytes.
+//   full[s]   count 33: producer lane 0's arrive.expect_tx(tile bytes), whose
+//             TMA copy completes the transaction bytes, and one arrive per
+//             producer lane after it has stored its share of the tile's
+//             cos/sin rows into the stage.
 //   empty[s]  count 1: consumer thread 0 arrives once the TMA store of the
 //             stage has finished reading shared memory.
 // Every wait is bounded (kWaitLimitNs of global time); a wait that runs out
@@ -142,16 +144,6 @@ __device__ __forceinline__ void tma_store_y(const CUtensorMap* map, const int* c
   }
 }
 
-// 1-D bulk copy global -> shared (16-byte aligned, size a multiple of 16).
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
-                                          uint32_t bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          dst),
-      "l"(src), "r"(bytes), "r"(bar)
-      : "memory");
-}
-
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 
 __device__ __forceinline__ void bulk_wait_read_1() {
@@ -273,7 +265,7 @@ __global__ void __launch_bounds__(kTmaThreads, 2)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < tp.K; ++s) {
-      mbar_init(full0 + 8 * s, 1);
+      mbar_init(full0 + 8 * s, 33);  // producer lane 0's arrive.expect_tx + every producer lane
       mbar_init(empty0 + 8 * s, 1);
     }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -319,24 +311,51 @@ __global__ void __launch_bounds__(kTmaThreads, 2)
         if (MODE != Coef::kCache3D && flags != (1u << SLOTS) - 1 && p.oor_flag) atomicOr(p.oor_flag, 1);
       }
       if (lane < tp.TS) reinterpret_cast<uint32_t*>(st + tp.flag_off)[lane] = flags;
-      const uint32_t lane_bytes = 2u * row_bytes * (uint32_t)__popc(flags);
-      const uint32_t coef_bytes = __reduce_add_sync(0xffffffffu, lane_bytes);
-      __syncwarp();
       if (lane == 0) {
-        mbar_arrive_expect_tx(full0 + 8 * s, tp.x_bytes + coef_bytes);
+        mbar_arrive_expect_tx(full0 + 8 * s, tp.x_bytes);
         tma_load_x<RANK4>(st_addr, &tmx, tl.c, full0 + 8 * s, pol);
       }
-      __syncwarp();
-      if (mine) {
+      // The tile's cos/sin rows (layout [token][slot][cos|sin][rd/2]) are
+      // gathered with coalesced 16-byte loads from the L2-resident tables:
+      // many small bulk copies would queue behind the tile copies in the
+      // SM's TMA unit. Piece c of the block is 16 bytes at byte offset 16*c.
+      const int ch = (int)(row_bytes / 16);
+      const int per_tok = SLOTS * 2 * ch;
+      const int pieces = tl.ntok * per_tok;
+      for (int base = 0; base < pieces; base += 32 * 8) {
+        uint4 v[8];
+        bool okv[8];
 #pragma unroll
-        for (int k = 0; k < SLOTS; ++k) {
-          if (!(flags & (1u << k))) continue;
-          const int64_t row = MODE == Coef::kCache3D ? (tl.tok0 + lane) : cur.v[k];
-          const uint32_t dst = st_addr + tp.coef_off + ((uint32_t)(lane * SLOTS + k) * 2u) * row_bytes;
-          bulk_load(dst, cosb + row * p.h, row_bytes, full0 + 8 * s);
-          bulk_load(dst + row_bytes, sinb + row * p.h, row_bytes, full0 + 8 * s);
+        for (int u = 0; u < 8; ++u) {
+          const int c = base + u * 32 + lane;
+          const int cl = c < pieces ? c : 0;
+          const int lt = cl / per_tok;
+          const int rem = cl - lt * per_tok;
+          const int k = rem / (2 * ch);
+          const int rem2 = rem - k * 2 * ch;
+          const int cs = rem2 / ch;
+          const int piece = rem2 - cs * ch;
+          const uint32_t fl = __shfl_sync(0xffffffffu, flags, lt);
+          int64_t row;
+          if (MODE == Coef::kCache3D) {
+            row = tl.tok0 + lt;
+          } else {
+            const int64_t p0 = __shfl_sync(0xffffffffu, cur.v[0], lt);
+            row = p0;
+            if (MODE == Coef::kMRope) {
+              const int64_t p1 = __shfl_sync(0xffffffffu, cur.v[SLOTS > 1 ? 1 : 0], lt);
+              const int64_t p2 = __shfl_sync(0xffffffffu, cur.v[SLOTS > 2 ? 2 : 0], lt);
+              row = k == 0 ? p0 : (k == 1 ? p1 : p2);
+            }
+          }
+          okv[u] = c < pieces && ((fl >> k) & 1u);
+          if (okv[u]) v[u] = __ldg(reinterpret_cast<const uint4*>((cs ? sinb : cosb) + row * p.h) + piece);
         }
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          if (okv[u]) reinterpret_cast<uint4*>(st + tp.coef_off)[base + u * 32 + lane] = v[u];
       }
+      mbar_arrive(full0 + 8 * s);  // each lane releases its own stores
       cur = nxt;
     }
     // Leave only after every load this warp issued has landed.
@@ -373,11 +392,13 @@ __global__ void __launch_bounds__(kTmaThreads, 2)
   unit_offsets<V, INTER>(k, p.h, oa, ob);
   const int oc = k * V;
   uint32_t um = 0, present = 0;  // M-RoPE: stream of each of the unit's V indices
+  uint32_t m0[4] = {0, 0, 0, 0}, m1[4] = {0, 0, 0, 0};
   if (MODE == Coef::kMRope) {
     const uint32_t word = p.smap[oc >> 4];
     um = (word >> ((oc & 15) * 2)) & (uint32_t)((1ull << (2 * V)) - 1);
 #pragma unroll
     for (int jj = 0; jj < V; ++jj) present |= 1u << ((um >> (2 * jj)) & 3);
+    stream_masks<V>(um, m0, m1);
   }
   const uint64_t pol = policy_evict_first();
   bool timed_out = false;
@@ -423,36 +444,32 @@ __global__ void __launch_bounds__(kTmaThreads, 2)
         }
       }
     } else {
-      using P = Pairs<T, V, INTER>;
 #pragma unroll
       for (int u = 0; u < RU; ++u) {
         if (!act[u]) continue;
         const bits* cr = scoef + (size_t)row_ts[u] * 3 * 2 * p.h;
+        const uint32_t valid = fl[u] & present;
         VT cs[3], ss[3];
 #pragma unroll
         for (int st3 = 0; st3 < 3; ++st3) {
-          if ((present >> st3) & (fl[u] >> st3) & 1u) {
+          cs[st3] = VT{};
+          ss[st3] = VT{};
+          if ((valid >> st3) & 1u) {
             cs[st3] = *reinterpret_cast<const VT*>(cr + (size_t)st3 * 2 * p.h + oc);
             ss[st3] = *reinterpret_cast<const VT*>(cr + (size_t)st3 * 2 * p.h + p.h + oc);
           }
         }
-        VT ya = a[u], yb = bv[u];
-#pragma unroll
-        for (int jj = 0; jj < V; ++jj) {
-          const int stream = (um >> (2 * jj)) & 3;
-          if (!((fl[u] >> stream) & 1u)) continue;  // out-of-range stream: the pair stays
-          const bits cb = stream == 0 ? cs[0].v[jj] : (stream == 1 ? cs[1].v[jj] : cs[2].v[jj]);
-          const bits sb = stream == 0 ? ss[0].v[jj] : (stream == 1 ? ss[1].v[jj] : ss[2].v[jj]);
-          float c = E::tof(cb), sv = E::tof(sb);
+        VT ya, yb;
+        if (valid == present) {
+          VT c = merge3(cs[0], cs[1], cs[2], m0, m1);
+          VT sn = merge3(ss[0], ss[1], ss[2], m0, m1);
           if (!p.scale_is_one) {
-            c = E::mul_round(c, p.scale);
-            sv = E::mul_round(sv, p.scale);
+            scale_round<T, V>(c, p.scale);
+            scale_round<T, V>(sn, p.scale);
           }
-          float y0, y1;
-          rotate(E::tof(P::get(a[u], bv[u], P::i0(jj))), E::tof(P::get(a[u], bv[u], P::i1(jj))), c, sv,
-                 y0, y1);
-          P::set(ya, yb, P::i0(jj), E::fromf(y0));
-          P::set(ya, yb, P::i1(jj), E::fromf(y1));
+          rotate_unit<T, V, INTER>(a[u], bv[u], c, sn, ya, yb);
+        } else {
+          mrope_unit_general<T, V, INTER>(a[u], bv[u], cs, ss, um, valid, !p.scale_is_one, p.scale, ya, yb);
         }
         bits* row = sx + (size_t)(r0 + u * rpp) * p.H;
         *reinterpret_cast<VT*>(row + oa) = ya;
