@@ -25,7 +25,7 @@
 #include <string>
 #include <tuple>
 
-#include "../../include/rope.h"
+#include "rope.h"
 #include "rope_internal.h"
 #include "rope_tma.cuh"
 
@@ -334,29 +334,30 @@ rope_status plan_tma(const Geom& g, int es, int rank, int slots, const void* fn,
     if (TS < 1) TS = 1;
     if (TS > 32) TS = 32;
     if (TS > g.ntok) TS = g.ntok;
-    tp.head_groups = (int32_t)((g.N + NG - 1) / NG);
-    tp.ntiles = ((g.ntok + TS - 1) / TS) * tp.head_groups;
   } else {
     TS = g.S < 32 ? g.S : 32;
     NG = ROPE_TMA_TILE_BYTES / (TS * g.H * es);
     if (NG < 1) NG = 1;
     if (NG > g.N) NG = g.N;
     if (NG > 256) NG = 256;
-    tp.head_groups = (int32_t)((g.N + NG - 1) / NG);
-    tp.s_tiles = (int32_t)((g.S + TS - 1) / TS);
-    tp.ntiles = g.B * tp.head_groups * (int64_t)tp.s_tiles;
   }
-  // every consumer thread owns one pair unit of at most RU rows of a tile
+  // Consumer columns (token, pair unit) must fit the consumer threads, each
+  // thread covers at most kMaxHeads heads of its column, and the producer's
+  // 32 lanes gather at most kMaxGather 16-byte cos/sin pieces each.
   const int64_t nPu = g.h / V;
-  const int64_t ru = slots == 3 ? 2 : 4;
-  const int64_t max_rows = ru * (kTmaConsumers / nPu);
-  while (TS * NG > max_rows && TS > 1) --TS;
-  while (TS * NG > max_rows && NG > 1) --NG;
+  const int64_t pieces_per_tok = (int64_t)slots * 2 * (g.h * es / 16);
+  auto fits = [&](int64_t ts, int64_t ng) {
+    if (ts * nPu > kTmaConsumers) return false;
+    if (ts * pieces_per_tok > 32 * kMaxGather) return false;
+    return ng <= kMaxHeads * (kTmaConsumers / (ts * nPu));
+  };
+  while (!fits(TS, NG) && TS > 1) --TS;
+  while (!fits(TS, NG) && NG > 1) --NG;
+  if (!fits(TS, NG)) return ROPE_ERR_UNSUPPORTED;
+  tp.head_groups = (int32_t)((g.N + NG - 1) / NG);
   if (rank == 3) {
-    tp.head_groups = (int32_t)((g.N + NG - 1) / NG);
     tp.ntiles = ((g.ntok + TS - 1) / TS) * tp.head_groups;
   } else {
-    tp.head_groups = (int32_t)((g.N + NG - 1) / NG);
     tp.s_tiles = (int32_t)((g.S + TS - 1) / TS);
     tp.ntiles = g.B * tp.head_groups * (int64_t)tp.s_tiles;
   }
@@ -367,7 +368,8 @@ rope_status plan_tma(const Geom& g, int es, int rank, int slots, const void* fn,
   tp.x_bytes = (uint32_t)(TS * NG * g.H * es);
   tp.coef_off = tp.x_bytes;
   tp.flag_off = tp.coef_off + (uint32_t)(TS * slots * 2 * g.h * es);
-  tp.stage_bytes = (tp.flag_off + (uint32_t)TS * 4 + 1023) / 1024 * 1024;
+  tp.pos_off = (tp.flag_off + (uint32_t)TS * 4 + 15) / 16 * 16;
+  tp.stage_bytes = (tp.pos_off + (uint32_t)TS * slots * 8 + 1023) / 1024 * 1024;
   tp.bar_bytes = 1024;
   int64_t K = (ROPE_TMA_SMEM_BUDGET - tp.bar_bytes) / tp.stage_bytes;
   if (K > ROPE_TMA_MAX_STAGES) K = ROPE_TMA_MAX_STAGES;

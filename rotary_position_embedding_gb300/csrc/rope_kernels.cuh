@@ -303,9 +303,11 @@ __device__ __forceinline__ void scale_round(VecT<T, V>& c, float scale) {
 }
 
 // M-RoPE unit with per-element stream choice and per-pair copy-through of
-// out-of-range streams (the general path: any V, any validity).
+// out-of-range streams (the general path: any V, any validity). Kept out of
+// line: it runs only for units that touch an out-of-range position, and
+// inlining it would cost the common path registers.
 template <class T, int V, bool INTER>
-__device__ __forceinline__ void mrope_unit_general(const VecT<T, V>& a, const VecT<T, V>& bv,
+__device__ __noinline__ void mrope_unit_general(const VecT<T, V>& a, const VecT<T, V>& bv,
                                                    const VecT<T, V> (&cs)[3], const VecT<T, V> (&ss)[3],
                                                    uint32_t um, uint32_t valid, bool scaled, float scale,
                                                    VecT<T, V>& ya, VecT<T, V>& yb) {

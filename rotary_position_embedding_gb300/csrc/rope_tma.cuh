@@ -4,17 +4,17 @@
 // kernel reaches is set by how many bytes it keeps in flight. Here the bytes
 // in flight live in shared memory, not registers: a producer warp moves whole
 // tiles of X (TS tokens x NG heads x H) into a K-stage ring with TMA tensor
-// copies, and gathers each token's cos/sin rows next to the tile with
-// coalesced loads; eight consumer warps rotate the tile in place; one consumer thread
+// copies, and gathers each token's cos/sin rows next to the tile with 16-byte
+// asynchronous copies; eight consumer warps rotate the tile in place; one consumer thread
 // writes the tile back with a TMA tensor store. Pass-through elements (the
 // tail past the rotary width, tokens or pairs whose position is out of range)
 // are never touched: the store writes back the bytes the load brought in.
 //
 // Pipeline protocol (per stage s, round r = tile index / K):
 //   full[s]   count 33: producer lane 0's arrive.expect_tx(tile bytes), whose
-//             TMA copy completes the transaction bytes, and one arrive per
-//             producer lane after it has stored its share of the tile's
-//             cos/sin rows into the stage.
+//             TMA copy completes the transaction bytes, and one asynchronous
+//             arrive per producer lane, triggered when that lane's cp.async
+//             copies of the tile's cos/sin rows have landed.
 //   empty[s]  count 1: consumer thread 0 arrives once the TMA store of the
 //             stage has finished reading shared memory.
 // Every wait is bounded (kWaitLimitNs of global time); a wait that runs out
@@ -38,6 +38,8 @@ constexpr int kTmaConsumerWarps = 8;
 constexpr int kTmaConsumers = kTmaConsumerWarps * 32;
 constexpr int kTmaThreads = kTmaConsumers + 32;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+constexpr int kMaxGather = 8;  // 16-byte cos/sin pieces per producer lane per tile
+constexpr int kMaxHeads = 4;   // heads one consumer thread rotates per tile column
 
 struct TParams {
   int32_t TS, NG, K;    // tokens per tile, heads per tile, pipeline stages
@@ -48,6 +50,7 @@ struct TParams {
   uint32_t x_bytes;     // bytes of one X box
   uint32_t coef_off;    // stage offsets: coefficient rows, per-token flags
   uint32_t flag_off;
+  uint32_t pos_off;     // the tile's positions (producer scratch inside the stage)
   uint32_t stage_bytes;
   uint32_t bar_bytes;   // barrier block in front of stage 0
 };
@@ -72,14 +75,19 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
+// A waiting thread is suspended (it issues nothing) until the phase completes
+// or kSuspendHintNs elapse, so waiting warps leave the issue slots to the
+// warps that have work.
+constexpr uint32_t kSuspendHintNs = 1000000;
+
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
       "selp.u32 %0, 1, 0, p;\n\t}"
       : "=r"(ok)
-      : "r"(bar), "r"(parity)
+      : "r"(bar), "r"(parity), "r"(kSuspendHintNs)
       : "memory");
   return ok != 0;
 }
@@ -144,6 +152,17 @@ __device__ __forceinline__ void tma_store_y(const CUtensorMap* map, const int* c
   }
 }
 
+// 16-byte asynchronous copy global -> shared (LSU path, not the TMA unit).
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+
+// Arrive on `bar` once this thread's earlier cp.async copies have landed
+// (counts as one of the barrier's expected arrivals).
+__device__ __forceinline__ void cp_async_arrive(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 
 __device__ __forceinline__ void bulk_wait_read_1() {
@@ -154,10 +173,6 @@ __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wa
 
 __device__ __forceinline__ void fence_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
-__device__ __forceinline__ void consumer_sync() {
-  asm volatile("bar.sync 1, %0;" ::"n"(kTmaConsumers) : "memory");
 }
 
 // Barrier among the consumer warps that also ORs a predicate across them.
@@ -279,6 +294,29 @@ __global__ void __launch_bounds__(kTmaThreads, 2)
     const bits* cosb = static_cast<const bits*>(p.cos);
     const bits* sinb = static_cast<const bits*>(p.sin);
     bool timed_out = false;
+    // Gather roles: piece c of a full tile's coefficient block (16 bytes at
+    // byte 16*c, layout [token][slot][cos|sin][rd/2]) goes to lane c % 32;
+    // each lane's pieces are the same for every tile, so they are decoded once.
+    const int ch = (int)(row_bytes / 16);
+    const int per_tok = SLOTS * 2 * ch;
+    const int pieces = tp.TS * per_tok;
+    const int n_gather = (pieces - lane + 31) / 32;
+    int g_lt[kMaxGather], g_k[kMaxGather], g_piece[kMaxGather];
+    bool g_sin[kMaxGather];
+    uint32_t g_dst[kMaxGather];
+#pragma unroll
+    for (int g = 0; g < kMaxGather; ++g) {
+      const int c = lane + 32 * g;
+      const int lt = c / per_tok;
+      const int rem = c - lt * per_tok;
+      const int k = rem / (2 * ch);
+      const int rem2 = rem - k * 2 * ch;
+      g_lt[g] = lt;
+      g_k[g] = k;
+      g_sin[g] = rem2 >= ch;
+      g_piece[g] = rem2 % ch;
+      g_dst[g] = 16u * (uint32_t)c;
+    }
     int64_t j = 0;
     int64_t t = blockIdx.x;
     TilePos<MODE> cur{};
@@ -310,52 +348,43 @@ __global__ void __launch_bounds__(kTmaThreads, 2)
         }
         if (MODE != Coef::kCache3D && flags != (1u << SLOTS) - 1 && p.oor_flag) atomicOr(p.oor_flag, 1);
       }
-      if (lane < tp.TS) reinterpret_cast<uint32_t*>(st + tp.flag_off)[lane] = flags;
+      if (lane < tp.TS) {
+        reinterpret_cast<uint32_t*>(st + tp.flag_off)[lane] = flags;
+        if (MODE != Coef::kCache3D) {
+#pragma unroll
+          for (int k = 0; k < SLOTS; ++k) reinterpret_cast<int64_t*>(st + tp.pos_off)[lane * SLOTS + k] = cur.v[k];
+        }
+      }
+      __syncwarp();  // the flags and positions precede lane 0's (releasing) arrive and the gather
       if (lane == 0) {
         mbar_arrive_expect_tx(full0 + 8 * s, tp.x_bytes);
         tma_load_x<RANK4>(st_addr, &tmx, tl.c, full0 + 8 * s, pol);
       }
       // The tile's cos/sin rows (layout [token][slot][cos|sin][rd/2]) are
-      // gathered with coalesced 16-byte loads from the L2-resident tables:
-      // many small bulk copies would queue behind the tile copies in the
-      // SM's TMA unit. Piece c of the block is 16 bytes at byte offset 16*c.
-      const int ch = (int)(row_bytes / 16);
-      const int per_tok = SLOTS * 2 * ch;
-      const int pieces = tl.ntok * per_tok;
-      for (int base = 0; base < pieces; base += 32 * 8) {
-        uint4 v[8];
-        bool okv[8];
+      // gathered 16 bytes per copy from the L2-resident tables with
+      // asynchronous copies that arrive on full[s] when they land, so the
+      // producer never waits on the gather. Piece c sits at byte 16*c.
+      const uint32_t coef_addr = st_addr + tp.coef_off;
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const int c = base + u * 32 + lane;
-          const int cl = c < pieces ? c : 0;
-          const int lt = cl / per_tok;
-          const int rem = cl - lt * per_tok;
-          const int k = rem / (2 * ch);
-          const int rem2 = rem - k * 2 * ch;
-          const int cs = rem2 / ch;
-          const int piece = rem2 - cs * ch;
-          const uint32_t fl = __shfl_sync(0xffffffffu, flags, lt);
-          int64_t row;
-          if (MODE == Coef::kCache3D) {
-            row = tl.tok0 + lt;
-          } else {
-            const int64_t p0 = __shfl_sync(0xffffffffu, cur.v[0], lt);
-            row = p0;
-            if (MODE == Coef::kMRope) {
-              const int64_t p1 = __shfl_sync(0xffffffffu, cur.v[SLOTS > 1 ? 1 : 0], lt);
-              const int64_t p2 = __shfl_sync(0xffffffffu, cur.v[SLOTS > 2 ? 2 : 0], lt);
-              row = k == 0 ? p0 : (k == 1 ? p1 : p2);
-            }
-          }
-          okv[u] = c < pieces && ((fl >> k) & 1u);
-          if (okv[u]) v[u] = __ldg(reinterpret_cast<const uint4*>((cs ? sinb : cosb) + row * p.h) + piece);
+      for (int g = 0; g < kMaxGather; ++g) {
+        if (g >= n_gather) break;
+        const int lt = g_lt[g];
+        if (lt >= tl.ntok) continue;
+        int64_t row;
+        uint32_t fl;
+        if (MODE == Coef::kCache3D) {
+          row = tl.tok0 + lt;
+          fl = 1u;
+        } else {
+          // token lt's position(s) and flags were published by lane lt above
+          fl = reinterpret_cast<const uint32_t*>(st + tp.flag_off)[lt];
+          row = reinterpret_cast<const int64_t*>(st + tp.pos_off)[lt * SLOTS + g_k[g]];
         }
-#pragma unroll
-        for (int u = 0; u < 8; ++u)
-          if (okv[u]) reinterpret_cast<uint4*>(st + tp.coef_off)[base + u * 32 + lane] = v[u];
+        if ((fl >> g_k[g]) & 1u)
+          cp_async16(coef_addr + g_dst[g], reinterpret_cast<const uint4*>(
+                                               (g_sin[g] ? sinb : cosb) + row * p.h) + g_piece[g]);
       }
-      mbar_arrive(full0 + 8 * s);  // each lane releases its own stores
+      cp_async_arrive(full0 + 8 * s);
       cur = nxt;
     }
     // Leave only after every load this warp issued has landed.
@@ -369,25 +398,18 @@ __global__ void __launch_bounds__(kTmaThreads, 2)
   }
 
   // -------------------------------------------------------------- consumers
-  // Thread q owns pair unit k of rows r0, r0 + rpp, ... (at most RU rows of a
-  // tile; the host sizes tiles so). The rows' (token, head) coordinates are
-  // the same for every tile, so they are worked out once.
-  constexpr int RU = MODE == Coef::kMRope ? 2 : 4;
+  // Thread q owns column (token ts, pair unit k) of the tile for up to
+  // kMaxHeads heads ng = hq, hq + tpc, ... The column's cos/sin (for M-RoPE:
+  // the three streams merged) are read once and reused for every head.
   const int q = threadIdx.x - 32;
   const int nP = p.nP;
-  const int k = q % nP;
-  const int r0 = q / nP;
-  const int rpp = kTmaConsumers / nP;
-  const int nrows = tp.TS * tp.NG;
-  int row_ts[RU], row_ng[RU];
-  bool row_in[RU];
-#pragma unroll
-  for (int u = 0; u < RU; ++u) {
-    const int r = r0 + u * rpp;
-    row_in[u] = r0 < rpp && r < nrows;
-    row_ts[u] = RANK4 ? r % tp.TS : r / tp.NG;
-    row_ng[u] = RANK4 ? r / tp.TS : r % tp.NG;
-  }
+  const int cols = tp.TS * nP;
+  const int tpc = kTmaConsumers / cols;  // threads per column (the host keeps cols <= consumers)
+  const int col = q % cols;
+  const int hq = q / cols;
+  const bool has_col = hq < tpc;
+  const int ts = col / nP;
+  const int k = col - ts * nP;
   int oa, ob;
   unit_offsets<V, INTER>(k, p.h, oa, ob);
   const int oc = k * V;
@@ -406,49 +428,34 @@ __global__ void __launch_bounds__(kTmaThreads, 2)
   for (int64_t t = blockIdx.x; t < tp.ntiles; t += gridDim.x, ++j) {
     const int s = (int)(j % tp.K);
     const bool ok = mbar_wait(full0 + 8 * s, (uint32_t)((j / tp.K) & 1));
-    if (consumer_any(!ok)) {
-      timed_out = true;
-      break;
-    }
     const Tile tl = tile_of<RANK4>(p, tp, t);
     unsigned char* st = stage0 + (size_t)s * tp.stage_bytes;
-    const uint32_t* sflags = reinterpret_cast<const uint32_t*>(st + tp.flag_off);
-    const bits* scoef = reinterpret_cast<const bits*>(st + tp.coef_off);
-    bits* sx = reinterpret_cast<bits*>(st);
-    bool act[RU];
-    uint32_t fl[RU];
-    VT a[RU], bv[RU];
+    if (ok && has_col && ts < tl.ntok) {
+      const uint32_t fl = reinterpret_cast<const uint32_t*>(st + tp.flag_off)[ts];
+      const bits* scoef = reinterpret_cast<const bits*>(st + tp.coef_off);
+      bits* sx = reinterpret_cast<bits*>(st);
+      // the column's rows (element offsets into the stage)
+      bool act[kMaxHeads];
+      uint32_t rowo[kMaxHeads];
 #pragma unroll
-    for (int u = 0; u < RU; ++u) {
-      act[u] = row_in[u] && row_ts[u] < tl.ntok && tl.n0 + row_ng[u] < p.N;
-      fl[u] = act[u] ? sflags[row_ts[u]] : 0u;
-      if (MODE != Coef::kMRope) act[u] = act[u] && (fl[u] & 1u);  // out of range: row stays as loaded
-      if (act[u]) {
-        const bits* row = sx + (size_t)(r0 + u * rpp) * p.H;
-        a[u] = *reinterpret_cast<const VT*>(row + oa);
-        bv[u] = *reinterpret_cast<const VT*>(row + ob);
+      for (int u = 0; u < kMaxHeads; ++u) {
+        const int ng = hq + u * tpc;
+        act[u] = ng < tp.NG && tl.n0 + ng < p.N;
+        const int r = RANK4 ? ng * tp.TS + ts : ts * tp.NG + ng;
+        rowo[u] = (uint32_t)r * (uint32_t)p.H;
       }
-    }
-    if (MODE != Coef::kMRope) {
-#pragma unroll
-      for (int u = 0; u < RU; ++u) {
-        if (act[u]) {
-          const bits* cr = scoef + (size_t)row_ts[u] * 2 * p.h;
-          const VT c = *reinterpret_cast<const VT*>(cr + oc);
-          const VT sn = *reinterpret_cast<const VT*>(cr + p.h + oc);
-          VT ya, yb;
-          rotate_unit<T, V, INTER>(a[u], bv[u], c, sn, ya, yb);
-          bits* row = sx + (size_t)(r0 + u * rpp) * p.H;
-          *reinterpret_cast<VT*>(row + oa) = ya;
-          *reinterpret_cast<VT*>(row + ob) = yb;
+      bool fast = true;
+      VT c, sn;
+      if (MODE != Coef::kMRope) {
+        fast = fl & 1u;  // otherwise the position is out of range: the rows stay as loaded
+        if (fast) {
+          const bits* cr = scoef + (size_t)ts * 2 * p.h;
+          c = *reinterpret_cast<const VT*>(cr + oc);
+          sn = *reinterpret_cast<const VT*>(cr + p.h + oc);
         }
-      }
-    } else {
-#pragma unroll
-      for (int u = 0; u < RU; ++u) {
-        if (!act[u]) continue;
-        const bits* cr = scoef + (size_t)row_ts[u] * 3 * 2 * p.h;
-        const uint32_t valid = fl[u] & present;
+      } else {
+        const bits* cr = scoef + (size_t)ts * 3 * 2 * p.h;
+        const uint32_t valid = fl & present;
         VT cs[3], ss[3];
 #pragma unroll
         for (int st3 = 0; st3 < 3; ++st3) {
@@ -459,25 +466,58 @@ __global__ void __launch_bounds__(kTmaThreads, 2)
             ss[st3] = *reinterpret_cast<const VT*>(cr + (size_t)st3 * 2 * p.h + p.h + oc);
           }
         }
-        VT ya, yb;
         if (valid == present) {
-          VT c = merge3(cs[0], cs[1], cs[2], m0, m1);
-          VT sn = merge3(ss[0], ss[1], ss[2], m0, m1);
+          c = merge3(cs[0], cs[1], cs[2], m0, m1);
+          sn = merge3(ss[0], ss[1], ss[2], m0, m1);
           if (!p.scale_is_one) {
             scale_round<T, V>(c, p.scale);
             scale_round<T, V>(sn, p.scale);
           }
-          rotate_unit<T, V, INTER>(a[u], bv[u], c, sn, ya, yb);
         } else {
-          mrope_unit_general<T, V, INTER>(a[u], bv[u], cs, ss, um, valid, !p.scale_is_one, p.scale, ya, yb);
+          // a stream this unit uses is out of range: element-wise, one head at a time
+          fast = false;
+#pragma unroll 1
+          for (int u = 0; u < kMaxHeads; ++u) {
+            if (!act[u]) continue;
+            bits* row = sx + rowo[u];
+            const VT a = *reinterpret_cast<const VT*>(row + oa);
+            const VT bv = *reinterpret_cast<const VT*>(row + ob);
+            VT ya, yb;
+            mrope_unit_general<T, V, INTER>(a, bv, cs, ss, um, valid, !p.scale_is_one, p.scale, ya, yb);
+            *reinterpret_cast<VT*>(row + oa) = ya;
+            *reinterpret_cast<VT*>(row + ob) = yb;
+          }
         }
-        bits* row = sx + (size_t)(r0 + u * rpp) * p.H;
-        *reinterpret_cast<VT*>(row + oa) = ya;
-        *reinterpret_cast<VT*>(row + ob) = yb;
+      }
+      if (fast) {
+        // X loads of HOIST heads are issued together, then rotated and stored
+        constexpr int HOIST = MODE == Coef::kMRope ? 2 : kMaxHeads;
+#pragma unroll
+        for (int u0 = 0; u0 < kMaxHeads; u0 += HOIST) {
+          VT a[HOIST], bv[HOIST];
+#pragma unroll
+          for (int u = 0; u < HOIST; ++u) {
+            if (act[u0 + u]) {
+              a[u] = *reinterpret_cast<const VT*>(sx + rowo[u0 + u] + oa);
+              bv[u] = *reinterpret_cast<const VT*>(sx + rowo[u0 + u] + ob);
+            }
+          }
+#pragma unroll
+          for (int u = 0; u < HOIST; ++u) {
+            if (!act[u0 + u]) continue;
+            VT ya, yb;
+            rotate_unit<T, V, INTER>(a[u], bv[u], c, sn, ya, yb);
+            *reinterpret_cast<VT*>(sx + rowo[u0 + u] + oa) = ya;
+            *reinterpret_cast<VT*>(sx + rowo[u0 + u] + ob) = yb;
+          }
+        }
       }
     }
     fence_async_smem();
-    consumer_sync();
+    if (consumer_any(!ok)) {  // also the barrier before the store
+      timed_out = true;
+      break;
+    }
     if (q == 0) {
       tma_store_y<RANK4>(&tmy, tl.c, smem_addr(st), pol);
       bulk_commit();
