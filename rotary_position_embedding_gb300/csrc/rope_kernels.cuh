@@ -294,6 +294,40 @@ __device__ __forceinline__ VT merge3(const VT& c0, const VT& c1, const VT& c2, c
   return out;
 }
 
+// Masks of the output elements of a unit whose pair follows one of the
+// streams in `streams` (bit k = stream k). Half split: pair j is element j of
+// a and of b; interleaved: pair j is elements 2j, 2j+1 of the run a||b.
+template <int V, bool INTER>
+__device__ __forceinline__ void pair_masks(uint32_t um, uint32_t streams, uint32_t (&ma)[4],
+                                           uint32_t (&mb)[4]) {
+  uint32_t sa = 0, sb = 0;
+#pragma unroll
+  for (int j = 0; j < V; ++j) {
+    const uint32_t on = (streams >> ((um >> (2 * j)) & 3u)) & 1u;
+    if (!INTER) {
+      sa |= on << j;
+      sb |= on << j;
+    } else if (2 * j < V) {
+      sa |= (on * 3u) << (2 * j);
+    } else {
+      sb |= (on * 3u) << (2 * j - V);
+    }
+  }
+  unit_mask<V>(sa, ma);
+  unit_mask<V>(sb, mb);
+}
+
+// y = m ? y : x, word-wise (restores the pass-through elements).
+template <class VT>
+__device__ __forceinline__ void blend(VT& y, const VT& x, const uint32_t (&m)[4]) {
+  uint32_t a[4], b[4];
+  __builtin_memcpy(a, &y, 16);
+  __builtin_memcpy(b, &x, 16);
+#pragma unroll
+  for (int w = 0; w < 4; ++w) a[w] = (a[w] & m[w]) | (b[w] & ~m[w]);
+  __builtin_memcpy(&y, a, 16);
+}
+
 // The scaled coefficient rounded to T (M-RoPE attribute scale), element-wise.
 template <class T, int V>
 __device__ __forceinline__ void scale_round(VecT<T, V>& c, float scale) {
@@ -437,24 +471,26 @@ __global__ void __launch_bounds__(kMaxRowThreads) rope_rows_kernel(const KParams
             }
           }
         }
-        bool merged = false;
         if constexpr (V * sizeof(bits) == 16) {
-          if ((present & ~valid) == 0) {
-            // every stream this unit uses is in range: merge, then one rotation
-            uint32_t m0[4], m1[4];
-            stream_masks<V>(um, m0, m1);
-            VT c = merge3(cs[0], cs[1], cs[2], m0, m1);
-            VT sn = merge3(ss[0], ss[1], ss[2], m0, m1);
-            if (!p.scale_is_one) {
-              scale_round<T, V>(c, p.scale);
-              scale_round<T, V>(sn, p.scale);
-            }
-            rotate_unit<T, V, INTER>(a, bv, c, sn, ya, yb);
-            merged = true;
+          // merge the streams, rotate once, restore pairs of out-of-range streams
+          uint32_t m0[4], m1[4];
+          stream_masks<V>(um, m0, m1);
+          VT c = merge3(cs[0], cs[1], cs[2], m0, m1);
+          VT sn = merge3(ss[0], ss[1], ss[2], m0, m1);
+          if (!p.scale_is_one) {
+            scale_round<T, V>(c, p.scale);
+            scale_round<T, V>(sn, p.scale);
           }
-        }
-        if (!merged)
+          rotate_unit<T, V, INTER>(a, bv, c, sn, ya, yb);
+          if (present & ~valid) {
+            uint32_t ma[4], mb[4];
+            pair_masks<V, INTER>(um, valid, ma, mb);
+            blend(ya, a, ma);
+            blend(yb, bv, mb);
+          }
+        } else {
           mrope_unit_general<T, V, INTER>(a, bv, cs, ss, um, valid, !p.scale_is_one, p.scale, ya, yb);
+        }
       }
       st_stream(reinterpret_cast<VT*>(yr + oa), ya);
       st_stream(reinterpret_cast<VT*>(yr + ob), yb);

@@ -445,6 +445,8 @@ __global__ void __launch_bounds__(kTmaThreads, 2)
         rowo[u] = (uint32_t)r * (uint32_t)p.H;
       }
       bool fast = true;
+      bool blend_on = false;
+      uint32_t ma[4], mb[4];
       VT c, sn;
       if (MODE != Coef::kMRope) {
         fast = fl & 1u;  // otherwise the position is out of range: the rows stay as loaded
@@ -466,28 +468,15 @@ __global__ void __launch_bounds__(kTmaThreads, 2)
             ss[st3] = *reinterpret_cast<const VT*>(cr + (size_t)st3 * 2 * p.h + p.h + oc);
           }
         }
-        if (valid == present) {
-          c = merge3(cs[0], cs[1], cs[2], m0, m1);
-          sn = merge3(ss[0], ss[1], ss[2], m0, m1);
-          if (!p.scale_is_one) {
-            scale_round<T, V>(c, p.scale);
-            scale_round<T, V>(sn, p.scale);
-          }
-        } else {
-          // a stream this unit uses is out of range: element-wise, one head at a time
-          fast = false;
-#pragma unroll 1
-          for (int u = 0; u < kMaxHeads; ++u) {
-            if (!act[u]) continue;
-            bits* row = sx + rowo[u];
-            const VT a = *reinterpret_cast<const VT*>(row + oa);
-            const VT bv = *reinterpret_cast<const VT*>(row + ob);
-            VT ya, yb;
-            mrope_unit_general<T, V, INTER>(a, bv, cs, ss, um, valid, !p.scale_is_one, p.scale, ya, yb);
-            *reinterpret_cast<VT*>(row + oa) = ya;
-            *reinterpret_cast<VT*>(row + ob) = yb;
-          }
+        c = merge3(cs[0], cs[1], cs[2], m0, m1);
+        sn = merge3(ss[0], ss[1], ss[2], m0, m1);
+        if (!p.scale_is_one) {
+          scale_round<T, V>(c, p.scale);
+          scale_round<T, V>(sn, p.scale);
         }
+        // pairs whose stream is out of range are put back from X after the rotation
+        blend_on = valid != present;
+        if (blend_on) pair_masks<V, INTER>(um, valid, ma, mb);
       }
       if (fast) {
         // X loads of HOIST heads are issued together, then rotated and stored
@@ -507,6 +496,10 @@ __global__ void __launch_bounds__(kTmaThreads, 2)
             if (!act[u0 + u]) continue;
             VT ya, yb;
             rotate_unit<T, V, INTER>(a[u], bv[u], c, sn, ya, yb);
+            if (MODE == Coef::kMRope && blend_on) {
+              blend(ya, a[u], ma);
+              blend(yb, bv[u], mb);
+            }
             *reinterpret_cast<VT*>(sx + rowo[u0 + u] + oa) = ya;
             *reinterpret_cast<VT*>(sx + rowo[u0 + u] + ob) = yb;
           }
