@@ -400,16 +400,36 @@ rope_status plan_tma(const Geom& g, int es, int rank, int slots, const void* fn,
   return ROPE_OK;
 }
 
+// Every kernel is launched with programmatic stream serialization: it may be
+// scheduled while the previous kernel in the stream finishes, sets up its
+// shared memory and barriers, and waits (griddepcontrol.wait) before its
+// first read of global memory, so the stream's ordering is unchanged.
+cudaError_t launch_pdl(const void* fn, dim3 grid, dim3 block, size_t smem, rope_stream_t stream,
+                       void** args) {
+  cudaLaunchConfig_t cfg;
+  memset(&cfg, 0, sizeof(cfg));
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = (cudaStream_t)stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelExC(&cfg, fn, args);
+}
+
 rope_status launch_tma(const void* fn, TmaLaunch* T, KParams* kp, rope_stream_t stream) {
   void* args[] = {kp, &T->tp, &T->mx, &T->my};
-  cudaError_t e = cudaLaunchKernel(fn, T->L.grid, T->L.block, args, T->L.smem, (cudaStream_t)stream);
+  cudaError_t e = launch_pdl(fn, T->L.grid, T->L.block, T->L.smem, stream, args);
   if (e != cudaSuccess) return cuda_fail(e, "TMA kernel launch");
   return ROPE_OK;
 }
 
 rope_status launch(const void* fn, const Launch& L, KParams* kp, rope_stream_t stream) {
   void* args[] = {kp};
-  cudaError_t e = cudaLaunchKernel(fn, L.grid, L.block, args, L.smem, (cudaStream_t)stream);
+  cudaError_t e = launch_pdl(fn, L.grid, L.block, L.smem, stream, args);
   if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
   return ROPE_OK;
 }
@@ -701,7 +721,7 @@ rope_status rope_cache_build(rope_dtype dtype, const float* inv_freq, int32_t ha
   int64_t blocks = (total + 255) / 256;
   if (blocks > (int64_t)sms * per_sm) blocks = (int64_t)sms * per_sm;
   void* args[] = {&inv_freq, &half, &rows, &attention_scaling, &cos_out, &sin_out};
-  cudaError_t e = cudaLaunchKernel(fn, dim3((unsigned)blocks), dim3(256), args, 0, (cudaStream_t)stream);
+  cudaError_t e = launch_pdl(fn, dim3((unsigned)blocks), dim3(256), 0, stream, args);
   if (e != cudaSuccess) return cuda_fail(e, "rope_cache_build launch");
   return ROPE_OK;
 }

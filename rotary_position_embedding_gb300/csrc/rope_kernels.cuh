@@ -380,6 +380,14 @@ __device__ __forceinline__ void unit_offsets(int k, int h, int& oa, int& ob) {
   }
 }
 
+// Programmatic dependent launch: wait until the preceding kernel in the
+// stream has completed and its writes are visible (a no-op when the kernel was
+// not launched as a dependent), and let the next kernel be scheduled early.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ void flag_oor(int32_t* flag) {
   if (flag) atomicOr(flag, 1);
 }
@@ -402,6 +410,8 @@ __global__ void __launch_bounds__(kMaxRowThreads) rope_rows_kernel(const KParams
   const int ng = r / p.Ublk;
   const int k0 = r - ng * p.Ublk;
   const int64_t n = (int64_t)blockIdx.y * p.NG + ng;
+  pdl_launch_dependents();
+  pdl_wait();
   if (slot >= p.TTs || n >= p.N) return;  // no barrier below
 
   const bits* __restrict__ x = static_cast<const bits*>(p.x);
@@ -545,6 +555,8 @@ __global__ void __launch_bounds__(kMaxRowThreads) rope_fused_kernel(const KParam
   const bits* __restrict__ x = static_cast<const bits*>(p.x);
   bits* __restrict__ y = static_cast<bits*>(p.y);
   const int items = p.TTs * p.h;
+  pdl_launch_dependents();
+  pdl_wait();
 
   for (int64_t tile0 = (int64_t)blockIdx.x * p.TTs; tile0 < p.ntok; tile0 += p.step_tok) {
     __syncthreads();  // the previous tile's readers are done with the table
@@ -602,6 +614,8 @@ __global__ void __launch_bounds__(256) rope_cache_build_kernel(const float* __re
   bits* co = static_cast<bits*>(cos_out);
   bits* so = static_cast<bits*>(sin_out);
   const int64_t total = rows * half;
+  pdl_launch_dependents();
+  pdl_wait();
   for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
        idx += (int64_t)gridDim.x * blockDim.x) {
     const int64_t pr = idx / half;

@@ -285,8 +285,12 @@ __global__ void __launch_bounds__(kTmaThreads, 2)
     }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmx)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&tmy)) : "memory");
   }
   __syncthreads();
+  pdl_launch_dependents();
+  pdl_wait();  // everything above overlaps the previous kernel's tail
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
