@@ -15,8 +15,10 @@
 //             TMA copy completes the transaction bytes, and one asynchronous
 //             arrive per producer lane, triggered when that lane's cp.async
 //             copies of the tile's cos/sin rows have landed.
-//   empty[s]  count 1: consumer thread 0 arrives once the TMA store of the
-//             stage has finished reading shared memory.
+//   computed[s] count = consumer warps: each consumer warp arrives after it
+//             has rotated its rows of the stage (and fenced them for TMA).
+//   empty[s]  count 1: the store warp arrives once the TMA store of the stage
+//             has finished reading shared memory, so the producer may refill it.
 // Every wait is bounded (kWaitLimitNs of global time); a wait that runs out
 // sets bit 1 of the caller's status word (if given) and the kernel leaves
 // uniformly (consumers agree through a barrier reduction), after the
@@ -34,9 +36,15 @@
 
 namespace rope_gb300 {
 
-constexpr int kTmaConsumerWarps = 8;
+#ifndef ROPE_TMA_CONSUMER_WARPS
+#define ROPE_TMA_CONSUMER_WARPS 8
+#endif
+#ifndef ROPE_TMA_MIN_CTAS
+#define ROPE_TMA_MIN_CTAS 2
+#endif
+constexpr int kTmaConsumerWarps = ROPE_TMA_CONSUMER_WARPS;
 constexpr int kTmaConsumers = kTmaConsumerWarps * 32;
-constexpr int kTmaThreads = kTmaConsumers + 32;
+constexpr int kTmaThreads = kTmaConsumers + 64;  // + producer warp + store warp
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 constexpr int kMaxGather = 8;  // 16-byte cos/sin pieces per producer lane per tile
 constexpr int kMaxHeads = 4;   // heads one consumer thread rotates per tile column
@@ -165,28 +173,14 @@ __device__ __forceinline__ void cp_async_arrive(uint32_t bar) {
 
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 
-__device__ __forceinline__ void bulk_wait_read_1() {
-  asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+__device__ __forceinline__ void bulk_wait_read_0() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 __device__ __forceinline__ void fence_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
-// Barrier among the consumer warps that also ORs a predicate across them.
-__device__ __forceinline__ bool consumer_any(bool pred) {
-  uint32_t out;
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\t"
-      "setp.ne.u32 p, %1, 0;\n\t"
-      "bar.red.or.pred q, 2, %2, p;\n\t"
-      "selp.u32 %0, 1, 0, q;\n\t}"
-      : "=r"(out)
-      : "r"((uint32_t)pred), "n"(kTmaConsumers)
-      : "memory");
-  return out != 0;
 }
 
 // ---------------------------------------------------------------------------
@@ -260,7 +254,7 @@ __device__ __forceinline__ TilePos<MODE> load_tile_pos(const KParams& p, const T
 // The kernel
 // ---------------------------------------------------------------------------
 template <class T, bool INTER, bool RANK4, Coef MODE>
-__global__ void __launch_bounds__(kTmaThreads, 2)
+__global__ void __launch_bounds__(kTmaThreads, ROPE_TMA_MIN_CTAS)
     rope_tma_kernel(const KParams p, const TParams tp, const __grid_constant__ CUtensorMap tmx,
                     const __grid_constant__ CUtensorMap tmy) {
   using E = Elem<T>;
@@ -271,8 +265,9 @@ __global__ void __launch_bounds__(kTmaThreads, 2)
 
   extern __shared__ __align__(1024) unsigned char smem[];
   const uint32_t sbase = smem_addr(smem);
-  const uint32_t full0 = sbase;                 // full[s]  at  8*s
-  const uint32_t empty0 = sbase + 8 * tp.K;     // empty[s] at  8*(K+s)
+  const uint32_t full0 = sbase;                  // full[s]      at 8*s
+  const uint32_t empty0 = sbase + 8 * tp.K;      // empty[s]     at 8*(K+s)
+  const uint32_t done0 = sbase + 16 * tp.K;      // computed[s]  at 8*(2K+s)
   unsigned char* stage0 = smem + tp.bar_bytes;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -281,7 +276,8 @@ __global__ void __launch_bounds__(kTmaThreads, 2)
   if (threadIdx.x == 0) {
     for (int s = 0; s < tp.K; ++s) {
       mbar_init(full0 + 8 * s, 33);  // producer lane 0's arrive.expect_tx + every producer lane
-      mbar_init(empty0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, 1);  // the store warp, once the stage's store has read it
+      mbar_init(done0 + 8 * s, kTmaConsumerWarps);  // one arrive per consumer warp
     }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -331,7 +327,7 @@ __global__ void __launch_bounds__(kTmaThreads, 2)
       TilePos<MODE> nxt{};
       if (t + gridDim.x < tp.ntiles)
         nxt = load_tile_pos<MODE>(p, tile_of<RANK4>(p, tp, t + gridDim.x), lane);
-      if (r > 0 && !mbar_wait(empty0 + 8 * s, (uint32_t)((r - 1) & 1))) {
+      if (r > 0 && !__all_sync(0xffffffffu, mbar_wait(empty0 + 8 * s, (uint32_t)((r - 1) & 1)))) {
         timed_out = true;
         break;
       }
@@ -401,11 +397,36 @@ __global__ void __launch_bounds__(kTmaThreads, 2)
     return;
   }
 
+  if (warp == 1) {
+    // ---------------------------------------------------------- store warp
+    const uint64_t pol = policy_evict_first();
+    bool timed_out = false;
+    int64_t j = 0;
+    for (int64_t t = blockIdx.x; t < tp.ntiles; t += gridDim.x, ++j) {
+      const int s = (int)(j % tp.K);
+      if (!__all_sync(0xffffffffu, mbar_wait(done0 + 8 * s, (uint32_t)((j / tp.K) & 1)))) {
+        timed_out = true;
+        break;
+      }
+      if (lane == 0) {
+        const Tile tl = tile_of<RANK4>(p, tp, t);
+        tma_store_y<RANK4>(&tmy, tl.c, smem_addr(stage0 + (size_t)s * tp.stage_bytes), pol);
+        bulk_commit();
+        bulk_wait_read_0();  // the stage may be refilled once the store has read it
+        mbar_arrive(empty0 + 8 * s);
+      }
+      __syncwarp();
+    }
+    if (lane == 0) bulk_wait_all();
+    if (timed_out && lane == 0 && p.oor_flag) atomicOr(p.oor_flag, 2);
+    return;
+  }
+
   // -------------------------------------------------------------- consumers
   // Thread q owns column (token ts, pair unit k) of the tile for up to
   // kMaxHeads heads ng = hq, hq + tpc, ... The column's cos/sin (for M-RoPE:
   // the three streams merged) are read once and reused for every head.
-  const int q = threadIdx.x - 32;
+  const int q = threadIdx.x - 64;
   const int nP = p.nP;
   const int cols = tp.TS * nP;
   const int tpc = kTmaConsumers / cols;  // threads per column (the host keeps cols <= consumers)
@@ -426,12 +447,12 @@ __global__ void __launch_bounds__(kTmaThreads, 2)
     for (int jj = 0; jj < V; ++jj) present |= 1u << ((um >> (2 * jj)) & 3);
     stream_masks<V>(um, m0, m1);
   }
-  const uint64_t pol = policy_evict_first();
   bool timed_out = false;
   int64_t j = 0;
   for (int64_t t = blockIdx.x; t < tp.ntiles; t += gridDim.x, ++j) {
     const int s = (int)(j % tp.K);
-    const bool ok = mbar_wait(full0 + 8 * s, (uint32_t)((j / tp.K) & 1));
+    // the lanes of a warp agree, so a timeout never splits a warp
+    const bool ok = __all_sync(0xffffffffu, mbar_wait(full0 + 8 * s, (uint32_t)((j / tp.K) & 1)));
     const Tile tl = tile_of<RANK4>(p, tp, t);
     unsigned char* st = stage0 + (size_t)s * tp.stage_bytes;
     if (ok && has_col && ts < tl.ntok) {
@@ -510,20 +531,15 @@ __global__ void __launch_bounds__(kTmaThreads, 2)
         }
       }
     }
-    fence_async_smem();
-    if (consumer_any(!ok)) {  // also the barrier before the store
+    if (!ok) {  // the producer, the store warp and the other consumer warps also give up
       timed_out = true;
       break;
     }
-    if (q == 0) {
-      tma_store_y<RANK4>(&tmy, tl.c, smem_addr(st), pol);
-      bulk_commit();
-      bulk_wait_read_1();  // the previous tile's store has read its stage
-      if (j > 0) mbar_arrive(empty0 + 8 * ((j - 1) % tp.K));
-    }
+    fence_async_smem();  // this thread's smem writes, before the TMA store reads them
+    __syncwarp();
+    if (lane == 0) mbar_arrive(done0 + 8 * s);
   }
-  if (q == 0) bulk_wait_all();
-  if (timed_out && q == 0 && p.oor_flag) atomicOr(p.oor_flag, 2);
+  if (timed_out && lane == 0 && p.oor_flag) atomicOr(p.oor_flag, 2);
 }
 
 }  // namespace rope_gb300
