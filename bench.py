@@ -221,10 +221,11 @@ class Step:
         y = ctypes.c_void_p(self.ys[k].data_ptr())
         return self.call(x, y, stream, fused)
 
-    def call(self, x, y, stream, fused=False):
+    def call(self, x, y, stream, fused=False, pos=None):
         w = self.w
         lib = self.lib
-        pos = None if self.pos is None else ctypes.c_void_p(self.pos.data_ptr())
+        pt = self.pos if pos is None else pos
+        pos = None if pt is None else ctypes.c_void_p(pt.data_ptr())
         cos = ctypes.c_void_p(self.cos.data_ptr())
         sin = ctypes.c_void_p(self.sin.data_ptr())
         if w.kind == "mrope":
@@ -247,26 +248,33 @@ def n_buffer_sets(w):
     return max(2, math.ceil(4 * L2_BYTES / per_set))
 
 
-def time_steps(torch, step, steps, stream_handle, fused=False, per_kernel=True):
-    """Time `steps` launches (rotating buffer sets) with CUDA events on the launching stream."""
+def time_steps(torch, step, steps, stream_handle, fused=False, sample_every=1):
+    """Time `steps` launches (rotating buffer sets) with CUDA events on the launching stream.
+
+    One event pair brackets the whole run (the throughput); every
+    `sample_every`-th launch is also bracketed by its own pair (its duration).
+    Unbracketed launches follow each other directly, as in a real stream, so
+    the next launch can start its prologue while the previous one drains.
+    """
     n_sets = len(step.xs)
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)] if per_kernel else None
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)] if per_kernel else None
+    sampled = list(range(0, steps, max(1, sample_every)))
+    starts = {k: torch.cuda.Event(enable_timing=True) for k in sampled}
+    ends = {k: torch.cuda.Event(enable_timing=True) for k in sampled}
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
     torch.cuda._sleep(2_000_000)  # let the host queue launches ahead of the GPU
     t_start.record()
     for k in range(steps):
-        if per_kernel:
+        if k in starts:
             starts[k].record()
         step.launch(k % n_sets, stream_handle, fused)
-        if per_kernel:
+        if k in ends:
             ends[k].record()
     t_end.record()
     torch.cuda.synchronize()
     total_ms = t_start.elapsed_time(t_end)
-    kern = [s.elapsed_time(e) for s, e in zip(starts, ends)] if per_kernel else []
+    kern = [starts[k].elapsed_time(ends[k]) for k in sampled]
     return total_ms, kern
 
 
@@ -300,7 +308,7 @@ def gpu_arm(args, rank, world, local_rank):
         torch.distributed.barrier()
     torch.cuda.synchronize()
     t0 = time.time()
-    total_ms, kern = time_steps(torch, step, args.steps, sh)
+    total_ms, kern = time_steps(torch, step, args.steps, sh, sample_every=8)
     t1 = time.time()
     if world > 1:
         torch.distributed.barrier()
@@ -342,7 +350,8 @@ def gpu_arm(args, rank, world, local_rank):
                 "l2": f"inputs rotate over {len(step.xs)} X/Y buffer sets "
                       f"({len(step.xs) * 2 * w.numel * 2 / 2**20:.0f} MiB) > 129 MiB L2; no flush kernel",
                 "launch": "one C-ABI call per step on torch's current stream; the host queues launches "
-                          "ahead of the GPU; timed region = CUDA events around the K steps",
+                          "ahead of the GPU; timed region = CUDA events around the K steps; every 8th "
+                          "step also bracketed by its own events (kernel duration for the roofline)",
                 "parallelism": f"{world} independent replicas (per-GPU batch)",
             },
             "roofline": {
@@ -410,36 +419,48 @@ def measure_rows(args, torch, rp, device, peak):
 
 
 def measure_e2e(args, torch, step, sh, nbytes):
-    """Same metric through the C ABI with host buffers: H2D of X and positions from
-    pinned memory, the launch, D2H of Y into pinned memory, every step."""
-    x_host = torch.from_numpy(step.x_host).pin_memory()
-    y_host = torch.empty_like(x_host).pin_memory()
+    """Same metric through the C ABI with host buffers, every step: H2D of that
+    step's X and positions from pinned memory, the launch, D2H of Y into pinned
+    memory. Two streams alternate steps, so one step's D2H overlaps the next
+    step's H2D (the copy engines run both directions at once)."""
+    x_host = [torch.from_numpy(step.x_host).pin_memory() for _ in range(2)]
+    y_host = [torch.empty_like(x_host[0]).pin_memory() for _ in range(2)]
     pos_host = None if step.pos_host is None else torch.from_numpy(step.pos_host).pin_memory()
-    xd, yd = step.xs[0], step.ys[0]
+    streams = [torch.cuda.Stream() for _ in range(2)]
+    xd = [step.xs[0], step.xs[1 % len(step.xs)]]
+    yd = [step.ys[0], step.ys[1 % len(step.ys)]]
+    pd = [step.pos, None if step.pos is None else step.pos.clone()]
 
-    def one():
-        xd.copy_(x_host, non_blocking=True)
-        if pos_host is not None:
-            step.pos.copy_(pos_host, non_blocking=True)
-        step.call(ctypes.c_void_p(xd.data_ptr()), ctypes.c_void_p(yd.data_ptr()), sh)
-        y_host.copy_(yd, non_blocking=True)
+    def one(k):
+        i = k % 2
+        with torch.cuda.stream(streams[i]):
+            xd[i].copy_(x_host[i], non_blocking=True)
+            if pos_host is not None:
+                pd[i].copy_(pos_host, non_blocking=True)
+            step.call(ctypes.c_void_p(xd[i].data_ptr()), ctypes.c_void_p(yd[i].data_ptr()),
+                      ctypes.c_void_p(streams[i].cuda_stream), pos=pd[i])
+            y_host[i].copy_(yd[i], non_blocking=True)
 
-    for _ in range(3):
-        one()
+    for k in range(4):
+        one(k)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record()
-    for _ in range(args.e2e_steps):
-        one()
+    for s_ in streams:
+        s_.wait_event(e0)
+    for k in range(args.e2e_steps):
+        one(k)
+    for s_ in streams:
+        torch.cuda.current_stream().wait_stream(s_)
     e1.record()
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / args.e2e_steps
-    h2d = x_host.numel() * x_host.element_size() + (0 if pos_host is None else pos_host.numel() * 8)
-    d2h = y_host.numel() * y_host.element_size()
+    h2d = x_host[0].numel() * x_host[0].element_size() + (0 if pos_host is None else pos_host.numel() * 8)
+    d2h = y_host[0].numel() * y_host[0].element_size()
     return {"value": round(nbytes / (ms * 1e-3) / 1e9, 2), "unit": "GB/s", "ms_per_step": round(ms, 4),
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "note": "pinned host X/positions -> device, rope_apply, device Y -> pinned host; cos/sin cache "
-                    "stays resident (model constant)"}
+            "note": "per step: pinned host X/positions -> device, rope_apply, device Y -> pinned host; two "
+                    "streams alternate steps; the cos/sin cache stays resident (model constant)"}
 
 
 # ---------------------------------------------------------------------------
