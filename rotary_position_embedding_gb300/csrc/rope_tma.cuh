@@ -317,21 +317,38 @@ __global__ void __launch_bounds__(kTmaThreads, ROPE_TMA_MIN_CTAS)
       g_piece[g] = rem2 % ch;
       g_dst[g] = 16u * (uint32_t)c;
     }
-    int64_t j = 0;
-    int64_t t = blockIdx.x;
-    TilePos<MODE> cur{};
-    if (t < tp.ntiles) cur = load_tile_pos<MODE>(p, tile_of<RANK4>(p, tp, t), lane);
-    for (; t < tp.ntiles; t += gridDim.x, ++j) {
-      const int s = (int)(j % tp.K);
-      const int64_t r = j / tp.K;
-      TilePos<MODE> nxt{};
-      if (t + gridDim.x < tp.ntiles)
-        nxt = load_tile_pos<MODE>(p, tile_of<RANK4>(p, tp, t + gridDim.x), lane);
-      if (r > 0 && !__all_sync(0xffffffffu, mbar_wait(empty0 + 8 * s, (uint32_t)((r - 1) & 1)))) {
-        timed_out = true;
-        break;
+    // X tiles run D = K-1 tiles ahead of the cos/sin work: they depend only on
+    // the tile index and a free stage, so the first K-1 copies leave at once and
+    // the positions' latency never delays an X copy.
+    const int64_t n_mine = tp.ntiles > blockIdx.x ? (tp.ntiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+    const int64_t D = tp.K - 1;
+    auto tile_at = [&](int64_t jj) -> int64_t { return blockIdx.x + jj * (int64_t)gridDim.x; };
+    auto issue_x = [&](int64_t jj) {
+      if (lane == 0) {
+        const int s = (int)(jj % tp.K);
+        const Tile tl = tile_of<RANK4>(p, tp, tile_at(jj));
+        mbar_arrive_expect_tx(full0 + 8 * s, tp.x_bytes);
+        tma_load_x<RANK4>(smem_addr(stage0 + (size_t)s * tp.stage_bytes), &tmx, tl.c, full0 + 8 * s, pol);
       }
-      const Tile tl = tile_of<RANK4>(p, tp, t);
+    };
+    for (int64_t jj = 0; jj < D && jj < n_mine; ++jj) issue_x(jj);
+    int64_t j = 0;
+    TilePos<MODE> cur{};
+    if (n_mine > 0) cur = load_tile_pos<MODE>(p, tile_of<RANK4>(p, tp, tile_at(0)), lane);
+    for (; j < n_mine; ++j) {
+      const int s = (int)(j % tp.K);
+      TilePos<MODE> nxt{};
+      if (j + 1 < n_mine) nxt = load_tile_pos<MODE>(p, tile_of<RANK4>(p, tp, tile_at(j + 1)), lane);
+      if (j + D < n_mine) {
+        const int64_t jx = j + D;  // its stage was used by tile jx - K = j - 1
+        const int64_t rx = jx / tp.K;
+        if (rx > 0 && !__all_sync(0xffffffffu, mbar_wait(empty0 + 8 * (jx % tp.K), (uint32_t)((rx - 1) & 1)))) {
+          timed_out = true;
+          break;
+        }
+        issue_x(jx);
+      }
+      const Tile tl = tile_of<RANK4>(p, tp, tile_at(j));
       unsigned char* st = stage0 + (size_t)s * tp.stage_bytes;
       const uint32_t st_addr = smem_addr(st);
       uint32_t flags = 0;
@@ -355,11 +372,7 @@ __global__ void __launch_bounds__(kTmaThreads, ROPE_TMA_MIN_CTAS)
           for (int k = 0; k < SLOTS; ++k) reinterpret_cast<int64_t*>(st + tp.pos_off)[lane * SLOTS + k] = cur.v[k];
         }
       }
-      __syncwarp();  // the flags and positions precede lane 0's (releasing) arrive and the gather
-      if (lane == 0) {
-        mbar_arrive_expect_tx(full0 + 8 * s, tp.x_bytes);
-        tma_load_x<RANK4>(st_addr, &tmx, tl.c, full0 + 8 * s, pol);
-      }
+      __syncwarp();  // the flags and positions precede the gather and the lanes' (releasing) arrivals
       // The tile's cos/sin rows (layout [token][slot][cos|sin][rd/2]) are
       // gathered 16 bytes per copy from the L2-resident tables with
       // asynchronous copies that arrive on full[s] when they land, so the
@@ -387,11 +400,19 @@ __global__ void __launch_bounds__(kTmaThreads, ROPE_TMA_MIN_CTAS)
       cp_async_arrive(full0 + 8 * s);
       cur = nxt;
     }
-    // Leave only after every load this warp issued has landed.
+    // Leave only after every copy this warp issued has landed (tiles whose
+    // full barrier can still complete: those it finished arriving on).
     const int64_t issued = j;
     for (int64_t q = issued - tp.K > 0 ? issued - tp.K : 0; q < issued; ++q) {
       const int s = (int)(q % tp.K);
       if (!mbar_wait(full0 + 8 * s, (uint32_t)((q / tp.K) & 1))) timed_out = true;
+    }
+    if (timed_out) {
+      // X copies issued ahead for tiles whose cos/sin were never gathered: let them land
+      // before the CTA's shared memory is released (bounded, like every wait here).
+      const uint64_t t0 = global_ns();
+      while (global_ns() - t0 < 1000000ull) {
+      }
     }
     if (timed_out && lane == 0 && p.oor_flag) atomicOr(p.oor_flag, 2);
     return;
