@@ -54,6 +54,8 @@ def parse_args():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--variant", choices=["auto", "simt", "tma"], default="auto",
                     help="kernel variant for the timed region (the library's automatic choice by default)")
+    ap.add_argument("--schedule", choices=["dynamic", "static"], default="dynamic",
+                    help="tile schedule of the pipelined kernel: a scratch counter (dynamic) or round robin")
     ap.add_argument("--quick", action="store_true",
                     help="timed region only: no per-workload rows, end-to-end or CPU legs (profiling runs)")
     return ap.parse_args()
@@ -188,9 +190,12 @@ class ClockSampler:
 class Step:
     """One workload pass through the C ABI with pre-marshalled ctypes arguments."""
 
-    def __init__(self, rp, torch, w, device, n_sets, shard=0):
+    def __init__(self, rp, torch, w, device, n_sets, shard=0, dynamic=True):
         self.w = w
         self.torch = torch
+        # one zeroed scratch per stream this Step launches on (dynamic schedule)
+        self.dynamic = dynamic
+        self.scratch = {}
         lib = rp.load_library()
         self.lib = lib
         inp = wl.make_inputs(w, shard=shard)
@@ -221,24 +226,35 @@ class Step:
         y = ctypes.c_void_p(self.ys[k].data_ptr())
         return self.call(x, y, stream, fused)
 
+    def scratch_for(self, stream):
+        if not self.dynamic:
+            return None
+        key = stream.value if isinstance(stream, ctypes.c_void_p) else stream
+        buf = self.scratch.get(key)
+        if buf is None:
+            buf = self.torch.zeros(8, dtype=self.torch.int64, device=self.xs[0].device)
+            self.scratch[key] = buf
+        return ctypes.c_void_p(buf.data_ptr())
+
     def call(self, x, y, stream, fused=False, pos=None):
         w = self.w
         lib = self.lib
         pt = self.pos if pos is None else pos
         pos = None if pt is None else ctypes.c_void_p(pt.data_ptr())
+        scr = self.scratch_for(stream)
         cos = ctypes.c_void_p(self.cos.data_ptr())
         sin = ctypes.c_void_p(self.sin.data_ptr())
         if w.kind == "mrope":
             st = lib.mrope_apply(self.code, w.rank, self.xshape, x, y, w.cache_rows, cos, sin, pos, self.sec,
                                  w.mrope_layout, w.scale, w.interleaved, w.rotary_embedding_dim, self.nh, 0,
-                                 None, stream)
+                                 None, scr, stream)
         elif w.kind == "fused" and fused:
             st = lib.rope_apply_fused(self.code, w.rank, self.xshape, x, y, ctypes.c_void_p(self.inv.data_ptr()),
                                       w.attention_scaling, pos, w.interleaved, w.rotary_embedding_dim, self.nh,
                                       stream)
         else:
             st = lib.rope_apply(self.code, w.rank, self.xshape, x, y, self.cos.dim(), self.cshape, cos, sin, pos,
-                                w.interleaved, w.rotary_embedding_dim, self.nh, None, stream)
+                                w.interleaved, w.rotary_embedding_dim, self.nh, None, scr, stream)
         if st != 0:
             raise RuntimeError(f"{w.name}: status {st}: {lib.rope_last_error().decode()}")
 
@@ -295,7 +311,7 @@ def gpu_arm(args, rank, world, local_rank):
     stream = torch.cuda.current_stream(device)
     sh = ctypes.c_void_p(stream.cuda_stream)
     nbytes = wl.algorithmic_bytes(w)
-    step = Step(rp, torch, w, device, n_buffer_sets(w), shard=rank)
+    step = Step(rp, torch, w, device, n_buffer_sets(w), shard=rank, dynamic=args.schedule == "dynamic")
     for k in range(args.warmup):
         step.launch(k % len(step.xs), sh)
     torch.cuda.synchronize()
@@ -353,6 +369,8 @@ def gpu_arm(args, rank, world, local_rank):
                           "ahead of the GPU; timed region = CUDA events around the K steps; every 8th "
                           "step also bracketed by its own events (kernel duration for the roofline)",
                 "parallelism": f"{world} independent replicas (per-GPU batch)",
+                "schedule": args.schedule + (" (tiles drawn from a scratch counter)" if args.schedule == "dynamic"
+                                             else " (tiles dealt round robin)"),
             },
             "roofline": {
                 "bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",

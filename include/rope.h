@@ -59,6 +59,19 @@ typedef enum rope_status {
 
 typedef enum rope_dtype { ROPE_F32 = 0, ROPE_F16 = 1 } rope_dtype;
 
+/*
+ * Scratch for the dynamic tile schedule (optional `scratch` argument of
+ * rope_apply, mrope_apply and mrope_apply_stream_map): ROPE_SCRATCH_BYTES of
+ * caller-owned device memory, 8-byte aligned, set to zero once before its first
+ * use. With it, the pipelined kernel hands tiles to whichever CTA asks next, so
+ * CTAs that run faster take more tiles and the launch ends sooner; every launch
+ * leaves the scratch zeroed again when it completes. Launches that may run on
+ * the GPU at the same time (other streams, other threads) must use different
+ * scratch buffers; launches in one stream can share one. NULL keeps the static
+ * schedule (tiles dealt round robin). The result is the same either way.
+ */
+#define ROPE_SCRATCH_BYTES 64
+
 /* A cudaStream_t (the two types are the same pointer type). */
 typedef struct CUstream_st* rope_stream_t;
 
@@ -87,6 +100,7 @@ typedef struct CUstream_st* rope_stream_t;
  *               [rd, H) of every head are copied through.
  * num_heads     required (>= 1, dividing the last dimension) for rank 3; for
  *               rank 4 it must be 0 or equal to N.
+ * scratch       NULL or ROPE_SCRATCH_BYTES of device scratch (see above).
  * The shape contract is the manifest's "derive" rank3Contract, rank4Contract,
  * rank3PosContract, rank4PosContract: cache width * 2 == rd, 3-D cache
  * leading dims == (B, S), position_ids present iff the cache is 2-D.
@@ -95,7 +109,7 @@ rope_status rope_apply(rope_dtype dtype, int32_t x_rank, const int64_t* x_shape,
                        void* y, int32_t cache_rank, const int64_t* cache_shape,
                        const void* cos_cache, const void* sin_cache, const int64_t* position_ids,
                        int32_t interleaved, int32_t rotary_embedding_dim, int32_t num_heads,
-                       int32_t* oor_flag, rope_stream_t stream);
+                       int32_t* oor_flag, void* scratch, rope_stream_t stream);
 
 /*
  * mrope_apply -- MRotaryEmbedding (multimodal RoPE).
@@ -125,13 +139,15 @@ rope_status rope_apply(rope_dtype dtype, int32_t x_rank, const int64_t* x_shape,
  *               rounded once from its exact value.
  * is_packed_batching  must be 0; 1 returns ROPE_ERR_UNSUPPORTED ([README,
  *               Attributes/is_packed_batching]).
+ * scratch       NULL or ROPE_SCRATCH_BYTES of device scratch (see above).
  */
 rope_status mrope_apply(rope_dtype dtype, int32_t x_rank, const int64_t* x_shape, const void* x,
                         void* y, int64_t cache_rows, const void* cos_cache,
                         const void* sin_cache, const int64_t* position_ids,
                         const int32_t* mrope_section, int32_t mrope_layout, float scale,
                         int32_t interleaved, int32_t rotary_embedding_dim, int32_t num_heads,
-                        int32_t is_packed_batching, int32_t* oor_flag, rope_stream_t stream);
+                        int32_t is_packed_batching, int32_t* oor_flag, void* scratch,
+                        rope_stream_t stream);
 
 /*
  * mrope_apply_stream_map -- MRotaryEmbedding with an explicit stream per
@@ -148,7 +164,7 @@ rope_status mrope_apply_stream_map(rope_dtype dtype, int32_t x_rank, const int64
                                    const int64_t* position_ids, const uint8_t* stream_map,
                                    float scale, int32_t interleaved,
                                    int32_t rotary_embedding_dim, int32_t num_heads,
-                                   int32_t* oor_flag, rope_stream_t stream);
+                                   int32_t* oor_flag, void* scratch, rope_stream_t stream);
 
 /*
  * mrope_stream_map -- host-only helper: the stream of each of the `half`

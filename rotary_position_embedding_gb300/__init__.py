@@ -24,6 +24,7 @@ __all__ = [
 
 ROPE_OK, ROPE_ERR_INVALID_ARG, ROPE_ERR_UNSUPPORTED, ROPE_ERR_CUDA = 0, 1, 2, 3
 ROPE_F32, ROPE_F16 = 0, 1
+ROPE_SCRATCH_BYTES = 64
 VARIANTS = {"auto": 0, "simt": 1, "tma": 2}
 _UNSUPPORTED_DTYPE = 99  # passed through so the library reports ROPE_ERR_UNSUPPORTED
 
@@ -40,11 +41,12 @@ _u8p = ctypes.POINTER(ctypes.c_uint8)
 
 # name -> argtypes (restype is the int status unless listed in _RESTYPES)
 SIGNATURES = {
-    "rope_apply": [_i32, _i32, _i64p, _vp, _vp, _i32, _i64p, _vp, _vp, _vp, _i32, _i32, _i32, _vp, _vp],
+    "rope_apply": [_i32, _i32, _i64p, _vp, _vp, _i32, _i64p, _vp, _vp, _vp, _i32, _i32, _i32, _vp, _vp,
+                   _vp],
     "mrope_apply": [_i32, _i32, _i64p, _vp, _vp, _i64, _vp, _vp, _vp, _i32p, _i32, _f32, _i32, _i32,
-                    _i32, _i32, _vp, _vp],
+                    _i32, _i32, _vp, _vp, _vp],
     "mrope_apply_stream_map": [_i32, _i32, _i64p, _vp, _vp, _i64, _vp, _vp, _vp, _u8p, _f32, _i32,
-                               _i32, _i32, _vp, _vp],
+                               _i32, _i32, _vp, _vp, _vp],
     "mrope_stream_map": [_i32p, _i32, _i32, _u8p],
     "rope_apply_fused": [_i32, _i32, _i64p, _vp, _vp, _vp, _f32, _vp, _i32, _i32, _i32, _vp],
     "rope_cache_build": [_i32, _vp, _i32, _i64, _f32, _vp, _vp, _vp],
@@ -130,6 +132,31 @@ def _stream(x, stream):
     return ctypes.c_void_p(s.cuda_stream)
 
 
+_scratch = {}
+
+
+def _scratch_ptr(x, stream, scratch):
+    """The scratch argument: None/False -> static schedule; a tensor -> that
+    buffer; "auto" (default) -> one zeroed buffer per (device, stream), owned by
+    this module, so launches on one stream share it and streams never do."""
+    import torch
+
+    if scratch is None or scratch is False:
+        return None
+    if isinstance(scratch, torch.Tensor):
+        _cuda("scratch", scratch)
+        if scratch.numel() * scratch.element_size() < ROPE_SCRATCH_BYTES:
+            raise ValueError(f"scratch needs {ROPE_SCRATCH_BYTES} bytes")
+        return ctypes.c_void_p(scratch.data_ptr())
+    s = stream if stream is not None else torch.cuda.current_stream(x.device)
+    key = (x.device.index, s.cuda_stream)
+    buf = _scratch.get(key)
+    if buf is None:
+        buf = torch.zeros(ROPE_SCRATCH_BYTES // 8, dtype=torch.int64, device=x.device)
+        _scratch[key] = buf
+    return ctypes.c_void_p(buf.data_ptr())
+
+
 def _out(x, out):
     import torch
 
@@ -146,7 +173,7 @@ def _out(x, out):
 # --------------------------------------------------------------------------
 
 def rope_apply(x, cos_cache, sin_cache, position_ids=None, *, interleaved=0, rotary_embedding_dim=0,
-               num_heads=0, out=None, oor_flag=None, stream=None):
+               num_heads=0, out=None, oor_flag=None, stream=None, scratch="auto"):
     """RotaryEmbedding (see ``rope_apply`` in include/rope.h). Returns Y."""
     import torch
 
@@ -161,14 +188,14 @@ def rope_apply(x, cos_cache, sin_cache, position_ids=None, *, interleaved=0, rot
         st = lib.rope_apply(_dtype_code(x), x.dim(), _shape(x), _ptr(x), _ptr(y), cos_cache.dim(),
                             _shape(cos_cache), _ptr(cos_cache), _ptr(sin_cache), _ptr(position_ids),
                             int(interleaved), int(rotary_embedding_dim), int(num_heads), _ptr(oor_flag),
-                            _stream(x, stream))
+                            _scratch_ptr(x, stream, scratch), _stream(x, stream))
     _check("rope_apply", st)
     return y
 
 
 def mrope_apply(x, cos_cache, sin_cache, position_ids, mrope_section, *, mrope_layout=0, scale=1.0,
                 interleaved=0, rotary_embedding_dim=0, num_heads=0, is_packed_batching=0, out=None,
-                oor_flag=None, stream=None):
+                oor_flag=None, stream=None, scratch="auto"):
     """MRotaryEmbedding (see ``mrope_apply`` in include/rope.h). Returns Y."""
     import torch
 
@@ -184,13 +211,15 @@ def mrope_apply(x, cos_cache, sin_cache, position_ids, mrope_section, *, mrope_l
         st = lib.mrope_apply(_dtype_code(x), x.dim(), _shape(x), _ptr(x), _ptr(y), int(cos_cache.shape[0]),
                              _ptr(cos_cache), _ptr(sin_cache), _ptr(position_ids), sec, int(mrope_layout),
                              float(scale), int(interleaved), int(rotary_embedding_dim), int(num_heads),
-                             int(is_packed_batching), _ptr(oor_flag), _stream(x, stream))
+                             int(is_packed_batching), _ptr(oor_flag), _scratch_ptr(x, stream, scratch),
+                             _stream(x, stream))
     _check("mrope_apply", st)
     return y
 
 
 def mrope_apply_stream_map(x, cos_cache, sin_cache, position_ids, stream_map, *, scale=1.0, interleaved=0,
-                           rotary_embedding_dim=0, num_heads=0, out=None, oor_flag=None, stream=None):
+                           rotary_embedding_dim=0, num_heads=0, out=None, oor_flag=None, stream=None,
+                           scratch="auto"):
     """MRotaryEmbedding with an explicit stream (0 t, 1 h, 2 w) per half-rotary index."""
     import torch
 
@@ -208,7 +237,7 @@ def mrope_apply_stream_map(x, cos_cache, sin_cache, position_ids, stream_map, *,
                                         int(cos_cache.shape[0]), _ptr(cos_cache), _ptr(sin_cache),
                                         _ptr(position_ids), arr, float(scale), int(interleaved),
                                         int(rotary_embedding_dim), int(num_heads), _ptr(oor_flag),
-                                        _stream(x, stream))
+                                        _scratch_ptr(x, stream, scratch), _stream(x, stream))
     _check("mrope_apply_stream_map", st)
     return y
 

@@ -369,7 +369,8 @@ rope_status plan_tma(const Geom& g, int es, int rank, int slots, const void* fn,
   tp.coef_off = tp.x_bytes;
   tp.flag_off = tp.coef_off + (uint32_t)(TS * slots * 2 * g.h * es);
   tp.pos_off = (tp.flag_off + (uint32_t)TS * 4 + 15) / 16 * 16;
-  tp.stage_bytes = (tp.pos_off + (uint32_t)TS * slots * 8 + 1023) / 1024 * 1024;
+  tp.hdr_off = (tp.pos_off + (uint32_t)TS * slots * 8 + 15) / 16 * 16;
+  tp.stage_bytes = (tp.hdr_off + 16 + 1023) / 1024 * 1024;
   tp.bar_bytes = 1024;
   int64_t K = (ROPE_TMA_SMEM_BUDGET - tp.bar_bytes) / tp.stage_bytes;
   if (K > ROPE_TMA_MAX_STAGES) K = ROPE_TMA_MAX_STAGES;
@@ -493,7 +494,8 @@ rope_status mrope_common(rope_dtype dtype, int32_t x_rank, const int64_t* x_shap
                          void* y, int64_t cache_rows, const void* cos_cache, const void* sin_cache,
                          const int64_t* position_ids, const int32_t* sec, int32_t layout,
                          const uint8_t* explicit_map, float scale, int32_t interleaved,
-                         int32_t rde, int32_t num_heads, int32_t* oor_flag, rope_stream_t stream) {
+                         int32_t rde, int32_t num_heads, int32_t* oor_flag, void* scratch,
+                         rope_stream_t stream) {
   ROPE_TRY(check_dtype(dtype));
   Geom g;
   ROPE_TRY(x_geometry(x_rank, x_shape, num_heads, &g));
@@ -525,10 +527,12 @@ rope_status mrope_common(rope_dtype dtype, int32_t x_rank, const int64_t* x_shap
     ROPE_TRY(check_elem_ptr(sin_cache, "sin_cache", es));
   }
   if (oor_flag && !aligned(oor_flag, 4)) return fail(ROPE_ERR_INVALID_ARG, "oor_flag is misaligned");
+  if (scratch && !aligned(scratch, 8)) return fail(ROPE_ERR_INVALID_ARG, "scratch is not aligned to 8 bytes");
 
   const bool vec = vector_ok(g, es, {x, y, cos_cache, sin_cache});
   KParams kp;
   memset(&kp, 0, sizeof(kp));
+  kp.sched = static_cast<unsigned long long*>(scratch);
   kp.x = x;
   kp.y = y;
   kp.cos = cos_cache;
@@ -560,7 +564,7 @@ rope_status rope_apply(rope_dtype dtype, int32_t x_rank, const int64_t* x_shape,
                        void* y, int32_t cache_rank, const int64_t* cache_shape,
                        const void* cos_cache, const void* sin_cache, const int64_t* position_ids,
                        int32_t interleaved, int32_t rotary_embedding_dim, int32_t num_heads,
-                       int32_t* oor_flag, rope_stream_t stream) {
+                       int32_t* oor_flag, void* scratch, rope_stream_t stream) {
   g_last_error.clear();
   ROPE_TRY(check_dtype(dtype));
   Geom g;
@@ -602,6 +606,7 @@ rope_status rope_apply(rope_dtype dtype, int32_t x_rank, const int64_t* x_shape,
   }
   if (gather) ROPE_TRY(check_elem_ptr(position_ids, "position_ids", 8));
   if (oor_flag && !aligned(oor_flag, 4)) return fail(ROPE_ERR_INVALID_ARG, "oor_flag is misaligned");
+  if (scratch && !aligned(scratch, 8)) return fail(ROPE_ERR_INVALID_ARG, "scratch is not aligned to 8 bytes");
 
   const bool vec = vector_ok(g, es, {x, y, cos_cache, sin_cache});
   const Coef mode = gather ? Coef::kCache2D : Coef::kCache3D;
@@ -616,6 +621,7 @@ rope_status rope_apply(rope_dtype dtype, int32_t x_rank, const int64_t* x_shape,
   kp.scale = 1.0f;
   kp.scale_is_one = 1;
   kp.cache_rows = rows;
+  kp.sched = static_cast<unsigned long long*>(scratch);
   if (tma_eligible(g, es, vec)) {
     const void* tfn = tma_kernel(dtype, interleaved != 0, x_rank == 4, mode);
     TmaLaunch T;
@@ -634,7 +640,8 @@ rope_status mrope_apply(rope_dtype dtype, int32_t x_rank, const int64_t* x_shape
                         const void* sin_cache, const int64_t* position_ids,
                         const int32_t* mrope_section, int32_t mrope_layout, float scale,
                         int32_t interleaved, int32_t rotary_embedding_dim, int32_t num_heads,
-                        int32_t is_packed_batching, int32_t* oor_flag, rope_stream_t stream) {
+                        int32_t is_packed_batching, int32_t* oor_flag, void* scratch,
+                        rope_stream_t stream) {
   g_last_error.clear();
   if (is_packed_batching == 1)
     return fail(ROPE_ERR_UNSUPPORTED, "is_packed_batching = 1 (packed batching) is not implemented");
@@ -643,7 +650,7 @@ rope_status mrope_apply(rope_dtype dtype, int32_t x_rank, const int64_t* x_shape
   if (!mrope_section) return fail(ROPE_ERR_INVALID_ARG, "mrope_section is NULL");
   return mrope_common(dtype, x_rank, x_shape, x, y, cache_rows, cos_cache, sin_cache, position_ids,
                       mrope_section, mrope_layout, nullptr, scale, interleaved,
-                      rotary_embedding_dim, num_heads, oor_flag, stream);
+                      rotary_embedding_dim, num_heads, oor_flag, scratch, stream);
 }
 
 rope_status mrope_apply_stream_map(rope_dtype dtype, int32_t x_rank, const int64_t* x_shape,
@@ -652,12 +659,12 @@ rope_status mrope_apply_stream_map(rope_dtype dtype, int32_t x_rank, const int64
                                    const int64_t* position_ids, const uint8_t* stream_map,
                                    float scale, int32_t interleaved,
                                    int32_t rotary_embedding_dim, int32_t num_heads,
-                                   int32_t* oor_flag, rope_stream_t stream) {
+                                   int32_t* oor_flag, void* scratch, rope_stream_t stream) {
   g_last_error.clear();
   if (!stream_map) return fail(ROPE_ERR_INVALID_ARG, "stream_map is NULL");
   return mrope_common(dtype, x_rank, x_shape, x, y, cache_rows, cos_cache, sin_cache, position_ids,
                       nullptr, 0, stream_map, scale, interleaved, rotary_embedding_dim, num_heads,
-                      oor_flag, stream);
+                      oor_flag, scratch, stream);
 }
 
 rope_status mrope_stream_map(const int32_t* mrope_section, int32_t mrope_layout, int32_t half,

@@ -48,6 +48,7 @@ struct KParams {
   int64_t step_tok;      // gridDim.x * TTs
   int64_t step_b, step_s;  // step_tok = step_b * S + step_s
   uint32_t smap[kMaxMRopeHalf / 16];  // M-RoPE: 2-bit stream of each coefficient index
+  unsigned long long* sched;  // TMA path: tile counter pair for the dynamic schedule, or null
 };
 
 // Kernel entry points for cudaLaunchKernel / occupancy queries. `vec` selects

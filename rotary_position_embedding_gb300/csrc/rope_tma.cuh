@@ -15,6 +15,9 @@
 //             TMA copy completes the transaction bytes, and one asynchronous
 //             arrive per producer lane, triggered when that lane's cp.async
 //             copies of the tile's cos/sin rows have landed.
+// Tiles go to CTAs round robin, or -- when the caller gives a scratch counter --
+// to whichever CTA's producer asks next (dynamic schedule); each stage records
+// its tile index, and an index past the last tile ends the pipeline.
 //   computed[s] count = consumer warps: each consumer warp arrives after it
 //             has rotated its rows of the stage (and fenced them for TMA).
 //   empty[s]  count 1: the store warp arrives once the TMA store of the stage
@@ -59,6 +62,7 @@ struct TParams {
   uint32_t coef_off;    // stage offsets: coefficient rows, per-token flags
   uint32_t flag_off;
   uint32_t pos_off;     // the tile's positions (producer scratch inside the stage)
+  uint32_t hdr_off;     // the stage's tile index (8 bytes)
   uint32_t stage_bytes;
   uint32_t bar_bytes;   // barrier block in front of stage 0
 };
@@ -288,6 +292,13 @@ __global__ void __launch_bounds__(kTmaThreads, ROPE_TMA_MIN_CTAS)
   pdl_launch_dependents();
   pdl_wait();  // everything above overlaps the previous kernel's tail
 
+  // Each stage starts with the index of the tile it holds (written by the
+  // producer before the stage's full barrier can complete); an index >= ntiles
+  // is the sentinel that ends the consumers and the store warp.
+  auto stage_tile = [&](int s) -> int64_t* {
+    return reinterpret_cast<int64_t*>(stage0 + (size_t)s * tp.stage_bytes + tp.hdr_off);
+  };
+
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     const uint64_t pol = policy_evict_first();
@@ -317,38 +328,61 @@ __global__ void __launch_bounds__(kTmaThreads, ROPE_TMA_MIN_CTAS)
       g_piece[g] = rem2 % ch;
       g_dst[g] = 16u * (uint32_t)c;
     }
-    // X tiles run D = K-1 tiles ahead of the cos/sin work: they depend only on
-    // the tile index and a free stage, so the first K-1 copies leave at once and
-    // the positions' latency never delays an X copy.
-    const int64_t n_mine = tp.ntiles > blockIdx.x ? (tp.ntiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+    // Tile j of this CTA: blockIdx.x + j*gridDim.x (static schedule), or the
+    // next index drawn from the shared counter (dynamic schedule: CTAs that
+    // run faster take more tiles, so all of them finish together).
+    // X copies run D = K-1 tiles ahead of the cos/sin work: they need only the
+    // tile index and a free stage, so the first copies leave at once and the
+    // positions' latency never delays a tile copy.
     const int64_t D = tp.K - 1;
-    auto tile_at = [&](int64_t jj) -> int64_t { return blockIdx.x + jj * (int64_t)gridDim.x; };
-    auto issue_x = [&](int64_t jj) {
+    // issue_x: lane 0 picks tile jj's index, records it in the stage and starts
+    // its X copy; returns (on every lane) whether that was the sentinel.
+    auto issue_x = [&](int64_t jj) -> bool {
+      int64_t t = 0;
       if (lane == 0) {
         const int s = (int)(jj % tp.K);
-        const Tile tl = tile_of<RANK4>(p, tp, tile_at(jj));
-        mbar_arrive_expect_tx(full0 + 8 * s, tp.x_bytes);
-        tma_load_x<RANK4>(smem_addr(stage0 + (size_t)s * tp.stage_bytes), &tmx, tl.c, full0 + 8 * s, pol);
+        t = p.sched ? (int64_t)atomicAdd(p.sched, 1ull) : (int64_t)blockIdx.x + jj * (int64_t)gridDim.x;
+        *stage_tile(s) = t;
+        if (t < tp.ntiles) {
+          const Tile tl = tile_of<RANK4>(p, tp, t);
+          mbar_arrive_expect_tx(full0 + 8 * s, tp.x_bytes);
+          tma_load_x<RANK4>(smem_addr(stage0 + (size_t)s * tp.stage_bytes), &tmx, tl.c, full0 + 8 * s, pol);
+        } else {
+          mbar_arrive(full0 + 8 * s);  // the sentinel carries no bytes
+        }
       }
+      t = __shfl_sync(0xffffffffu, t, 0);
+      return t >= tp.ntiles;
     };
-    for (int64_t jj = 0; jj < D && jj < n_mine; ++jj) issue_x(jj);
+    bool ended = false;
+    int64_t jx = 0;  // tiles whose X copy (or the sentinel) is issued
+    for (; jx < D && !ended; ++jx) ended = issue_x(jx);
+    __syncwarp();
     int64_t j = 0;
     TilePos<MODE> cur{};
-    if (n_mine > 0) cur = load_tile_pos<MODE>(p, tile_of<RANK4>(p, tp, tile_at(0)), lane);
-    for (; j < n_mine; ++j) {
+    {
+      const int64_t t0 = *stage_tile(0);
+      if (t0 < tp.ntiles) cur = load_tile_pos<MODE>(p, tile_of<RANK4>(p, tp, t0), lane);
+    }
+    // Invariant: tile j's copy (or the sentinel) is out (j < jx) at the top of
+    // every iteration, since the prologue issues D >= 1 of them and each
+    // iteration issues one more until the sentinel.
+    for (;; ++j) {
       const int s = (int)(j % tp.K);
-      TilePos<MODE> nxt{};
-      if (j + 1 < n_mine) nxt = load_tile_pos<MODE>(p, tile_of<RANK4>(p, tp, tile_at(j + 1)), lane);
-      if (j + D < n_mine) {
-        const int64_t jx = j + D;  // its stage was used by tile jx - K = j - 1
-        const int64_t rx = jx / tp.K;
-        if (rx > 0 && !__all_sync(0xffffffffu, mbar_wait(empty0 + 8 * (jx % tp.K), (uint32_t)((rx - 1) & 1)))) {
-          timed_out = true;
-          break;
-        }
-        issue_x(jx);
+      const int64_t t = *stage_tile(s);
+      if (t >= tp.ntiles) {  // sentinel: complete its full barrier and stop
+        cp_async_arrive(full0 + 8 * s);
+        ++j;
+        break;
       }
-      const Tile tl = tile_of<RANK4>(p, tp, tile_at(j));
+      // prefetch the next tile's positions (when its copy is already out)
+      TilePos<MODE> nxt{};
+      const bool have_nxt = j + 1 < jx;
+      if (have_nxt) {
+        const int64_t tn = *stage_tile((int)((j + 1) % tp.K));
+        if (tn < tp.ntiles) nxt = load_tile_pos<MODE>(p, tile_of<RANK4>(p, tp, tn), lane);
+      }
+      const Tile tl = tile_of<RANK4>(p, tp, t);
       unsigned char* st = stage0 + (size_t)s * tp.stage_bytes;
       const uint32_t st_addr = smem_addr(st);
       uint32_t flags = 0;
@@ -398,23 +432,46 @@ __global__ void __launch_bounds__(kTmaThreads, ROPE_TMA_MIN_CTAS)
                                                (g_sin[g] ? sinb : cosb) + row * p.h) + g_piece[g]);
       }
       cp_async_arrive(full0 + 8 * s);
+      if (!ended && jx == j + D) {  // the next copy goes into the stage tile j-1 used
+        const int64_t rx = jx / tp.K;
+        if (rx > 0 && !__all_sync(0xffffffffu, mbar_wait(empty0 + 8 * (jx % tp.K), (uint32_t)((rx - 1) & 1)))) {
+          ++j;  // tile j's arrivals are complete
+          timed_out = true;
+          break;
+        }
+        ended = issue_x(jx);
+        ++jx;
+        __syncwarp();
+      }
+      if (!have_nxt && j + 1 < jx) {  // D = 1: the next copy only just went out
+        const int64_t tn = *stage_tile((int)((j + 1) % tp.K));
+        if (tn < tp.ntiles) nxt = load_tile_pos<MODE>(p, tile_of<RANK4>(p, tp, tn), lane);
+      }
       cur = nxt;
     }
-    // Leave only after every copy this warp issued has landed (tiles whose
-    // full barrier can still complete: those it finished arriving on).
-    const int64_t issued = j;
-    for (int64_t q = issued - tp.K > 0 ? issued - tp.K : 0; q < issued; ++q) {
+    // Leave only after every copy this warp issued has landed: the full
+    // barriers of the stages it completed (the last K of them).
+    for (int64_t q = j - tp.K > 0 ? j - tp.K : 0; q < j; ++q) {
       const int s = (int)(q % tp.K);
       if (!mbar_wait(full0 + 8 * s, (uint32_t)((q / tp.K) & 1))) timed_out = true;
     }
     if (timed_out) {
-      // X copies issued ahead for tiles whose cos/sin were never gathered: let them land
-      // before the CTA's shared memory is released (bounded, like every wait here).
+      // X copies issued ahead of cos/sin work that never happened: give them
+      // time to land before the CTA's shared memory goes away (bounded).
       const uint64_t t0 = global_ns();
       while (global_ns() - t0 < 1000000ull) {
       }
+      if (lane == 0 && p.oor_flag) atomicOr(p.oor_flag, 2);
     }
-    if (timed_out && lane == 0 && p.oor_flag) atomicOr(p.oor_flag, 2);
+    if (p.sched && lane == 0) {
+      // The last CTA to stop drawing resets the counter pair for the next launch.
+      __threadfence();
+      if (atomicAdd(p.sched + 1, 1ull) == (unsigned long long)gridDim.x - 1) {
+        p.sched[0] = 0;
+        p.sched[1] = 0;
+        __threadfence();
+      }
+    }
     return;
   }
 
@@ -423,12 +480,14 @@ __global__ void __launch_bounds__(kTmaThreads, ROPE_TMA_MIN_CTAS)
     const uint64_t pol = policy_evict_first();
     bool timed_out = false;
     int64_t j = 0;
-    for (int64_t t = blockIdx.x; t < tp.ntiles; t += gridDim.x, ++j) {
+    for (;; ++j) {
       const int s = (int)(j % tp.K);
       if (!__all_sync(0xffffffffu, mbar_wait(done0 + 8 * s, (uint32_t)((j / tp.K) & 1)))) {
         timed_out = true;
         break;
       }
+      const int64_t t = *stage_tile(s);
+      if (t >= tp.ntiles) break;  // sentinel
       if (lane == 0) {
         const Tile tl = tile_of<RANK4>(p, tp, t);
         tma_store_y<RANK4>(&tmy, tl.c, smem_addr(stage0 + (size_t)s * tp.stage_bytes), pol);
@@ -470,10 +529,16 @@ __global__ void __launch_bounds__(kTmaThreads, ROPE_TMA_MIN_CTAS)
   }
   bool timed_out = false;
   int64_t j = 0;
-  for (int64_t t = blockIdx.x; t < tp.ntiles; t += gridDim.x, ++j) {
+  for (;; ++j) {
     const int s = (int)(j % tp.K);
     // the lanes of a warp agree, so a timeout never splits a warp
     const bool ok = __all_sync(0xffffffffu, mbar_wait(full0 + 8 * s, (uint32_t)((j / tp.K) & 1)));
+    const int64_t t = ok ? *stage_tile(s) : 0;
+    if (ok && t >= tp.ntiles) {  // sentinel: hand it to the store warp and stop
+      __syncwarp();
+      if (lane == 0) mbar_arrive(done0 + 8 * s);
+      break;
+    }
     const Tile tl = tile_of<RANK4>(p, tp, t);
     unsigned char* st = stage0 + (size_t)s * tp.stage_bytes;
     if (ok && has_col && ts < tl.ntok) {

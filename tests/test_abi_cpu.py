@@ -55,10 +55,10 @@ FAKE2 = ctypes.c_void_p(0x20000)
 
 def _rope(so, **kw):
     a = dict(dtype=F16, rank=3, xs=_i64(2, 4, 64), x=FAKE, y=FAKE2, crank=2, cs=_i64(16, 8), cos=FAKE,
-             sin=FAKE, pos=FAKE, inter=0, rd=0, nh=4, flag=None, stream=None)
+             sin=FAKE, pos=FAKE, inter=0, rd=0, nh=4, flag=None, scratch=None, stream=None)
     a.update(kw)
     return so.rope_apply(a["dtype"], a["rank"], a["xs"], a["x"], a["y"], a["crank"], a["cs"], a["cos"],
-                         a["sin"], a["pos"], a["inter"], a["rd"], a["nh"], a["flag"], a["stream"])
+                         a["sin"], a["pos"], a["inter"], a["rd"], a["nh"], a["flag"], a["scratch"], a["stream"])
 
 
 @pytest.mark.parametrize("kw,status", [
@@ -82,6 +82,7 @@ def _rope(so, **kw):
     (dict(x=ctypes.c_void_p(0x10001)), INVALID),        # misaligned float16 pointer
     (dict(pos=ctypes.c_void_p(0x10004)), INVALID),      # misaligned int64 pointer
     (dict(x=None), INVALID),
+    (dict(scratch=ctypes.c_void_p(0x20004)), INVALID),  # misaligned scratch
 ])
 def test_rope_apply_rejects_before_launch(lib, kw, status):
     so = lib.load_library()
@@ -100,11 +101,11 @@ def test_empty_inputs_launch_nothing(lib):
 def _mrope(so, **kw):
     a = dict(dtype=F16, rank=3, xs=_i64(2, 4, 32), x=FAKE, y=FAKE2, rows=16, cos=FAKE, sin=FAKE,
              pos=FAKE, sec=(ctypes.c_int32 * 3)(2, 1, 1), layout=0, scale=1.0, inter=0, rd=0, nh=4,
-             packed=0, flag=None, stream=None)
+             packed=0, flag=None, scratch=None, stream=None)
     a.update(kw)
     return so.mrope_apply(a["dtype"], a["rank"], a["xs"], a["x"], a["y"], a["rows"], a["cos"], a["sin"],
                           a["pos"], a["sec"], a["layout"], a["scale"], a["inter"], a["rd"], a["nh"],
-                          a["packed"], a["flag"], a["stream"])
+                          a["packed"], a["flag"], a["scratch"], a["stream"])
 
 
 @pytest.mark.parametrize("kw,status", [

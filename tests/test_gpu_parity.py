@@ -229,7 +229,8 @@ TMA_SHAPES = [
 
 @pytest.mark.parametrize("case", TMA_SHAPES, ids=[c[0] for c in TMA_SHAPES])
 @pytest.mark.parametrize("in_place", [False, True])
-def test_tma_pipeline_shapes(lib, orc, cuda, torch_mod, case, in_place):
+@pytest.mark.parametrize("schedule", ["static", "dynamic"])
+def test_tma_pipeline_shapes(lib, orc, cuda, torch_mod, case, in_place, schedule):
     torch = torch_mod
     name, kind, rank, dt, B, S, N, H, rd, inter = case
     dtype = DT[dt]
@@ -243,6 +244,7 @@ def test_tma_pipeline_shapes(lib, orc, cuda, torch_mod, case, in_place):
     nh = N if rank == 3 else 0
     xd = _dev(x, torch, cuda)
     flag = torch.zeros(1, dtype=torch.int32, device=cuda)
+    scratch = torch.zeros(8, dtype=torch.int64, device=cuda) if schedule == "dynamic" else None
     if kind == "rope":
         pos = rng.integers(0, R, (B, S))
         pos.ravel()[rng.choice(pos.size, size=max(1, pos.size // 50), replace=False)] = R + 3
@@ -250,7 +252,7 @@ def test_tma_pipeline_shapes(lib, orc, cuda, torch_mod, case, in_place):
         with lib.variant("tma"):
             yd = lib.rope_apply(xd, _dev(cos, torch, cuda), _dev(sin, torch, cuda), _dev(pos, torch, cuda),
                                 interleaved=inter, rotary_embedding_dim=rd, num_heads=nh, oor_flag=flag,
-                                out=xd if in_place else None)
+                                out=xd if in_place else None, scratch=scratch)
         mask = rope_passthrough_mask(shape, rank, N, rd, pos, R)
     else:
         sec = (h - 2 * (h // 3), h // 3, h // 3)
@@ -263,12 +265,35 @@ def test_tma_pipeline_shapes(lib, orc, cuda, torch_mod, case, in_place):
             yd = lib.mrope_apply(xd, _dev(cos, torch, cuda), _dev(sin, torch, cuda), _dev(pos3, torch, cuda),
                                  sec, mrope_layout=layout, scale=scale, interleaved=inter,
                                  rotary_embedding_dim=rd, num_heads=nh, oor_flag=flag,
-                                 out=xd if in_place else None)
+                                 out=xd if in_place else None, scratch=scratch)
         smap = orc.mrope_stream_map(sec, layout, h)
         mask = mrope_passthrough_mask(shape, rank, N, rd, pos3, R, smap, inter)
     torch.cuda.synchronize()
     compare(_host(yd), y_ref, x, rank, N, mask)
     assert int(flag.item()) == 1   # some positions were out of range; no pipeline timeout (bit 1)
+    if scratch is not None:
+        assert not scratch.any()   # the launch left its counters zeroed for the next one
+
+
+def test_dynamic_schedule_back_to_back_and_shared_scratch(lib, orc, cuda, torch_mod):
+    """Many launches in one stream share one scratch (each leaves it zeroed); results
+    equal the static schedule's bit for bit."""
+    torch = torch_mod
+    rng = np.random.default_rng(31)
+    B, S, N, H = 4, 1024, 16, 128
+    x = rng.standard_normal((B, S, N * H)).astype(np.float16)
+    inv = wl.inv_freq(10000.0, H, H // 2)
+    cos, sin = orc.cache_build(inv, 3000, np.float16)
+    pos = rng.integers(0, 3000, (B, S))
+    xd, cd, sd, pd = (_dev(a, torch, cuda) for a in (x, cos, sin, pos))
+    scratch = torch.zeros(8, dtype=torch.int64, device=cuda)
+    with lib.variant("tma"):
+        ref = lib.rope_apply(xd, cd, sd, pd, num_heads=N, scratch=None)
+        outs = [lib.rope_apply(xd, cd, sd, pd, num_heads=N, scratch=scratch) for _ in range(20)]
+    torch.cuda.synchronize()
+    for o in outs:
+        assert torch.equal(o.view(torch.int16), ref.view(torch.int16))
+    assert not scratch.any()
 
 
 # ---------------------------------------------------------------------------
