@@ -232,6 +232,35 @@ typedef enum rope_variant {
 rope_status rope_set_variant(rope_variant variant);
 rope_variant rope_get_variant(void);
 
+/*
+ * rope_apply_no_alloc -- rope_apply for callers that cannot allocate device
+ * memory. The operator pages have no counterpart: this is a library-level
+ * variant. rope_apply's dynamic tile schedule needs ROPE_SCRATCH_BYTES of
+ * caller-owned device scratch; some callers cannot provide even that -- code
+ * running inside CUDA stream capture (where allocating is not allowed),
+ * plugins or runtimes that are handed only their input and output buffers,
+ * callers without a device allocator. This entry point takes the scratch from
+ * a fixed 256-byte array in the library's own device memory (every GPU that
+ * loads the library holds it until the process exits; the schedule uses 16
+ * bytes of it and no input size needs more). It allocates nothing: no
+ * cudaMalloc, no cudaFree, no allocating library call.
+ *
+ * Arguments, results and errors are those of rope_apply without `scratch`
+ * (shapes the pipelined kernel cannot take run the SIMT kernels, which use no
+ * scratch). The first call on a device sets the array up (finds its device
+ * address and clears it, synchronously), so make that first call before any
+ * stream capture that includes this entry point. Every call on a device shares
+ * the one array and each completed launch leaves it cleared for the next:
+ * calls that overlap on the GPU (different streams, different threads) race on
+ * it and must not be issued; calls in one stream are fine.
+ */
+rope_status rope_apply_no_alloc(rope_dtype dtype, int32_t x_rank, const int64_t* x_shape,
+                                const void* x, void* y, int32_t cache_rank,
+                                const int64_t* cache_shape, const void* cos_cache,
+                                const void* sin_cache, const int64_t* position_ids,
+                                int32_t interleaved, int32_t rotary_embedding_dim,
+                                int32_t num_heads, int32_t* oor_flag, rope_stream_t stream);
+
 /* Static name of a status code. */
 const char* rope_status_string(rope_status status);
 

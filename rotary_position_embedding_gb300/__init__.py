@@ -50,6 +50,8 @@ SIGNATURES = {
     "mrope_stream_map": [_i32p, _i32, _i32, _u8p],
     "rope_apply_fused": [_i32, _i32, _i64p, _vp, _vp, _vp, _f32, _vp, _i32, _i32, _i32, _vp],
     "rope_cache_build": [_i32, _vp, _i32, _i64, _f32, _vp, _vp, _vp],
+    "rope_apply_no_alloc": [_i32, _i32, _i64p, _vp, _vp, _i32, _i64p, _vp, _vp, _vp, _i32, _i32, _i32, _vp,
+                            _vp],
     "rope_set_variant": [_i32],
     "rope_get_variant": [],
     "rope_status_string": [_i32],

@@ -558,6 +558,8 @@ rope_status mrope_common(rope_dtype dtype, int32_t x_rank, const int64_t* x_shap
 
 }  // namespace
 
+void rope_gb300::set_last_error(const char* msg) { g_last_error = msg; }
+
 extern "C" {
 
 rope_status rope_apply(rope_dtype dtype, int32_t x_rank, const int64_t* x_shape, const void* x,

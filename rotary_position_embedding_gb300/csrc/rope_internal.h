@@ -57,6 +57,9 @@ const void* rope_kernel_cached(int dtype, bool vec, bool interleaved, bool rank4
 const void* rope_kernel_mrope(int dtype, bool vec, bool interleaved, bool rank4);
 const void* fused_kernel(int dtype, bool vec, bool interleaved, bool rank4);
 const void* cache_build_kernel(int dtype);
+// Records the message rope_last_error() returns on the calling thread.
+void set_last_error(const char* msg);
+
 // TMA-pipelined variant (vector path, head size <= 256 elements); its launch
 // takes (KParams, TParams, CUtensorMap x, CUtensorMap y).
 const void* tma_kernel(int dtype, bool interleaved, bool rank4, Coef mode);
