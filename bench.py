@@ -54,7 +54,7 @@ def parse_args():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--variant", choices=["auto", "simt", "tma"], default="auto",
                     help="kernel variant for the timed region (the library's automatic choice by default)")
-    ap.add_argument("--schedule", choices=["dynamic", "static"], default="dynamic",
+    ap.add_argument("--schedule", choices=["dynamic", "static"], default="static",
                     help="tile schedule of the pipelined kernel: a scratch counter (dynamic) or round robin")
     ap.add_argument("--quick", action="store_true",
                     help="timed region only: no per-workload rows, end-to-end or CPU legs (profiling runs)")

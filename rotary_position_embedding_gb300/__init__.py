@@ -138,9 +138,10 @@ _scratch = {}
 
 
 def _scratch_ptr(x, stream, scratch):
-    """The scratch argument: None/False -> static schedule; a tensor -> that
-    buffer; "auto" (default) -> one zeroed buffer per (device, stream), owned by
-    this module, so launches on one stream share it and streams never do."""
+    """The scratch argument: None (default) -> the static schedule; a tensor ->
+    that buffer (ROPE_SCRATCH_BYTES, zeroed before its first use); "auto" -> one
+    zeroed buffer per (device, stream), owned by this module, so launches on one
+    stream share it and streams never do."""
     import torch
 
     if scratch is None or scratch is False:
@@ -175,7 +176,7 @@ def _out(x, out):
 # --------------------------------------------------------------------------
 
 def rope_apply(x, cos_cache, sin_cache, position_ids=None, *, interleaved=0, rotary_embedding_dim=0,
-               num_heads=0, out=None, oor_flag=None, stream=None, scratch="auto"):
+               num_heads=0, out=None, oor_flag=None, stream=None, scratch=None):
     """RotaryEmbedding (see ``rope_apply`` in include/rope.h). Returns Y."""
     import torch
 
@@ -197,7 +198,7 @@ def rope_apply(x, cos_cache, sin_cache, position_ids=None, *, interleaved=0, rot
 
 def mrope_apply(x, cos_cache, sin_cache, position_ids, mrope_section, *, mrope_layout=0, scale=1.0,
                 interleaved=0, rotary_embedding_dim=0, num_heads=0, is_packed_batching=0, out=None,
-                oor_flag=None, stream=None, scratch="auto"):
+                oor_flag=None, stream=None, scratch=None):
     """MRotaryEmbedding (see ``mrope_apply`` in include/rope.h). Returns Y."""
     import torch
 
@@ -221,7 +222,7 @@ def mrope_apply(x, cos_cache, sin_cache, position_ids, mrope_section, *, mrope_l
 
 def mrope_apply_stream_map(x, cos_cache, sin_cache, position_ids, stream_map, *, scale=1.0, interleaved=0,
                            rotary_embedding_dim=0, num_heads=0, out=None, oor_flag=None, stream=None,
-                           scratch="auto"):
+                           scratch=None):
     """MRotaryEmbedding with an explicit stream (0 t, 1 h, 2 w) per half-rotary index."""
     import torch
 
