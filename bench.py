@@ -37,8 +37,8 @@ from rotary_position_embedding_gb300 import workloads as wl  # noqa: E402
 L2_BYTES = 129 * 2 ** 20
 FALLBACK_HBM_GBS = 6800.0
 METRIC = "RoPE achieved HBM GB/s and Gelem/s, fp16, as % of GB300 HBM roofline"
-KERNEL_SOURCES = ["rope_kernels.cuh", "rope_internal.h", "rope_api.cu", "k_rope.cu", "k_mrope.cu",
-                  "k_fused.cu"]
+KERNEL_SOURCES = ["rope_kernels.cuh", "rope_tma.cuh", "rope_internal.h", "rope_api.cu", "k_rope.cu",
+                  "k_mrope.cu", "k_fused.cu", "k_tma.cu"]
 
 
 def parse_args():

@@ -342,8 +342,8 @@ rope_status plan_tma(const Geom& g, int es, int rank, int slots, const void* fn,
     if (NG > 256) NG = 256;
   }
   // Consumer columns (token, pair unit) must fit the consumer threads, each
-  // thread covers at most kMaxHeads heads of its column, and the producer's
-  // 32 lanes gather at most kMaxGather 16-byte cos/sin pieces each.
+  // thread covers at most kMaxHeads heads of its column, and the gather
+  // warp's 32 lanes gather at most kMaxGather 16-byte cos/sin pieces each.
   const int64_t nPu = g.h / V;
   const int64_t pieces_per_tok = (int64_t)slots * 2 * (g.h * es / 16);
   auto fits = [&](int64_t ts, int64_t ng) {

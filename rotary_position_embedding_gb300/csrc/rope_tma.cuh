@@ -2,30 +2,35 @@
 //
 // The operation streams X once and writes Y once; the bandwidth a streaming
 // kernel reaches is set by how many bytes it keeps in flight. Here the bytes
-// in flight live in shared memory, not registers: a producer warp moves whole
-// tiles of X (TS tokens x NG heads x H) into a K-stage ring with TMA tensor
-// copies, and gathers each token's cos/sin rows next to the tile with 16-byte
-// asynchronous copies; eight consumer warps rotate the tile in place; one consumer thread
-// writes the tile back with a TMA tensor store. Pass-through elements (the
-// tail past the rotary width, tokens or pairs whose position is out of range)
-// are never touched: the store writes back the bytes the load brought in.
+// in flight live in shared memory, not registers. Each CTA runs a K-stage ring
+// of tiles (TS tokens x NG heads x H) with three warp roles:
+//   copy warp     (lane 0) starts each tile's TMA tensor copy into a free
+//                 stage and writes rotated tiles back with TMA tensor stores;
+//                 a stage is refilled the moment its store has read it;
+//   gather warp   loads the tile's positions (one tile ahead) and gathers each
+//                 token's cos/sin rows next to the tile with 16-byte
+//                 asynchronous copies;
+//   consumers     rotate the tile in place (ROPE_TMA_CONSUMER_WARPS warps).
+// Pass-through elements (the tail past the rotary width, tokens or pairs whose
+// position is out of range) are never touched: the store writes back the
+// bytes the load brought in.
 //
 // Pipeline protocol (per stage s, round r = tile index / K):
-//   full[s]   count 33: producer lane 0's arrive.expect_tx(tile bytes), whose
-//             TMA copy completes the transaction bytes, and one asynchronous
-//             arrive per producer lane, triggered when that lane's cp.async
-//             copies of the tile's cos/sin rows have landed.
-// Tiles go to CTAs round robin, or -- when the caller gives a scratch counter --
-// to whichever CTA's producer asks next (dynamic schedule); each stage records
-// its tile index, and an index past the last tile ends the pipeline.
+//   issued[s]   count 1: the copy warp, after writing the stage's tile index
+//               (its header) and starting the copy.
+//   full[s]     count 33: the copy warp's arrive.expect_tx(tile bytes), whose
+//               TMA copy completes the transaction bytes, and one asynchronous
+//               arrive per gather lane, triggered when that lane's cp.async
+//               copies of the tile's cos/sin rows have landed.
 //   computed[s] count = consumer warps: each consumer warp arrives after it
-//             has rotated its rows of the stage (and fenced them for TMA).
-//   empty[s]  count 1: the store warp arrives once the TMA store of the stage
-//             has finished reading shared memory, so the producer may refill it.
+//               has rotated its rows of the stage (and fenced them for TMA).
+// Tiles go to CTAs round robin, or -- when the caller gives a scratch counter --
+// to whichever CTA's copy warp asks next (dynamic schedule); an index past the
+// last tile (the sentinel) ends the pipeline.
 // Every wait is bounded (kWaitLimitNs of global time); a wait that runs out
 // sets bit 1 of the caller's status word (if given) and the kernel leaves
-// uniformly (consumers agree through a barrier reduction), after the
-// producer has waited, again bounded, for the loads it issued.
+// uniformly (each warp agrees through a warp vote), after the copy warp has
+// waited, again bounded, for the copies it issued.
 //
 // Definitions followed: "ai.onnx.RotaryEmbedding" WebGPU manifest (inputs,
 // attributeDescriptions) and "com.microsoft.MRotaryEmbedding" README (Inputs,
@@ -47,9 +52,10 @@ namespace rope_gb300 {
 #endif
 constexpr int kTmaConsumerWarps = ROPE_TMA_CONSUMER_WARPS;
 constexpr int kTmaConsumers = kTmaConsumerWarps * 32;
-constexpr int kTmaThreads = kTmaConsumers + 64;  // + producer warp + store warp
+constexpr int kTmaRoleWarps = 2;  // the copy warp and the gather warp
+constexpr int kTmaThreads = kTmaConsumers + 32 * kTmaRoleWarps;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
-constexpr int kMaxGather = 8;  // 16-byte cos/sin pieces per producer lane per tile
+constexpr int kMaxGather = 8;  // 16-byte cos/sin pieces per gather lane per tile
 constexpr int kMaxHeads = 4;   // heads one consumer thread rotates per tile column
 
 struct TParams {
@@ -61,7 +67,7 @@ struct TParams {
   uint32_t x_bytes;     // bytes of one X box
   uint32_t coef_off;    // stage offsets: coefficient rows, per-token flags
   uint32_t flag_off;
-  uint32_t pos_off;     // the tile's positions (producer scratch inside the stage)
+  uint32_t pos_off;     // the tile's positions (gather warp scratch inside the stage)
   uint32_t hdr_off;     // the stage's tile index (8 bytes)
   uint32_t stage_bytes;
   uint32_t bar_bytes;   // barrier block in front of stage 0
@@ -108,6 +114,19 @@ __device__ __forceinline__ uint64_t global_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
+}
+
+// Whether the phase of `bar` with parity `parity` has completed (no waiting).
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
 }
 
 // Wait for the phase of `bar` with parity `parity` to complete; false after
@@ -232,7 +251,7 @@ __device__ __forceinline__ Tile tile_of(const KParams& p, const TParams& tp, int
   return tl;
 }
 
-// Positions of token `lane` of a tile (producer lanes), prefetched one tile ahead.
+// Positions of token `lane` of a tile (gather lanes), prefetched one tile ahead.
 template <Coef MODE>
 struct TilePos {
   int64_t v[MODE == Coef::kMRope ? 3 : 1];
@@ -270,8 +289,8 @@ __global__ void __launch_bounds__(kTmaThreads, ROPE_TMA_MIN_CTAS)
   extern __shared__ __align__(1024) unsigned char smem[];
   const uint32_t sbase = smem_addr(smem);
   const uint32_t full0 = sbase;                  // full[s]      at 8*s
-  const uint32_t empty0 = sbase + 8 * tp.K;      // empty[s]     at 8*(K+s)
-  const uint32_t done0 = sbase + 16 * tp.K;      // computed[s]  at 8*(2K+s)
+  const uint32_t done0 = sbase + 8 * tp.K;       // computed[s]  at 8*(K+s)
+  const uint32_t issued0 = sbase + 16 * tp.K;    // issued[s]    at 8*(2K+s)
   unsigned char* stage0 = smem + tp.bar_bytes;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -279,9 +298,9 @@ __global__ void __launch_bounds__(kTmaThreads, ROPE_TMA_MIN_CTAS)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < tp.K; ++s) {
-      mbar_init(full0 + 8 * s, 33);  // producer lane 0's arrive.expect_tx + every producer lane
-      mbar_init(empty0 + 8 * s, 1);  // the store warp, once the stage's store has read it
+      mbar_init(full0 + 8 * s, 33);  // the X copy's arrive.expect_tx + every gather lane
       mbar_init(done0 + 8 * s, kTmaConsumerWarps);  // one arrive per consumer warp
+      mbar_init(issued0 + 8 * s, 1);  // the copy warp, once the stage header is written
     }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -293,21 +312,113 @@ __global__ void __launch_bounds__(kTmaThreads, ROPE_TMA_MIN_CTAS)
   pdl_wait();  // everything above overlaps the previous kernel's tail
 
   // Each stage starts with the index of the tile it holds (written by the
-  // producer before the stage's full barrier can complete); an index >= ntiles
-  // is the sentinel that ends the consumers and the store warp.
+  // copy warp before the stage's full barrier can complete); an index >= ntiles
+  // is the sentinel that ends the gather warp, the consumers and the copy warp.
   auto stage_tile = [&](int s) -> int64_t* {
     return reinterpret_cast<int64_t*>(stage0 + (size_t)s * tp.stage_bytes + tp.hdr_off);
   };
 
   if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    const uint64_t pol = policy_evict_first();
+    // --------------------------------------------------- copy warp (lane 0)
+    // Starts the X copies and writes the rotated tiles back. The first K
+    // tiles' copies leave at once; after that, the moment the TMA store of
+    // tile j has finished reading its stage, the same lane refills the stage
+    // with tile j+K. Tile indices are blockIdx.x + j*gridDim.x, or -- dynamic
+    // schedule -- the next value of the shared counter, so CTAs that run
+    // faster take more tiles. Each index is recorded in the stage header and
+    // published to the gather warp through issued[s].
+    if (lane == 0) {
+      const uint64_t pol = policy_evict_first();
+      bool timed_out = false;
+      auto pick = [&](int64_t jj) -> int64_t {  // the index of this CTA's tile jj
+        return p.sched ? (int64_t)atomicAdd(p.sched, 1ull) : (int64_t)blockIdx.x + jj * (int64_t)gridDim.x;
+      };
+      auto issue = [&](int64_t jj, int64_t t, const Tile& tl) {
+        const int s = (int)(jj % tp.K);
+        *stage_tile(s) = t;
+        if (t < tp.ntiles) {
+          mbar_arrive_expect_tx(full0 + 8 * s, tp.x_bytes);
+          tma_load_x<RANK4>(smem_addr(stage0 + (size_t)s * tp.stage_bytes), &tmx, tl.c, full0 + 8 * s, pol);
+        } else {
+          mbar_arrive(full0 + 8 * s);  // the sentinel carries no bytes
+        }
+        mbar_arrive(issued0 + 8 * s);  // publishes the header to the gather warp
+      };
+      bool ended = false;
+      int64_t jx = 0;  // tiles issued (the sentinel included)
+      for (; jx < tp.K && !ended; ++jx) {
+        const int64_t t = pick(jx);
+        Tile tl{};
+        if (t < tp.ntiles) tl = tile_of<RANK4>(p, tp, t);
+        issue(jx, t, tl);
+        ended = t >= tp.ntiles;
+      }
+      // The next store's tile and the next refill's tile are worked out while
+      // the previous store is still reading its stage, so nothing but the
+      // copies' issue sits between one store and the next.
+      int64_t t_st = *stage_tile(0);
+      Tile tl_st{};
+      if (t_st < tp.ntiles) tl_st = tile_of<RANK4>(p, tp, t_st);
+      for (int64_t j = 0;; ++j) {
+        const int s = (int)(j % tp.K);
+        if (!mbar_wait(done0 + 8 * s, (uint32_t)((j / tp.K) & 1))) {
+          timed_out = true;
+          break;
+        }
+        if (t_st >= tp.ntiles) break;  // sentinel
+        tma_store_y<RANK4>(&tmy, tl_st.c, smem_addr(stage0 + (size_t)s * tp.stage_bytes), pol);
+        bulk_commit();
+        int64_t t_new = 0;
+        Tile tl_new{};
+        if (!ended) {
+          t_new = pick(jx);
+          if (t_new < tp.ntiles) tl_new = tile_of<RANK4>(p, tp, t_new);
+        }
+        // tile j+1 is already issued (K >= 2), so its header is in place
+        t_st = *stage_tile((int)((j + 1) % tp.K));
+        if (t_st < tp.ntiles) tl_st = tile_of<RANK4>(p, tp, t_st);
+        if (!ended) {
+          bulk_wait_read_0();  // the stage may be refilled once the store has read it
+          issue(jx, t_new, tl_new);  // jx == j + K: the tile that goes into stage s next
+          ended = t_new >= tp.ntiles;
+          ++jx;
+        }
+      }
+      bulk_wait_all();
+      if (timed_out) {
+        // copies already issued must land before the CTA's shared memory goes
+        // away: the other warps time out too, so give them time (bounded)
+        const uint64_t t0 = global_ns();
+        while (global_ns() - t0 < 1000000ull) {
+        }
+        if (p.oor_flag) atomicOr(p.oor_flag, 2);
+      }
+      if (p.sched) {
+        // The last CTA to stop drawing resets the counter pair for the next launch.
+        __threadfence();
+        if (atomicAdd(p.sched + 1, 1ull) == (unsigned long long)gridDim.x - 1) {
+          p.sched[0] = 0;
+          p.sched[1] = 0;
+          __threadfence();
+        }
+      }
+    }
+    return;
+  }
+
+  if (warp == 1) {
+    // ------------------------------------------------------------ gather warp
+    // For each tile, once its stage holds the header: the tokens' flags and
+    // positions, then the cos/sin rows (layout [token][slot][cos|sin][rd/2])
+    // gathered 16 bytes per copy from the L2-resident tables by asynchronous
+    // copies that arrive on full[s] when they land, so this warp never waits
+    // on the gather. The next tile's positions are loaded one tile ahead.
     const bits* cosb = static_cast<const bits*>(p.cos);
     const bits* sinb = static_cast<const bits*>(p.sin);
     bool timed_out = false;
-    // Gather roles: piece c of a full tile's coefficient block (16 bytes at
-    // byte 16*c, layout [token][slot][cos|sin][rd/2]) goes to lane c % 32;
-    // each lane's pieces are the same for every tile, so they are decoded once.
+    // Piece c of a full tile's coefficient block (16 bytes at byte 16*c) goes
+    // to lane c % 32; each lane's pieces are the same for every tile, so they
+    // are decoded once.
     const int ch = (int)(row_bytes / 16);
     const int per_tok = SLOTS * 2 * ch;
     const int pieces = tp.TS * per_tok;
@@ -328,66 +439,56 @@ __global__ void __launch_bounds__(kTmaThreads, ROPE_TMA_MIN_CTAS)
       g_piece[g] = rem2 % ch;
       g_dst[g] = 16u * (uint32_t)c;
     }
-    // Tile j of this CTA: blockIdx.x + j*gridDim.x (static schedule), or the
-    // next index drawn from the shared counter (dynamic schedule: CTAs that
-    // run faster take more tiles, so all of them finish together).
-    // X copies run D = K-1 tiles ahead of the cos/sin work: they need only the
-    // tile index and a free stage, so the first copies leave at once and the
-    // positions' latency never delays a tile copy.
-    const int64_t D = tp.K - 1;
-    // issue_x: lane 0 picks tile jj's index, records it in the stage and starts
-    // its X copy; returns (on every lane) whether that was the sentinel.
-    auto issue_x = [&](int64_t jj) -> bool {
-      int64_t t = 0;
-      if (lane == 0) {
-        const int s = (int)(jj % tp.K);
-        t = p.sched ? (int64_t)atomicAdd(p.sched, 1ull) : (int64_t)blockIdx.x + jj * (int64_t)gridDim.x;
-        *stage_tile(s) = t;
-        if (t < tp.ntiles) {
-          const Tile tl = tile_of<RANK4>(p, tp, t);
-          mbar_arrive_expect_tx(full0 + 8 * s, tp.x_bytes);
-          tma_load_x<RANK4>(smem_addr(stage0 + (size_t)s * tp.stage_bytes), &tmx, tl.c, full0 + 8 * s, pol);
-        } else {
-          mbar_arrive(full0 + 8 * s);  // the sentinel carries no bytes
-        }
-      }
-      t = __shfl_sync(0xffffffffu, t, 0);
-      return t >= tp.ntiles;
-    };
-    bool ended = false;
-    int64_t jx = 0;  // tiles whose X copy (or the sentinel) is issued
-    for (; jx < D && !ended; ++jx) ended = issue_x(jx);
-    __syncwarp();
-    int64_t j = 0;
+    // Static schedule: tile indices are known in advance, so positions are
+    // prefetched before the stage is even free. Dynamic schedule: the next
+    // index is read from its stage header when that is already published.
     TilePos<MODE> cur{};
-    {
-      const int64_t t0 = *stage_tile(0);
-      if (t0 < tp.ntiles) cur = load_tile_pos<MODE>(p, tile_of<RANK4>(p, tp, t0), lane);
+    bool have_cur = false;
+    if (!p.sched) {
+      if ((int64_t)blockIdx.x < tp.ntiles) cur = load_tile_pos<MODE>(p, tile_of<RANK4>(p, tp, blockIdx.x), lane);
+      have_cur = true;
     }
-    // Invariant: tile j's copy (or the sentinel) is out (j < jx) at the top of
-    // every iteration, since the prologue issues D >= 1 of them and each
-    // iteration issues one more until the sentinel.
-    for (;; ++j) {
+    for (int64_t j = 0;; ++j) {
       const int s = (int)(j % tp.K);
+      if (!__all_sync(0xffffffffu, mbar_wait(issued0 + 8 * s, (uint32_t)((j / tp.K) & 1)))) {
+        timed_out = true;
+        break;
+      }
       const int64_t t = *stage_tile(s);
       if (t >= tp.ntiles) {  // sentinel: complete its full barrier and stop
         cp_async_arrive(full0 + 8 * s);
-        ++j;
         break;
       }
-      // prefetch the next tile's positions (when its copy is already out)
-      TilePos<MODE> nxt{};
-      const bool have_nxt = j + 1 < jx;
-      if (have_nxt) {
-        const int64_t tn = *stage_tile((int)((j + 1) % tp.K));
-        if (tn < tp.ntiles) nxt = load_tile_pos<MODE>(p, tile_of<RANK4>(p, tp, tn), lane);
-      }
       const Tile tl = tile_of<RANK4>(p, tp, t);
+      if (!have_cur) cur = load_tile_pos<MODE>(p, tl, lane);
+      // Rank 4: a tile is NG strided blocks of TS*H elements, and those loads
+      // run best with the least in flight, so the gather of tile j waits for
+      // tile j-1's data (a phase this warp took part in, so it cannot alias).
+      if (RANK4 && j > 0 &&
+          !__all_sync(0xffffffffu, mbar_wait(full0 + 8 * ((j - 1) % tp.K), (uint32_t)(((j - 1) / tp.K) & 1)))) {
+        timed_out = true;
+        break;
+      }
+      TilePos<MODE> nxt{};
+      bool have_nxt = false;
+      if (!p.sched) {
+        const int64_t tn = (int64_t)blockIdx.x + (j + 1) * (int64_t)gridDim.x;
+        if (tn < tp.ntiles) nxt = load_tile_pos<MODE>(p, tile_of<RANK4>(p, tp, tn), lane);
+        have_nxt = true;
+      } else {
+        // the copy warp publishes headers in tile order, and tile j+1-K's
+        // phase of that barrier is already complete, so the parity test
+        // cannot alias
+        const int sn = (int)((j + 1) % tp.K);
+        if (__all_sync(0xffffffffu, mbar_test(issued0 + 8 * sn, (uint32_t)(((j + 1) / tp.K) & 1)))) {
+          const int64_t tn = *stage_tile(sn);
+          if (tn < tp.ntiles) nxt = load_tile_pos<MODE>(p, tile_of<RANK4>(p, tp, tn), lane);
+          have_nxt = true;
+        }
+      }
       unsigned char* st = stage0 + (size_t)s * tp.stage_bytes;
-      const uint32_t st_addr = smem_addr(st);
       uint32_t flags = 0;
-      const bool mine = lane < tl.ntok;
-      if (mine) {
+      if (lane < tl.ntok) {
 #pragma unroll
         for (int k = 0; k < SLOTS; ++k) {
           bool ok;
@@ -407,11 +508,7 @@ __global__ void __launch_bounds__(kTmaThreads, ROPE_TMA_MIN_CTAS)
         }
       }
       __syncwarp();  // the flags and positions precede the gather and the lanes' (releasing) arrivals
-      // The tile's cos/sin rows (layout [token][slot][cos|sin][rd/2]) are
-      // gathered 16 bytes per copy from the L2-resident tables with
-      // asynchronous copies that arrive on full[s] when they land, so the
-      // producer never waits on the gather. Piece c sits at byte 16*c.
-      const uint32_t coef_addr = st_addr + tp.coef_off;
+      const uint32_t coef_addr = smem_addr(st) + tp.coef_off;
 #pragma unroll
       for (int g = 0; g < kMaxGather; ++g) {
         if (g >= n_gather) break;
@@ -432,81 +529,19 @@ __global__ void __launch_bounds__(kTmaThreads, ROPE_TMA_MIN_CTAS)
                                                (g_sin[g] ? sinb : cosb) + row * p.h) + g_piece[g]);
       }
       cp_async_arrive(full0 + 8 * s);
-      if (!ended && jx == j + D) {  // the next copy goes into the stage tile j-1 used
-        const int64_t rx = jx / tp.K;
-        if (rx > 0 && !__all_sync(0xffffffffu, mbar_wait(empty0 + 8 * (jx % tp.K), (uint32_t)((rx - 1) & 1)))) {
-          ++j;  // tile j's arrivals are complete
-          timed_out = true;
-          break;
-        }
-        ended = issue_x(jx);
-        ++jx;
-        __syncwarp();
-      }
-      if (!have_nxt && j + 1 < jx) {  // D = 1: the next copy only just went out
-        const int64_t tn = *stage_tile((int)((j + 1) % tp.K));
-        if (tn < tp.ntiles) nxt = load_tile_pos<MODE>(p, tile_of<RANK4>(p, tp, tn), lane);
-      }
       cur = nxt;
+      have_cur = have_nxt;
     }
-    // Leave only after every copy this warp issued has landed: the full
-    // barriers of the stages it completed (the last K of them).
-    for (int64_t q = j - tp.K > 0 ? j - tp.K : 0; q < j; ++q) {
-      const int s = (int)(q % tp.K);
-      if (!mbar_wait(full0 + 8 * s, (uint32_t)((q / tp.K) & 1))) timed_out = true;
-    }
-    if (timed_out) {
-      // X copies issued ahead of cos/sin work that never happened: give them
-      // time to land before the CTA's shared memory goes away (bounded).
-      const uint64_t t0 = global_ns();
-      while (global_ns() - t0 < 1000000ull) {
-      }
-      if (lane == 0 && p.oor_flag) atomicOr(p.oor_flag, 2);
-    }
-    if (p.sched && lane == 0) {
-      // The last CTA to stop drawing resets the counter pair for the next launch.
-      __threadfence();
-      if (atomicAdd(p.sched + 1, 1ull) == (unsigned long long)gridDim.x - 1) {
-        p.sched[0] = 0;
-        p.sched[1] = 0;
-        __threadfence();
-      }
-    }
-    return;
-  }
-
-  if (warp == 1) {
-    // ---------------------------------------------------------- store warp
-    const uint64_t pol = policy_evict_first();
-    bool timed_out = false;
-    int64_t j = 0;
-    for (;; ++j) {
-      const int s = (int)(j % tp.K);
-      if (!__all_sync(0xffffffffu, mbar_wait(done0 + 8 * s, (uint32_t)((j / tp.K) & 1)))) {
-        timed_out = true;
-        break;
-      }
-      const int64_t t = *stage_tile(s);
-      if (t >= tp.ntiles) break;  // sentinel
-      if (lane == 0) {
-        const Tile tl = tile_of<RANK4>(p, tp, t);
-        tma_store_y<RANK4>(&tmy, tl.c, smem_addr(stage0 + (size_t)s * tp.stage_bytes), pol);
-        bulk_commit();
-        bulk_wait_read_0();  // the stage may be refilled once the store has read it
-        mbar_arrive(empty0 + 8 * s);
-      }
-      __syncwarp();
-    }
-    if (lane == 0) bulk_wait_all();
+    // every copy this warp issued has landed before it leaves
+    asm volatile("cp.async.wait_all;" ::: "memory");
     if (timed_out && lane == 0 && p.oor_flag) atomicOr(p.oor_flag, 2);
     return;
   }
-
   // -------------------------------------------------------------- consumers
   // Thread q owns column (token ts, pair unit k) of the tile for up to
   // kMaxHeads heads ng = hq, hq + tpc, ... The column's cos/sin (for M-RoPE:
   // the three streams merged) are read once and reused for every head.
-  const int q = threadIdx.x - 64;
+  const int q = threadIdx.x - 32 * kTmaRoleWarps;
   const int nP = p.nP;
   const int cols = tp.TS * nP;
   const int tpc = kTmaConsumers / cols;  // threads per column (the host keeps cols <= consumers)
@@ -534,7 +569,7 @@ __global__ void __launch_bounds__(kTmaThreads, ROPE_TMA_MIN_CTAS)
     // the lanes of a warp agree, so a timeout never splits a warp
     const bool ok = __all_sync(0xffffffffu, mbar_wait(full0 + 8 * s, (uint32_t)((j / tp.K) & 1)));
     const int64_t t = ok ? *stage_tile(s) : 0;
-    if (ok && t >= tp.ntiles) {  // sentinel: hand it to the store warp and stop
+    if (ok && t >= tp.ntiles) {  // sentinel: hand it to the copy warp and stop
       __syncwarp();
       if (lane == 0) mbar_arrive(done0 + 8 * s);
       break;
@@ -617,7 +652,7 @@ __global__ void __launch_bounds__(kTmaThreads, ROPE_TMA_MIN_CTAS)
         }
       }
     }
-    if (!ok) {  // the producer, the store warp and the other consumer warps also give up
+    if (!ok) {  // the copy and gather warps and the other consumer warps also give up
       timed_out = true;
       break;
     }
