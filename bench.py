@@ -315,6 +315,7 @@ def gpu_arm(args, rank, world, local_rank):
     for k in range(args.warmup):
         step.launch(k % len(step.xs), sh)
     torch.cuda.synchronize()
+    kernel_family = rp.last_kernel()  # what the variant chose for this workload
 
     sampler = ClockSampler(local_rank if "CUDA_VISIBLE_DEVICES" not in os.environ else
                            os.environ["CUDA_VISIBLE_DEVICES"].split(",")[local_rank])
@@ -374,10 +375,9 @@ def gpu_arm(args, rank, world, local_rank):
             },
             "roofline": {
                 "bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
-                "frac": round(achieved / peak, 4), "traffic": profiled_traffic("rope_rows_kernel", w.name),
+                "frac": round(achieved / peak, 4), "traffic": profiled_traffic(kernel_family, w.name),
                 "peak_source": peak_src,
-                "kernel": "rope_tma_kernel<half,half-split,rank3,cache2d> (the automatic variant for "
-                          "X >= 8 MiB on the 128-bit path)",
+                "kernel": f"{kernel_family} (variant {args.variant}: the one kernel of the step)",
                 "kernel_us": round(kern_ms * 1e3, 3),
                 "frac_of_nominal_8tbs": round(achieved / 8000.0, 4),
             },

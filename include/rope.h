@@ -213,9 +213,11 @@ rope_status rope_cache_build(rope_dtype dtype, const float* inv_freq, int32_t ha
 
 /*
  * Kernel variant selection (process-wide; default ROPE_VARIANT_AUTO).
- *   ROPE_VARIANT_AUTO  the 128-bit vector path of a large enough X goes
- *                      through the TMA pipeline (shared-memory stage ring);
- *                      everything else through the SIMT kernels.
+ *   ROPE_VARIANT_AUTO  M-RoPE and partial rotation (rotary_embedding_dim <
+ *                      head size) on the 128-bit vector path with X of at
+ *                      least 8 MiB go through the TMA pipeline (shared-memory
+ *                      stage ring); everything else, full-rotation RoPE
+ *                      included, through the SIMT kernels (faster there).
  *   ROPE_VARIANT_SIMT  always the SIMT kernels.
  *   ROPE_VARIANT_TMA   the TMA pipeline whenever the shape allows it (vector
  *                      path, head size <= 256 elements), whatever its size.
@@ -267,6 +269,14 @@ const char* rope_status_string(rope_status status);
 /* Message describing the last failed call on the calling thread ("" if none).
    Valid until the next call into the library on this thread. */
 const char* rope_last_error(void);
+
+/* Kernel family that the last call on the calling thread which launched work
+   used: "rope_rows_kernel" (SIMT), "rope_tma_kernel" (TMA pipeline),
+   "rope_fused_kernel" or "rope_cache_build_kernel"; "" before the first
+   launch. Calls that fail or launch nothing (empty X) leave it unchanged.
+   A diagnostic for profilers and benchmarks: the pages have no counterpart.
+   The string is static; never free it. */
+const char* rope_last_kernel(void);
 
 #ifdef __cplusplus
 }

@@ -56,8 +56,10 @@ SIGNATURES = {
     "rope_get_variant": [],
     "rope_status_string": [_i32],
     "rope_last_error": [],
+    "rope_last_kernel": [],
 }
-_RESTYPES = {"rope_status_string": ctypes.c_char_p, "rope_last_error": ctypes.c_char_p}
+_RESTYPES = {"rope_status_string": ctypes.c_char_p, "rope_last_error": ctypes.c_char_p,
+             "rope_last_kernel": ctypes.c_char_p}
 
 
 class RopeError(RuntimeError):
@@ -304,6 +306,11 @@ def set_variant(name):
 def get_variant():
     code = load_library().rope_get_variant()
     return {v: k for k, v in VARIANTS.items()}[code]
+
+
+def last_kernel():
+    """Kernel family the calling thread's last launching call used ("" before any)."""
+    return load_library().rope_last_kernel().decode()
 
 
 class variant:

@@ -63,6 +63,7 @@ using namespace rope_gb300;
 namespace {
 
 thread_local std::string g_last_error;
+thread_local const char* g_last_kernel = "";
 std::atomic<int> g_variant{ROPE_VARIANT_AUTO};
 
 rope_status fail(rope_status st, const char* fmt, ...) {
@@ -277,14 +278,24 @@ EncodeTiledFn encode_tiled() {
   return fn;
 }
 
-bool tma_eligible(const Geom& g, int es, bool vec) {
+// The automatic choice, from measurements on GB300 (kernel and chained step
+// times of both paths over rank 3/4, both pairings, fp16/fp32, full and
+// partial rotation, 34 MB to 545 MB): the TMA pipeline wins where the SIMT
+// kernels do extra work per element -- partial rotation (its consumers never
+// touch the tail; 17-36 % faster) and M-RoPE (the three streams' merge runs
+// once per tile column; 1.9x) -- and loses on full rotation (SIMT 2-8 %
+// faster at rank 3, 36-127 % at rank 4), where a SIMT thread's 128-bit loads
+// already keep enough bytes in flight.
+bool tma_eligible(const Geom& g, int es, bool vec, bool mrope) {
   const int variant = g_variant.load(std::memory_order_relaxed);
   if (variant == ROPE_VARIANT_SIMT) return false;
   if (!vec || g.H > 256) return false;
   const int64_t nP = g.h / (16 / es);
   if (nP < 1 || nP > kTmaConsumers) return false;
   if (g.ntok > INT32_MAX || g.N > INT32_MAX || g.S > INT32_MAX || g.B > INT32_MAX) return false;
-  if (variant == ROPE_VARIANT_AUTO && g.numel * es < (int64_t)ROPE_TMA_MIN_BYTES) return false;
+  if (variant == ROPE_VARIANT_AUTO &&
+      (g.numel * es < (int64_t)ROPE_TMA_MIN_BYTES || (!mrope && g.rd == g.H)))
+    return false;
   return encode_tiled() != nullptr;
 }
 
@@ -425,13 +436,16 @@ rope_status launch_tma(const void* fn, TmaLaunch* T, KParams* kp, rope_stream_t 
   void* args[] = {kp, &T->tp, &T->mx, &T->my};
   cudaError_t e = launch_pdl(fn, T->L.grid, T->L.block, T->L.smem, stream, args);
   if (e != cudaSuccess) return cuda_fail(e, "TMA kernel launch");
+  g_last_kernel = "rope_tma_kernel";
   return ROPE_OK;
 }
 
-rope_status launch(const void* fn, const Launch& L, KParams* kp, rope_stream_t stream) {
+rope_status launch(const void* fn, const Launch& L, KParams* kp, rope_stream_t stream,
+                   const char* family = "rope_rows_kernel") {
   void* args[] = {kp};
   cudaError_t e = launch_pdl(fn, L.grid, L.block, L.smem, stream, args);
   if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
+  g_last_kernel = family;
   return ROPE_OK;
 }
 
@@ -543,7 +557,7 @@ rope_status mrope_common(rope_dtype dtype, int32_t x_rank, const int64_t* x_shap
   kp.scale_is_one = scale == 1.0f;
   kp.cache_rows = cache_rows;
   for (int64_t i = 0; i < g.h; ++i) kp.smap[i >> 4] |= (uint32_t)map[i] << ((i & 15) * 2);
-  if (tma_eligible(g, es, vec)) {
+  if (tma_eligible(g, es, vec, true)) {
     const void* tfn = tma_kernel(dtype, interleaved != 0, x_rank == 4, Coef::kMRope);
     TmaLaunch T;
     const rope_status ts = plan_tma(g, es, x_rank, 3, tfn, x, y, &kp, &T);
@@ -624,7 +638,7 @@ rope_status rope_apply(rope_dtype dtype, int32_t x_rank, const int64_t* x_shape,
   kp.scale_is_one = 1;
   kp.cache_rows = rows;
   kp.sched = static_cast<unsigned long long*>(scratch);
-  if (tma_eligible(g, es, vec)) {
+  if (tma_eligible(g, es, vec, false)) {
     const void* tfn = tma_kernel(dtype, interleaved != 0, x_rank == 4, mode);
     TmaLaunch T;
     const rope_status ts = plan_tma(g, es, x_rank, 1, tfn, x, y, &kp, &T);
@@ -707,7 +721,7 @@ rope_status rope_apply_fused(rope_dtype dtype, int32_t x_rank, const int64_t* x_
   kp.scale = attention_scaling;
   Launch L;
   ROPE_TRY(plan(g, es, vec, fn, true, &kp, &L));
-  return launch(fn, L, &kp, stream);
+  return launch(fn, L, &kp, stream, "rope_fused_kernel");
 }
 
 rope_status rope_cache_build(rope_dtype dtype, const float* inv_freq, int32_t half, int64_t rows,
@@ -732,6 +746,7 @@ rope_status rope_cache_build(rope_dtype dtype, const float* inv_freq, int32_t ha
   void* args[] = {&inv_freq, &half, &rows, &attention_scaling, &cos_out, &sin_out};
   cudaError_t e = launch_pdl(fn, dim3((unsigned)blocks), dim3(256), 0, stream, args);
   if (e != cudaSuccess) return cuda_fail(e, "rope_cache_build launch");
+  g_last_kernel = "rope_cache_build_kernel";
   return ROPE_OK;
 }
 
@@ -744,6 +759,8 @@ rope_status rope_set_variant(rope_variant variant) {
 }
 
 rope_variant rope_get_variant(void) { return (rope_variant)g_variant.load(std::memory_order_relaxed); }
+
+const char* rope_last_kernel(void) { return g_last_kernel; }
 
 const char* rope_status_string(rope_status status) {
   switch (status) {

@@ -29,7 +29,7 @@ def test_header_declares_the_abi():
     fns = declared_functions()
     for name in ("rope_apply", "mrope_apply", "mrope_apply_stream_map", "mrope_stream_map",
                  "rope_apply_fused", "rope_cache_build", "rope_status_string", "rope_last_error",
-                 "rope_set_variant", "rope_get_variant"):
+                 "rope_set_variant", "rope_get_variant", "rope_last_kernel", "rope_apply_no_alloc"):
         assert name in fns
 
 

@@ -296,6 +296,43 @@ def test_dynamic_schedule_back_to_back_and_shared_scratch(lib, orc, cuda, torch_
     assert not scratch.any()
 
 
+def test_automatic_variant_choice(lib, orc, cuda, torch_mod):
+    """The automatic choice: full-rotation RoPE runs the SIMT kernel at any size;
+    partial rotation of a large X and M-RoPE of a large X run the TMA pipeline;
+    small X always runs SIMT. Every choice still matches the oracle."""
+    torch = torch_mod
+    rng = np.random.default_rng(37)
+    B, S, N, H = 2, 1024, 32, 128                 # 16 MiB of float16: above the pipeline's threshold
+    x = rng.standard_normal((B, S, N * H)).astype(np.float16)
+    R = 4096
+    pos = rng.integers(0, R, (B, S))
+    xd, pd = _dev(x, torch, cuda), _dev(pos, torch, cuda)
+    cases = [(0, "rope_rows_kernel"), (64, "rope_tma_kernel")]
+    tables = {}
+    with lib.variant("auto"):
+        for rd, family in cases:
+            h = (rd or H) // 2
+            cos, sin = orc.cache_build(wl.inv_freq(10000.0, rd or H, h), R, np.float16)
+            tables[rd] = (_dev(cos, torch, cuda), _dev(sin, torch, cuda))
+            y = lib.rope_apply(xd, *tables[rd], pd, num_heads=N, rotary_embedding_dim=rd)
+            assert lib.last_kernel() == family, (rd, lib.last_kernel())
+            torch.cuda.synchronize()
+            y_ref, _ = orc.rope(x, cos, sin, pos, 0, rd, N)
+            compare(_host(y), y_ref, x, 3, N, rope_passthrough_mask(x.shape, 3, N, rd, pos, R))
+        cos, sin = orc.cache_build(wl.inv_freq(10000.0, H, H // 2), R, np.float16)
+        pos3 = rng.integers(0, R, (3, B, S))
+        y = lib.mrope_apply(xd, _dev(cos, torch, cuda), _dev(sin, torch, cuda), _dev(pos3, torch, cuda),
+                            (16, 24, 24), mrope_layout=1, num_heads=N)
+        assert lib.last_kernel() == "rope_tma_kernel"
+        torch.cuda.synchronize()
+        y_ref, _ = orc.mrope(x, cos, sin, pos3, (16, 24, 24), 1, 1.0, 0, 0, N)
+        smap = orc.mrope_stream_map((16, 24, 24), 1, H // 2)
+        compare(_host(y), y_ref, x, 3, N, mrope_passthrough_mask(x.shape, 3, N, 0, pos3, R, smap, 0))
+        small = xd[:, :64].contiguous()           # 1 MiB: SIMT whatever the rotation
+        lib.rope_apply(small, *tables[64], pd[:, :64].contiguous(), num_heads=N, rotary_embedding_dim=64)
+        assert lib.last_kernel() == "rope_rows_kernel"
+
+
 # ---------------------------------------------------------------------------
 # MRotaryEmbedding
 # ---------------------------------------------------------------------------
