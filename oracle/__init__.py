@@ -17,4 +17,5 @@ from .oracle import (  # noqa: F401
     mrope_stream_map,
     rope,
     rope_fused,
+    rope_qkv,
 )

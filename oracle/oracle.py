@@ -54,8 +54,10 @@ def _load():
                                          f32, vp, _i64p]
             lib.oracle_rope_fused.argtypes = [i32, i32, _i64p, i64, i32, i64, vp, vp, f32, vp, vp]
             lib.oracle_cache_build.argtypes = [i32, vp, i64, i64, f32, vp, vp]
+            lib.oracle_rope_qkv.argtypes = [i32, i64, i64, i64, i64, i64, i32, i64, vp, vp, vp, vp, vp, i64,
+                                            vp, vp, vp, vp, vp, vp, i64, _i64p, _i64p]
             for name in ("oracle_rope", "oracle_mrope_stream_map", "oracle_mrope_map", "oracle_mrope",
-                         "oracle_rope_fused", "oracle_cache_build"):
+                         "oracle_rope_fused", "oracle_cache_build", "oracle_rope_qkv"):
                 getattr(lib, name).restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -190,3 +192,40 @@ def cache_build(inv_freq, rows, dtype=np.float16, attention_scaling=1.0):
     if rc:
         raise ValueError("oracle_cache_build: malformed arguments")
     return cos, sin
+
+
+def rope_qkv(query, cos, sin, position_ids=None, *, num_heads, kv_num_heads, key=None, value=None,
+             interleaved=0, rotary_embedding_dim=0, k_cache=None, v_cache=None, past_seq_lens=None):
+    """Q and K rotation with grouped-query heads and the optional cache append.
+
+    query is (B, S, Nq*H), or packed (B, S, (Nq + 2*Nkv)*H) when key and value
+    are None. With k_cache/v_cache (B, Nkv, max_len, H) the caches are copied,
+    the new rows written and the copies returned. Returns
+    (q_out, k_out or None, k_cache or None, v_cache or None, n_oor, n_skip).
+    """
+    lib = _load()
+    q = _c(query)
+    B, S, hidden = q.shape
+    packed = key is None and value is None
+    Ntot = num_heads + (2 * kv_num_heads if packed else 0)
+    H = hidden // Ntot
+    k = None if key is None else _c(key, q.dtype)
+    v = None if value is None else _c(value, q.dtype)
+    cos = _c(cos, q.dtype)
+    sin = _c(sin, q.dtype)
+    pos = None if position_ids is None else _c(position_ids, np.int64)
+    past = None if past_seq_lens is None else _c(past_seq_lens, np.int32)
+    q_out = np.empty((B, S, num_heads * H), dtype=q.dtype)
+    cache = k_cache is not None
+    k_out = None if cache else np.empty((B, S, kv_num_heads * H), dtype=q.dtype)
+    kc = None if k_cache is None else np.array(k_cache, dtype=q.dtype, copy=True, order="C")
+    vc = None if v_cache is None else np.array(v_cache, dtype=q.dtype, copy=True, order="C")
+    max_len = kc.shape[2] if cache else 0
+    n_oor, n_skip = ctypes.c_int64(0), ctypes.c_int64(0)
+    rc = lib.oracle_rope_qkv(_dt(q), B, S, int(num_heads), int(kv_num_heads), H, int(interleaved),
+                             int(rotary_embedding_dim), _ptr(q), _ptr(k), _ptr(v), _ptr(cos), _ptr(sin),
+                             int(cos.shape[0]), _ptr(pos), _ptr(past), _ptr(q_out), _ptr(k_out), _ptr(kc),
+                             _ptr(vc), int(max_len), ctypes.byref(n_oor), ctypes.byref(n_skip))
+    if rc:
+        raise ValueError("oracle_rope_qkv: malformed arguments")
+    return q_out, k_out, kc, vc, n_oor.value, n_skip.value

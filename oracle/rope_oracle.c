@@ -450,3 +450,102 @@ int oracle_cache_build(int dt, const float* inv_freq, int64_t half, int64_t rows
     }
   return 0;
 }
+
+/* ------------------------------------------------------------------------ */
+/* Q and K rotation for grouped-query attention, with the optional key/     */
+/* value cache append.                                                      */
+/* [SA] Description: grouped-query heads, separate or packed [Q|K|V] input, */
+/* partial or full rotary embedding in NeoX or interleaved layout; the past */
+/* key and value tensors are updated in place.                              */
+/* [SA] Inputs: query (B, S, Nq*H), or packed (B, S, (Nq + 2*Nkv)*H) when   */
+/* key and value are omitted; key and value (B, S, Nkv*H); past_key and     */
+/* past_value (B, Nkv, max_cache_sequence_length, H).                       */
+/* [SA] Attributes: do_rotary rotates Q, and K before it enters the cache;  */
+/* kv_num_heads divides num_heads.                                          */
+/* [PR] Verification and Qwen3 Architecture: RoPE is applied to both the Q  */
+/* and the K path of every layer, and GQA has fewer K/V heads than Q heads. */
+/* Readings:                                                                */
+/*  - every Q and K head is rotated exactly as oracle_rope rotates one head */
+/*    of a rank-3 X: same tables, positions, pairing, rotary width,         */
+/*    pass-through tail, and an out-of-range position copies the token's    */
+/*    heads through;                                                        */
+/*  - cache mode (k_cache given): new token s of batch b goes to cache row  */
+/*    past[b] + s of both caches (rotated K, V unchanged); rows outside the */
+/*    new tokens are left as they are; a token whose row falls outside      */
+/*    [0, max_len) is not stored (counted in *n_skip);                      */
+/*  - without position_ids the position of token s is past[b] + s, or s    */
+/*    when past is NULL (the new tokens follow the cached ones);            */
+/*  - without a cache the rotated K goes to k_out (B, S, Nkv*H) and V is    */
+/*    not touched.                                                          */
+/* Returns 0, or 1 on a malformed argument set.                             */
+/* ------------------------------------------------------------------------ */
+static void rope_one_head(int dt, int interleaved, int64_t H, int64_t rd, const void* x, int64_t xb,
+                          void* y, int64_t yb, const void* cos_t, const void* sin_t, int64_t crow,
+                          int valid) {
+  int64_t half = rd / 2;
+  if (!valid) {
+    for (int64_t j = 0; j < H; ++j) cp(dt, x, xb + j, y, yb + j);
+    return;
+  }
+  for (int64_t i = 0; i < half; ++i) {
+    int64_t j0, j1;
+    pair_elems(interleaved, half, i, &j0, &j1);
+    rotate_store(dt, y, yb + j0, yb + j1, ld(dt, x, xb + j0), ld(dt, x, xb + j1),
+                 ld(dt, cos_t, crow + i), ld(dt, sin_t, crow + i));
+  }
+  for (int64_t j = rd; j < H; ++j) cp(dt, x, xb + j, y, yb + j);
+}
+
+int oracle_rope_qkv(int dt, int64_t B, int64_t S, int64_t Nq, int64_t Nkv, int64_t H,
+                    int interleaved, int64_t rotary_dim, const void* q, const void* k,
+                    const void* v, const void* cos_t, const void* sin_t, int64_t cache_rows,
+                    const int64_t* pos, const int32_t* past, void* q_out, void* k_out,
+                    void* k_cache, void* v_cache, int64_t max_len, int64_t* n_oor,
+                    int64_t* n_skip) {
+  if (B < 0 || S < 0 || Nq < 1 || Nkv < 1 || Nq % Nkv || H < 2 || H % 2) return 1;
+  int64_t rd = rotary_dim ? rotary_dim : H;
+  if (rd % 2 || rd > H || rd <= 0) return 1;
+  int packed = (k == NULL && v == NULL);
+  int cache = (k_cache != NULL);
+  if (cache && (v_cache == NULL || past == NULL || max_len < 1)) return 1;
+  if (!cache && k_out == NULL) return 1;
+  if (!packed && (k == NULL || (cache && v == NULL))) return 1;
+  int64_t half = rd / 2;
+  int64_t Ntot = Nq + 2 * Nkv;
+  int64_t oor = 0, skip = 0;
+  for (int64_t b = 0; b < B; ++b) {
+    for (int64_t s = 0; s < S; ++s) {
+      int64_t tok = b * S + s;
+      int64_t p = pos ? pos[tok] : (past ? (int64_t)past[b] + s : s);
+      int valid = (p >= 0 && p < cache_rows);
+      if (!valid) ++oor;
+      int64_t crow = p * half;
+      for (int64_t n = 0; n < Nq; ++n) {
+        int64_t src = packed ? (tok * Ntot + n) * H : (tok * Nq + n) * H;
+        rope_one_head(dt, interleaved, H, rd, q, src, q_out, (tok * Nq + n) * H, cos_t, sin_t, crow,
+                      valid);
+      }
+      int64_t row = cache ? (int64_t)past[b] + s : 0;
+      int store = !cache || (row >= 0 && row < max_len);
+      if (cache && !store) ++skip;
+      for (int64_t n = 0; n < Nkv; ++n) {
+        const void* ks = packed ? q : k;
+        int64_t ksrc = packed ? (tok * Ntot + Nq + n) * H : (tok * Nkv + n) * H;
+        if (!cache) {
+          rope_one_head(dt, interleaved, H, rd, ks, ksrc, k_out, (tok * Nkv + n) * H, cos_t, sin_t,
+                        crow, valid);
+          continue;
+        }
+        if (!store) continue;
+        int64_t dst = ((b * Nkv + n) * max_len + row) * H;
+        rope_one_head(dt, interleaved, H, rd, ks, ksrc, k_cache, dst, cos_t, sin_t, crow, valid);
+        const void* vs = packed ? q : v;
+        int64_t vsrc = packed ? (tok * Ntot + Nq + Nkv + n) * H : (tok * Nkv + n) * H;
+        for (int64_t j = 0; j < H; ++j) cp(dt, vs, vsrc + j, v_cache, dst + j);
+      }
+    }
+  }
+  if (n_oor) *n_oor = oor;
+  if (n_skip) *n_skip = skip;
+  return 0;
+}

@@ -33,6 +33,15 @@ MUTATIONS = {
     "per_token_row_shifted": ("crow = tok * half;", "crow = tok * half + (tok > 0);"),
     "sin_from_cos_table": ("double sn = ld(dt, sin_t, crow + i);", "double sn = ld(dt, cos_t, crow + i);"),
     "scaling_dropped": ("float cs = c32 * scaling;", "float cs = c32;"),
+    "qkv_cache_row_ignores_past": ("int64_t row = cache ? (int64_t)past[b] + s : 0;",
+                                   "int64_t row = cache ? s : 0;"),
+    "qkv_value_read_from_key": ("const void* vs = packed ? q : v;", "const void* vs = packed ? q : k;"),
+    "qkv_packed_value_offset": ("int64_t vsrc = packed ? (tok * Ntot + Nq + Nkv + n) * H",
+                                "int64_t vsrc = packed ? (tok * Ntot + Nq + n) * H"),
+    "qkv_implicit_position_ignores_past": ("int64_t p = pos ? pos[tok] : (past ? (int64_t)past[b] + s : s);",
+                                           "int64_t p = pos ? pos[tok] : s;"),
+    "qkv_value_rotated": ("for (int64_t j = 0; j < H; ++j) cp(dt, vs, vsrc + j, v_cache, dst + j);",
+                          "rope_one_head(dt, interleaved, H, rd, vs, vsrc, v_cache, dst, cos_t, sin_t, crow, valid);"),
 }
 
 

@@ -491,3 +491,144 @@ def test_workload_inputs_are_seeded():
     text = ~oor[:, 0, :1000].any(axis=0)
     assert np.all(pos[0, 0, :1000][text] == pos[1, 0, :1000][text])
     assert np.all(pos[0, 0, :1000][text] == pos[2, 0, :1000][text])
+
+
+# --------------------------------------------------------------------------
+# Q and K rotation with grouped-query heads and the key/value cache append
+# (SparseAttention README: Description, Inputs, Attributes do_rotary and
+# kv_num_heads; Qwen3 fusion PR: Verification, Qwen3 Architecture)
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("dtype", [np.float32, np.float16])
+def test_qkv_hand_example_gqa(orc, dtype):
+    g = _gold("qkv_hand_example.json")
+    Nq, Nkv, H = g["num_heads"], g["kv_num_heads"], g["head_size"]
+    q = np.array(g["q"], dtype=dtype).reshape(1, 1, Nq * H)
+    k = np.array(g["k"], dtype=dtype).reshape(1, 1, Nkv * H)
+    v = np.array(g["v"], dtype=dtype).reshape(1, 1, Nkv * H)
+    cos, sin = np.array(g["cos"], dtype=dtype), np.array(g["sin"], dtype=dtype)
+    L = g["max_cache_len"]
+    fill = np.full((1, Nkv, L, H), g["cache_fill"], dtype=dtype)
+    past = np.array([g["past"]], dtype=np.int32)
+    for case in g["cases"]:
+        inter = case["interleaved"]
+        # explicit position, no cache
+        qo, ko, _, _, n_oor, _ = orc.rope_qkv(q, cos, sin, np.array([[g["past"]]]), num_heads=Nq,
+                                              kv_num_heads=Nkv, key=k, interleaved=inter)
+        assert n_oor == 0
+        assert qo.ravel().tolist() == case["q_out"] and ko.ravel().tolist() == case["k_out"]
+        # cache mode, implicit position past + s, separate and packed inputs
+        packed = np.concatenate([q, k, v], axis=-1)
+        for kw in (dict(key=k, value=v), dict()):
+            src = q if kw else packed
+            qo, ko, kc, vc, _, n_skip = orc.rope_qkv(src, cos, sin, None, num_heads=Nq, kv_num_heads=Nkv,
+                                                    interleaved=inter, k_cache=fill, v_cache=fill,
+                                                    past_seq_lens=past, **kw)
+            assert ko is None and n_skip == 0
+            assert qo.ravel().tolist() == case["q_out"]
+            assert kc[0, 0, 1].tolist() == case["k_out"] and vc[0, 0, 1].tolist() == g["v"]
+            for row in (0, 2):
+                assert (kc[0, 0, row] == g["cache_fill"]).all() and (vc[0, 0, row] == g["cache_fill"]).all()
+
+
+def _qkv_inputs(rng, dtype, B=3, S=5, Nq=6, Nkv=2, H=16, R=40):
+    q = rng.standard_normal((B, S, Nq * H)).astype(dtype)
+    k = rng.standard_normal((B, S, Nkv * H)).astype(dtype)
+    v = rng.standard_normal((B, S, Nkv * H)).astype(dtype)
+    theta = rng.uniform(-np.pi, np.pi, (R, H // 2))
+    return q, k, v, np.cos(theta).astype(dtype), np.sin(theta).astype(dtype)
+
+
+def test_qkv_complex_multiply_closed_form(orc):
+    """Every Q and K pair is (x0 + i x1) * (c + i s) at its token's position, rounded once."""
+    rng = np.random.default_rng(71)
+    B, S, Nq, Nkv, H, R = 3, 5, 6, 2, 16, 40
+    q, k, v, cos, sin = _qkv_inputs(rng, np.float32)
+    pos = rng.integers(0, R, (B, S))
+    h = H // 2
+    for inter in (0, 1):
+        qo, ko, _, _, _, _ = orc.rope_qkv(q, cos, sin, pos, num_heads=Nq, kv_num_heads=Nkv, key=k,
+                                          interleaved=inter)
+        i0 = np.arange(h) * 2 if inter else np.arange(h)
+        i1 = i0 + 1 if inter else i0 + h
+        w = cos.astype(np.float64)[pos] + 1j * sin.astype(np.float64)[pos]   # (B, S, h)
+        for x, y, n in ((q, qo, Nq), (k, ko, Nkv)):
+            xr, yr = x.reshape(B, S, n, H), y.reshape(B, S, n, H)
+            z = xr[..., i0].astype(np.complex128) + 1j * xr[..., i1].astype(np.complex128)
+            prod = z * w[:, :, None, :]
+            assert np.array_equal(yr[..., i0], prod.real.astype(np.float32))
+            assert np.array_equal(yr[..., i1], prod.imag.astype(np.float32))
+
+
+def test_qkv_cache_rows_values_and_skips(orc):
+    """Cache mode: token s of batch b lands in row past[b] + s of both caches (K rotated at
+    position past[b] + s, V bit-exact); every other row keeps its bits; rows past the end
+    are skipped and counted."""
+    rng = np.random.default_rng(72)
+    B, S, Nq, Nkv, H, L = 3, 5, 6, 2, 16, 9
+    for dtype in (np.float16, np.float32):
+        q, k, v, cos, sin = _qkv_inputs(rng, dtype)
+        kc0 = rng.standard_normal((B, Nkv, L, H)).astype(dtype)
+        vc0 = rng.standard_normal((B, Nkv, L, H)).astype(dtype)
+        past = np.array([0, 4, 6], dtype=np.int32)            # batch 2: rows 6..10, two past the end
+        qo, ko, kc, vc, n_oor, n_skip = orc.rope_qkv(q, cos, sin, None, num_heads=Nq, kv_num_heads=Nkv,
+                                                    key=k, value=v, k_cache=kc0, v_cache=vc0,
+                                                    past_seq_lens=past)
+        assert ko is None and n_oor == 0 and n_skip == 2
+        # the rotation the cache must hold: explicit positions past[b] + s, no cache
+        pos = past[:, None].astype(np.int64) + np.arange(S)[None, :]
+        qe, ke, _, _, _, _ = orc.rope_qkv(q, cos, sin, pos, num_heads=Nq, kv_num_heads=Nkv, key=k)
+        assert np.array_equal(qo.view(np.uint8), qe.view(np.uint8))
+        kexp, vexp = kc0.copy(), vc0.copy()
+        ke4, v4 = ke.reshape(B, S, Nkv, H), v.reshape(B, S, Nkv, H)
+        for b in range(B):
+            for s in range(S):
+                r = past[b] + s
+                if r < L:
+                    kexp[b, :, r] = ke4[b, s]
+                    vexp[b, :, r] = v4[b, s]
+        assert np.array_equal(kc.view(np.uint8), kexp.view(np.uint8))
+        assert np.array_equal(vc.view(np.uint8), vexp.view(np.uint8))
+
+
+def test_qkv_reduces_to_rotary_embedding_and_packed_equals_separate(orc):
+    """Q and K each come out exactly as RotaryEmbedding rotates a rank-3 X of those heads
+    (including out-of-range positions and a partial rotary width), and a packed [Q|K|V]
+    input gives the same bits as separate tensors."""
+    rng = np.random.default_rng(73)
+    B, S, Nq, Nkv, H, R = 2, 7, 8, 2, 16, 30
+    for dtype in (np.float16, np.float32):
+        q, k, v, cos8, sin8 = _qkv_inputs(rng, dtype, B, S, Nq, Nkv, H, R)
+        for rd in (0, 8):
+            cos, sin = (cos8, sin8) if rd == 0 else (cos8[:, :rd // 2].copy(), sin8[:, :rd // 2].copy())
+            pos = rng.integers(0, R, (B, S))
+            pos[0, 3], pos[1, 0] = R, -1
+            for inter in (0, 1):
+                qo, ko, _, _, n_oor, _ = orc.rope_qkv(q, cos, sin, pos, num_heads=Nq, kv_num_heads=Nkv,
+                                                      key=k, interleaved=inter, rotary_embedding_dim=rd)
+                assert n_oor == 2
+                yq, _ = orc.rope(q, cos, sin, pos, inter, rd, Nq)
+                yk, _ = orc.rope(k, cos, sin, pos, inter, rd, Nkv)
+                assert np.array_equal(qo.view(np.uint8), yq.view(np.uint8))
+                assert np.array_equal(ko.view(np.uint8), yk.view(np.uint8))
+                packed = np.concatenate([q, k, v], axis=-1)
+                qp, kp, _, _, _, _ = orc.rope_qkv(packed, cos, sin, pos, num_heads=Nq, kv_num_heads=Nkv,
+                                                  interleaved=inter, rotary_embedding_dim=rd)
+                assert np.array_equal(qp.view(np.uint8), qo.view(np.uint8))
+                assert np.array_equal(kp.view(np.uint8), ko.view(np.uint8))
+
+
+def test_qkv_implicit_positions_follow_the_cache(orc):
+    """Without position_ids, token s takes position past[b] + s (s without past)."""
+    rng = np.random.default_rng(74)
+    B, S, Nq, Nkv, H = 3, 4, 4, 4, 8
+    q, k, v, cos, sin = _qkv_inputs(rng, np.float32, B, S, Nq, Nkv, H, 20)
+    past = np.array([0, 3, 9], dtype=np.int32)
+    a = orc.rope_qkv(q, cos, sin, None, num_heads=Nq, kv_num_heads=Nkv, key=k, past_seq_lens=past)
+    b = orc.rope_qkv(q, cos, sin, past[:, None] + np.arange(S)[None, :], num_heads=Nq, kv_num_heads=Nkv,
+                     key=k)
+    c = orc.rope_qkv(q, cos, sin, None, num_heads=Nq, kv_num_heads=Nkv, key=k)
+    d = orc.rope_qkv(q, cos, sin, np.tile(np.arange(S), (B, 1)), num_heads=Nq, kv_num_heads=Nkv, key=k)
+    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+    assert np.array_equal(c[0], d[0]) and np.array_equal(c[1], d[1])
+    assert not np.array_equal(a[0], c[0])
