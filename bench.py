@@ -37,8 +37,8 @@ from rotary_position_embedding_gb300 import workloads as wl  # noqa: E402
 L2_BYTES = 129 * 2 ** 20
 FALLBACK_HBM_GBS = 6800.0
 METRIC = "RoPE achieved HBM GB/s and Gelem/s, fp16, as % of GB300 HBM roofline"
-KERNEL_SOURCES = ["rope_kernels.cuh", "rope_tma.cuh", "rope_internal.h", "rope_api.cu", "k_rope.cu",
-                  "k_mrope.cu", "k_fused.cu", "k_tma.cu"]
+KERNEL_SOURCES = ["rope_kernels.cuh", "rope_tma.cuh", "rope_qkv.cuh", "rope_internal.h", "rope_api.cu",
+                  "k_rope.cu", "k_mrope.cu", "k_fused.cu", "k_tma.cu", "k_qkv.cu"]
 
 
 def parse_args():
@@ -187,6 +187,61 @@ class ClockSampler:
 # GPU arm
 # ---------------------------------------------------------------------------
 
+class QKVStep:
+    """Q/K rotation with the cache append: one rope_apply_qkv call per step (packed
+    [Q|K|V] in, Q out, rotated K and V into the caches at rows past[b] + s).
+
+    With fused=False a step is what a caller does without that entry point:
+    split Q and K out of the packed tensor (torch copies), rope_apply on each,
+    and scatter K and V into the caches (torch indexing).
+    """
+
+    def __init__(self, rp, torch, w, device, n_sets, shard=0):
+        self.w, self.torch, self.rp = w, torch, rp
+        self.lib = rp.load_library()
+        inp = wl.make_inputs(w, shard=shard)
+        tdt = torch.float16 if w.dtype == "float16" else torch.float32
+        x0 = torch.from_numpy(inp["x"]).to(device)
+        self.xs = [x0] + [x0.clone() for _ in range(n_sets - 1)]
+        B, S, H = w.batch, w.seq, w.head_size
+        self.Nq, self.Nkv = w.num_heads, w.extra["kv_num_heads"]
+        self.qo = [torch.empty((B, S, self.Nq * H), dtype=tdt, device=device) for _ in range(n_sets)]
+        L = w.extra["max_len"]
+        self.kc = torch.zeros((B, self.Nkv, L, H), dtype=tdt, device=device)
+        self.vc = torch.zeros_like(self.kc)
+        self.past = torch.from_numpy(inp["past_seq_lens"]).to(device)
+        inv = torch.from_numpy(inp["inv_freq"]).to(device)
+        self.cos, self.sin = rp.rope_cache_build(inv, w.cache_rows, tdt)
+        self.code = 1 if w.dtype == "float16" else 0
+        self.H = H
+        # unfused path: positions past[b] + s and the (b, row) scatter indices
+        s_idx = torch.arange(S, device=device, dtype=torch.int64)[None, :]
+        self.pos = (self.past.to(torch.int64)[:, None] + s_idx).contiguous()
+        self.bi = torch.arange(B, device=device)[:, None].expand(B, S)
+        self.ri = self.pos
+        torch.cuda.synchronize()
+
+    def launch(self, k, stream, fused=True):
+        w, lib = self.w, self.lib
+        if fused:
+            return lib.rope_apply_qkv(self.code, w.batch, w.seq, self.Nq, self.Nkv, self.H,
+                                      ctypes.c_void_p(self.xs[k].data_ptr()), None, None,
+                                      ctypes.c_void_p(self.cos.data_ptr()), ctypes.c_void_p(self.sin.data_ptr()),
+                                      w.cache_rows, None, ctypes.c_void_p(self.past.data_ptr()), 0, 0,
+                                      ctypes.c_void_p(self.qo[k].data_ptr()), None,
+                                      ctypes.c_void_p(self.kc.data_ptr()), ctypes.c_void_p(self.vc.data_ptr()),
+                                      w.extra["max_len"], None, stream)
+        B, S, H, Nq, Nkv = w.batch, w.seq, self.H, self.Nq, self.Nkv
+        x = self.xs[k].view(B, S, Nq + 2 * Nkv, H)
+        q = x[:, :, :Nq].reshape(B, S, Nq * H).contiguous()
+        kk = x[:, :, Nq:Nq + Nkv].reshape(B, S, Nkv * H).contiguous()
+        self.rp.rope_apply(q, self.cos, self.sin, self.pos, num_heads=Nq, out=self.qo[k])
+        kr = self.rp.rope_apply(kk, self.cos, self.sin, self.pos, num_heads=Nkv)
+        self.kc[self.bi, :, self.ri] = kr.view(B, S, Nkv, H)
+        self.vc[self.bi, :, self.ri] = x[:, :, Nq + Nkv:]
+        return 0
+
+
 class Step:
     """One workload pass through the C ABI with pre-marshalled ctypes arguments."""
 
@@ -259,6 +314,12 @@ class Step:
             raise RuntimeError(f"{w.name}: status {st}: {lib.rope_last_error().decode()}")
 
 
+def make_step(rp, torch, w, device, n_sets, shard=0, dynamic=False):
+    if w.kind == "qkv":
+        return QKVStep(rp, torch, w, device, n_sets, shard=shard)
+    return Step(rp, torch, w, device, n_sets, shard=shard, dynamic=dynamic)
+
+
 def n_buffer_sets(w):
     per_set = 2 * w.numel * np.dtype(w.dtype).itemsize
     return max(2, math.ceil(4 * L2_BYTES / per_set))
@@ -311,7 +372,7 @@ def gpu_arm(args, rank, world, local_rank):
     stream = torch.cuda.current_stream(device)
     sh = ctypes.c_void_p(stream.cuda_stream)
     nbytes = wl.algorithmic_bytes(w)
-    step = Step(rp, torch, w, device, n_buffer_sets(w), shard=rank, dynamic=args.schedule == "dynamic")
+    step = make_step(rp, torch, w, device, n_buffer_sets(w), shard=rank, dynamic=args.schedule == "dynamic")
     for k in range(args.warmup):
         step.launch(k % len(step.xs), sh)
     torch.cuda.synchronize()
@@ -325,7 +386,7 @@ def gpu_arm(args, rank, world, local_rank):
         torch.distributed.barrier()
     torch.cuda.synchronize()
     t0 = time.time()
-    total_ms, kern = time_steps(torch, step, args.steps, sh, sample_every=8)
+    total_ms, kern = time_steps(torch, step, args.steps, sh, fused=w.kind == "qkv", sample_every=8)
     t1 = time.time()
     if world > 1:
         torch.distributed.barrier()
@@ -341,7 +402,7 @@ def gpu_arm(args, rank, world, local_rank):
     out = None
     if rank == 0:
         rows = {} if (args.no_rows or args.quick) else measure_rows(args, torch, rp, device, peak)
-        e2e = None if args.quick else measure_e2e(args, torch, step, sh, nbytes)
+        e2e = None if (args.quick or w.kind == "qkv") else measure_e2e(args, torch, step, sh, nbytes)
         cpu = cpu_baseline(args, w) if (world == 1 and not args.quick) else None
         out = {
             "metric": METRIC,
@@ -403,14 +464,16 @@ def measure_rows(args, torch, rp, device, peak):
         variants = [("cached", False, "auto"), ("cached", False, "simt")]
         if w.kind == "fused":
             variants = [("fused", True, "auto"), ("cached", False, "auto")]
-        step = Step(rp, torch, w, device, n_buffer_sets(w))
+        if w.kind == "qkv":
+            variants = [("fused", True, "auto"), ("unfused", False, "auto")]
+        step = make_step(rp, torch, w, device, n_buffer_sets(w))
         for label, fused, variant in variants:
             rp.set_variant(variant)
             for k in range(20):
                 step.launch(k % len(step.xs), sh, fused)
             total_ms, kern = time_steps(torch, step, args.row_steps, sh, fused)
             rp.set_variant(prev)
-            nbytes = wl.algorithmic_bytes(w, cached=not fused)
+            nbytes = wl.algorithmic_bytes(w, cached=not fused or w.kind == "qkv")
             kern_ms = float(np.median(kern))
             gbs = nbytes / (kern_ms * 1e-3) / 1e9
             key = f"{name}:{label}:{variant}"
@@ -520,10 +583,18 @@ class OracleStep:
             self.sin = self.sin.reshape(w.batch, w.seq, w.half)[:nb, :s_keep]
         self.inv = inp["inv_freq"]
         self.bytes = wl.algorithmic_bytes(w) * self.tokens / w.tokens
+        if w.kind == "qkv":
+            self.past = inp["past_seq_lens"][:nb]
+            shape = (nb, w.extra["kv_num_heads"], w.extra["max_len"], w.head_size)
+            self.kc, self.vc = np.zeros(shape, dtype), np.zeros(shape, dtype)
 
     def run(self):
         w, o = self.w, self.oracle
-        if w.kind == "mrope":
+        if w.kind == "qkv":
+            o.rope_qkv(self.x, self.cos, self.sin, None, num_heads=w.num_heads,
+                       kv_num_heads=w.extra["kv_num_heads"], k_cache=self.kc, v_cache=self.vc,
+                       past_seq_lens=self.past)
+        elif w.kind == "mrope":
             o.mrope(self.x, self.cos, self.sin, self.pos, w.mrope_section, w.mrope_layout, w.scale,
                     w.interleaved, w.rotary_embedding_dim, self.nh)
         else:

@@ -199,6 +199,62 @@ rope_status rope_apply_fused(rope_dtype dtype, int32_t x_rank, const int64_t* x_
                              int32_t num_heads, rope_stream_t stream);
 
 /*
+ * rope_apply_qkv -- Q and K rotation for grouped-query attention in one
+ * launch, optionally appending the rotated K and the V of the new tokens to a
+ * key/value cache ([SparseAttention README, Description: grouped-query heads,
+ * separate or packed [Q|K|V] input, rotary embedding in NeoX or interleaved
+ * layout, past key/value updated in place; Inputs: query, key, value,
+ * past_key, past_value; Attributes: do_rotary rotates Q and K before K enters
+ * the cache, kv_num_heads divides num_heads] and [Qwen3 fusion pull request,
+ * Verification and Qwen3 Architecture: RoPE on both the Q and the K path,
+ * fewer K/V heads than Q heads]).
+ *
+ * Every Q and K head is rotated exactly as rope_apply rotates one head of a
+ * rank-3 X: tables (cache_rows, rd/2) gathered at the token's position,
+ * pairing `interleaved`, rotary width `rotary_embedding_dim` (0 = head_size)
+ * with the tail copied, and a position outside [0, cache_rows) copies the
+ * token's Q and K heads through (status bit 0). V heads are copied bit for
+ * bit.
+ *
+ * query     device T (B, S, num_heads*H), or packed (B, S, (num_heads +
+ *           2*kv_num_heads)*H) = [Q|K|V] per token when key and value are
+ *           both NULL.
+ * key       device T (B, S, kv_num_heads*H), or NULL (packed).
+ * value     device T (B, S, kv_num_heads*H): required in cache mode unless
+ *           packed; must be NULL without a cache (V is not touched then).
+ * position_ids  device int64 (B, S), or NULL: token s of batch b then takes
+ *           position past_seq_lens[b] + s (s when past_seq_lens is NULL).
+ * past_seq_lens device int32 (B): rows each batch's cache already holds;
+ *           required in cache mode, optional otherwise (positions only).
+ * q_out     device T (B, S, num_heads*H); may equal query unless packed.
+ * Without a cache (k_cache NULL): k_out is device T (B, S, kv_num_heads*H)
+ *           (may equal key) and v_cache must be NULL.
+ * Cache mode (k_cache non-NULL): k_out must be NULL; k_cache and v_cache are
+ *           device T (B, kv_num_heads, max_cache_len, H), updated in place:
+ *           token s of batch b goes to row past_seq_lens[b] + s of both
+ *           (rotated K, V as given); no other row is written. A token whose
+ *           row falls outside [0, max_cache_len) is not stored (status bit 2).
+ * status_flags  NULL or a device int32 the kernel ORs bits into (never
+ *           clears): bit 0 a position out of range, bit 2 a cache row out of
+ *           range.
+ * All buffers are caller-owned; nothing is allocated. Buffers other than the
+ * aliases named above must not overlap. ROPE_ERR_INVALID_ARG (before any
+ * launch) for: num_heads or kv_num_heads < 1, kv_num_heads not dividing
+ * num_heads, an odd or < 2 head_size, a bad rotary width, interleaved not 0/1,
+ * an inconsistent set of key/value/k_out/k_cache/v_cache/past_seq_lens,
+ * max_cache_len < 1 in cache mode, negative cache_rows, NULL or misaligned
+ * pointers, or element counts beyond 2^63. B*S == 0 launches nothing.
+ */
+rope_status rope_apply_qkv(rope_dtype dtype, int64_t batch, int64_t seq, int32_t num_heads,
+                           int32_t kv_num_heads, int64_t head_size, const void* query,
+                           const void* key, const void* value, const void* cos_cache,
+                           const void* sin_cache, int64_t cache_rows, const int64_t* position_ids,
+                           const int32_t* past_seq_lens, int32_t interleaved,
+                           int32_t rotary_embedding_dim, void* q_out, void* k_out, void* k_cache,
+                           void* v_cache, int64_t max_cache_len, int32_t* status_flags,
+                           rope_stream_t stream);
+
+/*
  * rope_cache_build -- the (rows, half) cos and sin tables of rope_apply's
  * 2-D cache: row p holds the coefficients rope_apply_fused computes for
  * position p ([Qwen3 fusion pull request, Medium Issues 4: cos(freqs) *
@@ -272,7 +328,7 @@ const char* rope_last_error(void);
 
 /* Kernel family that the last call on the calling thread which launched work
    used: "rope_rows_kernel" (SIMT), "rope_tma_kernel" (TMA pipeline),
-   "rope_fused_kernel" or "rope_cache_build_kernel"; "" before the first
+   "rope_fused_kernel", "rope_qkv_kernel" or "rope_cache_build_kernel"; "" before the first
    launch. Calls that fail or launch nothing (empty X) leave it unchanged.
    A diagnostic for profilers and benchmarks: the pages have no counterpart.
    The string is static; never free it. */

@@ -50,6 +50,8 @@ SIGNATURES = {
     "mrope_stream_map": [_i32p, _i32, _i32, _u8p],
     "rope_apply_fused": [_i32, _i32, _i64p, _vp, _vp, _vp, _f32, _vp, _i32, _i32, _i32, _vp],
     "rope_cache_build": [_i32, _vp, _i32, _i64, _f32, _vp, _vp, _vp],
+    "rope_apply_qkv": [_i32, _i64, _i64, _i32, _i32, _i64, _vp, _vp, _vp, _vp, _vp, _i64, _vp, _vp, _i32,
+                       _i32, _vp, _vp, _vp, _vp, _i64, _vp, _vp],
     "rope_apply_no_alloc": [_i32, _i32, _i64p, _vp, _vp, _i32, _i64p, _vp, _vp, _vp, _i32, _i32, _i32, _vp,
                             _vp],
     "rope_set_variant": [_i32],
@@ -272,6 +274,50 @@ def rope_apply_fused(x, inv_freq, position_ids, *, attention_scaling=1.0, interl
                                   int(rotary_embedding_dim), int(num_heads), _stream(x, stream))
     _check("rope_apply_fused", st)
     return y
+
+
+def rope_apply_qkv(query, cos_cache, sin_cache, position_ids=None, *, num_heads, kv_num_heads, key=None,
+                   value=None, interleaved=0, rotary_embedding_dim=0, k_cache=None, v_cache=None,
+                   past_seq_lens=None, q_out=None, k_out=None, status=None, stream=None):
+    """Q and K rotation for grouped-query attention in one launch, optionally
+    appending rotated K and V to (B, kv_num_heads, max_len, H) caches in place.
+
+    query is (B, S, num_heads*H), or packed [Q|K|V] (B, S, (num_heads +
+    2*kv_num_heads)*H) when key and value are None. Returns (q_out, k_out);
+    k_out is None in cache mode (the caches hold the result).
+    """
+    import torch
+
+    lib = load_library()
+    _cuda("query", query)
+    for name, t in (("key", key), ("value", value), ("k_cache", k_cache), ("v_cache", v_cache),
+                    ("cos_cache", cos_cache), ("sin_cache", sin_cache)):
+        _cuda(name, t, query.dtype)
+    _cuda("position_ids", position_ids, torch.int64)
+    _cuda("past_seq_lens", past_seq_lens, torch.int32)
+    if query.dim() != 3:
+        raise ValueError("query must be (B, S, hidden)")
+    B, S, hidden = query.shape
+    packed = key is None and value is None
+    rows_per_tok = num_heads + (2 * kv_num_heads if packed else 0)
+    if hidden % rows_per_tok:
+        raise ValueError(f"query hidden size {hidden} is not a multiple of {rows_per_tok} heads")
+    H = hidden // rows_per_tok
+    if q_out is None:
+        q_out = torch.empty((B, S, num_heads * H), dtype=query.dtype, device=query.device)
+    cache = k_cache is not None
+    if not cache and k_out is None:
+        k_out = torch.empty((B, S, kv_num_heads * H), dtype=query.dtype, device=query.device)
+    max_len = k_cache.shape[2] if cache else 0
+    with torch.cuda.device(query.device):
+        st = lib.rope_apply_qkv(_dtype_code(query), B, S, int(num_heads), int(kv_num_heads), H, _ptr(query),
+                                _ptr(key), _ptr(value), _ptr(cos_cache), _ptr(sin_cache),
+                                int(cos_cache.shape[0]), _ptr(position_ids), _ptr(past_seq_lens),
+                                int(interleaved), int(rotary_embedding_dim), _ptr(q_out), _ptr(k_out),
+                                _ptr(k_cache), _ptr(v_cache), int(max_len), _ptr(status),
+                                _stream(query, stream))
+    _check("rope_apply_qkv", st)
+    return q_out, (None if cache else k_out)
 
 
 def rope_cache_build(inv_freq, rows, dtype=None, *, attention_scaling=1.0, cos_out=None, sin_out=None,

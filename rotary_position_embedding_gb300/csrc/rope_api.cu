@@ -724,6 +724,118 @@ rope_status rope_apply_fused(rope_dtype dtype, int32_t x_rank, const int64_t* x_
   return launch(fn, L, &kp, stream, "rope_fused_kernel");
 }
 
+rope_status rope_apply_qkv(rope_dtype dtype, int64_t batch, int64_t seq, int32_t num_heads,
+                           int32_t kv_num_heads, int64_t head_size, const void* query,
+                           const void* key, const void* value, const void* cos_cache,
+                           const void* sin_cache, int64_t cache_rows, const int64_t* position_ids,
+                           const int32_t* past_seq_lens, int32_t interleaved,
+                           int32_t rotary_embedding_dim, void* q_out, void* k_out, void* k_cache,
+                           void* v_cache, int64_t max_cache_len, int32_t* status_flags,
+                           rope_stream_t stream) {
+  g_last_error.clear();
+  ROPE_TRY(check_dtype(dtype));
+  if (batch < 0 || seq < 0) return fail(ROPE_ERR_INVALID_ARG, "batch and seq must be >= 0");
+  if (num_heads < 1 || kv_num_heads < 1)
+    return fail(ROPE_ERR_INVALID_ARG, "num_heads (%d) and kv_num_heads (%d) must be >= 1", num_heads,
+                kv_num_heads);
+  if (num_heads % kv_num_heads)
+    return fail(ROPE_ERR_INVALID_ARG, "kv_num_heads %d does not divide num_heads %d", kv_num_heads,
+                num_heads);
+  if (head_size < 2) return fail(ROPE_ERR_INVALID_ARG, "head_size must be >= 2");
+  if (interleaved != 0 && interleaved != 1)
+    return fail(ROPE_ERR_INVALID_ARG, "interleaved must be 0 or 1 (got %d)", interleaved);
+  if (cache_rows < 0) return fail(ROPE_ERR_INVALID_ARG, "cache_rows is negative");
+  {
+    Geom w;
+    w.H = head_size;
+    ROPE_TRY(rotary_width(rotary_embedding_dim, /*odd_head_ok=*/false, &w));
+  }
+  // No tokens: nothing to launch (zero-size tensors may come with NULL pointers).
+  if (batch == 0 || seq == 0) return ROPE_OK;
+  const bool packed = !key && !value;
+  const bool cache = k_cache != nullptr;
+  if (!packed && !key) return fail(ROPE_ERR_INVALID_ARG, "value given without key");
+  if (cache) {
+    if (!v_cache || !past_seq_lens)
+      return fail(ROPE_ERR_INVALID_ARG, "k_cache needs v_cache and past_seq_lens");
+    if (!packed && !value) return fail(ROPE_ERR_INVALID_ARG, "k_cache needs value (or a packed query)");
+    if (k_out) return fail(ROPE_ERR_INVALID_ARG, "k_out must be NULL when k_cache is given");
+    if (max_cache_len < 1) return fail(ROPE_ERR_INVALID_ARG, "max_cache_len must be >= 1");
+  } else {
+    if (v_cache) return fail(ROPE_ERR_INVALID_ARG, "v_cache given without k_cache");
+    if (!k_out) return fail(ROPE_ERR_INVALID_ARG, "k_out is NULL (and no k_cache)");
+    if (value && !packed) return fail(ROPE_ERR_INVALID_ARG, "value is only read in cache mode");
+  }
+  // The kernel's view: a rank-3 X of Nq + Nkv (+ Nkv) head rows per token.
+  Geom g;
+  g.B = batch;
+  g.S = seq;
+  g.N = (int64_t)num_heads + kv_num_heads + (cache ? kv_num_heads : 0);
+  g.H = head_size;
+  int64_t t, packed_numel;
+  if (!mul_ok(g.B, g.S, &g.ntok) || !mul_ok(g.ntok, g.N, &t) || !mul_ok(t, g.H, &g.numel) ||
+      !mul_ok(g.ntok, (int64_t)num_heads + 2 * kv_num_heads, &t) || !mul_ok(t, g.H, &packed_numel))
+    return fail(ROPE_ERR_INVALID_ARG, "Q/K/V have more than 2^63 elements");
+  if (cache) {
+    int64_t c;
+    if (!mul_ok(g.B, kv_num_heads, &t) || !mul_ok(t, max_cache_len, &c) || !mul_ok(c, g.H, &t))
+      return fail(ROPE_ERR_INVALID_ARG, "the caches have more than 2^63 elements");
+  }
+  ROPE_TRY(rotary_width(rotary_embedding_dim, /*odd_head_ok=*/false, &g));
+  if (g.numel == 0) return ROPE_OK;
+  const int es = elem_size(dtype);
+  ROPE_TRY(check_elem_ptr(query, "query", es));
+  ROPE_TRY(check_elem_ptr(q_out, "q_out", es));
+  if (packed && q_out == query)
+    return fail(ROPE_ERR_INVALID_ARG, "q_out cannot alias a packed query (different row strides)");
+  if (!packed) ROPE_TRY(check_elem_ptr(key, "key", es));
+  if (value) ROPE_TRY(check_elem_ptr(value, "value", es));
+  if (k_out) ROPE_TRY(check_elem_ptr(k_out, "k_out", es));
+  if (cache) {
+    ROPE_TRY(check_elem_ptr(k_cache, "k_cache", es));
+    ROPE_TRY(check_elem_ptr(v_cache, "v_cache", es));
+  }
+  if (cache_rows > 0) {
+    ROPE_TRY(check_elem_ptr(cos_cache, "cos_cache", es));
+    ROPE_TRY(check_elem_ptr(sin_cache, "sin_cache", es));
+  }
+  if (position_ids) ROPE_TRY(check_elem_ptr(position_ids, "position_ids", 8));
+  if (past_seq_lens) ROPE_TRY(check_elem_ptr(past_seq_lens, "past_seq_lens", 4));
+  if (status_flags && !aligned(status_flags, 4)) return fail(ROPE_ERR_INVALID_ARG, "status_flags is misaligned");
+
+  const bool vec = vector_ok(g, es, {query, key, value, q_out, k_out, k_cache, v_cache, cos_cache, sin_cache});
+  const void* fn = qkv_kernel(dtype, vec, interleaved != 0, position_ids == nullptr);
+  KParams kp;
+  memset(&kp, 0, sizeof(kp));
+  kp.x = query;
+  kp.y = q_out;
+  kp.cos = cos_cache;
+  kp.sin = sin_cache;
+  kp.pos = position_ids;
+  kp.oor_flag = status_flags;
+  kp.cache_rows = cache_rows;
+  QKVParams qa;
+  memset(&qa, 0, sizeof(qa));
+  qa.k = key;
+  qa.v = value;
+  qa.k_out = k_out;
+  qa.k_cache = k_cache;
+  qa.v_cache = v_cache;
+  qa.past = past_seq_lens;
+  qa.max_len = max_cache_len;
+  qa.Nq = num_heads;
+  qa.Nkv = kv_num_heads;
+  qa.packed = packed;
+  qa.cache = cache;
+  Launch L;
+  ROPE_TRY(plan(g, es, vec, fn, false, &kp, &L));
+  void* args[] = {&kp, &qa};
+  cudaError_t e = launch_pdl(fn, L.grid, L.block, L.smem, stream, args);
+  if (e != cudaSuccess) return cuda_fail(e, "rope_apply_qkv launch");
+  g_last_kernel = "rope_qkv_kernel";
+  return ROPE_OK;
+}
+
 rope_status rope_cache_build(rope_dtype dtype, const float* inv_freq, int32_t half, int64_t rows,
                              float attention_scaling, void* cos_out, void* sin_out,
                              rope_stream_t stream) {

@@ -51,12 +51,30 @@ struct KParams {
   unsigned long long* sched;  // TMA path: tile counter pair for the dynamic schedule, or null
 };
 
+// Q/K rotation with the key/value cache append (rope_qkv_kernel): the routing
+// that KParams does not carry. KParams.x is the query (or packed [Q|K|V])
+// tensor, KParams.y the rotated Q, KParams.N = Nq + Nkv (+ Nkv in cache mode).
+struct QKVParams {
+  const void* k;         // key (B, S, Nkv*H), or null when x is packed
+  const void* v;         // value (B, S, Nkv*H), or null
+  void* k_out;           // no-cache mode: rotated K (B, S, Nkv*H)
+  void* k_cache;         // cache mode: (B, Nkv, max_len, H); token s of batch b -> row past[b] + s
+  void* v_cache;
+  const int32_t* past;   // (B) rows already cached (implicit positions, cache rows), or null
+  int64_t max_len;
+  int32_t Nq, Nkv;
+  int32_t packed;        // x is packed [Q|K|V]
+  int32_t cache;         // cache mode
+};
+
 // Kernel entry points for cudaLaunchKernel / occupancy queries. `vec` selects
 // the 128-bit vector path. Return nullptr for unsupported combinations.
 const void* rope_kernel_cached(int dtype, bool vec, bool interleaved, bool rank4, Coef mode);
 const void* rope_kernel_mrope(int dtype, bool vec, bool interleaved, bool rank4);
 const void* fused_kernel(int dtype, bool vec, bool interleaved, bool rank4);
 const void* cache_build_kernel(int dtype);
+// rope_qkv_kernel instance; its launch takes (KParams, QKVParams).
+const void* qkv_kernel(int dtype, bool vec, bool interleaved, bool implicit_pos);
 // Records the message rope_last_error() returns on the calling thread.
 void set_last_error(const char* msg);
 

@@ -1,0 +1,136 @@
+// Q and K rotation for grouped-query attention in one launch, with the
+// optional key/value cache append.
+//
+// Definitions followed (web pages, by title and section):
+//  - "com.microsoft.SparseAttention" README: Description (grouped-query heads,
+//    separate or packed [Q|K|V] input, partial or full rotary embedding in
+//    NeoX or interleaved layout, past key/value updated in place), Inputs
+//    (query (B, S, Nq*H) or packed (B, S, (Nq + 2*Nkv)*H); key, value
+//    (B, S, Nkv*H); past_key, past_value (B, Nkv, max_cache_len, H)),
+//    Attributes (do_rotary: Q and K rotated before K enters the cache;
+//    kv_num_heads divides num_heads).
+//  - onnxruntime pull request "Add RotaryEmbedding fusion for Qwen3 on-the-fly
+//    RoPE patterns": Verification and Qwen3 Architecture (RoPE on both the Q
+//    and the K path, GQA with fewer K/V heads).
+// Every Q and K head is rotated exactly as rope_rows_kernel rotates one head of
+// a rank-3 X (same tables, positions, pairing, rotary width and out-of-range
+// rule); V heads are copied bit for bit.
+#pragma once
+
+#include "rope_kernels.cuh"
+
+namespace rope_gb300 {
+
+__device__ __forceinline__ void flag_cache_row(int32_t* flag) {
+  if (flag) atomicOr(flag, 4);
+}
+
+// The kernel sees each token as N = Nq + Nkv (+ Nkv in cache mode) head rows
+// in the packed [Q|K|V] order and keeps rope_rows_kernel's fixed thread roles
+// (KParams): a thread's head row -- and with it its source, its destination and
+// whether it rotates -- never changes, so the routing is decided once.
+template <class T, int V, bool INTER, bool IMPLICIT>
+__global__ void __launch_bounds__(kMaxRowThreads) rope_qkv_kernel(const KParams p, const QKVParams a) {
+  using VT = VecT<T, V>;
+  using bits = typename Elem<T>::bits;
+  const int tid = threadIdx.x;
+  const int per_tok = p.NG * p.Ublk;
+  const int slot = tid / per_tok;
+  const int r = tid - slot * per_tok;
+  const int ng = r / p.Ublk;
+  const int k0 = r - ng * p.Ublk;
+  const int64_t n = (int64_t)blockIdx.y * p.NG + ng;
+  pdl_launch_dependents();
+  pdl_wait();
+  if (slot >= p.TTs || n >= p.N) return;  // no barrier below
+
+  // role 0: Q head, 1: K head, 2: V head (cache mode only)
+  const int role = n < a.Nq ? 0 : (n < a.Nq + a.Nkv ? 1 : 2);
+  const int64_t hd = role == 0 ? n : (role == 1 ? n - a.Nq : n - a.Nq - a.Nkv);
+  const int64_t H = p.H;
+  const bits* src;
+  int64_t sstride;  // elements between the rows of consecutive tokens
+  if (a.packed) {
+    src = static_cast<const bits*>(p.x) + n * H;
+    sstride = (int64_t)(a.Nq + 2 * a.Nkv) * H;
+  } else {
+    const void* base = role == 0 ? p.x : (role == 1 ? a.k : a.v);
+    src = static_cast<const bits*>(base) + hd * H;
+    sstride = (int64_t)(role == 0 ? a.Nq : a.Nkv) * H;
+  }
+  const bool to_cache = role != 0 && a.cache;
+  bits* dst;
+  int64_t dstride = 0;
+  if (role == 0) {
+    dst = static_cast<bits*>(p.y) + hd * H;
+    dstride = (int64_t)a.Nq * H;
+  } else if (!a.cache) {
+    dst = static_cast<bits*>(a.k_out) + hd * H;
+    dstride = (int64_t)a.Nkv * H;
+  } else {
+    dst = static_cast<bits*>(role == 1 ? a.k_cache : a.v_cache) + hd * a.max_len * H;
+  }
+  const bool rotates = role != 2;
+  const bits* __restrict__ cosb = static_cast<const bits*>(p.cos);
+  const bits* __restrict__ sinb = static_cast<const bits*>(p.sin);
+
+  int64_t tok = (int64_t)blockIdx.x * p.TTs + slot;
+  int64_t b = tok / p.S;
+  int64_t s = tok - b * p.S;
+  for (; tok < p.ntok; tok += p.step_tok) {
+    const int64_t past = a.past ? (int64_t)__ldg(a.past + b) : 0;
+    const bits* xr = src + tok * sstride;
+    bits* yr = nullptr;
+    if (to_cache) {
+      const int64_t row = past + s;
+      if (row >= 0 && row < a.max_len) {
+        yr = dst + (b * a.Nkv * a.max_len + row) * H;
+      } else if (role == 1 && hd == 0 && k0 == 0) {
+        flag_cache_row(p.oor_flag);
+      }
+    } else {
+      yr = dst + tok * dstride;
+    }
+    if (yr) {
+      bool valid = false;
+      int64_t crow = 0;
+      if (rotates) {
+        const int64_t pp = IMPLICIT ? past + s : __ldg(p.pos + tok);
+        valid = (uint64_t)pp < (uint64_t)p.cache_rows;
+        if (!valid && role == 0 && hd == 0 && k0 == 0) flag_oor(p.oor_flag);
+        crow = pp * p.h;
+      }
+      for (int k = k0; k < p.U; k += p.Ublk) {
+        if (k >= p.nP) {  // tail unit: bit copy
+          const int off = p.rd + (k - p.nP) * V;
+          st_stream(reinterpret_cast<VT*>(yr + off), ld_stream(reinterpret_cast<const VT*>(xr + off)));
+          continue;
+        }
+        int oa, ob;
+        unit_offsets<V, INTER>(k, p.h, oa, ob);
+        const VT xa = ld_stream(reinterpret_cast<const VT*>(xr + oa));
+        const VT xb = ld_stream(reinterpret_cast<const VT*>(xr + ob));
+        if (!valid) {  // V head, or an out-of-range position: copied through
+          st_stream(reinterpret_cast<VT*>(yr + oa), xa);
+          st_stream(reinterpret_cast<VT*>(yr + ob), xb);
+          continue;
+        }
+        const int oc = k * V;
+        const VT c = ld_shared_ro(reinterpret_cast<const VT*>(cosb + crow + oc));
+        const VT sn = ld_shared_ro(reinterpret_cast<const VT*>(sinb + crow + oc));
+        VT ya, yb;
+        rotate_unit<T, V, INTER>(xa, xb, c, sn, ya, yb);
+        st_stream(reinterpret_cast<VT*>(yr + oa), ya);
+        st_stream(reinterpret_cast<VT*>(yr + ob), yb);
+      }
+    }
+    s += p.step_s;
+    b += p.step_b;
+    if (s >= p.S) {
+      s -= p.S;
+      ++b;
+    }
+  }
+}
+
+}  // namespace rope_gb300

@@ -48,6 +48,8 @@ class Workload:
 
     @property
     def head_size(self):
+        if self.kind == "qkv":  # packed [Q|K|V] rows: num_heads + 2 * kv_num_heads per token
+            return self.shape[2] // (self.num_heads + 2 * self.extra["kv_num_heads"])
         return self.shape[2] // self.num_heads if self.rank == 3 else self.shape[3]
 
     @property
@@ -112,6 +114,17 @@ WORKLOADS = {
         name="mrope_r3_f16_layout1", kind="mrope", rank=3, shape=(2, 8192, 28 * 128), dtype="float16",
         num_heads=28, positions="mrope", cache_rows=32768, rope_base=10000.0, rope_dim=128,
         mrope_section=(16, 24, 24), mrope_layout=1, scale=1.0),
+    # Q/K rotation with the key/value cache append, Qwen3-8B attention shape
+    # (32 query heads, 8 key/value heads, head size 128), packed [Q|K|V] input,
+    # positions past[b] + s: a chunked prefill and a decode step.
+    "qkv_prefill_r3_f16": Workload(
+        name="qkv_prefill_r3_f16", kind="qkv", rank=3, shape=(4, 2048, (32 + 2 * 8) * 128), dtype="float16",
+        num_heads=32, positions="past", cache_rows=8192, rope_base=1.0e6, rope_dim=128,
+        extra={"kv_num_heads": 8, "max_len": 4096, "max_past": 2048}),
+    "qkv_decode_r3_f16": Workload(
+        name="qkv_decode_r3_f16", kind="qkv", rank=3, shape=(256, 1, (32 + 2 * 8) * 128), dtype="float16",
+        num_heads=32, positions="past", cache_rows=8192, rope_base=1.0e6, rope_dim=128,
+        extra={"kv_num_heads": 8, "max_len": 4096, "max_past": 4095}),
     "fused_decode_r3_f16": Workload(
         name="fused_decode_r3_f16", kind="fused", rank=3, shape=(256, 1, 40 * 128), dtype="float16",
         num_heads=40, positions="uniform", cache_rows=32768, rope_base=1.0e6, rope_dim=128,
@@ -196,10 +209,16 @@ def make_inputs(w: Workload, shard=0):
         pos = positions_uniform(B, S, w.cache_rows, seed=base + 1)
     elif w.positions == "mrope":
         pos = mrope_ids(B, S, w.cache_rows, seed=base + 1, oor_seed=base + 2)
+    elif w.positions == "past":  # implicit positions past[b] + s; past drawn here
+        pos = None
     else:
         raise ValueError(w.positions)
     inv = inv_freq(w.rope_base, w.rope_dim or w.rotary_dim, w.half)
-    return {"x": x, "position_ids": pos, "inv_freq": inv}
+    out = {"x": x, "position_ids": pos, "inv_freq": inv}
+    if w.kind == "qkv":
+        rng = np.random.default_rng(base + 1)
+        out["past_seq_lens"] = rng.integers(0, w.extra["max_past"] + 1, size=B).astype(np.int32)
+    return out
 
 
 def algorithmic_bytes(w: Workload, cached=True):
@@ -211,6 +230,10 @@ def algorithmic_bytes(w: Workload, cached=True):
     """
     esz = np.dtype(w.dtype).itemsize
     xy = 2 * w.numel * esz
+    if w.kind == "qkv":
+        # Q, K, V read once; Q out, K and V into the caches; one cos/sin row
+        # per token; the int32 past lengths (positions are implicit).
+        return xy + 2 * w.tokens * w.half * esz + 4 * w.batch
     npos = 3 if w.kind == "mrope" else (0 if w.positions == "none" else 1)
     pos = npos * w.tokens * 8
     if w.kind == "fused" and not cached:

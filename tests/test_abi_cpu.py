@@ -182,3 +182,61 @@ def test_stream_map_matches_oracle(lib, orc):
     with pytest.raises(lib.RopeError) as e:
         lib.mrope_stream_map((1, 2, 3), 0, 7)
     assert e.value.status == INVALID
+
+
+FAKE3 = ctypes.c_void_p(0x30000)
+FAKE4 = ctypes.c_void_p(0x40000)
+
+
+def _qkv(so, **kw):
+    a = dict(dtype=F16, B=2, S=4, nq=8, nkv=2, H=16, q=FAKE, k=FAKE2, v=None, cos=FAKE3, sin=FAKE3, rows=32,
+             pos=FAKE4, past=None, inter=0, rd=0, q_out=ctypes.c_void_p(0x50000),
+             k_out=ctypes.c_void_p(0x60000), kc=None, vc=None, max_len=0, flag=None, stream=None)
+    a.update(kw)
+    return so.rope_apply_qkv(a["dtype"], a["B"], a["S"], a["nq"], a["nkv"], a["H"], a["q"], a["k"], a["v"],
+                             a["cos"], a["sin"], a["rows"], a["pos"], a["past"], a["inter"], a["rd"],
+                             a["q_out"], a["k_out"], a["kc"], a["vc"], a["max_len"], a["flag"], a["stream"])
+
+
+CACHE = dict(v=ctypes.c_void_p(0x70000), k_out=None, kc=ctypes.c_void_p(0x80000), vc=ctypes.c_void_p(0x90000),
+             past=ctypes.c_void_p(0xa0000), max_len=64)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(dtype=99), UNSUPPORTED),
+    (dict(nkv=3), INVALID),                              # kv_num_heads must divide num_heads
+    (dict(nq=0), INVALID),
+    (dict(nkv=0), INVALID),
+    (dict(H=15), INVALID),                               # odd head size
+    (dict(H=0), INVALID),
+    (dict(inter=2), INVALID),
+    (dict(rd=18), INVALID),
+    (dict(rd=5), INVALID),
+    (dict(B=-1), INVALID),
+    (dict(rows=-1), INVALID),
+    (dict(k=None, v=ctypes.c_void_p(0x70000)), INVALID),  # value without key
+    (dict(v=ctypes.c_void_p(0x70000)), INVALID),         # value is only read in cache mode
+    (dict(k_out=None), INVALID),                         # no cache and no k_out
+    (dict(vc=ctypes.c_void_p(0x90000)), INVALID),        # v_cache without k_cache
+    (dict(CACHE, vc=None), INVALID),                     # k_cache without v_cache
+    (dict(CACHE, past=None), INVALID),                   # cache rows need past_seq_lens
+    (dict(CACHE, v=None), INVALID),                      # separate inputs need value in cache mode
+    (dict(CACHE, k_out=ctypes.c_void_p(0x60000)), INVALID),   # k_out and a cache
+    (dict(CACHE, max_len=0), INVALID),
+    (dict(k=None, q_out=FAKE), INVALID),                 # q_out aliasing a packed query
+    (dict(q=ctypes.c_void_p(0x10001)), INVALID),         # misaligned float16 pointer
+    (dict(pos=ctypes.c_void_p(0x40004)), INVALID),       # misaligned int64 pointer
+    (dict(CACHE, past=ctypes.c_void_p(0xa0002)), INVALID),   # misaligned int32 pointer
+    (dict(q_out=None), INVALID),
+])
+def test_rope_apply_qkv_rejects_before_launch(lib, kw, status):
+    so = lib.load_library()
+    st = _qkv(so, **kw)
+    assert st == status, so.rope_last_error().decode()
+    assert so.rope_last_error().decode() != ""
+
+
+def test_rope_apply_qkv_empty_launches_nothing(lib):
+    so = lib.load_library()
+    assert _qkv(so, S=0, q=None, k=None, q_out=None, k_out=ctypes.c_void_p(0x60000)) == OK
+    assert _qkv(so, B=0) == OK

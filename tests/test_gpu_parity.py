@@ -468,7 +468,7 @@ def test_cache_build_vs_oracle(lib, orc, cuda, torch_mod, dt, base, scaling):
 # Full-size workloads, launched exactly as the benchmark launches them
 # ---------------------------------------------------------------------------
 
-@pytest.mark.parametrize("name", list(wl.WORKLOADS))
+@pytest.mark.parametrize("name", [n for n, w in wl.WORKLOADS.items() if w.kind != "qkv"])
 def test_workload_full_size(lib, orc, cuda, torch_mod, name):
     torch = torch_mod
     w = wl.WORKLOADS[name]
