@@ -37,8 +37,14 @@ from rotary_position_embedding_gb300 import workloads as wl  # noqa: E402
 L2_BYTES = 129 * 2 ** 20
 FALLBACK_HBM_GBS = 6800.0
 METRIC = "RoPE achieved HBM GB/s and Gelem/s, fp16, as % of GB300 HBM roofline"
-KERNEL_SOURCES = ["rope_kernels.cuh", "rope_tma.cuh", "rope_qkv.cuh", "rope_internal.h", "rope_api.cu",
-                  "k_rope.cu", "k_mrope.cu", "k_fused.cu", "k_tma.cu", "k_qkv.cu"]
+# Device sources of each kernel family: a profiled DRAM figure is reported only
+# while the sources it was captured on are unchanged.
+KERNEL_SOURCES = {
+    "rope_rows_kernel": ["rope_kernels.cuh", "k_rope.cu", "k_mrope.cu"],
+    "rope_tma_kernel": ["rope_kernels.cuh", "rope_tma.cuh", "k_tma.cu"],
+    "rope_fused_kernel": ["rope_kernels.cuh", "k_fused.cu"],
+    "rope_qkv_kernel": ["rope_kernels.cuh", "rope_qkv.cuh", "k_qkv.cu"],
+}
 
 
 def parse_args():
@@ -86,9 +92,9 @@ def aggregate_throughput(nbytes, numel, steps, total_ms, world):
     return world * nbytes * steps / sec / 1e9, world * numel * steps / sec / 1e9
 
 
-def kernel_source_hash():
+def kernel_source_hash(family):
     h = hashlib.sha256()
-    for f in KERNEL_SOURCES:
+    for f in KERNEL_SOURCES[family]:
         with open(os.path.join(ROOT, "rotary_position_embedding_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -111,7 +117,7 @@ def profiled_traffic(kernel, workload):
         with open(p) as f:
             d = json.load(f)
         e = d[f"{kernel}:{workload}"]
-        if e.get("source_hash") == kernel_source_hash():
+        if e.get("source_hash") == kernel_source_hash(kernel):
             return e["dram_bytes_per_launch"]
     except Exception:
         pass

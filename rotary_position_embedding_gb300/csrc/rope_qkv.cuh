@@ -29,8 +29,16 @@ __device__ __forceinline__ void flag_cache_row(int32_t* flag) {
 // in the packed [Q|K|V] order and keeps rope_rows_kernel's fixed thread roles
 // (KParams): a thread's head row -- and with it its source, its destination and
 // whether it rotates -- never changes, so the routing is decided once.
+// Register cap. A token's 48 head rows (Qwen3-8B shape) make 384-thread CTAs;
+// uncapped the kernel takes 58 registers, so only 2 CTAs fit an SM. At 48
+// registers 3 fit (a few bytes of spills): the prefill workload runs 41.0 us
+// instead of 45.1 us (40 registers: 4 CTAs but heavier spills, 43.0 us).
+#ifndef ROPE_QKV_MAXNREG
+#define ROPE_QKV_MAXNREG 48
+#endif
+#define ROPE_QKV_BOUNDS __maxnreg__(ROPE_QKV_MAXNREG)
 template <class T, int V, bool INTER, bool IMPLICIT>
-__global__ void __launch_bounds__(kMaxRowThreads) rope_qkv_kernel(const KParams p, const QKVParams a) {
+__global__ void ROPE_QKV_BOUNDS rope_qkv_kernel(const KParams p, const QKVParams a) {
   using VT = VecT<T, V>;
   using bits = typename Elem<T>::bits;
   const int tid = threadIdx.x;
