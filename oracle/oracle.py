@@ -56,8 +56,12 @@ def _load():
             lib.oracle_cache_build.argtypes = [i32, vp, i64, i64, f32, vp, vp]
             lib.oracle_rope_qkv.argtypes = [i32, i64, i64, i64, i64, i64, i32, i64, vp, vp, vp, vp, vp, i64,
                                             vp, vp, vp, vp, vp, vp, i64, _i64p, _i64p]
+            lib.oracle_rope_qkv_rmsnorm.argtypes = [i32, i64, i64, i64, i64, i64, i32, i64, vp, vp, vp, vp, vp,
+                                                    ctypes.c_double, vp, vp, i64, vp, vp, vp, vp, vp, vp, i64,
+                                                    _i64p, _i64p]
             for name in ("oracle_rope", "oracle_mrope_stream_map", "oracle_mrope_map", "oracle_mrope",
-                         "oracle_rope_fused", "oracle_cache_build", "oracle_rope_qkv"):
+                         "oracle_rope_fused", "oracle_cache_build", "oracle_rope_qkv",
+                         "oracle_rope_qkv_rmsnorm"):
                 getattr(lib, name).restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -195,8 +199,11 @@ def cache_build(inv_freq, rows, dtype=np.float16, attention_scaling=1.0):
 
 
 def rope_qkv(query, cos, sin, position_ids=None, *, num_heads, kv_num_heads, key=None, value=None,
-             interleaved=0, rotary_embedding_dim=0, k_cache=None, v_cache=None, past_seq_lens=None):
-    """Q and K rotation with grouped-query heads and the optional cache append.
+             interleaved=0, rotary_embedding_dim=0, k_cache=None, v_cache=None, past_seq_lens=None,
+             q_norm_weight=None, k_norm_weight=None, epsilon=1e-6):
+    """Q and K rotation with grouped-query heads and the optional cache append;
+    with q_norm_weight and k_norm_weight (head-size vectors) each Q and K head
+    is RMS-normalised (epsilon) before the rotation.
 
     query is (B, S, Nq*H), or packed (B, S, (Nq + 2*Nkv)*H) when key and value
     are None. With k_cache/v_cache (B, Nkv, max_len, H) the caches are copied,
@@ -222,10 +229,19 @@ def rope_qkv(query, cos, sin, position_ids=None, *, num_heads, kv_num_heads, key
     vc = None if v_cache is None else np.array(v_cache, dtype=q.dtype, copy=True, order="C")
     max_len = kc.shape[2] if cache else 0
     n_oor, n_skip = ctypes.c_int64(0), ctypes.c_int64(0)
-    rc = lib.oracle_rope_qkv(_dt(q), B, S, int(num_heads), int(kv_num_heads), H, int(interleaved),
-                             int(rotary_embedding_dim), _ptr(q), _ptr(k), _ptr(v), _ptr(cos), _ptr(sin),
-                             int(cos.shape[0]), _ptr(pos), _ptr(past), _ptr(q_out), _ptr(k_out), _ptr(kc),
-                             _ptr(vc), int(max_len), ctypes.byref(n_oor), ctypes.byref(n_skip))
+    if q_norm_weight is None and k_norm_weight is None:
+        rc = lib.oracle_rope_qkv(_dt(q), B, S, int(num_heads), int(kv_num_heads), H, int(interleaved),
+                                 int(rotary_embedding_dim), _ptr(q), _ptr(k), _ptr(v), _ptr(cos), _ptr(sin),
+                                 int(cos.shape[0]), _ptr(pos), _ptr(past), _ptr(q_out), _ptr(k_out), _ptr(kc),
+                                 _ptr(vc), int(max_len), ctypes.byref(n_oor), ctypes.byref(n_skip))
+    else:
+        qw = _c(q_norm_weight, q.dtype)
+        kw = _c(k_norm_weight, q.dtype)
+        rc = lib.oracle_rope_qkv_rmsnorm(_dt(q), B, S, int(num_heads), int(kv_num_heads), H, int(interleaved),
+                                         int(rotary_embedding_dim), _ptr(q), _ptr(k), _ptr(v), _ptr(qw),
+                                         _ptr(kw), float(epsilon), _ptr(cos), _ptr(sin), int(cos.shape[0]),
+                                         _ptr(pos), _ptr(past), _ptr(q_out), _ptr(k_out), _ptr(kc), _ptr(vc),
+                                         int(max_len), ctypes.byref(n_oor), ctypes.byref(n_skip))
     if rc:
         raise ValueError("oracle_rope_qkv: malformed arguments")
     return q_out, k_out, kc, vc, n_oor.value, n_skip.value

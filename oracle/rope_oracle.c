@@ -41,6 +41,7 @@
  * page's own example applies).
  */
 #include <math.h>
+#include <stdlib.h>
 #include <stdint.h>
 #include <string.h>
 
@@ -496,12 +497,29 @@ static void rope_one_head(int dt, int interleaved, int64_t H, int64_t rd, const 
   for (int64_t j = rd; j < H; ++j) cp(dt, x, xb + j, y, yb + j);
 }
 
-int oracle_rope_qkv(int dt, int64_t B, int64_t S, int64_t Nq, int64_t Nkv, int64_t H,
-                    int interleaved, int64_t rotary_dim, const void* q, const void* k,
-                    const void* v, const void* cos_t, const void* sin_t, int64_t cache_rows,
-                    const int64_t* pos, const int32_t* past, void* q_out, void* k_out,
-                    void* k_cache, void* v_cache, int64_t max_len, int64_t* n_oor,
-                    int64_t* n_skip) {
+/* RMS normalisation of one head (H elements at x + xb) followed by the
+   per-channel weight, into z[0..H): z_j = T(w_j * T(x_j * r)) with
+   r = 1 / sqrt(mean_j(x_j^2) + eps), the mean and r in binary64. */
+static void rms_norm_head(int dt, const void* x, int64_t xb, int64_t H, const void* w, double eps,
+                          void* z) {
+  double ss = 0.0;
+  for (int64_t j = 0; j < H; ++j) {
+    double v = ld(dt, x, xb + j);
+    ss += v * v;
+  }
+  double r = 1.0 / sqrt(ss / (double)H + eps);
+  for (int64_t j = 0; j < H; ++j) {
+    double n = round_to(dt, ld(dt, x, xb + j) * r);
+    st(dt, z, j, n * ld(dt, w, j));
+  }
+}
+
+static int qkv_core(int dt, int64_t B, int64_t S, int64_t Nq, int64_t Nkv, int64_t H, int interleaved,
+                    int64_t rotary_dim, const void* q, const void* k, const void* v,
+                    const void* q_weight, const void* k_weight, double eps, const void* cos_t,
+                    const void* sin_t, int64_t cache_rows, const int64_t* pos, const int32_t* past,
+                    void* q_out, void* k_out, void* k_cache, void* v_cache, int64_t max_len,
+                    int64_t* n_oor, int64_t* n_skip) {
   if (B < 0 || S < 0 || Nq < 1 || Nkv < 1 || Nq % Nkv || H < 2 || H % 2) return 1;
   int64_t rd = rotary_dim ? rotary_dim : H;
   if (rd % 2 || rd > H || rd <= 0) return 1;
@@ -510,9 +528,14 @@ int oracle_rope_qkv(int dt, int64_t B, int64_t S, int64_t Nq, int64_t Nkv, int64
   if (cache && (v_cache == NULL || past == NULL || max_len < 1)) return 1;
   if (!cache && k_out == NULL) return 1;
   if (!packed && (k == NULL || (cache && v == NULL))) return 1;
+  int norm = (q_weight != NULL);
+  if (norm && (k_weight == NULL || !(eps >= 0))) return 1;
   int64_t half = rd / 2;
   int64_t Ntot = Nq + 2 * Nkv;
   int64_t oor = 0, skip = 0;
+  /* normalised head (rotation input) when RMSNorm comes first */
+  void* zq = norm ? malloc((size_t)H * 8) : NULL;
+  if (norm && zq == NULL) return 1;
   for (int64_t b = 0; b < B; ++b) {
     for (int64_t s = 0; s < S; ++s) {
       int64_t tok = b * S + s;
@@ -522,7 +545,13 @@ int oracle_rope_qkv(int dt, int64_t B, int64_t S, int64_t Nq, int64_t Nkv, int64
       int64_t crow = p * half;
       for (int64_t n = 0; n < Nq; ++n) {
         int64_t src = packed ? (tok * Ntot + n) * H : (tok * Nq + n) * H;
-        rope_one_head(dt, interleaved, H, rd, q, src, q_out, (tok * Nq + n) * H, cos_t, sin_t, crow,
+        const void* qs = q;
+        if (norm) {
+          rms_norm_head(dt, q, src, H, q_weight, eps, zq);
+          qs = zq;
+          src = 0;
+        }
+        rope_one_head(dt, interleaved, H, rd, qs, src, q_out, (tok * Nq + n) * H, cos_t, sin_t, crow,
                       valid);
       }
       int64_t row = cache ? (int64_t)past[b] + s : 0;
@@ -531,6 +560,11 @@ int oracle_rope_qkv(int dt, int64_t B, int64_t S, int64_t Nq, int64_t Nkv, int64
       for (int64_t n = 0; n < Nkv; ++n) {
         const void* ks = packed ? q : k;
         int64_t ksrc = packed ? (tok * Ntot + Nq + n) * H : (tok * Nkv + n) * H;
+        if (norm && (!cache || store)) {
+          rms_norm_head(dt, ks, ksrc, H, k_weight, eps, zq);
+          ks = zq;
+          ksrc = 0;
+        }
         if (!cache) {
           rope_one_head(dt, interleaved, H, rd, ks, ksrc, k_out, (tok * Nkv + n) * H, cos_t, sin_t,
                         crow, valid);
@@ -545,7 +579,45 @@ int oracle_rope_qkv(int dt, int64_t B, int64_t S, int64_t Nq, int64_t Nkv, int64
       }
     }
   }
+  free(zq);
   if (n_oor) *n_oor = oor;
   if (n_skip) *n_skip = skip;
   return 0;
+}
+
+int oracle_rope_qkv(int dt, int64_t B, int64_t S, int64_t Nq, int64_t Nkv, int64_t H,
+                    int interleaved, int64_t rotary_dim, const void* q, const void* k,
+                    const void* v, const void* cos_t, const void* sin_t, int64_t cache_rows,
+                    const int64_t* pos, const int32_t* past, void* q_out, void* k_out,
+                    void* k_cache, void* v_cache, int64_t max_len, int64_t* n_oor,
+                    int64_t* n_skip) {
+  return qkv_core(dt, B, S, Nq, Nkv, H, interleaved, rotary_dim, q, k, v, NULL, NULL, 0.0, cos_t,
+                  sin_t, cache_rows, pos, past, q_out, k_out, k_cache, v_cache, max_len, n_oor,
+                  n_skip);
+}
+
+/* ------------------------------------------------------------------------ */
+/* The same, with each Q and K head RMS-normalised before the rotation.     */
+/* [PR] Qwen3 Architecture (QK-Norm): Qwen3 applies RMSNorm to Q and K      */
+/* after the projection and reshape and before RoPE; Verification counts    */
+/* the SimplifiedLayerNormalization (RMSNorm) nodes it fuses.               */
+/* Reading (the pages name RMSNorm without printing it): over the head's H  */
+/* elements, r = 1/sqrt(mean(x^2) + eps); the normalised value x*r is       */
+/* rounded to T, multiplied by the head-size weight (q_weight for Q heads,  */
+/* k_weight for K heads) and rounded to T again -- the modelling code casts */
+/* back to the activation type before the weight -- and that z is what the  */
+/* rotation of oracle_rope_qkv receives (an out-of-range position copies z  */
+/* through; the tail past rd is z). V is not normalised.                    */
+/* ------------------------------------------------------------------------ */
+int oracle_rope_qkv_rmsnorm(int dt, int64_t B, int64_t S, int64_t Nq, int64_t Nkv, int64_t H,
+                            int interleaved, int64_t rotary_dim, const void* q, const void* k,
+                            const void* v, const void* q_weight, const void* k_weight, double eps,
+                            const void* cos_t, const void* sin_t, int64_t cache_rows,
+                            const int64_t* pos, const int32_t* past, void* q_out, void* k_out,
+                            void* k_cache, void* v_cache, int64_t max_len, int64_t* n_oor,
+                            int64_t* n_skip) {
+  if (q_weight == NULL || k_weight == NULL) return 1;
+  return qkv_core(dt, B, S, Nq, Nkv, H, interleaved, rotary_dim, q, k, v, q_weight, k_weight, eps,
+                  cos_t, sin_t, cache_rows, pos, past, q_out, k_out, k_cache, v_cache, max_len,
+                  n_oor, n_skip);
 }

@@ -40,6 +40,13 @@ MUTATIONS = {
                                 "int64_t vsrc = packed ? (tok * Ntot + Nq + n) * H"),
     "qkv_implicit_position_ignores_past": ("int64_t p = pos ? pos[tok] : (past ? (int64_t)past[b] + s : s);",
                                            "int64_t p = pos ? pos[tok] : s;"),
+    "norm_mean_over_half_head": ("double r = 1.0 / sqrt(ss / (double)H + eps);",
+                                 "double r = 1.0 / sqrt(ss / (double)(H / 2) + eps);"),
+    "norm_epsilon_dropped": ("double r = 1.0 / sqrt(ss / (double)H + eps);", "double r = 1.0 / sqrt(ss / (double)H);"),
+    "norm_weight_before_rounding": ("double n = round_to(dt, ld(dt, x, xb + j) * r);",
+                                    "double n = ld(dt, x, xb + j) * r;"),
+    "norm_key_uses_query_weight": ("rms_norm_head(dt, ks, ksrc, H, k_weight, eps, zq);",
+                                   "rms_norm_head(dt, ks, ksrc, H, q_weight, eps, zq);"),
     "qkv_value_rotated": ("for (int64_t j = 0; j < H; ++j) cp(dt, vs, vsrc + j, v_cache, dst + j);",
                           "rope_one_head(dt, interleaved, H, rd, vs, vsrc, v_cache, dst, cos_t, sin_t, crow, valid);"),
 }

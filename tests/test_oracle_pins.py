@@ -632,3 +632,106 @@ def test_qkv_implicit_positions_follow_the_cache(orc):
     assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
     assert np.array_equal(c[0], d[0]) and np.array_equal(c[1], d[1])
     assert not np.array_equal(a[0], c[0])
+
+
+# --------------------------------------------------------------------------
+# QK-RMSNorm before the rotation (Qwen3 fusion PR: Qwen3 Architecture,
+# Verification). Reading: z = T(w * T(x / sqrt(mean(x^2) + eps))) per head.
+# --------------------------------------------------------------------------
+
+@pytest.mark.parametrize("dtype", [np.float16, np.float32])
+def test_qkv_rmsnorm_hand_example(orc, dtype):
+    g = _gold("qkv_rmsnorm_hand_example.json")
+    H = g["head_size"]
+    arr = lambda v: np.array(v, dtype=dtype)  # noqa: E731
+    q, k = arr(g["q"]).reshape(1, 1, H), arr(g["k"]).reshape(1, 1, H)
+    exp = g["expected"][np.dtype(dtype).name]
+    qo, ko, _, _, _, _ = orc.rope_qkv(q, arr(g["cos"]), arr(g["sin"]), np.array([[g["position"]]]),
+                                      num_heads=1, kv_num_heads=1, key=k, q_norm_weight=arr(g["q_weight"]),
+                                      k_norm_weight=arr(g["k_weight"]), epsilon=g["epsilon"])
+    assert qo.ravel().tolist() == [float(dtype(v)) for v in exp["q_out"]]
+    assert ko.ravel().tolist() == [float(dtype(v)) for v in exp["k_out"]]
+
+
+def test_qkv_rmsnorm_epsilon_closed_form(orc):
+    """A constant head a normalises to a / sqrt(a^2 + eps) (mpmath, rounded to T)."""
+    H, a, eps = 8, 2.0, 1e-3
+    for dtype in (np.float16, np.float32):
+        q = np.full((1, 1, H), a, dtype=dtype)
+        one = np.ones((1, H // 2), dtype=dtype)
+        zero = np.zeros((1, H // 2), dtype=dtype)
+        qo, _, _, _, _, _ = orc.rope_qkv(q, one, zero, np.zeros((1, 1), np.int64), num_heads=1, kv_num_heads=1,
+                                         key=q.copy(), q_norm_weight=np.ones(H, dtype), k_norm_weight=np.ones(H, dtype),
+                                         epsilon=eps)
+        exact = mpmath.mpf(a) / mpmath.sqrt(mpmath.mpf(a) ** 2 + mpmath.mpf(eps))
+        assert (qo.ravel() == dtype(float(exact))).all()
+        assert float(dtype(float(exact))) != 1.0 or dtype == np.float16
+
+
+def _rmsnorm_numpy(x, w, eps, H, dtype):
+    """Independent formulation: numpy float64 mean of squares, rounded with astype."""
+    xs = x.reshape(*x.shape[:-1], -1, H).astype(np.float64)
+    r = 1.0 / np.sqrt(np.mean(xs * xs, axis=-1, keepdims=True) + eps)
+    n = (xs * r).astype(dtype).astype(np.float64)
+    return (n * w.astype(np.float64)).astype(dtype).reshape(x.shape)
+
+
+def test_qkv_rmsnorm_equals_numpy_norm_then_rotation(orc):
+    """Fused == numpy RMSNorm followed by the pinned RotaryEmbedding oracle, bit for bit, on Q
+    and K (separate weights), packed and separate, partial width, out-of-range positions
+    (the normalised head is copied through); V is never normalised."""
+    rng = np.random.default_rng(75)
+    B, S, Nq, Nkv, H, R, L = 2, 6, 4, 2, 16, 30, 12
+    for dtype in (np.float16, np.float32):
+        q, k, v, cos8, sin8 = _qkv_inputs(rng, dtype, B, S, Nq, Nkv, H, R)
+        q = (q * 3).astype(dtype)
+        wq = rng.uniform(0.5, 1.5, H).astype(dtype)
+        wk = rng.uniform(0.5, 1.5, H).astype(dtype)
+        eps = 1e-6
+        for rd in (0, 8):
+            cos, sin = (cos8, sin8) if rd == 0 else (cos8[:, :rd // 2].copy(), sin8[:, :rd // 2].copy())
+            pos = rng.integers(0, R, (B, S))
+            pos[1, 2] = R + 1
+            zq = _rmsnorm_numpy(q, wq, eps, H, dtype)
+            zk = _rmsnorm_numpy(k, wk, eps, H, dtype)
+            yq, _ = orc.rope(zq, cos, sin, pos, 0, rd, Nq)
+            yk, _ = orc.rope(zk, cos, sin, pos, 0, rd, Nkv)
+            qo, ko, _, _, n_oor, _ = orc.rope_qkv(q, cos, sin, pos, num_heads=Nq, kv_num_heads=Nkv, key=k,
+                                                  rotary_embedding_dim=rd, q_norm_weight=wq, k_norm_weight=wk,
+                                                  epsilon=eps)
+            assert n_oor == 1
+            assert np.array_equal(qo.view(np.uint8), yq.view(np.uint8))
+            assert np.array_equal(ko.view(np.uint8), yk.view(np.uint8))
+            # packed input and cache mode: same Q, K in the cache rows, V copied unchanged
+            packed = np.concatenate([q, k, v], axis=-1)
+            past = np.array([0, 3], dtype=np.int32)
+            kc0 = np.zeros((B, Nkv, L, H), dtype)
+            qp, _, kc, vc, _, _ = orc.rope_qkv(packed, cos, sin, past[:, None] + np.arange(S)[None, :],
+                                               num_heads=Nq, kv_num_heads=Nkv, rotary_embedding_dim=rd,
+                                               k_cache=kc0, v_cache=kc0, past_seq_lens=past, q_norm_weight=wq,
+                                               k_norm_weight=wk, epsilon=eps)
+            pos2 = past[:, None] + np.arange(S)[None, :]
+            yq2, _ = orc.rope(zq, cos, sin, pos2, 0, rd, Nq)
+            yk2, _ = orc.rope(zk, cos, sin, pos2, 0, rd, Nkv)
+            assert np.array_equal(qp.view(np.uint8), yq2.view(np.uint8))
+            for b in range(B):
+                for s in range(S):
+                    row = past[b] + s
+                    assert np.array_equal(kc[b, :, row].view(np.uint8),
+                                          yk2.reshape(B, S, Nkv, H)[b, s].view(np.uint8))
+                    assert np.array_equal(vc[b, :, row].view(np.uint8), v.reshape(B, S, Nkv, H)[b, s].view(np.uint8))
+
+
+def test_qkv_rmsnorm_scale_invariant_without_epsilon(orc):
+    rng = np.random.default_rng(76)
+    B, S, N, H, R = 2, 3, 2, 16, 10
+    for dtype in (np.float16, np.float32):
+        q, k, _, cos, sin = _qkv_inputs(rng, dtype, B, S, N, N, H, R)
+        w = rng.uniform(0.5, 1.5, H).astype(dtype)
+        pos = rng.integers(0, R, (B, S))
+        a = orc.rope_qkv(q, cos, sin, pos, num_heads=N, kv_num_heads=N, key=k, q_norm_weight=w, k_norm_weight=w,
+                         epsilon=0.0)
+        b = orc.rope_qkv((q * 4).astype(dtype), cos, sin, pos, num_heads=N, kv_num_heads=N,
+                         key=(k / 8).astype(dtype), q_norm_weight=w, k_norm_weight=w, epsilon=0.0)
+        assert np.array_equal(a[0].view(np.uint8), b[0].view(np.uint8))
+        assert np.array_equal(a[1].view(np.uint8), b[1].view(np.uint8))
