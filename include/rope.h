@@ -255,6 +255,39 @@ rope_status rope_apply_qkv(rope_dtype dtype, int64_t batch, int64_t seq, int32_t
                            rope_stream_t stream);
 
 /*
+ * rope_apply_qkv_rmsnorm -- rope_apply_qkv with each Q and K head
+ * RMS-normalised first, in the same launch ([Qwen3 fusion pull request, Qwen3
+ * Architecture: QK-Norm applies RMSNorm to Q and K after the projection and
+ * reshape, before RoPE; Verification: SimplifiedLayerNormalization, i.e.
+ * RMSNorm, nodes]). For every Q (resp. K) head x of H elements:
+ *   r = 1 / sqrt(mean_j(x_j^2) + epsilon),  z_j = T(w_j * T(x_j * r)),
+ * with w = q_norm_weight (resp. k_norm_weight), each product rounded once to T
+ * and the mean and r in float32; z is then rotated exactly as rope_apply_qkv
+ * rotates a head (an out-of-range position copies z through; the tail past
+ * the rotary width is z). V heads are not normalised.
+ *
+ * q_norm_weight, k_norm_weight  device T[head_size], both required.
+ * epsilon       finite, >= 0 (Qwen3 uses 1e-6). With epsilon 0 an all-zero
+ *               head divides by zero (inf/NaN), as the definition does.
+ * Every other argument, layout, ownership and status bit as rope_apply_qkv.
+ * The mean is computed by one group of at most 32 threads per head:
+ * ROPE_ERR_UNSUPPORTED when a head has more than 32 units (16-byte vectors
+ * on the aligned path: head_size <= 256 float16 or 128 float32 at full
+ * rotation; single elements otherwise). ROPE_ERR_INVALID_ARG as
+ * rope_apply_qkv, and for a missing weight, a misaligned weight or a bad
+ * epsilon.
+ */
+rope_status rope_apply_qkv_rmsnorm(rope_dtype dtype, int64_t batch, int64_t seq, int32_t num_heads,
+                                   int32_t kv_num_heads, int64_t head_size, const void* query,
+                                   const void* key, const void* value, const void* q_norm_weight,
+                                   const void* k_norm_weight, float epsilon, const void* cos_cache,
+                                   const void* sin_cache, int64_t cache_rows,
+                                   const int64_t* position_ids, const int32_t* past_seq_lens,
+                                   int32_t interleaved, int32_t rotary_embedding_dim, void* q_out,
+                                   void* k_out, void* k_cache, void* v_cache, int64_t max_cache_len,
+                                   int32_t* status_flags, rope_stream_t stream);
+
+/*
  * rope_cache_build -- the (rows, half) cos and sin tables of rope_apply's
  * 2-D cache: row p holds the coefficients rope_apply_fused computes for
  * position p ([Qwen3 fusion pull request, Medium Issues 4: cos(freqs) *

@@ -16,6 +16,7 @@
 #include <cuda_runtime.h>
 
 #include <atomic>
+#include <cmath>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -206,14 +207,25 @@ struct Launch {
   size_t smem = 0;
 };
 
+// unit_groups: a row's units go to a power-of-two group of at most 32 lanes,
+// one unit per lane (kernels that reduce over a row with warp shuffles).
 rope_status plan(const Geom& g, int es, bool vec, const void* fn, bool smem_table, KParams* kp,
-                 Launch* L) {
+                 Launch* L, bool unit_groups = false) {
   const int V = vec ? 16 / es : 1;
   const int64_t nP = g.h / V;
   const int64_t nT = (g.H - g.rd) / V;
   const int64_t U = nP + nT;
   if (U < 1) return fail(ROPE_ERR_INVALID_ARG, "empty head");
-  const int64_t Ublk = U < kMaxRowThreads ? U : kMaxRowThreads;
+  int64_t Ublk = U < kMaxRowThreads ? U : kMaxRowThreads;
+  if (unit_groups) {
+    Ublk = 1;
+    while (Ublk < U) Ublk *= 2;
+    if (Ublk > 32)
+      return fail(ROPE_ERR_UNSUPPORTED,
+                  "a head of %lld %d-element units does not fit one 32-lane group (RMSNorm needs head_size "
+                  "<= 256 float16 / 128 float32 elements on the 16-byte path, or 32 on the scalar path)",
+                  (long long)U, V);
+  }
   int64_t NG = g.N;
   if (NG * Ublk > kMaxRowThreads) {
     NG = kMaxRowThreads / Ublk;
@@ -724,16 +736,25 @@ rope_status rope_apply_fused(rope_dtype dtype, int32_t x_rank, const int64_t* x_
   return launch(fn, L, &kp, stream, "rope_fused_kernel");
 }
 
-rope_status rope_apply_qkv(rope_dtype dtype, int64_t batch, int64_t seq, int32_t num_heads,
-                           int32_t kv_num_heads, int64_t head_size, const void* query,
-                           const void* key, const void* value, const void* cos_cache,
-                           const void* sin_cache, int64_t cache_rows, const int64_t* position_ids,
-                           const int32_t* past_seq_lens, int32_t interleaved,
-                           int32_t rotary_embedding_dim, void* q_out, void* k_out, void* k_cache,
-                           void* v_cache, int64_t max_cache_len, int32_t* status_flags,
-                           rope_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// rope_apply_qkv and rope_apply_qkv_rmsnorm (q_weight == NULL: no norm).
+rope_status qkv_impl(rope_dtype dtype, int64_t batch, int64_t seq, int32_t num_heads, int32_t kv_num_heads,
+                     int64_t head_size, const void* query, const void* key, const void* value,
+                     const void* q_weight, const void* k_weight, float epsilon, const void* cos_cache,
+                     const void* sin_cache, int64_t cache_rows, const int64_t* position_ids,
+                     const int32_t* past_seq_lens, int32_t interleaved, int32_t rotary_embedding_dim,
+                     void* q_out, void* k_out, void* k_cache, void* v_cache, int64_t max_cache_len,
+                     int32_t* status_flags, rope_stream_t stream) {
   g_last_error.clear();
   ROPE_TRY(check_dtype(dtype));
+  const bool norm = q_weight != nullptr || k_weight != nullptr;
+  if (norm && (!q_weight || !k_weight))
+    return fail(ROPE_ERR_INVALID_ARG, "RMSNorm needs both q_norm_weight and k_norm_weight");
+  if (norm && !(epsilon >= 0.0f && epsilon < INFINITY))
+    return fail(ROPE_ERR_INVALID_ARG, "epsilon must be finite and >= 0");
   if (batch < 0 || seq < 0) return fail(ROPE_ERR_INVALID_ARG, "batch and seq must be >= 0");
   if (num_heads < 1 || kv_num_heads < 1)
     return fail(ROPE_ERR_INVALID_ARG, "num_heads (%d) and kv_num_heads (%d) must be >= 1", num_heads,
@@ -801,10 +822,15 @@ rope_status rope_apply_qkv(rope_dtype dtype, int64_t batch, int64_t seq, int32_t
   }
   if (position_ids) ROPE_TRY(check_elem_ptr(position_ids, "position_ids", 8));
   if (past_seq_lens) ROPE_TRY(check_elem_ptr(past_seq_lens, "past_seq_lens", 4));
+  if (norm) {
+    ROPE_TRY(check_elem_ptr(q_weight, "q_norm_weight", es));
+    ROPE_TRY(check_elem_ptr(k_weight, "k_norm_weight", es));
+  }
   if (status_flags && !aligned(status_flags, 4)) return fail(ROPE_ERR_INVALID_ARG, "status_flags is misaligned");
 
-  const bool vec = vector_ok(g, es, {query, key, value, q_out, k_out, k_cache, v_cache, cos_cache, sin_cache});
-  const void* fn = qkv_kernel(dtype, vec, interleaved != 0, position_ids == nullptr);
+  const bool vec = vector_ok(g, es, {query, key, value, q_out, k_out, k_cache, v_cache, cos_cache, sin_cache,
+                                     q_weight, k_weight});
+  const void* fn = qkv_kernel(dtype, vec, interleaved != 0, position_ids == nullptr, norm);
   KParams kp;
   memset(&kp, 0, sizeof(kp));
   kp.x = query;
@@ -827,13 +853,52 @@ rope_status rope_apply_qkv(rope_dtype dtype, int64_t batch, int64_t seq, int32_t
   qa.Nkv = kv_num_heads;
   qa.packed = packed;
   qa.cache = cache;
+  qa.qw = q_weight;
+  qa.kw = k_weight;
+  qa.eps = epsilon;
   Launch L;
-  ROPE_TRY(plan(g, es, vec, fn, false, &kp, &L));
+  ROPE_TRY(plan(g, es, vec, fn, false, &kp, &L, /*unit_groups=*/norm));
   void* args[] = {&kp, &qa};
   cudaError_t e = launch_pdl(fn, L.grid, L.block, L.smem, stream, args);
   if (e != cudaSuccess) return cuda_fail(e, "rope_apply_qkv launch");
   g_last_kernel = "rope_qkv_kernel";
   return ROPE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+rope_status rope_apply_qkv(rope_dtype dtype, int64_t batch, int64_t seq, int32_t num_heads,
+                           int32_t kv_num_heads, int64_t head_size, const void* query,
+                           const void* key, const void* value, const void* cos_cache,
+                           const void* sin_cache, int64_t cache_rows, const int64_t* position_ids,
+                           const int32_t* past_seq_lens, int32_t interleaved,
+                           int32_t rotary_embedding_dim, void* q_out, void* k_out, void* k_cache,
+                           void* v_cache, int64_t max_cache_len, int32_t* status_flags,
+                           rope_stream_t stream) {
+  return qkv_impl(dtype, batch, seq, num_heads, kv_num_heads, head_size, query, key, value, nullptr, nullptr,
+                  0.0f, cos_cache, sin_cache, cache_rows, position_ids, past_seq_lens, interleaved,
+                  rotary_embedding_dim, q_out, k_out, k_cache, v_cache, max_cache_len, status_flags, stream);
+}
+
+rope_status rope_apply_qkv_rmsnorm(rope_dtype dtype, int64_t batch, int64_t seq, int32_t num_heads,
+                                   int32_t kv_num_heads, int64_t head_size, const void* query,
+                                   const void* key, const void* value, const void* q_norm_weight,
+                                   const void* k_norm_weight, float epsilon, const void* cos_cache,
+                                   const void* sin_cache, int64_t cache_rows,
+                                   const int64_t* position_ids, const int32_t* past_seq_lens,
+                                   int32_t interleaved, int32_t rotary_embedding_dim, void* q_out,
+                                   void* k_out, void* k_cache, void* v_cache, int64_t max_cache_len,
+                                   int32_t* status_flags, rope_stream_t stream) {
+  if (!q_norm_weight || !k_norm_weight) {
+    g_last_error.clear();
+    return fail(ROPE_ERR_INVALID_ARG, "q_norm_weight and k_norm_weight are required");
+  }
+  return qkv_impl(dtype, batch, seq, num_heads, kv_num_heads, head_size, query, key, value, q_norm_weight,
+                  k_norm_weight, epsilon, cos_cache, sin_cache, cache_rows, position_ids, past_seq_lens,
+                  interleaved, rotary_embedding_dim, q_out, k_out, k_cache, v_cache, max_cache_len,
+                  status_flags, stream);
 }
 
 rope_status rope_cache_build(rope_dtype dtype, const float* inv_freq, int32_t half, int64_t rows,

@@ -65,6 +65,9 @@ struct QKVParams {
   int32_t Nq, Nkv;
   int32_t packed;        // x is packed [Q|K|V]
   int32_t cache;         // cache mode
+  const void* qw;        // RMSNorm: head-size weights of Q and K heads (null: no norm)
+  const void* kw;
+  float eps;
 };
 
 // Kernel entry points for cudaLaunchKernel / occupancy queries. `vec` selects
@@ -74,7 +77,7 @@ const void* rope_kernel_mrope(int dtype, bool vec, bool interleaved, bool rank4)
 const void* fused_kernel(int dtype, bool vec, bool interleaved, bool rank4);
 const void* cache_build_kernel(int dtype);
 // rope_qkv_kernel instance; its launch takes (KParams, QKVParams).
-const void* qkv_kernel(int dtype, bool vec, bool interleaved, bool implicit_pos);
+const void* qkv_kernel(int dtype, bool vec, bool interleaved, bool implicit_pos, bool rms_norm);
 // Records the message rope_last_error() returns on the calling thread.
 void set_last_error(const char* msg);
 

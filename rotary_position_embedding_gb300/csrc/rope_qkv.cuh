@@ -11,10 +11,13 @@
 //    kv_num_heads divides num_heads).
 //  - onnxruntime pull request "Add RotaryEmbedding fusion for Qwen3 on-the-fly
 //    RoPE patterns": Verification and Qwen3 Architecture (RoPE on both the Q
-//    and the K path, GQA with fewer K/V heads).
+//    and the K path, GQA with fewer K/V heads; QK-Norm: RMSNorm on Q and K
+//    after the projection and before RoPE).
 // Every Q and K head is rotated exactly as rope_rows_kernel rotates one head of
 // a rank-3 X (same tables, positions, pairing, rotary width and out-of-range
-// rule); V heads are copied bit for bit.
+// rule); V heads are copied bit for bit. With NORM, each Q and K head is first
+// RMS-normalised: z = T(w * T(x * r)), r = 1/sqrt(mean(x^2) + eps) over the
+// head (the products rounded once to T), and z is what gets rotated.
 #pragma once
 
 #include "rope_kernels.cuh"
@@ -23,6 +26,30 @@ namespace rope_gb300 {
 
 __device__ __forceinline__ void flag_cache_row(int32_t* flag) {
   if (flag) atomicOr(flag, 4);
+}
+
+template <class T, int V>
+__device__ __forceinline__ float sum_squares(const VecT<T, V>& x) {
+  float s = 0.f;
+#pragma unroll
+  for (int j = 0; j < V; ++j) {
+    const float v = Elem<T>::tof(x.v[j]);
+    s = __fmaf_rn(v, v, s);
+  }
+  return s;
+}
+
+// z_j = T(w_j * T(x_j * r)), each product rounded once to T.
+template <class T, int V>
+__device__ __forceinline__ VecT<T, V> norm_weight(const VecT<T, V>& x, float r, const VecT<T, V>& w) {
+  using E = Elem<T>;
+  VecT<T, V> z;
+#pragma unroll
+  for (int j = 0; j < V; ++j) {
+    const float n = E::mul_round(E::tof(x.v[j]), r);
+    z.v[j] = E::fromf(E::mul_round(n, E::tof(w.v[j])));
+  }
+  return z;
 }
 
 // The kernel sees each token as N = Nq + Nkv (+ Nkv in cache mode) head rows
@@ -37,7 +64,7 @@ __device__ __forceinline__ void flag_cache_row(int32_t* flag) {
 #define ROPE_QKV_MAXNREG 48
 #endif
 #define ROPE_QKV_BOUNDS __maxnreg__(ROPE_QKV_MAXNREG)
-template <class T, int V, bool INTER, bool IMPLICIT>
+template <class T, int V, bool INTER, bool IMPLICIT, bool NORM>
 __global__ void ROPE_QKV_BOUNDS rope_qkv_kernel(const KParams p, const QKVParams a) {
   using VT = VecT<T, V>;
   using bits = typename Elem<T>::bits;
@@ -81,6 +108,13 @@ __global__ void ROPE_QKV_BOUNDS rope_qkv_kernel(const KParams p, const QKVParams
   const bool rotates = role != 2;
   const bits* __restrict__ cosb = static_cast<const bits*>(p.cos);
   const bits* __restrict__ sinb = static_cast<const bits*>(p.sin);
+  // NORM: a row's Ublk lanes (a power of two <= 32, one unit each) are an
+  // aligned group of its warp; they add up the row's squares with shuffles.
+  unsigned gmask = 0u;
+  if (NORM) {
+    const unsigned lane = threadIdx.x & 31u;
+    gmask = p.Ublk >= 32 ? 0xffffffffu : (((1u << p.Ublk) - 1u) << (lane & ~(unsigned)(p.Ublk - 1)));
+  }
 
   int64_t tok = (int64_t)blockIdx.x * p.TTs + slot;
   int64_t b = tok / p.S;
@@ -108,28 +142,68 @@ __global__ void ROPE_QKV_BOUNDS rope_qkv_kernel(const KParams p, const QKVParams
         if (!valid && role == 0 && hd == 0 && k0 == 0) flag_oor(p.oor_flag);
         crow = pp * p.h;
       }
-      for (int k = k0; k < p.U; k += p.Ublk) {
-        if (k >= p.nP) {  // tail unit: bit copy
-          const int off = p.rd + (k - p.nP) * V;
-          st_stream(reinterpret_cast<VT*>(yr + off), ld_stream(reinterpret_cast<const VT*>(xr + off)));
-          continue;
+      if (NORM && rotates) {
+        // at most one unit per lane; lanes past the row's units add zeros
+        const bool has = k0 < p.U;
+        const bool tail = k0 >= p.nP;
+        int oa = 0, ob = 0;
+        if (tail)
+          oa = p.rd + (k0 - p.nP) * V;
+        else
+          unit_offsets<V, INTER>(k0, p.h, oa, ob);
+        VT xa{}, xb{};
+        if (has) {
+          xa = ld_stream(reinterpret_cast<const VT*>(xr + oa));
+          if (!tail) xb = ld_stream(reinterpret_cast<const VT*>(xr + ob));
         }
-        int oa, ob;
-        unit_offsets<V, INTER>(k, p.h, oa, ob);
-        const VT xa = ld_stream(reinterpret_cast<const VT*>(xr + oa));
-        const VT xb = ld_stream(reinterpret_cast<const VT*>(xr + ob));
-        if (!valid) {  // V head, or an out-of-range position: copied through
-          st_stream(reinterpret_cast<VT*>(yr + oa), xa);
-          st_stream(reinterpret_cast<VT*>(yr + ob), xb);
-          continue;
+        float ss = sum_squares<T, V>(xa) + sum_squares<T, V>(xb);
+        for (int o = p.Ublk >> 1; o > 0; o >>= 1) ss += __shfl_xor_sync(gmask, ss, o);
+        const float r = 1.0f / sqrtf(ss / (float)H + a.eps);
+        if (has) {
+          const bits* w = static_cast<const bits*>(role == 0 ? a.qw : a.kw);
+          const VT za = norm_weight<T, V>(xa, r, ld_shared_ro(reinterpret_cast<const VT*>(w + oa)));
+          if (tail) {
+            st_stream(reinterpret_cast<VT*>(yr + oa), za);
+          } else {
+            const VT zb = norm_weight<T, V>(xb, r, ld_shared_ro(reinterpret_cast<const VT*>(w + ob)));
+            if (valid) {
+              const int oc = k0 * V;
+              const VT c = ld_shared_ro(reinterpret_cast<const VT*>(cosb + crow + oc));
+              const VT sn = ld_shared_ro(reinterpret_cast<const VT*>(sinb + crow + oc));
+              VT ya, yb;
+              rotate_unit<T, V, INTER>(za, zb, c, sn, ya, yb);
+              st_stream(reinterpret_cast<VT*>(yr + oa), ya);
+              st_stream(reinterpret_cast<VT*>(yr + ob), yb);
+            } else {  // out-of-range position: the normalised head passes through
+              st_stream(reinterpret_cast<VT*>(yr + oa), za);
+              st_stream(reinterpret_cast<VT*>(yr + ob), zb);
+            }
+          }
         }
-        const int oc = k * V;
-        const VT c = ld_shared_ro(reinterpret_cast<const VT*>(cosb + crow + oc));
-        const VT sn = ld_shared_ro(reinterpret_cast<const VT*>(sinb + crow + oc));
-        VT ya, yb;
-        rotate_unit<T, V, INTER>(xa, xb, c, sn, ya, yb);
-        st_stream(reinterpret_cast<VT*>(yr + oa), ya);
-        st_stream(reinterpret_cast<VT*>(yr + ob), yb);
+      } else {
+        for (int k = k0; k < p.U; k += p.Ublk) {
+          if (k >= p.nP) {  // tail unit: bit copy
+            const int off = p.rd + (k - p.nP) * V;
+            st_stream(reinterpret_cast<VT*>(yr + off), ld_stream(reinterpret_cast<const VT*>(xr + off)));
+            continue;
+          }
+          int oa, ob;
+          unit_offsets<V, INTER>(k, p.h, oa, ob);
+          const VT xa = ld_stream(reinterpret_cast<const VT*>(xr + oa));
+          const VT xb = ld_stream(reinterpret_cast<const VT*>(xr + ob));
+          if (!valid) {  // V head, or an out-of-range position: copied through
+            st_stream(reinterpret_cast<VT*>(yr + oa), xa);
+            st_stream(reinterpret_cast<VT*>(yr + ob), xb);
+            continue;
+          }
+          const int oc = k * V;
+          const VT c = ld_shared_ro(reinterpret_cast<const VT*>(cosb + crow + oc));
+          const VT sn = ld_shared_ro(reinterpret_cast<const VT*>(sinb + crow + oc));
+          VT ya, yb;
+          rotate_unit<T, V, INTER>(xa, xb, c, sn, ya, yb);
+          st_stream(reinterpret_cast<VT*>(yr + oa), ya);
+          st_stream(reinterpret_cast<VT*>(yr + ob), yb);
+        }
       }
     }
     s += p.step_s;

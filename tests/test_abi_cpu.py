@@ -29,7 +29,8 @@ def test_header_declares_the_abi():
     fns = declared_functions()
     for name in ("rope_apply", "mrope_apply", "mrope_apply_stream_map", "mrope_stream_map",
                  "rope_apply_fused", "rope_cache_build", "rope_status_string", "rope_last_error",
-                 "rope_set_variant", "rope_get_variant", "rope_last_kernel", "rope_apply_no_alloc"):
+                 "rope_set_variant", "rope_get_variant", "rope_last_kernel", "rope_apply_no_alloc",
+                 "rope_apply_qkv", "rope_apply_qkv_rmsnorm"):
         assert name in fns
 
 
@@ -240,3 +241,33 @@ def test_rope_apply_qkv_empty_launches_nothing(lib):
     so = lib.load_library()
     assert _qkv(so, S=0, q=None, k=None, q_out=None, k_out=ctypes.c_void_p(0x60000)) == OK
     assert _qkv(so, B=0) == OK
+
+
+def _qkv_norm(so, **kw):
+    a = dict(dtype=F16, B=2, S=4, nq=8, nkv=2, H=16, q=FAKE, k=FAKE2, v=None, qw=ctypes.c_void_p(0xb0000),
+             kw_=ctypes.c_void_p(0xc0000), eps=1e-6, cos=FAKE3, sin=FAKE3, rows=32, pos=FAKE4, past=None, inter=0,
+             rd=0, q_out=ctypes.c_void_p(0x50000), k_out=ctypes.c_void_p(0x60000), kc=None, vc=None, max_len=0,
+             flag=None, stream=None)
+    a.update(kw)
+    return so.rope_apply_qkv_rmsnorm(a["dtype"], a["B"], a["S"], a["nq"], a["nkv"], a["H"], a["q"], a["k"],
+                                     a["v"], a["qw"], a["kw_"], a["eps"], a["cos"], a["sin"], a["rows"], a["pos"],
+                                     a["past"], a["inter"], a["rd"], a["q_out"], a["k_out"], a["kc"], a["vc"],
+                                     a["max_len"], a["flag"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(qw=None), INVALID),                            # both weights are required
+    (dict(kw_=None), INVALID),
+    (dict(eps=-1e-6), INVALID),
+    (dict(eps=float("inf")), INVALID),
+    (dict(eps=float("nan")), INVALID),
+    (dict(qw=ctypes.c_void_p(0xb0001)), INVALID),        # misaligned weight
+    (dict(nkv=3), INVALID),                              # the rope_apply_qkv contracts still apply
+    (dict(H=1024, rows=32), UNSUPPORTED),                # 64 units of 16 bytes: more than one 32-lane group
+    (dict(H=64, rd=32, q=ctypes.c_void_p(0x10002)), UNSUPPORTED),  # scalar path: 16 pairs + 32 tail elements
+])
+def test_rope_apply_qkv_rmsnorm_rejects_before_launch(lib, kw, status):
+    so = lib.load_library()
+    st = _qkv_norm(so, **kw)
+    assert st == status, so.rope_last_error().decode()
+    assert so.rope_last_error().decode() != ""

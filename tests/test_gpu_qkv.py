@@ -210,3 +210,157 @@ def test_qkv_workload_full_size(lib, orc, cuda, name):
     kc[bi, :, ri] = fill
     vc[bi, :, ri] = fill
     assert bool(torch.all(kc == fill)) and bool(torch.all(vc == fill))
+
+
+# ---------------------------------------------------------------------------
+# QK-RMSNorm before the rotation (rope_apply_qkv_rmsnorm)
+# ---------------------------------------------------------------------------
+
+def _ulp(v, dtype):
+    a = np.abs(v.astype(np.float64))
+    if dtype == np.float16:
+        return 2.0 ** (np.floor(np.log2(np.maximum(a, 2.0 ** -14))) - 10)
+    return 2.0 ** (np.floor(np.log2(np.maximum(a, 2.0 ** -126))) - 23)
+
+
+def compare_norm(got, ref, N, H, rd, inter):
+    """Outputs of RMS-normalised, rotated heads against the oracle.
+
+    The kernel forms r = 1/sqrt(mean(x^2) + eps) in float32 -- per-lane fused
+    multiply-adds of 2V squares, a shuffle tree of at most 5 additions, the
+    mean, epsilon, a correctly rounded sqrt and division: relative error at
+    most about 11 units of 2^-24 (6.6e-7) -- the oracle in binary64.
+      float16: that moves T(x*r) by at most one float16 ulp and T(w*T(x*r))
+        (w <= 2) by at most two ulps of z; the rotation maps a change of z
+        into at most |c| + |s| <= sqrt(2) times as much in the output, and
+        rounds once more. Bound: 1 ulp of the result + 3 ulps of the pair's
+        magnitude (which bounds |z| and which the rotation preserves). Such
+        flips need x*r within 6.6e-7 of a rounding boundary (a 2^-11 grid),
+        so at least 97 % of the elements must match bit for bit.
+      float32: r's error carries into z at ~1.3e-6 relative (two more
+        roundings) and through the float32 rotation (one more product and
+        the final rounding). Bound: 1 ulp of the result + 3e-6 of the pair's
+        magnitude; no bit-exact fraction is expected."""
+    assert got.shape == ref.shape and got.dtype == ref.dtype
+    dtype = ref.dtype.type
+    g = got.reshape(-1, N, H).astype(np.float64)
+    r = ref.reshape(-1, N, H).astype(np.float64)
+    h = rd // 2
+    i0 = np.arange(h) * 2 if inter else np.arange(h)
+    i1 = i0 + 1 if inter else i0 + h
+    rho = np.abs(r)
+    pr = np.sqrt(r[..., i0] ** 2 + r[..., i1] ** 2)
+    rho[..., i0] = np.maximum(rho[..., i0], pr)
+    rho[..., i1] = np.maximum(rho[..., i1], pr)
+    if dtype == np.float16:
+        tol = _ulp(r, dtype) + 3 * _ulp(rho, dtype)
+    else:
+        tol = _ulp(r, dtype) + 3e-6 * rho
+    d = np.abs(g - r)
+    bad = d > tol
+    assert not bad.any(), f"{int(bad.sum())} elements beyond the bound; worst excess {float((d - tol).max())}"
+    exact = float((d == 0).mean())
+    if dtype == np.float16:
+        assert exact >= 0.97, f"only {exact:.4f} of the elements are bit-exact"
+    return exact
+
+
+def _run_norm_case(lib, orc, torch, cuda, dt, packed, cache, inter, rot, implicit, H, offset=0, Nq=8, Nkv=2,
+                   B=3, S=37, R=64, L=80, seed=0, eps=1e-6):
+    rng = np.random.default_rng(1000 + seed)
+    npdt = np.float16 if dt == "f16" else np.float32
+    rd = 0 if rot == "full" else H // 2
+    rdw = rd or H
+    h = rdw // 2
+    Ntot = Nq + 2 * Nkv
+    qkv = (rng.standard_normal((B, S, Ntot * H)) * rng.uniform(0.1, 10.0, (B, S, Ntot, 1)).repeat(H, -1)
+           .reshape(B, S, Ntot * H)).astype(npdt)
+    q, k, v = _heads(qkv, B, S, 0, Nq, Ntot, H), _heads(qkv, B, S, Nq, Nq + Nkv, Ntot, H), \
+        _heads(qkv, B, S, Nq + Nkv, Ntot, Ntot, H)
+    wq = rng.uniform(0.5, 2.0, H).astype(npdt)
+    wk = rng.uniform(0.5, 2.0, H).astype(npdt)
+    theta = rng.uniform(-np.pi, np.pi, (R, h))
+    cos, sin = np.cos(theta).astype(npdt), np.sin(theta).astype(npdt)
+    past = np.array([0, 11, 50], dtype=np.int32)[:B]
+    if implicit:
+        pos = None
+    else:
+        pos = rng.integers(0, R, (B, S))
+        pos[0, 5], pos[1, 0], pos[-1, -1] = R + 3, -1, R
+    kc0 = rng.standard_normal((B, Nkv, L, H)).astype(npdt) if cache else None
+    vc0 = rng.standard_normal((B, Nkv, L, H)).astype(npdt) if cache else None
+    use_past = cache or implicit
+    q_ref, k_ref, kc_ref, vc_ref, n_oor, n_skip = orc.rope_qkv(
+        qkv if packed else q, cos, sin, pos, num_heads=Nq, kv_num_heads=Nkv, key=None if packed else k,
+        value=None if (packed or not cache) else v, interleaved=inter, rotary_embedding_dim=rd, k_cache=kc0,
+        v_cache=vc0, past_seq_lens=past if use_past else None, q_norm_weight=wq, k_norm_weight=wk, epsilon=eps)
+    dv = lambda a: None if a is None else _dev(a, torch, cuda, offset)  # noqa: E731
+    status = torch.zeros(1, dtype=torch.int32, device=cuda)
+    kc_d, vc_d = dv(kc0), dv(vc0)
+    qo, ko = lib.rope_apply_qkv(dv(qkv if packed else q), dv(cos), dv(sin),
+                                None if pos is None else _dev(pos, torch, cuda), num_heads=Nq, kv_num_heads=Nkv,
+                                key=None if packed else dv(k), value=None if (packed or not cache) else dv(v),
+                                interleaved=inter, rotary_embedding_dim=rd, k_cache=kc_d, v_cache=vc_d,
+                                past_seq_lens=_dev(past, torch, cuda) if use_past else None, status=status,
+                                q_norm_weight=dv(wq), k_norm_weight=dv(wk), epsilon=eps)
+    torch.cuda.synchronize()
+    compare_norm(qo.cpu().numpy(), q_ref, Nq, H, rdw, inter)
+    if not cache:
+        compare_norm(ko.cpu().numpy(), k_ref, Nkv, H, rdw, inter)
+    else:
+        kc_g, vc_g = kc_d.cpu().numpy(), vc_d.cpu().numpy()
+        assert np.array_equal(vc_g.view(np.uint8), vc_ref.view(np.uint8))   # V: copies, rest untouched
+        written = np.zeros((B, L), dtype=bool)
+        for b in range(B):
+            rows = past[b] + np.arange(S)
+            written[b, rows[rows < L]] = True
+        # untouched K rows keep their bits; written rows within the norm bound
+        assert np.array_equal(kc_g.transpose(0, 2, 1, 3)[~written].view(np.uint8),
+                              kc0.transpose(0, 2, 1, 3)[~written].view(np.uint8))
+        compare_norm(np.ascontiguousarray(kc_g.transpose(0, 2, 1, 3)[written]),
+                     np.ascontiguousarray(kc_ref.transpose(0, 2, 1, 3)[written]), Nkv, H, rdw, inter)
+    assert int(status.item()) == (1 if n_oor else 0) | (4 if n_skip else 0)
+
+
+NORM_GRID = list(itertools.product(["f16", "f32"], [0, 1], [0, 1], ["full", "partial"], [(0, 0), (1, 1)]))
+
+
+@pytest.mark.parametrize("dt,cache,inter,rot,pk_impl", NORM_GRID)
+def test_qkv_rmsnorm_grid(lib, orc, cuda, dt, cache, inter, rot, pk_impl):
+    import torch
+
+    packed, implicit = pk_impl
+    _run_norm_case(lib, orc, torch, cuda, dt, packed, cache, inter, rot, implicit, H=64,
+                   seed=NORM_GRID.index((dt, cache, inter, rot, pk_impl)))
+
+
+@pytest.mark.parametrize("dt,H,offset,rot", [("f16", 128, 0, "full"), ("f16", 256, 0, "full"),
+                                             ("f32", 128, 0, "full"), ("f16", 12, 0, "full"),
+                                             ("f16", 32, 1, "full"), ("f32", 16, 1, "partial")])
+def test_qkv_rmsnorm_head_sizes_and_scalar_path(lib, orc, cuda, dt, H, offset, rot):
+    """Head sizes whose units fill 4 to 32 lanes, and the single-element path."""
+    import torch
+
+    _run_norm_case(lib, orc, torch, cuda, dt, 1, 1, 0, rot, 1, H=H, offset=offset, seed=H + offset)
+
+
+def test_qkv_rmsnorm_zero_head_and_unsupported(lib, orc, cuda):
+    """An all-zero head normalises to zeros (epsilon > 0); a head too wide for one
+    32-lane group is refused before any launch."""
+    import torch
+
+    B, S, N, H = 1, 4, 2, 64
+    q = torch.zeros((B, S, N * H), dtype=torch.float16, device=cuda)
+    w = torch.ones(H, dtype=torch.float16, device=cuda)
+    c = torch.ones((8, H // 2), dtype=torch.float16, device=cuda)
+    qo, ko = lib.rope_apply_qkv(q, c, c, None, num_heads=N, kv_num_heads=N, key=q.clone(), q_norm_weight=w,
+                                k_norm_weight=w)
+    torch.cuda.synchronize()
+    assert not qo.any() and not ko.any()
+    big = torch.zeros((1, 2, 2 * 1024), dtype=torch.float16, device=cuda)
+    wb = torch.ones(1024, dtype=torch.float16, device=cuda)
+    cb = torch.ones((8, 512), dtype=torch.float16, device=cuda)
+    with pytest.raises(lib.RopeError):
+        lib.rope_apply_qkv(big, cb, cb, None, num_heads=1, kv_num_heads=1,
+                           key=torch.zeros((1, 2, 1024), dtype=torch.float16, device=cuda), q_norm_weight=wb,
+                           k_norm_weight=wb)
