@@ -220,6 +220,11 @@ class QKVStep:
         self.cos, self.sin = rp.rope_cache_build(inv, w.cache_rows, tdt)
         self.code = 1 if w.dtype == "float16" else 0
         self.H = H
+        self.norm = bool(w.extra.get("rms_norm"))
+        if self.norm:
+            self.qw = torch.from_numpy(inp["q_norm_weight"]).to(device)
+            self.kw = torch.from_numpy(inp["k_norm_weight"]).to(device)
+            self.eps = float(w.extra["epsilon"])
         # unfused path: positions past[b] + s and the (b, row) scatter indices
         s_idx = torch.arange(S, device=device, dtype=torch.int64)[None, :]
         self.pos = (self.past.to(torch.int64)[:, None] + s_idx).contiguous()
@@ -229,6 +234,14 @@ class QKVStep:
 
     def launch(self, k, stream, fused=True):
         w, lib = self.w, self.lib
+        vp = ctypes.c_void_p
+        if fused and self.norm:
+            return lib.rope_apply_qkv_rmsnorm(
+                self.code, w.batch, w.seq, self.Nq, self.Nkv, self.H, vp(self.xs[k].data_ptr()), None, None,
+                vp(self.qw.data_ptr()), vp(self.kw.data_ptr()), self.eps, vp(self.cos.data_ptr()),
+                vp(self.sin.data_ptr()), w.cache_rows, None, vp(self.past.data_ptr()), 0, 0,
+                vp(self.qo[k].data_ptr()), None, vp(self.kc.data_ptr()), vp(self.vc.data_ptr()),
+                w.extra["max_len"], None, stream)
         if fused:
             return lib.rope_apply_qkv(self.code, w.batch, w.seq, self.Nq, self.Nkv, self.H,
                                       ctypes.c_void_p(self.xs[k].data_ptr()), None, None,
@@ -239,6 +252,18 @@ class QKVStep:
                                       w.extra["max_len"], None, stream)
         B, S, H, Nq, Nkv = w.batch, w.seq, self.H, self.Nq, self.Nkv
         x = self.xs[k].view(B, S, Nq + 2 * Nkv, H)
+        if self.norm:
+            # QK-Norm as separate torch ops, then the fused rotation + append
+            torch = self.torch
+            xf = x[:, :, :Nq + Nkv].float()
+            n = (xf * torch.rsqrt(xf.pow(2).mean(-1, keepdim=True) + self.eps)).to(x.dtype)
+            wqk = torch.cat([self.qw.expand(Nq, H), self.kw.expand(Nkv, H)])
+            xn = torch.cat([n * wqk, x[:, :, Nq + Nkv:]], dim=2).contiguous()
+            return lib.rope_apply_qkv(self.code, B, S, Nq, Nkv, H, vp(xn.data_ptr()), None, None,
+                                      vp(self.cos.data_ptr()), vp(self.sin.data_ptr()), w.cache_rows, None,
+                                      vp(self.past.data_ptr()), 0, 0, vp(self.qo[k].data_ptr()), None,
+                                      vp(self.kc.data_ptr()), vp(self.vc.data_ptr()), w.extra["max_len"], None,
+                                      stream)
         q = x[:, :, :Nq].reshape(B, S, Nq * H).contiguous()
         kk = x[:, :, Nq:Nq + Nkv].reshape(B, S, Nkv * H).contiguous()
         self.rp.rope_apply(q, self.cos, self.sin, self.pos, num_heads=Nq, out=self.qo[k])

@@ -39,15 +39,19 @@ __device__ __forceinline__ float sum_squares(const VecT<T, V>& x) {
   return s;
 }
 
-// z_j = T(w_j * T(x_j * r)), each product rounded once to T.
+// z_j = T(w_j * T(x_j * r)). Both products are float32 products rounded to
+// T; w * n is exact in float32 for float16 data, and x * r (r itself a
+// float32 approximation of the exact scale) may land on a float16 midpoint
+// only where the exact product is within 2^-24 of it -- inside the one-ulp
+// flips that r's own error already allows.
 template <class T, int V>
 __device__ __forceinline__ VecT<T, V> norm_weight(const VecT<T, V>& x, float r, const VecT<T, V>& w) {
   using E = Elem<T>;
   VecT<T, V> z;
 #pragma unroll
   for (int j = 0; j < V; ++j) {
-    const float n = E::mul_round(E::tof(x.v[j]), r);
-    z.v[j] = E::fromf(E::mul_round(n, E::tof(w.v[j])));
+    const float n = E::tof(E::fromf(__fmul_rn(E::tof(x.v[j]), r)));
+    z.v[j] = E::fromf(__fmul_rn(n, E::tof(w.v[j])));
   }
   return z;
 }
@@ -63,7 +67,15 @@ __device__ __forceinline__ VecT<T, V> norm_weight(const VecT<T, V>& x, float r, 
 #ifndef ROPE_QKV_MAXNREG
 #define ROPE_QKV_MAXNREG 48
 #endif
-#define ROPE_QKV_BOUNDS __maxnreg__(ROPE_QKV_MAXNREG)
+// With RMSNorm a lane also holds the weights and its cos/sin while the
+// head's mean is formed: 56 registers (still 3 CTAs of 384 threads per SM).
+#ifndef ROPE_QKV_NORM_MAXNREG
+#define ROPE_QKV_NORM_MAXNREG 56
+#endif
+#ifndef ROPE_QKV_NORM_HOIST
+#define ROPE_QKV_NORM_HOIST 1
+#endif
+#define ROPE_QKV_BOUNDS __maxnreg__(NORM ? ROPE_QKV_NORM_MAXNREG : ROPE_QKV_MAXNREG)
 template <class T, int V, bool INTER, bool IMPLICIT, bool NORM>
 __global__ void ROPE_QKV_BOUNDS rope_qkv_kernel(const KParams p, const QKVParams a) {
   using VT = VecT<T, V>;
@@ -151,25 +163,48 @@ __global__ void ROPE_QKV_BOUNDS rope_qkv_kernel(const KParams p, const QKVParams
           oa = p.rd + (k0 - p.nP) * V;
         else
           unit_offsets<V, INTER>(k0, p.h, oa, ob);
-        VT xa{}, xb{};
+        // every load that does not depend on the mean goes out before the
+        // reduction, so their latencies overlap X's
+        VT xa{}, xb{}, wa{}, wb{}, c{}, sn{};
+        const bits* w = static_cast<const bits*>(role == 0 ? a.qw : a.kw);
         if (has) {
           xa = ld_stream(reinterpret_cast<const VT*>(xr + oa));
           if (!tail) xb = ld_stream(reinterpret_cast<const VT*>(xr + ob));
+#if ROPE_QKV_NORM_HOIST
+          wa = ld_shared_ro(reinterpret_cast<const VT*>(w + oa));
+          if (!tail) {
+            wb = ld_shared_ro(reinterpret_cast<const VT*>(w + ob));
+            if (valid) {
+              const int oc = k0 * V;
+              c = ld_shared_ro(reinterpret_cast<const VT*>(cosb + crow + oc));
+              sn = ld_shared_ro(reinterpret_cast<const VT*>(sinb + crow + oc));
+            }
+          }
+#endif
         }
         float ss = sum_squares<T, V>(xa) + sum_squares<T, V>(xb);
         for (int o = p.Ublk >> 1; o > 0; o >>= 1) ss += __shfl_xor_sync(gmask, ss, o);
         const float r = 1.0f / sqrtf(ss / (float)H + a.eps);
+#if !ROPE_QKV_NORM_HOIST
         if (has) {
-          const bits* w = static_cast<const bits*>(role == 0 ? a.qw : a.kw);
-          const VT za = norm_weight<T, V>(xa, r, ld_shared_ro(reinterpret_cast<const VT*>(w + oa)));
+          wa = ld_shared_ro(reinterpret_cast<const VT*>(w + oa));
+          if (!tail) {
+            wb = ld_shared_ro(reinterpret_cast<const VT*>(w + ob));
+            if (valid) {
+              const int oc = k0 * V;
+              c = ld_shared_ro(reinterpret_cast<const VT*>(cosb + crow + oc));
+              sn = ld_shared_ro(reinterpret_cast<const VT*>(sinb + crow + oc));
+            }
+          }
+        }
+#endif
+        if (has) {
+          const VT za = norm_weight<T, V>(xa, r, wa);
           if (tail) {
             st_stream(reinterpret_cast<VT*>(yr + oa), za);
           } else {
-            const VT zb = norm_weight<T, V>(xb, r, ld_shared_ro(reinterpret_cast<const VT*>(w + ob)));
+            const VT zb = norm_weight<T, V>(xb, r, wb);
             if (valid) {
-              const int oc = k0 * V;
-              const VT c = ld_shared_ro(reinterpret_cast<const VT*>(cosb + crow + oc));
-              const VT sn = ld_shared_ro(reinterpret_cast<const VT*>(sinb + crow + oc));
               VT ya, yb;
               rotate_unit<T, V, INTER>(za, zb, c, sn, ya, yb);
               st_stream(reinterpret_cast<VT*>(yr + oa), ya);

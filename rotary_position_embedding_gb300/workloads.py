@@ -12,6 +12,9 @@ seed 2):
   X            N(0, 1) drawn in float32, rounded to the storage type.
   RoPE ids     ``pos[b, s] = s + off_b`` with ``off_b ~ U[0, 4096)`` (gather
                workload), or uniform over the cache rows.
+  Q/K/V        packed [Q|K|V] activations like X; past lengths
+               ``past[b] ~ U[0, max_past]`` (seed 1), positions past[b] + s;
+               QK-Norm weights ``U[0.5, 1.5)`` per channel (seed 3).
   M-RoPE ids   per batch: 1024 text tokens (t = h = w), 4 frames of a 32x32
                image grid (t = st + f, h = st + r, w = st + c), 1024 text
                tokens starting at the previous maximum + 1, 2 frames of a
@@ -121,6 +124,11 @@ WORKLOADS = {
         name="qkv_prefill_r3_f16", kind="qkv", rank=3, shape=(4, 2048, (32 + 2 * 8) * 128), dtype="float16",
         num_heads=32, positions="past", cache_rows=8192, rope_base=1.0e6, rope_dim=128,
         extra={"kv_num_heads": 8, "max_len": 4096, "max_past": 2048}),
+    # the same prefill with Qwen3's QK-Norm (RMSNorm of every Q and K head) first
+    "qkv_norm_prefill_r3_f16": Workload(
+        name="qkv_norm_prefill_r3_f16", kind="qkv", rank=3, shape=(4, 2048, (32 + 2 * 8) * 128),
+        dtype="float16", num_heads=32, positions="past", cache_rows=8192, rope_base=1.0e6, rope_dim=128,
+        extra={"kv_num_heads": 8, "max_len": 4096, "max_past": 2048, "rms_norm": True, "epsilon": 1e-6}),
     "qkv_decode_r3_f16": Workload(
         name="qkv_decode_r3_f16", kind="qkv", rank=3, shape=(256, 1, (32 + 2 * 8) * 128), dtype="float16",
         num_heads=32, positions="past", cache_rows=8192, rope_base=1.0e6, rope_dim=128,
@@ -218,6 +226,10 @@ def make_inputs(w: Workload, shard=0):
     if w.kind == "qkv":
         rng = np.random.default_rng(base + 1)
         out["past_seq_lens"] = rng.integers(0, w.extra["max_past"] + 1, size=B).astype(np.int32)
+        if w.extra.get("rms_norm"):
+            wrng = np.random.default_rng(base + 3)
+            out["q_norm_weight"] = wrng.uniform(0.5, 1.5, w.head_size).astype(w.dtype)
+            out["k_norm_weight"] = wrng.uniform(0.5, 1.5, w.head_size).astype(w.dtype)
     return out
 
 
@@ -233,7 +245,8 @@ def algorithmic_bytes(w: Workload, cached=True):
     if w.kind == "qkv":
         # Q, K, V read once; Q out, K and V into the caches; one cos/sin row
         # per token; the int32 past lengths (positions are implicit).
-        return xy + 2 * w.tokens * w.half * esz + 4 * w.batch
+        norm_w = 2 * w.head_size * esz if w.extra.get("rms_norm") else 0
+        return xy + 2 * w.tokens * w.half * esz + 4 * w.batch + norm_w
     npos = 3 if w.kind == "mrope" else (0 if w.positions == "none" else 1)
     pos = npos * w.tokens * 8
     if w.kind == "fused" and not cached:

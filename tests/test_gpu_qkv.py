@@ -193,19 +193,32 @@ def test_qkv_workload_full_size(lib, orc, cuda, name):
     kc = torch.full((B, Nkv, L, H), fill, dtype=torch.float16, device=cuda)
     vc = torch.full_like(kc, fill)
     status = torch.zeros(1, dtype=torch.int32, device=cuda)
+    norm = bool(w.extra.get("rms_norm"))
+    nkw = {}
+    if norm:
+        nkw = dict(q_norm_weight=inp["q_norm_weight"], k_norm_weight=inp["k_norm_weight"],
+                   epsilon=w.extra["epsilon"])
+        q_ref, k_ref, _, _, _, _ = orc.rope_qkv(x, cos, sin, pos, num_heads=Nq, kv_num_heads=Nkv, **nkw)
+        nkw = {**nkw, "q_norm_weight": _dev(nkw["q_norm_weight"], torch, cuda),
+               "k_norm_weight": _dev(nkw["k_norm_weight"], torch, cuda)}
     qo, ko = lib.rope_apply_qkv(_dev(x, torch, cuda), _dev(cos, torch, cuda), _dev(sin, torch, cuda), None,
                                 num_heads=Nq, kv_num_heads=Nkv, k_cache=kc, v_cache=vc,
-                                past_seq_lens=_dev(past, torch, cuda), status=status)
+                                past_seq_lens=_dev(past, torch, cuda), status=status, **nkw)
     torch.cuda.synchronize()
     assert ko is None and int(status.item()) == 0
     none_bad = np.zeros((B, S), dtype=bool)
-    compare(qo.cpu().numpy(), q_ref, _heads(x, B, S, 0, Nq, Ntot, H), 3, Nq,
-            _token_mask(B, S, Nq, H, H, none_bad))
     bi = torch.arange(B, device=cuda)[:, None].expand(B, S)
     ri = torch.from_numpy(pos).to(cuda)
     k_rows = kc[bi, :, ri].reshape(B, S, Nkv * H).cpu().numpy()
     v_rows = vc[bi, :, ri].reshape(B, S, Nkv * H).cpu().numpy()
-    compare(k_rows, k_ref, _heads(x, B, S, Nq, Nq + Nkv, Ntot, H), 3, Nkv, _token_mask(B, S, Nkv, H, H, none_bad))
+    if norm:
+        compare_norm(qo.cpu().numpy(), q_ref, Nq, H, H, 0)
+        compare_norm(k_rows, k_ref, Nkv, H, H, 0)
+    else:
+        compare(qo.cpu().numpy(), q_ref, _heads(x, B, S, 0, Nq, Ntot, H), 3, Nq,
+                _token_mask(B, S, Nq, H, H, none_bad))
+        compare(k_rows, k_ref, _heads(x, B, S, Nq, Nq + Nkv, Ntot, H), 3, Nkv,
+                _token_mask(B, S, Nkv, H, H, none_bad))
     assert np.array_equal(v_rows.view(np.uint16), _heads(x, B, S, Nq + Nkv, Ntot, Ntot, H).view(np.uint16))
     kc[bi, :, ri] = fill
     vc[bi, :, ri] = fill
