@@ -13,6 +13,7 @@ from .oracle import (  # noqa: F401
     double_to_half,
     half_to_double,
     mrope,
+    mrope_fused,
     mrope_map,
     mrope_stream_map,
     rope,

@@ -59,9 +59,11 @@ def _load():
             lib.oracle_rope_qkv_rmsnorm.argtypes = [i32, i64, i64, i64, i64, i64, i32, i64, vp, vp, vp, vp, vp,
                                                     ctypes.c_double, vp, vp, i64, vp, vp, vp, vp, vp, vp, i64,
                                                     _i64p, _i64p]
+            lib.oracle_mrope_fused.argtypes = [i32, i32, _i64p, i64, i32, i64, vp, vp, f32, vp, vp, i32, f32,
+                                               vp]
             for name in ("oracle_rope", "oracle_mrope_stream_map", "oracle_mrope_map", "oracle_mrope",
                          "oracle_rope_fused", "oracle_cache_build", "oracle_rope_qkv",
-                         "oracle_rope_qkv_rmsnorm"):
+                         "oracle_rope_qkv_rmsnorm", "oracle_mrope_fused"):
                 getattr(lib, name).restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -181,6 +183,23 @@ def rope_fused(x, inv_freq, position_ids, attention_scaling=1.0, interleaved=0, 
                                _ptr(pos), _ptr(y))
     if rc:
         raise ValueError("oracle_rope_fused: malformed arguments")
+    return y
+
+
+def mrope_fused(x, inv_freq, position_ids, mrope_section, mrope_layout=0, scale=1.0, attention_scaling=1.0,
+                interleaved=0, rotary_embedding_dim=0, num_heads=0):
+    """MRotaryEmbedding with cos/sin computed on the fly from inv_freq (three position streams)."""
+    lib = _load()
+    x = _c(x)
+    inv = _c(inv_freq, np.float32)
+    pos = _c(position_ids, np.int64)
+    sec = np.ascontiguousarray(mrope_section, dtype=np.int32)
+    y = np.empty_like(x)
+    rc = lib.oracle_mrope_fused(_dt(x), x.ndim, _shape(x), int(num_heads), int(interleaved),
+                                int(rotary_embedding_dim), _ptr(x), _ptr(inv), float(attention_scaling), _ptr(pos),
+                                _ptr(sec), int(mrope_layout), float(scale), _ptr(y))
+    if rc:
+        raise ValueError("oracle_mrope_fused: malformed arguments")
     return y
 
 

@@ -437,6 +437,53 @@ int oracle_rope_fused(int dt, int rank, const int64_t* xs, int64_t num_heads, in
   return 0;
 }
 
+/* ------------------------------------------------------------------------ */
+/* MRotaryEmbedding with on-the-fly coefficients.                           */
+/* [MR] Description and Inputs: coefficient index i follows one of the t,   */
+/* h, w position streams (mrope_section, mrope_layout) and the cached cos   */
+/* and sin are scaled by `scale` and rounded to T; [PR] Motivation and      */
+/* Context: the cache is cos/sin(p * inv_freq) * attention_scaling, which   */
+/* the on-the-fly form computes where it is used.                           */
+/* Reading: index i of token (b, s) takes the coefficients the cache build  */
+/* would store at row p = pos3[map[i], b, s] (coef_on_the_fly), then the    */
+/* scale step of oracle_mrope_map; with no table, no position is out of     */
+/* range (as oracle_rope_fused). For in-range positions this equals         */
+/* oracle_mrope over the oracle_cache_build table, bit for bit.             */
+/* ------------------------------------------------------------------------ */
+int oracle_mrope_fused(int dt, int rank, const int64_t* xs, int64_t num_heads, int interleaved,
+                       int64_t rotary_dim, const void* x, const float* inv_freq, float scaling,
+                       const int64_t* pos3, const int32_t* sec, int layout, float scale, void* y) {
+  geom g;
+  if (make_geom(rank, xs, num_heads, &g)) return 1;
+  int64_t rd = rotary_dim ? rotary_dim : g.H;
+  int64_t half = rd / 2;
+  if (rd % 2 || rd > g.H || rd <= 0 || half > 65536) return 1;
+  uint8_t map[65536];
+  if (oracle_mrope_stream_map(sec, layout, half, map)) return 1;
+  int64_t ntok = g.B * g.S;
+  for (int64_t b = 0; b < g.B; ++b) {
+    for (int64_t s = 0; s < g.S; ++s) {
+      int64_t tok = b * g.S + s;
+      for (int64_t n = 0; n < g.N; ++n) {
+        int64_t base = row_start(&g, b, s, n);
+        for (int64_t i = 0; i < half; ++i) {
+          int64_t j0, j1;
+          pair_elems(interleaved, half, i, &j0, &j1);
+          int64_t p = pos3[(int64_t)map[i] * ntok + tok];
+          double c, sn;
+          coef_on_the_fly(dt, p, inv_freq[i], scaling, &c, &sn);
+          c = round_to(dt, c * (double)scale);
+          sn = round_to(dt, sn * (double)scale);
+          rotate_store(dt, y, base + j0, base + j1, ld(dt, x, base + j0), ld(dt, x, base + j1), c,
+                       sn);
+        }
+        for (int64_t j = rd; j < g.H; ++j) cp(dt, x, base + j, y, base + j);
+      }
+    }
+  }
+  return 0;
+}
+
 /* The (rows, half) cos and sin tables: row p holds the on-the-fly
    coefficients of position p ([PR] Medium Issues 4: cos(freqs) * scaling). */
 int oracle_cache_build(int dt, const float* inv_freq, int64_t half, int64_t rows, float scaling,

@@ -47,6 +47,8 @@ MUTATIONS = {
                                     "double n = ld(dt, x, xb + j) * r;"),
     "norm_key_uses_query_weight": ("rms_norm_head(dt, ks, ksrc, H, k_weight, eps, zq);",
                                    "rms_norm_head(dt, ks, ksrc, H, q_weight, eps, zq);"),
+    "mrope_fused_stream_ignored": ("int64_t p = pos3[(int64_t)map[i] * ntok + tok];", "int64_t p = pos3[tok];"),
+    "mrope_fused_scale_dropped": ("c = round_to(dt, c * (double)scale);", "c = round_to(dt, c);"),
     "qkv_value_rotated": ("for (int64_t j = 0; j < H; ++j) cp(dt, vs, vsrc + j, v_cache, dst + j);",
                           "rope_one_head(dt, interleaved, H, rd, vs, vsrc, v_cache, dst, cos_t, sin_t, crow, valid);"),
 }

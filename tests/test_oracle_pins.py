@@ -735,3 +735,45 @@ def test_qkv_rmsnorm_scale_invariant_without_epsilon(orc):
                          key=(k / 8).astype(dtype), q_norm_weight=w, k_norm_weight=w, epsilon=0.0)
         assert np.array_equal(a[0].view(np.uint8), b[0].view(np.uint8))
         assert np.array_equal(a[1].view(np.uint8), b[1].view(np.uint8))
+
+
+# --------------------------------------------------------------------------
+# MRotaryEmbedding with on-the-fly coefficients (MRotaryEmbedding README:
+# Description, Inputs, Attributes; Qwen3 fusion PR: Motivation and Context)
+# --------------------------------------------------------------------------
+
+def test_mrope_fused_equals_cached_table(orc):
+    """On-the-fly M-RoPE == M-RoPE over the cache build's table, bit for bit, for every
+    layout, pairing, scale and a partial width (all positions in range)."""
+    rng = np.random.default_rng(81)
+    B, S, N, H, R = 2, 9, 3, 32, 200
+    for dtype in (np.float16, np.float32):
+        x = rng.standard_normal((B, S, N * H)).astype(dtype)
+        for rd, sec in ((0, (6, 5, 5)), (16, (4, 2, 2))):
+            h = (rd or H) // 2
+            inv = wl.inv_freq(10000.0, rd or H, h)
+            cos, sin = orc.cache_build(inv, R, dtype, 1.25)
+            pos3 = rng.integers(0, R, (3, B, S))
+            for layout in (0, 1):
+                for inter in (0, 1):
+                    for scale in (1.0, float(np.float32(0.7))):
+                        y_c, n_oor = orc.mrope(x, cos, sin, pos3, sec, layout, scale, inter, rd, N)
+                        assert n_oor == 0
+                        y_f = orc.mrope_fused(x, inv, pos3, sec, layout, scale, 1.25, inter, rd, N)
+                        assert np.array_equal(y_f.view(np.uint8), y_c.view(np.uint8)), (dtype, rd, layout, inter)
+
+
+def test_mrope_fused_equal_streams_reduce_to_fused_rope(orc):
+    """Equal t/h/w streams and scale 1: exactly the on-the-fly RotaryEmbedding (which has no
+    out-of-range positions either, so large and negative positions are fine)."""
+    rng = np.random.default_rng(82)
+    B, S, N, H = 2, 7, 2, 16
+    for dtype in (np.float16, np.float32):
+        x = rng.standard_normal((B, S, N * H)).astype(dtype)
+        inv = wl.inv_freq(1.0e6, H, H // 2)
+        pos = rng.integers(-5000, 1 << 40, (B, S))
+        pos3 = np.stack([pos, pos, pos])
+        y_r = orc.rope_fused(x, inv, pos, 1.0, 0, 0, N)
+        for layout in (0, 1):
+            y_m = orc.mrope_fused(x, inv, pos3, (4, 2, 2), layout, 1.0, 1.0, 0, 0, N)
+            assert np.array_equal(y_m.view(np.uint8), y_r.view(np.uint8))
