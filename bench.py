@@ -299,7 +299,7 @@ class Step:
         if w.kind == "rope" and w.positions == "none":
             c, s = rp.rope_cache_build(self.inv, w.tokens, tdt)
             self.cos, self.sin = c.view(w.batch, w.seq, w.half), s.view(w.batch, w.seq, w.half)
-        elif w.kind in ("rope", "mrope") or w.kind == "fused":
+        elif w.kind in ("rope", "mrope", "fused", "mrope_fused"):
             self.cos, self.sin = rp.rope_cache_build(self.inv, w.cache_rows, tdt,
                                                      attention_scaling=w.attention_scaling)
         self.cshape = (ctypes.c_int64 * self.cos.dim())(*self.cos.shape)
@@ -330,7 +330,11 @@ class Step:
         scr = self.scratch_for(stream)
         cos = ctypes.c_void_p(self.cos.data_ptr())
         sin = ctypes.c_void_p(self.sin.data_ptr())
-        if w.kind == "mrope":
+        if w.kind == "mrope_fused" and fused:
+            st = lib.mrope_apply_fused(self.code, w.rank, self.xshape, x, y, ctypes.c_void_p(self.inv.data_ptr()),
+                                       w.attention_scaling, pos, self.sec, w.mrope_layout, w.scale, w.interleaved,
+                                       w.rotary_embedding_dim, self.nh, stream)
+        elif w.kind in ("mrope", "mrope_fused"):
             st = lib.mrope_apply(self.code, w.rank, self.xshape, x, y, w.cache_rows, cos, sin, pos, self.sec,
                                  w.mrope_layout, w.scale, w.interleaved, w.rotary_embedding_dim, self.nh, 0,
                                  None, scr, stream)
@@ -493,7 +497,7 @@ def measure_rows(args, torch, rp, device, peak):
     prev = rp.get_variant()
     for name, w in wl.WORKLOADS.items():
         variants = [("cached", False, "auto"), ("cached", False, "simt")]
-        if w.kind == "fused":
+        if w.kind in ("fused", "mrope_fused"):
             variants = [("fused", True, "auto"), ("cached", False, "auto")]
         if w.kind == "qkv":
             variants = [("fused", True, "auto"), ("unfused", False, "auto")]
@@ -601,7 +605,7 @@ class OracleStep:
             self.x = np.ascontiguousarray(x[:nb, :, :s_keep])
         if pos is None:
             self.pos = None
-        elif w.kind == "mrope":
+        elif w.kind in ("mrope", "mrope_fused"):
             self.pos = np.ascontiguousarray(pos[:, :nb, :s_keep])
         else:
             self.pos = np.ascontiguousarray(pos[:nb, :s_keep])
@@ -628,6 +632,9 @@ class OracleStep:
         elif w.kind == "mrope":
             o.mrope(self.x, self.cos, self.sin, self.pos, w.mrope_section, w.mrope_layout, w.scale,
                     w.interleaved, w.rotary_embedding_dim, self.nh)
+        elif w.kind == "mrope_fused":
+            o.mrope_fused(self.x, self.inv, self.pos, w.mrope_section, w.mrope_layout, w.scale,
+                          w.attention_scaling, w.interleaved, w.rotary_embedding_dim, self.nh)
         else:
             o.rope(self.x, self.cos, self.sin, self.pos, w.interleaved, w.rotary_embedding_dim, self.nh)
 

@@ -288,6 +288,31 @@ rope_status rope_apply_qkv_rmsnorm(rope_dtype dtype, int64_t batch, int64_t seq,
                                    int32_t* status_flags, rope_stream_t stream);
 
 /*
+ * mrope_apply_fused -- MRotaryEmbedding with cos/sin computed on the fly
+ * ([MRotaryEmbedding README, Description, Inputs, Attributes] for the three
+ * position streams, mrope_section / mrope_layout and scale; [Qwen3 fusion
+ * pull request, Motivation and Context] for the on-the-fly coefficients).
+ *
+ * Coefficient index i of token (b, s) follows stream m(i) (the map of
+ * mrope_apply) at position p = position_ids[m(i), b, s]; its cos/sin are the
+ * values rope_cache_build(inv_freq, attention_scaling) stores at row p, then
+ * multiplied by `scale` and rounded to T as mrope_apply does. With no table
+ * no position is out of range. Wherever the positions lie inside a table
+ * built by rope_cache_build, the result equals mrope_apply over that table,
+ * bit for bit.
+ *
+ * inv_freq      device float32[rd/2].
+ * position_ids  device int64 (3, B, S), required.
+ * Other arguments, layouts, ownership and errors as mrope_apply (no cache,
+ * no status word, no scratch; packed batching is not offered).
+ */
+rope_status mrope_apply_fused(rope_dtype dtype, int32_t x_rank, const int64_t* x_shape, const void* x,
+                              void* y, const float* inv_freq, float attention_scaling,
+                              const int64_t* position_ids, const int32_t* mrope_section,
+                              int32_t mrope_layout, float scale, int32_t interleaved,
+                              int32_t rotary_embedding_dim, int32_t num_heads, rope_stream_t stream);
+
+/*
  * rope_cache_build -- the (rows, half) cos and sin tables of rope_apply's
  * 2-D cache: row p holds the coefficients rope_apply_fused computes for
  * position p ([Qwen3 fusion pull request, Medium Issues 4: cos(freqs) *

@@ -49,6 +49,7 @@ SIGNATURES = {
                                _i32, _i32, _vp, _vp, _vp],
     "mrope_stream_map": [_i32p, _i32, _i32, _u8p],
     "rope_apply_fused": [_i32, _i32, _i64p, _vp, _vp, _vp, _f32, _vp, _i32, _i32, _i32, _vp],
+    "mrope_apply_fused": [_i32, _i32, _i64p, _vp, _vp, _vp, _f32, _vp, _i32p, _i32, _f32, _i32, _i32, _i32, _vp],
     "rope_cache_build": [_i32, _vp, _i32, _i64, _f32, _vp, _vp, _vp],
     "rope_apply_qkv": [_i32, _i64, _i64, _i32, _i32, _i64, _vp, _vp, _vp, _vp, _vp, _i64, _vp, _vp, _i32,
                        _i32, _vp, _vp, _vp, _vp, _i64, _vp, _vp],
@@ -334,6 +335,27 @@ def rope_apply_qkv(query, cos_cache, sin_cache, position_ids=None, *, num_heads,
                                     _stream(query, stream))
     _check("rope_apply_qkv_rmsnorm" if norm else "rope_apply_qkv", st)
     return q_out, (None if cache else k_out)
+
+
+def mrope_apply_fused(x, inv_freq, position_ids, mrope_section, *, mrope_layout=0, scale=1.0,
+                      attention_scaling=1.0, interleaved=0, rotary_embedding_dim=0, num_heads=0, out=None,
+                      stream=None):
+    """MRotaryEmbedding with cos/sin computed on the fly from inv_freq (three position streams)."""
+    import torch
+
+    lib = load_library()
+    _cuda("x", x)
+    _cuda("inv_freq", inv_freq, torch.float32)
+    _cuda("position_ids", position_ids, torch.int64)
+    y = _out(x, out)
+    sec = (ctypes.c_int32 * 3)(*[int(v) for v in mrope_section])
+    with torch.cuda.device(x.device):
+        st = lib.mrope_apply_fused(_dtype_code(x), x.dim(), _shape(x), _ptr(x), _ptr(y), _ptr(inv_freq),
+                                   float(attention_scaling), _ptr(position_ids), sec, int(mrope_layout),
+                                   float(scale), int(interleaved), int(rotary_embedding_dim), int(num_heads),
+                                   _stream(x, stream))
+    _check("mrope_apply_fused", st)
+    return y
 
 
 def rope_cache_build(inv_freq, rows, dtype=None, *, attention_scaling=1.0, cos_out=None, sin_out=None,

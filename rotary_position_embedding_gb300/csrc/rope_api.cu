@@ -955,4 +955,46 @@ const char* rope_status_string(rope_status status) {
 
 const char* rope_last_error(void) { return g_last_error.c_str(); }
 
+rope_status mrope_apply_fused(rope_dtype dtype, int32_t x_rank, const int64_t* x_shape, const void* x,
+                              void* y, const float* inv_freq, float attention_scaling,
+                              const int64_t* position_ids, const int32_t* mrope_section,
+                              int32_t mrope_layout, float scale, int32_t interleaved,
+                              int32_t rotary_embedding_dim, int32_t num_heads, rope_stream_t stream) {
+  g_last_error.clear();
+  ROPE_TRY(check_dtype(dtype));
+  if (!mrope_section) return fail(ROPE_ERR_INVALID_ARG, "mrope_section is NULL");
+  Geom g;
+  ROPE_TRY(x_geometry(x_rank, x_shape, num_heads, &g));
+  if (interleaved != 0 && interleaved != 1)
+    return fail(ROPE_ERR_INVALID_ARG, "interleaved must be 0 or 1 (got %d)", interleaved);
+  ROPE_TRY(rotary_width(rotary_embedding_dim, /*odd_head_ok=*/true, &g));
+  if (g.h > kMaxMRopeHalf)
+    return fail(ROPE_ERR_UNSUPPORTED, "M-RoPE rotary width / 2 = %lld exceeds %d", (long long)g.h,
+                kMaxMRopeHalf);
+  uint8_t map[kMaxMRopeHalf];
+  if (g.h > 0) ROPE_TRY(build_stream_map(mrope_section, mrope_layout, g.h, map));
+  if (g.numel == 0) return ROPE_OK;
+  const int es = elem_size(dtype);
+  ROPE_TRY(check_elem_ptr(x, "x", es));
+  ROPE_TRY(check_elem_ptr(y, "y", es));
+  ROPE_TRY(check_elem_ptr(inv_freq, "inv_freq", 4));
+  ROPE_TRY(check_elem_ptr(position_ids, "position_ids", 8));
+
+  const bool vec = vector_ok(g, es, {x, y});
+  const void* fn = fused_kernel(dtype, vec, interleaved != 0, x_rank == 4, /*mrope=*/true);
+  KParams kp;
+  memset(&kp, 0, sizeof(kp));
+  kp.x = x;
+  kp.y = y;
+  kp.pos = position_ids;
+  kp.inv_freq = inv_freq;
+  kp.scale = attention_scaling;
+  kp.mscale = scale;
+  kp.mscale_is_one = scale == 1.0f;
+  for (int64_t i = 0; i < g.h; ++i) kp.smap[i >> 4] |= (uint32_t)map[i] << ((i & 15) * 2);
+  Launch L;
+  ROPE_TRY(plan(g, es, vec, fn, true, &kp, &L));
+  return launch(fn, L, &kp, stream, "rope_fused_kernel");
+}
+
 }  // extern "C"

@@ -49,6 +49,8 @@ struct KParams {
   int64_t step_b, step_s;  // step_tok = step_b * S + step_s
   uint32_t smap[kMaxMRopeHalf / 16];  // M-RoPE: 2-bit stream of each coefficient index
   unsigned long long* sched;  // TMA path: tile counter pair for the dynamic schedule, or null
+  float mscale;          // on-the-fly M-RoPE: the M-RoPE scale (scale holds attention scaling)
+  int32_t mscale_is_one;
 };
 
 // Q/K rotation with the key/value cache append (rope_qkv_kernel): the routing
@@ -74,7 +76,7 @@ struct QKVParams {
 // the 128-bit vector path. Return nullptr for unsupported combinations.
 const void* rope_kernel_cached(int dtype, bool vec, bool interleaved, bool rank4, Coef mode);
 const void* rope_kernel_mrope(int dtype, bool vec, bool interleaved, bool rank4);
-const void* fused_kernel(int dtype, bool vec, bool interleaved, bool rank4);
+const void* fused_kernel(int dtype, bool vec, bool interleaved, bool rank4, bool mrope = false);
 const void* cache_build_kernel(int dtype);
 // rope_qkv_kernel instance; its launch takes (KParams, QKVParams).
 const void* qkv_kernel(int dtype, bool vec, bool interleaved, bool implicit_pos, bool rms_norm);

@@ -534,7 +534,12 @@ __device__ __forceinline__ void coef_on_the_fly(int64_t pos, float inv, float sc
 // Fused rotation: per tile of TTs tokens the CTA first fills a shared-memory
 // table of the tile's rd/2 coefficients (one double-precision sincos per
 // token and index, not per head), then every thread rotates its unit from it.
-template <class T, int V, bool INTER, bool RANK4>
+// MROPE: index i takes the position of its stream (t, h or w, from the stream
+// map), and the coefficient is then scaled and rounded to T as the cached
+// M-RoPE path does ("com.microsoft.MRotaryEmbedding" README, Description and
+// Attributes/scale), so the result equals M-RoPE over rope_cache_build's
+// table wherever the positions are inside that table.
+template <class T, int V, bool INTER, bool RANK4, bool MROPE>
 __global__ void __launch_bounds__(kMaxRowThreads) rope_fused_kernel(const KParams p) {
   using E = Elem<T>;
   using VT = VecT<T, V>;
@@ -565,10 +570,22 @@ __global__ void __launch_bounds__(kMaxRowThreads) rope_fused_kernel(const KParam
       const int i = it - ls * p.h;
       const int64_t t = tile0 + ls;
       if (t < p.ntok) {
+        int64_t pp;
+        if (MROPE) {
+          const int st = (int)((p.smap[i >> 4] >> ((i & 15) * 2)) & 3u);
+          pp = __ldg(p.pos + st * p.ntok + t);
+        } else {
+          pp = __ldg(p.pos + t);
+        }
         float c, s;
-        coef_on_the_fly(__ldg(p.pos + t), __ldg(p.inv_freq + i), p.scale, c, s);
-        sc[it] = E::fromf(c);
-        ss[it] = E::fromf(s);
+        coef_on_the_fly(pp, __ldg(p.inv_freq + i), p.scale, c, s);
+        bits cb = E::fromf(c), sb = E::fromf(s);
+        if (MROPE && !p.mscale_is_one) {
+          cb = E::fromf(E::mul_round(E::tof(cb), p.mscale));
+          sb = E::fromf(E::mul_round(E::tof(sb), p.mscale));
+        }
+        sc[it] = cb;
+        ss[it] = sb;
       }
     }
     __syncthreads();

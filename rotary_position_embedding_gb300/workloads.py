@@ -133,6 +133,13 @@ WORKLOADS = {
         name="qkv_decode_r3_f16", kind="qkv", rank=3, shape=(256, 1, (32 + 2 * 8) * 128), dtype="float16",
         num_heads=32, positions="past", cache_rows=8192, rope_base=1.0e6, rope_dim=128,
         extra={"kv_num_heads": 8, "max_len": 4096, "max_past": 4095}),
+    # M-RoPE decode with the coefficients computed on the fly (Qwen-VL
+    # attention shape: 28 heads of 128, sections [16, 24, 24], interleaved
+    # layout), against the same step over a (32768, 64) table
+    "mrope_fused_decode_r3_f16": Workload(
+        name="mrope_fused_decode_r3_f16", kind="mrope_fused", rank=3, shape=(256, 1, 28 * 128), dtype="float16",
+        num_heads=28, positions="mrope", cache_rows=32768, rope_base=1.0e6, rope_dim=128,
+        mrope_section=(16, 24, 24), mrope_layout=1, scale=1.0),
     "fused_decode_r3_f16": Workload(
         name="fused_decode_r3_f16", kind="fused", rank=3, shape=(256, 1, 40 * 128), dtype="float16",
         num_heads=40, positions="uniform", cache_rows=32768, rope_base=1.0e6, rope_dim=128,
@@ -247,9 +254,9 @@ def algorithmic_bytes(w: Workload, cached=True):
         # per token; the int32 past lengths (positions are implicit).
         norm_w = 2 * w.head_size * esz if w.extra.get("rms_norm") else 0
         return xy + 2 * w.tokens * w.half * esz + 4 * w.batch + norm_w
-    npos = 3 if w.kind == "mrope" else (0 if w.positions == "none" else 1)
+    npos = 3 if w.kind in ("mrope", "mrope_fused") else (0 if w.positions == "none" else 1)
     pos = npos * w.tokens * 8
-    if w.kind == "fused" and not cached:
+    if w.kind in ("fused", "mrope_fused") and not cached:
         coef = w.half * 4
     else:
         coef = 2 * w.tokens * w.half * esz

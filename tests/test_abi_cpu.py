@@ -30,7 +30,7 @@ def test_header_declares_the_abi():
     for name in ("rope_apply", "mrope_apply", "mrope_apply_stream_map", "mrope_stream_map",
                  "rope_apply_fused", "rope_cache_build", "rope_status_string", "rope_last_error",
                  "rope_set_variant", "rope_get_variant", "rope_last_kernel", "rope_apply_no_alloc",
-                 "rope_apply_qkv", "rope_apply_qkv_rmsnorm"):
+                 "rope_apply_qkv", "rope_apply_qkv_rmsnorm", "mrope_apply_fused"):
         assert name in fns
 
 
@@ -269,5 +269,32 @@ def _qkv_norm(so, **kw):
 def test_rope_apply_qkv_rmsnorm_rejects_before_launch(lib, kw, status):
     so = lib.load_library()
     st = _qkv_norm(so, **kw)
+    assert st == status, so.rope_last_error().decode()
+    assert so.rope_last_error().decode() != ""
+
+
+def _mrope_fused(so, **kw):
+    a = dict(dtype=F16, rank=3, xs=_i64(2, 4, 32), x=FAKE, y=FAKE2, inv=FAKE3, scaling=1.0, pos=FAKE4,
+             sec=(ctypes.c_int32 * 3)(2, 1, 1), layout=0, scale=1.0, inter=0, rd=0, nh=4, stream=None)
+    a.update(kw)
+    return so.mrope_apply_fused(a["dtype"], a["rank"], a["xs"], a["x"], a["y"], a["inv"], a["scaling"], a["pos"],
+                                a["sec"], a["layout"], a["scale"], a["inter"], a["rd"], a["nh"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(dtype=99), UNSUPPORTED),
+    (dict(sec=None), INVALID),
+    (dict(sec=(ctypes.c_int32 * 3)(2, 2, 1)), INVALID),     # sections must sum to rd/2 = 4
+    (dict(sec=(ctypes.c_int32 * 3)(5, -1, 0)), INVALID),
+    (dict(layout=2), INVALID),
+    (dict(inter=3), INVALID),
+    (dict(nh=3), INVALID),
+    (dict(pos=None), INVALID),
+    (dict(inv=ctypes.c_void_p(0x30002)), INVALID),           # misaligned float32 inv_freq
+    (dict(x=None), INVALID),
+])
+def test_mrope_apply_fused_rejects_before_launch(lib, kw, status):
+    so = lib.load_library()
+    st = _mrope_fused(so, **kw)
     assert st == status, so.rope_last_error().decode()
     assert so.rope_last_error().decode() != ""

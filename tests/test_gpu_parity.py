@@ -439,6 +439,58 @@ def test_fused_grid(lib, orc, cuda, torch_mod, dt, rank, inter, rd, scaling):
     assert torch.equal(yc.view(bits), yf.view(bits))
 
 
+@pytest.mark.parametrize("dt,rank,layout,inter,rd,scale,path", [c + ("vector",) for c in itertools.product(
+    ["f16", "f32"], [3, 4], [0, 1], [0, 1], [0, 32], [1.0, 0.7])] + [
+    ("f16", 3, 1, 0, 0, 0.7, "scalar_misaligned"), ("f32", 4, 0, 1, 32, 1.0, "scalar_misaligned"),
+    ("f16", 3, 1, 1, 10, 0.7, "scalar_shape")])
+def test_mrope_fused_grid(lib, orc, cuda, torch_mod, dt, rank, layout, inter, rd, scale, path):
+    """M-RoPE on the fly against the oracle; where every position lies inside a
+    rope_cache_build table, bit for bit equal to mrope_apply over that table."""
+    torch = torch_mod
+    dtype = DT[dt]
+    rng = np.random.default_rng(_seed(dt, rank, layout, inter, rd, scale, path))
+    B, S, N, H = 4, 29, 5, 64 if path != "scalar_shape" else 14
+    h = (rd or H) // 2
+    sec = (h - 2 * (h // 3), h // 3, h // 3)
+    shape = _x_shape(rank, B, S, N, H)
+    x = rng.standard_normal(shape).astype(dtype)
+    inv = wl.inv_freq(1e6, rd or H, h)
+    R = 8192
+    pos3 = rng.integers(0, R, (3, B, S))
+    scale = float(np.float32(scale))
+    nh = N if rank == 3 else 0
+    off = 1 if path == "scalar_misaligned" else 0
+    y_ref = orc.mrope_fused(x, inv, pos3, sec, layout, scale, 0.9, inter, rd, nh)
+    xd, ind, pd = _dev(x, torch, cuda, off), _dev(inv, torch, cuda), _dev(pos3, torch, cuda)
+    yf = lib.mrope_apply_fused(xd, ind, pd, sec, mrope_layout=layout, scale=scale, attention_scaling=0.9,
+                               interleaved=inter, rotary_embedding_dim=rd, num_heads=nh)
+    torch.cuda.synchronize()
+    assert lib.last_kernel() == "rope_fused_kernel"
+    compare(_host(yf), y_ref, x, rank, N, rope_passthrough_mask(shape, rank, N, rd, None, 0))
+    cd, sd = lib.rope_cache_build(ind, R, torch.float16 if dt == "f16" else torch.float32,
+                                  attention_scaling=0.9)
+    yc = lib.mrope_apply(xd, cd, sd, pd, sec, mrope_layout=layout, scale=scale, interleaved=inter,
+                         rotary_embedding_dim=rd, num_heads=nh)
+    torch.cuda.synchronize()
+    bits = torch.int16 if dt == "f16" else torch.int32
+    assert torch.equal(yc.view(bits), yf.view(bits))
+
+
+def test_mrope_fused_any_position(lib, orc, cuda, torch_mod):
+    """No table, so no position is out of range: large and negative ids rotate too."""
+    torch = torch_mod
+    rng = np.random.default_rng(91)
+    B, S, N, H = 2, 16, 4, 128
+    x = rng.standard_normal((B, S, N * H)).astype(np.float16)
+    inv = wl.inv_freq(1e6, H, H // 2)
+    pos3 = rng.integers(-(1 << 20), 1 << 40, (3, B, S))
+    y_ref = orc.mrope_fused(x, inv, pos3, (16, 24, 24), 1, 1.0, 1.0, 0, 0, N)
+    yf = lib.mrope_apply_fused(_dev(x, torch, cuda), _dev(inv, torch, cuda), _dev(pos3, torch, cuda),
+                               (16, 24, 24), mrope_layout=1, num_heads=N)
+    torch.cuda.synchronize()
+    compare(_host(yf), y_ref, x, 3, N, None)
+
+
 @pytest.mark.parametrize("dt,base,scaling", list(itertools.product(["f16", "f32"], [1e4, 1e6],
                                                                     [1.0, 0.7071067690849304])))
 def test_cache_build_vs_oracle(lib, orc, cuda, torch_mod, dt, base, scaling):
@@ -516,6 +568,14 @@ def test_workload_full_size(lib, orc, cuda, torch_mod, name):
                                       w.cache_rows, smap, w.interleaved)
         torch.cuda.synchronize()
         assert int(flag.item()) == 1
+    elif w.kind == "mrope_fused":
+        y_ref = orc.mrope_fused(x, inv, pos, w.mrope_section, w.mrope_layout, w.scale, w.attention_scaling,
+                                w.interleaved, w.rotary_embedding_dim, nh)
+        yd = lib.mrope_apply_fused(xd, ind, _dev(pos, torch, cuda), w.mrope_section, mrope_layout=w.mrope_layout,
+                                   scale=w.scale, attention_scaling=w.attention_scaling, interleaved=w.interleaved,
+                                   rotary_embedding_dim=w.rotary_embedding_dim, num_heads=nh)
+        mask = rope_passthrough_mask(x.shape, w.rank, w.num_heads, w.rotary_embedding_dim, None, 0)
+        torch.cuda.synchronize()
     else:  # fused decode, and the cached path it replaces
         y_ref = orc.rope_fused(x, inv, pos, w.attention_scaling, w.interleaved, w.rotary_embedding_dim, nh)
         pd = _dev(pos, torch, cuda)
