@@ -8,8 +8,11 @@ only compiles it and marshals numpy arrays through ctypes.
 """
 
 from .oracle import (  # noqa: F401
+    BF16_BITS,
+    bf16_to_double,
     build,
     cache_build,
+    double_to_bf16,
     double_to_half,
     half_to_double,
     mrope,

@@ -18,7 +18,9 @@ _LIB = os.path.join(_HERE, "_build", "librope_oracle.so")
 _lock = threading.Lock()
 _lib = None
 
-F32, F16 = 0, 1
+F32, F16, BF16 = 0, 1, 2
+# numpy has no bfloat16: bfloat16 arrays travel as their uint16 bit patterns.
+BF16_BITS = np.uint16
 
 _i64p = ctypes.POINTER(ctypes.c_int64)
 
@@ -46,6 +48,10 @@ def _load():
             lib.oracle_half_to_double.restype = ctypes.c_double
             lib.oracle_double_to_half.argtypes = [ctypes.c_double]
             lib.oracle_double_to_half.restype = ctypes.c_uint16
+            lib.oracle_bf16_to_double.argtypes = [ctypes.c_uint16]
+            lib.oracle_bf16_to_double.restype = ctypes.c_double
+            lib.oracle_double_to_bf16.argtypes = [ctypes.c_double]
+            lib.oracle_double_to_bf16.restype = ctypes.c_uint16
             lib.oracle_rope.argtypes = [i32, i32, _i64p, i64, i32, i64, vp, vp, vp, i64, vp, vp, _i64p]
             lib.oracle_mrope_stream_map.argtypes = [vp, i32, i64, vp]
             lib.oracle_mrope_map.argtypes = [i32, i32, _i64p, i64, i32, i64, vp, vp, vp, i64, vp, vp,
@@ -74,10 +80,14 @@ def _dt(a):
         return F16
     if a.dtype == np.float32:
         return F32
-    raise TypeError(f"oracle supports float16/float32, got {a.dtype}")
+    if a.dtype == BF16_BITS:
+        return BF16
+    raise TypeError(f"oracle supports float16, float32 and bfloat16 (uint16 bits), got {a.dtype}")
 
 
 def _c(a, dtype=None):
+    if dtype is not None and np.dtype(dtype) == BF16_BITS and np.asarray(a).dtype != BF16_BITS:
+        raise TypeError("bfloat16 arrays travel as uint16 bit patterns; convert before the call")
     a = np.ascontiguousarray(a if dtype is None else a.astype(dtype, copy=False))
     return a
 
@@ -93,6 +103,14 @@ def _shape(x):
 
 def half_to_double(bits):
     return _load().oracle_half_to_double(int(bits))
+
+
+def bf16_to_double(bits):
+    return _load().oracle_bf16_to_double(int(bits))
+
+
+def double_to_bf16(v):
+    return _load().oracle_double_to_bf16(float(v))
 
 
 def double_to_half(v):

@@ -11,7 +11,7 @@
  * Plain, single-threaded and slow on purpose. Every loop follows the operator
  * definition element by element. Arithmetic is binary64 wherever the
  * definition does not fix a narrower type, and each output is rounded once,
- * to nearest-even, to the storage type T (float32 or float16). The only steps
+ * to nearest-even, to the storage type T (float32, float16 or bfloat16). The only steps
  * done in binary32 are the ones the modelling code fixes to float32 (the
  * angle product and the cos/sin values of the on-the-fly variant).
  *
@@ -45,7 +45,7 @@
 #include <stdint.h>
 #include <string.h>
 
-enum { ORC_F32 = 0, ORC_F16 = 1 };
+enum { ORC_F32 = 0, ORC_F16 = 1, ORC_BF16 = 2 };
 
 /* ------------------------------------------------------------------------ */
 /* IEEE 754 binary16, written out from the format: 1 sign bit, 5 exponent   */
@@ -93,22 +93,73 @@ uint16_t oracle_double_to_half(double v) {
   return (uint16_t)(sign | (uint16_t)((E + 15) << 10) | (uint16_t)(r - 1024.0));
 }
 
+/* ------------------------------------------------------------------------ */
+/* bfloat16, written out from the format: 1 sign bit, 8 exponent bits      */
+/* (bias 127), 7 fraction bits; exponent field 0 is subnormal (unit        */
+/* 2^-133), field 255 is infinity or NaN. (The pages list only float32 and  */
+/* float16; bfloat16 storage is offered beyond them with the same          */
+/* arithmetic and one final rounding.)                                     */
+/* ------------------------------------------------------------------------ */
+double oracle_bf16_to_double(uint16_t h) {
+  int sign = (h >> 15) & 1;
+  int e = (h >> 7) & 0xff;
+  int m = h & 0x7f;
+  double v;
+  if (e == 0) {
+    v = ldexp((double)m, -133);
+  } else if (e == 255) {
+    v = m ? NAN : INFINITY;
+  } else {
+    v = ldexp((double)(m + 128), e - 134);
+  }
+  return sign ? -v : v;
+}
+
+/* Round a binary64 value to bfloat16, nearest-even, in one step. */
+uint16_t oracle_double_to_bf16(double v) {
+  uint16_t sign = signbit(v) ? 0x8000 : 0;
+  double a = fabs(v);
+  if (isnan(v)) return (uint16_t)(sign | 0x7fc0);
+  /* 255 * 2^120 is the largest finite value; 255.5 * 2^120, the midpoint to
+     2^128, ties to the even neighbour, which is the overflow to infinity. */
+  if (a >= ldexp(255.5, 120)) return (uint16_t)(sign | 0x7f80);
+  if (a < ldexp(1.0, -126)) {
+    /* subnormal range: an integer number of 2^-133 units (128 is the
+       smallest normal, which the encoding below gives for free) */
+    double r = nearbyint(ldexp(a, 133));
+    return (uint16_t)(sign | (uint16_t)r);
+  }
+  int e;
+  (void)frexp(a, &e);
+  int E = e - 1;
+  double r = nearbyint(ldexp(a, 7 - E)); /* significand in [128, 256] */
+  if (r == 256.0) {
+    r = 128.0;
+    E += 1;
+  }
+  if (E > 127) return (uint16_t)(sign | 0x7f80);
+  return (uint16_t)(sign | (uint16_t)((E + 127) << 7) | (uint16_t)(r - 128.0));
+}
+
 /* Element access by storage type T. */
 static double ld(int dt, const void* base, int64_t i) {
   if (dt == ORC_F16) return oracle_half_to_double(((const uint16_t*)base)[i]);
+  if (dt == ORC_BF16) return oracle_bf16_to_double(((const uint16_t*)base)[i]);
   return (double)((const float*)base)[i];
 }
 
 static void st(int dt, void* base, int64_t i, double v) {
   if (dt == ORC_F16)
     ((uint16_t*)base)[i] = oracle_double_to_half(v);
+  else if (dt == ORC_BF16)
+    ((uint16_t*)base)[i] = oracle_double_to_bf16(v);
   else
     ((float*)base)[i] = (float)v;
 }
 
 /* Bit-exact copy of one element: pass-through never re-rounds. */
 static void cp(int dt, const void* src, int64_t si, void* dst, int64_t di) {
-  if (dt == ORC_F16)
+  if (dt == ORC_F16 || dt == ORC_BF16)
     ((uint16_t*)dst)[di] = ((const uint16_t*)src)[si];
   else
     memcpy((float*)dst + di, (const float*)src + si, sizeof(float));
@@ -117,6 +168,7 @@ static void cp(int dt, const void* src, int64_t si, void* dst, int64_t di) {
 /* The value of v after rounding to T. */
 static double round_to(int dt, double v) {
   if (dt == ORC_F16) return oracle_half_to_double(oracle_double_to_half(v));
+  if (dt == ORC_BF16) return oracle_bf16_to_double(oracle_double_to_bf16(v));
   return (double)(float)v;
 }
 

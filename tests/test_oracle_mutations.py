@@ -49,6 +49,8 @@ MUTATIONS = {
                                    "rms_norm_head(dt, ks, ksrc, H, q_weight, eps, zq);"),
     "mrope_fused_stream_ignored": ("int64_t p = pos3[(int64_t)map[i] * ntok + tok];", "int64_t p = pos3[tok];"),
     "mrope_fused_scale_dropped": ("c = round_to(dt, c * (double)scale);", "c = round_to(dt, c);"),
+    "bf16_exponent_bias": ("v = ldexp((double)(m + 128), e - 134);", "v = ldexp((double)(m + 128), e - 133);"),
+    "bf16_rounding_truncates": ("double r = nearbyint(ldexp(a, 7 - E));", "double r = floor(ldexp(a, 7 - E));"),
     "qkv_value_rotated": ("for (int64_t j = 0; j < H; ++j) cp(dt, vs, vsrc + j, v_cache, dst + j);",
                           "rope_one_head(dt, interleaved, H, rd, vs, vsrc, v_cache, dst, cos_t, sin_t, crow, valid);"),
 }

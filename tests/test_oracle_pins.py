@@ -777,3 +777,89 @@ def test_mrope_fused_equal_streams_reduce_to_fused_rope(orc):
         for layout in (0, 1):
             y_m = orc.mrope_fused(x, inv, pos3, (4, 2, 2), layout, 1.0, 1.0, 0, 0, N)
             assert np.array_equal(y_m.view(np.uint8), y_r.view(np.uint8))
+
+
+# --------------------------------------------------------------------------
+# bfloat16 conversion (storage offered beyond the pages' float32/float16)
+# against torch's independent implementation and exact arithmetic
+# --------------------------------------------------------------------------
+
+def test_bf16_to_double_all_patterns(orc):
+    torch = pytest.importorskip("torch")
+    bits = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    ref = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
+    got = np.array([orc.bf16_to_double(int(b)) for b in bits])
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], ref[~nan])
+
+
+def test_double_to_bf16_midpoints_and_random_float32(orc):
+    """float32 inputs (so torch's float32 -> bfloat16 rounding is a single rounding):
+    every bf16 midpoint, its float32 neighbours, and random values across the range."""
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(61)
+    finite = np.arange(0, 0x7f80, dtype=np.uint32)
+    mids = ((finite << 16) | 0x8000).view(np.float32)                 # exactly halfway
+    vals = np.concatenate([mids, np.nextafter(mids, np.float32(np.inf)), np.nextafter(mids, np.float32(0)),
+                           rng.standard_normal(20000).astype(np.float32) * np.float32(10.0) ** rng.integers(
+                               -40, 38, 20000).astype(np.float32)])
+    vals = vals[np.isfinite(vals)]
+    vals = np.concatenate([vals, -vals])
+    ref = torch.from_numpy(vals).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    got = np.array([orc.double_to_bf16(float(v)) for v in vals], dtype=np.uint16)
+    assert np.array_equal(got, ref)
+
+
+def test_double_to_bf16_single_rounding_from_binary64(orc):
+    """Values a hair above or below a bf16 midpoint that float32 cannot hold: a correct
+    single rounding must go to the nearer neighbour (rounding through float32 first would
+    land on the midpoint and tie to even)."""
+    for bits in (0x3f80, 0x3f81, 0x4049, 0x0001, 0x7f7e):
+        lo, hi = Fraction(orc.bf16_to_double(bits)), Fraction(orc.bf16_to_double(bits + 1))
+        mid = (lo + hi) / 2
+        eps = (hi - lo) / (1 << 40)
+        assert orc.double_to_bf16(float(mid + eps)) == bits + 1
+        assert orc.double_to_bf16(float(mid - eps)) == bits
+        assert orc.double_to_bf16(float(mid)) == (bits if bits % 2 == 0 else bits + 1)
+
+
+def _bf16_bits(values):
+    """float32 values that bfloat16 holds exactly -> their bit patterns (truncation is exact here)."""
+    f = np.asarray(values, dtype=np.float32)
+    b = (f.view(np.uint32) >> 16).astype(np.uint16)
+    assert np.array_equal(((b.astype(np.uint32) << 16).view(np.float32)), f)
+    return b
+
+
+def test_hand_example_bfloat16(orc):
+    g = _gold("hand_example.json")
+    x = _bf16_bits(g["x"]).reshape(1, 1, g["head_size"])
+    for case in g["cases"]:
+        c = _bf16_bits(case["cos"]).reshape(1, -1)
+        s = _bf16_bits(case["sin"]).reshape(1, -1)
+        y, _ = orc.rope(x, c, s, np.zeros((1, 1), np.int64), case["interleaved"], case["rotary_embedding_dim"], 1)
+        assert y.dtype == np.uint16
+        assert [orc.bf16_to_double(int(v)) for v in y.ravel()] == case["y"], case["name"]
+
+
+def test_bfloat16_rotation_rounds_once(orc):
+    """Each bf16 output is the exact rotation (rational arithmetic on the bf16 inputs)
+    rounded once to nearest-even bf16."""
+    rng = np.random.default_rng(62)
+    H = 8
+    xs = _bf16_bits(np.round(rng.standard_normal((1, 4, H)) * 64) / 64).reshape(1, 4, H)
+    th = rng.uniform(-np.pi, np.pi, (4, H // 2))
+    cos = (np.cos(th).astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    sin = (np.sin(th).astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    pos = np.arange(4).reshape(1, 4)
+    y, _ = orc.rope(xs, cos, sin, pos, 0, 0, 1)
+    val = lambda b: Fraction(orc.bf16_to_double(int(b)))  # noqa: E731
+    for s_ in range(4):
+        for i in range(H // 2):
+            x0, x1 = val(xs[0, s_, i]), val(xs[0, s_, i + H // 2])
+            c, sn = val(cos[s_, i]), val(sin[s_, i])
+            for j, exact in ((i, x0 * c - x1 * sn), (i + H // 2, x1 * c + x0 * sn)):
+                lo = orc.double_to_bf16(float(exact))
+                # the exact value's nearest bf16 (float(exact) is within 2^-53 relative: no tie shifts)
+                assert int(y[0, s_, j]) == lo
