@@ -206,8 +206,8 @@ class QKVStep:
         self.w, self.torch, self.rp = w, torch, rp
         self.lib = rp.load_library()
         inp = wl.make_inputs(w, shard=shard)
-        tdt = torch.float16 if w.dtype == "float16" else torch.float32
-        x0 = torch.from_numpy(inp["x"]).to(device)
+        tdt = torch_dtype(torch, w.dtype)
+        x0 = host_to_torch(torch, inp["x"]).to(device)
         self.xs = [x0] + [x0.clone() for _ in range(n_sets - 1)]
         B, S, H = w.batch, w.seq, w.head_size
         self.Nq, self.Nkv = w.num_heads, w.extra["kv_num_heads"]
@@ -218,12 +218,12 @@ class QKVStep:
         self.past = torch.from_numpy(inp["past_seq_lens"]).to(device)
         inv = torch.from_numpy(inp["inv_freq"]).to(device)
         self.cos, self.sin = rp.rope_cache_build(inv, w.cache_rows, tdt)
-        self.code = 1 if w.dtype == "float16" else 0
+        self.code = DTYPE_CODES[w.dtype]
         self.H = H
         self.norm = bool(w.extra.get("rms_norm"))
         if self.norm:
-            self.qw = torch.from_numpy(inp["q_norm_weight"]).to(device)
-            self.kw = torch.from_numpy(inp["k_norm_weight"]).to(device)
+            self.qw = host_to_torch(torch, inp["q_norm_weight"]).to(device)
+            self.kw = host_to_torch(torch, inp["k_norm_weight"]).to(device)
             self.eps = float(w.extra["epsilon"])
         # unfused path: positions past[b] + s and the (b, row) scatter indices
         s_idx = torch.arange(S, device=device, dtype=torch.int64)[None, :]
@@ -287,10 +287,10 @@ class Step:
         inp = wl.make_inputs(w, shard=shard)
         self.x_host = inp["x"]
         self.pos_host = inp["position_ids"]
-        tdt = torch.float16 if w.dtype == "float16" else torch.float32
-        self.code = 1 if w.dtype == "float16" else 0
+        tdt = torch_dtype(torch, w.dtype)
+        self.code = DTYPE_CODES[w.dtype]
         self.inv = torch.from_numpy(inp["inv_freq"]).to(device)
-        x0 = torch.from_numpy(self.x_host).to(device)
+        x0 = host_to_torch(torch, self.x_host).to(device)
         self.xs = [x0] + [x0.clone() for _ in range(n_sets - 1)]
         self.ys = [torch.empty_like(x0) for _ in range(n_sets)]
         self.pos = None if self.pos_host is None else torch.from_numpy(self.pos_host).to(device)
@@ -349,6 +349,21 @@ class Step:
             raise RuntimeError(f"{w.name}: status {st}: {lib.rope_last_error().decode()}")
 
 
+DTYPE_CODES = {"float32": 0, "float16": 1, "bfloat16": 2}
+
+
+def torch_dtype(torch, name):
+    return {"float32": torch.float32, "float16": torch.float16, "bfloat16": torch.bfloat16}[name]
+
+
+def host_to_torch(torch, a):
+    """Host tensor over a numpy array (bfloat16 arrays are uint16 bit patterns)."""
+    a = np.ascontiguousarray(a)
+    if a.dtype == wl.BF16_BITS:
+        return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16)
+    return torch.from_numpy(a)
+
+
 def make_step(rp, torch, w, device, n_sets, shard=0, dynamic=False):
     if w.kind == "qkv":
         return QKVStep(rp, torch, w, device, n_sets, shard=shard)
@@ -356,7 +371,7 @@ def make_step(rp, torch, w, device, n_sets, shard=0, dynamic=False):
 
 
 def n_buffer_sets(w):
-    per_set = 2 * w.numel * np.dtype(w.dtype).itemsize
+    per_set = 2 * w.numel * wl.itemsize(w.dtype)
     return max(2, math.ceil(4 * L2_BYTES / per_set))
 
 
@@ -452,7 +467,7 @@ def gpu_arm(args, rank, world, local_rank):
             "higher_is_better": True,
             "scaling": "weak",
             "vs_baseline": None,
-            "dtype": "f16",
+            "dtype": {"float32": "f32", "float16": "f16", "bfloat16": "bf16"}[w.dtype],
             "data": "synthetic (seeded N(0,1) X, position ids per the workload recipe; caches from "
                     "rope_cache_build)",
             "config": {
@@ -539,7 +554,7 @@ def measure_e2e(args, torch, step, sh, nbytes):
     step's X and positions from pinned memory, the launch, D2H of Y into pinned
     memory. Two streams alternate steps, so one step's D2H overlaps the next
     step's H2D (the copy engines run both directions at once)."""
-    x_host = [torch.from_numpy(step.x_host).pin_memory() for _ in range(2)]
+    x_host = [host_to_torch(torch, step.x_host).pin_memory() for _ in range(2)]
     y_host = [torch.empty_like(x_host[0]).pin_memory() for _ in range(2)]
     pos_host = None if step.pos_host is None else torch.from_numpy(step.pos_host).pin_memory()
     streams = [torch.cuda.Stream() for _ in range(2)]
@@ -593,7 +608,7 @@ class OracleStep:
         self.w = w
         inp = wl.make_inputs(w)
         x, pos = inp["x"], inp["position_ids"]
-        dtype = np.dtype(w.dtype)
+        dtype = wl.storage_dtype(w.dtype)
         T = w.tokens if tokens is None else max(1, min(tokens, w.tokens))
         S = w.seq
         nb = max(1, math.ceil(T / S))
@@ -680,7 +695,8 @@ def reference_arm(args, rank, world):
         "impl": "reference", "metric": METRIC, "value": round(gbs, 5), "unit": "GB/s",
         "gelem_per_s": round(gelem, 6), "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(el / args.steps * 1e3, 4), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f16", "data": "synthetic (same generator as the GPU arm)",
+        "vs_baseline": None, "dtype": {"float32": "f32", "float16": "f16", "bfloat16": "bf16"}[w.dtype],
+        "data": "synthetic (same generator as the GPU arm)",
         "config": {"workload": w.name, "shape": list(w.shape), "sample_tokens_per_step": st.tokens,
                    "note": "the pages publish no implementation to run; the reference arm is the CPU "
                            "oracle on a bounded sample of the workload per step"},

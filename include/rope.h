@@ -24,8 +24,8 @@
  *   - Work is enqueued asynchronously on `stream` (NULL = legacy default
  *     stream) on the current CUDA device; all device pointers must belong to
  *     that device.
- *   - Element type T is float32 (ROPE_F32) or float16 (ROPE_F16); positions
- *     are int64. Every pointer must be aligned to its element size. 16-byte
+ *   - Element type T is float32 (ROPE_F32), float16 (ROPE_F16) or bfloat16
+ *     (ROPE_BF16, beyond the pages); positions are int64. Every pointer must be aligned to its element size. 16-byte
  *     aligned tensors whose head and half-rotary widths are multiples of 16
  *     bytes take the 128-bit vector path; anything else takes the scalar path.
  *     Alignment is never an error.
@@ -57,7 +57,10 @@ typedef enum rope_status {
   ROPE_ERR_CUDA = 3         /* a CUDA runtime call failed */
 } rope_status;
 
-typedef enum rope_dtype { ROPE_F32 = 0, ROPE_F16 = 1 } rope_dtype;
+/* ROPE_BF16: bfloat16 storage. The pages list float32 and float16 only (and
+   mark bfloat16 unimplemented); it is offered here with the same float32
+   arithmetic and one final rounding to nearest-even bfloat16. */
+typedef enum rope_dtype { ROPE_F32 = 0, ROPE_F16 = 1, ROPE_BF16 = 2 } rope_dtype;
 
 /*
  * Scratch for the dynamic tile schedule (optional `scratch` argument of

@@ -23,7 +23,7 @@ __all__ = [
 ]
 
 ROPE_OK, ROPE_ERR_INVALID_ARG, ROPE_ERR_UNSUPPORTED, ROPE_ERR_CUDA = 0, 1, 2, 3
-ROPE_F32, ROPE_F16 = 0, 1
+ROPE_F32, ROPE_F16, ROPE_BF16 = 0, 1, 2
 ROPE_SCRATCH_BYTES = 64
 VARIANTS = {"auto": 0, "simt": 1, "tma": 2}
 _UNSUPPORTED_DTYPE = 99  # passed through so the library reports ROPE_ERR_UNSUPPORTED
@@ -111,7 +111,8 @@ def _check(fn, status):
 def _dtype_code(t):
     import torch
 
-    return {torch.float32: ROPE_F32, torch.float16: ROPE_F16}.get(t.dtype, _UNSUPPORTED_DTYPE)
+    return {torch.float32: ROPE_F32, torch.float16: ROPE_F16, torch.bfloat16: ROPE_BF16}.get(
+        t.dtype, _UNSUPPORTED_DTYPE)
 
 
 def _shape(t):

@@ -20,6 +20,7 @@ template <bool MROPE>
 const void* pick_dtype(int dtype, bool vec, bool inter, bool rank4) {
   if (dtype == 0) return vec ? pick<float, 4, MROPE>(inter, rank4) : pick<float, 1, MROPE>(inter, rank4);
   if (dtype == 1) return vec ? pick<__half, 8, MROPE>(inter, rank4) : pick<__half, 1, MROPE>(inter, rank4);
+  if (dtype == 2) return vec ? pick<__nv_bfloat16, 8, MROPE>(inter, rank4) : pick<__nv_bfloat16, 1, MROPE>(inter, rank4);
   return nullptr;
 }
 }  // namespace
@@ -31,6 +32,7 @@ const void* fused_kernel(int dtype, bool vec, bool inter, bool rank4, bool mrope
 const void* cache_build_kernel(int dtype) {
   if (dtype == 0) return (const void*)rope_cache_build_kernel<float>;
   if (dtype == 1) return (const void*)rope_cache_build_kernel<__half>;
+  if (dtype == 2) return (const void*)rope_cache_build_kernel<__nv_bfloat16>;
   return nullptr;
 }
 

@@ -18,6 +18,7 @@ const void* pick(bool inter, bool rank4) {
 const void* rope_kernel_mrope(int dtype, bool vec, bool inter, bool rank4) {
   if (dtype == 0) return vec ? pick<float, 4>(inter, rank4) : pick<float, 1>(inter, rank4);
   if (dtype == 1) return vec ? pick<__half, 8>(inter, rank4) : pick<__half, 1>(inter, rank4);
+  if (dtype == 2) return vec ? pick<__nv_bfloat16, 8>(inter, rank4) : pick<__nv_bfloat16, 1>(inter, rank4);
   return nullptr;
 }
 

@@ -20,6 +20,8 @@ const void* pick_dtype(int dtype, bool vec, bool inter, bool implicit_pos) {
     return vec ? pick<float, 4, NORM>(inter, implicit_pos) : pick<float, 1, NORM>(inter, implicit_pos);
   if (dtype == 1)
     return vec ? pick<__half, 8, NORM>(inter, implicit_pos) : pick<__half, 1, NORM>(inter, implicit_pos);
+  if (dtype == 2)
+    return vec ? pick<__nv_bfloat16, 8, NORM>(inter, implicit_pos) : pick<__nv_bfloat16, 1, NORM>(inter, implicit_pos);
   return nullptr;
 }
 }  // namespace

@@ -19,6 +19,7 @@ template <Coef M>
 const void* pick_dtype(int dtype, bool vec, bool inter, bool rank4) {
   if (dtype == 0) return vec ? pick<float, 4, M>(inter, rank4) : pick<float, 1, M>(inter, rank4);
   if (dtype == 1) return vec ? pick<__half, 8, M>(inter, rank4) : pick<__half, 1, M>(inter, rank4);
+  if (dtype == 2) return vec ? pick<__nv_bfloat16, 8, M>(inter, rank4) : pick<__nv_bfloat16, 1, M>(inter, rank4);
   return nullptr;
 }
 }  // namespace

@@ -31,6 +31,7 @@ const void* pick_mode(bool inter, bool rank4, Coef mode) {
 const void* tma_kernel(int dtype, bool inter, bool rank4, Coef mode) {
   if (dtype == 0) return pick_mode<float>(inter, rank4, mode);
   if (dtype == 1) return pick_mode<__half>(inter, rank4, mode);
+  if (dtype == 2) return pick_mode<__nv_bfloat16>(inter, rank4, mode);
   return nullptr;
 }
 

@@ -81,7 +81,7 @@ rope_status cuda_fail(cudaError_t e, const char* what) {
   return fail(ROPE_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
 }
 
-int elem_size(rope_dtype dt) { return dt == ROPE_F16 ? 2 : 4; }
+int elem_size(rope_dtype dt) { return dt == ROPE_F32 ? 4 : 2; }
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -318,7 +318,7 @@ struct TmaLaunch {
   Launch L;
 };
 
-rope_status encode_x_map(CUtensorMap* m, const Geom& g, int rank, int es, const void* base,
+rope_status encode_x_map(CUtensorMap* m, rope_dtype dt, const Geom& g, int rank, int es, const void* base,
                          const TParams& tp) {
   cuuint64_t dims[4], strides[3];
   cuuint32_t box[4], estr[4] = {1, 1, 1, 1};
@@ -334,7 +334,10 @@ rope_status encode_x_map(CUtensorMap* m, const Geom& g, int rank, int es, const 
     strides[0] = g.H * es, strides[1] = g.S * g.H * es, strides[2] = g.N * g.S * g.H * es;
     box[0] = (cuuint32_t)g.H, box[1] = tp.TS, box[2] = tp.NG, box[3] = 1;
   }
-  CUresult e = encode_tiled()(m, es == 2 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+  const CUtensorMapDataType ty = dt == ROPE_F32   ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                 : dt == ROPE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                   : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  CUresult e = encode_tiled()(m, ty,
                               r, const_cast<void*>(base), dims, strides, box, estr,
                               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -345,8 +348,8 @@ rope_status encode_x_map(CUtensorMap* m, const Geom& g, int rank, int es, const 
 // Fills kp's geometry and the TMA launch; ROPE_ERR_UNSUPPORTED (no message)
 // when the shape does not fit the pipeline, in which case the caller falls
 // back to the register-path kernel.
-rope_status plan_tma(const Geom& g, int es, int rank, int slots, const void* fn, const void* x, void* y,
-                     KParams* kp, TmaLaunch* T) {
+rope_status plan_tma(rope_dtype dt, const Geom& g, int es, int rank, int slots, const void* fn, const void* x,
+                     void* y, KParams* kp, TmaLaunch* T) {
   const int V = 16 / es;
   TParams& tp = T->tp;
   memset(&tp, 0, sizeof(tp));
@@ -419,8 +422,8 @@ rope_status plan_tma(const Geom& g, int es, int rank, int slots, const void* fn,
   T->L.grid = dim3((unsigned)gx, 1, 1);
   T->L.block = dim3(kTmaThreads, 1, 1);
   T->L.smem = smem;
-  ROPE_TRY(encode_x_map(&T->mx, g, rank, es, x, tp));
-  ROPE_TRY(encode_x_map(&T->my, g, rank, es, y, tp));
+  ROPE_TRY(encode_x_map(&T->mx, dt, g, rank, es, x, tp));
+  ROPE_TRY(encode_x_map(&T->my, dt, g, rank, es, y, tp));
   return ROPE_OK;
 }
 
@@ -470,8 +473,8 @@ bool vector_ok(const Geom& g, int es, std::initializer_list<const void*> ptrs) {
 }
 
 rope_status check_dtype(rope_dtype dt) {
-  if (dt != ROPE_F32 && dt != ROPE_F16)
-    return fail(ROPE_ERR_UNSUPPORTED, "dtype %d: only float32 (0) and float16 (1) are implemented",
+  if (dt != ROPE_F32 && dt != ROPE_F16 && dt != ROPE_BF16)
+    return fail(ROPE_ERR_UNSUPPORTED, "dtype %d: only float32 (0), float16 (1) and bfloat16 (2) are implemented",
                 (int)dt);
   return ROPE_OK;
 }
@@ -572,7 +575,7 @@ rope_status mrope_common(rope_dtype dtype, int32_t x_rank, const int64_t* x_shap
   if (tma_eligible(g, es, vec, true)) {
     const void* tfn = tma_kernel(dtype, interleaved != 0, x_rank == 4, Coef::kMRope);
     TmaLaunch T;
-    const rope_status ts = plan_tma(g, es, x_rank, 3, tfn, x, y, &kp, &T);
+    const rope_status ts = plan_tma(dtype, g, es, x_rank, 3, tfn, x, y, &kp, &T);
     if (ts == ROPE_OK) return launch_tma(tfn, &T, &kp, stream);
     if (ts != ROPE_ERR_UNSUPPORTED) return ts;
   }
@@ -653,7 +656,7 @@ rope_status rope_apply(rope_dtype dtype, int32_t x_rank, const int64_t* x_shape,
   if (tma_eligible(g, es, vec, false)) {
     const void* tfn = tma_kernel(dtype, interleaved != 0, x_rank == 4, mode);
     TmaLaunch T;
-    const rope_status ts = plan_tma(g, es, x_rank, 1, tfn, x, y, &kp, &T);
+    const rope_status ts = plan_tma(dtype, g, es, x_rank, 1, tfn, x, y, &kp, &T);
     if (ts == ROPE_OK) return launch_tma(tfn, &T, &kp, stream);
     if (ts != ROPE_ERR_UNSUPPORTED) return ts;
   }

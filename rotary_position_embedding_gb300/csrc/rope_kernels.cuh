@@ -21,6 +21,7 @@
 //    Issues 4 (cache = cos(freqs) * scaling).
 #pragma once
 
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <stdint.h>
 
@@ -66,6 +67,27 @@ struct Elem<__half> {
     float hi = __fmul_ru(a, b);
     if (lo != hi && isfinite(t)) t = __int_as_float(__float_as_int(t) | 1);
     return __half2float(__float2half_rn(t));
+  }
+};
+
+// bfloat16 (storage beyond the pages' float32 / float16): the top 16 bits of
+// a float32.
+template <>
+struct Elem<__nv_bfloat16> {
+  using bits = unsigned short;
+  static __device__ __forceinline__ float tof(unsigned short v) { return __uint_as_float((unsigned int)v << 16); }
+  static __device__ __forceinline__ unsigned short fromf(float v) {
+    return __bfloat16_as_ushort(__float2bfloat16_rn(v));
+  }
+  // bfloat16(a * b) rounded once from the exact product: round-to-odd float32
+  // product (16 spare bits), then nearest-even (Boldo and Melquiond, as for
+  // float16 above).
+  static __device__ __forceinline__ float mul_round(float a, float b) {
+    float t = __fmul_rz(a, b);
+    float lo = __fmul_rd(a, b);
+    float hi = __fmul_ru(a, b);
+    if (lo != hi && isfinite(t)) t = __int_as_float(__float_as_int(t) | 1);
+    return tof(fromf(t));
   }
 };
 

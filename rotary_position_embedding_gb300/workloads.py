@@ -105,6 +105,11 @@ WORKLOADS = {
         name="rope_r3_f16_gather", kind="rope", rank=3, shape=(4, 2048, 32 * 128), dtype="float16",
         num_heads=32, interleaved=0, positions="offset", cache_rows=8192, rope_base=10000.0,
         rope_dim=128),
+    # the headline shape in bfloat16 (storage beyond the pages' float32/float16)
+    "rope_r3_bf16_gather": Workload(
+        name="rope_r3_bf16_gather", kind="rope", rank=3, shape=(4, 2048, 32 * 128), dtype="bfloat16",
+        num_heads=32, interleaved=0, positions="offset", cache_rows=8192, rope_base=10000.0,
+        rope_dim=128),
     "rope_r4_f16_interleaved_partial": Workload(
         name="rope_r4_f16_interleaved_partial", kind="rope", rank=4, shape=(8, 32, 4096, 128),
         dtype="float16", num_heads=32, interleaved=1, rotary_embedding_dim=64, positions="uniform",
@@ -140,6 +145,10 @@ WORKLOADS = {
         name="mrope_fused_decode_r3_f16", kind="mrope_fused", rank=3, shape=(256, 1, 28 * 128), dtype="float16",
         num_heads=28, positions="mrope", cache_rows=32768, rope_base=1.0e6, rope_dim=128,
         mrope_section=(16, 24, 24), mrope_layout=1, scale=1.0),
+    "mrope_r3_bf16_layout1": Workload(
+        name="mrope_r3_bf16_layout1", kind="mrope", rank=3, shape=(2, 8192, 28 * 128), dtype="bfloat16",
+        num_heads=28, positions="mrope", cache_rows=32768, rope_base=10000.0, rope_dim=128,
+        mrope_section=(16, 24, 24), mrope_layout=1, scale=1.0),
     "fused_decode_r3_f16": Workload(
         name="fused_decode_r3_f16", kind="fused", rank=3, shape=(256, 1, 40 * 128), dtype="float16",
         num_heads=40, positions="uniform", cache_rows=32768, rope_base=1.0e6, rope_dim=128,
@@ -149,11 +158,37 @@ WORKLOADS = {
 HEADLINE = "rope_r3_f16_gather"
 
 
+# numpy has no bfloat16: bfloat16 data is carried as its uint16 bit patterns.
+BF16_BITS = np.uint16
+
+
+def storage_dtype(name):
+    """numpy dtype carrying storage type ``name`` ("float32", "float16", "bfloat16")."""
+    return np.dtype(BF16_BITS) if name == "bfloat16" else np.dtype(name)
+
+
+def itemsize(name):
+    return 2 if name == "bfloat16" else np.dtype(name).itemsize
+
+
+def to_bf16_bits(a):
+    """float32 values rounded to nearest-even bfloat16, as bit patterns (finite inputs)."""
+    u = np.asarray(a, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    return ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint16)
+
+
+def to_storage(a, dtype):
+    """Float data rounded to the storage type carried by numpy dtype ``dtype``."""
+    if np.dtype(dtype) == BF16_BITS:
+        return to_bf16_bits(a)
+    return np.asarray(a).astype(dtype)
+
+
 def x_normal(shape, dtype, seed=0):
-    """N(0, 1) drawn in float32 and rounded to ``dtype`` (numpy rounds to nearest-even)."""
+    """N(0, 1) drawn in float32 and rounded to ``dtype`` (nearest-even)."""
     rng = np.random.default_rng(seed)
     x = rng.standard_normal(size=shape, dtype=np.float32)
-    return x.astype(dtype)
+    return to_storage(x, dtype)
 
 
 def inv_freq(base, d, half):
@@ -214,7 +249,7 @@ def make_inputs(w: Workload, shard=0):
     when several GPUs each process their own batch); shard 0 is the default.
     """
     base = 1000 * int(shard)
-    x = x_normal(w.shape, np.dtype(w.dtype), seed=base + 0)
+    x = x_normal(w.shape, storage_dtype(w.dtype), seed=base + 0)
     B, S = w.batch, w.seq
     if w.positions == "none":
         pos = None
@@ -235,8 +270,8 @@ def make_inputs(w: Workload, shard=0):
         out["past_seq_lens"] = rng.integers(0, w.extra["max_past"] + 1, size=B).astype(np.int32)
         if w.extra.get("rms_norm"):
             wrng = np.random.default_rng(base + 3)
-            out["q_norm_weight"] = wrng.uniform(0.5, 1.5, w.head_size).astype(w.dtype)
-            out["k_norm_weight"] = wrng.uniform(0.5, 1.5, w.head_size).astype(w.dtype)
+            out["q_norm_weight"] = to_storage(wrng.uniform(0.5, 1.5, w.head_size), storage_dtype(w.dtype))
+            out["k_norm_weight"] = to_storage(wrng.uniform(0.5, 1.5, w.head_size), storage_dtype(w.dtype))
     return out
 
 
@@ -247,7 +282,7 @@ def algorithmic_bytes(w: Workload, cached=True):
     per-token gather, not unique rows); the on-the-fly variant reads inv_freq
     once instead.
     """
-    esz = np.dtype(w.dtype).itemsize
+    esz = itemsize(w.dtype)
     xy = 2 * w.numel * esz
     if w.kind == "qkv":
         # Q, K, V read once; Q out, K and V into the caches; one cos/sin row

@@ -13,6 +13,30 @@ import numpy as np
 TOL_F32_ABS = 1e-5
 TOL_F16_ULP = 1
 
+# numpy has no bfloat16: bfloat16 data travels as its uint16 bit patterns (as
+# the oracle takes it). Its tolerance is the float16 one: one ulp of the type.
+BF16 = np.uint16
+
+
+def cast(a, dtype):
+    """Float data rounded to the storage type: float16 / float32 by numpy,
+    bfloat16 by nearest-even on the float32 bit pattern (finite inputs)."""
+    from rotary_position_embedding_gb300.workloads import to_storage
+
+    return to_storage(a, dtype)
+
+
+def to_float64(a):
+    """Values of storage-typed data as float64 (bfloat16 bit patterns decoded)."""
+    a = np.asarray(a)
+    if a.dtype == BF16:
+        return (a.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    return a.astype(np.float64)
+
+
+def is_half_width(dtype):
+    return np.dtype(dtype) in (np.dtype(np.float16), np.dtype(BF16))
+
 
 def f16_ordinal(a):
     u = a.view(np.uint16).astype(np.int32)
@@ -70,18 +94,19 @@ def compare(y_gpu, y_ref, x, rank, N, exact_mask=None):
     xv = head_view(x, rank, N)
     stats = {}
     if exact_mask is not None and exact_mask.any():
-        bits = np.uint16 if y_gpu.dtype == np.float16 else np.uint32
+        bits = np.uint16 if is_half_width(y_gpu.dtype) else np.uint32
         gb, xb, rb = g.view(bits), xv.view(bits), r.view(bits)
         assert np.array_equal(rb[exact_mask], xb[exact_mask]), "oracle pass-through is not a copy"
         bad = gb[exact_mask] != xb[exact_mask]
         assert not bad.any(), f"{int(bad.sum())} pass-through elements differ from X"
         stats["passthrough"] = int(exact_mask.sum())
     rot = ~exact_mask if exact_mask is not None else np.ones(g.shape, dtype=bool)
-    if y_gpu.dtype == np.float16:
+    if is_half_width(y_gpu.dtype):
+        # sign-magnitude ordinals: float16 and bfloat16 alike
         d = np.abs(f16_ordinal(np.ascontiguousarray(g)) - f16_ordinal(np.ascontiguousarray(r)))
         d = d[rot]
         worst = int(d.max()) if d.size else 0
-        assert worst <= TOL_F16_ULP, f"float16 error {worst} ulp > {TOL_F16_ULP} ({int((d > 1).sum())} elements)"
+        assert worst <= TOL_F16_ULP, f"16-bit error {worst} ulp > {TOL_F16_ULP} ({int((d > 1).sum())} elements)"
         stats["max_ulp"] = worst
         stats["bit_exact_frac"] = float((d == 0).mean()) if d.size else 1.0
     else:

@@ -63,7 +63,8 @@ def _rope(so, **kw):
 
 
 @pytest.mark.parametrize("kw,status", [
-    (dict(dtype=99), UNSUPPORTED),                      # bfloat16 and others: not implemented
+    (dict(dtype=99), UNSUPPORTED),                      # unknown element type codes
+    (dict(dtype=2, nh=3), INVALID),                     # bfloat16 passes the type gate; the shape is checked
     (dict(rank=5, xs=_i64(1, 1, 1, 1, 1)), INVALID),
     (dict(nh=0), INVALID),                              # rank 3 needs num_heads
     (dict(nh=3), INVALID),                              # 64 % 3 != 0

@@ -14,18 +14,27 @@ import zlib
 import numpy as np
 import pytest
 
-from parity_util import compare, mrope_passthrough_mask, rope_passthrough_mask
+from parity_util import BF16, cast, compare, mrope_passthrough_mask, rope_passthrough_mask
 from rotary_position_embedding_gb300 import workloads as wl
 
 pytestmark = pytest.mark.gpu
 
-DT = {"f16": np.float16, "f32": np.float32}
+DT = {"f16": np.float16, "f32": np.float32, "bf16": BF16}
+
+
+def _tdt(torch, dt):
+    return {"f16": torch.float16, "f32": torch.float32, "bf16": torch.bfloat16}[dt]
+
+
+def _bits(torch, dt):
+    return torch.int32 if dt == "f32" else torch.int16
 
 
 def _dev(a, torch, cuda, offset=0):
     """Device copy of a host array; offset > 0 places it that many elements past a
     16-byte boundary (contiguous but misaligned for the vector path)."""
-    t = torch.from_numpy(np.ascontiguousarray(a))
+    a = np.ascontiguousarray(a)
+    t = torch.from_numpy(a.view(np.int16)).view(torch.bfloat16) if a.dtype == BF16 else torch.from_numpy(a)
     if offset == 0:
         return t.to(cuda)
     big = torch.empty(t.numel() + offset, dtype=t.dtype, device=cuda)
@@ -39,6 +48,10 @@ def _seed(*params):
 
 
 def _host(t):
+    import torch
+
+    if t.dtype == torch.bfloat16:
+        return t.detach().view(torch.int16).cpu().numpy().view(BF16)
     return t.detach().cpu().numpy()
 
 
@@ -58,7 +71,7 @@ def torch_mod():
 # ---------------------------------------------------------------------------
 
 ROPE_GRID = [c + (v,) for c in itertools.product(
-    ["f16", "f32"], [3, 4], ["pos", "cache3d"], [0, 1], ["full", "partial"],
+    ["f16", "f32", "bf16"], [3, 4], ["pos", "cache3d"], [0, 1], ["full", "partial"],
     ["vector", "scalar_shape", "scalar_misaligned"]) for v in (["simt", "tma"] if c[-1] == "vector" else ["simt"])]
 
 
@@ -72,7 +85,7 @@ def test_rope_grid(lib, orc, cuda, torch_mod, dt, rank, cache, inter, rot, path,
     rd = 0 if rot == "full" else (4 if H == 6 else 16)
     h = (rd or H) // 2
     shape = _x_shape(rank, B, S, N, H)
-    x = rng.standard_normal(shape).astype(dtype)
+    x = cast(rng.standard_normal(shape), dtype)
     inv = wl.inv_freq(10000.0, rd or H, h)
     if cache == "pos":
         R = 97
@@ -99,14 +112,14 @@ def test_rope_grid(lib, orc, cuda, torch_mod, dt, rank, cache, inter, rot, path,
     assert int(flag.item()) == (1 if n_oor else 0)
 
 
-@pytest.mark.parametrize("dt,rank,inter", list(itertools.product(["f16", "f32"], [3, 4], [0, 1])))
+@pytest.mark.parametrize("dt,rank,inter", list(itertools.product(["f16", "f32", "bf16"], [3, 4], [0, 1])))
 def test_rope_in_place(lib, orc, cuda, torch_mod, dt, rank, inter):
     torch = torch_mod
     dtype = DT[dt]
     rng = np.random.default_rng(21)
     B, S, N, H = 2, 19, 4, 64
     shape = _x_shape(rank, B, S, N, H)
-    x = rng.standard_normal(shape).astype(dtype)
+    x = cast(rng.standard_normal(shape), dtype)
     inv = wl.inv_freq(10000.0, H, H // 2)
     cos, sin = orc.cache_build(inv, 50, dtype)
     pos = rng.integers(0, 50, (B, S))
@@ -141,7 +154,7 @@ def test_rope_edges(lib, orc, cuda, torch_mod, case):
     else:
         B, S, N, H, R = 2, 9, 2, 32, 1 << 20
     shape = _x_shape(rank, B, S, N, H)
-    x = rng.standard_normal(shape).astype(dtype)
+    x = cast(rng.standard_normal(shape), dtype)
     h = (rd or H) // 2
     inv = wl.inv_freq(10000.0, H, h)
     Rb = min(R, 4096) if case != "big_positions" else 4096
@@ -179,11 +192,11 @@ def test_empty_and_errors_on_gpu(lib, cuda, torch_mod):
     p = torch.empty((0, 4), dtype=torch.int64, device=cuda)
     y = lib.rope_apply(x, c, c, p, num_heads=4)
     assert y.shape == x.shape
-    xb = torch.zeros((2, 4, 64), dtype=torch.bfloat16, device=cuda)
-    cb = torch.zeros((8, 8), dtype=torch.bfloat16, device=cuda)
+    xd = torch.zeros((2, 4, 64), dtype=torch.float64, device=cuda)   # no float64 kernels
+    cd = torch.zeros((8, 8), dtype=torch.float64, device=cuda)
     pp = torch.zeros((2, 4), dtype=torch.int64, device=cuda)
     with pytest.raises(lib.RopeError) as e:
-        lib.rope_apply(xb, cb, cb, pp, num_heads=4)
+        lib.rope_apply(xd, cd, cd, pp, num_heads=4)
     assert e.value.status == lib.ROPE_ERR_UNSUPPORTED
     with pytest.raises(lib.RopeError) as e:
         lib.rope_apply(x.new_zeros((2, 4, 64)), c, c, pp, num_heads=3)
@@ -236,7 +249,7 @@ def test_tma_pipeline_shapes(lib, orc, cuda, torch_mod, case, in_place, schedule
     dtype = DT[dt]
     rng = np.random.default_rng(_seed(*case))
     shape = _x_shape(rank, B, S, N, H)
-    x = rng.standard_normal(shape).astype(dtype)
+    x = cast(rng.standard_normal(shape), dtype)
     h = (rd or H) // 2
     R = 5000
     inv = wl.inv_freq(10000.0, rd or H, h)
@@ -338,7 +351,7 @@ def test_automatic_variant_choice(lib, orc, cuda, torch_mod):
 # ---------------------------------------------------------------------------
 
 MROPE_GRID = [c + (v,) for c in itertools.product(
-    ["f16", "f32"], [3, 4], ["l0", "l1", "stride3"], [0, 1], ["full", "partial_odd_head"],
+    ["f16", "f32", "bf16"], [3, 4], ["l0", "l1", "stride3"], [0, 1], ["full", "partial_odd_head"],
     [1.0, 0.7], ["vector", "scalar_misaligned"])
     for v in (["simt", "tma"] if c[-1] == "vector" and c[4] == "full" else ["simt"])]
 
@@ -356,7 +369,7 @@ def test_mrope_grid(lib, orc, cuda, torch_mod, dt, rank, layout, inter, rot, sca
     h = (rd or H) // 2
     R = 120
     shape = _x_shape(rank, B, S, N, H)
-    x = rng.standard_normal(shape).astype(dtype)
+    x = cast(rng.standard_normal(shape), dtype)
     inv = wl.inv_freq(10000.0, rd or H, h)
     cos, sin = orc.cache_build(inv, R, dtype)
     pos3 = rng.integers(0, R, (3, B, S))
@@ -410,7 +423,7 @@ def test_mrope_equal_streams_equals_rope_on_gpu(lib, orc, cuda, torch_mod):
 # ---------------------------------------------------------------------------
 
 @pytest.mark.parametrize("dt,rank,inter,rd,scaling", list(itertools.product(
-    ["f16", "f32"], [3, 4], [0, 1], [0, 32], [1.0, 0.85])))
+    ["f16", "f32", "bf16"], [3, 4], [0, 1], [0, 32], [1.0, 0.85])))
 def test_fused_grid(lib, orc, cuda, torch_mod, dt, rank, inter, rd, scaling):
     torch = torch_mod
     dtype = DT[dt]
@@ -418,7 +431,7 @@ def test_fused_grid(lib, orc, cuda, torch_mod, dt, rank, inter, rd, scaling):
     B, S, N, H = 5, 13, 6, 64
     h = (rd or H) // 2
     shape = _x_shape(rank, B, S, N, H)
-    x = rng.standard_normal(shape).astype(dtype)
+    x = cast(rng.standard_normal(shape), dtype)
     inv = wl.inv_freq(1e6, rd or H, h)
     pos = rng.integers(0, 32768, (B, S))
     pos[0, 0], pos[1, 2] = 0, 32767
@@ -431,16 +444,16 @@ def test_fused_grid(lib, orc, cuda, torch_mod, dt, rank, inter, rd, scaling):
     torch.cuda.synchronize()
     compare(_host(yf), y_ref, x, rank, N, rope_passthrough_mask(shape, rank, N, rd, None, 0))
     # fused == gathering the library's own cache, bit for bit
-    cd, sd = lib.rope_cache_build(ind, 32768, torch.float16 if dt == "f16" else torch.float32,
+    cd, sd = lib.rope_cache_build(ind, 32768, _tdt(torch, dt),
                                   attention_scaling=scaling)
     yc = lib.rope_apply(xd, cd, sd, pd, interleaved=inter, rotary_embedding_dim=rd, num_heads=nh)
     torch.cuda.synchronize()
-    bits = torch.int16 if dt == "f16" else torch.int32
+    bits = _bits(torch, dt)
     assert torch.equal(yc.view(bits), yf.view(bits))
 
 
 @pytest.mark.parametrize("dt,rank,layout,inter,rd,scale,path", [c + ("vector",) for c in itertools.product(
-    ["f16", "f32"], [3, 4], [0, 1], [0, 1], [0, 32], [1.0, 0.7])] + [
+    ["f16", "f32", "bf16"], [3, 4], [0, 1], [0, 1], [0, 32], [1.0, 0.7])] + [
     ("f16", 3, 1, 0, 0, 0.7, "scalar_misaligned"), ("f32", 4, 0, 1, 32, 1.0, "scalar_misaligned"),
     ("f16", 3, 1, 1, 10, 0.7, "scalar_shape")])
 def test_mrope_fused_grid(lib, orc, cuda, torch_mod, dt, rank, layout, inter, rd, scale, path):
@@ -453,7 +466,7 @@ def test_mrope_fused_grid(lib, orc, cuda, torch_mod, dt, rank, layout, inter, rd
     h = (rd or H) // 2
     sec = (h - 2 * (h // 3), h // 3, h // 3)
     shape = _x_shape(rank, B, S, N, H)
-    x = rng.standard_normal(shape).astype(dtype)
+    x = cast(rng.standard_normal(shape), dtype)
     inv = wl.inv_freq(1e6, rd or H, h)
     R = 8192
     pos3 = rng.integers(0, R, (3, B, S))
@@ -467,12 +480,12 @@ def test_mrope_fused_grid(lib, orc, cuda, torch_mod, dt, rank, layout, inter, rd
     torch.cuda.synchronize()
     assert lib.last_kernel() == "rope_fused_kernel"
     compare(_host(yf), y_ref, x, rank, N, rope_passthrough_mask(shape, rank, N, rd, None, 0))
-    cd, sd = lib.rope_cache_build(ind, R, torch.float16 if dt == "f16" else torch.float32,
+    cd, sd = lib.rope_cache_build(ind, R, _tdt(torch, dt),
                                   attention_scaling=0.9)
     yc = lib.mrope_apply(xd, cd, sd, pd, sec, mrope_layout=layout, scale=scale, interleaved=inter,
                          rotary_embedding_dim=rd, num_heads=nh)
     torch.cuda.synchronize()
-    bits = torch.int16 if dt == "f16" else torch.int32
+    bits = _bits(torch, dt)
     assert torch.equal(yc.view(bits), yf.view(bits))
 
 
@@ -491,7 +504,7 @@ def test_mrope_fused_any_position(lib, orc, cuda, torch_mod):
     compare(_host(yf), y_ref, x, 3, N, None)
 
 
-@pytest.mark.parametrize("dt,base,scaling", list(itertools.product(["f16", "f32"], [1e4, 1e6],
+@pytest.mark.parametrize("dt,base,scaling", list(itertools.product(["f16", "f32", "bf16"], [1e4, 1e6],
                                                                     [1.0, 0.7071067690849304])))
 def test_cache_build_vs_oracle(lib, orc, cuda, torch_mod, dt, base, scaling):
     torch = torch_mod
@@ -500,11 +513,11 @@ def test_cache_build_vs_oracle(lib, orc, cuda, torch_mod, dt, base, scaling):
     inv = wl.inv_freq(base, 2 * half, half)
     c_ref, s_ref = orc.cache_build(inv, rows, dtype, scaling)
     cd, sd = lib.rope_cache_build(_dev(inv, torch, cuda), rows,
-                                  torch.float16 if dt == "f16" else torch.float32,
+                                  _tdt(torch, dt),
                                   attention_scaling=scaling)
     torch.cuda.synchronize()
     for got, ref in ((_host(cd), c_ref), (_host(sd), s_ref)):
-        if dtype == np.float16:
+        if dtype in (np.float16, BF16):
             from parity_util import f16_ordinal
             d = np.abs(f16_ordinal(got) - f16_ordinal(ref))
         else:
@@ -526,8 +539,8 @@ def test_workload_full_size(lib, orc, cuda, torch_mod, name):
     w = wl.WORKLOADS[name]
     inp = wl.make_inputs(w)
     x, pos, inv = inp["x"], inp["position_ids"], inp["inv_freq"]
-    dtype = np.dtype(w.dtype)
-    tdt = torch.float16 if dtype == np.float16 else torch.float32
+    dtype = wl.storage_dtype(w.dtype)
+    tdt = {"float32": torch.float32, "float16": torch.float16, "bfloat16": torch.bfloat16}[w.dtype]
     nh = w.num_heads if w.rank == 3 else 0
     xd, ind = _dev(x, torch, cuda), _dev(inv, torch, cuda)
     if w.kind == "rope" and w.positions == "none":

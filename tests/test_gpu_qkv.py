@@ -17,7 +17,7 @@ import itertools
 import numpy as np
 import pytest
 
-from parity_util import compare
+from parity_util import BF16, cast, compare, to_float64
 from rotary_position_embedding_gb300 import workloads as wl
 
 pytestmark = pytest.mark.gpu
@@ -26,13 +26,22 @@ TORCH_DT = {"f16": "float16", "f32": "float32"}
 
 
 def _dev(a, torch, cuda, offset=0):
-    t = torch.from_numpy(np.ascontiguousarray(a))
+    a = np.ascontiguousarray(a)
+    t = torch.from_numpy(a.view(np.int16)).view(torch.bfloat16) if a.dtype == BF16 else torch.from_numpy(a)
     if offset == 0:
         return t.to(cuda)
     flat = torch.empty(t.numel() + offset, dtype=t.dtype, device=cuda)
     v = flat[offset:].view(t.shape)
     v.copy_(t.to(cuda))
     return v
+
+
+def _host(t):
+    import torch
+
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16).cpu().numpy().view(BF16)
+    return t.cpu().numpy()
 
 
 def _heads(a, B, S, n0, n1, Ntot, H):
@@ -50,15 +59,15 @@ def _token_mask(B, S, N, H, rd, bad_tok):
 def _run_case(lib, orc, torch, cuda, dt, packed, cache, inter, rot, implicit, H, offset=0, Nq=8, Nkv=2,
               B=3, S=37, R=64, L=80, seed=0):
     rng = np.random.default_rng(seed)
-    npdt = np.float16 if dt == "f16" else np.float32
+    npdt = {"f16": np.float16, "f32": np.float32, "bf16": BF16}[dt]
     rd = 0 if rot == "full" else H // 2
     h = (rd or H) // 2
     Ntot = Nq + 2 * Nkv
-    qkv = rng.standard_normal((B, S, Ntot * H)).astype(npdt)
+    qkv = cast(rng.standard_normal((B, S, Ntot * H)), npdt)
     q, k, v = _heads(qkv, B, S, 0, Nq, Ntot, H), _heads(qkv, B, S, Nq, Nq + Nkv, Ntot, H), \
         _heads(qkv, B, S, Nq + Nkv, Ntot, Ntot, H)
     theta = rng.uniform(-np.pi, np.pi, (R, h))
-    cos, sin = np.cos(theta).astype(npdt), np.sin(theta).astype(npdt)
+    cos, sin = cast(np.cos(theta), npdt), cast(np.sin(theta), npdt)
     past = np.array([0, 11, 50], dtype=np.int32)[:B]
     if implicit:
         pos = None
@@ -68,8 +77,8 @@ def _run_case(lib, orc, torch, cuda, dt, packed, cache, inter, rot, implicit, H,
         pos[0, 5], pos[1, 0], pos[-1, -1] = R + 3, -1, R
         eff = pos
     bad_tok = (eff < 0) | (eff >= R)
-    kc0 = rng.standard_normal((B, Nkv, L, H)).astype(npdt) if cache else None
-    vc0 = rng.standard_normal((B, Nkv, L, H)).astype(npdt) if cache else None
+    kc0 = cast(rng.standard_normal((B, Nkv, L, H)), npdt) if cache else None
+    vc0 = cast(rng.standard_normal((B, Nkv, L, H)), npdt) if cache else None
     use_past = cache or implicit
     ref = orc.rope_qkv(qkv if packed else q, cos, sin, pos, num_heads=Nq, kv_num_heads=Nkv,
                        key=None if packed else k, value=None if (packed or not cache) else v,
@@ -90,14 +99,14 @@ def _run_case(lib, orc, torch, cuda, dt, packed, cache, inter, rot, implicit, H,
     torch.cuda.synchronize()
     assert lib.last_kernel() == "rope_qkv_kernel"
     rdw = rd or H
-    compare(qo.cpu().numpy(), q_ref, q, 3, Nq, _token_mask(B, S, Nq, H, rdw, bad_tok))
+    compare(_host(qo), q_ref, q, 3, Nq, _token_mask(B, S, Nq, H, rdw, bad_tok))
     if not cache:
         assert ko is not None
-        compare(ko.cpu().numpy(), k_ref, k, 3, Nkv, _token_mask(B, S, Nkv, H, rdw, bad_tok))
+        compare(_host(ko), k_ref, k, 3, Nkv, _token_mask(B, S, Nkv, H, rdw, bad_tok))
     else:
         assert ko is None
         # V cache: bit for bit (new rows are copies, the rest untouched)
-        assert np.array_equal(vc_d.cpu().numpy().view(np.uint8), vc_ref.view(np.uint8))
+        assert np.array_equal(_host(vc_d).view(np.uint8), vc_ref.view(np.uint8))
         # K cache: what pass-through means per row -- the old row, or the new token's K
         src = kc0.copy()
         mask = np.ones((B, L, Nkv, H), dtype=bool)          # token-major view of (B, Nkv, L, H)
@@ -111,12 +120,12 @@ def _run_case(lib, orc, torch, cuda, dt, packed, cache, inter, rot, implicit, H,
                     mask[b, row, :, rdw:] = True
                     if bad_tok[b, s]:
                         mask[b, row] = True
-        compare(kc_d.cpu().numpy(), kc_ref, src, 4, Nkv, mask)
+        compare(_host(kc_d), kc_ref, src, 4, Nkv, mask)
     want = 1 | (4 if n_skip else 0)
     assert int(status.item()) == want
 
 
-QKV_GRID = list(itertools.product(["f16", "f32"], [0, 1], [0, 1], [0, 1], ["full", "partial"], [0, 1]))
+QKV_GRID = list(itertools.product(["f16", "f32", "bf16"], [0, 1], [0, 1], [0, 1], ["full", "partial"], [0, 1]))
 
 
 @pytest.mark.parametrize("dt,packed,cache,inter,rot,implicit", QKV_GRID)
@@ -154,8 +163,8 @@ def test_qkv_multi_head_attention_and_in_place(lib, orc, cuda):
                                 num_heads=N, kv_num_heads=N, key=kd, q_out=qd, k_out=kd)
     torch.cuda.synchronize()
     assert qo.data_ptr() == qd.data_ptr() and ko.data_ptr() == kd.data_ptr()
-    compare(qd.cpu().numpy(), q_ref, q, 3, N, _token_mask(B, S, N, H, H, np.zeros((B, S), bool)))
-    compare(kd.cpu().numpy(), k_ref, k, 3, N, _token_mask(B, S, N, H, H, np.zeros((B, S), bool)))
+    compare(_host(qd), q_ref, q, 3, N, _token_mask(B, S, N, H, H, np.zeros((B, S), bool)))
+    compare(_host(kd), k_ref, k, 3, N, _token_mask(B, S, N, H, H, np.zeros((B, S), bool)))
 
 
 def test_qkv_empty_and_rejects(lib, cuda):
@@ -209,13 +218,13 @@ def test_qkv_workload_full_size(lib, orc, cuda, name):
     none_bad = np.zeros((B, S), dtype=bool)
     bi = torch.arange(B, device=cuda)[:, None].expand(B, S)
     ri = torch.from_numpy(pos).to(cuda)
-    k_rows = kc[bi, :, ri].reshape(B, S, Nkv * H).cpu().numpy()
-    v_rows = vc[bi, :, ri].reshape(B, S, Nkv * H).cpu().numpy()
+    k_rows = _host(kc[bi, :, ri].reshape(B, S, Nkv * H))
+    v_rows = _host(vc[bi, :, ri].reshape(B, S, Nkv * H))
     if norm:
-        compare_norm(qo.cpu().numpy(), q_ref, Nq, H, H, 0)
+        compare_norm(_host(qo), q_ref, Nq, H, H, 0)
         compare_norm(k_rows, k_ref, Nkv, H, H, 0)
     else:
-        compare(qo.cpu().numpy(), q_ref, _heads(x, B, S, 0, Nq, Ntot, H), 3, Nq,
+        compare(_host(qo), q_ref, _heads(x, B, S, 0, Nq, Ntot, H), 3, Nq,
                 _token_mask(B, S, Nq, H, H, none_bad))
         compare(k_rows, k_ref, _heads(x, B, S, Nq, Nq + Nkv, Ntot, H), 3, Nkv,
                 _token_mask(B, S, Nkv, H, H, none_bad))
@@ -230,9 +239,12 @@ def test_qkv_workload_full_size(lib, orc, cuda, name):
 # ---------------------------------------------------------------------------
 
 def _ulp(v, dtype):
-    a = np.abs(v.astype(np.float64))
+    """ulp of float64 values v in storage type dtype (float16, bfloat16 bits, float32)."""
+    a = np.abs(v)
     if dtype == np.float16:
         return 2.0 ** (np.floor(np.log2(np.maximum(a, 2.0 ** -14))) - 10)
+    if dtype == BF16:
+        return 2.0 ** (np.floor(np.log2(np.maximum(a, 2.0 ** -126))) - 7)
     return 2.0 ** (np.floor(np.log2(np.maximum(a, 2.0 ** -126))) - 23)
 
 
@@ -256,8 +268,8 @@ def compare_norm(got, ref, N, H, rd, inter):
         magnitude; no bit-exact fraction is expected."""
     assert got.shape == ref.shape and got.dtype == ref.dtype
     dtype = ref.dtype.type
-    g = got.reshape(-1, N, H).astype(np.float64)
-    r = ref.reshape(-1, N, H).astype(np.float64)
+    g = to_float64(got).reshape(-1, N, H)
+    r = to_float64(ref).reshape(-1, N, H)
     h = rd // 2
     i0 = np.arange(h) * 2 if inter else np.arange(h)
     i1 = i0 + 1 if inter else i0 + h
@@ -265,7 +277,7 @@ def compare_norm(got, ref, N, H, rd, inter):
     pr = np.sqrt(r[..., i0] ** 2 + r[..., i1] ** 2)
     rho[..., i0] = np.maximum(rho[..., i0], pr)
     rho[..., i1] = np.maximum(rho[..., i1], pr)
-    if dtype == np.float16:
+    if dtype in (np.float16, BF16):
         tol = _ulp(r, dtype) + 3 * _ulp(rho, dtype)
     else:
         tol = _ulp(r, dtype) + 3e-6 * rho
@@ -273,7 +285,7 @@ def compare_norm(got, ref, N, H, rd, inter):
     bad = d > tol
     assert not bad.any(), f"{int(bad.sum())} elements beyond the bound; worst excess {float((d - tol).max())}"
     exact = float((d == 0).mean())
-    if dtype == np.float16:
+    if dtype in (np.float16, BF16):
         assert exact >= 0.97, f"only {exact:.4f} of the elements are bit-exact"
     return exact
 
@@ -281,27 +293,27 @@ def compare_norm(got, ref, N, H, rd, inter):
 def _run_norm_case(lib, orc, torch, cuda, dt, packed, cache, inter, rot, implicit, H, offset=0, Nq=8, Nkv=2,
                    B=3, S=37, R=64, L=80, seed=0, eps=1e-6):
     rng = np.random.default_rng(1000 + seed)
-    npdt = np.float16 if dt == "f16" else np.float32
+    npdt = {"f16": np.float16, "f32": np.float32, "bf16": BF16}[dt]
     rd = 0 if rot == "full" else H // 2
     rdw = rd or H
     h = rdw // 2
     Ntot = Nq + 2 * Nkv
-    qkv = (rng.standard_normal((B, S, Ntot * H)) * rng.uniform(0.1, 10.0, (B, S, Ntot, 1)).repeat(H, -1)
-           .reshape(B, S, Ntot * H)).astype(npdt)
+    qkv = cast(rng.standard_normal((B, S, Ntot * H)) * rng.uniform(0.1, 10.0, (B, S, Ntot, 1)).repeat(H, -1)
+               .reshape(B, S, Ntot * H), npdt)
     q, k, v = _heads(qkv, B, S, 0, Nq, Ntot, H), _heads(qkv, B, S, Nq, Nq + Nkv, Ntot, H), \
         _heads(qkv, B, S, Nq + Nkv, Ntot, Ntot, H)
-    wq = rng.uniform(0.5, 2.0, H).astype(npdt)
-    wk = rng.uniform(0.5, 2.0, H).astype(npdt)
+    wq = cast(rng.uniform(0.5, 2.0, H), npdt)
+    wk = cast(rng.uniform(0.5, 2.0, H), npdt)
     theta = rng.uniform(-np.pi, np.pi, (R, h))
-    cos, sin = np.cos(theta).astype(npdt), np.sin(theta).astype(npdt)
+    cos, sin = cast(np.cos(theta), npdt), cast(np.sin(theta), npdt)
     past = np.array([0, 11, 50], dtype=np.int32)[:B]
     if implicit:
         pos = None
     else:
         pos = rng.integers(0, R, (B, S))
         pos[0, 5], pos[1, 0], pos[-1, -1] = R + 3, -1, R
-    kc0 = rng.standard_normal((B, Nkv, L, H)).astype(npdt) if cache else None
-    vc0 = rng.standard_normal((B, Nkv, L, H)).astype(npdt) if cache else None
+    kc0 = cast(rng.standard_normal((B, Nkv, L, H)), npdt) if cache else None
+    vc0 = cast(rng.standard_normal((B, Nkv, L, H)), npdt) if cache else None
     use_past = cache or implicit
     q_ref, k_ref, kc_ref, vc_ref, n_oor, n_skip = orc.rope_qkv(
         qkv if packed else q, cos, sin, pos, num_heads=Nq, kv_num_heads=Nkv, key=None if packed else k,
@@ -317,11 +329,11 @@ def _run_norm_case(lib, orc, torch, cuda, dt, packed, cache, inter, rot, implici
                                 past_seq_lens=_dev(past, torch, cuda) if use_past else None, status=status,
                                 q_norm_weight=dv(wq), k_norm_weight=dv(wk), epsilon=eps)
     torch.cuda.synchronize()
-    compare_norm(qo.cpu().numpy(), q_ref, Nq, H, rdw, inter)
+    compare_norm(_host(qo), q_ref, Nq, H, rdw, inter)
     if not cache:
-        compare_norm(ko.cpu().numpy(), k_ref, Nkv, H, rdw, inter)
+        compare_norm(_host(ko), k_ref, Nkv, H, rdw, inter)
     else:
-        kc_g, vc_g = kc_d.cpu().numpy(), vc_d.cpu().numpy()
+        kc_g, vc_g = _host(kc_d), _host(vc_d)
         assert np.array_equal(vc_g.view(np.uint8), vc_ref.view(np.uint8))   # V: copies, rest untouched
         written = np.zeros((B, L), dtype=bool)
         for b in range(B):
@@ -335,7 +347,7 @@ def _run_norm_case(lib, orc, torch, cuda, dt, packed, cache, inter, rot, implici
     assert int(status.item()) == (1 if n_oor else 0) | (4 if n_skip else 0)
 
 
-NORM_GRID = list(itertools.product(["f16", "f32"], [0, 1], [0, 1], ["full", "partial"], [(0, 0), (1, 1)]))
+NORM_GRID = list(itertools.product(["f16", "f32", "bf16"], [0, 1], [0, 1], ["full", "partial"], [(0, 0), (1, 1)]))
 
 
 @pytest.mark.parametrize("dt,cache,inter,rot,pk_impl", NORM_GRID)
