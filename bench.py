@@ -375,16 +375,17 @@ def n_buffer_sets(w):
     return max(2, math.ceil(4 * L2_BYTES / per_set))
 
 
-def time_steps(torch, step, steps, stream_handle, fused=False, sample_every=1):
+def time_steps(torch, step, steps, stream_handle, fused=False, sample_every=0):
     """Time `steps` launches (rotating buffer sets) with CUDA events on the launching stream.
 
-    One event pair brackets the whole run (the throughput); every
-    `sample_every`-th launch is also bracketed by its own pair (its duration).
-    Unbracketed launches follow each other directly, as in a real stream, so
-    the next launch can start its prologue while the previous one drains.
+    One event pair brackets the whole run (the throughput). With
+    `sample_every` > 0, every `sample_every`-th launch is also bracketed by its
+    own pair (an isolated launch: the pair stops the next launch from starting
+    its prologue while this one drains, and adds the event round trip).
+    Unbracketed launches follow each other directly, as in a real stream.
     """
     n_sets = len(step.xs)
-    sampled = list(range(0, steps, max(1, sample_every)))
+    sampled = list(range(0, steps, sample_every)) if sample_every > 0 else []
     starts = {k: torch.cuda.Event(enable_timing=True) for k in sampled}
     ends = {k: torch.cuda.Event(enable_timing=True) for k in sampled}
     t_start = torch.cuda.Event(enable_timing=True)
@@ -405,6 +406,37 @@ def time_steps(torch, step, steps, stream_handle, fused=False, sample_every=1):
     return total_ms, kern
 
 
+def time_graph(torch, step, launches, replays, fused=False):
+    """Device time per launch with no host in the loop: `launches` calls
+    (rotating buffer sets) captured once into a CUDA graph, replayed `replays`
+    times between one event pair. For workloads whose kernels are shorter
+    than the host's per-call cost, this is the GPU's own time per step."""
+    n_sets = len(step.xs)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for k in range(3):
+            step.launch(k % n_sets, ctypes.c_void_p(side.cuda_stream), fused)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        cap = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+        for k in range(launches):
+            step.launch(k % n_sets, cap, fused)
+    g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(replays):
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / (replays * launches)
+    del g
+    return ms
+
+
 def gpu_arm(args, rank, world, local_rank):
     import torch
 
@@ -421,10 +453,12 @@ def gpu_arm(args, rank, world, local_rank):
     w = wl.WORKLOADS[args.workload]
     stream = torch.cuda.current_stream(device)
     sh = ctypes.c_void_p(stream.cuda_stream)
-    nbytes = wl.algorithmic_bytes(w)
+    # the on-the-fly workloads time their fused entry point; the Q/K workloads the fused op
+    fused = w.kind in ("qkv", "fused", "mrope_fused")
+    nbytes = wl.algorithmic_bytes(w, cached=not fused or w.kind == "qkv")
     step = make_step(rp, torch, w, device, n_buffer_sets(w), shard=rank, dynamic=args.schedule == "dynamic")
     for k in range(args.warmup):
-        step.launch(k % len(step.xs), sh)
+        step.launch(k % len(step.xs), sh, fused)
     torch.cuda.synchronize()
     kernel_family = rp.last_kernel()  # what the variant chose for this workload
 
@@ -436,8 +470,9 @@ def gpu_arm(args, rank, world, local_rank):
         torch.distributed.barrier()
     torch.cuda.synchronize()
     t0 = time.time()
-    total_ms, kern = time_steps(torch, step, args.steps, sh, fused=w.kind == "qkv", sample_every=8)
+    total_ms, _ = time_steps(torch, step, args.steps, sh, fused=fused)
     t1 = time.time()
+    total_ms_local = total_ms
     if world > 1:
         torch.distributed.barrier()
         total_ms = max_over_ranks(total_ms, device)
@@ -445,14 +480,19 @@ def gpu_arm(args, rank, world, local_rank):
 
     ms_per_step = total_ms / args.steps
     value, gelem = aggregate_throughput(nbytes, w.numel, args.steps, total_ms, world)
-    kern_ms = float(np.mean(kern))
+    # A step is exactly one launch of one kernel, so that kernel's average
+    # launch duration is this rank's timed region over K.
+    kern_ms = total_ms_local / args.steps
     peak, peak_src = measured_peak()
     achieved = nbytes / (kern_ms * 1e-3) / 1e9
+    # context, outside the timed region: the same launch bracketed alone by an event pair
+    _, iso = time_steps(torch, step, min(400, args.steps), sh, fused=fused, sample_every=1)
+    iso_ms = float(np.median(iso))
 
     out = None
     if rank == 0:
         rows = {} if (args.no_rows or args.quick) else measure_rows(args, torch, rp, device, peak)
-        e2e = None if (args.quick or w.kind == "qkv") else measure_e2e(args, torch, step, sh, nbytes)
+        e2e = None if (args.quick or fused) else measure_e2e(args, torch, step, sh, nbytes)
         cpu = cpu_baseline(args, w) if (world == 1 and not args.quick) else None
         out = {
             "metric": METRIC,
@@ -478,8 +518,8 @@ def gpu_arm(args, rank, world, local_rank):
                 "l2": f"inputs rotate over {len(step.xs)} X/Y buffer sets "
                       f"({len(step.xs) * 2 * w.numel * 2 / 2**20:.0f} MiB) > 129 MiB L2; no flush kernel",
                 "launch": "one C-ABI call per step on torch's current stream; the host queues launches "
-                          "ahead of the GPU; timed region = CUDA events around the K steps; every 8th "
-                          "step also bracketed by its own events (kernel duration for the roofline)",
+                          "ahead of the GPU; timed region = one CUDA event pair around the K steps, "
+                          "nothing else in it",
                 "parallelism": f"{world} independent replicas (per-GPU batch)",
                 "schedule": args.schedule + (" (tiles drawn from a scratch counter)" if args.schedule == "dynamic"
                                              else " (tiles dealt round robin)"),
@@ -490,6 +530,13 @@ def gpu_arm(args, rank, world, local_rank):
                 "peak_source": peak_src,
                 "kernel": f"{kernel_family} (variant {args.variant}: the one kernel of the step)",
                 "kernel_us": round(kern_ms * 1e3, 3),
+                "kernel_us_how": "timed region / K on the launching stream (a step is one launch of this "
+                                 "kernel, back to back as in a real stream)",
+                "kernel_us_isolated": round(iso_ms * 1e3, 3),
+                "frac_isolated": round(nbytes / (iso_ms * 1e-3) / 1e9 / peak, 4),
+                "isolated_how": "median of 400 launches each bracketed alone by its own event pair, "
+                                "outside the timed region (adds the pair's round trip and the ramp that "
+                                "back-to-back launches overlap)",
                 "frac_of_nominal_8tbs": round(achieved / 8000.0, 4),
             },
             "clocks": clocks,
@@ -505,7 +552,10 @@ def gpu_arm(args, rank, world, local_rank):
 
 
 def measure_rows(args, torch, rp, device, peak):
-    """Every workload (and both M-RoPE layouts, fused and cached decode), timed the same way."""
+    """Every workload (and both M-RoPE layouts, fused and cached decode), timed three ways:
+    each launch alone between its own event pair (median), back to back from
+    the host (includes the host's per-call cost where that exceeds the
+    kernel), and replayed from a CUDA graph of 64 launches (device time)."""
     stream = torch.cuda.current_stream(device)
     sh = ctypes.c_void_p(stream.cuda_stream)
     rows = {}
@@ -521,7 +571,10 @@ def measure_rows(args, torch, rp, device, peak):
             rp.set_variant(variant)
             for k in range(20):
                 step.launch(k % len(step.xs), sh, fused)
-            total_ms, kern = time_steps(torch, step, args.row_steps, sh, fused)
+            total_ms, kern = time_steps(torch, step, args.row_steps, sh, fused, sample_every=1)
+            graph_ms = None
+            if not (w.kind == "qkv" and not fused):  # the unfused Q/K path is torch ops: not captured
+                graph_ms = time_graph(torch, step, 64, max(2, args.row_steps // 64), fused)
             rp.set_variant(prev)
             nbytes = wl.algorithmic_bytes(w, cached=not fused or w.kind == "qkv")
             kern_ms = float(np.median(kern))
@@ -534,6 +587,10 @@ def measure_rows(args, torch, rp, device, peak):
                 "frac_of_measured_peak": round(gbs / peak, 4), "frac_of_nominal_8tbs": round(gbs / 8000, 4),
                 "bytes": nbytes,
             }
+            if graph_ms is not None:
+                ggbs = nbytes / (graph_ms * 1e-3) / 1e9
+                rows[key].update({"us_per_step_graph": round(graph_ms * 1e3, 3), "GB_s_graph": round(ggbs, 1),
+                                  "frac_graph": round(ggbs / peak, 4)})
         del step
         torch.cuda.empty_cache()
     # one-time setup row: cache build of the largest table
