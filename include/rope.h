@@ -389,7 +389,8 @@ const char* rope_last_error(void);
 
 /* Kernel family that the last call on the calling thread which launched work
    used: "rope_rows_kernel" (SIMT), "rope_tma_kernel" (TMA pipeline),
-   "rope_fused_kernel", "rope_qkv_kernel" or "rope_cache_build_kernel"; "" before the first
+   "rope_fused_kernel", "rope_qkv_kernel" (SIMT), "rope_qkv_tma_kernel" (TMA pipeline) or
+   "rope_cache_build_kernel"; "" before the first
    launch. Calls that fail or launch nothing (empty X) leave it unchanged.
    A diagnostic for profilers and benchmarks: the pages have no counterpart.
    The string is static; never free it. */

@@ -28,6 +28,7 @@
 
 #include "rope.h"
 #include "rope_internal.h"
+#include "rope_qkv_tma.cuh"
 #include "rope_tma.cuh"
 
 // Launch-shape defaults (threads a CTA aims for; resident-CTA waves in the
@@ -51,6 +52,19 @@
 #endif
 #ifndef ROPE_TMA_MAX_STAGES
 #define ROPE_TMA_MAX_STAGES 8
+#endif
+// Pipelined Q/K kernel: largest tile (bytes of NG heads x TS tokens) and most
+// tokens per tile.
+#ifndef ROPE_QKV_TMA_TILE_BYTES
+#define ROPE_QKV_TMA_TILE_BYTES 32768
+#endif
+#ifndef ROPE_QKV_TMA_MAX_TS
+#define ROPE_QKV_TMA_MAX_TS 16
+#endif
+// Its shared-memory budget per CTA (two CTAs per SM): three stages of a
+// 32 KB tile with its cos/sin rows.
+#ifndef ROPE_QKV_TMA_SMEM_BUDGET
+#define ROPE_QKV_TMA_SMEM_BUDGET (112 * 1024)
 #endif
 
 using namespace rope_gb300;
@@ -424,6 +438,141 @@ rope_status plan_tma(rope_dtype dt, const Geom& g, int es, int rank, int slots, 
   T->L.smem = smem;
   ROPE_TRY(encode_x_map(&T->mx, dt, g, rank, es, x, tp));
   ROPE_TRY(encode_x_map(&T->my, dt, g, rank, es, y, tp));
+  return ROPE_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Pipelined Q/K planning (see rope_qkv_tma.cuh).
+// ---------------------------------------------------------------------------
+struct QkvTmaLaunch {
+  QTParams tp;
+  QKVMaps maps;
+  Launch L;
+};
+
+// One 4-D tiled tensor map: dims and strides innermost first (strides in
+// bytes, dims[1..3]), box (bx0..bx3).
+rope_status encode4(CUtensorMap* m, rope_dtype dt, const void* base, const cuuint64_t (&dims)[4],
+                    const cuuint64_t (&strides)[3], const cuuint32_t (&box)[4]) {
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  const CUtensorMapDataType ty = dt == ROPE_F32   ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                 : dt == ROPE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                   : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  CUresult e = encode_tiled()(m, ty, 4, const_cast<void*>(base), dims, strides, box, estr,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (e != CUDA_SUCCESS) return fail(ROPE_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)e);
+  return ROPE_OK;
+}
+
+// The pipelined Q/K kernel takes the 128-bit path with head sizes up to 256
+// elements; with RMSNorm, full rotation whose pair units fill a power-of-two
+// lane group. The automatic choice sends it the calls whose packed Q/K/V are
+// at least ROPE_TMA_MIN_BYTES (smaller ones are launch-bound either way).
+bool qkv_tma_eligible(const Geom& g, int es, bool vec, bool norm, int64_t n_all, int64_t max_len,
+                      int64_t qkv_bytes) {
+  const int variant = g_variant.load(std::memory_order_relaxed);
+  if (variant == ROPE_VARIANT_SIMT) return false;
+  if (!vec || g.H > 256) return false;
+  const int64_t nP = g.h / (16 / es);
+  if (nP < 1 || nP > 32) return false;
+  if (norm && (g.rd != g.H || (nP & (nP - 1)))) return false;
+  if (g.S > INT32_MAX || g.B > INT32_MAX || n_all > INT32_MAX || max_len > INT32_MAX) return false;
+  if (variant == ROPE_VARIANT_AUTO && qkv_bytes < (int64_t)ROPE_TMA_MIN_BYTES) return false;
+  return encode_tiled() != nullptr;
+}
+
+// Tile shape, stage layout, grid and tensor maps; ROPE_ERR_UNSUPPORTED (no
+// message) when the shape does not fit, and the caller takes the SIMT kernel.
+rope_status plan_qkv_tma(rope_dtype dt, const Geom& g, int es, const QKVParams& a, const void* query,
+                         const void* q_out, const void* fn, QkvTmaLaunch* T) {
+  const int V = 16 / es;
+  const int64_t nP = g.h / V;
+  QTParams& tp = T->tp;
+  memset(&tp, 0, sizeof(tp));
+  memset(&T->maps, 0, sizeof(T->maps));
+  // tokens: each gather lane holds one token's position, and a tile's cos/sin
+  // pieces fit the gather warp's kMaxGather copies per lane
+  int64_t TS = g.S < ROPE_QKV_TMA_MAX_TS ? g.S : ROPE_QKV_TMA_MAX_TS;
+  while (TS > 1 && TS * 2 * nP > 32 * kMaxGather) --TS;
+  if (TS < 1 || TS > 32 || TS * nP > kTmaConsumers) return ROPE_ERR_UNSUPPORTED;
+  const int64_t tpc = kTmaConsumers / (TS * nP);
+  // heads: a divisor of Nkv (so of Nq) that each column's threads cover with
+  // at most kMaxHeads heads apiece, within the tile budget
+  int64_t NG = 1;
+  for (int64_t d = 1; d <= a.Nkv; ++d) {
+    if (a.Nkv % d) continue;
+    if (d > kMaxHeads * tpc) break;
+    if (d > 1 && d * TS * g.H * es > ROPE_QKV_TMA_TILE_BYTES) break;
+    NG = d;
+  }
+  tp.TS = (int32_t)TS;
+  tp.NG = (int32_t)NG;
+  tp.Gq = (int32_t)(a.Nq / NG);
+  tp.Gk = (int32_t)(a.Nkv / NG);
+  tp.G = tp.Gq + tp.Gk + (a.cache ? tp.Gk : 0);
+  tp.s_tiles = (int32_t)((g.S + TS - 1) / TS);
+  tp.nT = (int32_t)((g.H - g.rd) / V);
+  tp.ntiles = g.B * (int64_t)tp.s_tiles * tp.G;
+  if (tp.ntiles >= INT32_MAX) return ROPE_ERR_UNSUPPORTED;
+  const uint32_t blk = (uint32_t)(TS * g.H * es);
+  tp.blk_bytes = (blk + 127) / 128 * 128;
+  tp.x_bytes = (uint32_t)NG * blk;
+  tp.coef_off = (uint32_t)NG * tp.blk_bytes;
+  tp.flag_off = tp.coef_off + (uint32_t)(TS * 2 * g.h * es);
+  tp.hdr_off = (tp.flag_off + (uint32_t)TS * 4 + 15) / 16 * 16;
+  tp.stage_bytes = (tp.hdr_off + 16 + 1023) / 1024 * 1024;
+  tp.bar_bytes = 1024;
+  int64_t K = (ROPE_QKV_TMA_SMEM_BUDGET - tp.bar_bytes) / tp.stage_bytes;
+  if (K > ROPE_TMA_MAX_STAGES) K = ROPE_TMA_MAX_STAGES;
+  if (K < 2) return ROPE_ERR_UNSUPPORTED;
+  tp.K = (int32_t)K;
+  const bool packed = a.packed != 0;
+  const int64_t n_all = (int64_t)a.Nq + 2 * a.Nkv;
+  tp.head_off[0] = 0;
+  tp.head_off[1] = packed ? a.Nq : 0;
+  tp.head_off[2] = packed ? a.Nq + a.Nkv : 0;
+  const size_t smem = tp.bar_bytes + (size_t)K * tp.stage_bytes;
+
+  int sms = 0, per_sm = 0;
+  rope_status st = device_facts(fn, kTmaThreads, smem, &sms, &per_sm);
+  if (st != ROPE_OK) return st;
+  int64_t gx = (int64_t)sms * per_sm;
+  if (gx > tp.ntiles) gx = tp.ntiles;
+  T->L.grid = dim3((unsigned)gx, 1, 1);
+  T->L.block = dim3(kTmaThreads, 1, 1);
+  T->L.smem = smem;
+
+  // maps: sources (H, heads, S, B) and q_out / k_out (H, heads, S, B) with a
+  // TS x NG-head box (Q, K without caches) or a one-head box (K and V into the
+  // caches); caches (H, max_len, Nkv, B), TS rows of one head
+  const cuuint64_t H = (cuuint64_t)g.H, S = (cuuint64_t)g.S, B = (cuuint64_t)g.B, E = (cuuint64_t)es;
+  const cuuint32_t box_wide[4] = {(cuuint32_t)g.H, (cuuint32_t)NG, (cuuint32_t)TS, 1};
+  const cuuint32_t box_head[4] = {(cuuint32_t)g.H, 1, (cuuint32_t)TS, 1};
+  const cuuint32_t box_row[4] = {(cuuint32_t)g.H, (cuuint32_t)TS, 1, 1};
+  auto seq_map = [&](CUtensorMap* m, const void* base, int64_t heads, bool wide) {
+    const cuuint64_t n = (cuuint64_t)heads;
+    const cuuint64_t dims[4] = {H, n, S, B};
+    const cuuint64_t strides[3] = {H * E, n * H * E, S * n * H * E};
+    return encode4(m, dt, base, dims, strides, wide ? box_wide : box_head);
+  };
+  auto cache_map = [&](CUtensorMap* m, const void* base) {
+    const cuuint64_t L = (cuuint64_t)a.max_len, n = (cuuint64_t)a.Nkv;
+    const cuuint64_t dims[4] = {H, L, n, B};
+    const cuuint64_t strides[3] = {H * E, L * H * E, n * L * H * E};
+    return encode4(m, dt, base, dims, strides, box_row);
+  };
+  const bool kv_wide = !a.cache;
+  ROPE_TRY(seq_map(&T->maps.src[0], query, packed ? n_all : a.Nq, true));
+  ROPE_TRY(seq_map(&T->maps.src[1], packed ? query : a.k, packed ? n_all : a.Nkv, kv_wide));
+  if (a.cache) ROPE_TRY(seq_map(&T->maps.src[2], packed ? query : a.v, packed ? n_all : a.Nkv, false));
+  ROPE_TRY(seq_map(&T->maps.dst[0], q_out, a.Nq, true));
+  if (a.cache) {
+    ROPE_TRY(cache_map(&T->maps.dst[1], a.k_cache));
+    ROPE_TRY(cache_map(&T->maps.dst[2], a.v_cache));
+  } else {
+    ROPE_TRY(seq_map(&T->maps.dst[1], a.k_out, a.Nkv, true));
+  }
   return ROPE_OK;
 }
 
@@ -859,6 +1008,26 @@ rope_status qkv_impl(rope_dtype dtype, int64_t batch, int64_t seq, int32_t num_h
   qa.qw = q_weight;
   qa.kw = k_weight;
   qa.eps = epsilon;
+  const int64_t n_all = (int64_t)num_heads + 2 * kv_num_heads;
+  if (qkv_tma_eligible(g, es, vec, norm, n_all, cache ? max_cache_len : 0, packed_numel * es)) {
+    const void* tfn = qkv_tma_kernel(dtype, interleaved != 0, position_ids == nullptr, norm);
+    QkvTmaLaunch T;
+    KParams tk = kp;
+    tk.S = g.S;
+    tk.H = g.H;
+    tk.h = (int32_t)g.h;
+    tk.rd = (int32_t)g.rd;
+    tk.nP = (int32_t)(g.h / (16 / es));
+    const rope_status ts = plan_qkv_tma(dtype, g, es, qa, query, q_out, tfn, &T);
+    if (ts == ROPE_OK) {
+      void* targs[] = {&tk, &qa, &T.tp, &T.maps};
+      cudaError_t e = launch_pdl(tfn, T.L.grid, T.L.block, T.L.smem, stream, targs);
+      if (e != cudaSuccess) return cuda_fail(e, "rope_apply_qkv launch (pipelined)");
+      g_last_kernel = "rope_qkv_tma_kernel";
+      return ROPE_OK;
+    }
+    if (ts != ROPE_ERR_UNSUPPORTED) return ts;
+  }
   Launch L;
   ROPE_TRY(plan(g, es, vec, fn, false, &kp, &L, /*unit_groups=*/norm));
   void* args[] = {&kp, &qa};

@@ -87,4 +87,8 @@ void set_last_error(const char* msg);
 // takes (KParams, TParams, CUtensorMap x, CUtensorMap y).
 const void* tma_kernel(int dtype, bool interleaved, bool rank4, Coef mode);
 
+// TMA-pipelined Q/K rotation with the cache append (vector path); its launch
+// takes (KParams, QKVParams, QTParams, QKVMaps).
+const void* qkv_tma_kernel(int dtype, bool interleaved, bool implicit_pos, bool rms_norm);
+
 }  // namespace rope_gb300

@@ -1,0 +1,589 @@
+// TMA-pipelined Q/K rotation with the key/value cache append (and the
+// optional QK-RMSNorm) for sm_103a.
+//
+// The same operation as rope_qkv_kernel (rope_qkv.cuh) -- every Q and K head
+// rotated as RotaryEmbedding rotates one head of a rank-3 X, V copied, K and V
+// appended to the caches at rows past[b] + s -- with the bytes in flight held
+// in shared memory instead of registers, as in rope_tma_kernel. A tile is NG
+// heads of one role (Q, K or V) times TS consecutive tokens of one batch. A Q
+// tile (and a K tile without caches) is one tensor box of TS x NG x H, laid
+// out in the stage as in the tensor and stored to q_out (k_out) as one box; a
+// cache tile is NG per-head boxes of TS x H, which are exactly TS consecutive
+// rows of one head of a (B, Nkv, max_len, H) cache.
+//   copy warp  (lane 0) starts a tile's tensor copies into a free stage and
+//              writes the finished tile back with tensor stores;
+//   gather warp loads the tile's positions and gathers its cos/sin rows
+//              (Q and K tiles) with asynchronous 16-byte copies;
+//   consumers  normalise (RMSNorm) and rotate Q and K tiles in place; V tiles
+//              pass through untouched.
+// A cache tile that is ragged (the batch's last, partial token tile) or whose
+// rows leave [0, max_len) is not given to the tensor store -- a store must
+// neither write rows past the batch's new tokens nor start at a negative row
+// -- but stored row by row by the consumers, which skip rows outside the cache
+// (status bit 2). Barrier protocol, bounded waits and the exit on a timeout
+// are those of rope_tma_kernel (rope_tma.cuh).
+//
+// Definitions followed (web pages, by title and section):
+//  - "com.microsoft.SparseAttention" README: Description, Inputs (query or
+//    packed [Q|K|V], key, value, past_key / past_value updated in place),
+//    Attributes (do_rotary, kv_num_heads, rotary_interleaved).
+//  - onnxruntime pull request "Add RotaryEmbedding fusion for Qwen3 on-the-fly
+//    RoPE patterns": Verification and Qwen3 Architecture (RoPE on Q and K; GQA;
+//    QK-Norm: RMSNorm on Q and K before RoPE).
+#pragma once
+
+#include "rope_qkv.cuh"
+#include "rope_tma.cuh"
+
+namespace rope_gb300 {
+
+// Heads a consumer thread loads and reduces together.
+#ifndef ROPE_QKV_TMA_HEAD_BATCH
+#define ROPE_QKV_TMA_HEAD_BATCH 2
+#endif
+
+// Tile geometry and stage layout of the pipelined Q/K kernel (host-planned).
+struct QTParams {
+  int32_t TS, NG, K;      // tokens per tile, heads per tile, stages
+  int32_t G, Gq, Gk;      // head groups per token tile: Gq of Q, Gk of K, then Gk of V (cache mode)
+  int32_t s_tiles;        // ceil(S / TS)
+  int32_t nT;             // tail units (H - rd) / V
+  int64_t ntiles;
+  uint32_t blk_bytes;     // cache tiles: one head's TS x H block in a stage (a multiple of 128 bytes)
+  uint32_t x_bytes;       // transaction bytes of a tile: NG boxes
+  uint32_t coef_off;      // stage offsets: cos/sin rows, per-token flags, positions, header
+  uint32_t flag_off;
+  uint32_t hdr_off;
+  uint32_t stage_bytes;
+  uint32_t bar_bytes;
+  int32_t head_off[3];    // source head of each role's head 0 (packed: 0, Nq, Nq + Nkv)
+};
+
+// Tensor maps: the source of each role (Q, K, V) and its destination (q_out;
+// k_out or k_cache; v_cache). Q and K-without-caches boxes are TS x NG heads;
+// cache-mode K and V boxes are one head's TS rows.
+struct QKVMaps {
+  CUtensorMap src[3];
+  CUtensorMap dst[3];
+};
+
+struct QTile {
+  int role;       // 0 Q, 1 K, 2 V
+  int n;          // tokens of the tile inside the sequence (the box may run past S)
+  int32_t head0;  // first head of the tile within its role
+  int32_t s0;     // first token (sequence index)
+  int32_t b;
+};
+
+__device__ __forceinline__ QTile qtile_of(const KParams& p, const QTParams& tp, int64_t t64) {
+  QTile q;
+  const uint32_t t = (uint32_t)t64;  // tile counts stay below 2^31
+  const uint32_t g = t % (uint32_t)tp.G;
+  const uint32_t rest = t / (uint32_t)tp.G;
+  const uint32_t st = rest % (uint32_t)tp.s_tiles;
+  q.b = (int32_t)(rest / (uint32_t)tp.s_tiles);
+  q.s0 = (int32_t)(st * (uint32_t)tp.TS);
+  const int64_t left = p.S - q.s0;
+  q.n = (int)(left < tp.TS ? left : tp.TS);
+  if ((int)g < tp.Gq) {
+    q.role = 0;
+    q.head0 = (int32_t)g * tp.NG;
+  } else if ((int)g < tp.Gq + tp.Gk) {
+    q.role = 1;
+    q.head0 = ((int32_t)g - tp.Gq) * tp.NG;
+  } else {
+    q.role = 2;
+    q.head0 = ((int32_t)g - tp.Gq - tp.Gk) * tp.NG;
+  }
+  return q;
+}
+
+// First cache row of a K or V tile in cache mode.
+__device__ __forceinline__ int64_t qtile_row0(const QKVParams& a, const QTile& q) {
+  return (a.past ? (int64_t)__ldg(a.past + q.b) : 0) + q.s0;
+}
+
+// Q tiles and (without caches) K tiles are one NG-head box in the stage,
+// laid out [TS][NG][H] like the tensor; cache tiles are NG per-head blocks of
+// TS x H, the rows of the cache.
+__device__ __forceinline__ bool qtile_wide(const QKVParams& a, const QTile& q) {
+  return q.role == 0 || !a.cache;
+}
+
+// Whether a cache tile goes out row by row from the consumers instead of by
+// tensor store: ragged, or not entirely inside [0, max_len).
+__device__ __forceinline__ bool qtile_direct(const QKVParams& a, const QTParams& tp, const QTile& q,
+                                             int64_t row0) {
+  return q.role != 0 && a.cache && (q.n < tp.TS || row0 < 0 || row0 + tp.TS > a.max_len);
+}
+
+// ---------------------------------------------------------------------------
+// Packed arithmetic for 16-bit storage (float16, bfloat16): two values per
+// 32-bit word, float32x2 operations (sm_100 and later). Each lane of a packed
+// operation rounds exactly as the scalar operation does, so every result has
+// the bits of rotate() and norm_weight() in rope_kernels.cuh / rope_qkv.cuh.
+// ---------------------------------------------------------------------------
+template <class T>
+struct P2;
+template <>
+struct P2<__half> {
+  using w2 = __half2;
+  static __device__ __forceinline__ float2 tof(w2 v) { return __half22float2(v); }
+  static __device__ __forceinline__ w2 fromf(float2 f) { return __float22half2_rn(f); }
+};
+template <>
+struct P2<__nv_bfloat16> {
+  using w2 = __nv_bfloat162;
+  static __device__ __forceinline__ float2 tof(w2 v) { return __bfloat1622float2(v); }
+  static __device__ __forceinline__ w2 fromf(float2 f) { return __float22bfloat162_rn(f); }
+};
+
+template <class T>
+struct Unit8 {  // one 16-byte unit of 8 values as 4 packed words
+  typename P2<T>::w2 w[4];
+};
+
+// Rotation of a unit pair (half split: pair j = (a[j], b[j]); interleaved:
+// pair j = elements 2j, 2j+1 of a||b) with unpacked coefficients cf/sf
+// (cf[k] = coefficients 2k, 2k+1): y0 = x0*c - x1*s, y1 = x1*c + x0*s, as
+// rotate() forms them (product, then fused multiply-add; -(x1*s) is x1*(-s)).
+template <class T, bool INTER>
+__device__ __forceinline__ void rotate8p(const Unit8<T>& a, const Unit8<T>& b, const float2 (&cf)[4],
+                                         const float2 (&sf)[4], Unit8<T>& ya, Unit8<T>& yb) {
+  using P = P2<T>;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float2 ns = make_float2(-sf[k].x, -sf[k].y);
+    if (!INTER) {
+      const float2 x0 = P::tof(a.w[k]), x1 = P::tof(b.w[k]);
+      ya.w[k] = P::fromf(__ffma2_rn(x0, cf[k], __fmul2_rn(x1, ns)));
+      yb.w[k] = P::fromf(__ffma2_rn(x1, cf[k], __fmul2_rn(x0, sf[k])));
+    } else {
+      // words 2k and 2k+1 of a||b hold pairs 2k and 2k+1
+      const float2 f0 = P::tof(k < 2 ? a.w[2 * k] : b.w[2 * k - 4]);
+      const float2 f1 = P::tof(k < 2 ? a.w[2 * k + 1] : b.w[2 * k - 3]);
+      const float2 x0 = make_float2(f0.x, f1.x), x1 = make_float2(f0.y, f1.y);
+      const float2 y0 = __ffma2_rn(x0, cf[k], __fmul2_rn(x1, ns));
+      const float2 y1 = __ffma2_rn(x1, cf[k], __fmul2_rn(x0, sf[k]));
+      const typename P::w2 p0 = P::fromf(make_float2(y0.x, y1.x));
+      const typename P::w2 p1 = P::fromf(make_float2(y0.y, y1.y));
+      if (k < 2) {
+        ya.w[2 * k] = p0;
+        ya.w[2 * k + 1] = p1;
+      } else {
+        yb.w[2 * k - 4] = p0;
+        yb.w[2 * k - 3] = p1;
+      }
+    }
+  }
+}
+
+// z = T(w * T(x * r)) on a unit whose values fx are already unpacked: the
+// first product in float32x2, the second on the 16-bit words (the product of
+// two 16-bit values is exact in float32, so the 16-bit multiply rounds it just
+// as float32-then-round does).
+template <class T>
+__device__ __forceinline__ Unit8<T> norm8p(const float2 (&fx)[4], float r, const Unit8<T>& w) {
+  using P = P2<T>;
+  const float2 r2 = make_float2(r, r);
+  Unit8<T> z;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) z.w[k] = __hmul2(P::fromf(__fmul2_rn(fx[k], r2)), w.w[k]);
+  return z;
+}
+
+template <class T, bool INTER, bool IMPLICIT, bool NORM>
+__global__ void __launch_bounds__(kTmaThreads, ROPE_TMA_MIN_CTAS)
+    rope_qkv_tma_kernel(const KParams p, const QKVParams a, const QTParams tp,
+                        const __grid_constant__ QKVMaps maps) {
+  using E = Elem<T>;
+  using bits = typename E::bits;
+  constexpr int V = 16 / sizeof(bits);
+  using VT = VecT<T, V>;
+
+  extern __shared__ __align__(1024) unsigned char smem[];
+  const uint32_t sbase = smem_addr(smem);
+  const uint32_t full0 = sbase;                // full[s]      at 8*s
+  const uint32_t done0 = sbase + 8 * tp.K;     // computed[s]  at 8*(K+s)
+  const uint32_t issued0 = sbase + 16 * tp.K;  // issued[s]    at 8*(2K+s)
+  unsigned char* stage0 = smem + tp.bar_bytes;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int H = (int)p.H;
+  const int h = p.h;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < tp.K; ++s) {
+      mbar_init(full0 + 8 * s, 33);  // the copies' arrive.expect_tx + every gather lane
+      mbar_init(done0 + 8 * s, kTmaConsumerWarps);
+      mbar_init(issued0 + 8 * s, 1);
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+#pragma unroll
+    for (int r = 0; r < 3; ++r) {
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&maps.src[r])) : "memory");
+      asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&maps.dst[r])) : "memory");
+    }
+  }
+  __syncthreads();
+  pdl_launch_dependents();
+  pdl_wait();
+
+  // stage header: [0] the tile index (copy warp), [1] a cache tile's first row (gather warp)
+  auto stage_hdr = [&](int s) -> int64_t* {
+    return reinterpret_cast<int64_t*>(stage0 + (size_t)s * tp.stage_bytes + tp.hdr_off);
+  };
+
+  if (warp == 0) {
+    // --------------------------------------------------- copy warp (lane 0)
+    if (lane == 0) {
+      const uint64_t pol = policy_evict_first();
+      bool timed_out = false;
+      auto tile_index = [&](int64_t jj) -> int64_t { return (int64_t)blockIdx.x + jj * (int64_t)gridDim.x; };
+      auto issue = [&](int64_t jj) {
+        const int s = (int)(jj % tp.K);
+        const int64_t t = tile_index(jj);
+        *stage_hdr(s) = t;
+        if (t < tp.ntiles) {
+          const QTile q = qtile_of(p, tp, t);
+          const uint32_t dst = smem_addr(stage0 + (size_t)s * tp.stage_bytes);
+          mbar_arrive_expect_tx(full0 + 8 * s, tp.x_bytes);
+          // one NG-head box, or (cache tiles) one box per head
+          const int nbox = qtile_wide(a, q) ? 1 : tp.NG;
+          for (int u = 0; u < nbox; ++u) {
+            const int c[4] = {0, tp.head_off[q.role] + q.head0 + u, q.s0, q.b};
+            tma_load_x<true>(dst + (uint32_t)u * tp.blk_bytes, &maps.src[q.role], c, full0 + 8 * s, pol);
+          }
+        } else {
+          mbar_arrive(full0 + 8 * s);  // the sentinel carries no bytes
+        }
+        mbar_arrive(issued0 + 8 * s);
+      };
+      int64_t jx = 0;
+      for (; jx < tp.K; ++jx) {
+        issue(jx);
+        if (tile_index(jx) >= tp.ntiles) break;
+      }
+      const bool all_issued_early = jx < tp.K;  // the sentinel went out with the first K
+      bool ended = all_issued_early;
+      if (!ended) jx = tp.K;
+      // the next store's tile and cache row are worked out while the previous
+      // store is still reading its stage
+      int64_t t_st = tile_index(0);
+      QTile q_st{};
+      int64_t row_st = 0;
+      auto prep = [&](int64_t t) {
+        if (t < tp.ntiles) {
+          q_st = qtile_of(p, tp, t);
+          row_st = (q_st.role != 0 && a.cache) ? qtile_row0(a, q_st) : 0;
+        }
+      };
+      prep(t_st);
+      for (int64_t j = 0;; ++j) {
+        const int s = (int)(j % tp.K);
+        if (!mbar_wait(done0 + 8 * s, (uint32_t)((j / tp.K) & 1))) {
+          timed_out = true;
+          break;
+        }
+        if (t_st >= tp.ntiles) break;  // sentinel
+        if (!qtile_direct(a, tp, q_st, row_st)) {
+          const uint32_t src = smem_addr(stage0 + (size_t)s * tp.stage_bytes);
+          const bool to_cache = !qtile_wide(a, q_st);
+          for (int u = 0; u < (to_cache ? tp.NG : 1); ++u) {
+            int c[4];
+            if (to_cache) {
+              c[0] = 0, c[1] = (int)row_st, c[2] = q_st.head0 + u, c[3] = q_st.b;
+            } else {
+              c[0] = 0, c[1] = q_st.head0 + u, c[2] = q_st.s0, c[3] = q_st.b;
+            }
+            tma_store_y<true>(&maps.dst[q_st.role], c, src + (uint32_t)u * tp.blk_bytes, pol);
+          }
+          bulk_commit();
+        }
+        t_st = tile_index(j + 1);
+        prep(t_st);
+        if (!ended) {
+          bulk_wait_read_0();  // the stage may be refilled once the store has read it
+          issue(jx);           // jx == j + K: the tile that goes into stage s next
+          ended = tile_index(jx) >= tp.ntiles;
+          ++jx;
+        }
+      }
+      bulk_wait_all();
+      if (timed_out) {
+        const uint64_t t0 = global_ns();
+        while (global_ns() - t0 < 1000000ull) {
+        }
+        if (p.oor_flag) atomicOr(p.oor_flag, 2);
+      }
+    }
+    return;
+  }
+
+  if (warp == 1) {
+    // ------------------------------------------------------------ gather warp
+    // Per Q or K tile: the tokens' positions (explicit, or past[b] + s) and
+    // range flags, then the cos/sin rows ([token][cos|sin][rd/2]) copied 16
+    // bytes at a time; the copies arrive on full[s] when they land. V tiles
+    // gather nothing. Cache tiles also get their first row in the header.
+    const bits* cosb = static_cast<const bits*>(p.cos);
+    const bits* sinb = static_cast<const bits*>(p.sin);
+    bool timed_out = false;
+    const int ch = h * (int)sizeof(bits) / 16;  // 16-byte pieces per cos (or sin) row
+    const int per_tok = 2 * ch;
+    const int pieces = tp.TS * per_tok;
+    const int rounds = (pieces + 31) / 32;  // the same for every lane: the shuffles below are warp-wide
+    for (int64_t j = 0;; ++j) {
+      const int s = (int)(j % tp.K);
+      if (!__all_sync(0xffffffffu, mbar_wait(issued0 + 8 * s, (uint32_t)((j / tp.K) & 1)))) {
+        timed_out = true;
+        break;
+      }
+      const int64_t t = *stage_hdr(s);
+      if (t >= tp.ntiles) {
+        cp_async_arrive(full0 + 8 * s);
+        break;
+      }
+      const QTile q = qtile_of(p, tp, t);
+      unsigned char* st = stage0 + (size_t)s * tp.stage_bytes;
+      if (q.role != 0 && a.cache && lane == 0) stage_hdr(s)[1] = qtile_row0(a, q);
+      if (q.role != 2) {
+        const int64_t past_b = (IMPLICIT && a.past) ? (int64_t)__ldg(a.past + q.b) : 0;
+        int64_t pp = -1;
+        uint32_t flag = 0;
+        if (lane < q.n) {
+          const int64_t sq = (int64_t)q.s0 + lane;
+          pp = IMPLICIT ? past_b + sq : __ldg(p.pos + (int64_t)q.b * p.S + sq);
+          flag = (uint64_t)pp < (uint64_t)p.cache_rows ? 1u : 0u;
+          if (!flag && q.role == 0 && q.head0 == 0 && p.oor_flag) atomicOr(p.oor_flag, 1);
+        }
+        if (lane < tp.TS) reinterpret_cast<uint32_t*>(st + tp.flag_off)[lane] = flag;
+        const uint32_t coef_addr = smem_addr(st) + tp.coef_off;
+#pragma unroll
+        for (int g = 0; g < kMaxGather; ++g) {
+          if (g >= rounds) break;
+          const int c = lane + 32 * g;
+          const bool mine = c < pieces;
+          const int lt = mine ? c / per_tok : 0;
+          const int rem = c - lt * per_tok;
+          const bool is_sin = rem >= ch;
+          const int piece = is_sin ? rem - ch : rem;
+          // token lt's position lives in lane lt
+          const int64_t row = __shfl_sync(0xffffffffu, pp, lt);
+          const uint32_t ok = __shfl_sync(0xffffffffu, flag, lt);
+          if (mine && ok)
+            cp_async16(coef_addr + 16u * (uint32_t)c,
+                       reinterpret_cast<const uint4*>((is_sin ? sinb : cosb) + row * h) + piece);
+        }
+      }
+      __syncwarp();  // flags and the header precede the lanes' (releasing) arrivals
+      cp_async_arrive(full0 + 8 * s);
+    }
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    if (timed_out && lane == 0 && p.oor_flag) atomicOr(p.oor_flag, 2);
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  // Thread q owns column (token ts, pair unit k) of the tile for heads
+  // hq, hq + tpc, ...; with RMSNorm the nP threads of one (token, head) row
+  // are an aligned lane group that adds up the row's squares with shuffles.
+  const int qi = threadIdx.x - 32 * kTmaRoleWarps;
+  const int nP = p.nP;
+  const int cols = tp.TS * nP;
+  const int tpc = kTmaConsumers / cols;  // the host keeps cols <= consumers
+  const int hpt = (tp.NG + tpc - 1) / tpc;  // heads per thread (the same for every thread)
+  const int col = qi % cols;
+  const int hq = qi / cols;
+  const bool has_col = hq < tpc;
+  const int ts = col / nP;
+  const int k = col - ts * nP;
+  int oa, ob;
+  unit_offsets<V, INTER>(k, h, oa, ob);
+  const int oc = k * V;
+  const uint32_t blk_elems = tp.blk_bytes / (uint32_t)sizeof(bits);
+  bool timed_out = false;
+  for (int64_t j = 0;; ++j) {
+    const int s = (int)(j % tp.K);
+    const bool ok = __all_sync(0xffffffffu, mbar_wait(full0 + 8 * s, (uint32_t)((j / tp.K) & 1)));
+    const int64_t t = ok ? *stage_hdr(s) : 0;
+    if (ok && t >= tp.ntiles) {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(done0 + 8 * s);
+      break;
+    }
+    if (!ok) {
+      timed_out = true;
+      break;
+    }
+    const QTile q = qtile_of(p, tp, t);
+    unsigned char* st = stage0 + (size_t)s * tp.stage_bytes;
+    bits* sx = reinterpret_cast<bits*>(st);
+    const bool tok_in = ts < q.n;
+    const bool wide = qtile_wide(a, q);
+    if (q.role != 2) {
+      const uint32_t fl = reinterpret_cast<const uint32_t*>(st + tp.flag_off)[ts];
+      const bool valid = tok_in && (fl & 1u);
+      VT c{}, sn{};
+      if (valid) {
+        const bits* cr = reinterpret_cast<const bits*>(st + tp.coef_off) + (size_t)ts * 2 * h;
+        c = *reinterpret_cast<const VT*>(cr + oc);
+        sn = *reinterpret_cast<const VT*>(cr + h + oc);
+      }
+      constexpr bool PACKED = sizeof(bits) == 2;  // float16 / bfloat16: packed arithmetic
+      VT wa{}, wb{};
+      if (NORM && has_col) {  // rd == H with the norm: the nP units cover the whole head
+        const bits* w = static_cast<const bits*>(q.role == 0 ? a.qw : a.kw);
+        wa = ld_shared_ro(reinterpret_cast<const VT*>(w + oa));
+        wb = ld_shared_ro(reinterpret_cast<const VT*>(w + ob));
+      }
+      float2 cf[4], sf[4];  // the column's coefficients, unpacked once per tile (packed path)
+      if constexpr (PACKED) {
+        Unit8<T> cu, su;
+        __builtin_memcpy(&cu, &c, 16);
+        __builtin_memcpy(&su, &sn, 16);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          cf[k] = P2<T>::tof(cu.w[k]);
+          sf[k] = P2<T>::tof(su.w[k]);
+        }
+      }
+      // A thread's heads go through in batches of HB: a batch's rows are
+      // loaded together and reduced together, so their latencies overlap.
+      constexpr int HB = ROPE_QKV_TMA_HEAD_BATCH;
+      for (int u0 = 0; u0 < hpt; u0 += HB) {  // hpt is the same for every lane
+        bool act[HB];
+        uint32_t ro[HB];
+        VT xa[HB], xb[HB];
+#pragma unroll
+        for (int u = 0; u < HB; ++u) {
+          const int hh = hq + (u0 + u) * tpc;
+          act[u] = u0 + u < hpt && has_col && tok_in && hh < tp.NG && (NORM || valid);
+          ro[u] = wide ? ((uint32_t)ts * (uint32_t)tp.NG + (uint32_t)hh) * (uint32_t)H
+                       : (uint32_t)hh * blk_elems + (uint32_t)ts * (uint32_t)H;
+          xa[u] = VT{};
+          xb[u] = VT{};
+          if (act[u]) {
+            xa[u] = *reinterpret_cast<const VT*>(sx + ro[u] + oa);
+            xb[u] = *reinterpret_cast<const VT*>(sx + ro[u] + ob);
+          }
+        }
+        if constexpr (PACKED) {
+          Unit8<T> ua[HB], ub[HB];
+          float2 fa[HB][4], fb[HB][4];
+#pragma unroll
+          for (int u = 0; u < HB; ++u) {
+            __builtin_memcpy(&ua[u], &xa[u], 16);
+            __builtin_memcpy(&ub[u], &xb[u], 16);
+          }
+          float r[HB];
+          if (NORM) {
+            float ss[HB];
+#pragma unroll
+            for (int u = 0; u < HB; ++u) {
+              // the squares in sum_squares' order: a's eight values, then b's
+              float sa = 0.f, sb = 0.f;
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                fa[u][k] = P2<T>::tof(ua[u].w[k]);
+                fb[u][k] = P2<T>::tof(ub[u].w[k]);
+                sa = __fmaf_rn(fa[u][k].x, fa[u][k].x, sa);
+                sa = __fmaf_rn(fa[u][k].y, fa[u][k].y, sa);
+                sb = __fmaf_rn(fb[u][k].x, fb[u][k].x, sb);
+                sb = __fmaf_rn(fb[u][k].y, fb[u][k].y, sb);
+              }
+              ss[u] = sa + sb;
+            }
+            for (int o = nP >> 1; o > 0; o >>= 1) {
+#pragma unroll
+              for (int u = 0; u < HB; ++u) ss[u] += __shfl_xor_sync(0xffffffffu, ss[u], o);
+            }
+#pragma unroll
+            for (int u = 0; u < HB; ++u) r[u] = 1.0f / sqrtf(ss[u] / (float)H + a.eps);
+          }
+#pragma unroll
+          for (int u = 0; u < HB; ++u) {
+            if (!act[u]) continue;
+            Unit8<T> za = ua[u], zb = ub[u], ya, yb;
+            if (NORM) {
+              Unit8<T> wua, wub;
+              __builtin_memcpy(&wua, &wa, 16);
+              __builtin_memcpy(&wub, &wb, 16);
+              za = norm8p<T>(fa[u], r[u], wua);
+              zb = norm8p<T>(fb[u], r[u], wub);
+            }
+            if (valid) {
+              rotate8p<T, INTER>(za, zb, cf, sf, ya, yb);
+            } else {
+              ya = za;
+              yb = zb;
+            }
+            *reinterpret_cast<Unit8<T>*>(sx + ro[u] + oa) = ya;
+            *reinterpret_cast<Unit8<T>*>(sx + ro[u] + ob) = yb;
+          }
+        } else {
+          float r[HB];
+          if (NORM) {
+            float ss[HB];
+#pragma unroll
+            for (int u = 0; u < HB; ++u) ss[u] = sum_squares<T, V>(xa[u]) + sum_squares<T, V>(xb[u]);
+            for (int o = nP >> 1; o > 0; o >>= 1) {
+#pragma unroll
+              for (int u = 0; u < HB; ++u) ss[u] += __shfl_xor_sync(0xffffffffu, ss[u], o);
+            }
+#pragma unroll
+            for (int u = 0; u < HB; ++u) r[u] = 1.0f / sqrtf(ss[u] / (float)H + a.eps);
+          }
+#pragma unroll
+          for (int u = 0; u < HB; ++u) {
+            if (!act[u]) continue;
+            VT ya, yb;
+            if (NORM) {
+              ya = norm_weight<T, V>(xa[u], r[u], wa);
+              yb = norm_weight<T, V>(xb[u], r[u], wb);
+              if (valid) {
+                const VT za = ya, zb = yb;
+                rotate_unit<T, V, INTER>(za, zb, c, sn, ya, yb);
+              }
+            } else {
+              rotate_unit<T, V, INTER>(xa[u], xb[u], c, sn, ya, yb);
+            }
+            *reinterpret_cast<VT*>(sx + ro[u] + oa) = ya;
+            *reinterpret_cast<VT*>(sx + ro[u] + ob) = yb;
+          }
+        }
+      }
+    }
+    if (q.role != 0 && a.cache) {
+      const int64_t row0 = stage_hdr(s)[1];
+      if (qtile_direct(a, tp, q, row0)) {
+        // rows inside the cache, stored by the threads that own them
+        if (q.role == 1 && q.head0 == 0 && qi == 0 && (row0 < 0 || row0 + q.n > a.max_len))
+          flag_cache_row(p.oor_flag);
+        const int64_t r = row0 + ts;
+        if (has_col && tok_in && r >= 0 && r < a.max_len) {
+          bits* cbase = static_cast<bits*>(q.role == 1 ? a.k_cache : a.v_cache);
+          for (int u = 0; u < hpt; ++u) {
+            const int hh = hq + u * tpc;
+            if (hh >= tp.NG) break;
+            const uint32_t ro = (uint32_t)hh * blk_elems + (uint32_t)ts * (uint32_t)H;
+            bits* dr = cbase + (((int64_t)q.b * a.Nkv + q.head0 + hh) * a.max_len + r) * H;
+            *reinterpret_cast<VT*>(dr + oa) = *reinterpret_cast<const VT*>(sx + ro + oa);
+            *reinterpret_cast<VT*>(dr + ob) = *reinterpret_cast<const VT*>(sx + ro + ob);
+            for (int tu = k; tu < tp.nT; tu += nP) {
+              const int off = p.rd + tu * V;
+              *reinterpret_cast<VT*>(dr + off) = *reinterpret_cast<const VT*>(sx + ro + off);
+            }
+          }
+        }
+      }
+    }
+    fence_async_smem();  // this thread's smem writes, before the TMA store reads them
+    __syncwarp();
+    if (lane == 0) mbar_arrive(done0 + 8 * s);
+  }
+  if (timed_out && lane == 0 && p.oor_flag) atomicOr(p.oor_flag, 2);
+}
+
+}  // namespace rope_gb300

@@ -57,7 +57,7 @@ def _token_mask(B, S, N, H, rd, bad_tok):
 
 
 def _run_case(lib, orc, torch, cuda, dt, packed, cache, inter, rot, implicit, H, offset=0, Nq=8, Nkv=2,
-              B=3, S=37, R=64, L=80, seed=0):
+              B=3, S=37, R=64, L=80, seed=0, variant="auto", kernel="rope_qkv_kernel"):
     rng = np.random.default_rng(seed)
     npdt = {"f16": np.float16, "f32": np.float32, "bf16": BF16}[dt]
     rd = 0 if rot == "full" else H // 2
@@ -90,14 +90,15 @@ def _run_case(lib, orc, torch, cuda, dt, packed, cache, inter, rot, implicit, H,
     dv = lambda a: None if a is None else _dev(a, torch, cuda, offset)  # noqa: E731
     status = torch.zeros(1, dtype=torch.int32, device=cuda)
     kc_d, vc_d = dv(kc0), dv(vc0)
-    qo, ko = lib.rope_apply_qkv(dv(qkv if packed else q), dv(cos), dv(sin),
-                                None if pos is None else _dev(pos, torch, cuda), num_heads=Nq,
-                                kv_num_heads=Nkv, key=None if packed else dv(k),
-                                value=None if (packed or not cache) else dv(v), interleaved=inter,
-                                rotary_embedding_dim=rd, k_cache=kc_d, v_cache=vc_d,
-                                past_seq_lens=_dev(past, torch, cuda) if use_past else None, status=status)
+    with lib.variant(variant):
+        qo, ko = lib.rope_apply_qkv(dv(qkv if packed else q), dv(cos), dv(sin),
+                                    None if pos is None else _dev(pos, torch, cuda), num_heads=Nq,
+                                    kv_num_heads=Nkv, key=None if packed else dv(k),
+                                    value=None if (packed or not cache) else dv(v), interleaved=inter,
+                                    rotary_embedding_dim=rd, k_cache=kc_d, v_cache=vc_d,
+                                    past_seq_lens=_dev(past, torch, cuda) if use_past else None, status=status)
     torch.cuda.synchronize()
-    assert lib.last_kernel() == "rope_qkv_kernel"
+    assert lib.last_kernel() == kernel
     rdw = rd or H
     compare(_host(qo), q_ref, q, 3, Nq, _token_mask(B, S, Nq, H, rdw, bad_tok))
     if not cache:
@@ -126,14 +127,44 @@ def _run_case(lib, orc, torch, cuda, dt, packed, cache, inter, rot, implicit, H,
 
 
 QKV_GRID = list(itertools.product(["f16", "f32", "bf16"], [0, 1], [0, 1], [0, 1], ["full", "partial"], [0, 1]))
+# the SIMT kernel (the automatic choice at these sizes) and the TMA pipeline (forced)
+QKV_KERNELS = {"auto": "rope_qkv_kernel", "tma": "rope_qkv_tma_kernel"}
 
 
+@pytest.mark.parametrize("variant", list(QKV_KERNELS))
 @pytest.mark.parametrize("dt,packed,cache,inter,rot,implicit", QKV_GRID)
-def test_qkv_grid(lib, orc, cuda, dt, packed, cache, inter, rot, implicit):
+def test_qkv_grid(lib, orc, cuda, dt, packed, cache, inter, rot, implicit, variant):
+    """S = 37 leaves a ragged last token tile; past lengths 0, 11 and 50 with an 80-row
+    cache put whole tiles inside the cache, tiles that cross its end and tiles past it."""
     import torch
 
     _run_case(lib, orc, torch, cuda, dt, packed, cache, inter, rot, implicit, H=64,
-              seed=QKV_GRID.index((dt, packed, cache, inter, rot, implicit)))
+              seed=QKV_GRID.index((dt, packed, cache, inter, rot, implicit)), variant=variant,
+              kernel=QKV_KERNELS[variant])
+
+
+# Pipelined kernel geometry: head sizes 32-256 (pair units per row 2-16), one to eight heads
+# per tile (kv heads 1, 2, 8; MHA), one-token tiles (S = 1, decode), tiles of 16 tokens.
+QKV_TMA_SHAPES = [
+    # dt, H, Nq, Nkv, B, S, packed, cache, inter, rot, implicit, R (table rows), L (cache rows)
+    ("f16", 128, 32, 8, 2, 40, 1, 1, 0, "full", 1, 48, 45),
+    ("f16", 128, 32, 8, 3, 1, 1, 1, 0, "full", 1, 40, 45),
+    ("bf16", 128, 16, 8, 2, 33, 0, 1, 1, "partial", 0, 64, 40),
+    ("f16", 256, 8, 1, 2, 21, 1, 1, 0, "full", 0, 64, 28),
+    ("f32", 128, 6, 3, 2, 19, 0, 0, 1, "full", 1, 25, 80),
+    ("f32", 32, 4, 4, 3, 50, 0, 1, 0, "partial", 0, 64, 80),
+    ("f16", 32, 12, 4, 2, 64, 1, 0, 0, "full", 0, 64, 80),
+]
+
+
+@pytest.mark.parametrize("dt,H,Nq,Nkv,B,S,packed,cache,inter,rot,implicit,R,L", QKV_TMA_SHAPES)
+def test_qkv_tma_shapes(lib, orc, cuda, dt, H, Nq, Nkv, B, S, packed, cache, inter, rot, implicit, R, L):
+    """Every case has out-of-range positions and, in cache mode, rows past the cache's end."""
+    import torch
+
+    case = (dt, H, Nq, Nkv, B, S, packed, cache, inter, rot, implicit, R, L)
+    _run_case(lib, orc, torch, cuda, dt, packed, cache, inter, rot, implicit, H=H, Nq=Nq, Nkv=Nkv, B=B, S=S,
+              R=R, L=L, seed=QKV_TMA_SHAPES.index(case), variant="tma", kernel="rope_qkv_tma_kernel")
 
 
 @pytest.mark.parametrize("dt,H,offset", [("f16", 12, 0), ("f32", 6, 0), ("f16", 64, 1), ("f32", 64, 1)])
@@ -181,8 +212,9 @@ def test_qkv_empty_and_rejects(lib, cuda):
                            key=torch.zeros((1, 4, 64), dtype=torch.float16, device=cuda))
 
 
+@pytest.mark.parametrize("variant", ["auto", "simt"])
 @pytest.mark.parametrize("name", [n for n, w in wl.WORKLOADS.items() if w.kind == "qkv"])
-def test_qkv_workload_full_size(lib, orc, cuda, name):
+def test_qkv_workload_full_size(lib, orc, cuda, name, variant):
     """The benchmark's own shapes and launch (packed [Q|K|V], implicit positions past[b] + s,
     cache append). Q is compared whole; the written cache rows are compared with the oracle's
     rotated K and with V bit for bit; every other cache row must still hold its fill."""
@@ -210,10 +242,13 @@ def test_qkv_workload_full_size(lib, orc, cuda, name):
         q_ref, k_ref, _, _, _, _ = orc.rope_qkv(x, cos, sin, pos, num_heads=Nq, kv_num_heads=Nkv, **nkw)
         nkw = {**nkw, "q_norm_weight": _dev(nkw["q_norm_weight"], torch, cuda),
                "k_norm_weight": _dev(nkw["k_norm_weight"], torch, cuda)}
-    qo, ko = lib.rope_apply_qkv(_dev(x, torch, cuda), _dev(cos, torch, cuda), _dev(sin, torch, cuda), None,
-                                num_heads=Nq, kv_num_heads=Nkv, k_cache=kc, v_cache=vc,
-                                past_seq_lens=_dev(past, torch, cuda), status=status, **nkw)
+    with lib.variant(variant):
+        qo, ko = lib.rope_apply_qkv(_dev(x, torch, cuda), _dev(cos, torch, cuda), _dev(sin, torch, cuda), None,
+                                    num_heads=Nq, kv_num_heads=Nkv, k_cache=kc, v_cache=vc,
+                                    past_seq_lens=_dev(past, torch, cuda), status=status, **nkw)
     torch.cuda.synchronize()
+    big = x.nbytes >= 8 << 20   # the automatic choice sends 8 MiB and more to the TMA pipeline
+    assert lib.last_kernel() == ("rope_qkv_tma_kernel" if variant == "auto" and big else "rope_qkv_kernel")
     assert ko is None and int(status.item()) == 0
     none_bad = np.zeros((B, S), dtype=bool)
     bi = torch.arange(B, device=cuda)[:, None].expand(B, S)
@@ -232,6 +267,48 @@ def test_qkv_workload_full_size(lib, orc, cuda, name):
     kc[bi, :, ri] = fill
     vc[bi, :, ri] = fill
     assert bool(torch.all(kc == fill)) and bool(torch.all(vc == fill))
+
+
+@pytest.mark.parametrize("dt", ["f16", "bf16", "f32"])
+@pytest.mark.parametrize("norm", [0, 1])
+@pytest.mark.parametrize("inter", [0, 1])
+def test_qkv_tma_bits_equal_simt(lib, cuda, dt, norm, inter):
+    """The two kernels round every value in the same order (the pipelined one on packed
+    16-bit words and float32 pairs, lane by lane as the scalar code rounds), so their
+    outputs agree bit for bit: Q, and every row of both caches."""
+    import torch
+
+    rng = np.random.default_rng(77 + norm + 2 * inter)
+    npdt = {"f16": np.float16, "f32": np.float32, "bf16": BF16}[dt]
+    B, S, Nq, Nkv, H, R, L = 2, 40, 32, 8, 128, 96, 64
+    Ntot = Nq + 2 * Nkv
+    qkv = cast(rng.standard_normal((B, S, Ntot * H)) * rng.uniform(0.1, 10.0, (B, S, Ntot, 1)).repeat(H, -1)
+               .reshape(B, S, Ntot * H), npdt)
+    theta = rng.uniform(-np.pi, np.pi, (R, H // 2))
+    cos, sin = cast(np.cos(theta), npdt), cast(np.sin(theta), npdt)
+    pos = rng.integers(0, R, (B, S))
+    pos[0, 3], pos[1, 7] = R, -2
+    past = np.array([5, 30], dtype=np.int32)
+    kw = {}
+    if norm:
+        kw = dict(q_norm_weight=_dev(cast(rng.uniform(0.5, 2.0, H), npdt), torch, cuda),
+                  k_norm_weight=_dev(cast(rng.uniform(0.5, 2.0, H), npdt), torch, cuda), epsilon=1e-6)
+    kc0 = cast(rng.standard_normal((B, Nkv, L, H)), npdt)
+    out = {}
+    for variant in ("simt", "tma"):
+        kc, vc = _dev(kc0, torch, cuda), _dev(kc0, torch, cuda)
+        status = torch.zeros(1, dtype=torch.int32, device=cuda)
+        with lib.variant(variant):
+            qo, _ = lib.rope_apply_qkv(_dev(qkv, torch, cuda), _dev(cos, torch, cuda), _dev(sin, torch, cuda),
+                                       _dev(pos, torch, cuda), num_heads=Nq, kv_num_heads=Nkv, interleaved=inter,
+                                       k_cache=kc, v_cache=vc, past_seq_lens=_dev(past, torch, cuda),
+                                       status=status, **kw)
+        torch.cuda.synchronize()
+        assert lib.last_kernel() == QKV_KERNELS.get(variant, "rope_qkv_kernel")
+        out[variant] = [_host(t) for t in (qo, kc, vc)] + [int(status.item())]
+    for a, b in zip(out["simt"][:3], out["tma"][:3]):
+        assert np.array_equal(a.view(np.uint8), b.view(np.uint8))
+    assert out["simt"][3] == out["tma"][3] == (1 | 4)
 
 
 # ---------------------------------------------------------------------------
@@ -291,7 +368,7 @@ def compare_norm(got, ref, N, H, rd, inter):
 
 
 def _run_norm_case(lib, orc, torch, cuda, dt, packed, cache, inter, rot, implicit, H, offset=0, Nq=8, Nkv=2,
-                   B=3, S=37, R=64, L=80, seed=0, eps=1e-6):
+                   B=3, S=37, R=64, L=80, seed=0, eps=1e-6, variant="auto", kernel=None):
     rng = np.random.default_rng(1000 + seed)
     npdt = {"f16": np.float16, "f32": np.float32, "bf16": BF16}[dt]
     rd = 0 if rot == "full" else H // 2
@@ -322,13 +399,17 @@ def _run_norm_case(lib, orc, torch, cuda, dt, packed, cache, inter, rot, implici
     dv = lambda a: None if a is None else _dev(a, torch, cuda, offset)  # noqa: E731
     status = torch.zeros(1, dtype=torch.int32, device=cuda)
     kc_d, vc_d = dv(kc0), dv(vc0)
-    qo, ko = lib.rope_apply_qkv(dv(qkv if packed else q), dv(cos), dv(sin),
-                                None if pos is None else _dev(pos, torch, cuda), num_heads=Nq, kv_num_heads=Nkv,
-                                key=None if packed else dv(k), value=None if (packed or not cache) else dv(v),
-                                interleaved=inter, rotary_embedding_dim=rd, k_cache=kc_d, v_cache=vc_d,
-                                past_seq_lens=_dev(past, torch, cuda) if use_past else None, status=status,
-                                q_norm_weight=dv(wq), k_norm_weight=dv(wk), epsilon=eps)
+    with lib.variant(variant):
+        qo, ko = lib.rope_apply_qkv(dv(qkv if packed else q), dv(cos), dv(sin),
+                                    None if pos is None else _dev(pos, torch, cuda), num_heads=Nq,
+                                    kv_num_heads=Nkv, key=None if packed else dv(k),
+                                    value=None if (packed or not cache) else dv(v), interleaved=inter,
+                                    rotary_embedding_dim=rd, k_cache=kc_d, v_cache=vc_d,
+                                    past_seq_lens=_dev(past, torch, cuda) if use_past else None, status=status,
+                                    q_norm_weight=dv(wq), k_norm_weight=dv(wk), epsilon=eps)
     torch.cuda.synchronize()
+    if kernel is not None:
+        assert lib.last_kernel() == kernel
     compare_norm(_host(qo), q_ref, Nq, H, rdw, inter)
     if not cache:
         compare_norm(_host(ko), k_ref, Nkv, H, rdw, inter)
@@ -350,13 +431,32 @@ def _run_norm_case(lib, orc, torch, cuda, dt, packed, cache, inter, rot, implici
 NORM_GRID = list(itertools.product(["f16", "f32", "bf16"], [0, 1], [0, 1], ["full", "partial"], [(0, 0), (1, 1)]))
 
 
+@pytest.mark.parametrize("variant", list(QKV_KERNELS))
 @pytest.mark.parametrize("dt,cache,inter,rot,pk_impl", NORM_GRID)
-def test_qkv_rmsnorm_grid(lib, orc, cuda, dt, cache, inter, rot, pk_impl):
+def test_qkv_rmsnorm_grid(lib, orc, cuda, dt, cache, inter, rot, pk_impl, variant):
+    """Forced onto the TMA pipeline, full rotation takes it; partial rotation with the
+    norm (the tail is normalised too) stays on the SIMT kernel."""
     import torch
 
     packed, implicit = pk_impl
+    kernel = QKV_KERNELS[variant] if rot == "full" else "rope_qkv_kernel"
     _run_norm_case(lib, orc, torch, cuda, dt, packed, cache, inter, rot, implicit, H=64,
-                   seed=NORM_GRID.index((dt, cache, inter, rot, pk_impl)))
+                   seed=NORM_GRID.index((dt, cache, inter, rot, pk_impl)), variant=variant, kernel=kernel)
+
+
+@pytest.mark.parametrize("dt,H,Nq,Nkv,B,S,packed,cache,inter,implicit", [
+    ("f16", 128, 32, 8, 2, 40, 1, 1, 0, 1),
+    ("bf16", 128, 16, 8, 3, 1, 1, 1, 1, 1),
+    ("f16", 256, 8, 1, 2, 21, 0, 1, 0, 0),
+    ("f32", 128, 6, 3, 2, 19, 0, 0, 1, 0),
+    ("f16", 32, 12, 4, 2, 64, 1, 0, 0, 0),
+])
+def test_qkv_rmsnorm_tma_shapes(lib, orc, cuda, dt, H, Nq, Nkv, B, S, packed, cache, inter, implicit):
+    """The pipelined norm: lane groups of 2 to 16 units, one to eight heads per tile."""
+    import torch
+
+    _run_norm_case(lib, orc, torch, cuda, dt, packed, cache, inter, "full", implicit, H=H, Nq=Nq, Nkv=Nkv, B=B,
+                   S=S, L=45, seed=H + S, variant="tma", kernel="rope_qkv_tma_kernel")
 
 
 @pytest.mark.parametrize("dt,H,offset,rot", [("f16", 128, 0, "full"), ("f16", 256, 0, "full"),
