@@ -44,7 +44,8 @@ KERNEL_SOURCES = {
     "rope_tma_kernel": ["rope_kernels.cuh", "rope_tma.cuh", "k_tma.cu"],
     "rope_fused_kernel": ["rope_kernels.cuh", "k_fused.cu"],
     "rope_qkv_kernel": ["rope_kernels.cuh", "rope_qkv.cuh", "k_qkv.cu"],
-    "rope_qkv_tma_kernel": ["rope_kernels.cuh", "rope_tma.cuh", "rope_qkv.cuh", "rope_qkv_tma.cuh", "k_qkv_tma.cu"],
+    "rope_qkv_tma_kernel": ["rope_kernels.cuh", "rope_tma.cuh", "rope_qkv.cuh", "rope_packed.cuh", "rope_qkv_tma.cuh",
+                            "k_qkv_tma.cu"],
 }
 
 

@@ -512,6 +512,8 @@ rope_status plan_qkv_tma(rope_dtype dt, const Geom& g, int es, const QKVParams& 
   tp.Gk = (int32_t)(a.Nkv / NG);
   tp.G = tp.Gq + tp.Gk + (a.cache ? tp.Gk : 0);
   tp.s_tiles = (int32_t)((g.S + TS - 1) / TS);
+  if (g.B * (int64_t)tp.s_tiles >= INT32_MAX) return ROPE_ERR_UNSUPPORTED;
+  tp.nt_tiles = (int32_t)(g.B * tp.s_tiles);
   tp.nT = (int32_t)((g.H - g.rd) / V);
   tp.ntiles = g.B * (int64_t)tp.s_tiles * tp.G;
   if (tp.ntiles >= INT32_MAX) return ROPE_ERR_UNSUPPORTED;

@@ -32,6 +32,7 @@
 //    QK-Norm: RMSNorm on Q and K before RoPE).
 #pragma once
 
+#include "rope_packed.cuh"
 #include "rope_qkv.cuh"
 #include "rope_tma.cuh"
 
@@ -47,6 +48,7 @@ struct QTParams {
   int32_t TS, NG, K;      // tokens per tile, heads per tile, stages
   int32_t G, Gq, Gk;      // head groups per token tile: Gq of Q, Gk of K, then Gk of V (cache mode)
   int32_t s_tiles;        // ceil(S / TS)
+  int32_t nt_tiles;       // token tiles: B * s_tiles
   int32_t nT;             // tail units (H - rd) / V
   int64_t ntiles;
   uint32_t blk_bytes;     // cache tiles: one head's TS x H block in a stage (a multiple of 128 bytes)
@@ -75,13 +77,18 @@ struct QTile {
   int32_t b;
 };
 
+// Tiles are numbered head group by head group (all token tiles of Q group 0,
+// then Q group 1, ..., the K groups, the V groups), so the round-robin
+// schedule deals every CTA the same mix of Q, K and V tiles -- which differ in
+// cost: V tiles gather and compute nothing -- and the tiles left over after
+// the last full round are the cheap V tiles.
 __device__ __forceinline__ QTile qtile_of(const KParams& p, const QTParams& tp, int64_t t64) {
   QTile q;
   const uint32_t t = (uint32_t)t64;  // tile counts stay below 2^31
-  const uint32_t g = t % (uint32_t)tp.G;
-  const uint32_t rest = t / (uint32_t)tp.G;
-  const uint32_t st = rest % (uint32_t)tp.s_tiles;
-  q.b = (int32_t)(rest / (uint32_t)tp.s_tiles);
+  const uint32_t g = t / (uint32_t)tp.nt_tiles;
+  const uint32_t tt = t - g * (uint32_t)tp.nt_tiles;
+  const uint32_t st = tt % (uint32_t)tp.s_tiles;
+  q.b = (int32_t)(tt / (uint32_t)tp.s_tiles);
   q.s0 = (int32_t)(st * (uint32_t)tp.TS);
   const int64_t left = p.S - q.s0;
   q.n = (int)(left < tp.TS ? left : tp.TS);
@@ -98,11 +105,6 @@ __device__ __forceinline__ QTile qtile_of(const KParams& p, const QTParams& tp, 
   return q;
 }
 
-// First cache row of a K or V tile in cache mode.
-__device__ __forceinline__ int64_t qtile_row0(const QKVParams& a, const QTile& q) {
-  return (a.past ? (int64_t)__ldg(a.past + q.b) : 0) + q.s0;
-}
-
 // Q tiles and (without caches) K tiles are one NG-head box in the stage,
 // laid out [TS][NG][H] like the tensor; cache tiles are NG per-head blocks of
 // TS x H, the rows of the cache.
@@ -115,67 +117,6 @@ __device__ __forceinline__ bool qtile_wide(const QKVParams& a, const QTile& q) {
 __device__ __forceinline__ bool qtile_direct(const QKVParams& a, const QTParams& tp, const QTile& q,
                                              int64_t row0) {
   return q.role != 0 && a.cache && (q.n < tp.TS || row0 < 0 || row0 + tp.TS > a.max_len);
-}
-
-// ---------------------------------------------------------------------------
-// Packed arithmetic for 16-bit storage (float16, bfloat16): two values per
-// 32-bit word, float32x2 operations (sm_100 and later). Each lane of a packed
-// operation rounds exactly as the scalar operation does, so every result has
-// the bits of rotate() and norm_weight() in rope_kernels.cuh / rope_qkv.cuh.
-// ---------------------------------------------------------------------------
-template <class T>
-struct P2;
-template <>
-struct P2<__half> {
-  using w2 = __half2;
-  static __device__ __forceinline__ float2 tof(w2 v) { return __half22float2(v); }
-  static __device__ __forceinline__ w2 fromf(float2 f) { return __float22half2_rn(f); }
-};
-template <>
-struct P2<__nv_bfloat16> {
-  using w2 = __nv_bfloat162;
-  static __device__ __forceinline__ float2 tof(w2 v) { return __bfloat1622float2(v); }
-  static __device__ __forceinline__ w2 fromf(float2 f) { return __float22bfloat162_rn(f); }
-};
-
-template <class T>
-struct Unit8 {  // one 16-byte unit of 8 values as 4 packed words
-  typename P2<T>::w2 w[4];
-};
-
-// Rotation of a unit pair (half split: pair j = (a[j], b[j]); interleaved:
-// pair j = elements 2j, 2j+1 of a||b) with unpacked coefficients cf/sf
-// (cf[k] = coefficients 2k, 2k+1): y0 = x0*c - x1*s, y1 = x1*c + x0*s, as
-// rotate() forms them (product, then fused multiply-add; -(x1*s) is x1*(-s)).
-template <class T, bool INTER>
-__device__ __forceinline__ void rotate8p(const Unit8<T>& a, const Unit8<T>& b, const float2 (&cf)[4],
-                                         const float2 (&sf)[4], Unit8<T>& ya, Unit8<T>& yb) {
-  using P = P2<T>;
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const float2 ns = make_float2(-sf[k].x, -sf[k].y);
-    if (!INTER) {
-      const float2 x0 = P::tof(a.w[k]), x1 = P::tof(b.w[k]);
-      ya.w[k] = P::fromf(__ffma2_rn(x0, cf[k], __fmul2_rn(x1, ns)));
-      yb.w[k] = P::fromf(__ffma2_rn(x1, cf[k], __fmul2_rn(x0, sf[k])));
-    } else {
-      // words 2k and 2k+1 of a||b hold pairs 2k and 2k+1
-      const float2 f0 = P::tof(k < 2 ? a.w[2 * k] : b.w[2 * k - 4]);
-      const float2 f1 = P::tof(k < 2 ? a.w[2 * k + 1] : b.w[2 * k - 3]);
-      const float2 x0 = make_float2(f0.x, f1.x), x1 = make_float2(f0.y, f1.y);
-      const float2 y0 = __ffma2_rn(x0, cf[k], __fmul2_rn(x1, ns));
-      const float2 y1 = __ffma2_rn(x1, cf[k], __fmul2_rn(x0, sf[k]));
-      const typename P::w2 p0 = P::fromf(make_float2(y0.x, y1.x));
-      const typename P::w2 p1 = P::fromf(make_float2(y0.y, y1.y));
-      if (k < 2) {
-        ya.w[2 * k] = p0;
-        ya.w[2 * k + 1] = p1;
-      } else {
-        yb.w[2 * k - 4] = p0;
-        yb.w[2 * k - 3] = p1;
-      }
-    }
-  }
 }
 
 // z = T(w * T(x * r)) on a unit whose values fx are already unpacked: the
@@ -272,11 +213,11 @@ __global__ void __launch_bounds__(kTmaThreads, ROPE_TMA_MIN_CTAS)
       // store is still reading its stage
       int64_t t_st = tile_index(0);
       QTile q_st{};
-      int64_t row_st = 0;
+      int64_t past_st = 0;  // raw past[b]: the load is consumed only at the store
       auto prep = [&](int64_t t) {
         if (t < tp.ntiles) {
           q_st = qtile_of(p, tp, t);
-          row_st = (q_st.role != 0 && a.cache) ? qtile_row0(a, q_st) : 0;
+          past_st = (q_st.role != 0 && a.cache && a.past) ? (int64_t)__ldg(a.past + q_st.b) : 0;
         }
       };
       prep(t_st);
@@ -287,6 +228,7 @@ __global__ void __launch_bounds__(kTmaThreads, ROPE_TMA_MIN_CTAS)
           break;
         }
         if (t_st >= tp.ntiles) break;  // sentinel
+        const int64_t row_st = past_st + q_st.s0;
         if (!qtile_direct(a, tp, q_st, row_st)) {
           const uint32_t src = smem_addr(stage0 + (size_t)s * tp.stage_bytes);
           const bool to_cache = !qtile_wide(a, q_st);
@@ -330,10 +272,41 @@ __global__ void __launch_bounds__(kTmaThreads, ROPE_TMA_MIN_CTAS)
     const bits* cosb = static_cast<const bits*>(p.cos);
     const bits* sinb = static_cast<const bits*>(p.sin);
     bool timed_out = false;
+    // Piece c (16 bytes) of a tile's coefficient block goes to lane c % 32:
+    // token c / per_tok, cos or sin, 16-byte piece within the row. Decoded once.
     const int ch = h * (int)sizeof(bits) / 16;  // 16-byte pieces per cos (or sin) row
     const int per_tok = 2 * ch;
     const int pieces = tp.TS * per_tok;
     const int rounds = (pieces + 31) / 32;  // the same for every lane: the shuffles below are warp-wide
+    int g_lt[kMaxGather], g_piece[kMaxGather];
+    bool g_mine[kMaxGather], g_sin[kMaxGather];
+#pragma unroll
+    for (int g = 0; g < kMaxGather; ++g) {
+      const int c = lane + 32 * g;
+      g_mine[g] = c < pieces;
+      g_lt[g] = g_mine[g] ? c / per_tok : 0;
+      const int rem = c - g_lt[g] * per_tok;
+      g_sin[g] = rem >= ch;
+      g_piece[g] = g_sin[g] ? rem - ch : rem;
+    }
+    // The schedule is static, so what a tile needs from global memory -- its
+    // positions, or the past length its positions and cache rows start from --
+    // is loaded one tile ahead: under a saturated memory system even these
+    // L2 hits take microseconds, and the gather of the tile waits on none.
+    struct Pre {
+      int64_t pos;   // explicit position of token `lane`
+      int64_t past;  // past[b]
+    };
+    auto prefetch = [&](int64_t t) -> Pre {
+      Pre r{0, 0};
+      if (t < tp.ntiles) {
+        const QTile q = qtile_of(p, tp, t);
+        if (a.past && (IMPLICIT || (q.role != 0 && a.cache))) r.past = (int64_t)__ldg(a.past + q.b);
+        if (!IMPLICIT && q.role != 2 && lane < q.n) r.pos = __ldg(p.pos + (int64_t)q.b * p.S + q.s0 + lane);
+      }
+      return r;
+    };
+    Pre cur = prefetch(blockIdx.x);
     for (int64_t j = 0;; ++j) {
       const int s = (int)(j % tp.K);
       if (!__all_sync(0xffffffffu, mbar_wait(issued0 + 8 * s, (uint32_t)((j / tp.K) & 1)))) {
@@ -345,16 +318,15 @@ __global__ void __launch_bounds__(kTmaThreads, ROPE_TMA_MIN_CTAS)
         cp_async_arrive(full0 + 8 * s);
         break;
       }
+      const Pre nxt = prefetch(t + gridDim.x);  // this CTA's next tile
       const QTile q = qtile_of(p, tp, t);
       unsigned char* st = stage0 + (size_t)s * tp.stage_bytes;
-      if (q.role != 0 && a.cache && lane == 0) stage_hdr(s)[1] = qtile_row0(a, q);
+      if (q.role != 0 && a.cache && lane == 0) stage_hdr(s)[1] = cur.past + q.s0;
       if (q.role != 2) {
-        const int64_t past_b = (IMPLICIT && a.past) ? (int64_t)__ldg(a.past + q.b) : 0;
         int64_t pp = -1;
         uint32_t flag = 0;
         if (lane < q.n) {
-          const int64_t sq = (int64_t)q.s0 + lane;
-          pp = IMPLICIT ? past_b + sq : __ldg(p.pos + (int64_t)q.b * p.S + sq);
+          pp = IMPLICIT ? cur.past + q.s0 + lane : cur.pos;
           flag = (uint64_t)pp < (uint64_t)p.cache_rows ? 1u : 0u;
           if (!flag && q.role == 0 && q.head0 == 0 && p.oor_flag) atomicOr(p.oor_flag, 1);
         }
@@ -363,22 +335,17 @@ __global__ void __launch_bounds__(kTmaThreads, ROPE_TMA_MIN_CTAS)
 #pragma unroll
         for (int g = 0; g < kMaxGather; ++g) {
           if (g >= rounds) break;
-          const int c = lane + 32 * g;
-          const bool mine = c < pieces;
-          const int lt = mine ? c / per_tok : 0;
-          const int rem = c - lt * per_tok;
-          const bool is_sin = rem >= ch;
-          const int piece = is_sin ? rem - ch : rem;
-          // token lt's position lives in lane lt
-          const int64_t row = __shfl_sync(0xffffffffu, pp, lt);
-          const uint32_t ok = __shfl_sync(0xffffffffu, flag, lt);
-          if (mine && ok)
-            cp_async16(coef_addr + 16u * (uint32_t)c,
-                       reinterpret_cast<const uint4*>((is_sin ? sinb : cosb) + row * h) + piece);
+          // token g_lt's position lives in lane g_lt
+          const int64_t row = __shfl_sync(0xffffffffu, pp, g_lt[g]);
+          const uint32_t ok = __shfl_sync(0xffffffffu, flag, g_lt[g]);
+          if (g_mine[g] && ok)
+            cp_async16(coef_addr + 16u * (uint32_t)(lane + 32 * g),
+                       reinterpret_cast<const uint4*>((g_sin[g] ? sinb : cosb) + row * h) + g_piece[g]);
         }
       }
       __syncwarp();  // flags and the header precede the lanes' (releasing) arrivals
       cp_async_arrive(full0 + 8 * s);
+      cur = nxt;
     }
     asm volatile("cp.async.wait_all;" ::: "memory");
     if (timed_out && lane == 0 && p.oor_flag) atomicOr(p.oor_flag, 2);
