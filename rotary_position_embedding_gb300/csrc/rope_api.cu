@@ -492,9 +492,10 @@ rope_status plan_qkv_tma(rope_dtype dt, const Geom& g, int es, const QKVParams& 
   memset(&tp, 0, sizeof(tp));
   memset(&T->maps, 0, sizeof(T->maps));
   // tokens: each gather lane holds one token's position, and a tile's cos/sin
-  // pieces fit the gather warp's kMaxGather copies per lane
+  // rows fit the gather warp's kMaxGather bulk copies per lane (kMaxGather
+  // bounds rows here, 16-byte pieces in the RoPE pipeline)
   int64_t TS = g.S < ROPE_QKV_TMA_MAX_TS ? g.S : ROPE_QKV_TMA_MAX_TS;
-  while (TS > 1 && TS * 2 * nP > 32 * kMaxGather) --TS;
+  while (TS > 1 && TS * 2 > 32 * kMaxGather) --TS;
   if (TS < 1 || TS > 32 || TS * nP > kTmaConsumers) return ROPE_ERR_UNSUPPORTED;
   const int64_t tpc = kTmaConsumers / (TS * nP);
   // heads: a divisor of Nkv (so of Nq) that each column's threads cover with

@@ -12,8 +12,8 @@
 // rows of one head of a (B, Nkv, max_len, H) cache.
 //   copy warp  (lane 0) starts a tile's tensor copies into a free stage and
 //              writes the finished tile back with tensor stores;
-//   gather warp loads the tile's positions and gathers its cos/sin rows
-//              (Q and K tiles) with asynchronous 16-byte copies;
+//   gather warp loads the tile's positions (a tile ahead) and gathers its
+//              cos/sin rows (Q and K tiles), one bulk copy per row;
 //   consumers  normalise (RMSNorm) and rotate Q and K tiles in place; V tiles
 //              pass through untouched.
 // A cache tile that is ragged (the batch's last, partial token tile) or whose
@@ -37,6 +37,18 @@
 #include "rope_tma.cuh"
 
 namespace rope_gb300 {
+
+// Bulk copy global -> shared on the TMA unit (no tensor map): `bytes` (a
+// multiple of 16, both addresses 16-byte aligned) completing as transaction
+// bytes on the mbarrier `bar`. The gather warp copies each cos/sin row of a
+// tile this way: one instruction per row instead of one per 16 bytes (the
+// RoPE pipeline keeps 16-byte copies, whose small rows would otherwise queue
+// behind its tile copies on the TMA unit; measured slower there).
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
 
 // Heads a consumer thread loads and reduces together.
 #ifndef ROPE_QKV_TMA_HEAD_BATCH
@@ -272,23 +284,11 @@ __global__ void __launch_bounds__(kTmaThreads, ROPE_TMA_MIN_CTAS)
     const bits* cosb = static_cast<const bits*>(p.cos);
     const bits* sinb = static_cast<const bits*>(p.sin);
     bool timed_out = false;
-    // Piece c (16 bytes) of a tile's coefficient block goes to lane c % 32:
-    // token c / per_tok, cos or sin, 16-byte piece within the row. Decoded once.
-    const int ch = h * (int)sizeof(bits) / 16;  // 16-byte pieces per cos (or sin) row
-    const int per_tok = 2 * ch;
-    const int pieces = tp.TS * per_tok;
-    const int rounds = (pieces + 31) / 32;  // the same for every lane: the shuffles below are warp-wide
-    int g_lt[kMaxGather], g_piece[kMaxGather];
-    bool g_mine[kMaxGather], g_sin[kMaxGather];
-#pragma unroll
-    for (int g = 0; g < kMaxGather; ++g) {
-      const int c = lane + 32 * g;
-      g_mine[g] = c < pieces;
-      g_lt[g] = g_mine[g] ? c / per_tok : 0;
-      const int rem = c - g_lt[g] * per_tok;
-      g_sin[g] = rem >= ch;
-      g_piece[g] = g_sin[g] ? rem - ch : rem;
-    }
+    // Row r of a tile's coefficient block (the cos or sin row of token r / 2,
+    // row_bytes at byte r*row_bytes) goes to lane r % 32 as one bulk copy.
+    const uint32_t row_bytes = (uint32_t)h * (uint32_t)sizeof(bits);
+    const int rows = tp.TS * 2;
+    const int rounds = (rows + 31) / 32;  // the same for every lane: the shuffles below are warp-wide
     // The schedule is static, so what a tile needs from global memory -- its
     // positions, or the past length its positions and cache rows start from --
     // is loaded one tile ahead: under a saturated memory system even these
@@ -332,19 +332,33 @@ __global__ void __launch_bounds__(kTmaThreads, ROPE_TMA_MIN_CTAS)
         }
         if (lane < tp.TS) reinterpret_cast<uint32_t*>(st + tp.flag_off)[lane] = flag;
         const uint32_t coef_addr = smem_addr(st) + tp.coef_off;
+        const bits* src[kMaxGather];
+        uint32_t bytes = 0, go = 0;
 #pragma unroll
         for (int g = 0; g < kMaxGather; ++g) {
           if (g >= rounds) break;
-          // token g_lt's position lives in lane g_lt
-          const int64_t row = __shfl_sync(0xffffffffu, pp, g_lt[g]);
-          const uint32_t ok = __shfl_sync(0xffffffffu, flag, g_lt[g]);
-          if (g_mine[g] && ok)
-            cp_async16(coef_addr + 16u * (uint32_t)(lane + 32 * g),
-                       reinterpret_cast<const uint4*>((g_sin[g] ? sinb : cosb) + row * h) + g_piece[g]);
+          const int r = lane + 32 * g;
+          const int lt = r < rows ? r >> 1 : 0;
+          // token lt's position lives in lane lt
+          const int64_t row = __shfl_sync(0xffffffffu, pp, lt);
+          const uint32_t ok = __shfl_sync(0xffffffffu, flag, lt);
+          src[g] = ((r & 1) ? sinb : cosb) + row * h;
+          if (r < rows && ok) {
+            bytes += row_bytes;
+            go |= 1u << g;
+          }
         }
+        __syncwarp();  // flags and the header precede the lanes' (releasing) arrivals
+        // this lane's arrival carries the bytes its copies will complete
+        mbar_arrive_expect_tx(full0 + 8 * s, bytes);
+#pragma unroll
+        for (int g = 0; g < kMaxGather; ++g)
+          if ((go >> g) & 1u) bulk_g2s(coef_addr + row_bytes * (uint32_t)(lane + 32 * g), src[g], row_bytes,
+                                       full0 + 8 * s);
+      } else {
+        __syncwarp();  // the header precedes the lanes' (releasing) arrivals
+        mbar_arrive(full0 + 8 * s);
       }
-      __syncwarp();  // flags and the header precede the lanes' (releasing) arrivals
-      cp_async_arrive(full0 + 8 * s);
       cur = nxt;
     }
     asm volatile("cp.async.wait_all;" ::: "memory");
