@@ -352,6 +352,13 @@ class Step:
 
 
 DTYPE_CODES = {"float32": 0, "float16": 1, "bfloat16": 2}
+POSITION_RECIPES = {
+    "none": "none: a (B, S, rd/2) table, row (b, s)",
+    "offset": "s + U[0,4096) per batch",
+    "uniform": "U[0, cache rows)",
+    "mrope": "t/h/w: text spans equal, 32x32 image grids per frame, per-batch offset; 1 % of ids past the table",
+    "past": "implicit: past[b] + s, past[b] ~ U[0, max past]",
+}
 
 
 def torch_dtype(torch, name):
@@ -515,7 +522,7 @@ def gpu_arm(args, rank, world, local_rank):
             "config": {
                 "workload": w.name, "shape": list(w.shape), "num_heads": w.num_heads,
                 "head_size": w.head_size, "rotary_dim": w.rotary_dim, "interleaved": w.interleaved,
-                "cache_rows": w.cache_rows, "positions": "s + U[0,4096) per batch",
+                "cache_rows": w.cache_rows, "positions": POSITION_RECIPES[w.positions],
                 "algorithmic_bytes_per_step": nbytes,
                 "l2": f"inputs rotate over {len(step.xs)} X/Y buffer sets "
                       f"({len(step.xs) * 2 * w.numel * 2 / 2**20:.0f} MiB) > 129 MiB L2; no flush kernel",
