@@ -359,6 +359,12 @@ rope_status encode_x_map(CUtensorMap* m, rope_dtype dt, const Geom& g, int rank,
   return ROPE_OK;
 }
 
+// Persistent grid of the pipelined kernels: one CTA per resident slot (at
+// most one per tile). Measured: shrinking the grid so that every CTA takes
+// the same number of round-robin tiles gained nothing on M-RoPE or rank 4
+// and cost the Q/K workloads 1-3 us.
+int64_t pipeline_grid(int64_t slots, int64_t ntiles) { return slots < ntiles ? slots : ntiles; }
+
 // Fills kp's geometry and the TMA launch; ROPE_ERR_UNSUPPORTED (no message)
 // when the shape does not fit the pipeline, in which case the caller falls
 // back to the register-path kernel.
@@ -431,8 +437,7 @@ rope_status plan_tma(rope_dtype dt, const Geom& g, int es, int rank, int slots, 
   int sms = 0, per_sm = 0;
   rope_status st = device_facts(fn, kTmaThreads, smem, &sms, &per_sm);
   if (st != ROPE_OK) return st;
-  int64_t gx = (int64_t)sms * per_sm;
-  if (gx > tp.ntiles) gx = tp.ntiles;
+  const int64_t gx = pipeline_grid((int64_t)sms * per_sm, tp.ntiles);
   T->L.grid = dim3((unsigned)gx, 1, 1);
   T->L.block = dim3(kTmaThreads, 1, 1);
   T->L.smem = smem;
@@ -540,8 +545,7 @@ rope_status plan_qkv_tma(rope_dtype dt, const Geom& g, int es, const QKVParams& 
   int sms = 0, per_sm = 0;
   rope_status st = device_facts(fn, kTmaThreads, smem, &sms, &per_sm);
   if (st != ROPE_OK) return st;
-  int64_t gx = (int64_t)sms * per_sm;
-  if (gx > tp.ntiles) gx = tp.ntiles;
+  const int64_t gx = pipeline_grid((int64_t)sms * per_sm, tp.ntiles);
   T->L.grid = dim3((unsigned)gx, 1, 1);
   T->L.block = dim3(kTmaThreads, 1, 1);
   T->L.smem = smem;
