@@ -42,7 +42,7 @@ METRIC = "RoPE achieved HBM GB/s and Gelem/s, fp16, as % of GB300 HBM roofline"
 KERNEL_SOURCES = {
     "rope_rows_kernel": ["rope_kernels.cuh", "k_rope.cu", "k_mrope.cu"],
     "rope_tma_kernel": ["rope_kernels.cuh", "rope_tma.cuh", "k_tma.cu"],
-    "rope_fused_kernel": ["rope_kernels.cuh", "k_fused.cu"],
+    "rope_fused_kernel": ["rope_kernels.cuh", "rope_fused.cuh", "k_fused.cu"],
     "rope_qkv_kernel": ["rope_kernels.cuh", "rope_qkv.cuh", "k_qkv.cu"],
     "rope_qkv_tma_kernel": ["rope_kernels.cuh", "rope_tma.cuh", "rope_qkv.cuh", "rope_packed.cuh", "rope_qkv_tma.cuh",
                             "k_qkv_tma.cu"],

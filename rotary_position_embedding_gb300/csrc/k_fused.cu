@@ -2,7 +2,7 @@
 // build (the onnxruntime Qwen3 on-the-fly RoPE fusion pull request: Modeling
 // Code Alignment Check, Medium Issues 4; "com.microsoft.MRotaryEmbedding"
 // README for the three position streams).
-#include "rope_kernels.cuh"
+#include "rope_fused.cuh"
 
 namespace rope_gb300 {
 
