@@ -57,7 +57,7 @@ def _token_mask(B, S, N, H, rd, bad_tok):
 
 
 def _run_case(lib, orc, torch, cuda, dt, packed, cache, inter, rot, implicit, H, offset=0, Nq=8, Nkv=2,
-              B=3, S=37, R=64, L=80, seed=0, variant="auto", kernel="rope_qkv_kernel"):
+              B=3, S=37, R=64, L=80, seed=0, variant="auto", kernel="rope_qkv_kernel", past=None):
     rng = np.random.default_rng(seed)
     npdt = {"f16": np.float16, "f32": np.float32, "bf16": BF16}[dt]
     rd = 0 if rot == "full" else H // 2
@@ -68,7 +68,7 @@ def _run_case(lib, orc, torch, cuda, dt, packed, cache, inter, rot, implicit, H,
         _heads(qkv, B, S, Nq + Nkv, Ntot, Ntot, H)
     theta = rng.uniform(-np.pi, np.pi, (R, h))
     cos, sin = cast(np.cos(theta), npdt), cast(np.sin(theta), npdt)
-    past = np.array([0, 11, 50], dtype=np.int32)[:B]
+    past = np.array([0, 11, 50], dtype=np.int32)[:B] if past is None else np.asarray(past, dtype=np.int32)
     if implicit:
         pos = None
         eff = past[:, None].astype(np.int64) + np.arange(S)[None, :]
@@ -115,7 +115,7 @@ def _run_case(lib, orc, torch, cuda, dt, packed, cache, inter, rot, implicit, H,
         for b in range(B):
             for s in range(S):
                 row = past[b] + s
-                if row < L:
+                if 0 <= row < L:
                     src[b, :, row] = k4[b, s]
                     mask[b, row] = False
                     mask[b, row, :, rdw:] = True
@@ -269,6 +269,32 @@ def test_qkv_workload_full_size(lib, orc, cuda, name, variant):
     assert bool(torch.all(kc == fill)) and bool(torch.all(vc == fill))
 
 
+@pytest.mark.parametrize("variant", list(QKV_KERNELS))
+@pytest.mark.parametrize("implicit", [0, 1])
+def test_qkv_negative_past_lengths(lib, orc, cuda, variant, implicit):
+    """A negative past length puts a batch's first cache rows below 0: those rows are
+    skipped (status bit 2) -- on the pipelined kernel a tile starting below row 0 is stored
+    row by row, never by a tensor store at a negative row -- and with implicit positions
+    their positions are negative, so those tokens are copied through."""
+    import torch
+
+    _run_case(lib, orc, torch, cuda, "f16", 1, 1, 0, "full", implicit, H=128, Nq=16, Nkv=8, B=2, S=40, R=64,
+              L=48, seed=5 + implicit, variant=variant, kernel=QKV_KERNELS[variant], past=[-21, 3])
+
+
+@pytest.mark.parametrize("dt,H", [("f16", 96), ("f16", 80), ("bf16", 96), ("f32", 48)])
+@pytest.mark.parametrize("cache", [0, 1])
+def test_qkv_tma_unit_counts(lib, orc, cuda, dt, H, cache):
+    """Rows of 6, 5 and 6 pair units (not a power of two): the pipelined kernel without the
+    norm takes them; with the norm they stay on the SIMT kernel."""
+    import torch
+
+    _run_case(lib, orc, torch, cuda, dt, 1, cache, 0, "full", 0, H=H, Nq=12, Nkv=4, B=2, S=33, L=40,
+              seed=H + cache, variant="tma", kernel="rope_qkv_tma_kernel")
+    _run_norm_case(lib, orc, torch, cuda, dt, 1, cache, 0, "full", 0, H=H, Nq=12, Nkv=4, B=2, S=33, L=40,
+                   seed=H + cache, variant="tma", kernel="rope_qkv_kernel")
+
+
 @pytest.mark.parametrize("dt", ["f16", "bf16", "f32"])
 @pytest.mark.parametrize("norm", [0, 1])
 @pytest.mark.parametrize("inter", [0, 1])
@@ -419,7 +445,7 @@ def _run_norm_case(lib, orc, torch, cuda, dt, packed, cache, inter, rot, implici
         written = np.zeros((B, L), dtype=bool)
         for b in range(B):
             rows = past[b] + np.arange(S)
-            written[b, rows[rows < L]] = True
+            written[b, rows[(rows >= 0) & (rows < L)]] = True
         # untouched K rows keep their bits; written rows within the norm bound
         assert np.array_equal(kc_g.transpose(0, 2, 1, 3)[~written].view(np.uint8),
                               kc0.transpose(0, 2, 1, 3)[~written].view(np.uint8))
