@@ -384,35 +384,41 @@ def n_buffer_sets(w):
     return max(2, math.ceil(4 * L2_BYTES / per_set))
 
 
-def time_steps(torch, step, steps, stream_handle, fused=False, sample_every=0):
-    """Time `steps` launches (rotating buffer sets) with CUDA events on the launching stream.
-
-    One event pair brackets the whole run (the throughput). With
-    `sample_every` > 0, every `sample_every`-th launch is also bracketed by its
-    own pair (an isolated launch: the pair stops the next launch from starting
-    its prologue while this one drains, and adds the event round trip).
-    Unbracketed launches follow each other directly, as in a real stream.
-    """
+def time_steps(torch, step, steps, stream_handle, fused=False):
+    """Time `steps` back-to-back launches (rotating buffer sets) with one CUDA
+    event pair on the launching stream around all of them."""
     n_sets = len(step.xs)
-    sampled = list(range(0, steps, sample_every)) if sample_every > 0 else []
-    starts = {k: torch.cuda.Event(enable_timing=True) for k in sampled}
-    ends = {k: torch.cuda.Event(enable_timing=True) for k in sampled}
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
     torch.cuda._sleep(2_000_000)  # let the host queue launches ahead of the GPU
     t_start.record()
     for k in range(steps):
-        if k in starts:
-            starts[k].record()
         step.launch(k % n_sets, stream_handle, fused)
-        if k in ends:
-            ends[k].record()
     t_end.record()
     torch.cuda.synchronize()
-    total_ms = t_start.elapsed_time(t_end)
-    kern = [starts[k].elapsed_time(ends[k]) for k in sampled]
-    return total_ms, kern
+    return t_start.elapsed_time(t_end)
+
+
+def time_isolated(torch, step, samples, stream_handle, fused=False):
+    """Durations of single launches, each alone between its own event pair.
+
+    A short device-side sleep goes in front of every sample, so the start
+    event, the launch and the end event are all queued before the GPU reaches
+    them: the pair brackets the launch and nothing of the host. It still
+    breaks the overlap that back-to-back launches get from programmatic
+    dependent launch."""
+    n_sets = len(step.xs)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(samples)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(samples)]
+    torch.cuda.synchronize()
+    for k in range(samples):
+        torch.cuda._sleep(100_000)  # ~50 us at 2 GHz
+        starts[k].record()
+        step.launch(k % n_sets, stream_handle, fused)
+        ends[k].record()
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in zip(starts, ends)]
 
 
 def time_graph(torch, step, launches, replays, fused=False):
@@ -479,7 +485,7 @@ def gpu_arm(args, rank, world, local_rank):
         torch.distributed.barrier()
     torch.cuda.synchronize()
     t0 = time.time()
-    total_ms, _ = time_steps(torch, step, args.steps, sh, fused=fused)
+    total_ms = time_steps(torch, step, args.steps, sh, fused=fused)
     t1 = time.time()
     total_ms_local = total_ms
     if world > 1:
@@ -495,8 +501,7 @@ def gpu_arm(args, rank, world, local_rank):
     peak, peak_src = measured_peak()
     achieved = nbytes / (kern_ms * 1e-3) / 1e9
     # context, outside the timed region: the same launch bracketed alone by an event pair
-    _, iso = time_steps(torch, step, min(400, args.steps), sh, fused=fused, sample_every=1)
-    iso_ms = float(np.median(iso))
+    iso_ms = float(np.median(time_isolated(torch, step, min(200, args.steps), sh, fused=fused)))
 
     out = None
     if rank == 0:
@@ -543,9 +548,9 @@ def gpu_arm(args, rank, world, local_rank):
                                  "kernel, back to back as in a real stream)",
                 "kernel_us_isolated": round(iso_ms * 1e3, 3),
                 "frac_isolated": round(nbytes / (iso_ms * 1e-3) / 1e9 / peak, 4),
-                "isolated_how": "median of 400 launches each bracketed alone by its own event pair, "
-                                "outside the timed region (adds the pair's round trip and the ramp that "
-                                "back-to-back launches overlap)",
+                "isolated_how": "median of 200 launches each bracketed alone by its own event pair behind a "
+                                "short device sleep, outside the timed region (no overlap with a previous "
+                                "launch)",
                 "frac_of_nominal_8tbs": round(achieved / 8000.0, 4),
             },
             "clocks": clocks,
@@ -562,9 +567,10 @@ def gpu_arm(args, rank, world, local_rank):
 
 def measure_rows(args, torch, rp, device, peak):
     """Every workload (and both M-RoPE layouts, fused and cached decode), timed three ways:
-    each launch alone between its own event pair (median), back to back from
-    the host (includes the host's per-call cost where that exceeds the
-    kernel), and replayed from a CUDA graph of 64 launches (device time)."""
+    each launch alone between its own event pair behind a device sleep
+    (median), back to back from the host (includes the host's per-call cost
+    where that exceeds the kernel), and replayed from a CUDA graph of 64
+    launches (device time)."""
     stream = torch.cuda.current_stream(device)
     sh = ctypes.c_void_p(stream.cuda_stream)
     rows = {}
@@ -580,7 +586,8 @@ def measure_rows(args, torch, rp, device, peak):
             rp.set_variant(variant)
             for k in range(20):
                 step.launch(k % len(step.xs), sh, fused)
-            total_ms, kern = time_steps(torch, step, args.row_steps, sh, fused, sample_every=1)
+            total_ms = time_steps(torch, step, args.row_steps, sh, fused)
+            kern = time_isolated(torch, step, min(200, args.row_steps), sh, fused)
             graph_ms = None
             if not (w.kind == "qkv" and not fused):  # the unfused Q/K path is torch ops: not captured
                 graph_ms = time_graph(torch, step, 64, max(2, args.row_steps // 64), fused)
