@@ -14,6 +14,15 @@
  *                     Modeling Code Alignment Check.
  *   rope_cache_build  the cos/sin cache that pull request precomputes from
  *                     inv_freq -- Critical Issues 1, Medium Issues 4.
+ *   mrope_apply_stream_map, mrope_apply_fused
+ *                     MRotaryEmbedding with an explicit stream per index, and
+ *                     with on-the-fly coefficients.
+ *   rope_apply_qkv, rope_apply_qkv_rmsnorm
+ *                     Q and K rotation for grouped-query attention with the
+ *                     key/value cache append ("com.microsoft.SparseAttention"
+ *                     README), and with QK-RMSNorm first (the pull request's
+ *                     Qwen3 Architecture).
+ *   rope_apply_no_alloc  rope_apply for callers that cannot allocate.
  *
  * Conventions shared by every entry point
  *   - All tensors are dense, contiguous, row-major. Tensor pointers are DEVICE
@@ -40,6 +49,13 @@
  *     failed while launching. rope_last_error() returns a message for the
  *     last failure on the calling thread.
  *   - An empty X (any dimension 0) is valid and launches nothing.
+ *   - Status word (the optional oor_flag / status_flags): a device int32 the
+ *     kernels OR bits into and never clear. Bit 0: some position was outside
+ *     the table (those elements were copied through). Bit 1: a pipelined
+ *     kernel gave up on one of its waits (each is bounded by 2 s of device
+ *     time) and returned early, so the output is incomplete; not expected in
+ *     normal operation. Bit 2 (Q/K entry points): some cache row was outside
+ *     the cache and was not stored.
  */
 #ifndef ROPE_GB300_H
 #define ROPE_GB300_H
@@ -96,8 +112,8 @@ typedef struct CUstream_st* rope_stream_t;
  *               ([manifest, inputs/position_ids])
  *               A position outside [0, max_sequence_length) never reads the
  *               cache: every element of that token is copied through and, if
- *               oor_flag is not NULL, the device int32 *oor_flag is set to 1
- *               (it is never cleared by the library).
+ *               oor_flag is not NULL, bit 0 of the device int32 *oor_flag is
+ *               set (the status word above; never cleared by the library).
  * interleaved   0: pair i is (i, i + rd/2); 1: pair i is (2i, 2i+1).
  * rotary_embedding_dim  0 = H; otherwise an even rd with 0 < rd <= H. Elements
  *               [rd, H) of every head are copied through.
@@ -126,7 +142,7 @@ rope_status rope_apply(rope_dtype dtype, int32_t x_rank, const int64_t* x_shape,
  * position_ids  device int64 (3, B, S): temporal, height and width streams
  *               ([README, Inputs/positionIds]). A pair whose stream position
  *               is negative or >= cache_rows is copied through unchanged and
- *               *oor_flag (if not NULL) is set to 1.
+ *               bit 0 of *oor_flag (if not NULL) is set.
  * mrope_section host int32[3], non-negative, summing to rd/2: how many
  *               half-rotary indices each stream drives ([README, Attributes/
  *               mrope_section]).
@@ -238,8 +254,8 @@ rope_status rope_apply_fused(rope_dtype dtype, int32_t x_rank, const int64_t* x_
  *           (rotated K, V as given); no other row is written. A token whose
  *           row falls outside [0, max_cache_len) is not stored (status bit 2).
  * status_flags  NULL or a device int32 the kernel ORs bits into (never
- *           clears): bit 0 a position out of range, bit 2 a cache row out of
- *           range.
+ *           clears): bit 0 a position out of range, bit 1 a pipelined wait
+ *           that gave up, bit 2 a cache row out of range.
  * All buffers are caller-owned; nothing is allocated. Buffers other than the
  * aliases named above must not overlap. ROPE_ERR_INVALID_ARG (before any
  * launch) for: num_heads or kv_num_heads < 1, kv_num_heads not dividing
