@@ -62,8 +62,9 @@ def parse_args():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--variant", choices=["auto", "simt", "tma"], default="auto",
                     help="kernel variant for the timed region (the library's automatic choice by default)")
-    ap.add_argument("--schedule", choices=["dynamic", "static"], default="static",
-                    help="tile schedule of the pipelined kernel: a scratch counter (dynamic) or round robin")
+    ap.add_argument("--schedule", choices=["dynamic", "static"], default="dynamic",
+                    help="tile schedule of the pipelined RoPE kernel: a 64-byte scratch counter per stream "
+                         "(dynamic; measured 3-3.5 %% faster on M-RoPE and rank 4) or round robin (no scratch)")
     ap.add_argument("--quick", action="store_true",
                     help="timed region only: no per-workload rows, end-to-end or CPU legs (profiling runs)")
     return ap.parse_args()
@@ -315,6 +316,9 @@ class Step:
         return self.call(x, y, stream, fused)
 
     def scratch_for(self, stream):
+        """The dynamic schedule's scratch for launches on `stream`: one zeroed buffer per
+        stream, made on first use (outside any timed region or graph capture: every
+        stream a timing loop uses gets its first launch in the warm-up)."""
         if not self.dynamic:
             return None
         key = stream.value if isinstance(stream, ctypes.c_void_p) else stream
@@ -581,7 +585,7 @@ def measure_rows(args, torch, rp, device, peak):
             variants = [("fused", True, "auto"), ("cached", False, "auto")]
         if w.kind == "qkv":
             variants = [("fused", True, "auto"), ("unfused", False, "auto")]
-        step = make_step(rp, torch, w, device, n_buffer_sets(w))
+        step = make_step(rp, torch, w, device, n_buffer_sets(w), dynamic=args.schedule == "dynamic")
         for label, fused, variant in variants:
             rp.set_variant(variant)
             for k in range(20):
