@@ -80,7 +80,8 @@ typedef enum rope_dtype { ROPE_F32 = 0, ROPE_F16 = 1, ROPE_BF16 = 2 } rope_dtype
 
 /*
  * Scratch for the dynamic tile schedule (optional `scratch` argument of
- * rope_apply, mrope_apply and mrope_apply_stream_map): ROPE_SCRATCH_BYTES of
+ * rope_apply, mrope_apply, mrope_apply_stream_map, rope_apply_qkv and
+ * rope_apply_qkv_rmsnorm): ROPE_SCRATCH_BYTES of
  * caller-owned device memory, 8-byte aligned, set to zero once before its first
  * use. With it, the pipelined kernel hands tiles to whichever CTA asks next, so
  * CTAs that run faster take more tiles and the launch ends sooner; every launch
@@ -256,6 +257,10 @@ rope_status rope_apply_fused(rope_dtype dtype, int32_t x_rank, const int64_t* x_
  * status_flags  NULL or a device int32 the kernel ORs bits into (never
  *           clears): bit 0 a position out of range, bit 1 a pipelined wait
  *           that gave up, bit 2 a cache row out of range.
+ * scratch   NULL or ROPE_SCRATCH_BYTES of device scratch for the dynamic tile
+ *           schedule of the pipelined kernel, with the rules of rope_apply's
+ *           scratch (zero before first use, one per concurrently running
+ *           stream); the result is the same either way.
  * All buffers are caller-owned; nothing is allocated. Buffers other than the
  * aliases named above must not overlap. ROPE_ERR_INVALID_ARG (before any
  * launch) for: num_heads or kv_num_heads < 1, kv_num_heads not dividing
@@ -270,7 +275,7 @@ rope_status rope_apply_qkv(rope_dtype dtype, int64_t batch, int64_t seq, int32_t
                            const void* sin_cache, int64_t cache_rows, const int64_t* position_ids,
                            const int32_t* past_seq_lens, int32_t interleaved,
                            int32_t rotary_embedding_dim, void* q_out, void* k_out, void* k_cache,
-                           void* v_cache, int64_t max_cache_len, int32_t* status_flags,
+                           void* v_cache, int64_t max_cache_len, int32_t* status_flags, void* scratch,
                            rope_stream_t stream);
 
 /*
@@ -304,7 +309,7 @@ rope_status rope_apply_qkv_rmsnorm(rope_dtype dtype, int64_t batch, int64_t seq,
                                    const int64_t* position_ids, const int32_t* past_seq_lens,
                                    int32_t interleaved, int32_t rotary_embedding_dim, void* q_out,
                                    void* k_out, void* k_cache, void* v_cache, int64_t max_cache_len,
-                                   int32_t* status_flags, rope_stream_t stream);
+                                   int32_t* status_flags, void* scratch, rope_stream_t stream);
 
 /*
  * mrope_apply_fused -- MRotaryEmbedding with cos/sin computed on the fly

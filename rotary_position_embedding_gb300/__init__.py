@@ -52,9 +52,9 @@ SIGNATURES = {
     "mrope_apply_fused": [_i32, _i32, _i64p, _vp, _vp, _vp, _f32, _vp, _i32p, _i32, _f32, _i32, _i32, _i32, _vp],
     "rope_cache_build": [_i32, _vp, _i32, _i64, _f32, _vp, _vp, _vp],
     "rope_apply_qkv": [_i32, _i64, _i64, _i32, _i32, _i64, _vp, _vp, _vp, _vp, _vp, _i64, _vp, _vp, _i32,
-                       _i32, _vp, _vp, _vp, _vp, _i64, _vp, _vp],
+                       _i32, _vp, _vp, _vp, _vp, _i64, _vp, _vp, _vp],
     "rope_apply_qkv_rmsnorm": [_i32, _i64, _i64, _i32, _i32, _i64, _vp, _vp, _vp, _vp, _vp, _f32, _vp, _vp,
-                               _i64, _vp, _vp, _i32, _i32, _vp, _vp, _vp, _vp, _i64, _vp, _vp],
+                               _i64, _vp, _vp, _i32, _i32, _vp, _vp, _vp, _vp, _i64, _vp, _vp, _vp],
     "rope_apply_no_alloc": [_i32, _i32, _i64p, _vp, _vp, _i32, _i64p, _vp, _vp, _vp, _i32, _i32, _i32, _vp,
                             _vp],
     "rope_set_variant": [_i32],
@@ -283,7 +283,7 @@ def rope_apply_fused(x, inv_freq, position_ids, *, attention_scaling=1.0, interl
 def rope_apply_qkv(query, cos_cache, sin_cache, position_ids=None, *, num_heads, kv_num_heads, key=None,
                    value=None, interleaved=0, rotary_embedding_dim=0, k_cache=None, v_cache=None,
                    past_seq_lens=None, q_out=None, k_out=None, status=None, q_norm_weight=None,
-                   k_norm_weight=None, epsilon=1e-6, stream=None):
+                   k_norm_weight=None, epsilon=1e-6, stream=None, scratch=None):
     """Q and K rotation for grouped-query attention in one launch, optionally
     appending rotated K and V to (B, kv_num_heads, max_len, H) caches in place.
     With q_norm_weight and k_norm_weight (head_size vectors) each Q and K head
@@ -291,7 +291,9 @@ def rope_apply_qkv(query, cos_cache, sin_cache, position_ids=None, *, num_heads,
 
     query is (B, S, num_heads*H), or packed [Q|K|V] (B, S, (num_heads +
     2*kv_num_heads)*H) when key and value are None. Returns (q_out, k_out);
-    k_out is None in cache mode (the caches hold the result).
+    k_out is None in cache mode (the caches hold the result). scratch: None,
+    or ROPE_SCRATCH_BYTES of zeroed device memory for the dynamic tile schedule
+    (one per concurrently running stream).
     """
     import torch
 
@@ -326,13 +328,13 @@ def rope_apply_qkv(query, cos_cache, sin_cache, position_ids=None, *, num_heads,
                 _ptr(value), _ptr(q_norm_weight), _ptr(k_norm_weight), float(epsilon), _ptr(cos_cache),
                 _ptr(sin_cache), int(cos_cache.shape[0]), _ptr(position_ids), _ptr(past_seq_lens),
                 int(interleaved), int(rotary_embedding_dim), _ptr(q_out), _ptr(k_out), _ptr(k_cache),
-                _ptr(v_cache), int(max_len), _ptr(status), _stream(query, stream))
+                _ptr(v_cache), int(max_len), _ptr(status), _ptr(scratch), _stream(query, stream))
         else:
             st = lib.rope_apply_qkv(_dtype_code(query), B, S, int(num_heads), int(kv_num_heads), H, _ptr(query),
                                     _ptr(key), _ptr(value), _ptr(cos_cache), _ptr(sin_cache),
                                     int(cos_cache.shape[0]), _ptr(position_ids), _ptr(past_seq_lens),
                                     int(interleaved), int(rotary_embedding_dim), _ptr(q_out), _ptr(k_out),
-                                    _ptr(k_cache), _ptr(v_cache), int(max_len), _ptr(status),
+                                    _ptr(k_cache), _ptr(v_cache), int(max_len), _ptr(status), _ptr(scratch),
                                     _stream(query, stream))
     _check("rope_apply_qkv_rmsnorm" if norm else "rope_apply_qkv", st)
     return q_out, (None if cache else k_out)

@@ -906,7 +906,7 @@ rope_status qkv_impl(rope_dtype dtype, int64_t batch, int64_t seq, int32_t num_h
                      const void* sin_cache, int64_t cache_rows, const int64_t* position_ids,
                      const int32_t* past_seq_lens, int32_t interleaved, int32_t rotary_embedding_dim,
                      void* q_out, void* k_out, void* k_cache, void* v_cache, int64_t max_cache_len,
-                     int32_t* status_flags, rope_stream_t stream) {
+                     int32_t* status_flags, void* scratch, rope_stream_t stream) {
   g_last_error.clear();
   ROPE_TRY(check_dtype(dtype));
   const bool norm = q_weight != nullptr || k_weight != nullptr;
@@ -986,6 +986,7 @@ rope_status qkv_impl(rope_dtype dtype, int64_t batch, int64_t seq, int32_t num_h
     ROPE_TRY(check_elem_ptr(k_weight, "k_norm_weight", es));
   }
   if (status_flags && !aligned(status_flags, 4)) return fail(ROPE_ERR_INVALID_ARG, "status_flags is misaligned");
+  if (scratch && !aligned(scratch, 8)) return fail(ROPE_ERR_INVALID_ARG, "scratch is not aligned to 8 bytes");
 
   const bool vec = vector_ok(g, es, {query, key, value, q_out, k_out, k_cache, v_cache, cos_cache, sin_cache,
                                      q_weight, k_weight});
@@ -999,6 +1000,7 @@ rope_status qkv_impl(rope_dtype dtype, int64_t batch, int64_t seq, int32_t num_h
   kp.pos = position_ids;
   kp.oor_flag = status_flags;
   kp.cache_rows = cache_rows;
+  kp.sched = static_cast<unsigned long long*>(scratch);
   QKVParams qa;
   memset(&qa, 0, sizeof(qa));
   qa.k = key;
@@ -1054,11 +1056,12 @@ rope_status rope_apply_qkv(rope_dtype dtype, int64_t batch, int64_t seq, int32_t
                            const void* sin_cache, int64_t cache_rows, const int64_t* position_ids,
                            const int32_t* past_seq_lens, int32_t interleaved,
                            int32_t rotary_embedding_dim, void* q_out, void* k_out, void* k_cache,
-                           void* v_cache, int64_t max_cache_len, int32_t* status_flags,
+                           void* v_cache, int64_t max_cache_len, int32_t* status_flags, void* scratch,
                            rope_stream_t stream) {
   return qkv_impl(dtype, batch, seq, num_heads, kv_num_heads, head_size, query, key, value, nullptr, nullptr,
                   0.0f, cos_cache, sin_cache, cache_rows, position_ids, past_seq_lens, interleaved,
-                  rotary_embedding_dim, q_out, k_out, k_cache, v_cache, max_cache_len, status_flags, stream);
+                  rotary_embedding_dim, q_out, k_out, k_cache, v_cache, max_cache_len, status_flags, scratch,
+                  stream);
 }
 
 rope_status rope_apply_qkv_rmsnorm(rope_dtype dtype, int64_t batch, int64_t seq, int32_t num_heads,
@@ -1069,7 +1072,7 @@ rope_status rope_apply_qkv_rmsnorm(rope_dtype dtype, int64_t batch, int64_t seq,
                                    const int64_t* position_ids, const int32_t* past_seq_lens,
                                    int32_t interleaved, int32_t rotary_embedding_dim, void* q_out,
                                    void* k_out, void* k_cache, void* v_cache, int64_t max_cache_len,
-                                   int32_t* status_flags, rope_stream_t stream) {
+                                   int32_t* status_flags, void* scratch, rope_stream_t stream) {
   if (!q_norm_weight || !k_norm_weight) {
     g_last_error.clear();
     return fail(ROPE_ERR_INVALID_ARG, "q_norm_weight and k_norm_weight are required");
@@ -1077,7 +1080,7 @@ rope_status rope_apply_qkv_rmsnorm(rope_dtype dtype, int64_t batch, int64_t seq,
   return qkv_impl(dtype, batch, seq, num_heads, kv_num_heads, head_size, query, key, value, q_norm_weight,
                   k_norm_weight, epsilon, cos_cache, sin_cache, cache_rows, position_ids, past_seq_lens,
                   interleaved, rotary_embedding_dim, q_out, k_out, k_cache, v_cache, max_cache_len,
-                  status_flags, stream);
+                  status_flags, scratch, stream);
 }
 
 rope_status rope_cache_build(rope_dtype dtype, const float* inv_freq, int32_t half, int64_t rows,

@@ -193,10 +193,16 @@ __global__ void __launch_bounds__(kTmaThreads, ROPE_TMA_MIN_CTAS)
     if (lane == 0) {
       const uint64_t pol = policy_evict_first();
       bool timed_out = false;
-      auto tile_index = [&](int64_t jj) -> int64_t { return (int64_t)blockIdx.x + jj * (int64_t)gridDim.x; };
-      auto issue = [&](int64_t jj) {
+      // Tile indices: blockIdx.x + jj*gridDim.x (static schedule), or -- with
+      // a caller scratch counter -- the next value of the counter, so CTAs
+      // that run faster take more tiles. Each index is recorded in its stage
+      // header; the first index past the last tile (the sentinel) ends the
+      // pipeline.
+      auto pick = [&](int64_t jj) -> int64_t {
+        return p.sched ? (int64_t)atomicAdd(p.sched, 1ull) : (int64_t)blockIdx.x + jj * (int64_t)gridDim.x;
+      };
+      auto issue = [&](int64_t jj, int64_t t) {
         const int s = (int)(jj % tp.K);
-        const int64_t t = tile_index(jj);
         *stage_hdr(s) = t;
         if (t < tp.ntiles) {
           const QTile q = qtile_of(p, tp, t);
@@ -213,17 +219,16 @@ __global__ void __launch_bounds__(kTmaThreads, ROPE_TMA_MIN_CTAS)
         }
         mbar_arrive(issued0 + 8 * s);
       };
-      int64_t jx = 0;
-      for (; jx < tp.K; ++jx) {
-        issue(jx);
-        if (tile_index(jx) >= tp.ntiles) break;
+      bool ended = false;
+      int64_t jx = 0;  // tiles issued (the sentinel included)
+      for (; jx < tp.K && !ended; ++jx) {
+        const int64_t t = pick(jx);
+        issue(jx, t);
+        ended = t >= tp.ntiles;
       }
-      const bool all_issued_early = jx < tp.K;  // the sentinel went out with the first K
-      bool ended = all_issued_early;
-      if (!ended) jx = tp.K;
       // the next store's tile and cache row are worked out while the previous
       // store is still reading its stage
-      int64_t t_st = tile_index(0);
+      int64_t t_st = *stage_hdr(0);
       QTile q_st{};
       int64_t past_st = 0;  // raw past[b]: the load is consumed only at the store
       auto prep = [&](int64_t t) {
@@ -255,12 +260,14 @@ __global__ void __launch_bounds__(kTmaThreads, ROPE_TMA_MIN_CTAS)
           }
           bulk_commit();
         }
-        t_st = tile_index(j + 1);
+        const int64_t t_new = ended ? 0 : pick(jx);
+        // tile j+1 is already issued (K >= 2), so its header is in place
+        t_st = *stage_hdr((int)((j + 1) % tp.K));
         prep(t_st);
         if (!ended) {
           bulk_wait_read_0();  // the stage may be refilled once the store has read it
-          issue(jx);           // jx == j + K: the tile that goes into stage s next
-          ended = tile_index(jx) >= tp.ntiles;
+          issue(jx, t_new);    // jx == j + K: the tile that goes into stage s next
+          ended = t_new >= tp.ntiles;
           ++jx;
         }
       }
@@ -270,6 +277,15 @@ __global__ void __launch_bounds__(kTmaThreads, ROPE_TMA_MIN_CTAS)
         while (global_ns() - t0 < 1000000ull) {
         }
         if (p.oor_flag) atomicOr(p.oor_flag, 2);
+      }
+      if (p.sched) {
+        // The last CTA to stop drawing resets the counter pair for the next launch.
+        __threadfence();
+        if (atomicAdd(p.sched + 1, 1ull) == (unsigned long long)gridDim.x - 1) {
+          p.sched[0] = 0;
+          p.sched[1] = 0;
+          __threadfence();
+        }
       }
     }
     return;
@@ -289,10 +305,10 @@ __global__ void __launch_bounds__(kTmaThreads, ROPE_TMA_MIN_CTAS)
     const uint32_t row_bytes = (uint32_t)h * (uint32_t)sizeof(bits);
     const int rows = tp.TS * 2;
     const int rounds = (rows + 31) / 32;  // the same for every lane: the shuffles below are warp-wide
-    // The schedule is static, so what a tile needs from global memory -- its
-    // positions, or the past length its positions and cache rows start from --
-    // is loaded one tile ahead: under a saturated memory system even these
-    // L2 hits take microseconds, and the gather of the tile waits on none.
+    // What a tile needs from global memory -- its positions, or the past
+    // length its positions and cache rows start from -- is loaded one tile
+    // ahead: under a saturated memory system even these L2 hits take
+    // microseconds, and the gather of the tile waits on none.
     struct Pre {
       int64_t pos;   // explicit position of token `lane`
       int64_t past;  // past[b]
@@ -306,7 +322,15 @@ __global__ void __launch_bounds__(kTmaThreads, ROPE_TMA_MIN_CTAS)
       }
       return r;
     };
-    Pre cur = prefetch(blockIdx.x);
+    // Dynamic schedule: the next index is read from its stage header when the
+    // copy warp has already published it; otherwise the tile's own values are
+    // loaded when it comes up.
+    Pre cur{0, 0};
+    bool have_cur = false;
+    if (!p.sched) {
+      cur = prefetch(blockIdx.x);
+      have_cur = true;
+    }
     for (int64_t j = 0;; ++j) {
       const int s = (int)(j % tp.K);
       if (!__all_sync(0xffffffffu, mbar_wait(issued0 + 8 * s, (uint32_t)((j / tp.K) & 1)))) {
@@ -318,7 +342,21 @@ __global__ void __launch_bounds__(kTmaThreads, ROPE_TMA_MIN_CTAS)
         cp_async_arrive(full0 + 8 * s);
         break;
       }
-      const Pre nxt = prefetch(t + gridDim.x);  // this CTA's next tile
+      if (!have_cur) cur = prefetch(t);
+      Pre nxt{0, 0};
+      bool have_nxt = false;
+      if (!p.sched) {
+        nxt = prefetch(t + gridDim.x);  // this CTA's next tile
+        have_nxt = true;
+      } else {
+        // headers are published in tile order and tile j+1-K's phase of this
+        // barrier is already complete, so the parity test cannot alias
+        const int sn = (int)((j + 1) % tp.K);
+        if (__all_sync(0xffffffffu, mbar_test(issued0 + 8 * sn, (uint32_t)(((j + 1) / tp.K) & 1)))) {
+          nxt = prefetch(*stage_hdr(sn));
+          have_nxt = true;
+        }
+      }
       const QTile q = qtile_of(p, tp, t);
       unsigned char* st = stage0 + (size_t)s * tp.stage_bytes;
       if (q.role != 0 && a.cache && lane == 0) stage_hdr(s)[1] = cur.past + q.s0;
@@ -360,6 +398,7 @@ __global__ void __launch_bounds__(kTmaThreads, ROPE_TMA_MIN_CTAS)
         mbar_arrive(full0 + 8 * s);
       }
       cur = nxt;
+      have_cur = have_nxt;
     }
     asm volatile("cp.async.wait_all;" ::: "memory");
     if (timed_out && lane == 0 && p.oor_flag) atomicOr(p.oor_flag, 2);

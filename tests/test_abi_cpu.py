@@ -193,11 +193,12 @@ FAKE4 = ctypes.c_void_p(0x40000)
 def _qkv(so, **kw):
     a = dict(dtype=F16, B=2, S=4, nq=8, nkv=2, H=16, q=FAKE, k=FAKE2, v=None, cos=FAKE3, sin=FAKE3, rows=32,
              pos=FAKE4, past=None, inter=0, rd=0, q_out=ctypes.c_void_p(0x50000),
-             k_out=ctypes.c_void_p(0x60000), kc=None, vc=None, max_len=0, flag=None, stream=None)
+             k_out=ctypes.c_void_p(0x60000), kc=None, vc=None, max_len=0, flag=None, scratch=None, stream=None)
     a.update(kw)
     return so.rope_apply_qkv(a["dtype"], a["B"], a["S"], a["nq"], a["nkv"], a["H"], a["q"], a["k"], a["v"],
                              a["cos"], a["sin"], a["rows"], a["pos"], a["past"], a["inter"], a["rd"],
-                             a["q_out"], a["k_out"], a["kc"], a["vc"], a["max_len"], a["flag"], a["stream"])
+                             a["q_out"], a["k_out"], a["kc"], a["vc"], a["max_len"], a["flag"], a["scratch"],
+                             a["stream"])
 
 
 CACHE = dict(v=ctypes.c_void_p(0x70000), k_out=None, kc=ctypes.c_void_p(0x80000), vc=ctypes.c_void_p(0x90000),
@@ -229,6 +230,7 @@ CACHE = dict(v=ctypes.c_void_p(0x70000), k_out=None, kc=ctypes.c_void_p(0x80000)
     (dict(q=ctypes.c_void_p(0x10001)), INVALID),         # misaligned float16 pointer
     (dict(pos=ctypes.c_void_p(0x40004)), INVALID),       # misaligned int64 pointer
     (dict(CACHE, past=ctypes.c_void_p(0xa0002)), INVALID),   # misaligned int32 pointer
+    (dict(scratch=ctypes.c_void_p(0xd0004)), INVALID),   # scratch not 8-byte aligned
     (dict(q_out=None), INVALID),
 ])
 def test_rope_apply_qkv_rejects_before_launch(lib, kw, status):
@@ -248,12 +250,12 @@ def _qkv_norm(so, **kw):
     a = dict(dtype=F16, B=2, S=4, nq=8, nkv=2, H=16, q=FAKE, k=FAKE2, v=None, qw=ctypes.c_void_p(0xb0000),
              kw_=ctypes.c_void_p(0xc0000), eps=1e-6, cos=FAKE3, sin=FAKE3, rows=32, pos=FAKE4, past=None, inter=0,
              rd=0, q_out=ctypes.c_void_p(0x50000), k_out=ctypes.c_void_p(0x60000), kc=None, vc=None, max_len=0,
-             flag=None, stream=None)
+             flag=None, scratch=None, stream=None)
     a.update(kw)
     return so.rope_apply_qkv_rmsnorm(a["dtype"], a["B"], a["S"], a["nq"], a["nkv"], a["H"], a["q"], a["k"],
                                      a["v"], a["qw"], a["kw_"], a["eps"], a["cos"], a["sin"], a["rows"], a["pos"],
                                      a["past"], a["inter"], a["rd"], a["q_out"], a["k_out"], a["kc"], a["vc"],
-                                     a["max_len"], a["flag"], a["stream"])
+                                     a["max_len"], a["flag"], a["scratch"], a["stream"])
 
 
 @pytest.mark.parametrize("kw,status", [

@@ -57,7 +57,8 @@ def _token_mask(B, S, N, H, rd, bad_tok):
 
 
 def _run_case(lib, orc, torch, cuda, dt, packed, cache, inter, rot, implicit, H, offset=0, Nq=8, Nkv=2,
-              B=3, S=37, R=64, L=80, seed=0, variant="auto", kernel="rope_qkv_kernel", past=None):
+              B=3, S=37, R=64, L=80, seed=0, variant="auto", kernel="rope_qkv_kernel", past=None,
+              dynamic=False):
     rng = np.random.default_rng(seed)
     npdt = {"f16": np.float16, "f32": np.float32, "bf16": BF16}[dt]
     rd = 0 if rot == "full" else H // 2
@@ -90,15 +91,19 @@ def _run_case(lib, orc, torch, cuda, dt, packed, cache, inter, rot, implicit, H,
     dv = lambda a: None if a is None else _dev(a, torch, cuda, offset)  # noqa: E731
     status = torch.zeros(1, dtype=torch.int32, device=cuda)
     kc_d, vc_d = dv(kc0), dv(vc0)
+    scratch = torch.zeros(8, dtype=torch.int64, device=cuda) if dynamic else None
     with lib.variant(variant):
         qo, ko = lib.rope_apply_qkv(dv(qkv if packed else q), dv(cos), dv(sin),
                                     None if pos is None else _dev(pos, torch, cuda), num_heads=Nq,
                                     kv_num_heads=Nkv, key=None if packed else dv(k),
                                     value=None if (packed or not cache) else dv(v), interleaved=inter,
                                     rotary_embedding_dim=rd, k_cache=kc_d, v_cache=vc_d,
-                                    past_seq_lens=_dev(past, torch, cuda) if use_past else None, status=status)
+                                    past_seq_lens=_dev(past, torch, cuda) if use_past else None, status=status,
+                                    scratch=scratch)
     torch.cuda.synchronize()
     assert lib.last_kernel() == kernel
+    if dynamic:  # the launch leaves its schedule counters at zero for the next one
+        assert not bool(scratch.any())
     rdw = rd or H
     compare(_host(qo), q_ref, q, 3, Nq, _token_mask(B, S, Nq, H, rdw, bad_tok))
     if not cache:
@@ -157,14 +162,18 @@ QKV_TMA_SHAPES = [
 ]
 
 
+@pytest.mark.parametrize("schedule", ["static", "dynamic"])
 @pytest.mark.parametrize("dt,H,Nq,Nkv,B,S,packed,cache,inter,rot,implicit,R,L", QKV_TMA_SHAPES)
-def test_qkv_tma_shapes(lib, orc, cuda, dt, H, Nq, Nkv, B, S, packed, cache, inter, rot, implicit, R, L):
-    """Every case has out-of-range positions and, in cache mode, rows past the cache's end."""
+def test_qkv_tma_shapes(lib, orc, cuda, dt, H, Nq, Nkv, B, S, packed, cache, inter, rot, implicit, R, L,
+                        schedule):
+    """Every case has out-of-range positions and, in cache mode, rows past the cache's end;
+    tiles dealt round robin (no scratch) or drawn from a scratch counter."""
     import torch
 
     case = (dt, H, Nq, Nkv, B, S, packed, cache, inter, rot, implicit, R, L)
     _run_case(lib, orc, torch, cuda, dt, packed, cache, inter, rot, implicit, H=H, Nq=Nq, Nkv=Nkv, B=B, S=S,
-              R=R, L=L, seed=QKV_TMA_SHAPES.index(case), variant="tma", kernel="rope_qkv_tma_kernel")
+              R=R, L=L, seed=QKV_TMA_SHAPES.index(case), variant="tma", kernel="rope_qkv_tma_kernel",
+              dynamic=schedule == "dynamic")
 
 
 @pytest.mark.parametrize("dt,H,offset", [("f16", 12, 0), ("f32", 6, 0), ("f16", 64, 1), ("f32", 64, 1)])
@@ -212,7 +221,7 @@ def test_qkv_empty_and_rejects(lib, cuda):
                            key=torch.zeros((1, 4, 64), dtype=torch.float16, device=cuda))
 
 
-@pytest.mark.parametrize("variant", ["auto", "simt"])
+@pytest.mark.parametrize("variant", ["auto", "auto_dynamic", "simt"])
 @pytest.mark.parametrize("name", [n for n, w in wl.WORKLOADS.items() if w.kind == "qkv"])
 def test_qkv_workload_full_size(lib, orc, cuda, name, variant):
     """The benchmark's own shapes and launch (packed [Q|K|V], implicit positions past[b] + s,
@@ -242,13 +251,14 @@ def test_qkv_workload_full_size(lib, orc, cuda, name, variant):
         q_ref, k_ref, _, _, _, _ = orc.rope_qkv(x, cos, sin, pos, num_heads=Nq, kv_num_heads=Nkv, **nkw)
         nkw = {**nkw, "q_norm_weight": _dev(nkw["q_norm_weight"], torch, cuda),
                "k_norm_weight": _dev(nkw["k_norm_weight"], torch, cuda)}
-    with lib.variant(variant):
+    scratch = torch.zeros(8, dtype=torch.int64, device=cuda) if variant == "auto_dynamic" else None
+    with lib.variant("simt" if variant == "simt" else "auto"):
         qo, ko = lib.rope_apply_qkv(_dev(x, torch, cuda), _dev(cos, torch, cuda), _dev(sin, torch, cuda), None,
                                     num_heads=Nq, kv_num_heads=Nkv, k_cache=kc, v_cache=vc,
-                                    past_seq_lens=_dev(past, torch, cuda), status=status, **nkw)
+                                    past_seq_lens=_dev(past, torch, cuda), status=status, scratch=scratch, **nkw)
     torch.cuda.synchronize()
     big = x.nbytes >= 8 << 20   # the automatic choice sends 8 MiB and more to the TMA pipeline
-    assert lib.last_kernel() == ("rope_qkv_tma_kernel" if variant == "auto" and big else "rope_qkv_kernel")
+    assert lib.last_kernel() == ("rope_qkv_tma_kernel" if variant != "simt" and big else "rope_qkv_kernel")
     assert ko is None and int(status.item()) == 0
     none_bad = np.zeros((B, S), dtype=bool)
     bi = torch.arange(B, device=cuda)[:, None].expand(B, S)
@@ -321,20 +331,23 @@ def test_qkv_tma_bits_equal_simt(lib, cuda, dt, norm, inter):
                   k_norm_weight=_dev(cast(rng.uniform(0.5, 2.0, H), npdt), torch, cuda), epsilon=1e-6)
     kc0 = cast(rng.standard_normal((B, Nkv, L, H)), npdt)
     out = {}
-    for variant in ("simt", "tma"):
+    for variant, dyn in (("simt", False), ("tma", False), ("tma", True)):
         kc, vc = _dev(kc0, torch, cuda), _dev(kc0, torch, cuda)
         status = torch.zeros(1, dtype=torch.int32, device=cuda)
+        scratch = torch.zeros(8, dtype=torch.int64, device=cuda) if dyn else None
         with lib.variant(variant):
             qo, _ = lib.rope_apply_qkv(_dev(qkv, torch, cuda), _dev(cos, torch, cuda), _dev(sin, torch, cuda),
                                        _dev(pos, torch, cuda), num_heads=Nq, kv_num_heads=Nkv, interleaved=inter,
                                        k_cache=kc, v_cache=vc, past_seq_lens=_dev(past, torch, cuda),
-                                       status=status, **kw)
+                                       status=status, scratch=scratch, **kw)
         torch.cuda.synchronize()
         assert lib.last_kernel() == QKV_KERNELS.get(variant, "rope_qkv_kernel")
-        out[variant] = [_host(t) for t in (qo, kc, vc)] + [int(status.item())]
-    for a, b in zip(out["simt"][:3], out["tma"][:3]):
-        assert np.array_equal(a.view(np.uint8), b.view(np.uint8))
-    assert out["simt"][3] == out["tma"][3] == (1 | 4)
+        out[(variant, dyn)] = [_host(t) for t in (qo, kc, vc)] + [int(status.item())]
+    for key in (("tma", False), ("tma", True)):
+        for a, b in zip(out[("simt", False)][:3], out[key][:3]):
+            assert np.array_equal(a.view(np.uint8), b.view(np.uint8))
+        assert out[key][3] == (1 | 4)
+    assert out[("simt", False)][3] == (1 | 4)
 
 
 # ---------------------------------------------------------------------------
