@@ -18,6 +18,7 @@ from .oracle import (  # noqa: F401
     mrope,
     mrope_fused,
     mrope_map,
+    mrope_qkv,
     mrope_stream_map,
     rope,
     rope_fused,

@@ -67,9 +67,12 @@ def _load():
                                                     _i64p, _i64p]
             lib.oracle_mrope_fused.argtypes = [i32, i32, _i64p, i64, i32, i64, vp, vp, f32, vp, vp, i32, f32,
                                                vp]
+            lib.oracle_mrope_qkv.argtypes = [i32, i64, i64, i64, i64, i64, i32, i64, vp, vp, vp, vp, vp,
+                                             ctypes.c_double, vp, vp, i64, vp, vp, i32, f32, vp, vp, vp, vp,
+                                             vp, i64, _i64p, _i64p]
             for name in ("oracle_rope", "oracle_mrope_stream_map", "oracle_mrope_map", "oracle_mrope",
                          "oracle_rope_fused", "oracle_cache_build", "oracle_rope_qkv",
-                         "oracle_rope_qkv_rmsnorm", "oracle_mrope_fused"):
+                         "oracle_rope_qkv_rmsnorm", "oracle_mrope_fused", "oracle_mrope_qkv"):
                 getattr(lib, name).restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -281,4 +284,42 @@ def rope_qkv(query, cos, sin, position_ids=None, *, num_heads, kv_num_heads, key
                                          int(max_len), ctypes.byref(n_oor), ctypes.byref(n_skip))
     if rc:
         raise ValueError("oracle_rope_qkv: malformed arguments")
+    return q_out, k_out, kc, vc, n_oor.value, n_skip.value
+
+
+def mrope_qkv(query, cos, sin, position_ids, mrope_section, mrope_layout=0, scale=1.0, *, num_heads,
+              kv_num_heads, key=None, value=None, interleaved=0, rotary_embedding_dim=0, k_cache=None,
+              v_cache=None, past_seq_lens=None, q_norm_weight=None, k_norm_weight=None, epsilon=1e-6):
+    """Q and K rotation with M-RoPE (position_ids (3, B, S): t, h, w), grouped-query
+    heads, the optional QK-RMSNorm and the optional cache append. Arguments and
+    returns as rope_qkv; n_oor counts Q and K pairs copied through."""
+    lib = _load()
+    q = _c(query)
+    B, S, hidden = q.shape
+    packed = key is None and value is None
+    Ntot = num_heads + (2 * kv_num_heads if packed else 0)
+    H = hidden // Ntot
+    k = None if key is None else _c(key, q.dtype)
+    v = None if value is None else _c(value, q.dtype)
+    cos = _c(cos, q.dtype)
+    sin = _c(sin, q.dtype)
+    pos = _c(position_ids, np.int64)
+    sec = np.ascontiguousarray(mrope_section, dtype=np.int32)
+    past = None if past_seq_lens is None else _c(past_seq_lens, np.int32)
+    q_out = np.empty((B, S, num_heads * H), dtype=q.dtype)
+    cache = k_cache is not None
+    k_out = None if cache else np.empty((B, S, kv_num_heads * H), dtype=q.dtype)
+    kc = None if k_cache is None else np.array(k_cache, dtype=q.dtype, copy=True, order="C")
+    vc = None if v_cache is None else np.array(v_cache, dtype=q.dtype, copy=True, order="C")
+    max_len = kc.shape[2] if cache else 0
+    qw = None if q_norm_weight is None else _c(q_norm_weight, q.dtype)
+    kw = None if k_norm_weight is None else _c(k_norm_weight, q.dtype)
+    n_oor, n_skip = ctypes.c_int64(0), ctypes.c_int64(0)
+    rc = lib.oracle_mrope_qkv(_dt(q), B, S, int(num_heads), int(kv_num_heads), H, int(interleaved),
+                              int(rotary_embedding_dim), _ptr(q), _ptr(k), _ptr(v), _ptr(qw), _ptr(kw),
+                              float(epsilon), _ptr(cos), _ptr(sin), int(cos.shape[0]), _ptr(pos), _ptr(sec),
+                              int(mrope_layout), float(scale), _ptr(past), _ptr(q_out), _ptr(k_out), _ptr(kc),
+                              _ptr(vc), int(max_len), ctypes.byref(n_oor), ctypes.byref(n_skip))
+    if rc:
+        raise ValueError("oracle_mrope_qkv: malformed arguments")
     return q_out, k_out, kc, vc, n_oor.value, n_skip.value

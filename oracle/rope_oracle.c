@@ -596,6 +596,31 @@ static void rope_one_head(int dt, int interleaved, int64_t H, int64_t rd, const 
   for (int64_t j = rd; j < H; ++j) cp(dt, x, xb + j, y, yb + j);
 }
 
+/* One head rotated as oracle_mrope_map rotates it: pair i takes the
+   position of its stream map[i] (p3[0..2] = t, h, w); a position outside
+   [0, cache_rows) copies the pair through (counted in *oor); otherwise the
+   coefficients are scaled and rounded to T before the rotation. */
+static void mrope_one_head(int dt, int interleaved, int64_t H, int64_t rd, const void* x, int64_t xb,
+                           void* y, int64_t yb, const void* cos_t, const void* sin_t, int64_t cache_rows,
+                           const int64_t* p3, const uint8_t* map, float scale, int64_t* oor) {
+  int64_t half = rd / 2;
+  for (int64_t i = 0; i < half; ++i) {
+    int64_t j0, j1;
+    pair_elems(interleaved, half, i, &j0, &j1);
+    const int64_t p = p3[map[i]];
+    if (p < 0 || p >= cache_rows) {
+      cp(dt, x, xb + j0, y, yb + j0);
+      cp(dt, x, xb + j1, y, yb + j1);
+      ++*oor;
+      continue;
+    }
+    const double c = round_to(dt, ld(dt, cos_t, p * half + i) * (double)scale);
+    const double sn = round_to(dt, ld(dt, sin_t, p * half + i) * (double)scale);
+    rotate_store(dt, y, yb + j0, yb + j1, ld(dt, x, xb + j0), ld(dt, x, xb + j1), c, sn);
+  }
+  for (int64_t j = rd; j < H; ++j) cp(dt, x, xb + j, y, yb + j);
+}
+
 /* RMS normalisation of one head (H elements at x + xb) followed by the
    per-channel weight, into z[0..H): z_j = T(w_j * T(x_j * r)) with
    r = 1 / sqrt(mean_j(x_j^2) + eps), the mean and r in binary64. */
@@ -613,12 +638,14 @@ static void rms_norm_head(int dt, const void* x, int64_t xb, int64_t H, const vo
   }
 }
 
+/* pos3 non-NULL: M-RoPE heads (mrope_one_head with map and scale; pos is
+   not used and *n_oor counts pairs); otherwise RotaryEmbedding heads. */
 static int qkv_core(int dt, int64_t B, int64_t S, int64_t Nq, int64_t Nkv, int64_t H, int interleaved,
                     int64_t rotary_dim, const void* q, const void* k, const void* v,
                     const void* q_weight, const void* k_weight, double eps, const void* cos_t,
-                    const void* sin_t, int64_t cache_rows, const int64_t* pos, const int32_t* past,
-                    void* q_out, void* k_out, void* k_cache, void* v_cache, int64_t max_len,
-                    int64_t* n_oor, int64_t* n_skip) {
+                    const void* sin_t, int64_t cache_rows, const int64_t* pos, const int64_t* pos3,
+                    const uint8_t* map, float scale, const int32_t* past, void* q_out, void* k_out,
+                    void* k_cache, void* v_cache, int64_t max_len, int64_t* n_oor, int64_t* n_skip) {
   if (B < 0 || S < 0 || Nq < 1 || Nkv < 1 || Nq % Nkv || H < 2 || H % 2) return 1;
   int64_t rd = rotary_dim ? rotary_dim : H;
   if (rd % 2 || rd > H || rd <= 0) return 1;
@@ -639,8 +666,11 @@ static int qkv_core(int dt, int64_t B, int64_t S, int64_t Nq, int64_t Nkv, int64
     for (int64_t s = 0; s < S; ++s) {
       int64_t tok = b * S + s;
       int64_t p = pos ? pos[tok] : (past ? (int64_t)past[b] + s : s);
+      int64_t p3[3] = {0, 0, 0};
+      if (pos3)
+        for (int st3 = 0; st3 < 3; ++st3) p3[st3] = pos3[st3 * B * S + tok];
       int valid = (p >= 0 && p < cache_rows);
-      if (!valid) ++oor;
+      if (!valid && !pos3) ++oor;
       int64_t crow = p * half;
       for (int64_t n = 0; n < Nq; ++n) {
         int64_t src = packed ? (tok * Ntot + n) * H : (tok * Nq + n) * H;
@@ -650,8 +680,12 @@ static int qkv_core(int dt, int64_t B, int64_t S, int64_t Nq, int64_t Nkv, int64
           qs = zq;
           src = 0;
         }
-        rope_one_head(dt, interleaved, H, rd, qs, src, q_out, (tok * Nq + n) * H, cos_t, sin_t, crow,
-                      valid);
+        if (pos3)
+          mrope_one_head(dt, interleaved, H, rd, qs, src, q_out, (tok * Nq + n) * H, cos_t, sin_t,
+                         cache_rows, p3, map, scale, &oor);
+        else
+          rope_one_head(dt, interleaved, H, rd, qs, src, q_out, (tok * Nq + n) * H, cos_t, sin_t, crow,
+                        valid);
       }
       int64_t row = cache ? (int64_t)past[b] + s : 0;
       int store = !cache || (row >= 0 && row < max_len);
@@ -665,13 +699,21 @@ static int qkv_core(int dt, int64_t B, int64_t S, int64_t Nq, int64_t Nkv, int64
           ksrc = 0;
         }
         if (!cache) {
-          rope_one_head(dt, interleaved, H, rd, ks, ksrc, k_out, (tok * Nkv + n) * H, cos_t, sin_t,
-                        crow, valid);
+          if (pos3)
+            mrope_one_head(dt, interleaved, H, rd, ks, ksrc, k_out, (tok * Nkv + n) * H, cos_t, sin_t,
+                           cache_rows, p3, map, scale, &oor);
+          else
+            rope_one_head(dt, interleaved, H, rd, ks, ksrc, k_out, (tok * Nkv + n) * H, cos_t, sin_t,
+                          crow, valid);
           continue;
         }
         if (!store) continue;
         int64_t dst = ((b * Nkv + n) * max_len + row) * H;
-        rope_one_head(dt, interleaved, H, rd, ks, ksrc, k_cache, dst, cos_t, sin_t, crow, valid);
+        if (pos3)
+          mrope_one_head(dt, interleaved, H, rd, ks, ksrc, k_cache, dst, cos_t, sin_t, cache_rows, p3, map,
+                         scale, &oor);
+        else
+          rope_one_head(dt, interleaved, H, rd, ks, ksrc, k_cache, dst, cos_t, sin_t, crow, valid);
         const void* vs = packed ? q : v;
         int64_t vsrc = packed ? (tok * Ntot + Nq + Nkv + n) * H : (tok * Nkv + n) * H;
         for (int64_t j = 0; j < H; ++j) cp(dt, vs, vsrc + j, v_cache, dst + j);
@@ -691,8 +733,8 @@ int oracle_rope_qkv(int dt, int64_t B, int64_t S, int64_t Nq, int64_t Nkv, int64
                     void* k_cache, void* v_cache, int64_t max_len, int64_t* n_oor,
                     int64_t* n_skip) {
   return qkv_core(dt, B, S, Nq, Nkv, H, interleaved, rotary_dim, q, k, v, NULL, NULL, 0.0, cos_t,
-                  sin_t, cache_rows, pos, past, q_out, k_out, k_cache, v_cache, max_len, n_oor,
-                  n_skip);
+                  sin_t, cache_rows, pos, NULL, NULL, 1.0f, past, q_out, k_out, k_cache, v_cache, max_len,
+                  n_oor, n_skip);
 }
 
 /* ------------------------------------------------------------------------ */
@@ -717,6 +759,45 @@ int oracle_rope_qkv_rmsnorm(int dt, int64_t B, int64_t S, int64_t Nq, int64_t Nk
                             int64_t* n_skip) {
   if (q_weight == NULL || k_weight == NULL) return 1;
   return qkv_core(dt, B, S, Nq, Nkv, H, interleaved, rotary_dim, q, k, v, q_weight, k_weight, eps,
-                  cos_t, sin_t, cache_rows, pos, past, q_out, k_out, k_cache, v_cache, max_len,
+                  cos_t, sin_t, cache_rows, pos, NULL, NULL, 1.0f, past, q_out, k_out, k_cache, v_cache,
+                  max_len, n_oor, n_skip);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Q and K rotation with M-RoPE, grouped-query heads and the cache append.  */
+/* [MR] Description, Inputs/positionIds and Attributes: multimodal RoPE     */
+/* with three position streams (t, h, w) that mrope_section / mrope_layout  */
+/* assign to the half-rotary indices, the scale applied to the gathered     */
+/* coefficient, and pairs whose stream position is out of range copied     */
+/* through. [SA] Description, Inputs and Attributes: Q and K rotated in one */
+/* pass for grouped-query heads, K and V appended to the caches. [PR] Qwen3 */
+/* Architecture: QK-Norm (RMSNorm on Q and K) before the rotary step.       */
+/* Reading: every Q and K head is rotated exactly as oracle_mrope_map       */
+/* rotates one head of a rank-3 X with the token's three positions          */
+/* pos3[k, b, s]; with q_weight and k_weight the head is first normalised   */
+/* as in oracle_rope_qkv_rmsnorm; the cache append, the k_out form and V    */
+/* are those of oracle_rope_qkv. Positions are required (three streams      */
+/* cannot follow from the past lengths). *n_oor counts Q and K pairs copied */
+/* through (in the K heads that are written).                               */
+/* ------------------------------------------------------------------------ */
+int oracle_mrope_qkv(int dt, int64_t B, int64_t S, int64_t Nq, int64_t Nkv, int64_t H, int interleaved,
+                     int64_t rotary_dim, const void* q, const void* k, const void* v,
+                     const void* q_weight, const void* k_weight, double eps, const void* cos_t,
+                     const void* sin_t, int64_t cache_rows, const int64_t* pos3, const int32_t* sec,
+                     int layout, float scale, const int32_t* past, void* q_out, void* k_out,
+                     void* k_cache, void* v_cache, int64_t max_len, int64_t* n_oor, int64_t* n_skip) {
+  if (pos3 == NULL || sec == NULL || H < 2) return 1;
+  if ((q_weight == NULL) != (k_weight == NULL)) return 1;
+  int64_t rd = rotary_dim ? rotary_dim : H;
+  int64_t half = rd / 2;
+  if (half <= 0 || half > 65536) return 1;
+  uint8_t* map = malloc((size_t)half);
+  if (map == NULL) return 1;
+  int rc = oracle_mrope_stream_map(sec, layout, half, map);
+  if (rc == 0)
+    rc = qkv_core(dt, B, S, Nq, Nkv, H, interleaved, rotary_dim, q, k, v, q_weight, k_weight, eps, cos_t,
+                  sin_t, cache_rows, NULL, pos3, map, scale, past, q_out, k_out, k_cache, v_cache, max_len,
                   n_oor, n_skip);
+  free(map);
+  return rc;
 }

@@ -51,6 +51,10 @@ MUTATIONS = {
     "mrope_fused_scale_dropped": ("c = round_to(dt, c * (double)scale);", "c = round_to(dt, c);"),
     "bf16_exponent_bias": ("v = ldexp((double)(m + 128), e - 134);", "v = ldexp((double)(m + 128), e - 133);"),
     "bf16_rounding_truncates": ("double r = nearbyint(ldexp(a, 7 - E));", "double r = floor(ldexp(a, 7 - E));"),
+    "mrope_qkv_stream_of_pair_ignored": ("const int64_t p = p3[map[i]];", "const int64_t p = p3[0];"),
+    "mrope_qkv_positions_of_wrong_token": ("p3[st3] = pos3[st3 * B * S + tok];", "p3[st3] = pos3[st3 * B * S + b];"),
+    "mrope_qkv_scale_dropped": ("const double c = round_to(dt, ld(dt, cos_t, p * half + i) * (double)scale);",
+                                "const double c = round_to(dt, ld(dt, cos_t, p * half + i));"),
     "qkv_value_rotated": ("for (int64_t j = 0; j < H; ++j) cp(dt, vs, vsrc + j, v_cache, dst + j);",
                           "rope_one_head(dt, interleaved, H, rd, vs, vsrc, v_cache, dst, cos_t, sin_t, crow, valid);"),
 }

@@ -863,3 +863,107 @@ def test_bfloat16_rotation_rounds_once(orc):
                 lo = orc.double_to_bf16(float(exact))
                 # the exact value's nearest bf16 (float(exact) is within 2^-53 relative: no tie shifts)
                 assert int(y[0, s_, j]) == lo
+
+
+# ---------------------------------------------------------------------------
+# M-RoPE Q/K rotation with the cache append (oracle_mrope_qkv): each Q and K head is
+# one head of MRotaryEmbedding ("com.microsoft.MRotaryEmbedding" README, Description,
+# Inputs/positionIds, Attributes); grouped-query heads and the cache as SparseAttention.
+# ---------------------------------------------------------------------------
+
+def test_mrope_qkv_reduces_to_mrope_per_head(orc):
+    """Q heads and K heads equal the pinned M-RoPE oracle run on Q and on K alone, bit for bit:
+    both layouts, both pairings, a partial width, a scale, and pairs whose stream position is
+    out of range (copied through); packed input equals separate input."""
+    rng = np.random.default_rng(81)
+    B, S, Nq, Nkv, H, R = 2, 7, 6, 2, 16, 30
+    for dtype in (np.float16, np.float32):
+        q, k, v, cos8, sin8 = _qkv_inputs(rng, dtype, B, S, Nq, Nkv, H, R)
+        for rd, sec in ((0, (2, 3, 3)), (8, (2, 1, 1))):
+            cos, sin = (cos8, sin8) if rd == 0 else (cos8[:, :rd // 2].copy(), sin8[:, :rd // 2].copy())
+            pos = rng.integers(0, R, (3, B, S))
+            pos[1, 0, 3], pos[2, 1, 6], pos[0, 1, 0] = R, -1, R + 9
+            for layout in (0, 1):
+                for inter in (0, 1):
+                    for scale in (1.0, 0.75):
+                        yq, nq = orc.mrope(q, cos, sin, pos, sec, layout, scale, inter, rd, Nq)
+                        yk, nk = orc.mrope(k, cos, sin, pos, sec, layout, scale, inter, rd, Nkv)
+                        qo, ko, _, _, n_oor, _ = orc.mrope_qkv(q, cos, sin, pos, sec, layout, scale, num_heads=Nq,
+                                                               kv_num_heads=Nkv, key=k, interleaved=inter,
+                                                               rotary_embedding_dim=rd)
+                        assert n_oor == nq + nk > 0
+                        assert np.array_equal(qo.view(np.uint8), yq.view(np.uint8))
+                        assert np.array_equal(ko.view(np.uint8), yk.view(np.uint8))
+                        packed = np.concatenate([q, k, v], axis=-1)
+                        qp, kp, _, _, _, _ = orc.mrope_qkv(packed, cos, sin, pos, sec, layout, scale,
+                                                           num_heads=Nq, kv_num_heads=Nkv, interleaved=inter,
+                                                           rotary_embedding_dim=rd)
+                        assert np.array_equal(qp.view(np.uint8), qo.view(np.uint8))
+                        assert np.array_equal(kp.view(np.uint8), ko.view(np.uint8))
+
+
+def test_mrope_qkv_equal_streams_equal_rope_qkv(orc):
+    """t = h = w and scale 1: the M-RoPE Q/K op is the pinned RotaryEmbedding Q/K op, bit for
+    bit, for every layout (cache mode included, with rows past its end skipped)."""
+    rng = np.random.default_rng(82)
+    B, S, Nq, Nkv, H, R, L = 2, 6, 4, 2, 16, 30, 9
+    q, k, v, cos, sin = _qkv_inputs(rng, np.float16, B, S, Nq, Nkv, H, R)
+    p = rng.integers(0, R, (B, S))
+    p[0, 2] = R + 2
+    pos3 = np.stack([p, p, p])
+    past = np.array([2, 5], dtype=np.int32)
+    kc0 = rng.standard_normal((B, Nkv, L, H)).astype(np.float16)
+    want = orc.rope_qkv(q, cos, sin, p, num_heads=Nq, kv_num_heads=Nkv, key=k, value=v, k_cache=kc0, v_cache=kc0,
+                        past_seq_lens=past)
+    for layout in (0, 1, 2):
+        got = orc.mrope_qkv(q, cos, sin, pos3, (3, 3, 2), layout, 1.0, num_heads=Nq, kv_num_heads=Nkv, key=k,
+                            value=v, k_cache=kc0, v_cache=kc0, past_seq_lens=past)
+        for a, b in zip(got[:4], want[:4]):
+            if a is None:
+                assert b is None
+            else:
+                assert np.array_equal(a.view(np.uint8), b.view(np.uint8))
+        assert got[5] == want[5] > 0
+
+
+def test_mrope_qkv_rmsnorm_cache_rows_and_values(orc):
+    """With QK-RMSNorm: numpy RMSNorm followed by the pinned M-RoPE oracle, bit for bit, on Q
+    and K; in cache mode the rotated K rows sit at past[b] + s, V rows are copies, rows outside
+    [0, max_len) are not written and are counted, every other row is untouched."""
+    rng = np.random.default_rng(83)
+    B, S, Nq, Nkv, H, R, L = 2, 6, 4, 2, 16, 30, 9
+    for dtype in (np.float16, np.float32):
+        q, k, v, cos, sin = _qkv_inputs(rng, dtype, B, S, Nq, Nkv, H, R)
+        q = (q * 3).astype(dtype)
+        wq = rng.uniform(0.5, 1.5, H).astype(dtype)
+        wk = rng.uniform(0.5, 1.5, H).astype(dtype)
+        pos = rng.integers(0, R, (3, B, S))
+        pos[2, 1, 1] = R
+        sec = (2, 3, 3)
+        zq = _rmsnorm_numpy(q, wq, 1e-6, H, dtype)
+        zk = _rmsnorm_numpy(k, wk, 1e-6, H, dtype)
+        yq, _ = orc.mrope(zq, cos, sin, pos, sec, 1, 1.0, 0, 0, Nq)
+        yk, _ = orc.mrope(zk, cos, sin, pos, sec, 1, 1.0, 0, 0, Nkv)
+        past = np.array([0, 5], dtype=np.int32)                # batch 1 runs past the 9-row cache
+        kc0 = rng.standard_normal((B, Nkv, L, H)).astype(dtype)
+        vc0 = rng.standard_normal((B, Nkv, L, H)).astype(dtype)
+        qo, ko, kc, vc, _, n_skip = orc.mrope_qkv(q, cos, sin, pos, sec, 1, 1.0, num_heads=Nq, kv_num_heads=Nkv,
+                                                  key=k, value=v, k_cache=kc0, v_cache=vc0, past_seq_lens=past,
+                                                  q_norm_weight=wq, k_norm_weight=wk, epsilon=1e-6)
+        assert ko is None
+        assert np.array_equal(qo.view(np.uint8), yq.view(np.uint8))
+        written = np.zeros((B, L), bool)
+        for b in range(B):
+            for s in range(S):
+                row = past[b] + s
+                if row >= L:
+                    continue
+                written[b, row] = True
+                assert np.array_equal(kc[b, :, row].view(np.uint8), yk.reshape(B, S, Nkv, H)[b, s].view(np.uint8))
+                assert np.array_equal(vc[b, :, row].view(np.uint8), v.reshape(B, S, Nkv, H)[b, s].view(np.uint8))
+        assert n_skip == int((past[:, None] + np.arange(S)[None, :] >= L).sum()) > 0
+        untouched = ~written
+        assert np.array_equal(kc.transpose(0, 2, 1, 3)[untouched].view(np.uint8),
+                              kc0.transpose(0, 2, 1, 3)[untouched].view(np.uint8))
+        assert np.array_equal(vc.transpose(0, 2, 1, 3)[untouched].view(np.uint8),
+                              vc0.transpose(0, 2, 1, 3)[untouched].view(np.uint8))
