@@ -17,11 +17,11 @@
  *   mrope_apply_stream_map, mrope_apply_fused
  *                     MRotaryEmbedding with an explicit stream per index, and
  *                     with on-the-fly coefficients.
- *   rope_apply_qkv, rope_apply_qkv_rmsnorm
+ *   rope_apply_qkv, rope_apply_qkv_rmsnorm, mrope_apply_qkv
  *                     Q and K rotation for grouped-query attention with the
  *                     key/value cache append ("com.microsoft.SparseAttention"
- *                     README), and with QK-RMSNorm first (the pull request's
- *                     Qwen3 Architecture).
+ *                     README), with QK-RMSNorm first (the pull request's
+ *                     Qwen3 Architecture), and with M-RoPE.
  *   rope_apply_no_alloc  rope_apply for callers that cannot allocate.
  *
  * Conventions shared by every entry point
@@ -371,6 +371,41 @@ typedef enum rope_variant {
 } rope_variant;
 rope_status rope_set_variant(rope_variant variant);
 rope_variant rope_get_variant(void);
+
+/*
+ * mrope_apply_qkv -- rope_apply_qkv with multimodal RoPE: every Q and K head is
+ * rotated exactly as mrope_apply rotates one head of a rank-3 X
+ * ([MRotaryEmbedding README, Description: the three position streams t, h, w;
+ * Inputs/positionIds; Attributes: mrope_section, mrope_layout, scale]), with
+ * the grouped-query heads, packed or separate inputs and the key/value cache
+ * append of rope_apply_qkv ([SparseAttention README, Description, Inputs]) and,
+ * when q_norm_weight and k_norm_weight are given, the RMS normalisation of
+ * rope_apply_qkv_rmsnorm first ([Qwen3 fusion pull request, Qwen3
+ * Architecture: QK-Norm before the rotary step]). The pages describe these
+ * pieces separately; their composition here follows each one unchanged.
+ *
+ * position_ids  device int64 (3, B, S), required: the t, h, w positions of
+ *               every token. A pair whose stream position is outside
+ *               [0, cache_rows) is copied through (the normalised value with
+ *               the norm) and bit 0 of status_flags is set.
+ * mrope_section, mrope_layout, scale  as mrope_apply (rd/2 <= 1024).
+ * q_norm_weight, k_norm_weight  both NULL (no norm) or both device T[head_size];
+ *               epsilon as rope_apply_qkv_rmsnorm.
+ * Every other argument, layout, ownership, status bit and error as
+ * rope_apply_qkv (head_size even; past_seq_lens only says where cache rows go,
+ * positions always come from position_ids). ROPE_ERR_INVALID_ARG also for a
+ * missing section or position_ids, sections that do not sum to rd/2, a layout
+ * other than 0 or 1, or a non-finite scale.
+ */
+rope_status mrope_apply_qkv(rope_dtype dtype, int64_t batch, int64_t seq, int32_t num_heads,
+                            int32_t kv_num_heads, int64_t head_size, const void* query, const void* key,
+                            const void* value, const void* q_norm_weight, const void* k_norm_weight,
+                            float epsilon, const void* cos_cache, const void* sin_cache, int64_t cache_rows,
+                            const int64_t* position_ids, const int32_t* mrope_section, int32_t mrope_layout,
+                            float scale, const int32_t* past_seq_lens, int32_t interleaved,
+                            int32_t rotary_embedding_dim, void* q_out, void* k_out, void* k_cache,
+                            void* v_cache, int64_t max_cache_len, int32_t* status_flags, void* scratch,
+                            rope_stream_t stream);
 
 /*
  * rope_apply_no_alloc -- rope_apply for callers that cannot allocate device

@@ -18,6 +18,7 @@ from .build import LIB_PATH, build_library  # noqa: F401
 __all__ = [
     "RopeError", "load_library", "build_library", "rope_apply", "mrope_apply",
     "mrope_apply_stream_map", "mrope_stream_map", "rope_apply_fused", "rope_cache_build",
+    "rope_apply_qkv", "mrope_apply_qkv",
     "set_variant", "get_variant", "variant",
     "ROPE_OK", "ROPE_ERR_INVALID_ARG", "ROPE_ERR_UNSUPPORTED", "ROPE_ERR_CUDA",
 ]
@@ -55,6 +56,8 @@ SIGNATURES = {
                        _i32, _vp, _vp, _vp, _vp, _i64, _vp, _vp, _vp],
     "rope_apply_qkv_rmsnorm": [_i32, _i64, _i64, _i32, _i32, _i64, _vp, _vp, _vp, _vp, _vp, _f32, _vp, _vp,
                                _i64, _vp, _vp, _i32, _i32, _vp, _vp, _vp, _vp, _i64, _vp, _vp, _vp],
+    "mrope_apply_qkv": [_i32, _i64, _i64, _i32, _i32, _i64, _vp, _vp, _vp, _vp, _vp, _f32, _vp, _vp, _i64, _vp,
+                        _i32p, _i32, _f32, _vp, _i32, _i32, _vp, _vp, _vp, _vp, _i64, _vp, _vp, _vp],
     "rope_apply_no_alloc": [_i32, _i32, _i64p, _vp, _vp, _i32, _i64p, _vp, _vp, _vp, _i32, _i32, _i32, _vp,
                             _vp],
     "rope_set_variant": [_i32],
@@ -337,6 +340,49 @@ def rope_apply_qkv(query, cos_cache, sin_cache, position_ids=None, *, num_heads,
                                     _ptr(k_cache), _ptr(v_cache), int(max_len), _ptr(status), _ptr(scratch),
                                     _stream(query, stream))
     _check("rope_apply_qkv_rmsnorm" if norm else "rope_apply_qkv", st)
+    return q_out, (None if cache else k_out)
+
+
+def mrope_apply_qkv(query, cos_cache, sin_cache, position_ids, mrope_section, *, num_heads, kv_num_heads,
+                    mrope_layout=0, scale=1.0, key=None, value=None, interleaved=0, rotary_embedding_dim=0,
+                    k_cache=None, v_cache=None, past_seq_lens=None, q_out=None, k_out=None, status=None,
+                    q_norm_weight=None, k_norm_weight=None, epsilon=1e-6, stream=None, scratch=None):
+    """rope_apply_qkv with M-RoPE: position_ids is (3, B, S) (t, h, w) and every Q and K
+    head is rotated as mrope_apply rotates a head; optional QK-RMSNorm first. Returns
+    (q_out, k_out); k_out is None in cache mode."""
+    import torch
+
+    lib = load_library()
+    _cuda("query", query)
+    for name, t in (("key", key), ("value", value), ("k_cache", k_cache), ("v_cache", v_cache),
+                    ("cos_cache", cos_cache), ("sin_cache", sin_cache), ("q_norm_weight", q_norm_weight),
+                    ("k_norm_weight", k_norm_weight)):
+        _cuda(name, t, query.dtype)
+    _cuda("position_ids", position_ids, torch.int64)
+    _cuda("past_seq_lens", past_seq_lens, torch.int32)
+    if query.dim() != 3:
+        raise ValueError("query must be (B, S, hidden)")
+    B, S, hidden = query.shape
+    packed = key is None and value is None
+    rows_per_tok = num_heads + (2 * kv_num_heads if packed else 0)
+    if hidden % rows_per_tok:
+        raise ValueError(f"query hidden size {hidden} is not a multiple of {rows_per_tok} heads")
+    H = hidden // rows_per_tok
+    if q_out is None:
+        q_out = torch.empty((B, S, num_heads * H), dtype=query.dtype, device=query.device)
+    cache = k_cache is not None
+    if not cache and k_out is None:
+        k_out = torch.empty((B, S, kv_num_heads * H), dtype=query.dtype, device=query.device)
+    max_len = k_cache.shape[2] if cache else 0
+    sec = (ctypes.c_int32 * 3)(*[int(v) for v in mrope_section])
+    with torch.cuda.device(query.device):
+        st = lib.mrope_apply_qkv(_dtype_code(query), B, S, int(num_heads), int(kv_num_heads), H, _ptr(query),
+                                 _ptr(key), _ptr(value), _ptr(q_norm_weight), _ptr(k_norm_weight), float(epsilon),
+                                 _ptr(cos_cache), _ptr(sin_cache), int(cos_cache.shape[0]), _ptr(position_ids),
+                                 sec, int(mrope_layout), float(scale), _ptr(past_seq_lens), int(interleaved),
+                                 int(rotary_embedding_dim), _ptr(q_out), _ptr(k_out), _ptr(k_cache), _ptr(v_cache),
+                                 int(max_len), _ptr(status), _ptr(scratch), _stream(query, stream))
+    _check("mrope_apply_qkv", st)
     return q_out, (None if cache else k_out)
 
 

@@ -906,10 +906,12 @@ rope_status qkv_impl(rope_dtype dtype, int64_t batch, int64_t seq, int32_t num_h
                      const void* sin_cache, int64_t cache_rows, const int64_t* position_ids,
                      const int32_t* past_seq_lens, int32_t interleaved, int32_t rotary_embedding_dim,
                      void* q_out, void* k_out, void* k_cache, void* v_cache, int64_t max_cache_len,
-                     int32_t* status_flags, void* scratch, rope_stream_t stream) {
+                     int32_t* status_flags, void* scratch, rope_stream_t stream,
+                     const int32_t* mrope_section = nullptr, int32_t mrope_layout = 0, float mrope_scale = 1.0f) {
   g_last_error.clear();
   ROPE_TRY(check_dtype(dtype));
   const bool norm = q_weight != nullptr || k_weight != nullptr;
+  const bool mrope = mrope_section != nullptr;
   if (norm && (!q_weight || !k_weight))
     return fail(ROPE_ERR_INVALID_ARG, "RMSNorm needs both q_norm_weight and k_norm_weight");
   if (norm && !(epsilon >= 0.0f && epsilon < INFINITY))
@@ -925,10 +927,17 @@ rope_status qkv_impl(rope_dtype dtype, int64_t batch, int64_t seq, int32_t num_h
   if (interleaved != 0 && interleaved != 1)
     return fail(ROPE_ERR_INVALID_ARG, "interleaved must be 0 or 1 (got %d)", interleaved);
   if (cache_rows < 0) return fail(ROPE_ERR_INVALID_ARG, "cache_rows is negative");
+  uint8_t smap[kMaxMRopeHalf];
   {
     Geom w;
     w.H = head_size;
     ROPE_TRY(rotary_width(rotary_embedding_dim, /*odd_head_ok=*/false, &w));
+    if (mrope) {
+      if (w.h > kMaxMRopeHalf)
+        return fail(ROPE_ERR_UNSUPPORTED, "M-RoPE rotary width / 2 = %lld exceeds %d", (long long)w.h,
+                    kMaxMRopeHalf);
+      ROPE_TRY(build_stream_map(mrope_section, mrope_layout, w.h, smap));
+    }
   }
   // No tokens: nothing to launch (zero-size tensors may come with NULL pointers).
   if (batch == 0 || seq == 0) return ROPE_OK;
@@ -979,6 +988,7 @@ rope_status qkv_impl(rope_dtype dtype, int64_t batch, int64_t seq, int32_t num_h
     ROPE_TRY(check_elem_ptr(cos_cache, "cos_cache", es));
     ROPE_TRY(check_elem_ptr(sin_cache, "sin_cache", es));
   }
+  if (mrope) ROPE_TRY(check_elem_ptr(position_ids, "position_ids (3, B, S)", 8));
   if (position_ids) ROPE_TRY(check_elem_ptr(position_ids, "position_ids", 8));
   if (past_seq_lens) ROPE_TRY(check_elem_ptr(past_seq_lens, "past_seq_lens", 4));
   if (norm) {
@@ -990,7 +1000,8 @@ rope_status qkv_impl(rope_dtype dtype, int64_t batch, int64_t seq, int32_t num_h
 
   const bool vec = vector_ok(g, es, {query, key, value, q_out, k_out, k_cache, v_cache, cos_cache, sin_cache,
                                      q_weight, k_weight});
-  const void* fn = qkv_kernel(dtype, vec, interleaved != 0, position_ids == nullptr, norm);
+  const void* fn = mrope ? mrope_qkv_kernel(dtype, vec, interleaved != 0, norm)
+                         : qkv_kernel(dtype, vec, interleaved != 0, position_ids == nullptr, norm);
   KParams kp;
   memset(&kp, 0, sizeof(kp));
   kp.x = query;
@@ -1001,6 +1012,11 @@ rope_status qkv_impl(rope_dtype dtype, int64_t batch, int64_t seq, int32_t num_h
   kp.oor_flag = status_flags;
   kp.cache_rows = cache_rows;
   kp.sched = static_cast<unsigned long long*>(scratch);
+  if (mrope) {
+    kp.scale = mrope_scale;
+    kp.scale_is_one = mrope_scale == 1.0f;
+    for (int64_t i = 0; i < g.h; ++i) kp.smap[i >> 4] |= (uint32_t)smap[i] << ((i & 15) * 2);
+  }
   QKVParams qa;
   memset(&qa, 0, sizeof(qa));
   qa.k = key;
@@ -1018,7 +1034,7 @@ rope_status qkv_impl(rope_dtype dtype, int64_t batch, int64_t seq, int32_t num_h
   qa.kw = k_weight;
   qa.eps = epsilon;
   const int64_t n_all = (int64_t)num_heads + 2 * kv_num_heads;
-  if (qkv_tma_eligible(g, es, vec, norm, n_all, cache ? max_cache_len : 0, packed_numel * es)) {
+  if (!mrope && qkv_tma_eligible(g, es, vec, norm, n_all, cache ? max_cache_len : 0, packed_numel * es)) {
     const void* tfn = qkv_tma_kernel(dtype, interleaved != 0, position_ids == nullptr, norm);
     QkvTmaLaunch T;
     KParams tk = kp;
@@ -1081,6 +1097,27 @@ rope_status rope_apply_qkv_rmsnorm(rope_dtype dtype, int64_t batch, int64_t seq,
                   k_norm_weight, epsilon, cos_cache, sin_cache, cache_rows, position_ids, past_seq_lens,
                   interleaved, rotary_embedding_dim, q_out, k_out, k_cache, v_cache, max_cache_len,
                   status_flags, scratch, stream);
+}
+
+rope_status mrope_apply_qkv(rope_dtype dtype, int64_t batch, int64_t seq, int32_t num_heads,
+                            int32_t kv_num_heads, int64_t head_size, const void* query, const void* key,
+                            const void* value, const void* q_norm_weight, const void* k_norm_weight,
+                            float epsilon, const void* cos_cache, const void* sin_cache, int64_t cache_rows,
+                            const int64_t* position_ids, const int32_t* mrope_section, int32_t mrope_layout,
+                            float scale, const int32_t* past_seq_lens, int32_t interleaved,
+                            int32_t rotary_embedding_dim, void* q_out, void* k_out, void* k_cache,
+                            void* v_cache, int64_t max_cache_len, int32_t* status_flags, void* scratch,
+                            rope_stream_t stream) {
+  g_last_error.clear();
+  if (!mrope_section) return fail(ROPE_ERR_INVALID_ARG, "mrope_section is NULL");
+  if (batch > 0 && seq > 0 && !position_ids)
+    return fail(ROPE_ERR_INVALID_ARG, "position_ids (3, B, S) are required");
+  if (!(scale == scale) || scale == INFINITY || scale == -INFINITY)
+    return fail(ROPE_ERR_INVALID_ARG, "scale must be finite");
+  return qkv_impl(dtype, batch, seq, num_heads, kv_num_heads, head_size, query, key, value, q_norm_weight,
+                  k_norm_weight, epsilon, cos_cache, sin_cache, cache_rows, position_ids, past_seq_lens,
+                  interleaved, rotary_embedding_dim, q_out, k_out, k_cache, v_cache, max_cache_len, status_flags,
+                  scratch, stream, mrope_section, mrope_layout, scale);
 }
 
 rope_status rope_cache_build(rope_dtype dtype, const float* inv_freq, int32_t half, int64_t rows,

@@ -80,6 +80,9 @@ const void* fused_kernel(int dtype, bool vec, bool interleaved, bool rank4, bool
 const void* cache_build_kernel(int dtype);
 // rope_qkv_kernel instance; its launch takes (KParams, QKVParams).
 const void* qkv_kernel(int dtype, bool vec, bool interleaved, bool implicit_pos, bool rms_norm);
+// The M-RoPE instance of rope_qkv_kernel (positions (3, B, S), KParams.smap /
+// scale as for mrope_apply); same launch.
+const void* mrope_qkv_kernel(int dtype, bool vec, bool interleaved, bool rms_norm);
 // Records the message rope_last_error() returns on the calling thread.
 void set_last_error(const char* msg);
 

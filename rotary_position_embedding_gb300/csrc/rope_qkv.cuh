@@ -75,8 +75,53 @@ __device__ __forceinline__ VecT<T, V> norm_weight(const VecT<T, V>& x, float r, 
 #ifndef ROPE_QKV_NORM_HOIST
 #define ROPE_QKV_NORM_HOIST 1
 #endif
-#define ROPE_QKV_BOUNDS __maxnreg__(NORM ? ROPE_QKV_NORM_MAXNREG : ROPE_QKV_MAXNREG)
-template <class T, int V, bool INTER, bool IMPLICIT, bool NORM>
+// M-RoPE heads gather three coefficient rows per unit: their own cap.
+#ifndef ROPE_QKV_MROPE_MAXNREG
+#define ROPE_QKV_MROPE_MAXNREG 64
+#endif
+#define ROPE_QKV_BOUNDS \
+  __maxnreg__(MROPE ? ROPE_QKV_MROPE_MAXNREG : (NORM ? ROPE_QKV_NORM_MAXNREG : ROPE_QKV_MAXNREG))
+
+// M-RoPE rotation of one unit of a Q or K head ("com.microsoft.MRotaryEmbedding"
+// README, Inputs/positionIds and Attributes): each of the unit's V coefficient
+// indices follows its stream's position pos3[stream, token]; a pair whose
+// position is outside the table is copied through (and reported in *oor);
+// the gathered coefficients are scaled and rounded to T first. The general
+// per-pair form (mrope_unit_general): these kernels serve the inputs the
+// pipelined kernel does not take.
+template <class T, int V, bool INTER>
+__device__ __forceinline__ void mrope_qkv_unit(const KParams& p, int64_t tok, int k, const VecT<T, V>& a,
+                                               const VecT<T, V>& bv, VecT<T, V>& ya, VecT<T, V>& yb,
+                                               bool& oor) {
+  using VT = VecT<T, V>;
+  using bits = typename Elem<T>::bits;
+  const int oc = k * V;
+  const uint32_t word = p.smap[oc >> 4];
+  const uint32_t um = (word >> ((oc & 15) * 2)) & (uint32_t)((1ull << (2 * V)) - 1);
+  uint32_t present = 0, valid = 0;
+#pragma unroll
+  for (int j = 0; j < V; ++j) present |= 1u << ((um >> (2 * j)) & 3);
+  const bits* cosb = static_cast<const bits*>(p.cos);
+  const bits* sinb = static_cast<const bits*>(p.sin);
+  VT cs[3], ss[3];
+#pragma unroll
+  for (int st = 0; st < 3; ++st) {
+    cs[st] = VT{};
+    ss[st] = VT{};
+    if (present & (1u << st)) {
+      const int64_t ps = __ldg(p.pos + st * p.ntok + tok);
+      if ((uint64_t)ps < (uint64_t)p.cache_rows) {
+        valid |= 1u << st;
+        cs[st] = ld_shared_ro(reinterpret_cast<const VT*>(cosb + ps * p.h + oc));
+        ss[st] = ld_shared_ro(reinterpret_cast<const VT*>(sinb + ps * p.h + oc));
+      }
+    }
+  }
+  if (present & ~valid) oor = true;
+  mrope_unit_general<T, V, INTER>(a, bv, cs, ss, um, valid, !p.scale_is_one, p.scale, ya, yb);
+}
+
+template <class T, int V, bool INTER, bool IMPLICIT, bool NORM, bool MROPE = false>
 __global__ void ROPE_QKV_BOUNDS rope_qkv_kernel(const KParams p, const QKVParams a) {
   using VT = VecT<T, V>;
   using bits = typename Elem<T>::bits;
@@ -148,12 +193,14 @@ __global__ void ROPE_QKV_BOUNDS rope_qkv_kernel(const KParams p, const QKVParams
     if (yr) {
       bool valid = false;
       int64_t crow = 0;
-      if (rotates) {
+      if (rotates && !MROPE) {
         const int64_t pp = IMPLICIT ? past + s : __ldg(p.pos + tok);
         valid = (uint64_t)pp < (uint64_t)p.cache_rows;
         if (!valid && role == 0 && hd == 0 && k0 == 0) flag_oor(p.oor_flag);
         crow = pp * p.h;
       }
+      if (MROPE) valid = rotates;  // out-of-range streams are handled pair by pair
+      bool oor = false;
       if (NORM && rotates) {
         // at most one unit per lane; lanes past the row's units add zeros
         const bool has = k0 < p.U;
@@ -174,7 +221,7 @@ __global__ void ROPE_QKV_BOUNDS rope_qkv_kernel(const KParams p, const QKVParams
           wa = ld_shared_ro(reinterpret_cast<const VT*>(w + oa));
           if (!tail) {
             wb = ld_shared_ro(reinterpret_cast<const VT*>(w + ob));
-            if (valid) {
+            if (valid && !MROPE) {
               const int oc = k0 * V;
               c = ld_shared_ro(reinterpret_cast<const VT*>(cosb + crow + oc));
               sn = ld_shared_ro(reinterpret_cast<const VT*>(sinb + crow + oc));
@@ -190,7 +237,7 @@ __global__ void ROPE_QKV_BOUNDS rope_qkv_kernel(const KParams p, const QKVParams
           wa = ld_shared_ro(reinterpret_cast<const VT*>(w + oa));
           if (!tail) {
             wb = ld_shared_ro(reinterpret_cast<const VT*>(w + ob));
-            if (valid) {
+            if (valid && !MROPE) {
               const int oc = k0 * V;
               c = ld_shared_ro(reinterpret_cast<const VT*>(cosb + crow + oc));
               sn = ld_shared_ro(reinterpret_cast<const VT*>(sinb + crow + oc));
@@ -206,7 +253,10 @@ __global__ void ROPE_QKV_BOUNDS rope_qkv_kernel(const KParams p, const QKVParams
             const VT zb = norm_weight<T, V>(xb, r, wb);
             if (valid) {
               VT ya, yb;
-              rotate_unit<T, V, INTER>(za, zb, c, sn, ya, yb);
+              if (MROPE)
+                mrope_qkv_unit<T, V, INTER>(p, tok, k0, za, zb, ya, yb, oor);
+              else
+                rotate_unit<T, V, INTER>(za, zb, c, sn, ya, yb);
               st_stream(reinterpret_cast<VT*>(yr + oa), ya);
               st_stream(reinterpret_cast<VT*>(yr + ob), yb);
             } else {  // out-of-range position: the normalised head passes through
@@ -231,15 +281,20 @@ __global__ void ROPE_QKV_BOUNDS rope_qkv_kernel(const KParams p, const QKVParams
             st_stream(reinterpret_cast<VT*>(yr + ob), xb);
             continue;
           }
-          const int oc = k * V;
-          const VT c = ld_shared_ro(reinterpret_cast<const VT*>(cosb + crow + oc));
-          const VT sn = ld_shared_ro(reinterpret_cast<const VT*>(sinb + crow + oc));
           VT ya, yb;
-          rotate_unit<T, V, INTER>(xa, xb, c, sn, ya, yb);
+          if (MROPE) {
+            mrope_qkv_unit<T, V, INTER>(p, tok, k, xa, xb, ya, yb, oor);
+          } else {
+            const int oc = k * V;
+            const VT c = ld_shared_ro(reinterpret_cast<const VT*>(cosb + crow + oc));
+            const VT sn = ld_shared_ro(reinterpret_cast<const VT*>(sinb + crow + oc));
+            rotate_unit<T, V, INTER>(xa, xb, c, sn, ya, yb);
+          }
           st_stream(reinterpret_cast<VT*>(yr + oa), ya);
           st_stream(reinterpret_cast<VT*>(yr + ob), yb);
         }
       }
+      if (MROPE && oor && role == 0) flag_oor(p.oor_flag);
     }
     s += p.step_s;
     b += p.step_b;

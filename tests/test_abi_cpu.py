@@ -30,7 +30,7 @@ def test_header_declares_the_abi():
     for name in ("rope_apply", "mrope_apply", "mrope_apply_stream_map", "mrope_stream_map",
                  "rope_apply_fused", "rope_cache_build", "rope_status_string", "rope_last_error",
                  "rope_set_variant", "rope_get_variant", "rope_last_kernel", "rope_apply_no_alloc",
-                 "rope_apply_qkv", "rope_apply_qkv_rmsnorm", "mrope_apply_fused"):
+                 "rope_apply_qkv", "rope_apply_qkv_rmsnorm", "mrope_apply_fused", "mrope_apply_qkv"):
         assert name in fns
 
 
@@ -301,3 +301,44 @@ def test_mrope_apply_fused_rejects_before_launch(lib, kw, status):
     st = _mrope_fused(so, **kw)
     assert st == status, so.rope_last_error().decode()
     assert so.rope_last_error().decode() != ""
+
+
+def _mqkv(so, **kw):
+    a = dict(dtype=F16, B=2, S=4, nq=8, nkv=2, H=16, q=FAKE, k=FAKE2, v=None, qw=None, kw_=None, eps=1e-6,
+             cos=FAKE3, sin=FAKE3, rows=32, pos=FAKE4, sec=(2, 3, 3), layout=1, scale=1.0, past=None, inter=0,
+             rd=0, q_out=ctypes.c_void_p(0x50000), k_out=ctypes.c_void_p(0x60000), kc=None, vc=None, max_len=0,
+             flag=None, scratch=None, stream=None)
+    a.update(kw)
+    sec = None if a["sec"] is None else (ctypes.c_int32 * 3)(*a["sec"])
+    return so.mrope_apply_qkv(a["dtype"], a["B"], a["S"], a["nq"], a["nkv"], a["H"], a["q"], a["k"], a["v"],
+                              a["qw"], a["kw_"], a["eps"], a["cos"], a["sin"], a["rows"], a["pos"], sec,
+                              a["layout"], a["scale"], a["past"], a["inter"], a["rd"], a["q_out"], a["k_out"],
+                              a["kc"], a["vc"], a["max_len"], a["flag"], a["scratch"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(sec=None), INVALID),                           # the section is required
+    (dict(pos=None), INVALID),                           # so are the three position streams
+    (dict(sec=(2, 3, 2)), INVALID),                      # sections must sum to rd/2
+    (dict(sec=(-1, 5, 4)), INVALID),
+    (dict(layout=2), INVALID),
+    (dict(scale=float("nan")), INVALID),
+    (dict(scale=float("inf")), INVALID),
+    (dict(qw=ctypes.c_void_p(0xb0000)), INVALID),        # a norm needs both weights
+    (dict(nkv=3), INVALID),                              # the rope_apply_qkv contract still holds
+    (dict(H=15), INVALID),
+    (dict(rd=8, sec=(2, 3, 3)), INVALID),                # rd 8: sections must sum to 4
+    (dict(pos=ctypes.c_void_p(0x40004)), INVALID),       # misaligned int64 positions
+    (dict(dtype=99), UNSUPPORTED),
+])
+def test_mrope_apply_qkv_rejects_before_launch(lib, kw, status):
+    so = lib.load_library()
+    st = _mqkv(so, **kw)
+    assert st == status, so.rope_last_error().decode()
+    assert so.rope_last_error().decode() != ""
+
+
+def test_mrope_apply_qkv_empty_launches_nothing(lib):
+    so = lib.load_library()
+    assert _mqkv(so, B=0, pos=None) == OK
+    assert _mqkv(so, S=0, pos=None, q=None, k=None, q_out=None) == OK

@@ -1,0 +1,127 @@
+"""GPU parity for mrope_apply_qkv (M-RoPE Q/K rotation with grouped-query heads, the
+optional QK-RMSNorm and the key/value cache append) against oracle_mrope_qkv, through
+the C ABI.
+
+Sources: "com.microsoft.MRotaryEmbedding" README (Description, Inputs/positionIds,
+Attributes); "com.microsoft.SparseAttention" README (Description, Inputs); onnxruntime PR
+"Add RotaryEmbedding fusion for Qwen3 on-the-fly RoPE patterns" (Qwen3 Architecture).
+
+Every case spans several CTAs with a ragged tail of tokens, pairs whose stream position is
+out of range (copied through), and in cache mode rows past the end of the cache (skipped).
+The bar is the one every parity test here uses: pass-through elements bit-exact, rotated
+float32 within 1e-5, float16 / bfloat16 within 1 ulp; with the norm, the bound derived in
+test_gpu_qkv.compare_norm.
+"""
+
+import itertools
+
+import numpy as np
+import pytest
+
+from parity_util import BF16, cast, compare, mrope_passthrough_mask
+from test_gpu_qkv import _dev, _heads, _host, compare_norm
+
+pytestmark = pytest.mark.gpu
+
+NPDT = {"f16": np.float16, "f32": np.float32, "bf16": BF16}
+
+
+def _run(lib, orc, torch, cuda, dt, packed, cache, inter, rot, layout, norm, H=64, Nq=8, Nkv=2, B=3, S=37, R=64,
+         L=80, scale=1.0, seed=0, variant="auto", kernel="rope_qkv_kernel", dynamic=False, past=None):
+    rng = np.random.default_rng(2000 + seed)
+    npdt = NPDT[dt]
+    rd = 0 if rot == "full" else H // 2
+    rdw = rd or H
+    h = rdw // 2
+    sec = {32: (8, 12, 12), 16: (4, 6, 6), 64: (16, 24, 24), 8: (2, 3, 3), 6: (2, 2, 2), 3: (1, 1, 1)}[h]
+    Ntot = Nq + 2 * Nkv
+    x = rng.standard_normal((B, S, Ntot * H))
+    if norm:
+        x = x * rng.uniform(0.1, 10.0, (B, S, Ntot, 1)).repeat(H, -1).reshape(B, S, Ntot * H)
+    qkv = cast(x, npdt)
+    q, k, v = _heads(qkv, B, S, 0, Nq, Ntot, H), _heads(qkv, B, S, Nq, Nq + Nkv, Ntot, H), \
+        _heads(qkv, B, S, Nq + Nkv, Ntot, Ntot, H)
+    theta = rng.uniform(-np.pi, np.pi, (R, h))
+    cos, sin = cast(np.cos(theta), npdt), cast(np.sin(theta), npdt)
+    pos = rng.integers(0, R, (3, B, S))
+    pos[0, 0, 5], pos[1, 1, 0], pos[2, -1, -1], pos[1, 0, 9] = R + 3, -1, R, 2 ** 40
+    past = np.array([0, 11, 50], dtype=np.int32)[:B] if past is None else np.asarray(past, dtype=np.int32)
+    nkw = {}
+    if norm:
+        nkw = dict(q_norm_weight=cast(rng.uniform(0.5, 2.0, H), npdt), k_norm_weight=cast(rng.uniform(0.5, 2.0, H),
+                                                                                        npdt), epsilon=1e-6)
+    kc0 = cast(rng.standard_normal((B, Nkv, L, H)), npdt) if cache else None
+    vc0 = cast(rng.standard_normal((B, Nkv, L, H)), npdt) if cache else None
+    q_ref, k_ref, kc_ref, vc_ref, n_oor, n_skip = orc.mrope_qkv(
+        qkv if packed else q, cos, sin, pos, sec, layout, scale, num_heads=Nq, kv_num_heads=Nkv,
+        key=None if packed else k, value=None if (packed or not cache) else v, interleaved=inter,
+        rotary_embedding_dim=rd, k_cache=kc0, v_cache=vc0, past_seq_lens=past if cache else None, **nkw)
+    assert n_oor > 0 and (n_skip > 0) == bool(cache)
+
+    dv = lambda a: None if a is None else _dev(a, torch, cuda)  # noqa: E731
+    status = torch.zeros(1, dtype=torch.int32, device=cuda)
+    kc_d, vc_d = dv(kc0), dv(vc0)
+    scratch = torch.zeros(8, dtype=torch.int64, device=cuda) if dynamic else None
+    dkw = {kk: (dv(vv) if isinstance(vv, np.ndarray) else vv) for kk, vv in nkw.items()}
+    with lib.variant(variant):
+        qo, ko = lib.mrope_apply_qkv(dv(qkv if packed else q), dv(cos), dv(sin), _dev(pos, torch, cuda), sec,
+                                     mrope_layout=layout, scale=scale, num_heads=Nq, kv_num_heads=Nkv,
+                                     key=None if packed else dv(k), value=None if (packed or not cache) else dv(v),
+                                     interleaved=inter, rotary_embedding_dim=rd, k_cache=kc_d, v_cache=vc_d,
+                                     past_seq_lens=_dev(past, torch, cuda) if cache else None, status=status,
+                                     scratch=scratch, **dkw)
+    torch.cuda.synchronize()
+    assert lib.last_kernel() == kernel
+    if dynamic:
+        assert not bool(scratch.any())
+    assert int(status.item()) == 1 | (4 if n_skip else 0)
+    smap = orc.mrope_stream_map(sec, layout, h)
+    cmp = (lambda got, ref, src, N: compare_norm(got, ref, N, H, rdw, inter)) if norm else \
+        (lambda got, ref, src, N: compare(got, ref, src, 3, N,
+                                          mrope_passthrough_mask(got.shape, 3, N, rd, pos, R, smap, inter)))
+    cmp(_host(qo), q_ref, q, Nq)
+    if not cache:
+        cmp(_host(ko), k_ref, k, Nkv)
+        return
+    assert ko is None
+    # V rows are copies and every other row of both caches keeps its bits
+    assert np.array_equal(_host(vc_d).view(np.uint8), vc_ref.view(np.uint8))
+    kc_g = _host(kc_d)
+    written = np.zeros((B, L), dtype=bool)
+    rows = []
+    for b in range(B):
+        for s in range(S):
+            row = past[b] + s
+            if 0 <= row < L:
+                written[b, row] = True
+                rows.append((b, s, row))
+    assert np.array_equal(kc_g.transpose(0, 2, 1, 3)[~written].view(np.uint8),
+                          kc0.transpose(0, 2, 1, 3)[~written].view(np.uint8))
+    # the written K rows, as a (1, n_rows, Nkv*H) sequence, against the oracle's rows
+    got = np.stack([kc_g[b, :, row].reshape(-1) for b, s, row in rows])[None]
+    ref = np.stack([kc_ref[b, :, row].reshape(-1) for b, s, row in rows])[None]
+    if norm:
+        compare_norm(got, ref, Nkv, H, rdw, inter)
+    else:
+        src = np.stack([k.reshape(B, S, Nkv * H)[b, s] for b, s, row in rows])[None]
+        p_rows = np.stack([pos[:, b, s] for b, s, row in rows], axis=1)[:, None, :]
+        compare(got, ref, src, 3, Nkv, mrope_passthrough_mask(got.shape, 3, Nkv, rd, p_rows, R, smap, inter))
+
+
+GRID = list(itertools.product(["f16", "f32", "bf16"], [0, 1], [0, 1], [0, 1], ["full", "partial"], [0, 1], [0, 1]))
+
+
+@pytest.mark.parametrize("dt,packed,cache,inter,rot,layout,norm", GRID)
+def test_mrope_qkv_grid(lib, orc, cuda, dt, packed, cache, inter, rot, layout, norm):
+    import torch
+
+    _run(lib, orc, torch, cuda, dt, packed, cache, inter, rot, layout, norm,
+         scale=0.75 if (inter + layout) % 2 else 1.0, seed=GRID.index((dt, packed, cache, inter, rot, layout, norm)))
+
+
+@pytest.mark.parametrize("dt,H", [("f16", 12), ("f32", 6)])
+def test_mrope_qkv_scalar_path(lib, orc, cuda, dt, H):
+    """Head rows that are not whole 16-byte vectors: the single-element path."""
+    import torch
+
+    _run(lib, orc, torch, cuda, dt, 1, 1, 0, "full", 1, 0, H=H, seed=H)
