@@ -45,7 +45,7 @@ KERNEL_SOURCES = {
     "rope_fused_kernel": ["rope_kernels.cuh", "rope_fused.cuh", "k_fused.cu"],
     "rope_qkv_kernel": ["rope_kernels.cuh", "rope_qkv.cuh", "k_qkv.cu"],
     "rope_qkv_tma_kernel": ["rope_kernels.cuh", "rope_tma.cuh", "rope_qkv.cuh", "rope_packed.cuh", "rope_qkv_tma.cuh",
-                            "k_qkv_tma.cu"],
+                            "k_qkv_tma.cu", "k_mrope_qkv_tma.cu"],
 }
 
 

@@ -490,27 +490,44 @@ bool qkv_tma_eligible(const Geom& g, int es, bool vec, bool norm, int64_t n_all,
 // Tile shape, stage layout, grid and tensor maps; ROPE_ERR_UNSUPPORTED (no
 // message) when the shape does not fit, and the caller takes the SIMT kernel.
 rope_status plan_qkv_tma(rope_dtype dt, const Geom& g, int es, const QKVParams& a, const void* query,
-                         const void* q_out, const void* fn, QkvTmaLaunch* T) {
+                         const void* q_out, const void* fn, bool mrope, QkvTmaLaunch* T) {
   const int V = 16 / es;
   const int64_t nP = g.h / V;
+  const int64_t slots = mrope ? 3 : 1;  // cos/sin rows per token: one per position stream
   QTParams& tp = T->tp;
   memset(&tp, 0, sizeof(tp));
   memset(&T->maps, 0, sizeof(T->maps));
-  // tokens: each gather lane holds one token's position, and a tile's cos/sin
-  // rows fit the gather warp's kMaxGather bulk copies per lane (kMaxGather
-  // bounds rows here, 16-byte pieces in the RoPE pipeline)
+  // tokens: each gather lane holds one token's position(s), and a tile's
+  // cos/sin rows fit the gather warp's kMaxGather bulk copies per lane
+  // (kMaxGather bounds rows here, 16-byte pieces in the RoPE pipeline)
   int64_t TS = g.S < ROPE_QKV_TMA_MAX_TS ? g.S : ROPE_QKV_TMA_MAX_TS;
-  while (TS > 1 && TS * 2 > 32 * kMaxGather) --TS;
-  if (TS < 1 || TS > 32 || TS * nP > kTmaConsumers) return ROPE_ERR_UNSUPPORTED;
-  const int64_t tpc = kTmaConsumers / (TS * nP);
-  // heads: a divisor of Nkv (so of Nq) that each column's threads cover with
-  // at most kMaxHeads heads apiece, within the tile budget
-  int64_t NG = 1;
-  for (int64_t d = 1; d <= a.Nkv; ++d) {
-    if (a.Nkv % d) continue;
-    if (d > kMaxHeads * tpc) break;
-    if (d > 1 && d * TS * g.H * es > ROPE_QKV_TMA_TILE_BYTES) break;
-    NG = d;
+  while (TS > 1 && TS * slots * 2 > 32 * kMaxGather) --TS;
+  int64_t K = 0, NG = 1;
+  for (;;) {
+    if (TS < 1 || TS > 32 || TS * nP > kTmaConsumers) return ROPE_ERR_UNSUPPORTED;
+    const int64_t tpc = kTmaConsumers / (TS * nP);
+    // heads: a divisor of Nkv (so of Nq) that each column's threads cover
+    // with at most kMaxHeads heads apiece, within the tile budget
+    NG = 1;
+    for (int64_t d = 1; d <= a.Nkv; ++d) {
+      if (a.Nkv % d) continue;
+      if (d > kMaxHeads * tpc) break;
+      if (d > 1 && d * TS * g.H * es > ROPE_QKV_TMA_TILE_BYTES) break;
+      NG = d;
+    }
+    const uint32_t blk = (uint32_t)(TS * g.H * es);
+    tp.blk_bytes = (blk + 127) / 128 * 128;
+    tp.x_bytes = (uint32_t)NG * blk;
+    tp.coef_off = (uint32_t)NG * tp.blk_bytes;
+    tp.flag_off = tp.coef_off + (uint32_t)(TS * slots * 2 * g.h * es);
+    tp.hdr_off = (tp.flag_off + (uint32_t)TS * 4 + 15) / 16 * 16;
+    tp.stage_bytes = (tp.hdr_off + 16 + 1023) / 1024 * 1024;
+    tp.bar_bytes = 1024;
+    K = (ROPE_QKV_TMA_SMEM_BUDGET - tp.bar_bytes) / tp.stage_bytes;
+    // M-RoPE's three coefficient rows per token make stages larger: fewer
+    // tokens per tile keep three stages in flight
+    if (K >= 3 || TS <= 4) break;
+    TS -= 4;
   }
   tp.TS = (int32_t)TS;
   tp.NG = (int32_t)NG;
@@ -523,15 +540,6 @@ rope_status plan_qkv_tma(rope_dtype dt, const Geom& g, int es, const QKVParams& 
   tp.nT = (int32_t)((g.H - g.rd) / V);
   tp.ntiles = g.B * (int64_t)tp.s_tiles * tp.G;
   if (tp.ntiles >= INT32_MAX) return ROPE_ERR_UNSUPPORTED;
-  const uint32_t blk = (uint32_t)(TS * g.H * es);
-  tp.blk_bytes = (blk + 127) / 128 * 128;
-  tp.x_bytes = (uint32_t)NG * blk;
-  tp.coef_off = (uint32_t)NG * tp.blk_bytes;
-  tp.flag_off = tp.coef_off + (uint32_t)(TS * 2 * g.h * es);
-  tp.hdr_off = (tp.flag_off + (uint32_t)TS * 4 + 15) / 16 * 16;
-  tp.stage_bytes = (tp.hdr_off + 16 + 1023) / 1024 * 1024;
-  tp.bar_bytes = 1024;
-  int64_t K = (ROPE_QKV_TMA_SMEM_BUDGET - tp.bar_bytes) / tp.stage_bytes;
   if (K > ROPE_TMA_MAX_STAGES) K = ROPE_TMA_MAX_STAGES;
   if (K < 2) return ROPE_ERR_UNSUPPORTED;
   tp.K = (int32_t)K;
@@ -1034,16 +1042,18 @@ rope_status qkv_impl(rope_dtype dtype, int64_t batch, int64_t seq, int32_t num_h
   qa.kw = k_weight;
   qa.eps = epsilon;
   const int64_t n_all = (int64_t)num_heads + 2 * kv_num_heads;
-  if (!mrope && qkv_tma_eligible(g, es, vec, norm, n_all, cache ? max_cache_len : 0, packed_numel * es)) {
-    const void* tfn = qkv_tma_kernel(dtype, interleaved != 0, position_ids == nullptr, norm);
+  if (qkv_tma_eligible(g, es, vec, norm, n_all, cache ? max_cache_len : 0, packed_numel * es)) {
+    const void* tfn = mrope ? mrope_qkv_tma_kernel(dtype, interleaved != 0, norm)
+                            : qkv_tma_kernel(dtype, interleaved != 0, position_ids == nullptr, norm);
     QkvTmaLaunch T;
     KParams tk = kp;
+    tk.ntok = g.ntok;  // M-RoPE: stream k of token t is position_ids[k * ntok + t]
     tk.S = g.S;
     tk.H = g.H;
     tk.h = (int32_t)g.h;
     tk.rd = (int32_t)g.rd;
     tk.nP = (int32_t)(g.h / (16 / es));
-    const rope_status ts = plan_qkv_tma(dtype, g, es, qa, query, q_out, tfn, &T);
+    const rope_status ts = plan_qkv_tma(dtype, g, es, qa, query, q_out, tfn, mrope, &T);
     if (ts == ROPE_OK) {
       void* targs[] = {&tk, &qa, &T.tp, &T.maps};
       cudaError_t e = launch_pdl(tfn, T.L.grid, T.L.block, T.L.smem, stream, targs);

@@ -93,5 +93,7 @@ const void* tma_kernel(int dtype, bool interleaved, bool rank4, Coef mode);
 // TMA-pipelined Q/K rotation with the cache append (vector path); its launch
 // takes (KParams, QKVParams, QTParams, QKVMaps).
 const void* qkv_tma_kernel(int dtype, bool interleaved, bool implicit_pos, bool rms_norm);
+// Its M-RoPE instances (positions (3, B, S)).
+const void* mrope_qkv_tma_kernel(int dtype, bool interleaved, bool rms_norm);
 
 }  // namespace rope_gb300

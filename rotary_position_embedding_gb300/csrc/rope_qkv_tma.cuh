@@ -145,7 +145,7 @@ __device__ __forceinline__ Unit8<T> norm8p(const float2 (&fx)[4], float r, const
   return z;
 }
 
-template <class T, bool INTER, bool IMPLICIT, bool NORM>
+template <class T, bool INTER, bool IMPLICIT, bool NORM, bool MROPE = false>
 __global__ void __launch_bounds__(kTmaThreads, ROPE_TMA_MIN_CTAS)
     rope_qkv_tma_kernel(const KParams p, const QKVParams a, const QTParams tp,
                         const __grid_constant__ QKVMaps maps) {
@@ -303,29 +303,41 @@ __global__ void __launch_bounds__(kTmaThreads, ROPE_TMA_MIN_CTAS)
     // Row r of a tile's coefficient block (the cos or sin row of token r / 2,
     // row_bytes at byte r*row_bytes) goes to lane r % 32 as one bulk copy.
     const uint32_t row_bytes = (uint32_t)h * (uint32_t)sizeof(bits);
-    const int rows = tp.TS * 2;
+    constexpr int SLOTS = MROPE ? 3 : 1;  // coefficient rows per token: one per position stream
+    const int rows = tp.TS * SLOTS * 2;
+    // M-RoPE: the streams some coefficient index uses (an unused stream's
+    // position never matters, nor does it flag anything)
+    uint32_t used = 1u;
+    if (MROPE) {
+      used = 0u;
+      for (int i = 0; i < h; ++i) used |= 1u << ((p.smap[i >> 4] >> ((i & 15) * 2)) & 3u);
+    }
     const int rounds = (rows + 31) / 32;  // the same for every lane: the shuffles below are warp-wide
     // What a tile needs from global memory -- its positions, or the past
     // length its positions and cache rows start from -- is loaded one tile
     // ahead: under a saturated memory system even these L2 hits take
     // microseconds, and the gather of the tile waits on none.
     struct Pre {
-      int64_t pos;   // explicit position of token `lane`
-      int64_t past;  // past[b]
+      int64_t pos[SLOTS];  // explicit position(s) of token `lane` (M-RoPE: t, h, w)
+      int64_t past;        // past[b]
     };
     auto prefetch = [&](int64_t t) -> Pre {
-      Pre r{0, 0};
+      Pre r{};
       if (t < tp.ntiles) {
         const QTile q = qtile_of(p, tp, t);
         if (a.past && (IMPLICIT || (q.role != 0 && a.cache))) r.past = (int64_t)__ldg(a.past + q.b);
-        if (!IMPLICIT && q.role != 2 && lane < q.n) r.pos = __ldg(p.pos + (int64_t)q.b * p.S + q.s0 + lane);
+        if (!IMPLICIT && q.role != 2 && lane < q.n) {
+          const int64_t tok = (int64_t)q.b * p.S + q.s0 + lane;
+#pragma unroll
+          for (int k = 0; k < SLOTS; ++k) r.pos[k] = __ldg(p.pos + k * p.ntok + tok);
+        }
       }
       return r;
     };
     // Dynamic schedule: the next index is read from its stage header when the
     // copy warp has already published it; otherwise the tile's own values are
     // loaded when it comes up.
-    Pre cur{0, 0};
+    Pre cur{};
     bool have_cur = false;
     if (!p.sched) {
       cur = prefetch(blockIdx.x);
@@ -343,7 +355,7 @@ __global__ void __launch_bounds__(kTmaThreads, ROPE_TMA_MIN_CTAS)
         break;
       }
       if (!have_cur) cur = prefetch(t);
-      Pre nxt{0, 0};
+      Pre nxt{};
       bool have_nxt = false;
       if (!p.sched) {
         nxt = prefetch(t + gridDim.x);  // this CTA's next tile
@@ -361,12 +373,17 @@ __global__ void __launch_bounds__(kTmaThreads, ROPE_TMA_MIN_CTAS)
       unsigned char* st = stage0 + (size_t)s * tp.stage_bytes;
       if (q.role != 0 && a.cache && lane == 0) stage_hdr(s)[1] = cur.past + q.s0;
       if (q.role != 2) {
-        int64_t pp = -1;
-        uint32_t flag = 0;
+        int64_t pp[SLOTS];
+        uint32_t flag = 0;  // bit k: stream k's position is inside the table
+#pragma unroll
+        for (int k = 0; k < SLOTS; ++k) pp[k] = -1;
         if (lane < q.n) {
-          pp = IMPLICIT ? cur.past + q.s0 + lane : cur.pos;
-          flag = (uint64_t)pp < (uint64_t)p.cache_rows ? 1u : 0u;
-          if (!flag && q.role == 0 && q.head0 == 0 && p.oor_flag) atomicOr(p.oor_flag, 1);
+#pragma unroll
+          for (int k = 0; k < SLOTS; ++k) {
+            pp[k] = MROPE ? cur.pos[k] : (IMPLICIT ? cur.past + q.s0 + lane : cur.pos[0]);
+            if ((uint64_t)pp[k] < (uint64_t)p.cache_rows) flag |= 1u << k;
+          }
+          if ((flag & used) != used && q.role == 0 && q.head0 == 0 && p.oor_flag) atomicOr(p.oor_flag, 1);
         }
         if (lane < tp.TS) reinterpret_cast<uint32_t*>(st + tp.flag_off)[lane] = flag;
         const uint32_t coef_addr = smem_addr(st) + tp.coef_off;
@@ -375,11 +392,18 @@ __global__ void __launch_bounds__(kTmaThreads, ROPE_TMA_MIN_CTAS)
 #pragma unroll
         for (int g = 0; g < kMaxGather; ++g) {
           if (g >= rounds) break;
+          // row r: token r / (2*SLOTS), stream (r / 2) % SLOTS, cos or sin (r % 2)
           const int r = lane + 32 * g;
-          const int lt = r < rows ? r >> 1 : 0;
-          // token lt's position lives in lane lt
-          const int64_t row = __shfl_sync(0xffffffffu, pp, lt);
-          const uint32_t ok = __shfl_sync(0xffffffffu, flag, lt);
+          const int lt = r < rows ? r / (2 * SLOTS) : 0;
+          const int k = (r >> 1) % SLOTS;
+          // token lt's positions live in lane lt
+          int64_t row = __shfl_sync(0xffffffffu, pp[0], lt);
+#pragma unroll
+          for (int kk = 1; kk < SLOTS; ++kk) {
+            const int64_t other = __shfl_sync(0xffffffffu, pp[kk], lt);
+            if (k == kk) row = other;
+          }
+          const uint32_t ok = (__shfl_sync(0xffffffffu, flag, lt) >> k) & 1u;
           src[g] = ((r & 1) ? sinb : cosb) + row * h;
           if (r < rows && ok) {
             bytes += row_bytes;
@@ -423,6 +447,17 @@ __global__ void __launch_bounds__(kTmaThreads, ROPE_TMA_MIN_CTAS)
   unit_offsets<V, INTER>(k, h, oa, ob);
   const int oc = k * V;
   const uint32_t blk_elems = tp.blk_bytes / (uint32_t)sizeof(bits);
+  // M-RoPE: the stream of each of the unit's V coefficient indices, and the
+  // masks that merge the three gathered rows word by word
+  uint32_t um = 0, present = 0;
+  uint32_t m0[4] = {0, 0, 0, 0}, m1[4] = {0, 0, 0, 0};
+  if (MROPE) {
+    const uint32_t word = p.smap[oc >> 4];
+    um = (word >> ((oc & 15) * 2)) & (uint32_t)((1ull << (2 * V)) - 1);
+#pragma unroll
+    for (int jj = 0; jj < V; ++jj) present |= 1u << ((um >> (2 * jj)) & 3);
+    stream_masks<V>(um, m0, m1);
+  }
   bool timed_out = false;
   for (int64_t j = 0;; ++j) {
     const int s = (int)(j % tp.K);
@@ -444,12 +479,38 @@ __global__ void __launch_bounds__(kTmaThreads, ROPE_TMA_MIN_CTAS)
     const bool wide = qtile_wide(a, q);
     if (q.role != 2) {
       const uint32_t fl = reinterpret_cast<const uint32_t*>(st + tp.flag_off)[ts];
-      const bool valid = tok_in && (fl & 1u);
+      // M-RoPE rotates every token and puts back the pairs of out-of-range streams
+      const bool valid = tok_in && (MROPE || (fl & 1u));
       VT c{}, sn{};
+      bool blend_on = false;
+      uint32_t ma[4] = {0, 0, 0, 0}, mb[4] = {0, 0, 0, 0};
       if (valid) {
-        const bits* cr = reinterpret_cast<const bits*>(st + tp.coef_off) + (size_t)ts * 2 * h;
-        c = *reinterpret_cast<const VT*>(cr + oc);
-        sn = *reinterpret_cast<const VT*>(cr + h + oc);
+        if (MROPE) {
+          const bits* cr = reinterpret_cast<const bits*>(st + tp.coef_off) + (size_t)ts * 3 * 2 * h;
+          const uint32_t vmask = fl & present;
+          VT cs[3], ss[3];
+#pragma unroll
+          for (int k3 = 0; k3 < 3; ++k3) {
+            cs[k3] = VT{};
+            ss[k3] = VT{};
+            if ((vmask >> k3) & 1u) {
+              cs[k3] = *reinterpret_cast<const VT*>(cr + (size_t)k3 * 2 * h + oc);
+              ss[k3] = *reinterpret_cast<const VT*>(cr + (size_t)k3 * 2 * h + h + oc);
+            }
+          }
+          c = merge3(cs[0], cs[1], cs[2], m0, m1);
+          sn = merge3(ss[0], ss[1], ss[2], m0, m1);
+          if (!p.scale_is_one) {
+            scale_round<T, V>(c, p.scale);
+            scale_round<T, V>(sn, p.scale);
+          }
+          blend_on = vmask != present;
+          if (blend_on) pair_masks<V, INTER>(um, vmask, ma, mb);
+        } else {
+          const bits* cr = reinterpret_cast<const bits*>(st + tp.coef_off) + (size_t)ts * 2 * h;
+          c = *reinterpret_cast<const VT*>(cr + oc);
+          sn = *reinterpret_cast<const VT*>(cr + h + oc);
+        }
       }
       constexpr bool PACKED = sizeof(bits) == 2;  // float16 / bfloat16: packed arithmetic
       VT wa{}, wb{};
@@ -535,6 +596,17 @@ __global__ void __launch_bounds__(kTmaThreads, ROPE_TMA_MIN_CTAS)
             }
             if (valid) {
               rotate8p<T, INTER>(za, zb, cf, sf, ya, yb);
+              if (MROPE && blend_on) {  // pairs of out-of-range streams keep their input
+                VT t0, t1, z0, z1;
+                __builtin_memcpy(&t0, &ya, 16);
+                __builtin_memcpy(&t1, &yb, 16);
+                __builtin_memcpy(&z0, &za, 16);
+                __builtin_memcpy(&z1, &zb, 16);
+                blend(t0, z0, ma);
+                blend(t1, z1, mb);
+                __builtin_memcpy(&ya, &t0, 16);
+                __builtin_memcpy(&yb, &t1, 16);
+              }
             } else {
               ya = za;
               yb = zb;
@@ -559,15 +631,20 @@ __global__ void __launch_bounds__(kTmaThreads, ROPE_TMA_MIN_CTAS)
           for (int u = 0; u < HB; ++u) {
             if (!act[u]) continue;
             VT ya, yb;
+            VT za = xa[u], zb = xb[u];
             if (NORM) {
-              ya = norm_weight<T, V>(xa[u], r[u], wa);
-              yb = norm_weight<T, V>(xb[u], r[u], wb);
-              if (valid) {
-                const VT za = ya, zb = yb;
-                rotate_unit<T, V, INTER>(za, zb, c, sn, ya, yb);
+              za = norm_weight<T, V>(xa[u], r[u], wa);
+              zb = norm_weight<T, V>(xb[u], r[u], wb);
+            }
+            if (valid) {
+              rotate_unit<T, V, INTER>(za, zb, c, sn, ya, yb);
+              if (MROPE && blend_on) {  // pairs of out-of-range streams keep their input
+                blend(ya, za, ma);
+                blend(yb, zb, mb);
               }
             } else {
-              rotate_unit<T, V, INTER>(xa[u], xb[u], c, sn, ya, yb);
+              ya = za;
+              yb = zb;
             }
             *reinterpret_cast<VT*>(sx + ro[u] + oa) = ya;
             *reinterpret_cast<VT*>(sx + ro[u] + ob) = yb;

@@ -111,12 +111,19 @@ def _run(lib, orc, torch, cuda, dt, packed, cache, inter, rot, layout, norm, H=6
 GRID = list(itertools.product(["f16", "f32", "bf16"], [0, 1], [0, 1], [0, 1], ["full", "partial"], [0, 1], [0, 1]))
 
 
+@pytest.mark.parametrize("variant", ["auto", "tma"])
 @pytest.mark.parametrize("dt,packed,cache,inter,rot,layout,norm", GRID)
-def test_mrope_qkv_grid(lib, orc, cuda, dt, packed, cache, inter, rot, layout, norm):
+def test_mrope_qkv_grid(lib, orc, cuda, dt, packed, cache, inter, rot, layout, norm, variant):
+    """At these sizes the automatic choice is the SIMT kernel; forced onto the TMA pipeline
+    every case takes it except the norm with partial rotation (the tail is normalised too).
+    Half of the pipeline cases draw their tiles from a scratch counter."""
     import torch
 
+    case = GRID.index((dt, packed, cache, inter, rot, layout, norm))
+    tma = variant == "tma" and not (norm and rot == "partial")
     _run(lib, orc, torch, cuda, dt, packed, cache, inter, rot, layout, norm,
-         scale=0.75 if (inter + layout) % 2 else 1.0, seed=GRID.index((dt, packed, cache, inter, rot, layout, norm)))
+         scale=0.75 if (inter + layout) % 2 else 1.0, seed=case, variant=variant,
+         kernel="rope_qkv_tma_kernel" if tma else "rope_qkv_kernel", dynamic=tma and case % 2 == 1)
 
 
 @pytest.mark.parametrize("dt,H", [("f16", 12), ("f32", 6)])
@@ -125,3 +132,43 @@ def test_mrope_qkv_scalar_path(lib, orc, cuda, dt, H):
     import torch
 
     _run(lib, orc, torch, cuda, dt, 1, 1, 0, "full", 1, 0, H=H, seed=H)
+
+
+@pytest.mark.parametrize("dt", ["f16", "bf16", "f32"])
+@pytest.mark.parametrize("norm", [0, 1])
+@pytest.mark.parametrize("layout", [0, 1])
+def test_mrope_qkv_tma_bits_equal_simt(lib, cuda, dt, norm, layout):
+    """The two kernels round every value in the same order: Q and both caches agree bit for
+    bit (Qwen2-VL-like heads: 16 Q, 8 K/V, H 128, sections [16, 24, 24])."""
+    import torch
+
+    rng = np.random.default_rng(90 + norm + 2 * layout)
+    npdt = NPDT[dt]
+    B, S, Nq, Nkv, H, R, L = 2, 40, 16, 8, 128, 96, 64
+    Ntot = Nq + 2 * Nkv
+    qkv = cast(rng.standard_normal((B, S, Ntot * H)) * 3, npdt)
+    theta = rng.uniform(-np.pi, np.pi, (R, H // 2))
+    cos, sin = cast(np.cos(theta), npdt), cast(np.sin(theta), npdt)
+    pos = rng.integers(0, R, (3, B, S))
+    pos[1, 0, 3], pos[2, 1, 7] = R, -2
+    past = np.array([5, 30], dtype=np.int32)
+    kw = {}
+    if norm:
+        kw = dict(q_norm_weight=_dev(cast(rng.uniform(0.5, 2.0, H), npdt), torch, cuda),
+                  k_norm_weight=_dev(cast(rng.uniform(0.5, 2.0, H), npdt), torch, cuda), epsilon=1e-6)
+    kc0 = cast(rng.standard_normal((B, Nkv, L, H)), npdt)
+    out = {}
+    for variant in ("simt", "tma"):
+        kc, vc = _dev(kc0, torch, cuda), _dev(kc0, torch, cuda)
+        status = torch.zeros(1, dtype=torch.int32, device=cuda)
+        with lib.variant(variant):
+            qo, _ = lib.mrope_apply_qkv(_dev(qkv, torch, cuda), _dev(cos, torch, cuda), _dev(sin, torch, cuda),
+                                        _dev(pos, torch, cuda), (16, 24, 24), mrope_layout=layout, scale=0.875,
+                                        num_heads=Nq, kv_num_heads=Nkv, k_cache=kc, v_cache=vc,
+                                        past_seq_lens=_dev(past, torch, cuda), status=status, **kw)
+        torch.cuda.synchronize()
+        assert lib.last_kernel() == ("rope_qkv_tma_kernel" if variant == "tma" else "rope_qkv_kernel")
+        out[variant] = [_host(t) for t in (qo, kc, vc)] + [int(status.item())]
+    for a, b in zip(out["simt"][:3], out["tma"][:3]):
+        assert np.array_equal(a.view(np.uint8), b.view(np.uint8))
+    assert out["simt"][3] == out["tma"][3] == (1 | 4)
