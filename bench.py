@@ -231,6 +231,10 @@ class QKVStep:
             self.qw = host_to_torch(torch, inp["q_norm_weight"]).to(device)
             self.kw = host_to_torch(torch, inp["k_norm_weight"]).to(device)
             self.eps = float(w.extra["epsilon"])
+        # M-RoPE: the three position streams and the section
+        self.mrope = w.positions == "mrope"
+        self.pos3 = torch.from_numpy(inp["position_ids"]).to(device) if self.mrope else None
+        self.sec = (ctypes.c_int32 * 3)(*(w.mrope_section or (0, 0, 0)))
         # unfused path: positions past[b] + s and the (b, row) scatter indices
         s_idx = torch.arange(S, device=device, dtype=torch.int64)[None, :]
         self.pos = (self.past.to(torch.int64)[:, None] + s_idx).contiguous()
@@ -245,6 +249,14 @@ class QKVStep:
         w, lib = self.w, self.lib
         vp = ctypes.c_void_p
         scr = self.scratch_for(stream)
+        if fused and self.mrope:
+            nw = (vp(self.qw.data_ptr()), vp(self.kw.data_ptr())) if self.norm else (None, None)
+            return lib.mrope_apply_qkv(
+                self.code, w.batch, w.seq, self.Nq, self.Nkv, self.H, vp(self.xs[k].data_ptr()), None, None,
+                nw[0], nw[1], self.eps if self.norm else 0.0, vp(self.cos.data_ptr()), vp(self.sin.data_ptr()),
+                w.cache_rows, vp(self.pos3.data_ptr()), self.sec, w.mrope_layout, w.scale,
+                vp(self.past.data_ptr()), 0, 0, vp(self.qo[k].data_ptr()), None, vp(self.kc.data_ptr()),
+                vp(self.vc.data_ptr()), w.extra["max_len"], None, scr, stream)
         if fused and self.norm:
             return lib.rope_apply_qkv_rmsnorm(
                 self.code, w.batch, w.seq, self.Nq, self.Nkv, self.H, vp(self.xs[k].data_ptr()), None, None,
@@ -262,6 +274,21 @@ class QKVStep:
                                       w.extra["max_len"], None, scr, stream)
         B, S, H, Nq, Nkv = w.batch, w.seq, self.H, self.Nq, self.Nkv
         x = self.xs[k].view(B, S, Nq + 2 * Nkv, H)
+        if self.mrope:
+            # torch RMSNorm, then M-RoPE on Q and on K (two library calls), then the cache scatter
+            torch = self.torch
+            xf = x[:, :, :Nq + Nkv].float()
+            n = (xf * torch.rsqrt(xf.pow(2).mean(-1, keepdim=True) + self.eps)).to(x.dtype)
+            q = (n[:, :, :Nq] * self.qw).reshape(B, S, Nq * H).contiguous()
+            kk = (n[:, :, Nq:] * self.kw).reshape(B, S, Nkv * H).contiguous()
+            sec = tuple(w.mrope_section)
+            self.rp.mrope_apply(q, self.cos, self.sin, self.pos3, sec, mrope_layout=w.mrope_layout,
+                                num_heads=Nq, out=self.qo[k])
+            kr = self.rp.mrope_apply(kk, self.cos, self.sin, self.pos3, sec, mrope_layout=w.mrope_layout,
+                                     num_heads=Nkv)
+            self.kc[self.bi, :, self.ri] = kr.view(B, S, Nkv, H)
+            self.vc[self.bi, :, self.ri] = x[:, :, Nq + Nkv:]
+            return 0
         if self.norm:
             # QK-Norm as separate torch ops, then the fused rotation + append
             torch = self.torch
@@ -706,7 +733,7 @@ class OracleStep:
             self.x = np.ascontiguousarray(x[:nb, :, :s_keep])
         if pos is None:
             self.pos = None
-        elif w.kind in ("mrope", "mrope_fused"):
+        elif w.positions == "mrope":
             self.pos = np.ascontiguousarray(pos[:, :nb, :s_keep])
         else:
             self.pos = np.ascontiguousarray(pos[:nb, :s_keep])
@@ -721,15 +748,26 @@ class OracleStep:
         self.bytes = wl.algorithmic_bytes(w) * self.tokens / w.tokens
         if w.kind == "qkv":
             self.past = inp["past_seq_lens"][:nb]
+            self.qw, self.kw = inp.get("q_norm_weight"), inp.get("k_norm_weight")
             shape = (nb, w.extra["kv_num_heads"], w.extra["max_len"], w.head_size)
             self.kc, self.vc = np.zeros(shape, dtype), np.zeros(shape, dtype)
 
     def run(self):
         w, o = self.w, self.oracle
-        if w.kind == "qkv":
+        if w.kind == "qkv" and w.positions == "mrope":
+            nkw = {}
+            if w.extra.get("rms_norm"):
+                nkw = dict(q_norm_weight=self.qw, k_norm_weight=self.kw, epsilon=w.extra["epsilon"])
+            o.mrope_qkv(self.x, self.cos, self.sin, self.pos, w.mrope_section, w.mrope_layout, w.scale,
+                        num_heads=w.num_heads, kv_num_heads=w.extra["kv_num_heads"], k_cache=self.kc,
+                        v_cache=self.vc, past_seq_lens=self.past, **nkw)
+        elif w.kind == "qkv":
+            nkw = {}
+            if w.extra.get("rms_norm"):
+                nkw = dict(q_norm_weight=self.qw, k_norm_weight=self.kw, epsilon=w.extra["epsilon"])
             o.rope_qkv(self.x, self.cos, self.sin, None, num_heads=w.num_heads,
                        kv_num_heads=w.extra["kv_num_heads"], k_cache=self.kc, v_cache=self.vc,
-                       past_seq_lens=self.past)
+                       past_seq_lens=self.past, **nkw)
         elif w.kind == "mrope":
             o.mrope(self.x, self.cos, self.sin, self.pos, w.mrope_section, w.mrope_layout, w.scale,
                     w.interleaved, w.rotary_embedding_dim, self.nh)

@@ -149,6 +149,14 @@ WORKLOADS = {
         name="mrope_r3_bf16_layout1", kind="mrope", rank=3, shape=(2, 8192, 28 * 128), dtype="bfloat16",
         num_heads=28, positions="mrope", cache_rows=32768, rope_base=10000.0, rope_dim=128,
         mrope_section=(16, 24, 24), mrope_layout=1, scale=1.0),
+    # M-RoPE Q/K rotation with QK-Norm and the cache append: a Qwen3-VL-8B-like
+    # attention prefill (32 query heads, 8 key/value heads, head size 128,
+    # interleaved sections [24, 20, 20]), t/h/w ids from the M-RoPE recipe
+    "mrope_qkv_norm_prefill_r3_f16": Workload(
+        name="mrope_qkv_norm_prefill_r3_f16", kind="qkv", rank=3, shape=(2, 4096, (32 + 2 * 8) * 128),
+        dtype="float16", num_heads=32, positions="mrope", cache_rows=32768, rope_base=5.0e6, rope_dim=128,
+        mrope_section=(24, 20, 20), mrope_layout=1, scale=1.0,
+        extra={"kv_num_heads": 8, "max_len": 8192, "max_past": 4096, "rms_norm": True, "epsilon": 1e-6}),
     "fused_decode_r3_f16": Workload(
         name="fused_decode_r3_f16", kind="fused", rank=3, shape=(256, 1, 40 * 128), dtype="float16",
         num_heads=40, positions="uniform", cache_rows=32768, rope_base=1.0e6, rope_dim=128,
@@ -285,10 +293,12 @@ def algorithmic_bytes(w: Workload, cached=True):
     esz = itemsize(w.dtype)
     xy = 2 * w.numel * esz
     if w.kind == "qkv":
-        # Q, K, V read once; Q out, K and V into the caches; one cos/sin row
-        # per token; the int32 past lengths (positions are implicit).
+        # Q, K, V read once; Q out, K and V into the caches; rd/2 cosines and
+        # rd/2 sines per token; the int32 past lengths; with M-RoPE the three
+        # int64 position streams (otherwise positions are implicit).
         norm_w = 2 * w.head_size * esz if w.extra.get("rms_norm") else 0
-        return xy + 2 * w.tokens * w.half * esz + 4 * w.batch + norm_w
+        pos = 3 * 8 * w.tokens if w.positions == "mrope" else 0
+        return xy + 2 * w.tokens * w.half * esz + 4 * w.batch + norm_w + pos
     npos = 3 if w.kind in ("mrope", "mrope_fused") else (0 if w.positions == "none" else 1)
     pos = npos * w.tokens * 8
     if w.kind in ("fused", "mrope_fused") and not cached:

@@ -172,3 +172,50 @@ def test_mrope_qkv_tma_bits_equal_simt(lib, cuda, dt, norm, layout):
     for a, b in zip(out["simt"][:3], out["tma"][:3]):
         assert np.array_equal(a.view(np.uint8), b.view(np.uint8))
     assert out["simt"][3] == out["tma"][3] == (1 | 4)
+
+
+def test_mrope_qkv_workload_full_size(lib, orc, cuda):
+    """The benchmark's M-RoPE Q/K workload as the benchmark launches it (packed [Q|K|V], QK-Norm,
+    t/h/w ids with 1 % past the table, cache append): Q whole; the written K rows against the
+    oracle, V rows bit for bit; every other cache row keeps its fill."""
+    import torch
+
+    from rotary_position_embedding_gb300 import workloads as wl
+
+    w = wl.WORKLOADS["mrope_qkv_norm_prefill_r3_f16"]
+    inp = wl.make_inputs(w)
+    x, inv, past, pos = inp["x"], inp["inv_freq"], inp["past_seq_lens"], inp["position_ids"]
+    B, S, H, Nq, Nkv, L = w.batch, w.seq, w.head_size, w.num_heads, w.extra["kv_num_heads"], w.extra["max_len"]
+    Ntot = Nq + 2 * Nkv
+    cos, sin = orc.cache_build(inv, w.cache_rows, np.float16)
+    nkw = dict(q_norm_weight=inp["q_norm_weight"], k_norm_weight=inp["k_norm_weight"], epsilon=w.extra["epsilon"])
+    fill = 3.0
+    kc0 = np.full((B, Nkv, L, H), fill, np.float16)
+    q_ref, _, kc_ref, vc_ref, n_oor, n_skip = orc.mrope_qkv(x, cos, sin, pos, w.mrope_section, w.mrope_layout,
+                                                            w.scale, num_heads=Nq, kv_num_heads=Nkv, k_cache=kc0,
+                                                            v_cache=kc0, past_seq_lens=past, **nkw)
+    assert n_oor > 0 and n_skip == 0
+    kc = torch.full((B, Nkv, L, H), fill, dtype=torch.float16, device=cuda)
+    vc = torch.full_like(kc, fill)
+    status = torch.zeros(1, dtype=torch.int32, device=cuda)
+    qo, ko = lib.mrope_apply_qkv(_dev(x, torch, cuda), _dev(cos, torch, cuda), _dev(sin, torch, cuda),
+                                 _dev(pos, torch, cuda), w.mrope_section, mrope_layout=w.mrope_layout, scale=w.scale,
+                                 num_heads=Nq, kv_num_heads=Nkv, k_cache=kc, v_cache=vc,
+                                 past_seq_lens=_dev(past, torch, cuda), status=status,
+                                 q_norm_weight=_dev(nkw["q_norm_weight"], torch, cuda),
+                                 k_norm_weight=_dev(nkw["k_norm_weight"], torch, cuda), epsilon=nkw["epsilon"])
+    torch.cuda.synchronize()
+    assert lib.last_kernel() == "rope_qkv_tma_kernel"
+    assert ko is None and int(status.item()) == 1
+    compare_norm(_host(qo), q_ref, Nq, H, H, 0)
+    rows = past[:, None].astype(np.int64) + np.arange(S)[None, :]
+    bi = torch.arange(B, device=cuda)[:, None].expand(B, S)
+    ri = torch.from_numpy(rows).to(cuda)
+    k_rows = _host(kc[bi, :, ri].reshape(B, S, Nkv * H))
+    k_ref = kc_ref[np.arange(B)[:, None], :, rows].reshape(B, S, Nkv * H)
+    compare_norm(k_rows, k_ref, Nkv, H, H, 0)
+    v_rows = _host(vc[bi, :, ri].reshape(B, S, Nkv * H))
+    assert np.array_equal(v_rows.view(np.uint16), _heads(x, B, S, Nq + Nkv, Ntot, Ntot, H).view(np.uint16))
+    kc[bi, :, ri] = fill
+    vc[bi, :, ri] = fill
+    assert bool(torch.all(kc == fill)) and bool(torch.all(vc == fill))
