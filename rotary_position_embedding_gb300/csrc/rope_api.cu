@@ -497,57 +497,108 @@ rope_status plan_qkv_tma(rope_dtype dt, const Geom& g, int es, const QKVParams& 
   QTParams& tp = T->tp;
   memset(&tp, 0, sizeof(tp));
   memset(&T->maps, 0, sizeof(T->maps));
-  // tokens: each gather lane holds one token's position(s), and a tile's
-  // cos/sin rows fit the gather warp's kMaxGather bulk copies per lane
-  // (kMaxGather bounds rows here, 16-byte pieces in the RoPE pipeline)
-  int64_t TS = g.S < ROPE_QKV_TMA_MAX_TS ? g.S : ROPE_QKV_TMA_MAX_TS;
-  while (TS > 1 && TS * slots * 2 > 32 * kMaxGather) --TS;
-  int64_t K = 0, NG = 1;
-  for (;;) {
-    if (TS < 1 || TS > 32 || TS * nP > kTmaConsumers) return ROPE_ERR_UNSUPPORTED;
-    const int64_t tpc = kTmaConsumers / (TS * nP);
-    // heads: a divisor of Nkv (so of Nq) that each column's threads cover
-    // with at most kMaxHeads heads apiece, within the tile budget
-    NG = 1;
-    for (int64_t d = 1; d <= a.Nkv; ++d) {
-      if (a.Nkv % d) continue;
-      if (d > kMaxHeads * tpc) break;
-      if (d > 1 && d * TS * g.H * es > ROPE_QKV_TMA_TILE_BYTES) break;
-      NG = d;
+  const int64_t heads[3] = {a.Nq, a.Nkv, a.cache ? a.Nkv : 0};
+  const int nroles = a.cache ? 3 : 2;
+  const int64_t ts_cap = g.S < ROPE_QKV_TMA_MAX_TS ? g.S : ROPE_QKV_TMA_MAX_TS;
+  const int64_t coef_row = g.h * es;  // bytes of one cos or sin row
+  auto blk_of = [&](int64_t TS) { return (TS * g.H * es + 127) / 128 * 128; };
+  // the stage's tail: per-token flags, M-RoPE positions and the header, for up to 32 tokens
+  const int64_t tail = 32 * 4 + (mrope ? 32 * slots * 8 : 0) + 64;
+  int64_t TSr[3] = {0, 0, 0}, NGr[3] = {0, 0, 0};
+  // Stage layout for the roles' shapes: each role's NG blocks and then its
+  // cos/sin rows; the flags, positions and header after the largest of those.
+  // Returns the stages that fit the budget, or -1 when the tile counts overflow.
+  auto layout = [&]() -> int64_t {
+    int64_t end_max = 0, ts_max = 0, first = 0;
+    for (int r = 0; r < 3; ++r) {
+      QRole& R = tp.r[r];
+      R.TS = (int32_t)TSr[r];
+      R.NG = (int32_t)NGr[r];
+      R.G = (int32_t)(heads[r] / NGr[r]);
+      R.s_tiles = (int32_t)((g.S + TSr[r] - 1) / TSr[r]);
+      if (g.B * (int64_t)R.s_tiles >= INT32_MAX) return -1;
+      R.nt_tiles = (int32_t)(g.B * R.s_tiles);
+      R.blk_bytes = (uint32_t)blk_of(TSr[r]);
+      R.x_bytes = (uint32_t)(NGr[r] * TSr[r] * g.H * es);
+      R.coef_off = (uint32_t)NGr[r] * R.blk_bytes;
+      R.first = first;
+      first += (int64_t)R.nt_tiles * R.G;
+      if (r < nroles) {
+        const int64_t end = R.coef_off + (r < 2 ? TSr[r] * slots * 2 * coef_row : 0);
+        if (end > end_max) end_max = end;
+        if (TSr[r] > ts_max) ts_max = TSr[r];
+      }
     }
-    const uint32_t blk = (uint32_t)(TS * g.H * es);
-    tp.blk_bytes = (blk + 127) / 128 * 128;
-    tp.x_bytes = (uint32_t)NG * blk;
-    tp.coef_off = (uint32_t)NG * tp.blk_bytes;
-    tp.flag_off = tp.coef_off + (uint32_t)(TS * slots * 2 * g.h * es);
-    tp.hdr_off = (tp.flag_off + (uint32_t)TS * 4 + 15) / 16 * 16;
+    tp.ntiles = a.cache ? first : tp.r[2].first;
+    if (!a.cache) tp.r[2].first = tp.ntiles;  // no V tiles
+    if (tp.ntiles >= INT32_MAX) return -1;
+    tp.flag_off = (uint32_t)((end_max + 15) / 16 * 16);
+    tp.pos_off = (tp.flag_off + (uint32_t)ts_max * 4 + 15) / 16 * 16;
+    tp.hdr_off = (tp.pos_off + (uint32_t)(mrope ? ts_max * slots * 8 : 0) + 15) / 16 * 16;
     tp.stage_bytes = (tp.hdr_off + 16 + 1023) / 1024 * 1024;
     tp.bar_bytes = 1024;
-    K = (ROPE_QKV_TMA_SMEM_BUDGET - tp.bar_bytes) / tp.stage_bytes;
-    // M-RoPE's three coefficient rows per token make stages larger: fewer
-    // tokens per tile keep three stages in flight
-    if (K >= 3 || TS <= 4) break;
-    TS -= 4;
+    return (ROPE_QKV_TMA_SMEM_BUDGET - tp.bar_bytes) / tp.stage_bytes;
+  };
+  int64_t K = 0;
+  if (!mrope) {
+    // One tile shape for every role: TS tokens, each gather lane holding one
+    // token's position and copying at most kMaxGather cos/sin rows; NG a
+    // divisor of Nkv (so of Nq) that each column's threads cover with at most
+    // kMaxHeads heads apiece, within the tile budget. Fewer tokens while
+    // fewer than three stages fit.
+    int64_t TS = ts_cap;
+    while (TS > 1 && TS * slots * 2 > 32 * kMaxGather) --TS;
+    for (;;) {
+      if (TS < 1 || TS > 32 || TS * nP > kTmaConsumers) return ROPE_ERR_UNSUPPORTED;
+      const int64_t tpc = kTmaConsumers / (TS * nP);
+      int64_t NG = 1;
+      for (int64_t d = 1; d <= a.Nkv; ++d) {
+        if (a.Nkv % d) continue;
+        if (d > kMaxHeads * tpc) break;
+        if (d > 1 && d * TS * g.H * es > ROPE_QKV_TMA_TILE_BYTES) break;
+        NG = d;
+      }
+      for (int r = 0; r < 3; ++r) TSr[r] = TS, NGr[r] = NG;
+      K = layout();
+      if (K < 0) return ROPE_ERR_UNSUPPORTED;
+      if (K >= 3 || TS <= 4) break;
+      TS -= 4;
+    }
+  } else {
+    // Per role: the most heads a tile can take (a token's three coefficient
+    // rows are gathered once per tile, so a Q tile of all 32 heads gathers a
+    // quarter of what four tiles of 8 do), then the most tokens that keep the
+    // tile within the tile budget and its stage within a third of the shared
+    // memory, so that three stages are in flight.
+    const int64_t stage_cap = (ROPE_QKV_TMA_SMEM_BUDGET - 1024) / 3 / 1024 * 1024 - tail;
+    for (int r = 0; r < nroles; ++r) {
+      const int64_t coef_tok = r < 2 ? slots * 2 * coef_row : 0;  // V tiles gather nothing
+      for (int64_t d = heads[r]; d >= 1 && !TSr[r]; --d) {
+        if (heads[r] % d) continue;
+        for (int64_t TS = ts_cap; TS >= 1; --TS) {
+          if (TS > 32 || TS * nP > kTmaConsumers) continue;
+          if (d > kMaxHeads * (kTmaConsumers / (TS * nP))) continue;
+          if (d * TS * g.H * es > ROPE_QKV_TMA_TILE_BYTES && !(d == 1 && TS == 1)) continue;
+          if (d * blk_of(TS) + TS * coef_tok > stage_cap) continue;
+          TSr[r] = TS, NGr[r] = d;
+          break;
+        }
+      }
+      if (!TSr[r]) return ROPE_ERR_UNSUPPORTED;
+    }
+    if (!a.cache) TSr[2] = TSr[1], NGr[2] = NGr[1];
+    K = layout();
+    if (K < 0) return ROPE_ERR_UNSUPPORTED;
   }
-  tp.TS = (int32_t)TS;
-  tp.NG = (int32_t)NG;
-  tp.Gq = (int32_t)(a.Nq / NG);
-  tp.Gk = (int32_t)(a.Nkv / NG);
-  tp.G = tp.Gq + tp.Gk + (a.cache ? tp.Gk : 0);
-  tp.s_tiles = (int32_t)((g.S + TS - 1) / TS);
-  if (g.B * (int64_t)tp.s_tiles >= INT32_MAX) return ROPE_ERR_UNSUPPORTED;
-  tp.nt_tiles = (int32_t)(g.B * tp.s_tiles);
   tp.nT = (int32_t)((g.H - g.rd) / V);
-  tp.ntiles = g.B * (int64_t)tp.s_tiles * tp.G;
-  if (tp.ntiles >= INT32_MAX) return ROPE_ERR_UNSUPPORTED;
   if (K > ROPE_TMA_MAX_STAGES) K = ROPE_TMA_MAX_STAGES;
   if (K < 2) return ROPE_ERR_UNSUPPORTED;
   tp.K = (int32_t)K;
   const bool packed = a.packed != 0;
   const int64_t n_all = (int64_t)a.Nq + 2 * a.Nkv;
-  tp.head_off[0] = 0;
-  tp.head_off[1] = packed ? a.Nq : 0;
-  tp.head_off[2] = packed ? a.Nq + a.Nkv : 0;
+  tp.r[0].head_off = 0;
+  tp.r[1].head_off = packed ? a.Nq : 0;
+  tp.r[2].head_off = packed ? a.Nq + a.Nkv : 0;
   const size_t smem = tp.bar_bytes + (size_t)K * tp.stage_bytes;
 
   int sms = 0, per_sm = 0;
@@ -560,33 +611,33 @@ rope_status plan_qkv_tma(rope_dtype dt, const Geom& g, int es, const QKVParams& 
 
   // maps: sources (H, heads, S, B) and q_out / k_out (H, heads, S, B) with a
   // TS x NG-head box (Q, K without caches) or a one-head box (K and V into the
-  // caches); caches (H, max_len, Nkv, B), TS rows of one head
+  // caches); caches (H, max_len, Nkv, B), TS rows of one head -- TS and NG
+  // those of the map's role
   const cuuint64_t H = (cuuint64_t)g.H, S = (cuuint64_t)g.S, B = (cuuint64_t)g.B, E = (cuuint64_t)es;
-  const cuuint32_t box_wide[4] = {(cuuint32_t)g.H, (cuuint32_t)NG, (cuuint32_t)TS, 1};
-  const cuuint32_t box_head[4] = {(cuuint32_t)g.H, 1, (cuuint32_t)TS, 1};
-  const cuuint32_t box_row[4] = {(cuuint32_t)g.H, (cuuint32_t)TS, 1, 1};
-  auto seq_map = [&](CUtensorMap* m, const void* base, int64_t heads, bool wide) {
-    const cuuint64_t n = (cuuint64_t)heads;
+  auto seq_map = [&](CUtensorMap* m, const void* base, int64_t heads_all, int r, bool wide) {
+    const cuuint64_t n = (cuuint64_t)heads_all;
     const cuuint64_t dims[4] = {H, n, S, B};
     const cuuint64_t strides[3] = {H * E, n * H * E, S * n * H * E};
-    return encode4(m, dt, base, dims, strides, wide ? box_wide : box_head);
+    const cuuint32_t box[4] = {(cuuint32_t)g.H, wide ? (cuuint32_t)tp.r[r].NG : 1u, (cuuint32_t)tp.r[r].TS, 1};
+    return encode4(m, dt, base, dims, strides, box);
   };
-  auto cache_map = [&](CUtensorMap* m, const void* base) {
+  auto cache_map = [&](CUtensorMap* m, const void* base, int r) {
     const cuuint64_t L = (cuuint64_t)a.max_len, n = (cuuint64_t)a.Nkv;
     const cuuint64_t dims[4] = {H, L, n, B};
     const cuuint64_t strides[3] = {H * E, L * H * E, n * L * H * E};
-    return encode4(m, dt, base, dims, strides, box_row);
+    const cuuint32_t box[4] = {(cuuint32_t)g.H, (cuuint32_t)tp.r[r].TS, 1, 1};
+    return encode4(m, dt, base, dims, strides, box);
   };
   const bool kv_wide = !a.cache;
-  ROPE_TRY(seq_map(&T->maps.src[0], query, packed ? n_all : a.Nq, true));
-  ROPE_TRY(seq_map(&T->maps.src[1], packed ? query : a.k, packed ? n_all : a.Nkv, kv_wide));
-  if (a.cache) ROPE_TRY(seq_map(&T->maps.src[2], packed ? query : a.v, packed ? n_all : a.Nkv, false));
-  ROPE_TRY(seq_map(&T->maps.dst[0], q_out, a.Nq, true));
+  ROPE_TRY(seq_map(&T->maps.src[0], query, packed ? n_all : a.Nq, 0, true));
+  ROPE_TRY(seq_map(&T->maps.src[1], packed ? query : a.k, packed ? n_all : a.Nkv, 1, kv_wide));
+  if (a.cache) ROPE_TRY(seq_map(&T->maps.src[2], packed ? query : a.v, packed ? n_all : a.Nkv, 2, false));
+  ROPE_TRY(seq_map(&T->maps.dst[0], q_out, a.Nq, 0, true));
   if (a.cache) {
-    ROPE_TRY(cache_map(&T->maps.dst[1], a.k_cache));
-    ROPE_TRY(cache_map(&T->maps.dst[2], a.v_cache));
+    ROPE_TRY(cache_map(&T->maps.dst[1], a.k_cache, 1));
+    ROPE_TRY(cache_map(&T->maps.dst[2], a.v_cache, 2));
   } else {
-    ROPE_TRY(seq_map(&T->maps.dst[1], a.k_out, a.Nkv, true));
+    ROPE_TRY(seq_map(&T->maps.dst[1], a.k_out, a.Nkv, 1, true));
   }
   return ROPE_OK;
 }

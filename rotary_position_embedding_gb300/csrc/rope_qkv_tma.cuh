@@ -55,22 +55,30 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
 #define ROPE_QKV_TMA_HEAD_BATCH 2
 #endif
 
-// Tile geometry and stage layout of the pipelined Q/K kernel (host-planned).
-struct QTParams {
-  int32_t TS, NG, K;      // tokens per tile, heads per tile, stages
-  int32_t G, Gq, Gk;      // head groups per token tile: Gq of Q, Gk of K, then Gk of V (cache mode)
+// Tile geometry of one role (Q, K or V): TS tokens x NG heads (host-planned).
+struct QRole {
+  int32_t TS, NG;         // tokens and heads per tile
+  int32_t G;              // head groups of the role: its heads / NG
   int32_t s_tiles;        // ceil(S / TS)
   int32_t nt_tiles;       // token tiles: B * s_tiles
+  int32_t head_off;       // source head of the role's head 0 (packed: 0, Nq, Nq + Nkv)
+  uint32_t blk_bytes;     // cache tiles: one head's TS x H block in a stage (a multiple of 128 bytes)
+  uint32_t x_bytes;       // transaction bytes of a tile
+  uint32_t coef_off;      // stage offset of the tile's cos/sin rows (after its NG blocks)
+  int64_t first;          // index of the role's first tile (ntiles: the role has none)
+};
+
+// Tile geometry and stage layout of the pipelined Q/K kernel (host-planned).
+struct QTParams {
+  int32_t K;              // stages
   int32_t nT;             // tail units (H - rd) / V
   int64_t ntiles;
-  uint32_t blk_bytes;     // cache tiles: one head's TS x H block in a stage (a multiple of 128 bytes)
-  uint32_t x_bytes;       // transaction bytes of a tile: NG boxes
-  uint32_t coef_off;      // stage offsets: cos/sin rows, per-token flags, positions, header
-  uint32_t flag_off;
+  uint32_t flag_off;      // stage offsets: per-token flags, positions, header
+  uint32_t pos_off;       // M-RoPE: the tile's t/h/w positions (gather warp scratch)
   uint32_t hdr_off;
   uint32_t stage_bytes;
   uint32_t bar_bytes;
-  int32_t head_off[3];    // source head of each role's head 0 (packed: 0, Nq, Nq + Nkv)
+  QRole r[3];
 };
 
 // Tensor maps: the source of each role (Q, K, V) and its destination (q_out;
@@ -87,33 +95,40 @@ struct QTile {
   int32_t head0;  // first head of the tile within its role
   int32_t s0;     // first token (sequence index)
   int32_t b;
+  QRole R;        // the role's geometry
 };
+
+__device__ __forceinline__ QRole qrole(const QTParams& tp, int role) {
+  return role == 0 ? tp.r[0] : (role == 1 ? tp.r[1] : tp.r[2]);
+}
 
 // Tiles are numbered head group by head group (all token tiles of Q group 0,
 // then Q group 1, ..., the K groups, the V groups), so the round-robin
 // schedule deals every CTA the same mix of Q, K and V tiles -- which differ in
 // cost: V tiles gather and compute nothing -- and the tiles left over after
 // the last full round are the cheap V tiles.
+// UNIFORM: every role has the same TS and NG (the RoPE path), so those come
+// from role 0 and only the role's first tile and head offset differ.
+template <bool UNIFORM>
 __device__ __forceinline__ QTile qtile_of(const KParams& p, const QTParams& tp, int64_t t64) {
   QTile q;
-  const uint32_t t = (uint32_t)t64;  // tile counts stay below 2^31
-  const uint32_t g = t / (uint32_t)tp.nt_tiles;
-  const uint32_t tt = t - g * (uint32_t)tp.nt_tiles;
-  const uint32_t st = tt % (uint32_t)tp.s_tiles;
-  q.b = (int32_t)(tt / (uint32_t)tp.s_tiles);
-  q.s0 = (int32_t)(st * (uint32_t)tp.TS);
-  const int64_t left = p.S - q.s0;
-  q.n = (int)(left < tp.TS ? left : tp.TS);
-  if ((int)g < tp.Gq) {
-    q.role = 0;
-    q.head0 = (int32_t)g * tp.NG;
-  } else if ((int)g < tp.Gq + tp.Gk) {
-    q.role = 1;
-    q.head0 = ((int32_t)g - tp.Gq) * tp.NG;
+  q.role = t64 < tp.r[1].first ? 0 : (t64 < tp.r[2].first ? 1 : 2);
+  if (UNIFORM) {
+    q.R = tp.r[0];
+    q.R.first = q.role == 0 ? 0 : (q.role == 1 ? tp.r[1].first : tp.r[2].first);
+    q.R.head_off = q.role == 0 ? tp.r[0].head_off : (q.role == 1 ? tp.r[1].head_off : tp.r[2].head_off);
   } else {
-    q.role = 2;
-    q.head0 = ((int32_t)g - tp.Gq - tp.Gk) * tp.NG;
+    q.R = qrole(tp, q.role);
   }
+  const uint32_t t = (uint32_t)(t64 - q.R.first);  // tile counts stay below 2^31
+  const uint32_t g = t / (uint32_t)q.R.nt_tiles;
+  const uint32_t tt = t - g * (uint32_t)q.R.nt_tiles;
+  const uint32_t st = tt % (uint32_t)q.R.s_tiles;
+  q.b = (int32_t)(tt / (uint32_t)q.R.s_tiles);
+  q.s0 = (int32_t)(st * (uint32_t)q.R.TS);
+  const int64_t left = p.S - q.s0;
+  q.n = (int)(left < q.R.TS ? left : q.R.TS);
+  q.head0 = (int32_t)g * q.R.NG;
   return q;
 }
 
@@ -126,9 +141,8 @@ __device__ __forceinline__ bool qtile_wide(const QKVParams& a, const QTile& q) {
 
 // Whether a cache tile goes out row by row from the consumers instead of by
 // tensor store: ragged, or not entirely inside [0, max_len).
-__device__ __forceinline__ bool qtile_direct(const QKVParams& a, const QTParams& tp, const QTile& q,
-                                             int64_t row0) {
-  return q.role != 0 && a.cache && (q.n < tp.TS || row0 < 0 || row0 + tp.TS > a.max_len);
+__device__ __forceinline__ bool qtile_direct(const QKVParams& a, const QTile& q, int64_t row0) {
+  return q.role != 0 && a.cache && (q.n < q.R.TS || row0 < 0 || row0 + q.R.TS > a.max_len);
 }
 
 // z = T(w * T(x * r)) on a unit whose values fx are already unpacked: the
@@ -205,14 +219,14 @@ __global__ void __launch_bounds__(kTmaThreads, ROPE_TMA_MIN_CTAS)
         const int s = (int)(jj % tp.K);
         *stage_hdr(s) = t;
         if (t < tp.ntiles) {
-          const QTile q = qtile_of(p, tp, t);
+          const QTile q = qtile_of<!MROPE>(p, tp, t);
           const uint32_t dst = smem_addr(stage0 + (size_t)s * tp.stage_bytes);
-          mbar_arrive_expect_tx(full0 + 8 * s, tp.x_bytes);
+          mbar_arrive_expect_tx(full0 + 8 * s, q.R.x_bytes);
           // one NG-head box, or (cache tiles) one box per head
-          const int nbox = qtile_wide(a, q) ? 1 : tp.NG;
+          const int nbox = qtile_wide(a, q) ? 1 : q.R.NG;
           for (int u = 0; u < nbox; ++u) {
-            const int c[4] = {0, tp.head_off[q.role] + q.head0 + u, q.s0, q.b};
-            tma_load_x<true>(dst + (uint32_t)u * tp.blk_bytes, &maps.src[q.role], c, full0 + 8 * s, pol);
+            const int c[4] = {0, q.R.head_off + q.head0 + u, q.s0, q.b};
+            tma_load_x<true>(dst + (uint32_t)u * q.R.blk_bytes, &maps.src[q.role], c, full0 + 8 * s, pol);
           }
         } else {
           mbar_arrive(full0 + 8 * s);  // the sentinel carries no bytes
@@ -233,7 +247,7 @@ __global__ void __launch_bounds__(kTmaThreads, ROPE_TMA_MIN_CTAS)
       int64_t past_st = 0;  // raw past[b]: the load is consumed only at the store
       auto prep = [&](int64_t t) {
         if (t < tp.ntiles) {
-          q_st = qtile_of(p, tp, t);
+          q_st = qtile_of<!MROPE>(p, tp, t);
           past_st = (q_st.role != 0 && a.cache && a.past) ? (int64_t)__ldg(a.past + q_st.b) : 0;
         }
       };
@@ -246,17 +260,17 @@ __global__ void __launch_bounds__(kTmaThreads, ROPE_TMA_MIN_CTAS)
         }
         if (t_st >= tp.ntiles) break;  // sentinel
         const int64_t row_st = past_st + q_st.s0;
-        if (!qtile_direct(a, tp, q_st, row_st)) {
+        if (!qtile_direct(a, q_st, row_st)) {
           const uint32_t src = smem_addr(stage0 + (size_t)s * tp.stage_bytes);
           const bool to_cache = !qtile_wide(a, q_st);
-          for (int u = 0; u < (to_cache ? tp.NG : 1); ++u) {
+          for (int u = 0; u < (to_cache ? q_st.R.NG : 1); ++u) {
             int c[4];
             if (to_cache) {
               c[0] = 0, c[1] = (int)row_st, c[2] = q_st.head0 + u, c[3] = q_st.b;
             } else {
               c[0] = 0, c[1] = q_st.head0 + u, c[2] = q_st.s0, c[3] = q_st.b;
             }
-            tma_store_y<true>(&maps.dst[q_st.role], c, src + (uint32_t)u * tp.blk_bytes, pol);
+            tma_store_y<true>(&maps.dst[q_st.role], c, src + (uint32_t)u * q_st.R.blk_bytes, pol);
           }
           bulk_commit();
         }
@@ -304,7 +318,6 @@ __global__ void __launch_bounds__(kTmaThreads, ROPE_TMA_MIN_CTAS)
     // row_bytes at byte r*row_bytes) goes to lane r % 32 as one bulk copy.
     const uint32_t row_bytes = (uint32_t)h * (uint32_t)sizeof(bits);
     constexpr int SLOTS = MROPE ? 3 : 1;  // coefficient rows per token: one per position stream
-    const int rows = tp.TS * SLOTS * 2;
     // M-RoPE: the streams some coefficient index uses (an unused stream's
     // position never matters, nor does it flag anything)
     uint32_t used = 1u;
@@ -312,7 +325,10 @@ __global__ void __launch_bounds__(kTmaThreads, ROPE_TMA_MIN_CTAS)
       used = 0u;
       for (int i = 0; i < h; ++i) used |= 1u << ((p.smap[i >> 4] >> ((i & 15) * 2)) & 3u);
     }
-    const int rounds = (rows + 31) / 32;  // the same for every lane: the shuffles below are warp-wide
+    // M-RoPE: 16-byte pieces per row, and this lane's first piece and stride
+    const int ch = (int)(row_bytes / 16);
+    const int r_first = lane / ch, pc_first = lane % ch;
+    const int r_step = 32 / ch, pc_step = 32 % ch;
     // What a tile needs from global memory -- its positions, or the past
     // length its positions and cache rows start from -- is loaded one tile
     // ahead: under a saturated memory system even these L2 hits take
@@ -324,7 +340,7 @@ __global__ void __launch_bounds__(kTmaThreads, ROPE_TMA_MIN_CTAS)
     auto prefetch = [&](int64_t t) -> Pre {
       Pre r{};
       if (t < tp.ntiles) {
-        const QTile q = qtile_of(p, tp, t);
+        const QTile q = qtile_of<!MROPE>(p, tp, t);
         if (a.past && (IMPLICIT || (q.role != 0 && a.cache))) r.past = (int64_t)__ldg(a.past + q.b);
         if (!IMPLICIT && q.role != 2 && lane < q.n) {
           const int64_t tok = (int64_t)q.b * p.S + q.s0 + lane;
@@ -369,7 +385,7 @@ __global__ void __launch_bounds__(kTmaThreads, ROPE_TMA_MIN_CTAS)
           have_nxt = true;
         }
       }
-      const QTile q = qtile_of(p, tp, t);
+      const QTile q = qtile_of<!MROPE>(p, tp, t);
       unsigned char* st = stage0 + (size_t)s * tp.stage_bytes;
       if (q.role != 0 && a.cache && lane == 0) stage_hdr(s)[1] = cur.past + q.s0;
       if (q.role != 2) {
@@ -385,38 +401,75 @@ __global__ void __launch_bounds__(kTmaThreads, ROPE_TMA_MIN_CTAS)
           }
           if ((flag & used) != used && q.role == 0 && q.head0 == 0 && p.oor_flag) atomicOr(p.oor_flag, 1);
         }
-        if (lane < tp.TS) reinterpret_cast<uint32_t*>(st + tp.flag_off)[lane] = flag;
-        const uint32_t coef_addr = smem_addr(st) + tp.coef_off;
-        const bits* src[kMaxGather];
-        uint32_t bytes = 0, go = 0;
+        if (lane < q.R.TS) reinterpret_cast<uint32_t*>(st + tp.flag_off)[lane] = flag;
+        const uint32_t coef_addr = smem_addr(st) + q.R.coef_off;
+        if (MROPE) {
+          // Three rows per token: one bulk copy per row would queue 6 TS
+          // requests on the SM's copy engine behind the tile loads, so the
+          // rows go as 16-byte asynchronous copies through the load path,
+          // piece c of the block (row c / ch, piece c % ch) by lane c % 32.
+          // Positions go through the stage so that any lane can read any
+          // token's.
+          if (lane < q.R.TS) {
 #pragma unroll
-        for (int g = 0; g < kMaxGather; ++g) {
-          if (g >= rounds) break;
-          // row r: token r / (2*SLOTS), stream (r / 2) % SLOTS, cos or sin (r % 2)
-          const int r = lane + 32 * g;
-          const int lt = r < rows ? r / (2 * SLOTS) : 0;
-          const int k = (r >> 1) % SLOTS;
-          // token lt's positions live in lane lt
-          int64_t row = __shfl_sync(0xffffffffu, pp[0], lt);
+            for (int k = 0; k < SLOTS; ++k) reinterpret_cast<int64_t*>(st + tp.pos_off)[lane * SLOTS + k] = pp[k];
+          }
+          __syncwarp();  // positions and flags, before the lanes read them
+          const int64_t* pv = reinterpret_cast<const int64_t*>(st + tp.pos_off);
+          const uint32_t* fv = reinterpret_cast<const uint32_t*>(st + tp.flag_off);
+          const int lim = q.n * (2 * SLOTS);  // rows of the tile's tokens
+          int r = r_first, pc = pc_first;
+          while (r < lim) {
+            const int lt = r / (2 * SLOTS);
+            const int k = (r >> 1) % SLOTS;
+            if ((fv[lt] >> k) & 1u)
+              cp_async16(coef_addr + 16u * (uint32_t)(r * ch + pc),
+                         reinterpret_cast<const uint4*>(((r & 1) ? sinb : cosb) + pv[lt * SLOTS + k] * h) + pc);
+            r += r_step;
+            pc += pc_step;
+            if (pc >= ch) {
+              pc -= ch;
+              ++r;
+            }
+          }
+          // the copies' arrival is pending on full[s] until they land; the
+          // plain arrival releases the flags, positions and header
+          cp_async_arrive_pending(full0 + 8 * s);
+          mbar_arrive(full0 + 8 * s);
+        } else {
+          const int rows = q.R.TS * SLOTS * 2;
+          const int rounds = (rows + 31) / 32;  // the same for every lane: the shuffles below are warp-wide
+          const bits* src[kMaxGather];
+          uint32_t bytes = 0, go = 0;
 #pragma unroll
-          for (int kk = 1; kk < SLOTS; ++kk) {
-            const int64_t other = __shfl_sync(0xffffffffu, pp[kk], lt);
-            if (k == kk) row = other;
+          for (int g = 0; g < kMaxGather; ++g) {
+            if (g >= rounds) break;
+            // row r: token r / (2*SLOTS), stream (r / 2) % SLOTS, cos or sin (r % 2)
+            const int r = lane + 32 * g;
+            const int lt = r < rows ? r / (2 * SLOTS) : 0;
+            const int k = (r >> 1) % SLOTS;
+            // token lt's positions live in lane lt
+            int64_t row = __shfl_sync(0xffffffffu, pp[0], lt);
+#pragma unroll
+            for (int kk = 1; kk < SLOTS; ++kk) {
+              const int64_t other = __shfl_sync(0xffffffffu, pp[kk], lt);
+              if (k == kk) row = other;
+            }
+            const uint32_t ok = (__shfl_sync(0xffffffffu, flag, lt) >> k) & 1u;
+            src[g] = ((r & 1) ? sinb : cosb) + row * h;
+            if (r < rows && ok) {
+              bytes += row_bytes;
+              go |= 1u << g;
+            }
           }
-          const uint32_t ok = (__shfl_sync(0xffffffffu, flag, lt) >> k) & 1u;
-          src[g] = ((r & 1) ? sinb : cosb) + row * h;
-          if (r < rows && ok) {
-            bytes += row_bytes;
-            go |= 1u << g;
-          }
+          __syncwarp();  // flags and the header precede the lanes' (releasing) arrivals
+          // this lane's arrival carries the bytes its copies will complete
+          mbar_arrive_expect_tx(full0 + 8 * s, bytes);
+#pragma unroll
+          for (int g = 0; g < kMaxGather; ++g)
+            if ((go >> g) & 1u) bulk_g2s(coef_addr + row_bytes * (uint32_t)(lane + 32 * g), src[g], row_bytes,
+                                         full0 + 8 * s);
         }
-        __syncwarp();  // flags and the header precede the lanes' (releasing) arrivals
-        // this lane's arrival carries the bytes its copies will complete
-        mbar_arrive_expect_tx(full0 + 8 * s, bytes);
-#pragma unroll
-        for (int g = 0; g < kMaxGather; ++g)
-          if ((go >> g) & 1u) bulk_g2s(coef_addr + row_bytes * (uint32_t)(lane + 32 * g), src[g], row_bytes,
-                                       full0 + 8 * s);
       } else {
         __syncwarp();  // the header precedes the lanes' (releasing) arrivals
         mbar_arrive(full0 + 8 * s);
@@ -433,20 +486,28 @@ __global__ void __launch_bounds__(kTmaThreads, ROPE_TMA_MIN_CTAS)
   // Thread q owns column (token ts, pair unit k) of the tile for heads
   // hq, hq + tpc, ...; with RMSNorm the nP threads of one (token, head) row
   // are an aligned lane group that adds up the row's squares with shuffles.
+  // A role's TS x nP columns are a multiple of nP, so the unit k is the same
+  // in every role's layout; ts and hq follow the tile's role.
   const int qi = threadIdx.x - 32 * kTmaRoleWarps;
   const int nP = p.nP;
-  const int cols = tp.TS * nP;
-  const int tpc = kTmaConsumers / cols;  // the host keeps cols <= consumers
-  const int hpt = (tp.NG + tpc - 1) / tpc;  // heads per thread (the same for every thread)
-  const int col = qi % cols;
-  const int hq = qi / cols;
-  const bool has_col = hq < tpc;
-  const int ts = col / nP;
-  const int k = col - ts * nP;
+  const int k = qi % nP;
   int oa, ob;
   unit_offsets<V, INTER>(k, h, oa, ob);
   const int oc = k * V;
-  const uint32_t blk_elems = tp.blk_bytes / (uint32_t)sizeof(bits);
+  // the column of role r's tiles (once for all roles when they share a shape)
+  int cols = 0, tpc = 0, hpt = 0, hq = 0, ts = 0;
+  bool has_col = false;
+  uint32_t blk_elems = 0;
+  auto columns = [&](const QRole& R) {
+    cols = R.TS * nP;
+    tpc = kTmaConsumers / cols;        // the host keeps cols <= consumers
+    hpt = (R.NG + tpc - 1) / tpc;  // heads per thread (the same for every thread)
+    hq = qi / cols;
+    has_col = hq < tpc;
+    ts = (qi - hq * cols) / nP;
+    blk_elems = R.blk_bytes / (uint32_t)sizeof(bits);
+  };
+  if (!MROPE) columns(tp.r[0]);
   // M-RoPE: the stream of each of the unit's V coefficient indices, and the
   // masks that merge the three gathered rows word by word
   uint32_t um = 0, present = 0;
@@ -472,7 +533,8 @@ __global__ void __launch_bounds__(kTmaThreads, ROPE_TMA_MIN_CTAS)
       timed_out = true;
       break;
     }
-    const QTile q = qtile_of(p, tp, t);
+    const QTile q = qtile_of<!MROPE>(p, tp, t);
+    if (MROPE) columns(q.R);
     unsigned char* st = stage0 + (size_t)s * tp.stage_bytes;
     bits* sx = reinterpret_cast<bits*>(st);
     const bool tok_in = ts < q.n;
@@ -486,7 +548,7 @@ __global__ void __launch_bounds__(kTmaThreads, ROPE_TMA_MIN_CTAS)
       uint32_t ma[4] = {0, 0, 0, 0}, mb[4] = {0, 0, 0, 0};
       if (valid) {
         if (MROPE) {
-          const bits* cr = reinterpret_cast<const bits*>(st + tp.coef_off) + (size_t)ts * 3 * 2 * h;
+          const bits* cr = reinterpret_cast<const bits*>(st + q.R.coef_off) + (size_t)ts * 3 * 2 * h;
           const uint32_t vmask = fl & present;
           VT cs[3], ss[3];
 #pragma unroll
@@ -507,7 +569,7 @@ __global__ void __launch_bounds__(kTmaThreads, ROPE_TMA_MIN_CTAS)
           blend_on = vmask != present;
           if (blend_on) pair_masks<V, INTER>(um, vmask, ma, mb);
         } else {
-          const bits* cr = reinterpret_cast<const bits*>(st + tp.coef_off) + (size_t)ts * 2 * h;
+          const bits* cr = reinterpret_cast<const bits*>(st + q.R.coef_off) + (size_t)ts * 2 * h;
           c = *reinterpret_cast<const VT*>(cr + oc);
           sn = *reinterpret_cast<const VT*>(cr + h + oc);
         }
@@ -540,8 +602,8 @@ __global__ void __launch_bounds__(kTmaThreads, ROPE_TMA_MIN_CTAS)
 #pragma unroll
         for (int u = 0; u < HB; ++u) {
           const int hh = hq + (u0 + u) * tpc;
-          act[u] = u0 + u < hpt && has_col && tok_in && hh < tp.NG && (NORM || valid);
-          ro[u] = wide ? ((uint32_t)ts * (uint32_t)tp.NG + (uint32_t)hh) * (uint32_t)H
+          act[u] = u0 + u < hpt && has_col && tok_in && hh < q.R.NG && (NORM || valid);
+          ro[u] = wide ? ((uint32_t)ts * (uint32_t)q.R.NG + (uint32_t)hh) * (uint32_t)H
                        : (uint32_t)hh * blk_elems + (uint32_t)ts * (uint32_t)H;
           xa[u] = VT{};
           xb[u] = VT{};
@@ -654,7 +716,7 @@ __global__ void __launch_bounds__(kTmaThreads, ROPE_TMA_MIN_CTAS)
     }
     if (q.role != 0 && a.cache) {
       const int64_t row0 = stage_hdr(s)[1];
-      if (qtile_direct(a, tp, q, row0)) {
+      if (qtile_direct(a, q, row0)) {
         // rows inside the cache, stored by the threads that own them
         if (q.role == 1 && q.head0 == 0 && qi == 0 && (row0 < 0 || row0 + q.n > a.max_len))
           flag_cache_row(p.oor_flag);
@@ -663,7 +725,7 @@ __global__ void __launch_bounds__(kTmaThreads, ROPE_TMA_MIN_CTAS)
           bits* cbase = static_cast<bits*>(q.role == 1 ? a.k_cache : a.v_cache);
           for (int u = 0; u < hpt; ++u) {
             const int hh = hq + u * tpc;
-            if (hh >= tp.NG) break;
+            if (hh >= q.R.NG) break;
             const uint32_t ro = (uint32_t)hh * blk_elems + (uint32_t)ts * (uint32_t)H;
             bits* dr = cbase + (((int64_t)q.b * a.Nkv + q.head0 + hh) * a.max_len + r) * H;
             *reinterpret_cast<VT*>(dr + oa) = *reinterpret_cast<const VT*>(sx + ro + oa);
