@@ -50,6 +50,13 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
                : "memory");
 }
 
+// Arrive on `bar` once this thread's earlier cp.async copies have landed,
+// counted as a pending arrival of its own: the barrier's phase waits for it
+// without it taking one of the expected arrivals.
+__device__ __forceinline__ void cp_async_arrive_pending(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+
 // Heads a consumer thread loads and reduces together.
 #ifndef ROPE_QKV_TMA_HEAD_BATCH
 #define ROPE_QKV_TMA_HEAD_BATCH 2
