@@ -33,7 +33,8 @@ def _run(lib, orc, torch, cuda, dt, packed, cache, inter, rot, layout, norm, H=6
     rd = 0 if rot == "full" else H // 2
     rdw = rd or H
     h = rdw // 2
-    sec = {32: (8, 12, 12), 16: (4, 6, 6), 64: (16, 24, 24), 8: (2, 3, 3), 6: (2, 2, 2), 3: (1, 1, 1)}[h]
+    sec = {64: (16, 24, 24), 32: (8, 12, 12), 16: (4, 6, 6), 8: (2, 3, 3), 6: (2, 2, 2), 3: (1, 1, 1),
+           128: (32, 48, 48)}[h]
     Ntot = Nq + 2 * Nkv
     x = rng.standard_normal((B, S, Ntot * H))
     if norm:
@@ -124,6 +125,35 @@ def test_mrope_qkv_grid(lib, orc, cuda, dt, packed, cache, inter, rot, layout, n
     _run(lib, orc, torch, cuda, dt, packed, cache, inter, rot, layout, norm,
          scale=0.75 if (inter + layout) % 2 else 1.0, seed=case, variant=variant,
          kernel="rope_qkv_tma_kernel" if tma else "rope_qkv_kernel", dynamic=tma and case % 2 == 1)
+
+
+# Shapes whose roles get different tiles on the pipeline (tokens x heads per tile, from the
+# planner): e.g. H 128 with 32 Q and 8 K/V heads gives Q 4 x 32, K 13 x 8, V 16 x 8; H 256
+# with 16 and 2 gives Q 4 x 16, K 14 x 2, V 16 x 2. Sequence lengths leave ragged tiles in
+# every role, and cache rows run past the cache's end.
+MROPE_QKV_TMA_SHAPES = [
+    # dt, H, Nq, Nkv, B, S, packed, cache, inter, rot, layout, norm, L (cache rows)
+    ("f16", 128, 32, 8, 2, 41, 1, 1, 0, "full", 1, 1, 80),
+    ("bf16", 128, 32, 8, 3, 29, 0, 1, 1, "partial", 0, 0, 60),
+    ("f16", 256, 16, 2, 2, 33, 1, 1, 0, "full", 1, 1, 70),
+    ("f32", 128, 12, 4, 3, 23, 0, 0, 1, "full", 0, 0, 80),
+    ("f16", 64, 24, 8, 2, 50, 1, 0, 0, "full", 1, 1, 80),
+    ("bf16", 128, 40, 8, 3, 12, 1, 1, 1, "full", 1, 1, 45),
+]
+
+
+@pytest.mark.parametrize("schedule", ["static", "dynamic"])
+@pytest.mark.parametrize("dt,H,Nq,Nkv,B,S,packed,cache,inter,rot,layout,norm,L", MROPE_QKV_TMA_SHAPES)
+def test_mrope_qkv_tma_shapes(lib, orc, cuda, dt, H, Nq, Nkv, B, S, packed, cache, inter, rot, layout, norm, L,
+                              schedule):
+    """The pipeline with a tile shape per role, tiles dealt round robin or drawn from a
+    scratch counter."""
+    import torch
+
+    case = (dt, H, Nq, Nkv, B, S, packed, cache, inter, rot, layout, norm, L)
+    _run(lib, orc, torch, cuda, dt, packed, cache, inter, rot, layout, norm, H=H, Nq=Nq, Nkv=Nkv, B=B, S=S,
+         L=L, scale=0.75 if layout == 0 else 1.0, seed=300 + MROPE_QKV_TMA_SHAPES.index(case), variant="tma",
+         kernel="rope_qkv_tma_kernel", dynamic=schedule == "dynamic")
 
 
 @pytest.mark.parametrize("dt,H", [("f16", 12), ("f32", 6)])
