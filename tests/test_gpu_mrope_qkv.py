@@ -133,9 +133,9 @@ def test_mrope_qkv_grid(lib, orc, cuda, dt, packed, cache, inter, rot, layout, n
 # every role, and cache rows run past the cache's end.
 MROPE_QKV_TMA_SHAPES = [
     # dt, H, Nq, Nkv, B, S, packed, cache, inter, rot, layout, norm, L (cache rows)
-    ("f16", 128, 32, 8, 2, 41, 1, 1, 0, "full", 1, 1, 80),
+    ("f16", 128, 32, 8, 2, 41, 1, 1, 0, "full", 1, 1, 45),
     ("bf16", 128, 32, 8, 3, 29, 0, 1, 1, "partial", 0, 0, 60),
-    ("f16", 256, 16, 2, 2, 33, 1, 1, 0, "full", 1, 1, 70),
+    ("f16", 256, 16, 2, 2, 33, 1, 1, 0, "full", 1, 1, 40),
     ("f32", 128, 12, 4, 3, 23, 0, 0, 1, "full", 0, 0, 80),
     ("f16", 64, 24, 8, 2, 50, 1, 0, 0, "full", 1, 1, 80),
     ("bf16", 128, 40, 8, 3, 12, 1, 1, 1, "full", 1, 1, 45),
