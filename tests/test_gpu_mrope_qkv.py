@@ -34,7 +34,7 @@ def _run(lib, orc, torch, cuda, dt, packed, cache, inter, rot, layout, norm, H=6
     rdw = rd or H
     h = rdw // 2
     sec = {64: (16, 24, 24), 32: (8, 12, 12), 16: (4, 6, 6), 8: (2, 3, 3), 6: (2, 2, 2), 3: (1, 1, 1),
-           128: (32, 48, 48)}[h]
+           128: (32, 48, 48), 48: (16, 16, 16), 40: (16, 12, 12), 24: (8, 8, 8)}[h]
     Ntot = Nq + 2 * Nkv
     x = rng.standard_normal((B, S, Ntot * H))
     if norm:
@@ -154,6 +154,60 @@ def test_mrope_qkv_tma_shapes(lib, orc, cuda, dt, H, Nq, Nkv, B, S, packed, cach
     _run(lib, orc, torch, cuda, dt, packed, cache, inter, rot, layout, norm, H=H, Nq=Nq, Nkv=Nkv, B=B, S=S,
          L=L, scale=0.75 if layout == 0 else 1.0, seed=300 + MROPE_QKV_TMA_SHAPES.index(case), variant="tma",
          kernel="rope_qkv_tma_kernel", dynamic=schedule == "dynamic")
+
+
+@pytest.mark.parametrize("variant", ["simt", "tma"])
+@pytest.mark.parametrize("norm", [0, 1])
+def test_mrope_qkv_negative_past_lengths(lib, orc, cuda, variant, norm):
+    """A negative past length puts a batch's first cache rows below 0: those rows are
+    skipped (status bit 2); on the pipeline a tile starting below row 0 is stored row by row."""
+    import torch
+
+    _run(lib, orc, torch, cuda, "f16", 1, 1, 0, "full", 1, norm, H=128, Nq=16, Nkv=8, B=2, S=40, L=48,
+         seed=40 + norm, variant=variant, kernel="rope_qkv_tma_kernel" if variant == "tma" else "rope_qkv_kernel",
+         past=[-21, 3])
+
+
+@pytest.mark.parametrize("dt,H", [("f16", 96), ("f16", 80), ("bf16", 96), ("f32", 48)])
+@pytest.mark.parametrize("cache", [0, 1])
+def test_mrope_qkv_tma_unit_counts(lib, orc, cuda, dt, H, cache):
+    """Rows of 6 or 5 pair units (not a power of two): the pipeline takes them without the
+    norm; with the norm they stay on the SIMT kernel."""
+    import torch
+
+    for norm in (0, 1):
+        _run(lib, orc, torch, cuda, dt, 1, cache, 0, "full", 1, norm, H=H, Nq=12, Nkv=4, B=2, S=33, L=40,
+             seed=H + cache + 2 * norm, variant="tma", kernel="rope_qkv_kernel" if norm else "rope_qkv_tma_kernel")
+
+
+def test_mrope_qkv_multi_head_attention_in_place_and_empty(lib, orc, cuda):
+    """kv_num_heads == num_heads with q_out == query and k_out == key (separate inputs), and
+    an empty sequence."""
+    import torch
+
+    rng = np.random.default_rng(4)
+    B, S, N, H, R = 2, 50, 4, 64, 100
+    q = rng.standard_normal((B, S, N * H)).astype(np.float16)
+    k = rng.standard_normal((B, S, N * H)).astype(np.float16)
+    theta = rng.uniform(-np.pi, np.pi, (R, H // 2))
+    cos, sin = np.cos(theta).astype(np.float16), np.sin(theta).astype(np.float16)
+    pos = rng.integers(0, R, (3, B, S))
+    sec = (8, 12, 12)
+    q_ref, k_ref, _, _, n_oor, _ = orc.mrope_qkv(q, cos, sin, pos, sec, 1, 1.0, num_heads=N, kv_num_heads=N, key=k)
+    assert n_oor == 0
+    qd, kd = _dev(q, torch, cuda), _dev(k, torch, cuda)
+    qo, ko = lib.mrope_apply_qkv(qd, _dev(cos, torch, cuda), _dev(sin, torch, cuda), _dev(pos, torch, cuda), sec,
+                                 mrope_layout=1, num_heads=N, kv_num_heads=N, key=kd, q_out=qd, k_out=kd)
+    torch.cuda.synchronize()
+    assert qo.data_ptr() == qd.data_ptr() and ko.data_ptr() == kd.data_ptr()
+    smap = orc.mrope_stream_map(sec, 1, H // 2)
+    for got, ref, src in ((qd, q_ref, q), (kd, k_ref, k)):
+        compare(_host(got), ref, src, 3, N, mrope_passthrough_mask(src.shape, 3, N, 0, pos, R, smap, 0))
+    e = torch.zeros((2, 0, N * H), dtype=torch.float16, device=cuda)
+    qo, ko = lib.mrope_apply_qkv(e, _dev(cos, torch, cuda), _dev(sin, torch, cuda),
+                                 torch.zeros((3, 2, 0), dtype=torch.int64, device=cuda), sec, num_heads=N,
+                                 kv_num_heads=N, key=torch.zeros_like(e))
+    assert qo.shape == (2, 0, N * H) and ko.shape == (2, 0, N * H)
 
 
 @pytest.mark.parametrize("dt,H", [("f16", 12), ("f32", 6)])
