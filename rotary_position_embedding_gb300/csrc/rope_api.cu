@@ -455,6 +455,17 @@ struct QkvTmaLaunch {
   Launch L;
 };
 
+// Multiply-shift constants for dividing values below 2^31 by d (see Div).
+Div div_of(int64_t d) {
+  if (d < 1) d = 1;  // empty roles: never divided by
+  int l = 0;
+  while (((int64_t)1 << l) < d) ++l;
+  Div r;
+  r.m = (uint32_t)((((uint64_t)1 << (31 + l)) + (uint64_t)d - 1) / (uint64_t)d);
+  r.shift = 31 + l;
+  return r;
+}
+
 // One 4-D tiled tensor map: dims and strides innermost first (strides in
 // bytes, dims[1..3]), box (bx0..bx3).
 rope_status encode4(CUtensorMap* m, rope_dtype dt, const void* base, const cuuint64_t (&dims)[4],
@@ -521,6 +532,13 @@ rope_status plan_qkv_tma(rope_dtype dt, const Geom& g, int es, const QKVParams& 
       R.blk_bytes = (uint32_t)blk_of(TSr[r]);
       R.x_bytes = (uint32_t)(NGr[r] * TSr[r] * g.H * es);
       R.coef_off = (uint32_t)NGr[r] * R.blk_bytes;
+      R.by_nt = div_of(R.nt_tiles);
+      R.by_s = div_of(R.s_tiles);
+      R.cols = (int32_t)(TSr[r] * nP);
+      if (R.cols > kTmaConsumers) return -1;
+      R.tpc = kTmaConsumers / R.cols;
+      R.hpt = (R.NG + R.tpc - 1) / R.tpc;
+      R.by_cols = div_of(R.cols);
       R.first = first;
       first += (int64_t)R.nt_tiles * R.G;
       if (r < nroles) {
@@ -537,6 +555,7 @@ rope_status plan_qkv_tma(rope_dtype dt, const Geom& g, int es, const QKVParams& 
     tp.hdr_off = (tp.pos_off + (uint32_t)(mrope ? ts_max * slots * 8 : 0) + 15) / 16 * 16;
     tp.stage_bytes = (tp.hdr_off + 16 + 1023) / 1024 * 1024;
     tp.bar_bytes = 1024;
+    tp.by_nP = div_of(nP);
     return (ROPE_QKV_TMA_SMEM_BUDGET - tp.bar_bytes) / tp.stage_bytes;
   };
   int64_t K = 0;

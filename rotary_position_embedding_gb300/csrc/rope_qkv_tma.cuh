@@ -62,6 +62,19 @@ __device__ __forceinline__ void cp_async_arrive_pending(uint32_t bar) {
 #define ROPE_QKV_TMA_HEAD_BATCH 2
 #endif
 
+// Division of x < 2^31 by a divisor d fixed at planning time, as a multiply
+// and a shift: with l = ceil(log2 d) and m = ceil(2^(31+l) / d) (m < 2^32),
+// floor(x * m / 2^(31+l)) = floor(x / d) because the error x*(m*d - 2^(31+l))
+// / (d * 2^(31+l)) stays below 1/d (Granlund and Montgomery, "Division by
+// invariant integers using multiplication", 1994).
+struct Div {
+  uint32_t m;
+  int32_t shift;  // 31 + l
+};
+__device__ __forceinline__ uint32_t div_by(uint32_t x, Div d) {
+  return (uint32_t)(((uint64_t)x * d.m) >> d.shift);
+}
+
 // Tile geometry of one role (Q, K or V): TS tokens x NG heads (host-planned).
 struct QRole {
   int32_t TS, NG;         // tokens and heads per tile
@@ -73,6 +86,11 @@ struct QRole {
   uint32_t x_bytes;       // transaction bytes of a tile
   uint32_t coef_off;      // stage offset of the tile's cos/sin rows (after its NG blocks)
   int64_t first;          // index of the role's first tile (ntiles: the role has none)
+  Div by_nt, by_s;        // division by nt_tiles and by s_tiles
+  // consumer columns (token, pair unit): TS * nP of them, tpc threads each
+  // (cols <= consumers), hpt heads per thread
+  int32_t cols, tpc, hpt;
+  Div by_cols;
 };
 
 // Tile geometry and stage layout of the pipelined Q/K kernel (host-planned).
@@ -85,6 +103,7 @@ struct QTParams {
   uint32_t hdr_off;
   uint32_t stage_bytes;
   uint32_t bar_bytes;
+  Div by_nP;              // division by the pair units per row
   QRole r[3];
 };
 
@@ -128,10 +147,11 @@ __device__ __forceinline__ QTile qtile_of(const KParams& p, const QTParams& tp, 
     q.R = qrole(tp, q.role);
   }
   const uint32_t t = (uint32_t)(t64 - q.R.first);  // tile counts stay below 2^31
-  const uint32_t g = t / (uint32_t)q.R.nt_tiles;
+  const uint32_t g = div_by(t, q.R.by_nt);
   const uint32_t tt = t - g * (uint32_t)q.R.nt_tiles;
-  const uint32_t st = tt % (uint32_t)q.R.s_tiles;
-  q.b = (int32_t)(tt / (uint32_t)q.R.s_tiles);
+  const uint32_t bb = div_by(tt, q.R.by_s);
+  const uint32_t st = tt - bb * (uint32_t)q.R.s_tiles;
+  q.b = (int32_t)bb;
   q.s0 = (int32_t)(st * (uint32_t)q.R.TS);
   const int64_t left = p.S - q.s0;
   q.n = (int)(left < q.R.TS ? left : q.R.TS);
@@ -497,7 +517,7 @@ __global__ void __launch_bounds__(kTmaThreads, ROPE_TMA_MIN_CTAS)
   // in every role's layout; ts and hq follow the tile's role.
   const int qi = threadIdx.x - 32 * kTmaRoleWarps;
   const int nP = p.nP;
-  const int k = qi % nP;
+  const int k = qi - nP * (int)div_by((uint32_t)qi, tp.by_nP);
   int oa, ob;
   unit_offsets<V, INTER>(k, h, oa, ob);
   const int oc = k * V;
@@ -506,12 +526,12 @@ __global__ void __launch_bounds__(kTmaThreads, ROPE_TMA_MIN_CTAS)
   bool has_col = false;
   uint32_t blk_elems = 0;
   auto columns = [&](const QRole& R) {
-    cols = R.TS * nP;
-    tpc = kTmaConsumers / cols;        // the host keeps cols <= consumers
-    hpt = (R.NG + tpc - 1) / tpc;  // heads per thread (the same for every thread)
-    hq = qi / cols;
+    cols = R.cols;
+    tpc = R.tpc;
+    hpt = R.hpt;  // the same for every thread
+    hq = (int)div_by((uint32_t)qi, R.by_cols);
     has_col = hq < tpc;
-    ts = (qi - hq * cols) / nP;
+    ts = (int)div_by((uint32_t)(qi - hq * cols), tp.by_nP);
     blk_elems = R.blk_bytes / (uint32_t)sizeof(bits);
   };
   if (!MROPE) columns(tp.r[0]);
