@@ -546,6 +546,11 @@ __global__ void __launch_bounds__(kTmaThreads, ROPE_TMA_MIN_CTAS)
     for (int jj = 0; jj < V; ++jj) present |= 1u << ((um >> (2 * jj)) & 3);
     stream_masks<V>(um, m0, m1);
   }
+  // mean of a head's squares: for a power-of-two H the product with 1/H is the
+  // same correctly rounded value as the quotient, without the division
+  const bool h_pow2 = (H & (H - 1)) == 0;
+  const float inv_h = 1.0f / (float)H;
+  auto mean_sq = [&](float ss) -> float { return h_pow2 ? ss * inv_h : ss / (float)H; };
   bool timed_out = false;
   for (int64_t j = 0;; ++j) {
     const int s = (int)(j % tp.K);
@@ -670,7 +675,7 @@ __global__ void __launch_bounds__(kTmaThreads, ROPE_TMA_MIN_CTAS)
               for (int u = 0; u < HB; ++u) ss[u] += __shfl_xor_sync(0xffffffffu, ss[u], o);
             }
 #pragma unroll
-            for (int u = 0; u < HB; ++u) r[u] = 1.0f / sqrtf(ss[u] / (float)H + a.eps);
+            for (int u = 0; u < HB; ++u) r[u] = 1.0f / sqrtf(mean_sq(ss[u]) + a.eps);
           }
 #pragma unroll
           for (int u = 0; u < HB; ++u) {
@@ -714,7 +719,7 @@ __global__ void __launch_bounds__(kTmaThreads, ROPE_TMA_MIN_CTAS)
               for (int u = 0; u < HB; ++u) ss[u] += __shfl_xor_sync(0xffffffffu, ss[u], o);
             }
 #pragma unroll
-            for (int u = 0; u < HB; ++u) r[u] = 1.0f / sqrtf(ss[u] / (float)H + a.eps);
+            for (int u = 0; u < HB; ++u) r[u] = 1.0f / sqrtf(mean_sq(ss[u]) + a.eps);
           }
 #pragma unroll
           for (int u = 0; u < HB; ++u) {
