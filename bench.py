@@ -22,6 +22,7 @@ import hashlib
 import json
 import math
 import os
+import re
 import subprocess
 import sys
 import tempfile
@@ -37,15 +38,16 @@ from rotary_position_embedding_gb300 import workloads as wl  # noqa: E402
 L2_BYTES = 129 * 2 ** 20
 FALLBACK_HBM_GBS = 6800.0
 METRIC = "RoPE achieved HBM GB/s and Gelem/s, fp16, as % of GB300 HBM roofline"
-# Device sources of each kernel family: a profiled DRAM figure is reported only
-# while the sources it was captured on are unchanged.
+# Sources of each kernel family -- its device code and the host code that plans
+# its launches (rope_api.cu): a profiled DRAM figure is reported only while the
+# code it was captured on is unchanged (comments and blank lines aside).
 KERNEL_SOURCES = {
-    "rope_rows_kernel": ["rope_kernels.cuh", "k_rope.cu", "k_mrope.cu"],
-    "rope_tma_kernel": ["rope_kernels.cuh", "rope_tma.cuh", "k_tma.cu"],
-    "rope_fused_kernel": ["rope_kernels.cuh", "rope_fused.cuh", "k_fused.cu"],
-    "rope_qkv_kernel": ["rope_kernels.cuh", "rope_qkv.cuh", "k_qkv.cu"],
-    "rope_qkv_tma_kernel": ["rope_kernels.cuh", "rope_tma.cuh", "rope_qkv.cuh", "rope_packed.cuh", "rope_qkv_tma.cuh",
-                            "k_qkv_tma.cu", "k_mrope_qkv_tma.cu"],
+    "rope_rows_kernel": ["rope_api.cu", "rope_kernels.cuh", "k_rope.cu", "k_mrope.cu"],
+    "rope_tma_kernel": ["rope_api.cu", "rope_kernels.cuh", "rope_tma.cuh", "k_tma.cu"],
+    "rope_fused_kernel": ["rope_api.cu", "rope_kernels.cuh", "rope_fused.cuh", "k_fused.cu"],
+    "rope_qkv_kernel": ["rope_api.cu", "rope_kernels.cuh", "rope_qkv.cuh", "k_qkv.cu", "k_mrope_qkv.cu"],
+    "rope_qkv_tma_kernel": ["rope_api.cu", "rope_kernels.cuh", "rope_tma.cuh", "rope_qkv.cuh", "rope_packed.cuh",
+                            "rope_qkv_tma.cuh", "k_qkv_tma.cu", "k_mrope_qkv_tma.cu"],
 }
 
 
@@ -96,11 +98,18 @@ def aggregate_throughput(nbytes, numel, steps, total_ms, world):
     return world * nbytes * steps / sec / 1e9, world * numel * steps / sec / 1e9
 
 
+def _code_only(text):
+    """C/C++/CUDA source without comments, trailing blanks or blank lines."""
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    lines = (re.sub(r"//.*$", "", ln).rstrip() for ln in text.splitlines())
+    return "\n".join(ln for ln in lines if ln)
+
+
 def kernel_source_hash(family):
     h = hashlib.sha256()
     for f in KERNEL_SOURCES[family]:
-        with open(os.path.join(ROOT, "rotary_position_embedding_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "rotary_position_embedding_gb300", "csrc", f), encoding="utf-8") as fh:
+            h.update(_code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -2,10 +2,12 @@
 // optional QK-RMSNorm) for sm_103a.
 //
 // The same operation as rope_qkv_kernel (rope_qkv.cuh) -- every Q and K head
-// rotated as RotaryEmbedding rotates one head of a rank-3 X, V copied, K and V
-// appended to the caches at rows past[b] + s -- with the bytes in flight held
-// in shared memory instead of registers, as in rope_tma_kernel. A tile is NG
-// heads of one role (Q, K or V) times TS consecutive tokens of one batch. A Q
+// rotated as RotaryEmbedding (or, in the MROPE instances, MRotaryEmbedding)
+// rotates one head of a rank-3 X, V copied, K and V appended to the caches at
+// rows past[b] + s -- with the bytes in flight held in shared memory instead
+// of registers, as in rope_tma_kernel. A tile is NG heads of one role (Q, K or
+// V) times TS consecutive tokens of one batch; RoPE gives every role the same
+// TS x NG, M-RoPE gives each role its own (host-planned, QRole). A Q
 // tile (and a K tile without caches) is one tensor box of TS x NG x H, laid
 // out in the stage as in the tensor and stored to q_out (k_out) as one box; a
 // cache tile is NG per-head boxes of TS x H, which are exactly TS consecutive
@@ -13,7 +15,8 @@
 //   copy warp  (lane 0) starts a tile's tensor copies into a free stage and
 //              writes the finished tile back with tensor stores;
 //   gather warp loads the tile's positions (a tile ahead) and gathers its
-//              cos/sin rows (Q and K tiles), one bulk copy per row;
+//              cos/sin rows (Q and K tiles): one bulk copy per row for RoPE,
+//              16-byte asynchronous copies for M-RoPE's three rows per token;
 //   consumers  normalise (RMSNorm) and rotate Q and K tiles in place; V tiles
 //              pass through untouched.
 // A cache tile that is ragged (the batch's last, partial token tile) or whose
@@ -30,6 +33,8 @@
 //  - onnxruntime pull request "Add RotaryEmbedding fusion for Qwen3 on-the-fly
 //    RoPE patterns": Verification and Qwen3 Architecture (RoPE on Q and K; GQA;
 //    QK-Norm: RMSNorm on Q and K before RoPE).
+//  - "com.microsoft.MRotaryEmbedding" README: Description, Inputs/positionIds
+//    (t, h, w streams), Attributes (mrope_section, mrope_layout, scale).
 #pragma once
 
 #include "rope_packed.cuh"
