@@ -75,9 +75,11 @@ __device__ __forceinline__ VecT<T, V> norm_weight(const VecT<T, V>& x, float r, 
 #ifndef ROPE_QKV_NORM_HOIST
 #define ROPE_QKV_NORM_HOIST 1
 #endif
-// M-RoPE heads gather three coefficient rows per unit: their own cap.
+// M-RoPE heads gather three coefficient rows per unit and merge them: their
+// own cap. 80 registers keep two CTAs of 384 threads per SM, as 64 do, without
+// spills (M-RoPE QK-Norm decode, 256 tokens: 5.2 us from a graph; 5.9 us at 64).
 #ifndef ROPE_QKV_MROPE_MAXNREG
-#define ROPE_QKV_MROPE_MAXNREG 64
+#define ROPE_QKV_MROPE_MAXNREG 80
 #endif
 #define ROPE_QKV_BOUNDS \
   __maxnreg__(MROPE ? ROPE_QKV_MROPE_MAXNREG : (NORM ? ROPE_QKV_NORM_MAXNREG : ROPE_QKV_MAXNREG))
@@ -86,9 +88,9 @@ __device__ __forceinline__ VecT<T, V> norm_weight(const VecT<T, V>& x, float r, 
 // README, Inputs/positionIds and Attributes): each of the unit's V coefficient
 // indices follows its stream's position pos3[stream, token]; a pair whose
 // position is outside the table is copied through (and reported in *oor);
-// the gathered coefficients are scaled and rounded to T first. The general
-// per-pair form (mrope_unit_general): these kernels serve the inputs the
-// pipelined kernel does not take.
+// the gathered coefficients are scaled and rounded to T first. 128-bit units
+// merge the three streams by bit masks; single-element units take the general
+// per-pair form (mrope_unit_general).
 template <class T, int V, bool INTER>
 __device__ __forceinline__ void mrope_qkv_unit(const KParams& p, int64_t tok, int k, const VecT<T, V>& a,
                                                const VecT<T, V>& bv, VecT<T, V>& ya, VecT<T, V>& yb,
@@ -118,7 +120,27 @@ __device__ __forceinline__ void mrope_qkv_unit(const KParams& p, int64_t tok, in
     }
   }
   if (present & ~valid) oor = true;
-  mrope_unit_general<T, V, INTER>(a, bv, cs, ss, um, valid, !p.scale_is_one, p.scale, ya, yb);
+  if constexpr (V * sizeof(bits) == 16) {
+    // 128-bit units: merge the streams with bit masks, rotate once, restore
+    // the pairs of out-of-range streams (as rope_rows_kernel does)
+    uint32_t m0[4], m1[4];
+    stream_masks<V>(um, m0, m1);
+    VT c = merge3(cs[0], cs[1], cs[2], m0, m1);
+    VT sn = merge3(ss[0], ss[1], ss[2], m0, m1);
+    if (!p.scale_is_one) {
+      scale_round<T, V>(c, p.scale);
+      scale_round<T, V>(sn, p.scale);
+    }
+    rotate_unit<T, V, INTER>(a, bv, c, sn, ya, yb);
+    if (present & ~valid) {
+      uint32_t ma[4], mb[4];
+      pair_masks<V, INTER>(um, valid, ma, mb);
+      blend(ya, a, ma);
+      blend(yb, bv, mb);
+    }
+  } else {
+    mrope_unit_general<T, V, INTER>(a, bv, cs, ss, um, valid, !p.scale_is_one, p.scale, ya, yb);
+  }
 }
 
 template <class T, int V, bool INTER, bool IMPLICIT, bool NORM, bool MROPE = false>

@@ -157,6 +157,13 @@ WORKLOADS = {
         dtype="float16", num_heads=32, positions="mrope", cache_rows=32768, rope_base=5.0e6, rope_dim=128,
         mrope_section=(24, 20, 20), mrope_layout=1, scale=1.0,
         extra={"kv_num_heads": 8, "max_len": 8192, "max_past": 4096, "rms_norm": True, "epsilon": 1e-6}),
+    # the same model's decode step: one token per sequence, 256 sequences, the
+    # rest of the K/V history already in the caches (SIMT Q/K kernel: 3 MB)
+    "mrope_qkv_norm_decode_r3_f16": Workload(
+        name="mrope_qkv_norm_decode_r3_f16", kind="qkv", rank=3, shape=(256, 1, (32 + 2 * 8) * 128),
+        dtype="float16", num_heads=32, positions="mrope", cache_rows=32768, rope_base=5.0e6, rope_dim=128,
+        mrope_section=(24, 20, 20), mrope_layout=1, scale=1.0,
+        extra={"kv_num_heads": 8, "max_len": 8192, "max_past": 8191, "rms_norm": True, "epsilon": 1e-6}),
     "fused_decode_r3_f16": Workload(
         name="fused_decode_r3_f16", kind="fused", rank=3, shape=(256, 1, 40 * 128), dtype="float16",
         num_heads=40, positions="uniform", cache_rows=32768, rope_base=1.0e6, rope_dim=128,

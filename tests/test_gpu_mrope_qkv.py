@@ -258,15 +258,17 @@ def test_mrope_qkv_tma_bits_equal_simt(lib, cuda, dt, norm, layout):
     assert out["simt"][3] == out["tma"][3] == (1 | 4)
 
 
-def test_mrope_qkv_workload_full_size(lib, orc, cuda):
-    """The benchmark's M-RoPE Q/K workload as the benchmark launches it (packed [Q|K|V], QK-Norm,
-    t/h/w ids with 1 % past the table, cache append): Q whole; the written K rows against the
-    oracle, V rows bit for bit; every other cache row keeps its fill."""
+@pytest.mark.parametrize("name,kernel", [("mrope_qkv_norm_prefill_r3_f16", "rope_qkv_tma_kernel"),
+                                         ("mrope_qkv_norm_decode_r3_f16", "rope_qkv_kernel")])
+def test_mrope_qkv_workload_full_size(lib, orc, cuda, name, kernel):
+    """The benchmark's M-RoPE Q/K workloads as the benchmark launches them (packed [Q|K|V],
+    QK-Norm, t/h/w ids with 1 % past the table, cache append): Q whole; the written K rows
+    against the oracle, V rows bit for bit; every other cache row keeps its fill."""
     import torch
 
     from rotary_position_embedding_gb300 import workloads as wl
 
-    w = wl.WORKLOADS["mrope_qkv_norm_prefill_r3_f16"]
+    w = wl.WORKLOADS[name]
     inp = wl.make_inputs(w)
     x, inv, past, pos = inp["x"], inp["inv_freq"], inp["past_seq_lens"], inp["position_ids"]
     B, S, H, Nq, Nkv, L = w.batch, w.seq, w.head_size, w.num_heads, w.extra["kv_num_heads"], w.extra["max_len"]
@@ -289,7 +291,7 @@ def test_mrope_qkv_workload_full_size(lib, orc, cuda):
                                  q_norm_weight=_dev(nkw["q_norm_weight"], torch, cuda),
                                  k_norm_weight=_dev(nkw["k_norm_weight"], torch, cuda), epsilon=nkw["epsilon"])
     torch.cuda.synchronize()
-    assert lib.last_kernel() == "rope_qkv_tma_kernel"
+    assert lib.last_kernel() == kernel
     assert ko is None and int(status.item()) == 1
     compare_norm(_host(qo), q_ref, Nq, H, H, 0)
     rows = past[:, None].astype(np.int64) + np.arange(S)[None, :]
