@@ -618,14 +618,17 @@ rope_status plan_qkv_tma(rope_dtype dt, const Geom& g, int es, const QKVParams& 
   tp.r[0].head_off = 0;
   tp.r[1].head_off = packed ? a.Nq : 0;
   tp.r[2].head_off = packed ? a.Nq + a.Nkv : 0;
-  const size_t smem = tp.bar_bytes + (size_t)K * tp.stage_bytes;
+  // pipes pipelines per CTA, each with its own barriers and stages
+  const int pipes_per_cta = qkv_pipes(mrope);
+  const size_t smem = pipes_per_cta * (tp.bar_bytes + (size_t)K * tp.stage_bytes);
+  const int threads = kTmaThreads * pipes_per_cta;
 
   int sms = 0, per_sm = 0;
-  rope_status st = device_facts(fn, kTmaThreads, smem, &sms, &per_sm);
+  rope_status st = device_facts(fn, threads, smem, &sms, &per_sm);
   if (st != ROPE_OK) return st;
-  const int64_t gx = pipeline_grid((int64_t)sms * per_sm, tp.ntiles);
-  T->L.grid = dim3((unsigned)gx, 1, 1);
-  T->L.block = dim3(kTmaThreads, 1, 1);
+  const int64_t pipes = pipeline_grid((int64_t)sms * per_sm * pipes_per_cta, tp.ntiles);
+  T->L.grid = dim3((unsigned)((pipes + pipes_per_cta - 1) / pipes_per_cta), 1, 1);
+  T->L.block = dim3(threads, 1, 1);
   T->L.smem = smem;
 
   // maps: sources (H, heads, S, B) and q_out / k_out (H, heads, S, B) with a

@@ -62,6 +62,21 @@ __device__ __forceinline__ void cp_async_arrive_pending(uint32_t bar) {
   asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
 }
 
+// Pipelines per CTA. With two, a CTA holds two independent copies of the
+// pipeline (copy warp, gather warp, 8 consumers, K stages) whose warps
+// interleave (even warps pipeline 0, odd warps pipeline 1), in place of two
+// CTAs per SM. Two resident CTAs do not progress alike: the one launched first
+// refills its stages faster, and the other finishes last. For M-RoPE the
+// single two-pipeline CTA measured faster (44.6 against 46.0 us on the
+// M-RoPE QK-Norm prefill), for RoPE slower (37.7 against 36.1 us with the norm).
+#ifndef ROPE_QKV_TMA_PIPES
+#define ROPE_QKV_TMA_PIPES 1
+#endif
+#ifndef ROPE_QKV_TMA_MROPE_PIPES
+#define ROPE_QKV_TMA_MROPE_PIPES 2
+#endif
+__host__ __device__ constexpr int qkv_pipes(bool mrope) { return mrope ? ROPE_QKV_TMA_MROPE_PIPES : ROPE_QKV_TMA_PIPES; }
+
 // Heads a consumer thread loads and reduces together.
 #ifndef ROPE_QKV_TMA_HEAD_BATCH
 #define ROPE_QKV_TMA_HEAD_BATCH 2
@@ -192,7 +207,7 @@ __device__ __forceinline__ Unit8<T> norm8p(const float2 (&fx)[4], float r, const
 }
 
 template <class T, bool INTER, bool IMPLICIT, bool NORM, bool MROPE = false>
-__global__ void __launch_bounds__(kTmaThreads, ROPE_TMA_MIN_CTAS)
+__global__ void __launch_bounds__(kTmaThreads * qkv_pipes(MROPE), ROPE_TMA_MIN_CTAS / qkv_pipes(MROPE))
     rope_qkv_tma_kernel(const KParams p, const QKVParams a, const QTParams tp,
                         const __grid_constant__ QKVMaps maps) {
   using E = Elem<T>;
@@ -200,18 +215,25 @@ __global__ void __launch_bounds__(kTmaThreads, ROPE_TMA_MIN_CTAS)
   constexpr int V = 16 / sizeof(bits);
   using VT = VecT<T, V>;
 
-  extern __shared__ __align__(1024) unsigned char smem[];
+  constexpr int kQkvPipes = qkv_pipes(MROPE);
+  extern __shared__ __align__(1024) unsigned char smem_all[];
+  // this thread's pipeline: its shared memory, and its index among all
+  // pipelines (vb of vg), which the schedule uses as a CTA index
+  const int pipe = (int)(threadIdx.x >> 5) % kQkvPipes;
+  const int warp = (int)(threadIdx.x >> 5) / kQkvPipes;
+  const int lane = threadIdx.x & 31;
+  unsigned char* smem = smem_all + (size_t)pipe * (tp.bar_bytes + (size_t)tp.K * tp.stage_bytes);
+  const int64_t vb = (int64_t)blockIdx.x * kQkvPipes + pipe;
+  const int64_t vg = (int64_t)gridDim.x * kQkvPipes;
   const uint32_t sbase = smem_addr(smem);
   const uint32_t full0 = sbase;                // full[s]      at 8*s
   const uint32_t done0 = sbase + 8 * tp.K;     // computed[s]  at 8*(K+s)
   const uint32_t issued0 = sbase + 16 * tp.K;  // issued[s]    at 8*(2K+s)
   unsigned char* stage0 = smem + tp.bar_bytes;
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
   const int H = (int)p.H;
   const int h = p.h;
 
-  if (threadIdx.x == 0) {
+  if (warp == 0 && lane == 0) {
     for (int s = 0; s < tp.K; ++s) {
       mbar_init(full0 + 8 * s, 33);  // the copies' arrive.expect_tx + every gather lane
       mbar_init(done0 + 8 * s, kTmaConsumerWarps);
@@ -239,13 +261,13 @@ __global__ void __launch_bounds__(kTmaThreads, ROPE_TMA_MIN_CTAS)
     if (lane == 0) {
       const uint64_t pol = policy_evict_first();
       bool timed_out = false;
-      // Tile indices: blockIdx.x + jj*gridDim.x (static schedule), or -- with
+      // Tile indices: vb + jj*vg (static schedule), or -- with
       // a caller scratch counter -- the next value of the counter, so CTAs
       // that run faster take more tiles. Each index is recorded in its stage
       // header; the first index past the last tile (the sentinel) ends the
       // pipeline.
       auto pick = [&](int64_t jj) -> int64_t {
-        return p.sched ? (int64_t)atomicAdd(p.sched, 1ull) : (int64_t)blockIdx.x + jj * (int64_t)gridDim.x;
+        return p.sched ? (int64_t)atomicAdd(p.sched, 1ull) : vb + jj * vg;
       };
       auto issue = [&](int64_t jj, int64_t t) {
         const int s = (int)(jj % tp.K);
@@ -327,7 +349,7 @@ __global__ void __launch_bounds__(kTmaThreads, ROPE_TMA_MIN_CTAS)
       if (p.sched) {
         // The last CTA to stop drawing resets the counter pair for the next launch.
         __threadfence();
-        if (atomicAdd(p.sched + 1, 1ull) == (unsigned long long)gridDim.x - 1) {
+        if (atomicAdd(p.sched + 1, 1ull) == (unsigned long long)vg - 1) {
           p.sched[0] = 0;
           p.sched[1] = 0;
           __threadfence();
@@ -388,7 +410,7 @@ __global__ void __launch_bounds__(kTmaThreads, ROPE_TMA_MIN_CTAS)
     Pre cur{};
     bool have_cur = false;
     if (!p.sched) {
-      cur = prefetch(blockIdx.x);
+      cur = prefetch(vb);
       have_cur = true;
     }
     for (int64_t j = 0;; ++j) {
@@ -406,7 +428,7 @@ __global__ void __launch_bounds__(kTmaThreads, ROPE_TMA_MIN_CTAS)
       Pre nxt{};
       bool have_nxt = false;
       if (!p.sched) {
-        nxt = prefetch(t + gridDim.x);  // this CTA's next tile
+        nxt = prefetch(t + vg);  // this pipeline's next tile
         have_nxt = true;
       } else {
         // headers are published in tile order and tile j+1-K's phase of this
@@ -520,7 +542,7 @@ __global__ void __launch_bounds__(kTmaThreads, ROPE_TMA_MIN_CTAS)
   // are an aligned lane group that adds up the row's squares with shuffles.
   // A role's TS x nP columns are a multiple of nP, so the unit k is the same
   // in every role's layout; ts and hq follow the tile's role.
-  const int qi = threadIdx.x - 32 * kTmaRoleWarps;
+  const int qi = (warp - kTmaRoleWarps) * 32 + lane;
   const int nP = p.nP;
   const int k = qi - nP * (int)div_by((uint32_t)qi, tp.by_nP);
   int oa, ob;
