@@ -361,15 +361,16 @@ __global__ void __launch_bounds__(kTmaThreads * qkv_pipes(MROPE), ROPE_TMA_MIN_C
 
   if (warp == 1) {
     // ------------------------------------------------------------ gather warp
-    // Per Q or K tile: the tokens' positions (explicit, or past[b] + s) and
-    // range flags, then the cos/sin rows ([token][cos|sin][rd/2]) copied 16
-    // bytes at a time; the copies arrive on full[s] when they land. V tiles
-    // gather nothing. Cache tiles also get their first row in the header.
+    // Per Q or K tile: the tokens' positions (explicit, or past[b] + s; M-RoPE:
+    // t, h, w) and range flags, then the cos/sin rows ([token][stream][cos|sin]
+    // [rd/2]); the copies arrive on full[s] when they land. V tiles gather
+    // nothing. Cache tiles also get their first row in the header.
     const bits* cosb = static_cast<const bits*>(p.cos);
     const bits* sinb = static_cast<const bits*>(p.sin);
     bool timed_out = false;
-    // Row r of a tile's coefficient block (the cos or sin row of token r / 2,
-    // row_bytes at byte r*row_bytes) goes to lane r % 32 as one bulk copy.
+    // RoPE: row r of a tile's coefficient block (the cos or sin row of token
+    // r / 2, row_bytes at byte r*row_bytes) goes to lane r % 32 as one bulk
+    // copy. M-RoPE: 16-byte pieces, piece c by lane c % 32 (below).
     const uint32_t row_bytes = (uint32_t)h * (uint32_t)sizeof(bits);
     constexpr int SLOTS = MROPE ? 3 : 1;  // coefficient rows per token: one per position stream
     // M-RoPE: the streams some coefficient index uses (an unused stream's
