@@ -2,10 +2,15 @@
 """Throughput benchmark of the rotary position embedding hot path on GB300.
 
 One step = one pass of RotaryEmbedding over one batch of the headline
-workload (rank-3 float16 X (4, 2048, 32*128), half split, position_ids
-gather from an (8192, 64) cos/sin cache), launched through the library's C
-ABI. Inputs are resident in HBM when the timed region starts; X/Y rotate over
-enough buffer sets that no step finds its inputs in L2.
+workload, the largest published configuration: rank-4 float16 X
+(8, 32, 4096, 128), interleaved pairs, rotary_embedding_dim 64 (the other 64
+elements of every head copied through), position_ids uniform over a
+(16384, 32) cos/sin cache; 541 MB of algorithmic traffic per pass. Launched
+through the library's C ABI. Inputs are resident in HBM when the timed region
+starts; X/Y rotate over enough buffer sets that no step finds its inputs in
+L2. The other published configurations (the rank-3 gather, M-RoPE in both
+layouts, the decode step, the float32 parity case) are timed after the timed
+region and summarised under ``roofline.configs``.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gpu|reference]
 
@@ -58,7 +63,8 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=200)
     ap.add_argument("--impl", choices=["gpu", "reference"], default="gpu")
     ap.add_argument("--workload", default=wl.HEADLINE, choices=list(wl.WORKLOADS))
-    ap.add_argument("--no-rows", action="store_true", help="skip the per-workload table")
+    ap.add_argument("--no-rows", action="store_true",
+                    help="time only the published configurations, not every workload")
     ap.add_argument("--row-steps", type=int, default=400)
     ap.add_argument("--e2e-steps", type=int, default=30)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
@@ -433,6 +439,23 @@ def n_buffer_sets(w):
     return max(2, math.ceil(4 * L2_BYTES / per_set))
 
 
+def config_of(w, world):
+    """The ``config`` object of the JSON line: the workload and how it is fed.
+    Both arms print the same one."""
+    n = n_buffer_sets(w)
+    return {
+        "workload": w.name, "shape": list(w.shape), "num_heads": w.num_heads,
+        "head_size": w.head_size, "rotary_dim": w.rotary_dim, "interleaved": w.interleaved,
+        "cache_rows": w.cache_rows, "positions": POSITION_RECIPES[w.positions],
+        "algorithmic_bytes_per_step": wl.algorithmic_bytes(w),
+        "l2": f"inputs rotate over {n} X/Y buffer sets "
+              f"({n * 2 * w.numel * wl.itemsize(w.dtype) / 2**20:.0f} MiB) > 129 MiB L2; no flush kernel",
+        "launch": "one C-ABI call per step on the current stream, queued ahead of the GPU; "
+                  "timed region = one CUDA event pair around the K steps",
+        "parallelism": f"{world} independent replicas (per-GPU batch)",
+    }
+
+
 def time_steps(torch, step, steps, stream_handle, fused=False):
     """Time `steps` back-to-back launches (rotating buffer sets) with one CUDA
     event pair on the launching stream around all of them."""
@@ -468,6 +491,34 @@ def time_isolated(torch, step, samples, stream_handle, fused=False):
         ends[k].record()
     torch.cuda.synchronize()
     return [a.elapsed_time(b) for a, b in zip(starts, ends)]
+
+
+def isolation_floor(torch, step, samples, stream_handle):
+    """What an isolated launch costs beyond the kernel, measured the same way
+    as time_isolated (device sleep, then an event pair around one launch):
+      - an empty kernel (torch's device sleep of 0 cycles): the event pair and
+        the launch of a one-block grid;
+      - a device-to-device copy of X into Y (torch ``copy_``): the same pair
+        and launch around a plain stream of 2 |X| bytes, whose own ramp and
+        drain a bandwidth-bound kernel also pays.
+    Medians in microseconds."""
+    n_sets = len(step.xs)
+    res = {}
+    for label in ("empty_kernel", "copy_x_to_y"):
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(samples)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(samples)]
+        torch.cuda.synchronize()
+        for k in range(samples):
+            torch.cuda._sleep(100_000)
+            starts[k].record()
+            if label == "empty_kernel":
+                torch.cuda._sleep(0)
+            else:
+                step.ys[k % n_sets].copy_(step.xs[k % n_sets])
+            ends[k].record()
+        torch.cuda.synchronize()
+        res[label + "_us"] = round(float(np.median([a.elapsed_time(b) for a, b in zip(starts, ends)])) * 1e3, 3)
+    return res
 
 
 def time_graph(torch, step, launches, replays, fused=False):
@@ -550,11 +601,21 @@ def gpu_arm(args, rank, world, local_rank):
     peak, peak_src = measured_peak()
     achieved = nbytes / (kern_ms * 1e-3) / 1e9
     # context, outside the timed region: the same launch bracketed alone by an event pair
-    iso_ms = float(np.median(time_isolated(torch, step, min(200, args.steps), sh, fused=fused)))
+    iso_ms = float(np.median(time_isolated(torch, step, 200, sh, fused=fused)))
+    floor = isolation_floor(torch, step, 200, sh) if isinstance(step, Step) else None
+    if kernel_family == "rope_rows_kernel":
+        schedule = "n/a (SIMT kernel: fixed thread roles, no scratch)"
+    elif isinstance(step, QKVStep) or args.schedule == "static":
+        schedule = "static (tiles dealt round robin, no scratch)"
+    else:
+        schedule = "dynamic (tiles drawn from a 64-byte scratch counter per stream)"
 
     out = None
     if rank == 0:
-        rows = {} if (args.no_rows or args.quick) else measure_rows(args, torch, rp, device, peak)
+        rows = {}
+        if not args.quick:
+            rows = measure_rows(args, torch, rp, device, peak,
+                                names=wl.CONFIGS if args.no_rows else list(wl.WORKLOADS))
         e2e = None if (args.quick or fused) else measure_e2e(args, torch, step, sh, nbytes)
         cpu = cpu_baseline(args, w) if (world == 1 and not args.quick) else None
         out = {
@@ -573,25 +634,13 @@ def gpu_arm(args, rank, world, local_rank):
             "dtype": {"float32": "f32", "float16": "f16", "bfloat16": "bf16"}[w.dtype],
             "data": "synthetic (seeded N(0,1) X, position ids per the workload recipe; caches from "
                     "rope_cache_build)",
-            "config": {
-                "workload": w.name, "shape": list(w.shape), "num_heads": w.num_heads,
-                "head_size": w.head_size, "rotary_dim": w.rotary_dim, "interleaved": w.interleaved,
-                "cache_rows": w.cache_rows, "positions": POSITION_RECIPES[w.positions],
-                "algorithmic_bytes_per_step": nbytes,
-                "l2": f"inputs rotate over {len(step.xs)} X/Y buffer sets "
-                      f"({len(step.xs) * 2 * w.numel * 2 / 2**20:.0f} MiB) > 129 MiB L2; no flush kernel",
-                "launch": "one C-ABI call per step on torch's current stream; the host queues launches "
-                          "ahead of the GPU; timed region = one CUDA event pair around the K steps, "
-                          "nothing else in it",
-                "parallelism": f"{world} independent replicas (per-GPU batch)",
-                "schedule": args.schedule + (" (tiles drawn from a scratch counter)" if args.schedule == "dynamic"
-                                             else " (tiles dealt round robin)"),
-            },
+            "config": config_of(w, world),
             "roofline": {
                 "bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "traffic": profiled_traffic(kernel_family, w.name),
                 "peak_source": peak_src,
                 "kernel": f"{kernel_family} (variant {args.variant}: the one kernel of the step)",
+                "schedule": schedule,
                 "kernel_us": round(kern_ms * 1e3, 3),
                 "kernel_us_how": "timed region / K on the launching stream (a step is one launch of this "
                                  "kernel, back to back as in a real stream)",
@@ -600,7 +649,9 @@ def gpu_arm(args, rank, world, local_rank):
                 "isolated_how": "median of 200 launches each bracketed alone by its own event pair behind a "
                                 "short device sleep, outside the timed region (no overlap with a previous "
                                 "launch)",
+                "isolated_floor": floor,
                 "frac_of_nominal_8tbs": round(achieved / 8000.0, 4),
+                "configs": config_summary(rows, peak),
             },
             "clocks": clocks,
             "e2e": e2e,
@@ -614,8 +665,8 @@ def gpu_arm(args, rank, world, local_rank):
     return out
 
 
-def measure_rows(args, torch, rp, device, peak):
-    """Every workload (and both M-RoPE layouts, fused and cached decode), timed three ways:
+def measure_rows(args, torch, rp, device, peak, names):
+    """The workloads `names` (both M-RoPE layouts, fused and cached decode), timed three ways:
     each launch alone between its own event pair behind a device sleep
     (median), back to back from the host (includes the host's per-call cost
     where that exceeds the kernel), and replayed from a CUDA graph of 64
@@ -624,7 +675,8 @@ def measure_rows(args, torch, rp, device, peak):
     sh = ctypes.c_void_p(stream.cuda_stream)
     rows = {}
     prev = rp.get_variant()
-    for name, w in wl.WORKLOADS.items():
+    for name in names:
+        w = wl.WORKLOADS[name]
         variants = [("cached", False, "auto"), ("cached", False, "simt")]
         if w.kind in ("fused", "mrope_fused"):
             variants = [("fused", True, "auto"), ("cached", False, "auto")]
@@ -635,6 +687,8 @@ def measure_rows(args, torch, rp, device, peak):
             rp.set_variant(variant)
             for k in range(20):
                 step.launch(k % len(step.xs), sh, fused)
+            torch.cuda.synchronize()
+            kernel = rp.last_kernel() if not (w.kind == "qkv" and not fused) else "mixed (torch + library)"
             total_ms = time_steps(torch, step, args.row_steps, sh, fused)
             kern = time_isolated(torch, step, min(200, args.row_steps), sh, fused)
             graph_ms = None
@@ -646,6 +700,7 @@ def measure_rows(args, torch, rp, device, peak):
             gbs = nbytes / (kern_ms * 1e-3) / 1e9
             key = f"{name}:{label}:{variant}"
             rows[key] = {
+                "kernel": kernel,
                 "us_per_launch_median": round(kern_ms * 1e3, 3),
                 "us_per_step_incl_gaps": round(total_ms / args.row_steps * 1e3, 3),
                 "GB_s": round(gbs, 1), "Gelem_s": round(w.numel / (kern_ms * 1e-3) / 1e9, 2),
@@ -671,6 +726,28 @@ def measure_rows(args, torch, rp, device, peak):
     return rows
 
 
+def config_summary(rows, peak):
+    """Compact figures of every published configuration: kernel, microseconds
+    back to back (timed region / launches), from a CUDA graph and alone (median
+    of event-bracketed single launches), and the fractions of the measured
+    peak they give with the configuration's algorithmic bytes."""
+    out = {}
+    for name in wl.CONFIGS:
+        w = wl.WORKLOADS[name]
+        label = "fused" if w.kind in ("fused", "mrope_fused") else "cached"
+        r = rows.get(f"{name}:{label}:auto")
+        if r is None:
+            continue
+        nb = r["bytes"]
+        d = {"kernel": r["kernel"], "bytes": nb, "us_b2b": r["us_per_step_incl_gaps"],
+             "us_graph": r.get("us_per_step_graph"), "us_isolated": r["us_per_launch_median"]}
+        for k in ("b2b", "graph", "isolated"):
+            us = d["us_" + k]
+            d["frac_" + k] = None if not us else round(nb / (us * 1e-6) / 1e9 / peak, 4)
+        out[name] = d
+    return out
+
+
 def measure_e2e(args, torch, step, sh, nbytes):
     """Same metric through the C ABI with host buffers, every step: H2D of that
     step's X and positions from pinned memory, the launch, D2H of Y into pinned
@@ -684,36 +761,45 @@ def measure_e2e(args, torch, step, sh, nbytes):
     yd = [step.ys[0], step.ys[1 % len(step.ys)]]
     pd = [step.pos, None if step.pos is None else step.pos.clone()]
 
-    def one(k):
+    def one(k, kernel=True):
         i = k % 2
         with torch.cuda.stream(streams[i]):
             xd[i].copy_(x_host[i], non_blocking=True)
             if pos_host is not None:
                 pd[i].copy_(pos_host, non_blocking=True)
-            step.call(ctypes.c_void_p(xd[i].data_ptr()), ctypes.c_void_p(yd[i].data_ptr()),
-                      ctypes.c_void_p(streams[i].cuda_stream), pos=pd[i])
+            if kernel:
+                step.call(ctypes.c_void_p(xd[i].data_ptr()), ctypes.c_void_p(yd[i].data_ptr()),
+                          ctypes.c_void_p(streams[i].cuda_stream), pos=pd[i])
             y_host[i].copy_(yd[i], non_blocking=True)
 
-    for k in range(4):
-        one(k)
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for s_ in streams:
-        s_.wait_event(e0)
-    for k in range(args.e2e_steps):
-        one(k)
-    for s_ in streams:
-        torch.cuda.current_stream().wait_stream(s_)
-    e1.record()
-    torch.cuda.synchronize()
-    ms = e0.elapsed_time(e1) / args.e2e_steps
+    def timed(kernel):
+        for k in range(4):
+            one(k, kernel)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for s_ in streams:
+            s_.wait_event(e0)
+        for k in range(args.e2e_steps):
+            one(k, kernel)
+        for s_ in streams:
+            torch.cuda.current_stream().wait_stream(s_)
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / args.e2e_steps
+
+    ms = timed(True)
+    # the same loop with the copies only: the host link's own ceiling for this step
+    ms_copies = timed(False)
     h2d = x_host[0].numel() * x_host[0].element_size() + (0 if pos_host is None else pos_host.numel() * 8)
     d2h = y_host[0].numel() * y_host[0].element_size()
     return {"value": round(nbytes / (ms * 1e-3) / 1e9, 2), "unit": "GB/s", "ms_per_step": round(ms, 4),
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "note": "per step: pinned host X/positions -> device, rope_apply, device Y -> pinned host; two "
-                    "streams alternate steps; the cos/sin cache stays resident (model constant)"}
+            "copies_only": {"value": round(nbytes / (ms_copies * 1e-3) / 1e9, 2), "unit": "GB/s",
+                            "ms_per_step": round(ms_copies, 4),
+                            "link_GB_s": round((h2d + d2h) / (ms_copies * 1e-3) / 1e9, 1)},
+            "note": "transfer-bound: per step pinned host X/positions -> device, rope_apply, device Y -> "
+                    "pinned host, two streams alternating; copies_only = the same loop without the kernel"}
 
 
 # ---------------------------------------------------------------------------
@@ -830,11 +916,10 @@ def reference_arm(args, rank, world):
         "ms_per_step": round(el / args.steps * 1e3, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": {"float32": "f32", "float16": "f16", "bfloat16": "bf16"}[w.dtype],
         "data": "synthetic (same generator as the GPU arm)",
-        "config": {"workload": w.name, "shape": list(w.shape), "sample_tokens_per_step": st.tokens,
-                   "note": "the pages publish no implementation to run; the reference arm is the CPU "
-                           "oracle on a bounded sample of the workload per step"},
+        "config": config_of(w, world),
         "cpu_baseline": {"value": round(gbs, 5), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                         "sample": f"{st.tokens} of {w.tokens} tokens per step"},
+                         "sample": f"{st.tokens} of {w.tokens} tokens per step (bytes scaled to the sample); "
+                                   "the pages publish no implementation to run, so this arm is the CPU oracle"},
         "e2e": {"value": round(gbs, 5), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
     }

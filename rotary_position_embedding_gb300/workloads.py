@@ -96,7 +96,8 @@ class Workload:
 
 
 # The five workloads. Sizes follow the operator's published configurations;
-# the gather workload is the headline benchmark.
+# the largest of them, the rank-4 interleaved partial rotation (541 MB a
+# pass), is the headline benchmark.
 WORKLOADS = {
     "rope_r4_f32_cache3d": Workload(
         name="rope_r4_f32_cache3d", kind="rope", rank=4, shape=(1, 2, 8, 16), dtype="float32",
@@ -170,7 +171,13 @@ WORKLOADS = {
         attention_scaling=1.0),
 }
 
-HEADLINE = "rope_r3_f16_gather"
+HEADLINE = "rope_r4_f16_interleaved_partial"
+
+# The published configurations in order (the rank-4 float32 parity case, the
+# rank-3 gather, the rank-4 partial rotation, M-RoPE in both layouts, the
+# decode step with on-the-fly coefficients).
+CONFIGS = ["rope_r4_f32_cache3d", "rope_r3_f16_gather", "rope_r4_f16_interleaved_partial",
+           "mrope_r3_f16_layout0", "mrope_r3_f16_layout1", "fused_decode_r3_f16"]
 
 
 # numpy has no bfloat16: bfloat16 data is carried as its uint16 bit patterns.
