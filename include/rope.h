@@ -422,12 +422,14 @@ rope_status mrope_apply_qkv(rope_dtype dtype, int64_t batch, int64_t seq, int32_
  *
  * Arguments, results and errors are those of rope_apply without `scratch`
  * (shapes the pipelined kernel cannot take run the SIMT kernels, which use no
- * scratch). The first call on a device sets the array up (finds its device
- * address and clears it, synchronously), so make that first call before any
- * stream capture that includes this entry point. Every call on a device shares
- * the one array and each completed launch leaves it cleared for the next:
- * calls that overlap on the GPU (different streams, different threads) race on
- * it and must not be issued; calls in one stream are fine.
+ * scratch). The first call on a device (and again after the device was reset,
+ * or from another context on it) sets the array up: it looks up the array's
+ * device address for the current context. Make that first call before any
+ * stream capture that includes this entry point. The array is zero when the
+ * library's device code is loaded, every call on a device shares it, and each
+ * completed launch leaves it zero for the next: calls that overlap on the GPU
+ * (different streams, different threads) race on it and must not be issued;
+ * calls in one stream are fine.
  */
 rope_status rope_apply_no_alloc(rope_dtype dtype, int32_t x_rank, const int64_t* x_shape,
                                 const void* x, void* y, int32_t cache_rank,

@@ -5,6 +5,7 @@
 // pre-sized buffers for inputs and outputs, and callers without a device
 // allocator of their own. This entry point takes its scratch from a fixed
 // array that lives in the library's own device memory instead.
+#include <cuda.h>  // CUcontext; the two driver calls are fetched at run time
 #include <cuda_runtime.h>
 
 #include <cstdio>
@@ -18,27 +19,67 @@ namespace {
 // The schedule's scratch, shared by every call on a device. Fixed size: the
 // pipelined kernel's counter pair needs 16 of these bytes whatever the shapes,
 // so no input can need more. Device memory of the library image: every GPU
-// that loads the library holds it until the process exits.
+// that loads the library holds it until the process exits. It is zero when
+// the module is loaded, and every launch that uses it leaves it zero again.
 constexpr size_t kNoAllocScratchBytes = 256;
 static_assert(ROPE_SCRATCH_BYTES <= kNoAllocScratchBytes, "static scratch smaller than the schedule needs");
 static __device__ __align__(256) unsigned char g_no_alloc_scratch[kNoAllocScratchBytes];
 
 constexpr int kMaxDevices = 64;
+
+// The array's device address as seen from one context. A context's unique id
+// (cuCtxGetId) is never reused within the process, so a reset device or a
+// different context on the same device never matches an old entry.
+struct ScratchAddr {
+  unsigned long long ctx_id = 0;  // 0: not set up
+  void* ptr = nullptr;
+};
 std::mutex g_mu;
-void* g_scratch_addr[kMaxDevices];  // device address of g_no_alloc_scratch, per device
+ScratchAddr g_scratch_addr[kMaxDevices];
+
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
 
 // Failures are reported through rope_last_error(), like every other entry point.
 rope_status fail(rope_status st, const char* what, cudaError_t e) {
   char msg[256];
-  snprintf(msg, sizeof(msg), "%s: %s", what, e == cudaSuccess ? "" : cudaGetErrorString(e));
+  snprintf(msg, sizeof(msg), "%s%s%s", what, e == cudaSuccess ? "" : ": ",
+           e == cudaSuccess ? "" : cudaGetErrorString(e));
   rope_gb300::set_last_error(msg);
   return st;
 }
 
-// Set-up, once per device, with that device current: the array's device
-// address (in host code the symbol is only a host-side stand-in) and a cleared
-// array. It runs inside the first call on the device, which is why that first
-// call must not be made while the stream is being captured.
+// Unique id of the calling thread's current context, or 0 when none is
+// current yet (the runtime makes the device's primary context current on its
+// first call that needs one).
+bool current_context_id(unsigned long long* id) {
+  static std::once_flag once;
+  static CtxGetCurrentFn get_current = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<CtxGetCurrentFn>(f);
+    f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<CtxGetIdFn>(f);
+  });
+  if (!get_current || !get_id) return false;
+  CUcontext ctx = nullptr;
+  if (get_current(&ctx) != CUDA_SUCCESS) return false;
+  *id = 0;
+  if (ctx && get_id(ctx, id) != CUDA_SUCCESS) return false;
+  return true;
+}
+
+// Set-up, once per device and context, with that device current: the array's
+// device address (in host code the symbol is only a host-side stand-in, not
+// an address a kernel may be given). It runs inside the first call on the
+// device, which is why that first call must not be made while the stream is
+// being captured.
 rope_status scratch_for_current_device(void** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -46,16 +87,21 @@ rope_status scratch_for_current_device(void** out) {
   if (dev < 0 || dev >= kMaxDevices)
     return fail(ROPE_ERR_UNSUPPORTED, "device ordinal beyond the 64 devices rope_apply_no_alloc serves",
                 cudaSuccess);
+  unsigned long long id = 0;
+  if (!current_context_id(&id))
+    return fail(ROPE_ERR_CUDA, "cannot identify the current CUDA context (cuCtxGetCurrent / cuCtxGetId)",
+                cudaSuccess);
   std::lock_guard<std::mutex> lk(g_mu);
-  if (!g_scratch_addr[dev]) {
+  ScratchAddr& a = g_scratch_addr[dev];
+  if (id == 0 || a.ctx_id != id) {
     void* ptr = nullptr;
     e = cudaGetSymbolAddress(&ptr, g_no_alloc_scratch);
     if (e != cudaSuccess || !ptr) return fail(ROPE_ERR_CUDA, "cudaGetSymbolAddress(static scratch)", e);
-    e = cudaMemset(ptr, 0, kNoAllocScratchBytes);  // the schedule's counters start at zero
-    if (e != cudaSuccess) return fail(ROPE_ERR_CUDA, "clearing the static scratch", e);
-    g_scratch_addr[dev] = ptr;
+    if (id == 0 && !current_context_id(&id)) id = 0;  // the lookup made the primary context current
+    a.ptr = ptr;
+    a.ctx_id = id;
   }
-  *out = g_scratch_addr[dev];
+  *out = a.ptr;
   return ROPE_OK;
 }
 

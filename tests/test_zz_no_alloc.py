@@ -4,11 +4,14 @@ their input and output buffers, callers without a device allocator). It takes
 the dynamic tile schedule's scratch from a fixed array in the library's own
 device memory instead of a caller buffer.
 
-Checked through the C ABI against rope_apply on the same inputs, two calls in
-a row (the second call finds the array exactly as the first left it), with the
-tolerance every parity test here uses. This file is collected last so that a
-run stopping at the first failure has run every other test already; it also
-passes alone in a fresh process.
+Checked through the C ABI against rope_apply on the same inputs, three calls in
+a row (each call finds the array as the one before left it, so a counter left
+behind by one call would show on the next), with the tolerance every parity
+test here uses. Both cases are shapes the pipelined kernel takes (partial
+rotation, 16 MiB of float16), the only kernel that uses the scratch; each call
+asserts that this kernel ran. This file is collected last so that a run
+stopping at the first failure has run every other test already; it also passes
+alone in a fresh process.
 """
 
 import ctypes
@@ -34,34 +37,41 @@ def _call(so, fn, x, y, cos, sin, pos, N, rd, inter, stream, scratch=None, with_
     return fn(*args)
 
 
-@pytest.mark.parametrize("rank,inter,rd", [(3, 0, 0), (4, 1, 64)])
-def test_no_alloc_matches_rope_apply_twice(lib, orc, cuda, rank, inter, rd):
+@pytest.mark.parametrize("rank,inter,rd", [(3, 0, 64), (4, 1, 64)])
+def test_no_alloc_matches_rope_apply(lib, orc, cuda, rank, inter, rd):
     import torch
 
     so = lib.load_library()
-    rng = np.random.default_rng(41 + rank)
-    B, S, N, H = 2, 1024, 32, 128               # 16 MiB of float16: the pipelined (scratch) path
-    shape = (B, S, N * H) if rank == 3 else (B, N, S, H)
-    x = rng.standard_normal(shape).astype(np.float16)
-    h = (rd or H) // 2
-    R = 4096
-    cos, sin = orc.cache_build(wl.inv_freq(10000.0, rd or H, h), R, np.float16)
-    pos = rng.integers(0, R, (B, S))
-    pos[1, 7] = R + 1                           # one token past the table: copied through
-    nh = N if rank == 3 else 0
-    y_ref, _ = orc.rope(x, cos, sin, pos, inter, rd, nh)
-    xd = torch.from_numpy(x).to(cuda)
-    cd, sd, pd = (torch.from_numpy(a).to(cuda) for a in (cos, sin, pos))
-    stream = torch.cuda.current_stream().cuda_stream
+    prev = lib.get_variant()
+    lib.set_variant("auto")
+    try:
+        rng = np.random.default_rng(41 + rank)
+        B, S, N, H = 2, 1024, 32, 128           # 16 MiB of float16, partial rotation: the pipelined kernel
+        shape = (B, S, N * H) if rank == 3 else (B, N, S, H)
+        x = rng.standard_normal(shape).astype(np.float16)
+        h = rd // 2
+        R = 4096
+        cos, sin = orc.cache_build(wl.inv_freq(10000.0, rd, h), R, np.float16)
+        pos = rng.integers(0, R, (B, S))
+        pos[1, 7] = R + 1                       # one token past the table: copied through
+        nh = N if rank == 3 else 0
+        y_ref, _ = orc.rope(x, cos, sin, pos, inter, rd, nh)
+        xd = torch.from_numpy(x).to(cuda)
+        cd, sd, pd = (torch.from_numpy(a).to(cuda) for a in (cos, sin, pos))
+        stream = torch.cuda.current_stream().cuda_stream
 
-    y_api = torch.empty_like(xd)
-    assert _call(so, so.rope_apply, xd, y_api, cd, sd, pd, nh, rd, inter, stream, None, True) == 0
-    mask = rope_passthrough_mask(shape, rank, N, rd, pos, R)
-    for _ in range(2):
-        y_na = torch.full_like(xd, float("nan"))
-        st = _call(so, so.rope_apply_no_alloc, xd, y_na, cd, sd, pd, nh, rd, inter, stream)
-        assert st == 0, so.rope_last_error().decode()
-        torch.cuda.synchronize()
-        got = y_na.cpu().numpy()
-        compare(got, y_api.cpu().numpy(), x, rank, N, mask)   # against the existing entry point
-        compare(got, y_ref, x, rank, N, mask)                 # and against the oracle
+        y_api = torch.empty_like(xd)
+        assert _call(so, so.rope_apply, xd, y_api, cd, sd, pd, nh, rd, inter, stream, None, True) == 0
+        assert lib.last_kernel() == "rope_tma_kernel"
+        mask = rope_passthrough_mask(shape, rank, N, rd, pos, R)
+        for _ in range(3):
+            y_na = torch.full_like(xd, float("nan"))
+            st = _call(so, so.rope_apply_no_alloc, xd, y_na, cd, sd, pd, nh, rd, inter, stream)
+            assert st == 0, so.rope_last_error().decode()
+            assert lib.last_kernel() == "rope_tma_kernel"   # the kernel that uses the static scratch
+            torch.cuda.synchronize()
+            got = y_na.cpu().numpy()
+            compare(got, y_api.cpu().numpy(), x, rank, N, mask)   # against the existing entry point
+            compare(got, y_ref, x, rank, N, mask)                 # and against the oracle
+    finally:
+        lib.set_variant(prev)
