@@ -54,8 +54,9 @@ __global__ void __launch_bounds__(kMaxRowThreads) rope_fused_kernel(const KParam
   const int64_t n = (int64_t)blockIdx.y * p.NG + ng;
   const bool active = slot < p.TTs && n < p.N;
 
-  const bits* __restrict__ x = static_cast<const bits*>(p.x);
-  bits* __restrict__ y = static_cast<bits*>(p.y);
+  // x and y may be the same buffer (in place), so neither is __restrict__
+  const bits* x = static_cast<const bits*>(p.x);
+  bits* y = static_cast<bits*>(p.y);
   const int items = p.TTs * p.h;
   pdl_launch_dependents();
   pdl_wait();

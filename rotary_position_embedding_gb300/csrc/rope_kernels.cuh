@@ -436,8 +436,9 @@ __global__ void __launch_bounds__(kMaxRowThreads) rope_rows_kernel(const KParams
   pdl_wait();
   if (slot >= p.TTs || n >= p.N) return;  // no barrier below
 
-  const bits* __restrict__ x = static_cast<const bits*>(p.x);
-  bits* __restrict__ y = static_cast<bits*>(p.y);
+  // x and y may be the same buffer (in place), so neither is __restrict__
+  const bits* x = static_cast<const bits*>(p.x);
+  bits* y = static_cast<bits*>(p.y);
   const bits* __restrict__ cosb = static_cast<const bits*>(p.cos);
   const bits* __restrict__ sinb = static_cast<const bits*>(p.sin);
 
