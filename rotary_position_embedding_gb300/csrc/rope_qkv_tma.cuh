@@ -24,7 +24,10 @@
 // neither write rows past the batch's new tokens nor start at a negative row
 // -- but stored row by row by the consumers, which skip rows outside the cache
 // (status bit 2). Barrier protocol, bounded waits and the exit on a timeout
-// are those of rope_tma_kernel (rope_tma.cuh).
+// are those of rope_tma_kernel (rope_tma.cuh): a ring of 2K landed barriers
+// for the tile copies, full[s] for the gather lanes. Here the gather's RoPE
+// rows are bulk copies that complete on full[s], so a gather warp that gives
+// up also waits (bounded) for the full phases of the tiles it has served.
 //
 // Definitions followed (web pages, by title and section):
 //  - "com.microsoft.SparseAttention" README: Description, Inputs (query or
@@ -229,15 +232,21 @@ __global__ void __launch_bounds__(kTmaThreads * qkv_pipes(MROPE), ROPE_TMA_MIN_C
   const uint32_t full0 = sbase;                // full[s]      at 8*s
   const uint32_t done0 = sbase + 8 * tp.K;     // computed[s]  at 8*(K+s)
   const uint32_t issued0 = sbase + 16 * tp.K;  // issued[s]    at 8*(2K+s)
+  const uint32_t landed0 = sbase + 24 * tp.K;  // landed[b]    at 8*(3K+b), b < 2K
+  // tile jj's landed barrier and the parity of its phase there (see rope_tma.cuh)
+  auto landed_bar = [&](int64_t jj) -> uint32_t { return landed0 + 8 * (uint32_t)(jj % (2 * tp.K)); };
+  auto landed_par = [&](int64_t jj) -> uint32_t { return (uint32_t)((jj / (2 * tp.K)) & 1); };
   unsigned char* stage0 = smem + tp.bar_bytes;
   const int H = (int)p.H;
   const int h = p.h;
 
   if (warp == 0 && lane == 0) {
     for (int s = 0; s < tp.K; ++s) {
-      mbar_init(full0 + 8 * s, 33);  // the copies' arrive.expect_tx + every gather lane
+      mbar_init(full0 + 8 * s, 32);  // every gather lane
       mbar_init(done0 + 8 * s, kTmaConsumerWarps);
       mbar_init(issued0 + 8 * s, 1);
+      mbar_init(landed0 + 8 * s, 1);  // the tile copies' arrive.expect_tx (two per stage)
+      mbar_init(landed0 + 8 * (tp.K + s), 1);
     }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -275,15 +284,15 @@ __global__ void __launch_bounds__(kTmaThreads * qkv_pipes(MROPE), ROPE_TMA_MIN_C
         if (t < tp.ntiles) {
           const QTile q = qtile_of<!MROPE>(p, tp, t);
           const uint32_t dst = smem_addr(stage0 + (size_t)s * tp.stage_bytes);
-          mbar_arrive_expect_tx(full0 + 8 * s, q.R.x_bytes);
+          mbar_arrive_expect_tx(landed_bar(jj), q.R.x_bytes);
           // one NG-head box, or (cache tiles) one box per head
           const int nbox = qtile_wide(a, q) ? 1 : q.R.NG;
           for (int u = 0; u < nbox; ++u) {
             const int c[4] = {0, q.R.head_off + q.head0 + u, q.s0, q.b};
-            tma_load_x<true>(dst + (uint32_t)u * q.R.blk_bytes, &maps.src[q.role], c, full0 + 8 * s, pol);
+            tma_load_x<true>(dst + (uint32_t)u * q.R.blk_bytes, &maps.src[q.role], c, landed_bar(jj), pol);
           }
         } else {
-          mbar_arrive(full0 + 8 * s);  // the sentinel carries no bytes
+          mbar_arrive(landed_bar(jj));  // the sentinel carries no bytes
         }
         mbar_arrive(issued0 + 8 * s);
       };
@@ -306,7 +315,8 @@ __global__ void __launch_bounds__(kTmaThreads * qkv_pipes(MROPE), ROPE_TMA_MIN_C
         }
       };
       prep(t_st);
-      for (int64_t j = 0;; ++j) {
+      int64_t j = 0;  // the tile whose store comes next
+      for (;; ++j) {
         const int s = (int)(j % tp.K);
         if (!mbar_wait(done0 + 8 * s, (uint32_t)((j / tp.K) & 1))) {
           timed_out = true;
@@ -341,9 +351,9 @@ __global__ void __launch_bounds__(kTmaThreads * qkv_pipes(MROPE), ROPE_TMA_MIN_C
       }
       bulk_wait_all();
       if (timed_out) {
-        const uint64_t t0 = global_ns();
-        while (global_ns() - t0 < 1000000ull) {
-        }
+        // tiles j .. jx-1 were started and never stored: their loads land
+        // before the CTA's shared memory goes away (see rope_tma.cuh)
+        for (int64_t jj = j; jj < jx; ++jj) (void)mbar_wait(landed_bar(jj), landed_par(jj));
         if (p.oor_flag) atomicOr(p.oor_flag, 2);
       }
       if (p.sched) {
@@ -414,7 +424,8 @@ __global__ void __launch_bounds__(kTmaThreads * qkv_pipes(MROPE), ROPE_TMA_MIN_C
       cur = prefetch(vb);
       have_cur = true;
     }
-    for (int64_t j = 0;; ++j) {
+    int64_t j = 0;  // the tile served next
+    for (;; ++j) {
       const int s = (int)(j % tp.K);
       if (!__all_sync(0xffffffffu, mbar_wait(issued0 + 8 * s, (uint32_t)((j / tp.K) & 1)))) {
         timed_out = true;
@@ -533,7 +544,15 @@ __global__ void __launch_bounds__(kTmaThreads * qkv_pipes(MROPE), ROPE_TMA_MIN_C
       have_cur = have_nxt;
     }
     asm volatile("cp.async.wait_all;" ::: "memory");
-    if (timed_out && lane == 0 && p.oor_flag) atomicOr(p.oor_flag, 2);
+    if (timed_out) {
+      // The bulk copies of the last K tiles served may still be landing; each
+      // such tile's full phase has every lane's arrival, so it completes when
+      // they land (its next phase needs this warp's arrival for tile jj + K,
+      // never made: the parity wait cannot alias).
+      for (int64_t jj = j > tp.K ? j - tp.K : 0; jj < j; ++jj)
+        (void)mbar_wait(full0 + 8 * (int)(jj % tp.K), (uint32_t)((jj / tp.K) & 1));
+      if (lane == 0 && p.oor_flag) atomicOr(p.oor_flag, 2);
+    }
     return;
   }
 
@@ -580,9 +599,13 @@ __global__ void __launch_bounds__(kTmaThreads * qkv_pipes(MROPE), ROPE_TMA_MIN_C
   const float inv_h = 1.0f / (float)H;
   auto mean_sq = [&](float ss) -> float { return h_pow2 ? ss * inv_h : ss / (float)H; };
   bool timed_out = false;
-  for (int64_t j = 0;; ++j) {
-    const int s = (int)(j % tp.K);
-    const bool ok = __all_sync(0xffffffffu, mbar_wait(full0 + 8 * s, (uint32_t)((j / tp.K) & 1)));
+  // tile j's stage s and full parity, landed slot and parity (j % K,
+  // (j / K) & 1, j % 2K, (j / 2K) & 1), stepped once per tile
+  int s = 0, lsl = 0;
+  uint32_t ph = 0, lph = 0;
+  for (;;) {
+    const bool ok = __all_sync(0xffffffffu, mbar_wait(landed0 + 8 * (uint32_t)lsl, lph) &&
+                                                mbar_wait(full0 + 8 * s, ph));
     const int64_t t = ok ? *stage_hdr(s) : 0;
     if (ok && t >= tp.ntiles) {
       __syncwarp();
@@ -801,6 +824,14 @@ __global__ void __launch_bounds__(kTmaThreads * qkv_pipes(MROPE), ROPE_TMA_MIN_C
     fence_async_smem();  // this thread's smem writes, before the TMA store reads them
     __syncwarp();
     if (lane == 0) mbar_arrive(done0 + 8 * s);
+    if (++s == tp.K) {
+      s = 0;
+      ph ^= 1u;
+    }
+    if (++lsl == 2 * tp.K) {
+      lsl = 0;
+      lph ^= 1u;
+    }
   }
   if (timed_out && lane == 0 && p.oor_flag) atomicOr(p.oor_flag, 2);
 }

@@ -18,19 +18,29 @@
 // Pipeline protocol (per stage s, round r = tile index / K):
 //   issued[s]   count 1: the copy warp, after writing the stage's tile index
 //               (its header) and starting the copy.
-//   full[s]     count 33: the copy warp's arrive.expect_tx(tile bytes), whose
-//               TMA copy completes the transaction bytes, and one asynchronous
-//               arrive per gather lane, triggered when that lane's cp.async
-//               copies of the tile's cos/sin rows have landed.
+//   landed[b]   count 1, a ring of 2K (tile jj uses landed[jj mod 2K]): the
+//               copy warp's arrive.expect_tx(tile bytes), whose TMA copy
+//               completes the transaction bytes (a plain arrive for the
+//               sentinel). Only the copy hardware completes it, so the copy
+//               warp can always wait for its own loads. With 2K of them, the
+//               barrier of tile jj is reused by tile jj + 2K, which cannot be
+//               started before every warp has finished tile jj + K: a parity
+//               wait on tile jj's phase never sees a later one.
+//   full[s]     count 32: one asynchronous arrive per gather lane, triggered
+//               when that lane's cp.async copies of the tile's cos/sin rows
+//               have landed.
 //   computed[s] count = consumer warps: each consumer warp arrives after it
 //               has rotated its rows of the stage (and fenced them for TMA).
+// Consumers wait on tile j's landed barrier and full[s].
 // Tiles go to CTAs round robin, or -- when the caller gives a scratch counter --
 // to whichever CTA's copy warp asks next (dynamic schedule); an index past the
 // last tile (the sentinel) ends the pipeline.
 // Every wait is bounded (kWaitLimitNs of global time); a wait that runs out
 // sets bit 1 of the caller's status word (if given) and the kernel leaves
-// uniformly (each warp agrees through a warp vote), after the copy warp has
-// waited, again bounded, for the copies it issued.
+// uniformly (each warp agrees through a warp vote). No copy into shared
+// memory is left in flight when a CTA leaves: the gather warp waits for its
+// cp.async copies, and the copy warp waits, again bounded, on landed[] for
+// every tile load it started that no consumer has seen complete.
 //
 // Definitions followed: "ai.onnx.RotaryEmbedding" WebGPU manifest (inputs,
 // attributeDescriptions) and "com.microsoft.MRotaryEmbedding" README (Inputs,
@@ -291,6 +301,10 @@ __global__ void __launch_bounds__(kTmaThreads, ROPE_TMA_MIN_CTAS)
   const uint32_t full0 = sbase;                  // full[s]      at 8*s
   const uint32_t done0 = sbase + 8 * tp.K;       // computed[s]  at 8*(K+s)
   const uint32_t issued0 = sbase + 16 * tp.K;    // issued[s]    at 8*(2K+s)
+  const uint32_t landed0 = sbase + 24 * tp.K;    // landed[b]    at 8*(3K+b), b < 2K
+  // tile jj's landed barrier and the parity of its phase there
+  auto landed_bar = [&](int64_t jj) -> uint32_t { return landed0 + 8 * (uint32_t)(jj % (2 * tp.K)); };
+  auto landed_par = [&](int64_t jj) -> uint32_t { return (uint32_t)((jj / (2 * tp.K)) & 1); };
   unsigned char* stage0 = smem + tp.bar_bytes;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -298,9 +312,11 @@ __global__ void __launch_bounds__(kTmaThreads, ROPE_TMA_MIN_CTAS)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < tp.K; ++s) {
-      mbar_init(full0 + 8 * s, 33);  // the X copy's arrive.expect_tx + every gather lane
+      mbar_init(full0 + 8 * s, 32);  // every gather lane
       mbar_init(done0 + 8 * s, kTmaConsumerWarps);  // one arrive per consumer warp
       mbar_init(issued0 + 8 * s, 1);  // the copy warp, once the stage header is written
+      mbar_init(landed0 + 8 * s, 1);  // the X copy's arrive.expect_tx (two per stage)
+      mbar_init(landed0 + 8 * (tp.K + s), 1);
     }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -337,10 +353,10 @@ __global__ void __launch_bounds__(kTmaThreads, ROPE_TMA_MIN_CTAS)
         const int s = (int)(jj % tp.K);
         *stage_tile(s) = t;
         if (t < tp.ntiles) {
-          mbar_arrive_expect_tx(full0 + 8 * s, tp.x_bytes);
-          tma_load_x<RANK4>(smem_addr(stage0 + (size_t)s * tp.stage_bytes), &tmx, tl.c, full0 + 8 * s, pol);
+          mbar_arrive_expect_tx(landed_bar(jj), tp.x_bytes);
+          tma_load_x<RANK4>(smem_addr(stage0 + (size_t)s * tp.stage_bytes), &tmx, tl.c, landed_bar(jj), pol);
         } else {
-          mbar_arrive(full0 + 8 * s);  // the sentinel carries no bytes
+          mbar_arrive(landed_bar(jj));  // the sentinel carries no bytes
         }
         mbar_arrive(issued0 + 8 * s);  // publishes the header to the gather warp
       };
@@ -359,7 +375,8 @@ __global__ void __launch_bounds__(kTmaThreads, ROPE_TMA_MIN_CTAS)
       int64_t t_st = *stage_tile(0);
       Tile tl_st{};
       if (t_st < tp.ntiles) tl_st = tile_of<RANK4>(p, tp, t_st);
-      for (int64_t j = 0;; ++j) {
+      int64_t j = 0;  // the tile whose store comes next
+      for (;; ++j) {
         const int s = (int)(j % tp.K);
         if (!mbar_wait(done0 + 8 * s, (uint32_t)((j / tp.K) & 1))) {
           timed_out = true;
@@ -386,11 +403,11 @@ __global__ void __launch_bounds__(kTmaThreads, ROPE_TMA_MIN_CTAS)
       }
       bulk_wait_all();
       if (timed_out) {
-        // copies already issued must land before the CTA's shared memory goes
-        // away: the other warps time out too, so give them time (bounded)
-        const uint64_t t0 = global_ns();
-        while (global_ns() - t0 < 1000000ull) {
-        }
+        // Tiles j .. jx-1 were started and never stored: their loads must
+        // land before the CTA's shared memory goes away. Each one's landed
+        // phase is completed by the copy hardware alone (the sentinel's by its
+        // plain arrive), and nothing later was started, so no wait aliases.
+        for (int64_t jj = j; jj < jx; ++jj) (void)mbar_wait(landed_bar(jj), landed_par(jj));
         if (p.oor_flag) atomicOr(p.oor_flag, 2);
       }
       if (p.sched) {
@@ -463,9 +480,9 @@ __global__ void __launch_bounds__(kTmaThreads, ROPE_TMA_MIN_CTAS)
       if (!have_cur) cur = load_tile_pos<MODE>(p, tl, lane);
       // Rank 4: a tile is NG strided blocks of TS*H elements, and those loads
       // run best with the least in flight, so the gather of tile j waits for
-      // tile j-1's data (a phase this warp took part in, so it cannot alias).
-      if (RANK4 && j > 0 &&
-          !__all_sync(0xffffffffu, mbar_wait(full0 + 8 * ((j - 1) % tp.K), (uint32_t)(((j - 1) / tp.K) & 1)))) {
+      // tile j-1's data (its barrier's next use, tile j-1+2K, needs this
+      // warp's arrival for tile j-1+K first, so the parity cannot alias).
+      if (RANK4 && j > 0 && !__all_sync(0xffffffffu, mbar_wait(landed_bar(j - 1), landed_par(j - 1)))) {
         timed_out = true;
         break;
       }
@@ -563,11 +580,14 @@ __global__ void __launch_bounds__(kTmaThreads, ROPE_TMA_MIN_CTAS)
     stream_masks<V>(um, m0, m1);
   }
   bool timed_out = false;
-  int64_t j = 0;
-  for (;; ++j) {
-    const int s = (int)(j % tp.K);
+  // tile j's stage s and full parity, landed slot and parity (j % K,
+  // (j / K) & 1, j % 2K, (j / 2K) & 1), stepped once per tile
+  int s = 0, lsl = 0;
+  uint32_t ph = 0, lph = 0;
+  for (;;) {
     // the lanes of a warp agree, so a timeout never splits a warp
-    const bool ok = __all_sync(0xffffffffu, mbar_wait(full0 + 8 * s, (uint32_t)((j / tp.K) & 1)));
+    const bool ok = __all_sync(0xffffffffu, mbar_wait(landed0 + 8 * (uint32_t)lsl, lph) &&
+                                                mbar_wait(full0 + 8 * s, ph));
     const int64_t t = ok ? *stage_tile(s) : 0;
     if (ok && t >= tp.ntiles) {  // sentinel: hand it to the copy warp and stop
       __syncwarp();
@@ -659,6 +679,14 @@ __global__ void __launch_bounds__(kTmaThreads, ROPE_TMA_MIN_CTAS)
     fence_async_smem();  // this thread's smem writes, before the TMA store reads them
     __syncwarp();
     if (lane == 0) mbar_arrive(done0 + 8 * s);
+    if (++s == tp.K) {
+      s = 0;
+      ph ^= 1u;
+    }
+    if (++lsl == 2 * tp.K) {
+      lsl = 0;
+      lph ^= 1u;
+    }
   }
   if (timed_out && lane == 0 && p.oor_flag) atomicOr(p.oor_flag, 2);
 }
