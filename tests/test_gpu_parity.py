@@ -604,3 +604,39 @@ def test_workload_full_size(lib, orc, cuda, torch_mod, name):
     torch.cuda.synchronize()
     stats = compare(_host(yd), y_ref, x, w.rank, w.num_heads, mask)
     print(name, stats)
+
+
+@pytest.mark.parametrize("variant,kernel", [("auto", "rope_tma_kernel"), ("simt", "rope_rows_kernel")])
+@pytest.mark.parametrize("dt", ["float16", "bfloat16"])
+def test_mrope_full_size_stride3_reading(lib, orc, cuda, torch_mod, variant, kernel, dt):
+    """The M-RoPE workload ((2, 8192, 28 x 128), sections [16, 24, 24], 1 % of ids past the
+    table) under the other reading of the interleaved layout that the MRotaryEmbedding
+    README names without printing: stride-3 slots, h at i % 3 == 1 below 3 * 24, w at
+    i % 3 == 2 below 3 * 24, t elsewhere. For [16, 24, 24] that map differs from the
+    count-honouring one the library takes for layout 1, so it goes through
+    mrope_apply_stream_map, at full size, on both kernels."""
+    torch = torch_mod
+    w = wl.WORKLOADS["mrope_r3_f16_layout1"]
+    inp = wl.make_inputs(w.with_shape(dtype=dt))
+    x, pos, inv = inp["x"], inp["position_ids"], inp["inv_freq"]
+    dtype = wl.storage_dtype(dt)
+    smap = orc.mrope_stream_map(w.mrope_section, 2, w.half)
+    assert not np.array_equal(smap, orc.mrope_stream_map(w.mrope_section, 1, w.half))
+    assert np.bincount(smap, minlength=3).tolist() == [22, 21, 21]
+    cos, sin = orc.cache_build(inv, w.cache_rows, dtype)
+    y_ref, n_oor = orc.mrope_map(x, cos, sin, pos, smap, w.scale, w.interleaved, w.rotary_embedding_dim,
+                                 w.num_heads)
+    assert n_oor > 0
+    flag = torch.zeros(1, dtype=torch.int32, device=cuda)
+    with lib.variant(variant):
+        yd = lib.mrope_apply_stream_map(_dev(x, torch, cuda), _dev(cos, torch, cuda), _dev(sin, torch, cuda),
+                                        _dev(pos, torch, cuda), smap, scale=w.scale, interleaved=w.interleaved,
+                                        rotary_embedding_dim=w.rotary_embedding_dim, num_heads=w.num_heads,
+                                        oor_flag=flag)
+    torch.cuda.synchronize()
+    assert lib.last_kernel() == kernel
+    assert int(flag.item()) == 1
+    mask = mrope_passthrough_mask(x.shape, w.rank, w.num_heads, w.rotary_embedding_dim, pos, w.cache_rows, smap,
+                                  w.interleaved)
+    stats = compare(_host(yd), y_ref, x, w.rank, w.num_heads, mask)
+    print("stride-3 reading", dt, variant, stats)

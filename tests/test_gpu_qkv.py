@@ -401,6 +401,9 @@ def compare_norm(got, ref, N, H, rd, inter):
     bad = d > tol
     assert not bad.any(), f"{int(bad.sum())} elements beyond the bound; worst excess {float((d - tol).max())}"
     exact = float((d == 0).mean())
+    worst_ulp = float((d / _ulp(r, dtype)).max()) if d.size else 0.0
+    print(f"compare_norm {np.dtype(dtype).name if dtype is not BF16 else 'bfloat16'}: bit-exact {exact:.6f}, "
+          f"worst {worst_ulp:.2f} ulp of the result")
     if dtype in (np.float16, BF16):
         assert exact >= 0.97, f"only {exact:.4f} of the elements are bit-exact"
     return exact
@@ -528,3 +531,110 @@ def test_qkv_rmsnorm_zero_head_and_unsupported(lib, orc, cuda):
         lib.rope_apply_qkv(big, cb, cb, None, num_heads=1, kv_num_heads=1,
                            key=torch.zeros((1, 2, 1024), dtype=torch.float16, device=cuda), q_norm_weight=wb,
                            k_norm_weight=wb)
+
+
+# ---------------------------------------------------------------------------
+# QK-RMSNorm where r is exact: the 1-ulp bar with no allowance for r
+# ---------------------------------------------------------------------------
+
+_FOUR_SQUARES = {}
+
+
+def _four_squares(R, top=15):
+    """Four non-negative integers <= top whose squares add up to R, or None."""
+    if R not in _FOUR_SQUARES:
+        sol = None
+        for a in range(top + 1):
+            for b in range(a, top + 1):
+                for c in range(b, top + 1):
+                    d2 = R - a * a - b * b - c * c
+                    if d2 < c * c:
+                        break
+                    d = int(round(d2 ** 0.5))
+                    if d * d == d2 and d <= top:
+                        sol = (a, b, c, d)
+                        break
+                if sol:
+                    break
+            if sol:
+                break
+        _FOUR_SQUARES[R] = sol
+    return _FOUR_SQUARES[R]
+
+
+def exact_mean_square_heads(rng, nheads, H):
+    """`nheads` heads of H values n * 2^e (integers |n| <= 15, one e in [-8, 2] per
+    head) whose squares add up to exactly 64 * H * 4^e: the mean square is the
+    power of four 4^(3+e), so with epsilon 0 r = 2^-(3+e) is exact in every
+    precision, and every partial sum of squares (integers times 4^e below 2^24) is
+    exact in float32 as well. Returns float64 values, (nheads, H)."""
+    out = np.empty((nheads, H))
+    for i in range(nheads):
+        while True:
+            n = rng.integers(-13, 14, H - 4)
+            sol = _four_squares(64 * H - int((n * n).sum()))
+            if sol is not None and 64 * H - int((n * n).sum()) >= 0:
+                break
+        vals = np.concatenate([n, np.array(sol) * rng.choice([-1, 1], 4)]).astype(np.float64)
+        rng.shuffle(vals)
+        assert (vals * vals).sum() == 64 * H
+        out[i] = vals * 2.0 ** int(rng.integers(-8, 3))
+    return out
+
+
+@pytest.mark.parametrize("variant", list(QKV_KERNELS))
+@pytest.mark.parametrize("dt", ["f16", "bf16", "f32"])
+@pytest.mark.parametrize("H,inter", [(128, 0), (64, 1)])
+def test_qkv_rmsnorm_exact_r_one_ulp(lib, orc, cuda, variant, dt, H, inter):
+    """Heads whose mean square is a power of four, epsilon 0: r = 1/sqrt(mean(x^2)) is
+    a power of two on both sides, so the normalised z = T(w * T(x * r)) is the same
+    value on the GPU and in the oracle, and what is left is the rotation's single
+    rounding. Every output element -- rotated Q and K, out-of-range tokens (z copied),
+    appended K rows -- within 1 ulp (float32: 1e-5) of the oracle, the copied z and V
+    bit-exact. Packed [Q|K|V] with the cache append, on both Q/K kernels."""
+    import torch
+
+    rng = np.random.default_rng(77 + H + {"f16": 0, "bf16": 1, "f32": 2}[dt] + 10 * inter)
+    npdt = {"f16": np.float16, "f32": np.float32, "bf16": BF16}[dt]
+    B, S, Nq, Nkv, R, L = 3, 37, 8, 2, 64, 80
+    Ntot = Nq + 2 * Nkv
+    heads = exact_mean_square_heads(rng, B * S * Ntot, H)
+    qkv = cast(heads.reshape(B, S, Ntot * H), npdt)
+    assert np.array_equal(to_float64(qkv).reshape(-1, H), heads)          # the values are exact in T
+    wq = cast(rng.uniform(0.5, 2.0, H), npdt)
+    wk = cast(rng.uniform(0.5, 2.0, H), npdt)
+    theta = rng.uniform(-np.pi, np.pi, (R, H // 2))
+    cos, sin = cast(np.cos(theta), npdt), cast(np.sin(theta), npdt)
+    past = np.array([0, 11, 50], dtype=np.int32)
+    pos = rng.integers(0, R, (B, S))
+    pos[0, 5], pos[1, 0], pos[-1, -1] = R + 3, -1, R
+    bad = (pos < 0) | (pos >= R)
+    kc0 = cast(rng.standard_normal((B, Nkv, L, H)), npdt)
+    vc0 = cast(rng.standard_normal((B, Nkv, L, H)), npdt)
+    q_ref, _, kc_ref, vc_ref, n_oor, n_skip = orc.rope_qkv(
+        qkv, cos, sin, pos, num_heads=Nq, kv_num_heads=Nkv, interleaved=inter, k_cache=kc0, v_cache=vc0,
+        past_seq_lens=past, q_norm_weight=wq, k_norm_weight=wk, epsilon=0.0)
+    assert n_oor > 0 and n_skip > 0
+    status = torch.zeros(1, dtype=torch.int32, device=cuda)
+    kc_d, vc_d = _dev(kc0, torch, cuda), _dev(vc0, torch, cuda)
+    with lib.variant(variant):
+        qo, _ = lib.rope_apply_qkv(_dev(qkv, torch, cuda), _dev(cos, torch, cuda), _dev(sin, torch, cuda),
+                                   _dev(pos, torch, cuda), num_heads=Nq, kv_num_heads=Nkv, interleaved=inter,
+                                   k_cache=kc_d, v_cache=vc_d, past_seq_lens=_dev(past, torch, cuda),
+                                   status=status, q_norm_weight=_dev(wq, torch, cuda),
+                                   k_norm_weight=_dev(wk, torch, cuda), epsilon=0.0)
+    torch.cuda.synchronize()
+    assert lib.last_kernel() == QKV_KERNELS[variant]
+    assert int(status.item()) == 1 | 4
+    q_got = _host(qo)
+    bits = np.uint32 if dt == "f32" else np.uint16
+    # out-of-range tokens carry z itself: bit-exact with the oracle's z
+    qg, qr = q_got.reshape(B, S, Nq, H), q_ref.reshape(B, S, Nq, H)
+    assert np.array_equal(qg[bad].view(bits), qr[bad].view(bits))
+    st_q = compare(q_got, q_ref, q_ref, 3, Nq)
+    kc_g, vc_g = _host(kc_d), _host(vc_d)
+    assert np.array_equal(vc_g.view(bits), vc_ref.view(bits))            # V rows copied, the rest untouched
+    kt_g, kt_r = kc_g.transpose(0, 2, 1, 3), kc_ref.transpose(0, 2, 1, 3)  # (B, L, Nkv, H)
+    st_k = compare(np.ascontiguousarray(kt_g).reshape(B, L, Nkv * H),
+                   np.ascontiguousarray(kt_r).reshape(B, L, Nkv * H), kt_r.reshape(B, L, Nkv * H), 3, Nkv)
+    print(f"exact-r {dt} H={H}: Q {st_q}, K cache {st_k}")
