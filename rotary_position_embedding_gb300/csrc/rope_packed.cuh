@@ -1,4 +1,4 @@
-// Packed 16-bit arithmetic shared by the pipelined Q/K kernel.
+// Packed 16-bit arithmetic shared by the pipelined kernels.
 #pragma once
 
 #include "rope_kernels.cuh"
@@ -10,10 +10,10 @@ namespace rope_gb300 {
 // two values per 32-bit word, float32x2 operations (sm_100 and later). Each
 // lane of a packed operation rounds exactly as the scalar operation does, so
 // the results have the bits of rotate(): a product, then a fused multiply-add
-// (-(x1*s) is formed as x1*(-s), which rounds to the same value). Used where
-// the arithmetic, not memory, limits a kernel (the pipelined Q/K kernel with
-// RMSNorm); the memory-bound SIMT kernels keep the scalar form, which needs
-// fewer registers and so keeps more CTAs resident.
+// (-(x1*s) is formed as x1*(-s), which rounds to the same value). Used by the
+// pipelined kernels, whose consumers rotate several heads per coefficient
+// unpack; the SIMT kernels keep the scalar form, which needs fewer registers
+// and so keeps more CTAs resident.
 // ---------------------------------------------------------------------------
 template <class T>
 struct P2;

@@ -278,29 +278,35 @@ __global__ void __launch_bounds__(kTmaThreads * qkv_pipes(MROPE), ROPE_TMA_MIN_C
       auto pick = [&](int64_t jj) -> int64_t {
         return p.sched ? (int64_t)atomicAdd(p.sched, 1ull) : vb + jj * vg;
       };
-      auto issue = [&](int64_t jj, int64_t t) {
-        const int s = (int)(jj % tp.K);
+      // stage and landed slot of the next tile issued (jx % K, jx % 2K),
+      // stepped per issue (see rope_tma.cuh)
+      int is_s = 0, is_l = 0;
+      auto issue = [&](int64_t t) {
+        const int s = is_s;
+        const uint32_t lb = landed0 + 8 * (uint32_t)is_l;
         *stage_hdr(s) = t;
         if (t < tp.ntiles) {
           const QTile q = qtile_of<!MROPE>(p, tp, t);
           const uint32_t dst = smem_addr(stage0 + (size_t)s * tp.stage_bytes);
-          mbar_arrive_expect_tx(landed_bar(jj), q.R.x_bytes);
+          mbar_arrive_expect_tx(lb, q.R.x_bytes);
           // one NG-head box, or (cache tiles) one box per head
           const int nbox = qtile_wide(a, q) ? 1 : q.R.NG;
           for (int u = 0; u < nbox; ++u) {
             const int c[4] = {0, q.R.head_off + q.head0 + u, q.s0, q.b};
-            tma_load_x<true>(dst + (uint32_t)u * q.R.blk_bytes, &maps.src[q.role], c, landed_bar(jj), pol);
+            tma_load_x<true>(dst + (uint32_t)u * q.R.blk_bytes, &maps.src[q.role], c, lb, pol);
           }
         } else {
-          mbar_arrive(landed_bar(jj));  // the sentinel carries no bytes
+          mbar_arrive(lb);  // the sentinel carries no bytes
         }
         mbar_arrive(issued0 + 8 * s);
+        if (++is_s == tp.K) is_s = 0;
+        if (++is_l == 2 * tp.K) is_l = 0;
       };
       bool ended = false;
       int64_t jx = 0;  // tiles issued (the sentinel included)
       for (; jx < tp.K && !ended; ++jx) {
         const int64_t t = pick(jx);
-        issue(jx, t);
+        issue(t);
         ended = t >= tp.ntiles;
       }
       // the next store's tile and cache row are worked out while the previous
@@ -316,9 +322,10 @@ __global__ void __launch_bounds__(kTmaThreads * qkv_pipes(MROPE), ROPE_TMA_MIN_C
       };
       prep(t_st);
       int64_t j = 0;  // the tile whose store comes next
+      int s = 0;      // its stage (j % K) and the parity of its phase there
+      uint32_t ph = 0;
       for (;; ++j) {
-        const int s = (int)(j % tp.K);
-        if (!mbar_wait(done0 + 8 * s, (uint32_t)((j / tp.K) & 1))) {
+        if (!mbar_wait(done0 + 8 * s, ph)) {
           timed_out = true;
           break;
         }
@@ -339,12 +346,16 @@ __global__ void __launch_bounds__(kTmaThreads * qkv_pipes(MROPE), ROPE_TMA_MIN_C
           bulk_commit();
         }
         const int64_t t_new = ended ? 0 : pick(jx);
+        if (++s == tp.K) {
+          s = 0;
+          ph ^= 1u;
+        }
         // tile j+1 is already issued (K >= 2), so its header is in place
-        t_st = *stage_hdr((int)((j + 1) % tp.K));
+        t_st = *stage_hdr(s);
         prep(t_st);
         if (!ended) {
           bulk_wait_read_0();  // the stage may be refilled once the store has read it
-          issue(jx, t_new);    // jx == j + K: the tile that goes into stage s next
+          issue(t_new);        // jx == j + K: the tile that goes into tile j's stage next
           ended = t_new >= tp.ntiles;
           ++jx;
         }
@@ -425,9 +436,10 @@ __global__ void __launch_bounds__(kTmaThreads * qkv_pipes(MROPE), ROPE_TMA_MIN_C
       have_cur = true;
     }
     int64_t j = 0;  // the tile served next
+    int s = 0;      // its stage (j % K) and the parity of its phase there
+    uint32_t ph = 0;
     for (;; ++j) {
-      const int s = (int)(j % tp.K);
-      if (!__all_sync(0xffffffffu, mbar_wait(issued0 + 8 * s, (uint32_t)((j / tp.K) & 1)))) {
+      if (!__all_sync(0xffffffffu, mbar_wait(issued0 + 8 * s, ph))) {
         timed_out = true;
         break;
       }
@@ -437,6 +449,9 @@ __global__ void __launch_bounds__(kTmaThreads * qkv_pipes(MROPE), ROPE_TMA_MIN_C
         break;
       }
       if (!have_cur) cur = prefetch(t);
+      // the stage and parity of tile j+1
+      const int sn = s + 1 == tp.K ? 0 : s + 1;
+      const uint32_t phn = s + 1 == tp.K ? ph ^ 1u : ph;
       Pre nxt{};
       bool have_nxt = false;
       if (!p.sched) {
@@ -445,8 +460,7 @@ __global__ void __launch_bounds__(kTmaThreads * qkv_pipes(MROPE), ROPE_TMA_MIN_C
       } else {
         // headers are published in tile order and tile j+1-K's phase of this
         // barrier is already complete, so the parity test cannot alias
-        const int sn = (int)((j + 1) % tp.K);
-        if (__all_sync(0xffffffffu, mbar_test(issued0 + 8 * sn, (uint32_t)(((j + 1) / tp.K) & 1)))) {
+        if (__all_sync(0xffffffffu, mbar_test(issued0 + 8 * sn, phn))) {
           nxt = prefetch(*stage_hdr(sn));
           have_nxt = true;
         }
@@ -542,6 +556,8 @@ __global__ void __launch_bounds__(kTmaThreads * qkv_pipes(MROPE), ROPE_TMA_MIN_C
       }
       cur = nxt;
       have_cur = have_nxt;
+      s = sn;
+      ph = phn;
     }
     asm volatile("cp.async.wait_all;" ::: "memory");
     if (timed_out) {

@@ -51,8 +51,10 @@
 #include <cuda.h>
 
 #include "rope_kernels.cuh"
+#include "rope_packed.cuh"
 
 namespace rope_gb300 {
+
 
 #ifndef ROPE_TMA_CONSUMER_WARPS
 #define ROPE_TMA_CONSUMER_WARPS 8
@@ -349,16 +351,23 @@ __global__ void __launch_bounds__(kTmaThreads, ROPE_TMA_MIN_CTAS)
       auto pick = [&](int64_t jj) -> int64_t {  // the index of this CTA's tile jj
         return p.sched ? (int64_t)atomicAdd(p.sched, 1ull) : (int64_t)blockIdx.x + jj * (int64_t)gridDim.x;
       };
-      auto issue = [&](int64_t jj, int64_t t, const Tile& tl) {
-        const int s = (int)(jj % tp.K);
+      // stage and landed slot of the next tile issued (jx % K, jx % 2K),
+      // stepped per issue: this lane's serial path between a store and the
+      // refill it allows is the pipeline's critical path when K is 2
+      int is_s = 0, is_l = 0;
+      auto issue = [&](int64_t t, const Tile& tl) {
+        const int s = is_s;
+        const uint32_t lb = landed0 + 8 * (uint32_t)is_l;
         *stage_tile(s) = t;
         if (t < tp.ntiles) {
-          mbar_arrive_expect_tx(landed_bar(jj), tp.x_bytes);
-          tma_load_x<RANK4>(smem_addr(stage0 + (size_t)s * tp.stage_bytes), &tmx, tl.c, landed_bar(jj), pol);
+          mbar_arrive_expect_tx(lb, tp.x_bytes);
+          tma_load_x<RANK4>(smem_addr(stage0 + (size_t)s * tp.stage_bytes), &tmx, tl.c, lb, pol);
         } else {
-          mbar_arrive(landed_bar(jj));  // the sentinel carries no bytes
+          mbar_arrive(lb);  // the sentinel carries no bytes
         }
         mbar_arrive(issued0 + 8 * s);  // publishes the header to the gather warp
+        if (++is_s == tp.K) is_s = 0;
+        if (++is_l == 2 * tp.K) is_l = 0;
       };
       bool ended = false;
       int64_t jx = 0;  // tiles issued (the sentinel included)
@@ -366,7 +375,7 @@ __global__ void __launch_bounds__(kTmaThreads, ROPE_TMA_MIN_CTAS)
         const int64_t t = pick(jx);
         Tile tl{};
         if (t < tp.ntiles) tl = tile_of<RANK4>(p, tp, t);
-        issue(jx, t, tl);
+        issue(t, tl);
         ended = t >= tp.ntiles;
       }
       // The next store's tile and the next refill's tile are worked out while
@@ -376,9 +385,10 @@ __global__ void __launch_bounds__(kTmaThreads, ROPE_TMA_MIN_CTAS)
       Tile tl_st{};
       if (t_st < tp.ntiles) tl_st = tile_of<RANK4>(p, tp, t_st);
       int64_t j = 0;  // the tile whose store comes next
+      int s = 0;      // its stage (j % K) and the parity of its phase there
+      uint32_t ph = 0;
       for (;; ++j) {
-        const int s = (int)(j % tp.K);
-        if (!mbar_wait(done0 + 8 * s, (uint32_t)((j / tp.K) & 1))) {
+        if (!mbar_wait(done0 + 8 * s, ph)) {
           timed_out = true;
           break;
         }
@@ -391,12 +401,16 @@ __global__ void __launch_bounds__(kTmaThreads, ROPE_TMA_MIN_CTAS)
           t_new = pick(jx);
           if (t_new < tp.ntiles) tl_new = tile_of<RANK4>(p, tp, t_new);
         }
+        if (++s == tp.K) {
+          s = 0;
+          ph ^= 1u;
+        }
         // tile j+1 is already issued (K >= 2), so its header is in place
-        t_st = *stage_tile((int)((j + 1) % tp.K));
+        t_st = *stage_tile(s);
         if (t_st < tp.ntiles) tl_st = tile_of<RANK4>(p, tp, t_st);
         if (!ended) {
           bulk_wait_read_0();  // the stage may be refilled once the store has read it
-          issue(jx, t_new, tl_new);  // jx == j + K: the tile that goes into stage s next
+          issue(t_new, tl_new);  // jx == j + K: the tile that goes into tile j's stage next
           ended = t_new >= tp.ntiles;
           ++jx;
         }
@@ -465,9 +479,12 @@ __global__ void __launch_bounds__(kTmaThreads, ROPE_TMA_MIN_CTAS)
       if ((int64_t)blockIdx.x < tp.ntiles) cur = load_tile_pos<MODE>(p, tile_of<RANK4>(p, tp, blockIdx.x), lane);
       have_cur = true;
     }
+    // tile j's stage and phase parity (j % K, (j / K) & 1) and landed slot
+    // (j % 2K, (j / 2K) & 1); the same for tile j-1, which rank 4 waits on
+    int s = 0, lsl = 0, s_prev = 0, lsl_prev = 0;
+    uint32_t ph = 0, lph = 0, ph_prev = 0, lph_prev = 0;
     for (int64_t j = 0;; ++j) {
-      const int s = (int)(j % tp.K);
-      if (!__all_sync(0xffffffffu, mbar_wait(issued0 + 8 * s, (uint32_t)((j / tp.K) & 1)))) {
+      if (!__all_sync(0xffffffffu, mbar_wait(issued0 + 8 * s, ph))) {
         timed_out = true;
         break;
       }
@@ -479,13 +496,21 @@ __global__ void __launch_bounds__(kTmaThreads, ROPE_TMA_MIN_CTAS)
       const Tile tl = tile_of<RANK4>(p, tp, t);
       if (!have_cur) cur = load_tile_pos<MODE>(p, tl, lane);
       // Rank 4: a tile is NG strided blocks of TS*H elements, and those loads
-      // run best with the least in flight, so the gather of tile j waits for
-      // tile j-1's data (its barrier's next use, tile j-1+2K, needs this
-      // warp's arrival for tile j-1+K first, so the parity cannot alias).
-      if (RANK4 && j > 0 && !__all_sync(0xffffffffu, mbar_wait(landed_bar(j - 1), landed_par(j - 1)))) {
+      // run best with the least in flight, so the gather of tile j waits until
+      // tile j-1 is complete: its data and this warp's own row copies for it
+      // (measured: waiting for the data alone lets the row copies run ahead,
+      // rank-4 partial rotation 84.0 -> 90.7 us). Neither parity can alias:
+      // the landed barrier's next use, tile j-1+2K, and full[s]'s next phase,
+      // tile j-1+K, both need this warp's arrival for tile j-1+K first.
+      if (RANK4 && j > 0 &&
+          !__all_sync(0xffffffffu, mbar_wait(landed0 + 8 * (uint32_t)lsl_prev, lph_prev) &&
+                                       mbar_wait(full0 + 8 * s_prev, ph_prev))) {
         timed_out = true;
         break;
       }
+      // the stage and parity of tile j+1
+      const int sn = s + 1 == tp.K ? 0 : s + 1;
+      const uint32_t phn = s + 1 == tp.K ? ph ^ 1u : ph;
       TilePos<MODE> nxt{};
       bool have_nxt = false;
       if (!p.sched) {
@@ -496,8 +521,7 @@ __global__ void __launch_bounds__(kTmaThreads, ROPE_TMA_MIN_CTAS)
         // the copy warp publishes headers in tile order, and tile j+1-K's
         // phase of that barrier is already complete, so the parity test
         // cannot alias
-        const int sn = (int)((j + 1) % tp.K);
-        if (__all_sync(0xffffffffu, mbar_test(issued0 + 8 * sn, (uint32_t)(((j + 1) / tp.K) & 1)))) {
+        if (__all_sync(0xffffffffu, mbar_test(issued0 + 8 * sn, phn))) {
           const int64_t tn = *stage_tile(sn);
           if (tn < tp.ntiles) nxt = load_tile_pos<MODE>(p, tile_of<RANK4>(p, tp, tn), lane);
           have_nxt = true;
@@ -548,6 +572,16 @@ __global__ void __launch_bounds__(kTmaThreads, ROPE_TMA_MIN_CTAS)
       cp_async_arrive(full0 + 8 * s);
       cur = nxt;
       have_cur = have_nxt;
+      s_prev = s;
+      ph_prev = ph;
+      lsl_prev = lsl;
+      lph_prev = lph;
+      s = sn;
+      ph = phn;
+      if (++lsl == 2 * tp.K) {
+        lsl = 0;
+        lph ^= 1u;
+      }
     }
     // every copy this warp issued has landed before it leaves
     asm volatile("cp.async.wait_all;" ::: "memory");
@@ -644,6 +678,18 @@ __global__ void __launch_bounds__(kTmaThreads, ROPE_TMA_MIN_CTAS)
         blend_on = valid != present;
         if (blend_on) pair_masks<V, INTER>(um, valid, ma, mb);
       }
+      // 16-bit storage: the column's coefficients unpacked to float32 pairs
+      // once, every head rotated with float32x2 operations (the same bits as
+      // the scalar form; measured on M-RoPE 39.1 -> 38.4 us per launch from a
+      // graph and 44.6 -> 42.6 us alone, rank-4 partial rotation unchanged)
+      constexpr bool PACKED = sizeof(bits) == 2 && V == 8;
+      float2 cf[4], sf[4];
+      if constexpr (PACKED) {
+        if (fast) {
+          unpack_coef8<T>(reinterpret_cast<const VecT<T, 8>&>(c), cf);
+          unpack_coef8<T>(reinterpret_cast<const VecT<T, 8>&>(sn), sf);
+        }
+      }
       if (fast) {
         // X loads of HOIST heads are issued together, then rotated and stored
         constexpr int HOIST = MODE == Coef::kMRope ? 2 : kMaxHeads;
@@ -661,7 +707,16 @@ __global__ void __launch_bounds__(kTmaThreads, ROPE_TMA_MIN_CTAS)
           for (int u = 0; u < HOIST; ++u) {
             if (!act[u0 + u]) continue;
             VT ya, yb;
-            rotate_unit<T, V, INTER>(a[u], bv[u], c, sn, ya, yb);
+            if constexpr (PACKED) {
+              Unit8<T> ua, ub, ra, rb;
+              __builtin_memcpy(&ua, &a[u], 16);
+              __builtin_memcpy(&ub, &bv[u], 16);
+              rotate8p<T, INTER>(ua, ub, cf, sf, ra, rb);
+              __builtin_memcpy(&ya, &ra, 16);
+              __builtin_memcpy(&yb, &rb, 16);
+            } else {
+              rotate_unit<T, V, INTER>(a[u], bv[u], c, sn, ya, yb);
+            }
             if (MODE == Coef::kMRope && blend_on) {
               blend(ya, a[u], ma);
               blend(yb, bv[u], mb);

@@ -401,9 +401,9 @@ def compare_norm(got, ref, N, H, rd, inter):
     bad = d > tol
     assert not bad.any(), f"{int(bad.sum())} elements beyond the bound; worst excess {float((d - tol).max())}"
     exact = float((d == 0).mean())
-    worst_ulp = float((d / _ulp(r, dtype)).max()) if d.size else 0.0
+    worst = float((d / _ulp(rho, dtype)).max()) if d.size else 0.0
     print(f"compare_norm {np.dtype(dtype).name if dtype is not BF16 else 'bfloat16'}: bit-exact {exact:.6f}, "
-          f"worst {worst_ulp:.2f} ulp of the result")
+          f"worst {worst:.2f} ulps of the pair magnitude")
     if dtype in (np.float16, BF16):
         assert exact >= 0.97, f"only {exact:.4f} of the elements are bit-exact"
     return exact
