@@ -7,7 +7,8 @@ recomputes sampled tokens one by one: the first token, the last token (the
 highest addresses) and tokens spread over the whole tensor, all heads each.
 The cases cover the SIMT kernel (full rotation, rank 3 and rank 4) and the TMA
 pipeline (partial rotation and M-RoPE), each through the automatic variant
-choice, as the benchmark launches them; and the Q/K op (RoPE on both Q/K
+choice, as the benchmark launches them, the SIMT M-RoPE kernel (shared-memory
+coefficient table) by the SIMT variant; and the Q/K op (RoPE on both Q/K
 kernels, M-RoPE on the pipeline) over a packed [Q|K|V] of 3.2 G elements.
 """
 
@@ -33,9 +34,13 @@ def _sample_tokens(rng):
 @pytest.mark.parametrize("case,kernel", [("rope_full_rank3", "rope_rows_kernel"),
                                          ("rope_full_rank4", "rope_rows_kernel"),
                                          ("rope_partial_rank3", "rope_tma_kernel"),
-                                         ("mrope_rank3", "rope_tma_kernel")])
+                                         ("mrope_rank3", "rope_tma_kernel"),
+                                         ("mrope_rank3_simt", "rope_mrope_table_kernel")])
 def test_over_two_to_the_31_elements(lib, orc, cuda, case, kernel):
     import torch
+
+    simt = case.endswith("_simt")
+    case = case[:-len("_simt")] if simt else case
 
     assert B * S * N * H > 2 ** 31
     rank = 4 if case.endswith("rank4") else 3
@@ -55,8 +60,9 @@ def test_over_two_to_the_31_elements(lib, orc, cuda, case, kernel):
         pos = rng.integers(0, R, (3, B, S))
         pos[1, B - 1, S - 1] = R + 5          # the last token's h stream is past the table
         section = (16, 24, 24)
-        yd = lib.mrope_apply(xd, cd, sd, torch.from_numpy(pos).to(cuda), section, mrope_layout=1,
-                             num_heads=N, oor_flag=flag)
+        with lib.variant("simt" if simt else "auto"):
+            yd = lib.mrope_apply(xd, cd, sd, torch.from_numpy(pos).to(cuda), section, mrope_layout=1,
+                                 num_heads=N, oor_flag=flag)
     else:
         pos = rng.integers(0, R, (B, S))
         pos[B - 1, S - 1] = R + 5             # the last token is past the table: copied through

@@ -400,6 +400,79 @@ def test_mrope_grid(lib, orc, cuda, torch_mod, dt, rank, layout, inter, rot, sca
     assert int(flag.item()) == (1 if n_oor else 0)
 
 
+TABLE_GRID = list(itertools.product(["f16", "f32", "bf16"], [3, 4], ["l0", "l1", "stride3"], [0, 1],
+                                    ["full", "partial"], [1.0, 0.7]))
+
+
+@pytest.mark.parametrize("dt,rank,layout,inter,rot,scale", TABLE_GRID)
+def test_mrope_table_kernel(lib, orc, cuda, torch_mod, dt, rank, layout, inter, rot, scale):
+    """The SIMT M-RoPE path from 512 tokens: each token's three coefficient rows merged once
+    into shared memory. 600 tokens (several tiles per CTA), out-of-range ids in every
+    stream, partial rotation with a tail, both pairings, scaled coefficients."""
+    torch = torch_mod
+    dtype = DT[dt]
+    rng = np.random.default_rng(_seed(dt, rank, layout, inter, rot, scale, "table"))
+    B, S, N, H = 2, 300, 3, 64
+    rd, sec = (0, (8, 12, 12)) if rot == "full" else (32, (4, 6, 6))
+    h = (rd or H) // 2
+    R = 700
+    shape = _x_shape(rank, B, S, N, H)
+    x = cast(rng.standard_normal(shape), dtype)
+    cos, sin = orc.cache_build(wl.inv_freq(10000.0, rd or H, h), R, dtype)
+    pos3 = rng.integers(0, R, (3, B, S))
+    oor = rng.random((3, B, S)) < 0.05
+    pos3[oor] = rng.choice([-1, R, R + 5, 1 << 40], size=int(oor.sum()))
+    nh = N if rank == 3 else 0
+    scale = float(np.float32(scale))
+    if layout == "stride3":
+        smap = orc.mrope_stream_map(sec, 2, h)
+        y_ref, n_oor = orc.mrope_map(x, cos, sin, pos3, smap, scale, inter, rd, nh)
+    else:
+        lay = 0 if layout == "l0" else 1
+        smap = orc.mrope_stream_map(sec, lay, h)
+        y_ref, n_oor = orc.mrope(x, cos, sin, pos3, sec, lay, scale, inter, rd, nh)
+    args = (_dev(x, torch, cuda), _dev(cos, torch, cuda), _dev(sin, torch, cuda), _dev(pos3, torch, cuda))
+    flag = torch.zeros(1, dtype=torch.int32, device=cuda)
+    kw = dict(scale=scale, interleaved=inter, rotary_embedding_dim=rd, num_heads=nh, oor_flag=flag)
+    with lib.variant("simt"):
+        if layout == "stride3":
+            yd = lib.mrope_apply_stream_map(*args, smap.tolist(), **kw)
+        else:
+            yd = lib.mrope_apply(*args, sec, mrope_layout=0 if layout == "l0" else 1, **kw)
+        assert lib.last_kernel() == "rope_mrope_table_kernel"
+    torch.cuda.synchronize()
+    compare(_host(yd), y_ref, x, rank, N, mrope_passthrough_mask(shape, rank, N, rd, pos3, R, smap, inter))
+    assert int(flag.item()) == (1 if n_oor else 0)
+
+
+@pytest.mark.parametrize("dt", ["f16", "bf16", "f32"])
+def test_mrope_simt_kernels_agree_at_the_switch(lib, orc, cuda, torch_mod, dt):
+    """511 tokens take the per-thread merge, 512 the shared-memory table: the two SIMT
+    M-RoPE kernels and the pipeline give the same bits on the same tokens."""
+    torch = torch_mod
+    rng = np.random.default_rng(91)
+    N, H, R = 4, 128, 2048
+    x = cast(rng.standard_normal((1, 512, N * H)), DT[dt])
+    cos, sin = orc.cache_build(wl.inv_freq(1e6, H, H // 2), R, DT[dt])
+    pos3 = rng.integers(0, R, (3, 1, 512))
+    pos3[1, 0, 100] = R + 1
+    xd, cd, sd, pd = (_dev(a, torch, cuda) for a in (x, cos, sin, pos3))
+    outs = {}
+    with lib.variant("simt"):
+        outs["table"] = lib.mrope_apply(xd, cd, sd, pd, (16, 24, 24), mrope_layout=1, num_heads=N)
+        assert lib.last_kernel() == "rope_mrope_table_kernel"
+        outs["rows"] = lib.mrope_apply(xd[:, :511].contiguous(), cd, sd, pd[:, :, :511].contiguous(), (16, 24, 24),
+                                       mrope_layout=1, num_heads=N)
+        assert lib.last_kernel() == "rope_rows_kernel"
+    with lib.variant("tma"):
+        outs["tma"] = lib.mrope_apply(xd, cd, sd, pd, (16, 24, 24), mrope_layout=1, num_heads=N)
+        assert lib.last_kernel() == "rope_tma_kernel"
+    torch.cuda.synchronize()
+    bits = torch.int32 if dt == "f32" else torch.int16
+    assert torch.equal(outs["table"][:, :511].view(bits), outs["rows"].view(bits))
+    assert torch.equal(outs["table"].view(bits), outs["tma"].view(bits))
+
+
 def test_mrope_equal_streams_equals_rope_on_gpu(lib, orc, cuda, torch_mod):
     """Text tokens (t = h = w) reduce M-RoPE to RotaryEmbedding, bit for bit on the GPU too."""
     torch = torch_mod
@@ -606,7 +679,7 @@ def test_workload_full_size(lib, orc, cuda, torch_mod, name):
     print(name, stats)
 
 
-@pytest.mark.parametrize("variant,kernel", [("auto", "rope_tma_kernel"), ("simt", "rope_rows_kernel")])
+@pytest.mark.parametrize("variant,kernel", [("auto", "rope_tma_kernel"), ("simt", "rope_mrope_table_kernel")])
 @pytest.mark.parametrize("dt", ["float16", "bfloat16"])
 def test_mrope_full_size_stride3_reading(lib, orc, cuda, torch_mod, variant, kernel, dt):
     """The M-RoPE workload ((2, 8192, 28 x 128), sections [16, 24, 24], 1 % of ids past the

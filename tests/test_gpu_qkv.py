@@ -377,7 +377,11 @@ def compare_norm(got, ref, N, H, rd, inter):
         rounds once more. Bound: 1 ulp of the result + 3 ulps of the pair's
         magnitude (which bounds |z| and which the rotation preserves). Such
         flips need x*r within 6.6e-7 of a rounding boundary (a 2^-11 grid),
-        so at least 97 % of the elements must match bit for bit.
+        which the worst case puts at 0.3 % of the elements; r's actual error
+        is far below that bound, and over every norm case here (grids, tile
+        shapes, full-size workloads) at least 99.965 % of float16 and
+        99.993 % of bfloat16 elements match bit for bit, so at least 99.9 %
+        must.
       float32: r's error carries into z at ~1.3e-6 relative (two more
         roundings) and through the float32 rotation (one more product and
         the final rounding). Bound: 1 ulp of the result + 3e-6 of the pair's
@@ -405,7 +409,7 @@ def compare_norm(got, ref, N, H, rd, inter):
     print(f"compare_norm {np.dtype(dtype).name if dtype is not BF16 else 'bfloat16'}: bit-exact {exact:.6f}, "
           f"worst {worst:.2f} ulps of the pair magnitude")
     if dtype in (np.float16, BF16):
-        assert exact >= 0.97, f"only {exact:.4f} of the elements are bit-exact"
+        assert exact >= 0.999, f"only {exact:.5f} of the elements are bit-exact"
     return exact
 
 
