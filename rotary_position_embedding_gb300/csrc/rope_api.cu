@@ -62,8 +62,13 @@
 #ifndef ROPE_TMA_TILE_BYTES
 #define ROPE_TMA_TILE_BYTES 32768
 #endif
+// The budget is half an SM's shared memory less the per-CTA reserve, so two
+// CTAs fit per SM; at 112 KB the rank-4 tiles (32 KB of X and 4 KB of rows)
+// get a third stage: measured 80.4 -> 80.0 us per launch from a graph and
+// 85.5 -> 84.5 us alone on (8, 32, 4096, 128) float16 with rd 64 (110 KB
+// gave two); M-RoPE keeps three either way.
 #ifndef ROPE_TMA_SMEM_BUDGET
-#define ROPE_TMA_SMEM_BUDGET (110 * 1024)
+#define ROPE_TMA_SMEM_BUDGET (112 * 1024)
 #endif
 #ifndef ROPE_TMA_MIN_BYTES
 #define ROPE_TMA_MIN_BYTES (8 << 20)
