@@ -499,9 +499,10 @@ def isolation_floor(torch, step, samples, stream_handle):
     as time_isolated (device sleep, then an event pair around one launch):
       - an empty kernel (torch's device sleep of 0 cycles): the event pair and
         the launch of a one-block grid;
-      - a device-to-device copy of X into Y (torch ``copy_``): the same pair
-        and launch around a plain stream of 2 |X| bytes, whose own ramp and
-        drain a bandwidth-bound kernel also pays.
+      - a device-to-device copy of X into Y (torch ``copy_``, a
+        cudaMemcpyAsync, the operation the measured HBM peak was taken with):
+        the same pair around a plain stream of 2 |X| bytes, whose own ramp
+        and drain a bandwidth-bound kernel also pays.
     Medians in microseconds."""
     n_sets = len(step.xs)
     res = {}
