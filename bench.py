@@ -48,7 +48,7 @@ METRIC = "RoPE achieved HBM GB/s and Gelem/s, fp16, as % of GB300 HBM roofline"
 # code it was captured on is unchanged (comments and blank lines aside).
 KERNEL_SOURCES = {
     "rope_rows_kernel": ["rope_api.cu", "rope_kernels.cuh", "k_rope.cu", "k_mrope.cu"],
-    "rope_mrope_table_kernel": ["rope_api.cu", "rope_kernels.cuh", "k_mrope.cu"],
+    "rope_mrope_heads_kernel": ["rope_api.cu", "rope_kernels.cuh", "rope_mrope_heads.cuh", "k_mrope_heads.cu"],
     "rope_tma_kernel": ["rope_api.cu", "rope_kernels.cuh", "rope_packed.cuh", "rope_tma.cuh", "k_tma.cu"],
     "rope_fused_kernel": ["rope_api.cu", "rope_kernels.cuh", "rope_fused.cuh", "k_fused.cu"],
     "rope_qkv_kernel": ["rope_api.cu", "rope_kernels.cuh", "rope_qkv.cuh", "k_qkv.cu", "k_mrope_qkv.cu"],

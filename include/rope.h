@@ -446,8 +446,8 @@ const char* rope_status_string(rope_status status);
 const char* rope_last_error(void);
 
 /* Kernel family that the last call on the calling thread which launched work
-   used: "rope_rows_kernel" (SIMT), "rope_mrope_table_kernel" (SIMT M-RoPE with the
-   coefficients merged per token in shared memory), "rope_tma_kernel" (TMA pipeline),
+   used: "rope_rows_kernel" (SIMT), "rope_mrope_heads_kernel" (SIMT M-RoPE, several heads
+   per thread), "rope_tma_kernel" (TMA pipeline),
    "rope_fused_kernel", "rope_qkv_kernel" (SIMT), "rope_qkv_tma_kernel" (TMA pipeline) or
    "rope_cache_build_kernel"; "" before the first
    launch. Calls that fail or launch nothing (empty X) leave it unchanged.

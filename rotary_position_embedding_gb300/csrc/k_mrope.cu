@@ -14,27 +14,12 @@ const void* pick(bool inter, bool rank4) {
                : (const void*)rope_rows_kernel<T, V, false, false, Coef::kMRope>;
 }
 
-template <class T, int V>
-const void* pick_table(bool inter, bool rank4) {
-  if (inter)
-    return rank4 ? (const void*)rope_mrope_table_kernel<T, V, true, true>
-                 : (const void*)rope_mrope_table_kernel<T, V, true, false>;
-  return rank4 ? (const void*)rope_mrope_table_kernel<T, V, false, true>
-               : (const void*)rope_mrope_table_kernel<T, V, false, false>;
-}
 }  // namespace
 
 const void* rope_kernel_mrope(int dtype, bool vec, bool inter, bool rank4) {
   if (dtype == 0) return vec ? pick<float, 4>(inter, rank4) : pick<float, 1>(inter, rank4);
   if (dtype == 1) return vec ? pick<__half, 8>(inter, rank4) : pick<__half, 1>(inter, rank4);
   if (dtype == 2) return vec ? pick<__nv_bfloat16, 8>(inter, rank4) : pick<__nv_bfloat16, 1>(inter, rank4);
-  return nullptr;
-}
-
-const void* rope_kernel_mrope_table(int dtype, bool inter, bool rank4) {
-  if (dtype == 0) return pick_table<float, 4>(inter, rank4);
-  if (dtype == 1) return pick_table<__half, 8>(inter, rank4);
-  if (dtype == 2) return pick_table<__nv_bfloat16, 8>(inter, rank4);
   return nullptr;
 }
 

@@ -48,14 +48,22 @@
 #ifndef ROPE_ROWS_WAVES_RANK3
 #define ROPE_ROWS_WAVES_RANK3 5
 #endif
-// SIMT M-RoPE: calls of at least this many tokens merge each token's three
-// coefficient rows once, into shared memory (rope_mrope_table_kernel); smaller
-// ones merge them in every thread (rope_rows_kernel), which has no barrier on
-// its latency path. Measured on GB300, float16, 28 heads of 128, from a CUDA
-// graph: 256 tokens 3.44 us (rows) against 3.77 us (table); 1024 tokens 8.11
-// against 6.89 us; 16384 tokens about 75 against 65 us.
-#ifndef ROPE_MROPE_TABLE_MIN_TOKENS
-#define ROPE_MROPE_TABLE_MIN_TOKENS 512
+// M-RoPE on the 128-bit path. The SIMT kernel takes several heads per thread
+// (rope_mrope_heads_kernel): 2 below ROPE_MROPE_HEADS4_MIN_TOKENS tokens (more
+// threads for decode-sized calls), 4 from there. Measured on GB300, float16,
+// 28 heads of 128, from a CUDA graph (2 / 4 heads per thread; the per-thread
+// merge of rope_rows_kernel): 256 tokens 2.95 / 3.39 us (3.46); 1024 tokens
+// 5.51 / 4.40 us (7.98); 16384 tokens 45.6 / 38.8 us (80.6). The TMA pipeline
+// (38.2 us there) stays the automatic choice from 8 MiB of X where its tile
+// reaches ROPE_MROPE_TMA_MIN_TILE bytes: the three coefficient rows a token
+// gathers cap its tokens per tile, and with few heads the tiles shrink (16
+// heads: 20 KB tiles, 25.7 us against 24.0 us for the SIMT kernel; 4 heads:
+// 5 KB, 20.9 against 8.3 us; 32 heads: 32 KB, 43.0 against 43.0 us).
+#ifndef ROPE_MROPE_HEADS4_MIN_TOKENS
+#define ROPE_MROPE_HEADS4_MIN_TOKENS 512
+#endif
+#ifndef ROPE_MROPE_TMA_MIN_TILE
+#define ROPE_MROPE_TMA_MIN_TILE (24 * 1024)
 #endif
 // TMA pipeline: bytes of one X tile, shared-memory budget of the stage ring,
 // smallest X (bytes) sent down the pipeline, most stages.
@@ -246,10 +254,8 @@ struct Launch {
 
 // unit_groups: a row's units go to a power-of-two group of at most 32 lanes,
 // one unit per lane (kernels that reduce over a row with warp shuffles).
-// smem_table: a cos and a sin row per token slot in dynamic shared memory,
-// plus extra_per_slot bytes per slot after them.
 rope_status plan(const Geom& g, int es, bool vec, const void* fn, bool smem_table, KParams* kp,
-                 Launch* L, bool unit_groups = false, int waves = ROPE_GRID_WAVES, size_t extra_per_slot = 0) {
+                 Launch* L, bool unit_groups = false, int waves = ROPE_GRID_WAVES) {
   const int V = vec ? 16 / es : 1;
   const int64_t nP = g.h / V;
   const int64_t nT = (g.H - g.rd) / V;
@@ -276,7 +282,7 @@ rope_status plan(const Geom& g, int es, bool vec, const void* fn, bool smem_tabl
   if (TTs * per_tok > kMaxRowThreads) TTs = kMaxRowThreads / per_tok;
   if (TTs > g.ntok) TTs = g.ntok;
   const int threads = (int)(TTs * per_tok);
-  const size_t smem = smem_table ? (size_t)TTs * ((size_t)2 * g.h * es + extra_per_slot) : 0;
+  const size_t smem = smem_table ? (size_t)2 * TTs * g.h * es : 0;
   int sms = 0, per_sm = 0;
   rope_status st = device_facts(fn, threads, smem, &sms, &per_sm);
   if (st != ROPE_OK) return st;
@@ -304,6 +310,44 @@ rope_status plan(const Geom& g, int es, bool vec, const void* fn, bool smem_tabl
   L->grid = dim3((unsigned)gx, (unsigned)gy, 1);
   L->block = dim3((unsigned)threads, 1, 1);
   L->smem = smem;
+  return ROPE_OK;
+}
+
+// rope_mrope_heads_kernel: HPT heads per thread, one thread per (token slot,
+// head group, unit); ROPE_ERR_UNSUPPORTED when a token's threads exceed a CTA.
+rope_status plan_heads(const Geom& g, int es, const void* fn, int hpt, KParams* kp, Launch* L, int waves) {
+  const int V = 16 / es;
+  const int64_t nP = g.h / V;
+  const int64_t U = nP + (g.H - g.rd) / V;
+  const int64_t G = (g.N + hpt - 1) / hpt;
+  const int64_t per_tok = G * U;
+  if (per_tok < 1 || per_tok > kMaxRowThreads) return ROPE_ERR_UNSUPPORTED;
+  int64_t TTs = ROPE_TARGET_THREADS / per_tok;
+  if (TTs < 1) TTs = 1;
+  if (TTs * per_tok > kMaxRowThreads) TTs = kMaxRowThreads / per_tok;
+  if (TTs > g.ntok) TTs = g.ntok;
+  const int threads = (int)(TTs * per_tok);
+  int sms = 0, per_sm = 0;
+  ROPE_TRY(device_facts(fn, threads, 0, &sms, &per_sm));
+  const int64_t tiles = (g.ntok + TTs - 1) / TTs;
+  int64_t gx = (int64_t)sms * per_sm * waves;
+  if (gx > tiles) gx = tiles;
+  if (gx > 0x7fffffff) gx = 0x7fffffff;
+  kp->ntok = g.ntok;
+  kp->S = g.S;
+  kp->N = g.N;
+  kp->H = g.H;
+  kp->h = (int32_t)g.h;
+  kp->rd = (int32_t)g.rd;
+  kp->U = (int32_t)U;
+  kp->nP = (int32_t)nP;
+  kp->Ublk = (int32_t)U;
+  kp->NG = (int32_t)G;
+  kp->TTs = (int32_t)TTs;
+  kp->step_tok = gx * TTs;
+  L->grid = dim3((unsigned)gx, 1, 1);
+  L->block = dim3((unsigned)threads, 1, 1);
+  L->smem = 0;
   return ROPE_OK;
 }
 
@@ -838,16 +882,20 @@ rope_status mrope_common(rope_dtype dtype, int32_t x_rank, const int64_t* x_shap
     const void* tfn = tma_kernel(dtype, interleaved != 0, x_rank == 4, Coef::kMRope);
     TmaLaunch T;
     const rope_status ts = plan_tma(dtype, g, es, x_rank, 3, tfn, x, y, &kp, &T);
-    if (ts == ROPE_OK) return launch_tma(tfn, &T, &kp, stream);
-    if (ts != ROPE_ERR_UNSUPPORTED) return ts;
+    const bool forced = g_variant.load(std::memory_order_relaxed) == ROPE_VARIANT_TMA;
+    if (ts == ROPE_OK && (forced || T.tp.x_bytes >= (uint32_t)ROPE_MROPE_TMA_MIN_TILE))
+      return launch_tma(tfn, &T, &kp, stream);
+    if (ts != ROPE_OK && ts != ROPE_ERR_UNSUPPORTED) return ts;
   }
   const int waves = x_rank == 4 ? ROPE_GRID_WAVES : ROPE_ROWS_WAVES_RANK3;
   Launch L;
-  if (vec && g.ntok >= ROPE_MROPE_TABLE_MIN_TOKENS) {
-    // the three streams gathered and merged once per token, into shared memory
-    const void* fn = rope_kernel_mrope_table(dtype, interleaved != 0, x_rank == 4);
-    ROPE_TRY(plan(g, es, vec, fn, true, &kp, &L, false, waves, (size_t)(g.h / (16 / es)) * 4));
-    return launch(fn, L, &kp, stream, "rope_mrope_table_kernel");
+  if (vec) {
+    // each token's three coefficient rows gathered and merged once per 2 or 4 heads
+    const int hpt = g.ntok < ROPE_MROPE_HEADS4_MIN_TOKENS ? 2 : 4;
+    const void* fn = rope_kernel_mrope_heads(dtype, interleaved != 0, x_rank == 4, hpt);
+    const rope_status ps = plan_heads(g, es, fn, hpt, &kp, &L, waves);
+    if (ps == ROPE_OK) return launch(fn, L, &kp, stream, "rope_mrope_heads_kernel");
+    if (ps != ROPE_ERR_UNSUPPORTED) return ps;
   }
   const void* fn = rope_kernel_mrope(dtype, vec, interleaved != 0, x_rank == 4);
   ROPE_TRY(plan(g, es, vec, fn, false, &kp, &L, false, waves));

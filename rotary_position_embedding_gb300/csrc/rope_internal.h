@@ -76,10 +76,9 @@ struct QKVParams {
 // the 128-bit vector path. Return nullptr for unsupported combinations.
 const void* rope_kernel_cached(int dtype, bool vec, bool interleaved, bool rank4, Coef mode);
 const void* rope_kernel_mrope(int dtype, bool vec, bool interleaved, bool rank4);
-// Cached M-RoPE through a per-token shared-memory table (128-bit path only);
-// its launch takes (KParams) with TTs * (2 * h * elem + nP * 4) bytes of
-// dynamic shared memory.
-const void* rope_kernel_mrope_table(int dtype, bool interleaved, bool rank4);
+// Cached M-RoPE with hpt (2 or 4) heads per thread (128-bit path only); its
+// launch takes (KParams) with NG = head groups, Ublk = U, no shared memory.
+const void* rope_kernel_mrope_heads(int dtype, bool interleaved, bool rank4, int hpt);
 const void* fused_kernel(int dtype, bool vec, bool interleaved, bool rank4, bool mrope = false);
 const void* cache_build_kernel(int dtype);
 // rope_qkv_kernel instance; its launch takes (KParams, QKVParams).

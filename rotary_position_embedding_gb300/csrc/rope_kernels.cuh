@@ -539,169 +539,4 @@ __global__ void __launch_bounds__(kMaxRowThreads) rope_rows_kernel(const KParams
   }
 }
 
-// ---------------------------------------------------------------------------
-// Cached M-RoPE through a per-token shared-memory table (128-bit path). The
-// rows kernel above merges the three streams in every thread, so each token's
-// coefficients are gathered and merged once per head; here they are merged
-// once per token. Per tile of TTs tokens:
-//   1. each thread loads its first X unit (the DRAM latency overlaps 2-3);
-//   2. one thread per (token, V-index piece) of the half-rotary axis loads the
-//      token's positions of the streams the piece uses, gathers the in-range
-//      rows' cos/sin pieces, merges them by the stream map's masks, applies
-//      the scale step, and writes the merged pieces and the streams' validity
-//      to shared memory;
-//   3. every (token, head, unit) thread rotates from the table and puts back,
-//      from X, the pairs whose stream position is out of range.
-// The same arithmetic as the rows kernel and the TMA pipeline
-// ("com.microsoft.MRotaryEmbedding" README: Description, Inputs/positionIds,
-// Attributes mrope_section, mrope_layout, scale).
-// ---------------------------------------------------------------------------
-#ifndef ROPE_MROPE_TABLE_MAXREG
-#define ROPE_MROPE_TABLE_MAXREG 56
-#endif
-template <class T, int V, bool INTER, bool RANK4>
-__global__ void __maxnreg__(ROPE_MROPE_TABLE_MAXREG) rope_mrope_table_kernel(const KParams p) {
-  using E = Elem<T>;
-  using VT = VecT<T, V>;
-  using bits = typename E::bits;
-  static_assert(V * sizeof(bits) == 16, "128-bit units only");
-  extern __shared__ __align__(16) unsigned char smem_raw[];
-  bits* sc = reinterpret_cast<bits*>(smem_raw);           // [TTs][h] merged cos
-  bits* ss = sc + (size_t)p.TTs * p.h;                     // [TTs][h] merged sin
-  uint32_t* sv = reinterpret_cast<uint32_t*>(ss + (size_t)p.TTs * p.h);  // [TTs][nP] valid streams
-
-  const int tid = threadIdx.x;
-  const int per_tok = p.NG * p.Ublk;
-  const int slot = tid / per_tok;
-  const int r = tid - slot * per_tok;
-  const int ng = r / p.Ublk;
-  const int k0 = r - ng * p.Ublk;
-  const int64_t n = (int64_t)blockIdx.y * p.NG + ng;
-  const bool active = slot < p.TTs && n < p.N;
-  const int nP = p.nP;
-  const int items = p.TTs * nP;
-
-  // x and y may be the same buffer (in place), so neither is __restrict__
-  const bits* x = static_cast<const bits*>(p.x);
-  bits* y = static_cast<bits*>(p.y);
-  const bits* __restrict__ cosb = static_cast<const bits*>(p.cos);
-  const bits* __restrict__ sinb = static_cast<const bits*>(p.sin);
-  pdl_launch_dependents();
-  pdl_wait();
-
-  for (int64_t tile0 = (int64_t)blockIdx.x * p.TTs; tile0 < p.ntok; tile0 += p.step_tok) {
-    const int64_t tok = tile0 + slot;
-    const bool mine = active && tok < p.ntok;
-    int64_t row = 0;
-    if (mine) {
-      if (RANK4) {
-        const int64_t b = tok / p.S, s = tok - b * p.S;
-        row = ((b * p.N + n) * p.S + s) * p.H;
-      } else {
-        row = (tok * p.N + n) * p.H;
-      }
-    }
-    const bits* xr = x + row;
-    bits* yr = y + row;
-    const bool pre = mine && k0 < nP;
-    int pa = 0, pb = 0;
-    VT a0{}, b0{};
-    if (pre) {
-      unit_offsets<V, INTER>(k0, p.h, pa, pb);
-      a0 = ld_stream(reinterpret_cast<const VT*>(xr + pa));
-      b0 = ld_stream(reinterpret_cast<const VT*>(xr + pb));
-    }
-    __syncthreads();  // the previous tile's readers are done with the table
-    for (int it = tid; it < items; it += blockDim.x) {
-      const int ls = it / nP;
-      const int q = it - ls * nP;
-      const int64_t t = tile0 + ls;
-      if (t >= p.ntok) continue;
-      const int oc = q * V;
-      const uint32_t word = p.smap[oc >> 4];
-      const uint32_t um = (word >> ((oc & 15) * 2)) & (uint32_t)((1ull << (2 * V)) - 1);
-      uint32_t present = 0;
-#pragma unroll
-      for (int j = 0; j < V; ++j) present |= 1u << ((um >> (2 * j)) & 3);
-      // positions of the streams the piece uses, then each in-range stream's
-      // pieces accumulated under that stream's element mask
-      int64_t ps[3];
-#pragma unroll
-      for (int st = 0; st < 3; ++st) ps[st] = (present & (1u << st)) ? __ldg(p.pos + st * p.ntok + t) : -1;
-      uint32_t valid = 0;
-      uint32_t cw[4] = {0, 0, 0, 0}, sw[4] = {0, 0, 0, 0};
-#pragma unroll
-      for (int st = 0; st < 3; ++st) {
-        if ((present & (1u << st)) && (uint64_t)ps[st] < (uint64_t)p.cache_rows) {
-          valid |= 1u << st;
-          uint32_t sel = 0;
-#pragma unroll
-          for (int j = 0; j < V; ++j) sel |= (((um >> (2 * j)) & 3u) == (uint32_t)st ? 1u : 0u) << j;
-          uint32_t m[4];
-          unit_mask<V>(sel, m);
-          const VT cv = ld_shared_ro(reinterpret_cast<const VT*>(cosb + ps[st] * p.h + oc));
-          const VT sv2 = ld_shared_ro(reinterpret_cast<const VT*>(sinb + ps[st] * p.h + oc));
-          uint32_t cu[4], su[4];
-          __builtin_memcpy(cu, &cv, 16);
-          __builtin_memcpy(su, &sv2, 16);
-#pragma unroll
-          for (int w = 0; w < 4; ++w) {
-            cw[w] |= cu[w] & m[w];
-            sw[w] |= su[w] & m[w];
-          }
-        }
-      }
-      if (present & ~valid) flag_oor(p.oor_flag);
-      VT c, sn;
-      __builtin_memcpy(&c, cw, 16);
-      __builtin_memcpy(&sn, sw, 16);
-      if (!p.scale_is_one) {
-        scale_round<T, V>(c, p.scale);
-        scale_round<T, V>(sn, p.scale);
-      }
-      *reinterpret_cast<VT*>(sc + (size_t)ls * p.h + oc) = c;
-      *reinterpret_cast<VT*>(ss + (size_t)ls * p.h + oc) = sn;
-      sv[it] = valid;
-    }
-    __syncthreads();
-    if (!mine) continue;
-    for (int k = k0; k < p.U; k += p.Ublk) {
-      if (k >= nP) {  // tail unit: bit copy
-        const int off = p.rd + (k - nP) * V;
-        st_stream(reinterpret_cast<VT*>(yr + off), ld_stream(reinterpret_cast<const VT*>(xr + off)));
-        continue;
-      }
-      int oa, ob;
-      unit_offsets<V, INTER>(k, p.h, oa, ob);
-      VT a, bv;
-      if (k == k0) {  // loaded before the table
-        a = a0;
-        bv = b0;
-      } else {
-        a = ld_stream(reinterpret_cast<const VT*>(xr + oa));
-        bv = ld_stream(reinterpret_cast<const VT*>(xr + ob));
-      }
-      const int oc = k * V;
-      const VT c = *reinterpret_cast<const VT*>(sc + (size_t)slot * p.h + oc);
-      const VT sn = *reinterpret_cast<const VT*>(ss + (size_t)slot * p.h + oc);
-      VT ya, yb;
-      rotate_unit<T, V, INTER>(a, bv, c, sn, ya, yb);
-      const uint32_t valid = sv[slot * nP + k];
-      const uint32_t word = p.smap[oc >> 4];
-      const uint32_t um = (word >> ((oc & 15) * 2)) & (uint32_t)((1ull << (2 * V)) - 1);
-      uint32_t present = 0;
-#pragma unroll
-      for (int j = 0; j < V; ++j) present |= 1u << ((um >> (2 * j)) & 3);
-      if (present & ~valid) {  // pairs of out-of-range streams keep their input
-        uint32_t ma[4], mb[4];
-        pair_masks<V, INTER>(um, valid, ma, mb);
-        blend(ya, a, ma);
-        blend(yb, bv, mb);
-      }
-      st_stream(reinterpret_cast<VT*>(yr + oa), ya);
-      st_stream(reinterpret_cast<VT*>(yr + ob), yb);
-    }
-  }
-}
-
 }  // namespace rope_gb300

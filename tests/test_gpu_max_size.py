@@ -7,8 +7,8 @@ recomputes sampled tokens one by one: the first token, the last token (the
 highest addresses) and tokens spread over the whole tensor, all heads each.
 The cases cover the SIMT kernel (full rotation, rank 3 and rank 4) and the TMA
 pipeline (partial rotation and M-RoPE), each through the automatic variant
-choice, as the benchmark launches them, the SIMT M-RoPE kernel (shared-memory
-coefficient table) by the SIMT variant; and the Q/K op (RoPE on both Q/K
+choice, as the benchmark launches them, the SIMT M-RoPE kernel (several heads per
+thread) by the SIMT variant; and the Q/K op (RoPE on both Q/K
 kernels, M-RoPE on the pipeline) over a packed [Q|K|V] of 3.2 G elements.
 """
 
@@ -35,7 +35,7 @@ def _sample_tokens(rng):
                                          ("rope_full_rank4", "rope_rows_kernel"),
                                          ("rope_partial_rank3", "rope_tma_kernel"),
                                          ("mrope_rank3", "rope_tma_kernel"),
-                                         ("mrope_rank3_simt", "rope_mrope_table_kernel")])
+                                         ("mrope_rank3_simt", "rope_mrope_heads_kernel")])
 def test_over_two_to_the_31_elements(lib, orc, cuda, case, kernel):
     import torch
 

@@ -311,8 +311,10 @@ def test_dynamic_schedule_back_to_back_and_shared_scratch(lib, orc, cuda, torch_
 
 def test_automatic_variant_choice(lib, orc, cuda, torch_mod):
     """The automatic choice: full-rotation RoPE runs the SIMT kernel at any size;
-    partial rotation of a large X and M-RoPE of a large X run the TMA pipeline;
-    small X always runs SIMT. Every choice still matches the oracle."""
+    partial rotation of a large X and M-RoPE of a large X run the TMA pipeline, unless
+    M-RoPE's three coefficient rows per token shrink its tiles (few heads), when the
+    SIMT heads kernel runs; small X always runs SIMT. Every choice still matches the
+    oracle."""
     torch = torch_mod
     rng = np.random.default_rng(37)
     B, S, N, H = 2, 1024, 32, 128                 # 16 MiB of float16: above the pipeline's threshold
@@ -341,6 +343,15 @@ def test_automatic_variant_choice(lib, orc, cuda, torch_mod):
         y_ref, _ = orc.mrope(x, cos, sin, pos3, (16, 24, 24), 1, 1.0, 0, 0, N)
         smap = orc.mrope_stream_map((16, 24, 24), 1, H // 2)
         compare(_host(y), y_ref, x, 3, N, mrope_passthrough_mask(x.shape, 3, N, 0, pos3, R, smap, 0))
+        # 4 heads: 16 MiB, but the pipeline's M-RoPE tile would be 5 tokens x 4 heads (5 KB)
+        x4 = rng.standard_normal((2, 8192, 4 * H)).astype(np.float16)
+        p4 = rng.integers(0, R, (3, 2, 8192))
+        y4 = lib.mrope_apply(_dev(x4, torch, cuda), _dev(cos, torch, cuda), _dev(sin, torch, cuda),
+                             _dev(p4, torch, cuda), (16, 24, 24), mrope_layout=1, num_heads=4)
+        assert lib.last_kernel() == "rope_mrope_heads_kernel"
+        torch.cuda.synchronize()
+        y_ref4, _ = orc.mrope(x4, cos, sin, p4, (16, 24, 24), 1, 1.0, 0, 0, 4)
+        compare(_host(y4), y_ref4, x4, 3, 4, mrope_passthrough_mask(x4.shape, 3, 4, 0, p4, R, smap, 0))
         small = xd[:, :64].contiguous()           # 1 MiB: SIMT whatever the rotation
         lib.rope_apply(small, *tables[64], pd[:, :64].contiguous(), num_heads=N, rotary_embedding_dim=64)
         assert lib.last_kernel() == "rope_rows_kernel"
@@ -400,19 +411,21 @@ def test_mrope_grid(lib, orc, cuda, torch_mod, dt, rank, layout, inter, rot, sca
     assert int(flag.item()) == (1 if n_oor else 0)
 
 
-TABLE_GRID = list(itertools.product(["f16", "f32", "bf16"], [3, 4], ["l0", "l1", "stride3"], [0, 1],
-                                    ["full", "partial"], [1.0, 0.7]))
+HEADS_GRID = list(itertools.product(["f16", "f32", "bf16"], [3, 4], ["l0", "l1", "stride3"], [0, 1],
+                                    ["full", "partial"], [1.0, 0.7], [2, 4]))
 
 
-@pytest.mark.parametrize("dt,rank,layout,inter,rot,scale", TABLE_GRID)
-def test_mrope_table_kernel(lib, orc, cuda, torch_mod, dt, rank, layout, inter, rot, scale):
-    """The SIMT M-RoPE path from 512 tokens: each token's three coefficient rows merged once
-    into shared memory. 600 tokens (several tiles per CTA), out-of-range ids in every
-    stream, partial rotation with a tail, both pairings, scaled coefficients."""
+@pytest.mark.parametrize("dt,rank,layout,inter,rot,scale,hpt", HEADS_GRID)
+def test_mrope_heads_kernel(lib, orc, cuda, torch_mod, dt, rank, layout, inter, rot, scale, hpt):
+    """The SIMT M-RoPE kernel on the 128-bit path: each thread merges a unit's three
+    coefficient rows once and rotates 2 (below 512 tokens) or 4 heads with them. 5 heads
+    (an uneven last head group either way), out-of-range ids in every stream, partial
+    rotation with a tail, both pairings, scaled coefficients; 600 tokens for 4 heads per
+    thread, 250 for 2."""
     torch = torch_mod
     dtype = DT[dt]
-    rng = np.random.default_rng(_seed(dt, rank, layout, inter, rot, scale, "table"))
-    B, S, N, H = 2, 300, 3, 64
+    rng = np.random.default_rng(_seed(dt, rank, layout, inter, rot, scale, hpt, "heads"))
+    B, S, N, H = 2, (300 if hpt == 4 else 125), 5, 64
     rd, sec = (0, (8, 12, 12)) if rot == "full" else (32, (4, 6, 6))
     h = (rd or H) // 2
     R = 700
@@ -439,38 +452,43 @@ def test_mrope_table_kernel(lib, orc, cuda, torch_mod, dt, rank, layout, inter, 
             yd = lib.mrope_apply_stream_map(*args, smap.tolist(), **kw)
         else:
             yd = lib.mrope_apply(*args, sec, mrope_layout=0 if layout == "l0" else 1, **kw)
-        assert lib.last_kernel() == "rope_mrope_table_kernel"
+        assert lib.last_kernel() == "rope_mrope_heads_kernel"
     torch.cuda.synchronize()
     compare(_host(yd), y_ref, x, rank, N, mrope_passthrough_mask(shape, rank, N, rd, pos3, R, smap, inter))
     assert int(flag.item()) == (1 if n_oor else 0)
 
 
 @pytest.mark.parametrize("dt", ["f16", "bf16", "f32"])
-def test_mrope_simt_kernels_agree_at_the_switch(lib, orc, cuda, torch_mod, dt):
-    """511 tokens take the per-thread merge, 512 the shared-memory table: the two SIMT
-    M-RoPE kernels and the pipeline give the same bits on the same tokens."""
+def test_mrope_kernels_agree_bitwise(lib, orc, cuda, torch_mod, dt):
+    """The M-RoPE kernels give the same bits on the same tokens: 512 tokens take 4 heads
+    per thread, 511 take 2, the pipeline (forced), and the per-element scalar path (X one
+    element off 16-byte alignment)."""
     torch = torch_mod
     rng = np.random.default_rng(91)
-    N, H, R = 4, 128, 2048
+    N, H, R = 6, 128, 2048
     x = cast(rng.standard_normal((1, 512, N * H)), DT[dt])
     cos, sin = orc.cache_build(wl.inv_freq(1e6, H, H // 2), R, DT[dt])
     pos3 = rng.integers(0, R, (3, 1, 512))
     pos3[1, 0, 100] = R + 1
     xd, cd, sd, pd = (_dev(a, torch, cuda) for a in (x, cos, sin, pos3))
     outs = {}
+    kw = dict(mrope_layout=1, num_heads=N)
     with lib.variant("simt"):
-        outs["table"] = lib.mrope_apply(xd, cd, sd, pd, (16, 24, 24), mrope_layout=1, num_heads=N)
-        assert lib.last_kernel() == "rope_mrope_table_kernel"
-        outs["rows"] = lib.mrope_apply(xd[:, :511].contiguous(), cd, sd, pd[:, :, :511].contiguous(), (16, 24, 24),
-                                       mrope_layout=1, num_heads=N)
+        outs["heads4"] = lib.mrope_apply(xd, cd, sd, pd, (16, 24, 24), **kw)
+        assert lib.last_kernel() == "rope_mrope_heads_kernel"
+        outs["heads2"] = lib.mrope_apply(xd[:, :511].contiguous(), cd, sd, pd[:, :, :511].contiguous(), (16, 24, 24),
+                                         **kw)
+        assert lib.last_kernel() == "rope_mrope_heads_kernel"
+        outs["scalar"] = lib.mrope_apply(_dev(x, torch, cuda, 1), cd, sd, pd, (16, 24, 24), **kw)
         assert lib.last_kernel() == "rope_rows_kernel"
     with lib.variant("tma"):
-        outs["tma"] = lib.mrope_apply(xd, cd, sd, pd, (16, 24, 24), mrope_layout=1, num_heads=N)
+        outs["tma"] = lib.mrope_apply(xd, cd, sd, pd, (16, 24, 24), **kw)
         assert lib.last_kernel() == "rope_tma_kernel"
     torch.cuda.synchronize()
     bits = torch.int32 if dt == "f32" else torch.int16
-    assert torch.equal(outs["table"][:, :511].view(bits), outs["rows"].view(bits))
-    assert torch.equal(outs["table"].view(bits), outs["tma"].view(bits))
+    assert torch.equal(outs["heads4"][:, :511].view(bits), outs["heads2"].view(bits))
+    assert torch.equal(outs["heads4"].view(bits), outs["tma"].view(bits))
+    assert torch.equal(outs["heads4"].view(bits), outs["scalar"].view(bits))
 
 
 def test_mrope_equal_streams_equals_rope_on_gpu(lib, orc, cuda, torch_mod):
@@ -679,7 +697,7 @@ def test_workload_full_size(lib, orc, cuda, torch_mod, name):
     print(name, stats)
 
 
-@pytest.mark.parametrize("variant,kernel", [("auto", "rope_tma_kernel"), ("simt", "rope_mrope_table_kernel")])
+@pytest.mark.parametrize("variant,kernel", [("auto", "rope_tma_kernel"), ("simt", "rope_mrope_heads_kernel")])
 @pytest.mark.parametrize("dt", ["float16", "bfloat16"])
 def test_mrope_full_size_stride3_reading(lib, orc, cuda, torch_mod, variant, kernel, dt):
     """The M-RoPE workload ((2, 8192, 28 x 128), sections [16, 24, 24], 1 % of ids past the
