@@ -491,6 +491,38 @@ def test_mrope_kernels_agree_bitwise(lib, orc, cuda, torch_mod, dt):
     assert torch.equal(outs["heads4"].view(bits), outs["scalar"].view(bits))
 
 
+@pytest.mark.parametrize("dt,rank,inter", list(itertools.product(["f16", "f32", "bf16"], [3, 4], [0, 1])))
+@pytest.mark.parametrize("path", ["heads2", "heads4", "tma", "scalar"])
+def test_mrope_in_place(lib, orc, cuda, torch_mod, dt, rank, inter, path):
+    """y == x for M-RoPE on every path (each thread, or each consumer column, reads its
+    elements before it writes them): partial rotation with a tail, out-of-range ids in
+    every stream (pairs put back from X), 2 and 4 heads per thread, the pipeline and the
+    per-element scalar path."""
+    torch = torch_mod
+    dtype = DT[dt]
+    rng = np.random.default_rng(_seed(dt, rank, inter, path, "inplace"))
+    B, S, N, H, rd, sec = 2, (300 if path == "heads4" else 40), 5, 64, 48, (8, 8, 8)
+    R = 400
+    shape = _x_shape(rank, B, S, N, H)
+    x = cast(rng.standard_normal(shape), dtype)
+    cos, sin = orc.cache_build(wl.inv_freq(10000.0, rd, rd // 2), R, dtype)
+    pos3 = rng.integers(0, R, (3, B, S))
+    oor = rng.random((3, B, S)) < 0.05
+    pos3[oor] = R + 2
+    nh = N if rank == 3 else 0
+    y_ref, _ = orc.mrope(x, cos, sin, pos3, sec, 1, 1.0, inter, rd, nh)
+    xd = _dev(x, torch, cuda, 1 if path == "scalar" else 0)
+    with lib.variant("tma" if path == "tma" else "simt"):
+        out = lib.mrope_apply(xd, _dev(cos, torch, cuda), _dev(sin, torch, cuda), _dev(pos3, torch, cuda), sec,
+                              mrope_layout=1, interleaved=inter, rotary_embedding_dim=rd, num_heads=nh, out=xd)
+        kernel = {"tma": "rope_tma_kernel", "scalar": "rope_rows_kernel"}.get(path, "rope_mrope_heads_kernel")
+        assert lib.last_kernel() == kernel
+    torch.cuda.synchronize()
+    assert out.data_ptr() == xd.data_ptr()
+    smap = orc.mrope_stream_map(sec, 1, rd // 2)
+    compare(_host(xd), y_ref, x, rank, N, mrope_passthrough_mask(shape, rank, N, rd, pos3, R, smap, inter))
+
+
 def test_mrope_equal_streams_equals_rope_on_gpu(lib, orc, cuda, torch_mod):
     """Text tokens (t = h = w) reduce M-RoPE to RotaryEmbedding, bit for bit on the GPU too."""
     torch = torch_mod
