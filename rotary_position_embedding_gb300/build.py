@@ -19,9 +19,9 @@ INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(HERE, "_lib")
 LIB_PATH = os.path.join(OUT_DIR, "librope_gb300.so")
 SOURCES = ["rope_api.cu", "k_rope.cu", "k_mrope.cu", "k_fused.cu", "k_tma.cu", "k_qkv.cu", "k_mrope_qkv.cu", "k_qkv_tma.cu", "k_mrope_qkv_tma.cu",
-           "k_mrope_heads.cu", "no_alloc.cu"]
+           "k_mrope_heads.cu", "k_qkv_heads.cu", "no_alloc.cu"]
 HEADERS = ["rope_kernels.cuh", "rope_internal.h", "rope_tma.cuh", "rope_qkv.cuh", "rope_qkv_tma.cuh", "rope_packed.cuh", "rope_fused.cuh",
-           "rope_mrope_heads.cuh"]
+           "rope_mrope_heads.cuh", "rope_qkv_heads.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

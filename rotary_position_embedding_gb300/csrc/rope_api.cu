@@ -351,6 +351,50 @@ rope_status plan_heads(const Geom& g, int es, const void* fn, int hpt, KParams* 
   return ROPE_OK;
 }
 
+// rope_qkv_heads_kernel: hpt heads of one role per thread, one thread per
+// (token slot, head group, unit); ROPE_ERR_UNSUPPORTED when a token's threads
+// exceed a CTA or (RMSNorm) a row's units are not a power-of-two lane group.
+rope_status plan_qkv_heads(const Geom& g, int es, const void* fn, int hpt, int64_t nq, int64_t nkv, bool cache,
+                           bool norm, KParams* kp, Launch* L) {
+  const int V = 16 / es;
+  const int64_t nP = g.h / V;
+  const int64_t U = nP + (g.H - g.rd) / V;
+  if (U < 1) return ROPE_ERR_UNSUPPORTED;
+  if (norm && (U > 32 || (U & (U - 1)))) return ROPE_ERR_UNSUPPORTED;
+  const int64_t G = (nq + hpt - 1) / hpt + (cache ? 2 : 1) * ((nkv + hpt - 1) / hpt);
+  const int64_t per_tok = G * U;
+  if (per_tok > kMaxRowThreads) return ROPE_ERR_UNSUPPORTED;
+  int64_t TTs = ROPE_TARGET_THREADS / per_tok;
+  if (TTs < 1) TTs = 1;
+  if (TTs * per_tok > kMaxRowThreads) TTs = kMaxRowThreads / per_tok;
+  if (TTs > g.ntok) TTs = g.ntok;
+  const int threads = (int)(TTs * per_tok);
+  int sms = 0, per_sm = 0;
+  ROPE_TRY(device_facts(fn, threads, 0, &sms, &per_sm));
+  const int64_t tiles = (g.ntok + TTs - 1) / TTs;
+  int64_t gx = (int64_t)sms * per_sm;
+  if (gx > tiles) gx = tiles;
+  if (gx > 0x7fffffff) gx = 0x7fffffff;
+  kp->ntok = g.ntok;
+  kp->S = g.S;
+  kp->N = g.N;
+  kp->H = g.H;
+  kp->h = (int32_t)g.h;
+  kp->rd = (int32_t)g.rd;
+  kp->U = (int32_t)U;
+  kp->nP = (int32_t)nP;
+  kp->Ublk = (int32_t)U;
+  kp->NG = (int32_t)G;
+  kp->TTs = (int32_t)TTs;
+  kp->step_tok = gx * TTs;
+  kp->step_b = g.S ? kp->step_tok / g.S : 0;
+  kp->step_s = g.S ? kp->step_tok % g.S : 0;
+  L->grid = dim3((unsigned)gx, 1, 1);
+  L->block = dim3((unsigned)threads, 1, 1);
+  L->smem = 0;
+  return ROPE_OK;
+}
+
 // ---------------------------------------------------------------------------
 // TMA pipeline planning (see rope_tma.cuh).
 // ---------------------------------------------------------------------------
@@ -1060,6 +1104,63 @@ rope_status rope_apply_fused(rope_dtype dtype, int32_t x_rank, const int64_t* x_
 
 namespace {
 
+// Heads per thread of rope_qkv_heads_kernel: RoPE on 16-bit data, on float32
+// data, and RMSNorm + RoPE.
+#ifndef ROPE_QKV_HPT_ROPE
+#define ROPE_QKV_HPT_ROPE 4
+#endif
+#ifndef ROPE_QKV_HPT_ROPE32
+#define ROPE_QKV_HPT_ROPE32 2
+#endif
+#ifndef ROPE_QKV_HPT_NORM
+#define ROPE_QKV_HPT_NORM 2
+#endif
+// RoPE on 16-bit data takes ROPE_QKV_HPT_ROPE heads per thread from this many
+// tokens on, 2 below (more, smaller CTAs for decode-sized batches).
+#ifndef ROPE_QKV_HEADS4_MIN_TOKENS
+#define ROPE_QKV_HEADS4_MIN_TOKENS 4096
+#endif
+// rope_qkv_heads_kernel goes ahead of the pipeline for RoPE without QK-Norm
+// over the whole head, except in cache mode with the K/V heads at least half
+// the Q heads and [Q|K|V] of at least this many bytes: there the pipeline's
+// tiled cache writes (many tokens of one head per store) measured faster.
+#ifndef ROPE_QKV_PIPE_CACHE_MIN_BYTES
+#define ROPE_QKV_PIPE_CACHE_MIN_BYTES (128ll << 20)
+#endif
+
+// rope_qkv_heads_kernel launch (128-bit path, RoPE); ROPE_ERR_UNSUPPORTED (no
+// message) when the shape does not fit it, and the caller takes another kernel.
+rope_status launch_qkv_heads(int dtype, const Geom& g, int es, bool inter, bool implicit_pos, bool norm,
+                             int64_t nq, int64_t nkv, bool cache, KParams* kp, const QKVParams* qa,
+                             rope_stream_t stream) {
+  const int hpt0 = norm                                     ? ROPE_QKV_HPT_NORM
+                   : es == 4                                ? ROPE_QKV_HPT_ROPE32
+                   : g.ntok >= ROPE_QKV_HEADS4_MIN_TOKENS ? ROPE_QKV_HPT_ROPE
+                                                            : 2;
+  // the widest group up to `top` that divides both head counts, else `top` with
+  // a short last group per role; wider groups when a token's threads exceed a CTA
+  for (int top = hpt0; top <= (norm ? 2 : 4); top *= 2) {
+    int hpt = 0;
+    for (int w = top; w >= 2 && !hpt; w /= 2)
+      if (nq % w == 0 && nkv % w == 0) hpt = w;
+    const bool ragged = hpt == 0;
+    if (ragged) hpt = top;
+    const void* fn = qkv_heads_kernel(dtype, inter, implicit_pos, norm, hpt, ragged);
+    if (!fn) continue;
+    Launch L;
+    const rope_status st = plan_qkv_heads(g, es, fn, hpt, nq, nkv, cache, norm, kp, &L);
+    if (st == ROPE_ERR_UNSUPPORTED) continue;
+    if (st != ROPE_OK) return st;
+    QKVParams a = *qa;
+    void* args[] = {kp, &a};
+    cudaError_t e = launch_pdl(fn, L.grid, L.block, L.smem, stream, args);
+    if (e != cudaSuccess) return cuda_fail(e, "rope_apply_qkv launch (heads per thread)");
+    g_last_kernel = "rope_qkv_heads_kernel";
+    return ROPE_OK;
+  }
+  return ROPE_ERR_UNSUPPORTED;
+}
+
 // rope_apply_qkv and rope_apply_qkv_rmsnorm (q_weight == NULL: no norm).
 rope_status qkv_impl(rope_dtype dtype, int64_t batch, int64_t seq, int32_t num_heads, int32_t kv_num_heads,
                      int64_t head_size, const void* query, const void* key, const void* value,
@@ -1195,6 +1296,14 @@ rope_status qkv_impl(rope_dtype dtype, int64_t batch, int64_t seq, int32_t num_h
   qa.kw = k_weight;
   qa.eps = epsilon;
   const int64_t n_all = (int64_t)num_heads + 2 * kv_num_heads;
+  const bool pipe_first = cache && num_heads <= 2 * (int64_t)kv_num_heads &&
+                          packed_numel * es >= (int64_t)ROPE_QKV_PIPE_CACHE_MIN_BYTES;
+  if (vec && !mrope && !norm && g.rd == g.H && !pipe_first &&
+      g_variant.load(std::memory_order_relaxed) != ROPE_VARIANT_TMA) {
+    const rope_status hs = launch_qkv_heads(dtype, g, es, interleaved != 0, position_ids == nullptr, norm,
+                                            num_heads, kv_num_heads, cache, &kp, &qa, stream);
+    if (hs != ROPE_ERR_UNSUPPORTED) return hs;
+  }
   if (qkv_tma_eligible(g, es, vec, norm, n_all, cache ? max_cache_len : 0, packed_numel * es)) {
     const void* tfn = mrope ? mrope_qkv_tma_kernel(dtype, interleaved != 0, norm)
                             : qkv_tma_kernel(dtype, interleaved != 0, position_ids == nullptr, norm);
@@ -1217,6 +1326,11 @@ rope_status qkv_impl(rope_dtype dtype, int64_t batch, int64_t seq, int32_t num_h
     if (ts != ROPE_ERR_UNSUPPORTED) return ts;
   }
   Launch L;
+  if (vec && !mrope) {  // below the pipeline: the heads-per-thread kernel where it fits
+    const rope_status hs = launch_qkv_heads(dtype, g, es, interleaved != 0, position_ids == nullptr, norm,
+                                            num_heads, kv_num_heads, cache, &kp, &qa, stream);
+    if (hs != ROPE_ERR_UNSUPPORTED) return hs;
+  }
   ROPE_TRY(plan(g, es, vec, fn, false, &kp, &L, /*unit_groups=*/norm));
   void* args[] = {&kp, &qa};
   cudaError_t e = launch_pdl(fn, L.grid, L.block, L.smem, stream, args);

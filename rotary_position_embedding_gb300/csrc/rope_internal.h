@@ -86,6 +86,11 @@ const void* qkv_kernel(int dtype, bool vec, bool interleaved, bool implicit_pos,
 // The M-RoPE instance of rope_qkv_kernel (positions (3, B, S), KParams.smap /
 // scale as for mrope_apply); same launch.
 const void* mrope_qkv_kernel(int dtype, bool vec, bool interleaved, bool rms_norm);
+// rope_qkv_heads_kernel (128-bit path, RoPE): hpt heads of one role per thread
+// (RoPE: 2 or 4, RMSNorm: 2); ragged: a role's head count need not be a
+// multiple of hpt. Same launch, KParams.NG = head groups, Ublk = U; nullptr
+// for a shape not instantiated.
+const void* qkv_heads_kernel(int dtype, bool interleaved, bool implicit_pos, bool rms_norm, int hpt, bool ragged);
 // Records the message rope_last_error() returns on the calling thread.
 void set_last_error(const char* msg);
 

@@ -108,9 +108,10 @@ def test_over_two_to_the_31_elements(lib, orc, cuda, case, kernel):
 QB, QS, QNQ, QNKV, QH = 8, 65536, 32, 8, 128
 
 
-@pytest.mark.parametrize("op,variant,kernel", [("rope", "auto", "rope_qkv_tma_kernel"),
-                                               ("rope", "simt", "rope_qkv_kernel"),
-                                               ("mrope", "auto", "rope_qkv_tma_kernel")])
+@pytest.mark.parametrize("op,variant,kernel", [("rope", "auto", "rope_qkv_heads_kernel"),
+                                               ("rope", "tma", "rope_qkv_tma_kernel"),
+                                               ("mrope", "auto", "rope_qkv_tma_kernel"),
+                                               ("mrope", "simt", "rope_qkv_kernel")])
 def test_qkv_over_two_to_the_31_elements(lib, orc, cuda, op, variant, kernel):
     import torch
 

@@ -132,8 +132,8 @@ def _run_case(lib, orc, torch, cuda, dt, packed, cache, inter, rot, implicit, H,
 
 
 QKV_GRID = list(itertools.product(["f16", "f32", "bf16"], [0, 1], [0, 1], [0, 1], ["full", "partial"], [0, 1]))
-# the SIMT kernel (the automatic choice at these sizes) and the TMA pipeline (forced)
-QKV_KERNELS = {"auto": "rope_qkv_kernel", "tma": "rope_qkv_tma_kernel"}
+# the heads-per-thread kernel (the automatic choice at these sizes) and the TMA pipeline (forced)
+QKV_KERNELS = {"auto": "rope_qkv_heads_kernel", "tma": "rope_qkv_tma_kernel"}
 
 
 @pytest.mark.parametrize("variant", list(QKV_KERNELS))
@@ -221,6 +221,19 @@ def test_qkv_empty_and_rejects(lib, cuda):
                            key=torch.zeros((1, 4, 64), dtype=torch.float16, device=cuda))
 
 
+def expected_qkv_kernel(auto, norm, qkv_bytes, Nq, Nkv, cache):
+    """The automatic choice for whole-width rotation on the 128-bit path: QK-Norm takes
+    the TMA pipeline from 8 MiB of [Q|K|V] on; plain RoPE takes the heads-per-thread
+    kernel, except in cache mode with Nq <= 2*Nkv from 128 MiB on (the pipeline)."""
+    if not auto:
+        return "rope_qkv_heads_kernel"
+    if norm:
+        return "rope_qkv_tma_kernel" if qkv_bytes >= 8 << 20 else "rope_qkv_heads_kernel"
+    if cache and Nq <= 2 * Nkv and qkv_bytes >= 128 << 20:
+        return "rope_qkv_tma_kernel"
+    return "rope_qkv_heads_kernel"
+
+
 @pytest.mark.parametrize("variant", ["auto", "auto_dynamic", "simt"])
 @pytest.mark.parametrize("name", [n for n, w in wl.WORKLOADS.items() if w.kind == "qkv"])
 def test_qkv_workload_full_size(lib, orc, cuda, name, variant):
@@ -257,8 +270,7 @@ def test_qkv_workload_full_size(lib, orc, cuda, name, variant):
                                     num_heads=Nq, kv_num_heads=Nkv, k_cache=kc, v_cache=vc,
                                     past_seq_lens=_dev(past, torch, cuda), status=status, scratch=scratch, **nkw)
     torch.cuda.synchronize()
-    big = x.nbytes >= 8 << 20   # the automatic choice sends 8 MiB and more to the TMA pipeline
-    assert lib.last_kernel() == ("rope_qkv_tma_kernel" if variant != "simt" and big else "rope_qkv_kernel")
+    assert lib.last_kernel() == expected_qkv_kernel(variant != "simt", norm, x.nbytes, Nq, Nkv, cache=True)
     assert ko is None and int(status.item()) == 0
     none_bad = np.zeros((B, S), dtype=bool)
     bi = torch.arange(B, device=cuda)[:, None].expand(B, S)
@@ -292,6 +304,42 @@ def test_qkv_negative_past_lengths(lib, orc, cuda, variant, implicit):
               L=48, seed=5 + implicit, variant=variant, kernel=QKV_KERNELS[variant], past=[-21, 3])
 
 
+# rope_qkv_heads_kernel's head groups: 4 heads of a role per thread from 4096 tokens on
+# (16-bit RoPE), 2 below, for float32 and with QK-Norm, and a short last group where a
+# role's head count is not a multiple of the width.
+HEADS_SHAPES = [
+    # dt, H, Nq, Nkv, S (B = 3), packed, cache, inter, rot, implicit, norm
+    ("f16", 64, 8, 4, 1400, 1, 1, 0, "full", 0, 0),     # 4 per thread, 4200 tokens
+    ("bf16", 64, 6, 3, 1400, 1, 1, 1, "full", 0, 0),    # 4 per thread: Q groups 4 + 2, K and V 3
+    ("f16", 128, 6, 3, 37, 0, 1, 0, "full", 1, 0),      # 2 per thread, K and V groups 2 + 1
+    ("f16", 64, 8, 1, 37, 1, 1, 0, "full", 0, 0),       # one K/V head
+    ("f32", 64, 6, 3, 37, 1, 0, 1, "partial", 0, 0),    # float32, short group, no cache, tail units
+    ("f16", 64, 6, 3, 37, 1, 1, 0, "full", 0, 1),       # QK-Norm, short group
+    ("bf16", 128, 5, 1, 37, 0, 1, 1, "full", 1, 1),     # QK-Norm, odd Q heads, one K/V head
+]
+
+
+@pytest.mark.parametrize("dt,H,Nq,Nkv,S,packed,cache,inter,rot,implicit,norm", HEADS_SHAPES)
+def test_qkv_heads_kernel_groups(lib, orc, cuda, dt, H, Nq, Nkv, S, packed, cache, inter, rot, implicit, norm):
+    """Out-of-range tokens copied through, cache rows past the end skipped, every
+    element against the oracle."""
+    import torch
+
+    case = (dt, H, Nq, Nkv, S, packed, cache, inter, rot, implicit, norm)
+    run = _run_norm_case if norm else _run_case
+    run(lib, orc, torch, cuda, dt, packed, cache, inter, rot, implicit, H=H, Nq=Nq, Nkv=Nkv, S=S,
+        seed=300 + HEADS_SHAPES.index(case), kernel="rope_qkv_heads_kernel")
+
+
+def test_qkv_rows_kernel_vector_path(lib, orc, cuda):
+    """A token whose head groups would need more than a CTA's 512 threads (128 Q heads
+    of 256 values) takes the one-head-per-thread kernel on the 128-bit path."""
+    import torch
+
+    _run_case(lib, orc, torch, cuda, "f16", 1, 1, 0, "full", 0, H=256, Nq=128, Nkv=8, S=7, L=52, seed=9,
+              kernel="rope_qkv_kernel")
+
+
 @pytest.mark.parametrize("dt,H", [("f16", 96), ("f16", 80), ("bf16", 96), ("f32", 48)])
 @pytest.mark.parametrize("cache", [0, 1])
 def test_qkv_tma_unit_counts(lib, orc, cuda, dt, H, cache):
@@ -309,7 +357,7 @@ def test_qkv_tma_unit_counts(lib, orc, cuda, dt, H, cache):
 @pytest.mark.parametrize("norm", [0, 1])
 @pytest.mark.parametrize("inter", [0, 1])
 def test_qkv_tma_bits_equal_simt(lib, cuda, dt, norm, inter):
-    """The two kernels round every value in the same order (the pipelined one on packed
+    """The Q/K kernels round every value in the same order (the pipelined one on packed
     16-bit words and float32 pairs, lane by lane as the scalar code rounds), so their
     outputs agree bit for bit: Q, and every row of both caches."""
     import torch
@@ -331,23 +379,31 @@ def test_qkv_tma_bits_equal_simt(lib, cuda, dt, norm, inter):
                   k_norm_weight=_dev(cast(rng.uniform(0.5, 2.0, H), npdt), torch, cuda), epsilon=1e-6)
     kc0 = cast(rng.standard_normal((B, Nkv, L, H)), npdt)
     out = {}
-    for variant, dyn in (("simt", False), ("tma", False), ("tma", True)):
-        kc, vc = _dev(kc0, torch, cuda), _dev(kc0, torch, cuda)
+    # the heads-per-thread kernel, the pipeline on both schedules and (without the norm,
+    # whose sum of squares the scalar path adds in another order) the one-head-per-thread
+    # kernel on the scalar path (every buffer one element off 16-byte alignment)
+    runs = [("simt", False, 0, "rope_qkv_heads_kernel"), ("tma", False, 0, "rope_qkv_tma_kernel"),
+            ("tma", True, 0, "rope_qkv_tma_kernel")]
+    if not norm:
+        runs.append(("simt", False, 1, "rope_qkv_kernel"))
+    for variant, dyn, off, kernel in runs:
+        dv = lambda a: _dev(a, torch, cuda, off)  # noqa: E731
+        kc, vc = dv(kc0), dv(kc0)
         status = torch.zeros(1, dtype=torch.int32, device=cuda)
         scratch = torch.zeros(8, dtype=torch.int64, device=cuda) if dyn else None
         with lib.variant(variant):
-            qo, _ = lib.rope_apply_qkv(_dev(qkv, torch, cuda), _dev(cos, torch, cuda), _dev(sin, torch, cuda),
-                                       _dev(pos, torch, cuda), num_heads=Nq, kv_num_heads=Nkv, interleaved=inter,
-                                       k_cache=kc, v_cache=vc, past_seq_lens=_dev(past, torch, cuda),
-                                       status=status, scratch=scratch, **kw)
+            qo, _ = lib.rope_apply_qkv(dv(qkv), dv(cos), dv(sin), _dev(pos, torch, cuda), num_heads=Nq,
+                                       kv_num_heads=Nkv, interleaved=inter, k_cache=kc, v_cache=vc,
+                                       past_seq_lens=_dev(past, torch, cuda), status=status, scratch=scratch,
+                                       q_out=dv(np.zeros((B, S, Nq * H), npdt)), **kw)
         torch.cuda.synchronize()
-        assert lib.last_kernel() == QKV_KERNELS.get(variant, "rope_qkv_kernel")
-        out[(variant, dyn)] = [_host(t) for t in (qo, kc, vc)] + [int(status.item())]
-    for key in (("tma", False), ("tma", True)):
-        for a, b in zip(out[("simt", False)][:3], out[key][:3]):
+        assert lib.last_kernel() == kernel
+        out[(variant, dyn, off)] = [_host(t) for t in (qo, kc, vc)] + [int(status.item())]
+    first = out[("simt", False, 0)]
+    for key in out:
+        for a, b in zip(first[:3], out[key][:3]):
             assert np.array_equal(a.view(np.uint8), b.view(np.uint8))
         assert out[key][3] == (1 | 4)
-    assert out[("simt", False)][3] == (1 | 4)
 
 
 # ---------------------------------------------------------------------------
