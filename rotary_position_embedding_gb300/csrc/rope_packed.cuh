@@ -12,8 +12,9 @@ namespace rope_gb300 {
 // the results have the bits of rotate(): a product, then a fused multiply-add
 // (-(x1*s) is formed as x1*(-s), which rounds to the same value). Used by the
 // pipelined kernels, whose consumers rotate several heads per coefficient
-// unpack; the SIMT kernels keep the scalar form, which needs fewer registers
-// and so keeps more CTAs resident.
+// unpack, and by the SIMT Q/K heads kernel's QK-Norm path; the other SIMT
+// paths keep the scalar form, which needs fewer registers and so keeps more
+// CTAs resident.
 // ---------------------------------------------------------------------------
 template <class T>
 struct P2;
@@ -76,6 +77,20 @@ __device__ __forceinline__ void unpack_coef8(const VecT<T, 8>& c, float2 (&cf)[4
   __builtin_memcpy(&u, &c, 16);
 #pragma unroll
   for (int k = 0; k < 4; ++k) cf[k] = P2<T>::tof(u.w[k]);
+}
+
+// z = T(w * T(x * r)) on a unit whose values fx are already unpacked: the
+// first product in float32x2, the second on the 16-bit words (the product of
+// two 16-bit values is exact in float32, so the 16-bit multiply rounds it just
+// as float32-then-round does).
+template <class T>
+__device__ __forceinline__ Unit8<T> norm8p(const float2 (&fx)[4], float r, const Unit8<T>& w) {
+  using P = P2<T>;
+  const float2 r2 = make_float2(r, r);
+  Unit8<T> z;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) z.w[k] = __hmul2(P::fromf(__fmul2_rn(fx[k], r2)), w.w[k]);
+  return z;
 }
 
 }  // namespace rope_gb300

@@ -9,7 +9,10 @@
 // all its heads first (2*HPT 16-byte loads in flight), then loads the unit's
 // cos/sin (and norm weights) once and rotates every head with them. With NORM
 // a head's U units are an aligned power-of-two lane group that adds up each of
-// its heads' squares with shuffles, HPT reductions side by side. KParams:
+// its heads' squares with shuffles, HPT reductions side by side; on 16-bit
+// data the normalisation and rotation take the packed float32x2 form of
+// rope_packed.cuh (faster at the sizes this kernel gets the norm), otherwise
+// the scalar one; both round every value alike. KParams:
 // NG = head groups per token (ceil(Nq/HPT) + ceil(Nkv/HPT) [+ ceil(Nkv/HPT)
 // with caches]; with RAGGED a role's last group may hold fewer heads, without
 // it HPT divides both head counts), U = units per head row, Ublk = U.
@@ -21,6 +24,7 @@
 // before RoPE). Same arithmetic as rope_qkv_kernel, whose helpers it uses.
 #pragma once
 
+#include "rope_packed.cuh"
 #include "rope_qkv.cuh"
 
 namespace rope_gb300 {
@@ -134,7 +138,74 @@ __global__ void __launch_bounds__(kMaxRowThreads) rope_qkv_heads_kernel(const KP
           sn = ld_shared_ro(reinterpret_cast<const VT*>(sinb + pp * p.h + oc));
         }
       }
-      if (NORM && rotates) {
+      if constexpr (NORM && sizeof(bits) == 2) {
+        // 16-bit data: the packed form (float32x2 products, coefficients
+        // unpacked once per unit), which rounds every lane as the scalar form
+        // below does
+        if (rotates) {
+          using P = P2<T>;
+          float2 fa[HPT][4], fb[HPT][4];
+          float ss[HPT];
+#pragma unroll
+          for (int j = 0; j < HPT; ++j) {
+            Unit8<T> ua, ub;
+            __builtin_memcpy(&ua, &xa[j], 16);
+            __builtin_memcpy(&ub, &xb[j], 16);
+            float sa = 0.f, sb = 0.f;  // sum_squares' order: a's eight values, then b's
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              fa[j][q] = P::tof(ua.w[q]);
+              fb[j][q] = P::tof(ub.w[q]);
+              sa = __fmaf_rn(fa[j][q].x, fa[j][q].x, sa);
+              sa = __fmaf_rn(fa[j][q].y, fa[j][q].y, sa);
+              sb = __fmaf_rn(fb[j][q].x, fb[j][q].x, sb);
+              sb = __fmaf_rn(fb[j][q].y, fb[j][q].y, sb);
+            }
+            ss[j] = sa + sb;
+          }
+          for (int o = U >> 1; o > 0; o >>= 1) {
+#pragma unroll
+            for (int j = 0; j < HPT; ++j) ss[j] += __shfl_xor_sync(gmask, ss[j], o);
+          }
+          float2 cf[4], sf[4];
+          if (valid && pair) {
+            unpack_coef8<T>(c, cf);
+            unpack_coef8<T>(sn, sf);
+          }
+          Unit8<T> wua, wub;
+          __builtin_memcpy(&wua, &wa, 16);
+          __builtin_memcpy(&wub, &wb, 16);
+#pragma unroll
+          for (int j = 0; j < HPT; ++j) {
+            if (j >= nh) break;
+            const float rr = 1.0f / sqrtf(ss[j] / (float)H + a.eps);
+            const Unit8<T> za = norm8p<T>(fa[j], rr, wua);
+            bits* yj = yr + j * dhead;
+            if (!pair) {
+              st_stream(reinterpret_cast<VT*>(yj + oa), *reinterpret_cast<const VT*>(&za));
+              continue;
+            }
+            const Unit8<T> zb = norm8p<T>(fb[j], rr, wub);
+            if (valid) {
+              Unit8<T> ya, yb;
+              rotate8p<T, INTER>(za, zb, cf, sf, ya, yb);
+              st_stream(reinterpret_cast<VT*>(yj + oa), *reinterpret_cast<const VT*>(&ya));
+              st_stream(reinterpret_cast<VT*>(yj + ob), *reinterpret_cast<const VT*>(&yb));
+            } else {  // out-of-range position: the normalised head passes through
+              st_stream(reinterpret_cast<VT*>(yj + oa), *reinterpret_cast<const VT*>(&za));
+              st_stream(reinterpret_cast<VT*>(yj + ob), *reinterpret_cast<const VT*>(&zb));
+            }
+          }
+        } else {  // V heads: copied
+#pragma unroll
+          for (int j = 0; j < HPT; ++j) {
+            if (j >= nh) break;
+            bits* yj = yr + j * dhead;
+            st_stream(reinterpret_cast<VT*>(yj + oa), xa[j]);
+            if (pair) st_stream(reinterpret_cast<VT*>(yj + ob), xb[j]);
+          }
+        }
+      } else if (NORM && rotates) {
         float ss[HPT];
 #pragma unroll
         for (int j = 0; j < HPT; ++j) ss[j] = sum_squares<T, V>(xa[j]) + sum_squares<T, V>(xb[j]);

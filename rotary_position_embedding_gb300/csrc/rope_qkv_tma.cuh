@@ -195,20 +195,6 @@ __device__ __forceinline__ bool qtile_direct(const QKVParams& a, const QTile& q,
   return q.role != 0 && a.cache && (q.n < q.R.TS || row0 < 0 || row0 + q.R.TS > a.max_len);
 }
 
-// z = T(w * T(x * r)) on a unit whose values fx are already unpacked: the
-// first product in float32x2, the second on the 16-bit words (the product of
-// two 16-bit values is exact in float32, so the 16-bit multiply rounds it just
-// as float32-then-round does).
-template <class T>
-__device__ __forceinline__ Unit8<T> norm8p(const float2 (&fx)[4], float r, const Unit8<T>& w) {
-  using P = P2<T>;
-  const float2 r2 = make_float2(r, r);
-  Unit8<T> z;
-#pragma unroll
-  for (int k = 0; k < 4; ++k) z.w[k] = __hmul2(P::fromf(__fmul2_rn(fx[k], r2)), w.w[k]);
-  return z;
-}
-
 template <class T, bool INTER, bool IMPLICIT, bool NORM, bool MROPE = false>
 __global__ void __launch_bounds__(kTmaThreads * qkv_pipes(MROPE), ROPE_TMA_MIN_CTAS / qkv_pipes(MROPE))
     rope_qkv_tma_kernel(const KParams p, const QKVParams a, const QTParams tp,
