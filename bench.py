@@ -52,8 +52,8 @@ KERNEL_SOURCES = {
     "rope_tma_kernel": ["rope_api.cu", "rope_kernels.cuh", "rope_packed.cuh", "rope_tma.cuh", "k_tma.cu"],
     "rope_fused_kernel": ["rope_api.cu", "rope_kernels.cuh", "rope_fused.cuh", "k_fused.cu"],
     "rope_qkv_kernel": ["rope_api.cu", "rope_kernels.cuh", "rope_qkv.cuh", "k_qkv.cu", "k_mrope_qkv.cu"],
-    "rope_qkv_heads_kernel": ["rope_api.cu", "rope_kernels.cuh", "rope_qkv.cuh", "rope_qkv_heads.cuh",
-                              "k_qkv_heads.cu"],
+    "rope_qkv_heads_kernel": ["rope_api.cu", "rope_kernels.cuh", "rope_qkv.cuh", "rope_packed.cuh",
+                              "rope_qkv_heads.cuh", "k_qkv_heads.cu"],
     "rope_qkv_tma_kernel": ["rope_api.cu", "rope_kernels.cuh", "rope_tma.cuh", "rope_qkv.cuh", "rope_packed.cuh",
                             "rope_qkv_tma.cuh", "k_qkv_tma.cu", "k_mrope_qkv_tma.cu"],
 }
