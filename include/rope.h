@@ -448,8 +448,9 @@ const char* rope_last_error(void);
 /* Kernel family that the last call on the calling thread which launched work
    used: "rope_rows_kernel" (SIMT), "rope_mrope_heads_kernel" (SIMT M-RoPE, several heads
    per thread), "rope_tma_kernel" (TMA pipeline),
-   "rope_fused_kernel", "rope_qkv_kernel" (SIMT), "rope_qkv_tma_kernel" (TMA pipeline) or
-   "rope_cache_build_kernel"; "" before the first
+   "rope_fused_kernel", "rope_qkv_kernel" (SIMT, one head per thread),
+   "rope_qkv_heads_kernel" (SIMT Q/K, several heads of one role per thread),
+   "rope_qkv_tma_kernel" (TMA pipeline) or "rope_cache_build_kernel"; "" before the first
    launch. Calls that fail or launch nothing (empty X) leave it unchanged.
    A diagnostic for profilers and benchmarks: the pages have no counterpart.
    The string is static; never free it. */
