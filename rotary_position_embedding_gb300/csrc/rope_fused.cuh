@@ -28,9 +28,59 @@ __device__ __forceinline__ void coef_on_the_fly(int64_t pos, float inv, float sc
   s = __fmul_rn(__double2float_rn(sd), scaling);
 }
 
+// The same coefficients in T's storage, after the whole rounding chain of the
+// cached table: T(fl32(fl32(cos theta) * scaling)), and for M-RoPE then
+// T(cb * mscale) rounded once (MSCALE). On 16-bit storage most values come
+// from float arithmetic, exactly:
+//  - sincosf is within 2 ulp of the exact value (CUDA's documented bound for
+//    sinf/cosf/sincosf without fast-math), so the exact value lies in
+//    [v - e, v + e] with e = |v| * 2^-20 (at least 8 ulp of v), at least 4 ulp
+//    inside either end, and so does the double-precision value that
+//    coef_on_the_fly rounds to float32;
+//  - the chain x -> T(...) is monotone in x (products by a fixed factor and
+//    round-to-nearest are), so where the ends of that interval give the same
+//    bits, every point inside does, and the result is what coef_on_the_fly
+//    gives;
+//  - otherwise (about 0.1 % of float16 values: an end lies across a rounding
+//    boundary) the value is computed by coef_on_the_fly.
+// float32 storage always takes coef_on_the_fly (the chain there keeps the 2-ulp
+// uncertainty).
+template <class T, bool MSCALE>
+__device__ __forceinline__ typename Elem<T>::bits coef_chain(float x, float scaling, float mscale) {
+  using E = Elem<T>;
+  typename E::bits b = E::fromf(__fmul_rn(x, scaling));
+  if (MSCALE) b = E::fromf(E::mul_round(E::tof(b), mscale));
+  return b;
+}
+
+template <class T, bool MSCALE>
+__device__ __forceinline__ void coef_on_the_fly_bits(int64_t pos, float inv, float scaling, float mscale,
+                                                     typename Elem<T>::bits& cb, typename Elem<T>::bits& sb) {
+  if constexpr (sizeof(typename Elem<T>::bits) == 2) {
+    const float theta = __fmul_rn(__ll2float_rn(pos), inv);
+    float sf, cf;
+    sincosf(theta, &sf, &cf);
+    const float ec = __fmaf_ru(fabsf(cf), 0x1p-20f, 0x1p-100f);
+    const float es = __fmaf_ru(fabsf(sf), 0x1p-20f, 0x1p-100f);
+    const auto c0 = coef_chain<T, MSCALE>(__fsub_rd(cf, ec), scaling, mscale);
+    const auto c1 = coef_chain<T, MSCALE>(__fadd_ru(cf, ec), scaling, mscale);
+    const auto s0 = coef_chain<T, MSCALE>(__fsub_rd(sf, es), scaling, mscale);
+    const auto s1 = coef_chain<T, MSCALE>(__fadd_ru(sf, es), scaling, mscale);
+    if (c0 == c1 && s0 == s1) {
+      cb = c0;
+      sb = s0;
+      return;
+    }
+  }
+  float c, s;
+  coef_on_the_fly(pos, inv, scaling, c, s);
+  cb = coef_chain<T, MSCALE>(c, 1.0f, mscale);
+  sb = coef_chain<T, MSCALE>(s, 1.0f, mscale);
+}
+
 // Fused rotation: per tile of TTs tokens the CTA first fills a shared-memory
-// table of the tile's rd/2 coefficients (one double-precision sincos per
-// token and index, not per head), then every thread rotates its unit from it.
+// table of the tile's rd/2 coefficients (coef_on_the_fly_bits once per token
+// and index, not per head), then every thread rotates its unit from it.
 // MROPE: index i takes the position of its stream (t, h or w, from the stream
 // map), and the coefficient is then scaled and rounded to T as the cached
 // M-RoPE path does ("com.microsoft.MRotaryEmbedding" README, Description and
@@ -76,7 +126,7 @@ __global__ void __launch_bounds__(kMaxRowThreads) rope_fused_kernel(const KParam
     const bits* xr = x + row;
     bits* yr = y + row;
     // The thread's first pair unit is loaded before the table is built, so its
-    // DRAM latency overlaps the double-precision sincos.
+    // DRAM latency overlaps the coefficients' computation.
     const bool pre = mine && k0 < p.nP;
     int pa = 0, pb = 0;
     VT a0{}, b0{};
@@ -98,13 +148,11 @@ __global__ void __launch_bounds__(kMaxRowThreads) rope_fused_kernel(const KParam
         } else {
           pp = __ldg(p.pos + t);
         }
-        float c, s;
-        coef_on_the_fly(pp, __ldg(p.inv_freq + i), p.scale, c, s);
-        bits cb = E::fromf(c), sb = E::fromf(s);
-        if (MROPE && !p.mscale_is_one) {
-          cb = E::fromf(E::mul_round(E::tof(cb), p.mscale));
-          sb = E::fromf(E::mul_round(E::tof(sb), p.mscale));
-        }
+        bits cb, sb;
+        if (MROPE && !p.mscale_is_one)
+          coef_on_the_fly_bits<T, true>(pp, __ldg(p.inv_freq + i), p.scale, p.mscale, cb, sb);
+        else
+          coef_on_the_fly_bits<T, false>(pp, __ldg(p.inv_freq + i), p.scale, 1.0f, cb, sb);
         sc[it] = cb;
         ss[it] = sb;
       }
@@ -137,7 +185,8 @@ __global__ void __launch_bounds__(kMaxRowThreads) rope_fused_kernel(const KParam
   }
 }
 
-// (rows, half) cos/sin tables: row p = on-the-fly coefficients of position p.
+// (rows, half) cos/sin tables: row p = on-the-fly coefficients of position p,
+// through the same coef_on_the_fly_bits as the fused kernel.
 template <class T>
 __global__ void __launch_bounds__(256) rope_cache_build_kernel(const float* __restrict__ inv,
                                                                int32_t half, int64_t rows,
@@ -154,10 +203,10 @@ __global__ void __launch_bounds__(256) rope_cache_build_kernel(const float* __re
        idx += (int64_t)gridDim.x * blockDim.x) {
     const int64_t pr = idx / half;
     const int i = (int)(idx - pr * half);
-    float c, s;
-    coef_on_the_fly(pr, __ldg(inv + i), scaling, c, s);
-    co[idx] = E::fromf(c);
-    so[idx] = E::fromf(s);
+    bits cb, sb;
+    coef_on_the_fly_bits<T, false>(pr, __ldg(inv + i), scaling, 1.0f, cb, sb);
+    co[idx] = cb;
+    so[idx] = sb;
   }
 }
 

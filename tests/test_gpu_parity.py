@@ -652,6 +652,27 @@ def test_cache_build_vs_oracle(lib, orc, cuda, torch_mod, dt, base, scaling):
         assert (d == 0).mean() >= 0.99999
 
 
+@pytest.mark.parametrize("dt", ["f16", "bf16"])
+@pytest.mark.parametrize("scaling", [1.0, 0.7, -0.5])
+def test_cache_build_long_angles(lib, orc, cuda, torch_mod, dt, scaling):
+    """Angles up to 131072 rad on 16-bit storage, where most values come from float32
+    sincos kept only when the rounding chain cannot tell it from the binary64 one: the
+    same bar as above (the two binary64 libraries may round apart at a float32 boundary),
+    here with a count -- at most 1 in 10^6 values may differ, by one unit."""
+    torch = torch_mod
+    dtype = DT[dt]
+    rows, half = 1 << 17, 64
+    inv = wl.inv_freq(1e6, 2 * half, half)
+    c_ref, s_ref = orc.cache_build(inv, rows, dtype, scaling)
+    cd, sd = lib.rope_cache_build(_dev(inv, torch, cuda), rows, _tdt(torch, dt), attention_scaling=scaling)
+    torch.cuda.synchronize()
+    from parity_util import f16_ordinal
+    for got, ref in ((_host(cd), c_ref), (_host(sd), s_ref)):
+        d = np.abs(f16_ordinal(got) - f16_ordinal(ref))
+        assert d.max() <= 1
+        assert int((d != 0).sum()) <= ref.size // 10 ** 6
+
+
 # ---------------------------------------------------------------------------
 # Full-size workloads, launched exactly as the benchmark launches them
 # ---------------------------------------------------------------------------
