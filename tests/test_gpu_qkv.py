@@ -234,6 +234,52 @@ def expected_qkv_kernel(auto, norm, qkv_bytes, Nq, Nkv, cache):
     return "rope_qkv_heads_kernel"
 
 
+# The automatic choice at its boundaries (kernel numerics are tested above): plain RoPE takes the
+# heads kernel except in cache mode with Nq <= 2*Nkv from 128 MiB; QK-Norm and partial rotation
+# take the pipeline from 8 MiB.
+DISPATCH_CASES = [
+    # Nq, Nkv, B, S, rd (0: full), cache, norm, kernel
+    (32, 8, 4, 2048, 0, 1, 0, "rope_qkv_heads_kernel"),     # 100.7 MB, the Qwen3-8B prefill
+    (8, 8, 1, 22000, 0, 1, 0, "rope_qkv_tma_kernel"),       # MHA, 135.2 MB >= 128 MiB
+    (8, 8, 1, 21000, 0, 1, 0, "rope_qkv_heads_kernel"),     # MHA, 129.0 MB < 128 MiB
+    (16, 8, 1, 17000, 0, 1, 0, "rope_qkv_tma_kernel"),      # Nq = 2*Nkv, 139.3 MB
+    (8, 8, 1, 22000, 0, 0, 0, "rope_qkv_heads_kernel"),     # MHA without caches
+    (32, 8, 1, 1024, 0, 1, 1, "rope_qkv_tma_kernel"),       # QK-Norm, 12.6 MB
+    (32, 8, 1, 256, 0, 1, 1, "rope_qkv_heads_kernel"),      # QK-Norm, 3.1 MB
+    (32, 8, 1, 1024, 64, 1, 0, "rope_qkv_tma_kernel"),      # partial rotation, 12.6 MB
+    (32, 8, 1, 256, 64, 1, 0, "rope_qkv_heads_kernel"),     # partial rotation, 3.1 MB
+    (32, 8, 256, 1, 0, 1, 0, "rope_qkv_heads_kernel"),      # decode
+]
+
+
+@pytest.mark.parametrize("Nq,Nkv,B,S,rd,cache,norm,kernel", DISPATCH_CASES)
+def test_qkv_automatic_choice(lib, cuda, Nq, Nkv, B, S, rd, cache, norm, kernel):
+    import torch
+
+    H = 128
+    f16 = torch.float16
+    qkv = torch.zeros((B, S, (Nq + 2 * Nkv) * H), dtype=f16, device=cuda)
+    half = (rd or H) // 2
+    c = torch.ones((S + 64, half), dtype=f16, device=cuda)
+    past = torch.zeros(B, dtype=torch.int32, device=cuda)
+    kw = {}
+    if cache:
+        kc = torch.zeros((B, Nkv, S, H), dtype=f16, device=cuda)
+        kw = dict(k_cache=kc, v_cache=torch.zeros_like(kc), past_seq_lens=past)
+    if norm:
+        w = torch.ones(H, dtype=f16, device=cuda)
+        kw.update(q_norm_weight=w, k_norm_weight=w)
+    if not cache:  # plain RoPE without caches: K comes out rotated, V is not read
+        qkv = torch.zeros((B, S, Nq * H), dtype=f16, device=cuda)
+        kw.update(key=torch.zeros((B, S, Nkv * H), dtype=f16, device=cuda), past_seq_lens=past)
+    with lib.variant("auto"):
+        lib.rope_apply_qkv(qkv, c, c, None, num_heads=Nq, kv_num_heads=Nkv, rotary_embedding_dim=rd, **kw)
+    torch.cuda.synchronize()
+    assert lib.last_kernel() == kernel
+    del qkv, kw
+    torch.cuda.empty_cache()
+
+
 @pytest.mark.parametrize("variant", ["auto", "auto_dynamic", "simt"])
 @pytest.mark.parametrize("name", [n for n, w in wl.WORKLOADS.items() if w.kind == "qkv"])
 def test_qkv_workload_full_size(lib, orc, cuda, name, variant):
