@@ -411,6 +411,67 @@ def test_mrope_grid(lib, orc, cuda, torch_mod, dt, rank, layout, inter, rot, sca
     assert int(flag.item()) == (1 if n_oor else 0)
 
 
+def _random_mrope_cases(n, seed):
+    """n seeded shapes: dtype, rank, heads, head size, rotary width, a random three-way
+    section of the half width (every stream at least one index), layout (incl. the stride-3
+    reading), pairing, scale and token count (both sides of the 512-token switch)."""
+    rng = np.random.default_rng(seed)
+    out = []
+    for _ in range(n):
+        H = int([32, 64, 96, 128, 256][rng.integers(5)])
+        rd = [0, H // 2, H // 4][rng.integers(3)]
+        h = (rd or H) // 2
+        c1, c2 = sorted(rng.choice(np.arange(1, h), size=2, replace=False).tolist())
+        sec = (c1, c2 - c1, h - c2)
+        out.append((["f16", "bf16", "f32"][rng.integers(3)], int(rng.choice([3, 4])), int(rng.integers(1, 13)), H,
+                    int(rd), sec, ["l0", "l1", "stride3"][rng.integers(3)], int(rng.integers(2)),
+                    [1.0, 0.7][rng.integers(2)], int(rng.choice([40, 150, 400]))))
+    return out
+
+
+RANDOM_MROPE = _random_mrope_cases(24, 77)
+
+
+@pytest.mark.parametrize("variant", ["simt", "tma"])
+@pytest.mark.parametrize("dt,rank,N,H,rd,sec,layout,inter,scale,S", RANDOM_MROPE)
+def test_mrope_random_shapes(lib, orc, cuda, torch_mod, dt, rank, N, H, rd, sec, layout, inter, scale, S, variant):
+    """Whichever kernel the variant leads to (the heads kernel, the rows kernel or the
+    pipeline), every element against the oracle; 3% of the ids out of range."""
+    torch = torch_mod
+    dtype = DT[dt]
+    rng = np.random.default_rng(900 + RANDOM_MROPE.index((dt, rank, N, H, rd, sec, layout, inter, scale, S)))
+    B = 2
+    h = (rd or H) // 2
+    R = 1000
+    shape = _x_shape(rank, B, S, N, H)
+    x = cast(rng.standard_normal(shape), dtype)
+    cos, sin = orc.cache_build(wl.inv_freq(10000.0, rd or H, h), R, dtype)
+    pos3 = rng.integers(0, R, (3, B, S))
+    oor = rng.random((3, B, S)) < 0.03
+    pos3[oor] = rng.choice([-1, R, R + 5, 1 << 40], size=int(oor.sum()))
+    nh = N if rank == 3 else 0
+    scale = float(np.float32(scale))
+    if layout == "stride3":
+        smap = orc.mrope_stream_map(sec, 2, h)
+        y_ref, n_oor = orc.mrope_map(x, cos, sin, pos3, smap, scale, inter, rd, nh)
+    else:
+        lay = 0 if layout == "l0" else 1
+        smap = orc.mrope_stream_map(sec, lay, h)
+        y_ref, n_oor = orc.mrope(x, cos, sin, pos3, sec, lay, scale, inter, rd, nh)
+    args = (_dev(x, torch, cuda), _dev(cos, torch, cuda), _dev(sin, torch, cuda), _dev(pos3, torch, cuda))
+    flag = torch.zeros(1, dtype=torch.int32, device=cuda)
+    kw = dict(scale=scale, interleaved=inter, rotary_embedding_dim=rd, num_heads=nh, oor_flag=flag)
+    with lib.variant(variant):
+        if layout == "stride3":
+            yd = lib.mrope_apply_stream_map(*args, smap.tolist(), **kw)
+        else:
+            yd = lib.mrope_apply(*args, sec, mrope_layout=0 if layout == "l0" else 1, **kw)
+    torch.cuda.synchronize()
+    mask = mrope_passthrough_mask(shape, rank, N, rd, pos3, R, smap, inter)
+    compare(_host(yd), y_ref, x, rank, N, mask)
+    assert int(flag.item()) == (1 if n_oor else 0)
+
+
 HEADS_GRID = list(itertools.product(["f16", "f32", "bf16"], [3, 4], ["l0", "l1", "stride3"], [0, 1],
                                     ["full", "partial"], [1.0, 0.7], [2, 4]))
 
