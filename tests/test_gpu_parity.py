@@ -673,6 +673,56 @@ def test_mrope_fused_grid(lib, orc, cuda, torch_mod, dt, rank, layout, inter, rd
     assert torch.equal(yc.view(bits), yf.view(bits))
 
 
+def _random_fused_cases(n, seed):
+    rng = np.random.default_rng(seed)
+    out = []
+    for _ in range(n):
+        H = int([32, 64, 96, 128, 256][rng.integers(5)])
+        out.append((["f16", "bf16", "f32"][rng.integers(3)], int(rng.choice([3, 4])), int(rng.integers(1, 9)), H,
+                    [0, H // 2][rng.integers(2)], int(rng.integers(2)), float([1e4, 1e6, 5e6][rng.integers(3)]),
+                    float([1.0, 0.7071067690849304, 1.25, -0.5][rng.integers(4)])))
+    return out
+
+
+RANDOM_FUSED = _random_fused_cases(16, 31)
+
+
+@pytest.mark.parametrize("dt,rank,N,H,rd,inter,base,scaling", RANDOM_FUSED)
+def test_fused_random_shapes(lib, orc, cuda, torch_mod, dt, rank, N, H, rd, inter, base, scaling):
+    """On-the-fly RoPE, whose 16-bit coefficients come from float32 sincos wherever that
+    provably gives the binary64 result: positions in [0, 65536) bit for bit equal to
+    gathering rope_cache_build's 65536-row table, and positions out to +-2^20 against the
+    oracle."""
+    torch = torch_mod
+    dtype = DT[dt]
+    rng = np.random.default_rng(1300 + RANDOM_FUSED.index((dt, rank, N, H, rd, inter, base, scaling)))
+    B, S = 3, 37
+    h = (rd or H) // 2
+    shape = _x_shape(rank, B, S, N, H)
+    x = cast(rng.standard_normal(shape), dtype)
+    inv = wl.inv_freq(base, rd or H, h)
+    nh = N if rank == 3 else 0
+    xd, ind = _dev(x, torch, cuda), _dev(inv, torch, cuda)
+    kw = dict(attention_scaling=scaling, interleaved=inter, rotary_embedding_dim=rd, num_heads=nh)
+    # inside a 65536-row table: the fused result equals the cached one bit for bit
+    pos = rng.integers(0, 1 << 16, (B, S))
+    pd = _dev(pos, torch, cuda)
+    yf = lib.rope_apply_fused(xd, ind, pd, **kw)
+    cd, sd = lib.rope_cache_build(ind, 1 << 16, _tdt(torch, dt), attention_scaling=scaling)
+    yc = lib.rope_apply(xd, cd, sd, pd, interleaved=inter, rotary_embedding_dim=rd, num_heads=nh)
+    torch.cuda.synchronize()
+    bits = _bits(torch, dt)
+    assert torch.equal(yc.view(bits), yf.view(bits))
+    compare(_host(yf), orc.rope_fused(x, inv, pos, scaling, inter, rd, nh), x, rank, N,
+            rope_passthrough_mask(shape, rank, N, rd, None, 0))
+    # far positions, negative ones included: against the oracle
+    pos = rng.integers(-(1 << 20), 1 << 20, (B, S))
+    yf = lib.rope_apply_fused(xd, ind, _dev(pos, torch, cuda), **kw)
+    torch.cuda.synchronize()
+    compare(_host(yf), orc.rope_fused(x, inv, pos, scaling, inter, rd, nh), x, rank, N,
+            rope_passthrough_mask(shape, rank, N, rd, None, 0))
+
+
 def test_mrope_fused_any_position(lib, orc, cuda, torch_mod):
     """No table, so no position is out of range: large and negative ids rotate too."""
     torch = torch_mod
