@@ -715,6 +715,13 @@ def measure_rows(args, torch, rp, device, peak, names):
                 ggbs = nbytes / (graph_ms * 1e-3) / 1e9
                 rows[key].update({"us_per_step_graph": round(graph_ms * 1e3, 3), "GB_s_graph": round(ggbs, 1),
                                   "frac_graph": round(ggbs / peak, 4)})
+        if name in wl.CONFIGS and hasattr(step, "ys"):
+            # what a plain device copy of the same X into Y costs alone, measured the same way:
+            # the isolated launch's floor for this configuration's bytes
+            floor = isolation_floor(torch, step, min(200, args.row_steps), sh)
+            for key in rows:
+                if key.startswith(name + ":"):
+                    rows[key]["copy_x_to_y_us_isolated"] = floor["copy_x_to_y_us"]
         del step
         torch.cuda.empty_cache()
     # one-time setup row: cache build of the largest table
@@ -733,8 +740,9 @@ def measure_rows(args, torch, rp, device, peak, names):
 def config_summary(rows, peak):
     """Compact figures of every published configuration: kernel, microseconds
     back to back (timed region / launches), from a CUDA graph and alone (median
-    of event-bracketed single launches), and the fractions of the measured
-    peak they give with the configuration's algorithmic bytes."""
+    of event-bracketed single launches), the fractions of the measured peak they
+    give with the configuration's algorithmic bytes, and (X-to-Y kernels) the
+    time of a lone device copy of X into Y over the lone launch's time."""
     out = {}
     for name in wl.CONFIGS:
         w = wl.WORKLOADS[name]
@@ -748,6 +756,11 @@ def config_summary(rows, peak):
         for k in ("b2b", "graph", "isolated"):
             us = d["us_" + k]
             d["frac_" + k] = None if not us else round(nb / (us * 1e-6) / 1e9 / peak, 4)
+        copy_us = r.get("copy_x_to_y_us_isolated")
+        if copy_us:
+            # a lone launch against a lone device copy of X into Y: 1.0 = as fast as the copy
+            d["us_copy_x_to_y_isolated"] = copy_us
+            d["isolated_copy_over_kernel"] = round(copy_us / d["us_isolated"], 4)
         out[name] = d
     return out
 
